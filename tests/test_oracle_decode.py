@@ -1,0 +1,118 @@
+"""Pins of the oracle's decode step through cases that reduce to its pinned parts."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import ModelSpec
+
+TINY = dict(n_layers=2, hidden=512, n_heads=8, n_kv_heads=2, head_dim=64, ffn_dim=1536, vocab=4096, max_ctx=64)
+
+
+def _spec(**kw):
+    d = dict(TINY)
+    d.update(kw)
+    return ModelSpec(**d)
+
+
+def _w(spec, role, layer=0):
+    rows, cols, fmt = {
+        "q": (spec.n_heads * spec.head_dim, spec.hidden, spec.t_q),
+        "k": (spec.n_kv_heads * spec.head_dim, spec.hidden, spec.t_k),
+        "v": (spec.n_kv_heads * spec.head_dim, spec.hidden, spec.t_v),
+        "o": (spec.hidden, spec.n_heads * spec.head_dim, spec.t_o),
+        "gate": (spec.ffn_dim, spec.hidden, spec.t_gate),
+        "up": (spec.ffn_dim, spec.hidden, spec.t_up),
+        "down": (spec.hidden, spec.ffn_dim, spec.t_down),
+    }[role]
+    return fmt, rows, cols, oracle.qtensor_rows(fmt, rows, cols, spec.seed, oracle.uid_layer(layer, role),
+                                                 spec.init_std)
+
+
+def _embed(spec, tok):
+    b = oracle.qtensor_rows(spec.t_embd, spec.vocab, spec.hidden, spec.seed, oracle.UID_EMBD, spec.init_std,
+                            row0=tok, nrows=1)
+    return oracle.dequant_row(spec.t_embd, b[0], spec.hidden).astype(np.float64)
+
+
+def _logits(spec, x):
+    b = oracle.qtensor_rows(spec.t_out, spec.vocab, spec.hidden, spec.seed, oracle.UID_OUTPUT, spec.init_std)
+    return oracle.gemv(spec.t_out, b, spec.vocab, spec.hidden, oracle.rmsnorm(x, spec.rms_eps))
+
+
+def test_zero_layer_model_is_norm_then_output_gemv():
+    spec = _spec(n_layers=0, vocab=512)
+    m = oracle.Model(spec)
+    tok = 77
+    lg, nx, mg = m.decode_step(tok)
+    want = _logits(spec, _embed(spec, tok))
+    np.testing.assert_array_equal(lg, want)
+    i, marg = oracle.argmax(want)
+    assert nx == i and mg == marg and m.pos == 1
+
+
+def test_one_layer_at_position_zero_reduces_to_gemvs():
+    # With one cached position softmax has a single weight 1, so every query head
+    # j returns V of its group g = j // (n_heads / n_kv_heads), rounded to binary16.
+    spec = _spec(n_layers=1, vocab=512, t_v="q6_k", t_down="q4_k", t_gate="q4_0")
+    m = oracle.Model(spec)
+    tok = 5
+    lg, nx, _ = m.decode_step(tok)
+
+    def gemv(role, x):
+        fmt, rows, cols, b = _w(spec, role)
+        return oracle.gemv(fmt, b, rows, cols, x)
+
+    x = _embed(spec, tok)
+    xn = oracle.rmsnorm(x, spec.rms_eps)
+    v = gemv("v", xn)
+    v16 = v.astype(np.float16).astype(np.float64)
+    hd, group = spec.head_dim, spec.n_heads // spec.n_kv_heads
+    o = np.concatenate([v16[(j // group) * hd:(j // group + 1) * hd] for j in range(spec.n_heads)])
+    x = x + gemv("o", o)
+    xn = oracle.rmsnorm(x, spec.rms_eps)
+    g, u = gemv("gate", xn), gemv("up", xn)
+    h = np.array([oracle.silu(a) for a in g]) * u
+    x = x + gemv("down", h)
+    want = _logits(spec, x)
+    np.testing.assert_allclose(lg, want, rtol=1e-12, atol=1e-13)
+    assert nx == oracle.argmax(want)[0]
+    # the stored value at position 0 is the binary16 rounding of v
+    for d in (0, 1, 63):
+        assert m.kv_get(0, 1, 1, 0, d) == int(np.float16(v[hd + d]).view(np.uint16))
+
+
+def test_all_zero_weights_give_zero_logits():
+    m = oracle.Model(_spec(init_std=0.0))
+    for tok in (0, 9):
+        lg, nx, mg = m.decode_step(tok)
+        assert not lg.any() and nx == 0 and mg == 0.0
+
+
+def test_kv_prefill_is_rounded_unit_normal():
+    spec = _spec()
+    m = oracle.Model(spec)
+    m.kv_prefill(10, seed=2)
+    assert m.pos == 10
+    for (l, kv, g, t, d) in [(0, 0, 0, 0, 0), (1, 1, 1, 9, 63), (0, 1, 1, 3, 17)]:
+        i = (t * spec.n_kv_heads + g) * spec.head_dim + d
+        z = oracle.normal(2, oracle.uid_kv(l, kv), i)
+        assert m.kv_get(l, kv, g, t, d) == int(np.float16(z).view(np.uint16))
+
+
+def test_decode_deterministic_lazy_equals_resident_and_position_limit():
+    spec = _spec(max_ctx=4)
+    a, b = oracle.Model(spec), oracle.Model(spec, lazy=True, nthreads=3)
+    toks = oracle.tokens(0, 4, spec.vocab)
+    for t in toks:
+        la, na, _ = a.decode_step(t)
+        lb, nb, _ = b.decode_step(t)
+        np.testing.assert_array_equal(la, lb)
+        assert na == nb
+    with pytest.raises(RuntimeError):
+        a.decode_step(0)
+    a.kv_reset()
+    assert a.pos == 0
+    l0, _, _ = a.decode_step(toks[0])
+    c = oracle.Model(spec)
+    l1, _, _ = c.decode_step(toks[0])
+    np.testing.assert_array_equal(l0, l1)
