@@ -1,0 +1,458 @@
+"""Benchmark of the batch-1 quantized Llama decode step on GB300.
+
+Default workload: Llama-3.1-8B-shaped model, Q8_0 weights (8.0 GB) resident in
+HBM, f16 KV cache prefilled to context 512, greedy decode.  One step = one
+decode step (every kernel of the hot path).  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload llama8b_q8_0|llama70b_q4_k_m|llama70b_q6_k_streamed|tiny]
+                  [--no-sweep] [--no-cpu-baseline] [--profile-gemv FMT ROWS COLS LAUNCHES]
+
+value: tokens/s over the K timed steps, device-timed (CUDA events on the
+launching stream around a device-resident greedy loop; inputs already in HBM).
+e2e: tokens/s through nt_decode_step with the token copied host->device and
+the result device->host every step.  Inputs (8 GB of weights) are larger than
+L2 (129 MB), so no flush is needed between steps.
+--impl reference times the oracle (the C reference restatement) on the host
+cores on a bounded sample of the same workload.
+With N > 1 (torchrun) every rank runs an independent replica (the step does
+not shard); value = all ranks' tokens / max over ranks of the time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "batch-1 decode tok/s"
+PAGES_8B_Q8_0_TOK_S = 48.9   # RTX 3090, Llama 8B Q8_0 (hada "Roadmap", Phase 1); context, other hardware
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=256)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="llama8b_q8_0",
+                   choices=["llama8b_q8_0", "llama70b_q4_k_m", "llama70b_q6_k_streamed", "tiny"])
+    p.add_argument("--no-sweep", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile-gemv", nargs=4, metavar=("FMT", "ROWS", "COLS", "LAUNCHES"))
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------- workloads --
+
+def workload(name: str):
+    from quantized_decode_dequant_gb300 import workloads as W
+    if name == "llama8b_q8_0":
+        return dict(spec=W.LLAMA_8B_Q8_0, ctx=W.LLAMA_8B_CTX, resident=None,
+                    label="Llama-3.1-8B-shaped, Q8_0, ctx 512, batch 1", vs=PAGES_8B_Q8_0_TOK_S)
+    if name == "llama70b_q4_k_m":
+        return dict(spec=W.LLAMA_70B_Q4_K_M, ctx=W.LLAMA_70B_Q4_K_M_CTX, resident=None,
+                    label="Llama-3.1-70B-shaped, Q4_K_M mix, ctx 4096, batch 1", vs=None)
+    if name == "llama70b_q6_k_streamed":
+        return dict(spec=W.LLAMA_70B_Q6_K, ctx=W.LLAMA_70B_Q6_K_CTX, resident=W.LLAMA_70B_Q6_K_RESIDENT,
+                    label="Llama-3.1-70B-shaped, Q6_K, 26 layers resident, 54 streamed, ctx 1024", vs=None)
+    return dict(spec=W.TINY, ctx=0, resident=None, label="tiny Llama (2 layers, hidden 512), Q8_0", vs=None)
+
+
+def max_ctx_for(wl, steps: int, warmup: int) -> int:
+    # every phase restarts at the prefilled context, so the longest phase bounds the cache
+    return wl["ctx"] + max(steps, warmup, 8) + 8
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), source="measured")
+    return dict(hbm_gbs=6800.0, source="fallback")
+
+
+# --------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms during the timed region (clocks, throttle reasons)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# -------------------------------------------------------------- distributed --
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world <= 1:
+        return 0, 1, 0, None
+    import torch
+    import torch.distributed as dist
+    rank, local = int(os.environ["RANK"]), int(os.environ.get("LOCAL_RANK", "0"))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend == "nccl":
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend=backend)
+    return rank, world, local, dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def reduce_max(dist, value: float) -> float:
+    """Max over ranks (the timing rule: the slowest replica sets the job time)."""
+    if dist is None:
+        return value
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, world: int, max_seconds: float) -> float:
+    return units_per_rank * world / max_seconds
+
+
+# ------------------------------------------------------------ CPU baseline --
+
+def cpu_baseline(wl, sample_steps: int = 2, threads: int | None = None) -> dict:
+    """The oracle on the host cores, on a sample of the workload: the same
+    architecture truncated to one layer, decoded from the same prefilled context;
+    its per-token time is scaled to the full model by weight + KV bytes."""
+    import oracle
+    from quantized_decode_dequant_gb300 import workloads as W
+    spec = dict(wl["spec"])
+    threads = threads or os.cpu_count() or 1
+    sample = dict(spec, n_layers=1, max_ctx=wl["ctx"] + sample_steps + 1)
+    m = oracle.Model(oracle.ModelSpec(**sample, seed=W.SEED_WEIGHTS), nthreads=threads)
+    m.kv_prefill(wl["ctx"], W.SEED_KV)
+    tok = oracle.token(W.SEED_PROMPT, oracle.UID_TOKENS, 0, spec["vocab"])
+    t0 = time.perf_counter()
+    for _ in range(sample_steps):
+        _, tok, _ = m.decode_step(tok)
+    dt = (time.perf_counter() - t0) / sample_steps
+    m.close()
+    full = W.weight_bytes(spec) + W.kv_bytes(spec, wl["ctx"])
+    part = W.weight_bytes(sample) + W.kv_bytes(sample, wl["ctx"])
+    sec_per_tok = dt * full / part
+    return {"value": 1.0 / sec_per_tok, "unit": "tok/s", "cores": threads, "kind": "oracle",
+            "sample": (f"{sample_steps} oracle decode steps of the same architecture truncated to 1 layer "
+                       f"(ctx {wl['ctx']}), {dt:.2f} s/step, scaled to the full model by weight+KV bytes "
+                       f"({full / part:.1f}x)")}
+
+
+def run_reference(args, wl, rank, world, dist):
+    if rank != 0:
+        return
+    import oracle
+    from quantized_decode_dequant_gb300 import workloads as W
+    spec = wl["spec"]
+    threads = os.cpu_count() or 1
+    sample = dict(spec, n_layers=1, max_ctx=wl["ctx"] + args.steps + args.warmup + 2)
+    m = oracle.Model(oracle.ModelSpec(**sample, seed=W.SEED_WEIGHTS), nthreads=threads)
+    m.kv_prefill(wl["ctx"], W.SEED_KV)
+    tok = oracle.token(W.SEED_PROMPT, oracle.UID_TOKENS, 0, spec["vocab"])
+    for _ in range(args.warmup):
+        _, tok, _ = m.decode_step(tok)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _, tok, _ = m.decode_step(tok)
+    dt = (time.perf_counter() - t0) / args.steps
+    full = W.weight_bytes(spec) + W.kv_bytes(spec, wl["ctx"])
+    part = W.weight_bytes(sample) + W.kv_bytes(sample, wl["ctx"])
+    value = 1.0 / (dt * full / part)
+    line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * full / part * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": wl["label"], "parallelism": "replicas only"},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                             "sample": (f"each step: one oracle decode step of the architecture truncated to "
+                                        f"1 layer, scaled to the full model by weight+KV bytes ({full / part:.1f}x)")},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GEMV --
+
+def gemv_sweep(nt, torch, peak_gbs: float, l2_bytes: int) -> list[dict]:
+    """Isolated dequant-GEMV sweep at the 70B layer shapes; back-to-back launches
+    over weight copies that together exceed 4x L2; median of 5 repetitions."""
+    from quantized_decode_dequant_gb300 import workloads as W
+    out = []
+    stream = torch.cuda.current_stream()
+    for fmt in W.GEMV_FORMATS:
+        for rows, cols in W.GEMV_SHAPES:
+            wbytes = rows * cols // W.BLOCK_ELEMS[fmt] * W.BLOCK_BYTES[fmt]
+            copies = max(1, min(64, math.ceil(4 * l2_bytes / wbytes)))
+            ts = [nt.nt_qtensor_create(fmt, rows, cols, 0, 1000 + i, 0.02) for i in range(copies)]
+            try:
+                x = torch.randn(cols, device="cuda")
+                y = torch.empty(rows, device="cuda")
+                launches = max(copies, 2 * copies if wbytes < 64 << 20 else copies)
+                for i in range(copies):
+                    nt.nt_gemv_q(ts[i], x.data_ptr(), y.data_ptr(), stream)
+                times = []
+                for _ in range(5):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    for i in range(launches):
+                        nt.nt_gemv_q(ts[i % copies], x.data_ptr(), y.data_ptr(), stream)
+                    b.record(stream)
+                    b.synchronize()
+                    times.append(a.elapsed_time(b) / launches)
+                ms = statistics.median(times)
+                algo = wbytes + 4 * (rows + cols)
+                gbs = algo / (ms * 1e-3) / 1e9
+                out.append({"fmt": fmt, "rows": rows, "cols": cols, "us": round(ms * 1e3, 2),
+                            "GB_s": round(gbs, 1), "frac": round(gbs / peak_gbs, 3)})
+            finally:
+                for t in ts:
+                    nt.nt_qtensor_destroy(t)
+    return out
+
+
+def profile_gemv(nt, torch, fmt: str, rows: int, cols: int, launches: int):
+    """A few launches of one GEMV shape (for an ncu capture of a small case)."""
+    t = nt.nt_qtensor_create(fmt, rows, cols, 0, 1, 0.02)
+    x = torch.randn(cols, device="cuda")
+    y = torch.empty(rows, device="cuda")
+    for _ in range(launches):
+        nt.nt_gemv_q(t, x.data_ptr(), y.data_ptr(), torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    nt.nt_qtensor_destroy(t)
+    print(json.dumps({"profile_gemv": [fmt, rows, cols, launches]}))
+
+
+# ------------------------------------------------------------------ ours --
+
+def run_ours(args, wl, rank, world, local, dist):
+    import torch
+
+    from quantized_decode_dequant_gb300 import nt, workloads as W
+    torch.cuda.set_device(local)
+    nt.lib()
+    if args.profile_gemv:
+        fmt, r, c, n = args.profile_gemv
+        profile_gemv(nt, torch, fmt, int(r), int(c), int(n))
+        return
+    spec = dict(wl["spec"], max_ctx=max_ctx_for(wl, args.steps, args.warmup))
+    cfg = nt.make_config(**spec, seed=W.SEED_WEIGHTS)
+    m = nt.nt_model_create(cfg)
+    peaks = measured_peaks()
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 0) or (126 << 20)
+    stream = torch.cuda.current_stream()
+    try:
+        tok0 = _prompt_token(spec["vocab"])
+        streamed = wl["resident"] is not None
+        if streamed:
+            nt.nt_stream_layers(m, wl["resident"], 2)
+
+        def reset():
+            if wl["ctx"] > 0:
+                nt.nt_kv_prefill(m, wl["ctx"], W.SEED_KV)
+            else:
+                nt.nt_kv_reset(m)
+
+        # ---- warm-up
+        reset()
+        if streamed:
+            t = tok0
+            for _ in range(args.warmup):
+                t = nt.nt_decode_step(m, t)
+        else:
+            nt.nt_decode_run(m, tok0, args.warmup, stream)
+        torch.cuda.synchronize()
+
+        # ---- timed: device-resident greedy loop (streamed: per-step calls, copies inside)
+        reset()
+        clocks = ClockSampler(local)
+        h2d_stats = None
+        with clocks:
+            barrier(dist)
+            torch.cuda.synchronize()
+            if streamed:
+                t0 = time.perf_counter()
+                t = tok0
+                h2d_b = h2d_ms = comp_ms = ov = 0.0
+                for _ in range(args.steps):
+                    t = nt.nt_decode_step(m, t)
+                    st = nt.nt_get_stats(m)
+                    h2d_b += st.h2d_bytes
+                    h2d_ms += st.h2d_ms
+                    comp_ms += st.compute_ms
+                    ov += st.overlap
+                torch.cuda.synchronize()
+                sec = time.perf_counter() - t0
+                h2d_stats = {"h2d_GB_s": h2d_b / (h2d_ms * 1e-3) / 1e9 if h2d_ms else None,
+                             "h2d_GB_per_step": h2d_b / args.steps / 1e9, "overlap": ov / args.steps,
+                             "compute_ms_per_step": comp_ms / args.steps,
+                             "pcie_gen5_x16_nominal_GB_s": 64.0}
+            else:
+                ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                ev0.record(stream)
+                nt.nt_decode_run(m, tok0, args.steps, stream)
+                ev1.record(stream)
+                torch.cuda.synchronize()
+                sec = ev0.elapsed_time(ev1) * 1e-3
+            barrier(dist)
+        sec_max = reduce_max(dist, sec)
+        value = job_throughput(args.steps, world, sec_max)
+        ms_per_step = sec_max / args.steps * 1e3
+        tokens = None if streamed else nt.nt_get_tokens(m, wl["ctx"], min(args.steps, 8)).tolist()
+
+        # ---- e2e through the public call with host token in / result out every step
+        reset()
+        barrier(dist)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        t = tok0
+        for _ in range(args.steps):
+            t = nt.nt_decode_step(m, t)
+        e2e_sec = reduce_max(dist, time.perf_counter() - t0)
+        e2e = {"value": job_throughput(args.steps, world, e2e_sec), "unit": "tok/s",
+               "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 8}
+
+        # ---- per-kernel-class device times (event pair around every launch)
+        roofline = None
+        kt = None
+        if not streamed:
+            reset()
+            n_prof = max(4, min(args.steps, 32))
+            kt = nt.nt_profile_steps(m, tok0, n_prof)
+            g_ms = kt.ms[nt.KC_GEMV] / kt.launches[nt.KC_GEMV]
+            g_bytes = kt.bytes[nt.KC_GEMV] / kt.launches[nt.KC_GEMV]
+            achieved = g_bytes / (g_ms * 1e-3) / 1e9
+            roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                        "kernel": "k_gemv (fused dequant-GEMV, all launches of a step)",
+                        "peak_source": peaks["source"],
+                        "bytes_per_launch": round(g_bytes), "launches_per_step": kt.launches[nt.KC_GEMV] // n_prof,
+                        "us_per_launch": round(g_ms * 1e3, 3)}
+        stats = nt.nt_get_stats(m)
+        step_bytes = stats.weight_bytes + stats.kv_bytes_per_pos * (wl["ctx"] + args.steps / 2)
+        step_roofline = {"bytes_per_step": step_bytes,
+                         "achieved_GB_s": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
+                         "frac": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+        sweep = None
+        if not args.no_sweep and rank == 0 and wl["spec"]["n_layers"] <= 32:
+            nt.nt_model_destroy(m)
+            m = None
+            sweep = gemv_sweep(nt, torch, peaks["hbm_gbs"], l2)
+        cpu = None
+        if rank == 0 and not args.no_cpu_baseline:
+            cpu = cpu_baseline(wl)
+    finally:
+        if m is not None:
+            nt.nt_model_destroy(m)
+
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": round(value, 3), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": round(value / wl["vs"], 3) if wl["vs"] else None,
+            "dtype": "q8_0/q4_k/q6_k weights, f32 math, f16 KV" if wl["spec"].get("t_q", "q8_0") != "q8_0"
+            else "q8_0 weights, f32 math, f16 KV",
+            "data": "synthetic (seeded N(0,0.02) weights quantized on device; N(0,1) f16 KV prefill)",
+            "config": {"workload": wl["label"], "model": "llama", "global_batch": 1, "seq_len": wl["ctx"],
+                       "parallelism": "replicas only" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (weights > 4x L2), no flush"},
+            "roofline": roofline, "step_roofline": step_roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": None if kt is None else int(sum(kt.launches) // max(1, n_prof) * args.steps),
+            "clocks": clocks.summary(), "first_tokens": tokens}
+    if h2d_stats:
+        line["streaming"] = h2d_stats
+    if sweep:
+        line["gemv_sweep"] = sweep
+        line["gemv_sweep_min_frac"] = min(s["frac"] for s in sweep)
+    print(json.dumps(line), flush=True)
+
+
+def _prompt_token(vocab: int) -> int:
+    """Prompt token id: SplitMix64 output of the prompt stream's first counter, mod vocab."""
+    gamma, seed, uid = 0x9E3779B97F4A7C15, 3, 0x300000
+    z = (seed + gamma * ((uid << 40) + 1)) & (2**64 - 1)
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & (2**64 - 1)
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & (2**64 - 1)
+    return (z ^ (z >> 31)) % vocab
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local, dist = dist_setup()
+    wl = workload(args.workload)
+    try:
+        if args.impl == "reference":
+            run_reference(args, wl, rank, world, dist)
+        else:
+            run_ours(args, wl, rank, world, local, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

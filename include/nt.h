@@ -1,0 +1,214 @@
+/*
+ * nt.h -- C ABI of the batch-1 quantized Llama decode step for NVIDIA GB300 (sm_103a).
+ *
+ * What it computes.  The decode step of the layer-streaming Llama engine that
+ * the "ntransformer" pages describe (de.news.hada.io, "Überblick über
+ * NTransformer" and "Hauptfunktionen": GGUF-style Q4_0 / Q8_0 / Q4_K / Q6_K
+ * weights; Llama with RoPE, GQA, SwiGLU, RMSNorm and a KV cache; section
+ * "Architektur und Codestruktur": GEMV, RMSNorm, RoPE, SwiGLU and softmax
+ * kernels; "3-stufiges adaptives Caching" and "SLEP-Streaming": VRAM-resident
+ * layers plus pinned-RAM layers copied host-to-device with double buffering;
+ * blog.hotdry.top, "gpu-nvme-direct的实现架构": two staging buffers whose copy
+ * and compute overlap on CUDA streams).  The pages plan but never show a
+ * public C API ("Phase 5 ... öffentliche C-API (geplant)"), so the entry
+ * points below are this library's own.
+ *
+ * Conventions for every function:
+ *  - Returns nt_status; NT_OK on success.  On failure the output parameters
+ *    are left untouched and nt_last_error() returns a message (thread-local).
+ *    No C++ exception crosses this boundary.
+ *  - "dev" pointers are CUDA device pointers owned by the caller; "host"
+ *    pointers are ordinary host memory owned by the caller.  Objects created
+ *    by *_create are owned by the library until the matching *_destroy.
+ *  - "stream" is a cudaStream_t passed as void*; NULL means the legacy
+ *    default stream.  Functions that take a stream are asynchronous on it;
+ *    the others synchronise before they return.
+ *  - One model is used by one host thread at a time.
+ */
+#ifndef NT_H
+#define NT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NT_OK = 0,
+  NT_E_INVAL = 1,        /* invalid argument: shape, token, position, pointer, size */
+  NT_E_NOMEM = 2,        /* device or pinned-host allocation failed                 */
+  NT_E_CUDA = 3,         /* a CUDA runtime call failed (message has the CUDA error)  */
+  NT_E_TIMEOUT = 4,      /* the host watchdog gave up waiting for the device         */
+  NT_E_UNSUPPORTED = 5,  /* valid request this build does not implement              */
+  NT_E_STATE = 6         /* call not valid in the object's current state             */
+} nt_status;
+
+/* Weight formats ("Quantisierungsformate Q4_0, Q8_0, Q4_K_M, Q5_K, Q6_K, F16
+ * und F32", hada "Überblick").  Q5_K, F16 and F32 weights are not implemented
+ * (NT_E_UNSUPPORTED); F16 is used only for the KV cache.
+ * Canonical block bytes (little-endian), the export format:
+ *   Q8_0  32 weights, 34 B:  f16 d | int8 q[32]                  w = d*q
+ *   Q4_0  32 weights, 18 B:  f16 d | u8 qs[16]                   w = d*(q-8)
+ *         (element k in byte k/2, low nibble for even k)
+ *   Q4_K  256 weights, 144 B: f16 d | f16 dmin | 12 B of sixteen 6-bit fields
+ *         (sc_0..7 then m_0..7, least-significant bit first) | u8 qs[128]
+ *                                                               w = d*sc_j*q - dmin*m_j
+ *   Q6_K  256 weights, 210 B: u8 ql[128] (low 4 bits, as Q4_0) | u8 qh[64]
+ *         (high 2 bits of element k in byte k/4 at bits 2*(k%4)) | int8 sc[16] | f16 d
+ *                                                               w = d*sc_j*(q-32)
+ * On the device each tensor is held as separate 16-byte-aligned streams
+ * (codes, scales) with the same byte count. */
+typedef enum { NT_F32 = 0, NT_F16 = 1, NT_Q8_0 = 2, NT_Q4_0 = 3, NT_Q4_K = 4, NT_Q6_K = 5 } nt_qtype;
+
+/* Tensor roles inside a layer, and the two model-level matrices. */
+enum {
+  NT_ROLE_Q = 0, NT_ROLE_K = 1, NT_ROLE_V = 2, NT_ROLE_O = 3,
+  NT_ROLE_GATE = 4, NT_ROLE_UP = 5, NT_ROLE_DOWN = 6,
+  NT_ROLE_EMBD = 16,    /* [vocab x hidden], layer argument ignored */
+  NT_ROLE_OUTPUT = 17   /* [vocab x hidden], layer argument ignored */
+};
+
+typedef struct nt_model nt_model;
+typedef struct nt_qtensor nt_qtensor;
+
+/* Model description.  Llama architecture with untied embeddings and unit norm
+ * gains.  Weights are drawn from N(0, init_std^2) by the counter-based
+ * generator keyed by (seed, tensor uid, element index) and quantized on the
+ * device into the per-role formats. */
+typedef struct {
+  int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn_dim, vocab, max_ctx;
+  float rms_eps;      /* RMSNorm epsilon, e.g. 1e-5                  */
+  float rope_theta;   /* RoPE base, e.g. 500000                      */
+  float init_std;     /* weight standard deviation, e.g. 0.02        */
+  nt_qtype t_embd, t_q, t_k, t_v, t_o, t_gate, t_up, t_down, t_out;
+  uint64_t seed;
+} nt_config;
+
+/* Counters of the last steps (nt_get_stats). */
+typedef struct {
+  int64_t steps;           /* decode steps since create or reset                     */
+  int32_t pos;             /* current position (number of cached tokens)            */
+  int32_t n_resident;      /* layers resident in device memory                      */
+  double last_step_ms;     /* wall time of the last nt_decode_step, device events    */
+  double h2d_bytes;        /* bytes copied host-to-device in the last step          */
+  double h2d_ms;           /* summed duration of those copies (copy-stream events)  */
+  double compute_ms;       /* summed duration of the layer computations             */
+  double overlap;          /* (h2d_ms + compute_ms - last_step_ms) / min(...), in [0,1] */
+  int64_t weight_bytes;    /* quantized weight bytes read per step                  */
+  int64_t kv_bytes_per_pos;/* KV cache bytes read per cached position per step      */
+} nt_stats;
+
+/* Per-kernel-class device times of profiled steps (nt_profile_steps). */
+enum { NT_KC_GEMV = 0, NT_KC_ATTN = 1, NT_KC_OTHER = 2, NT_KC_COUNT = 3 };
+typedef struct {
+  int64_t launches[NT_KC_COUNT];
+  double ms[NT_KC_COUNT];          /* summed event-to-event time of the launches */
+  double bytes[NT_KC_COUNT];       /* summed algorithmic bytes of the launches   */
+  double step_ms;                  /* mean wall time of a profiled step          */
+} nt_kernel_times;
+
+/* Message of the last failure on this thread ("" if none).  Never NULL. */
+const char* nt_last_error(void);
+
+/* ------------------------------------------------------------------ model -- */
+
+/* Allocates device memory for all weights, the f16 KV cache ([layer][K|V]
+ * [kv_head][max_ctx][head_dim]) and the activations, then generates and
+ * quantizes every weight on the device.  Position starts at 0.
+ * NT_E_INVAL: non-positive sizes, n_heads not a multiple of n_kv_heads,
+ * head_dim odd, a column count not a multiple of the role format's block,
+ * unsupported format.  NT_E_NOMEM: device allocation failed. */
+nt_status nt_model_create(const nt_config* cfg, nt_model** out);
+void nt_model_destroy(nt_model* m);
+
+/* Sets the position to 0 (cache contents are kept but no longer attended). */
+nt_status nt_kv_reset(nt_model* m);
+
+/* Fills cache positions [0, n_ctx) of every layer with N(0,1) draws rounded to
+ * f16 (element (t, kv_head, d) of layer l uses counter index
+ * (t*n_kv_heads + kv_head)*head_dim + d), treated as already-rotated keys, and
+ * sets the position to n_ctx.  NT_E_INVAL if n_ctx > max_ctx. */
+nt_status nt_kv_prefill(nt_model* m, int32_t n_ctx, uint64_t seed);
+
+/* One decode step at the current position p (the pages' per-token loop:
+ * embedding, n_layers x [RMSNorm, Q/K/V GEMV, RoPE, KV append, GQA attention,
+ * O GEMV + residual, RMSNorm, gate/up GEMV, SwiGLU, down GEMV + residual],
+ * final RMSNorm, output GEMV, greedy argmax with ties to the lowest id).
+ * token: input id in [0, vocab).  next_token (host, required): the argmax.
+ * logits_host (nullable): vocab floats.  top2_margin (nullable): top-1 minus
+ * top-2 logit.  Synchronous.  Position becomes p+1.
+ * NT_E_INVAL: token out of range or p == max_ctx. */
+nt_status nt_decode_step(nt_model* m, int32_t token, int32_t* next_token, float* logits_host,
+                         float* top2_margin);
+
+/* n_steps greedy steps that feed each argmax back as the next input on the
+ * device, starting from token; asynchronous on stream (the model's own
+ * stream waits for it).  The produced ids are kept on the device
+ * (nt_get_tokens).  Layer-streamed models are not supported here
+ * (NT_E_STATE); use nt_decode_step. */
+nt_status nt_decode_run(nt_model* m, int32_t token, int32_t n_steps, void* stream);
+
+/* Copies the ids produced at positions [t0, t0+n) into host_out (n int32). */
+nt_status nt_get_tokens(nt_model* m, int32_t t0, int32_t n, int32_t* host_out);
+
+/* Reads n f16 cache values of (layer, kv: 0=K 1=V, kv_head) at positions
+ * [t0, t0+n), head_dim values each, into host_out (n*head_dim uint16). */
+nt_status nt_kv_export(nt_model* m, int32_t layer, int32_t kv, int32_t kv_head, int32_t t0, int32_t n,
+                       uint16_t* host_out);
+
+/* Layer streaming ("3-stufiges adaptives Caching": VRAM-resident layers plus
+ * pinned-RAM layers copied host-to-device; "SLEP-Streaming ... Double
+ * Buffering").  Layers [n_resident, n_layers) move to page-locked host memory
+ * and their device copies are freed.  Every later nt_decode_step copies each
+ * of them into one of n_staging device buffers on a copy stream while the
+ * previous layer computes.  n_staging must be 2.  Results are bitwise
+ * identical to the resident model.  Calling it again with n_resident =
+ * n_layers brings every layer back to the device. */
+nt_status nt_stream_layers(nt_model* m, int32_t n_resident, int32_t n_staging);
+
+nt_status nt_get_stats(const nt_model* m, nt_stats* out);
+
+/* Runs n_steps decode steps (from token, feeding back argmax) with a CUDA
+ * event pair around every kernel launch on the model's stream and returns
+ * per-class totals.  For measurement only; not graph-captured. */
+nt_status nt_profile_steps(nt_model* m, int32_t token, int32_t n_steps, nt_kernel_times* out);
+
+/* Pointer to a weight tensor of the model (owned by the model).  For a
+ * streamed layer the tensor refers to host memory: nt_qtensor_export works,
+ * nt_gemv_q and nt_dequant return NT_E_STATE. */
+nt_status nt_model_tensor(const nt_model* m, int32_t layer, int32_t role, const nt_qtensor** out);
+
+/* -------------------------------------------------- quantized tensors -- */
+
+/* A rows x cols quantized matrix (row-major, blocks along the columns)
+ * generated on the device: element (r, c) is N(0, std^2) from (seed, uid,
+ * r*cols + c), quantized by the format's rule.  NT_E_INVAL if cols is not a
+ * multiple of the block (32 for Q8_0/Q4_0, 256 for Q4_K/Q6_K). */
+nt_status nt_qtensor_create(nt_qtype type, int64_t rows, int64_t cols, uint64_t seed, uint32_t uid, float std,
+                            nt_qtensor** out);
+void nt_qtensor_destroy(nt_qtensor* t);
+
+/* Format, shape and device bytes (the sum of the streams = rows*cols*bpw). */
+nt_status nt_qtensor_info(const nt_qtensor* t, nt_qtype* type, int64_t* rows, int64_t* cols,
+                          size_t* device_bytes);
+
+/* Canonical block bytes of rows [row0, row0+nrows) into host_blocks;
+ * nbytes must be at least nrows * (cols / block) * block_bytes. */
+nt_status nt_qtensor_export(const nt_qtensor* t, int64_t row0, int64_t nrows, void* host_blocks, size_t nbytes);
+
+/* Dequantized fp32 weights of rows [row0, row0+nrows) into dev_out
+ * (nrows*cols floats, row-major), bit-exact under the formats' fp32
+ * formulas (Q4_K as one fused multiply-add: fma(d*sc, q, -(dmin*m))). */
+nt_status nt_dequant(const nt_qtensor* t, int64_t row0, int64_t nrows, float* dev_out, void* stream);
+
+/* y = W x (hada "cuda/: GEMV-...-Kernel"): dev_x fp32[cols], dev_y fp32[rows],
+ * fp32 accumulation of the dequantized products.  Asynchronous on stream.
+ * dev_x and dev_y must not overlap and must be 16-byte aligned. */
+nt_status nt_gemv_q(const nt_qtensor* t, const float* dev_x, float* dev_y, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NT_H */

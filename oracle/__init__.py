@@ -91,6 +91,7 @@ def lib():
         L.orc_kv_prefill.argtypes = [C.c_void_p, C.c_int32, C.c_uint64]
         L.orc_pos.restype = C.c_int32
         L.orc_pos.argtypes = [C.c_void_p]
+        L.orc_set_threads.argtypes = [C.c_void_p, C.c_int32]
         L.orc_decode_step.argtypes = [C.c_void_p, C.c_int32, f64p, C.POINTER(C.c_int32), f64p]
         L.orc_kv_get.restype = C.c_uint16
         L.orc_kv_get.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int]
@@ -304,6 +305,9 @@ class Model:
     @property
     def pos(self) -> int:
         return int(lib().orc_pos(self._h))
+
+    def set_threads(self, n: int):
+        lib().orc_set_threads(self._h, n)
 
     def kv_reset(self):
         lib().orc_kv_reset(self._h)

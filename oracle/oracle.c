@@ -567,6 +567,8 @@ void orc_model_destroy(orc_model* m) {
 
 int32_t orc_pos(const orc_model* m) { return m->pos; }
 
+void orc_set_threads(orc_model* m, int32_t nthreads) { m->c.nthreads = nthreads < 1 ? 1 : nthreads; }
+
 int orc_kv_reset(orc_model* m) {
   m->pos = 0;
   return 0;

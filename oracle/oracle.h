@@ -100,6 +100,7 @@ void       orc_model_destroy(orc_model* m);
 int        orc_kv_reset(orc_model* m);
 int        orc_kv_prefill(orc_model* m, int32_t n_ctx, uint64_t seed);
 int32_t    orc_pos(const orc_model* m);
+void       orc_set_threads(orc_model* m, int32_t nthreads);
 /* logits (vocab doubles, nullable), next token, top-2 margin (nullable) */
 int        orc_decode_step(orc_model* m, int32_t token, double* logits, int32_t* next, double* margin);
 /* read one cached f16 value (for tests) */

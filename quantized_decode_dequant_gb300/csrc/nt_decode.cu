@@ -1,0 +1,943 @@
+// nt_decode.cu -- the batch-1 Llama decode step, its model object, the layer
+// streaming pipeline and the measurement entry points.
+//
+// Step (hada "Hauptfunktionen": Llama with RoPE, GQA, SwiGLU, RMSNorm, KV cache;
+// "Architektur und Codestruktur": GEMV, RMSNorm, RoPE, SwiGLU, softmax kernels):
+//   x = dequant(embd[token])
+//   per layer:  [RMSNorm -> Q|K|V GEMV -> RoPE -> K,V to the f16 cache]   one GEMV launch
+//               split-context GQA attention + combine                      two launches
+//               [O GEMV + residual]                                        one GEMV launch
+//               [RMSNorm -> gate|up GEMV -> SwiGLU]                        one GEMV launch
+//               [down GEMV + residual]                                     one GEMV launch
+//   [RMSNorm -> output GEMV -> per-CTA top-2] -> argmax                   two launches
+// Resident models replay the step as one CUDA graph with programmatic
+// dependent launch between consecutive GEMVs.
+//
+// Streaming (hada "3-stufiges adaptives Caching", "SLEP-Streaming ... Double
+// Buffering"; hotdry "gpu-nvme-direct的实现架构": two staging buffers, copy and
+// compute overlapped on CUDA streams): layers >= n_resident live in page-locked
+// host memory; each step copies layer l into staging buffer (l - n_resident) % 2
+// on a copy stream while layer l-1 computes; the copy into a buffer waits for
+// the compute that last read it.
+#include <chrono>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+#include "nt_internal.cuh"
+
+namespace nt {
+
+constexpr int kAttnChunk = 64;      // cached positions per attention CTA
+constexpr int kAttnThreads = 128;
+constexpr uint32_t kUidEmbd = 0x100000u, kUidOutput = 0x100001u, kUidKv = 0x200000u;
+
+// ---------------------------------------------------------------- kernels --
+
+__global__ void k_embed(const QMat e, const int32_t* __restrict__ d_token, float* __restrict__ x) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= e.cols) return;
+  int64_t tok = *d_token;
+  if (tok < 0 || tok >= e.rows) tok = 0;   // ids come validated from the host or from k_argmax
+  x[i] = dequant_elem(e, tok * e.cols + i);
+}
+
+// One CTA per (kv head g, chunk of kAttnChunk cached positions): scores of the
+// G = n_heads/n_kv_heads query heads that share g against the chunk's keys,
+// chunk-local softmax statistics (max, sum of exp) and the unnormalised
+// exp-weighted sum of the chunk's values.  Keys and values are read once per
+// kv head for the whole query group.
+template <int HD>
+__global__ void __launch_bounds__(kAttnThreads) k_attn(const float* __restrict__ q, const __half* __restrict__ kc,
+                                                       const __half* __restrict__ vc, int max_ctx,
+                                                       const int32_t* __restrict__ d_pos, int G, float scale,
+                                                       float* __restrict__ part_o, float2* __restrict__ part_ml,
+                                                       int n_chunks) {
+  constexpr int C = kAttnChunk, KP = HD + 8;   // padded rows: 16-byte reads of 8 rows hit distinct banks
+  extern __shared__ uint4 smem_u4[];
+  __half* Ks = reinterpret_cast<__half*>(smem_u4);
+  __half* Vs = Ks + C * KP;
+  float* qs = reinterpret_cast<float*>(Vs + C * KP);
+  float* S = qs + G * HD;
+  const int g = blockIdx.x, chunk = blockIdx.y, tid = threadIdx.x;
+  const int n = *d_pos + 1;                    // positions 0..pos are attended (current one stored first)
+  const int t0 = chunk * C;
+  if (t0 >= n) return;
+  const int cnt = min(C, n - t0);
+  const __half* kb = kc + (int64_t(g) * max_ctx + t0) * HD;
+  const __half* vb = vc + (int64_t(g) * max_ctx + t0) * HD;
+  constexpr int VPR = HD / 8;
+  for (int i = tid; i < cnt * VPR; i += blockDim.x) {
+    const int r = i / VPR, c = i % VPR;
+    *reinterpret_cast<uint4*>(Ks + r * KP + c * 8) = __ldg(reinterpret_cast<const uint4*>(kb + r * HD + c * 8));
+    *reinterpret_cast<uint4*>(Vs + r * KP + c * 8) = __ldg(reinterpret_cast<const uint4*>(vb + r * HD + c * 8));
+  }
+  for (int i = tid; i < G * HD; i += blockDim.x) qs[i] = q[int64_t(g) * G * HD + i];
+  __syncthreads();
+  for (int i = tid; i < G * C; i += blockDim.x) {
+    const int h = i / C, c = i % C;
+    float s = -INFINITY;
+    if (c < cnt) {
+      const __half* kr = Ks + c * KP;
+      const float* qh = qs + h * HD;
+      float acc = 0.f;
+#pragma unroll 4
+      for (int d = 0; d < HD; d += 8) {
+        const uint4 kv = *reinterpret_cast<const uint4*>(kr + d);
+        const __half2* k2 = reinterpret_cast<const __half2*>(&kv);
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+          const float2 f = __half22float2(k2[j]);
+          acc = fmaf(qh[d + 2 * j], f.x, acc);
+          acc = fmaf(qh[d + 2 * j + 1], f.y, acc);
+        }
+      }
+      s = acc * scale;
+    }
+    S[i] = s;
+  }
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int h = warp; h < G; h += blockDim.x / 32) {
+    float mx = -INFINITY;
+    for (int c = lane; c < C; c += 32) mx = fmaxf(mx, S[h * C + c]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float l = 0.f;
+    for (int c = lane; c < C; c += 32) {
+      const float e = c < cnt ? expf(S[h * C + c] - mx) : 0.f;
+      S[h * C + c] = e;
+      l += e;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if (lane == 0) part_ml[int64_t(g * G + h) * n_chunks + chunk] = make_float2(mx, l);
+  }
+  __syncthreads();
+  for (int i = tid; i < G * HD; i += blockDim.x) {
+    const int h = i / HD, d = i % HD;
+    float acc = 0.f;
+    for (int c = 0; c < cnt; c++) acc = fmaf(S[h * C + c], __half2float(Vs[c * KP + d]), acc);
+    part_o[(int64_t(g * G + h) * n_chunks + chunk) * HD + d] = acc;
+  }
+}
+
+// Merges the chunks of query head j: M = max m_c, L = sum l_c e^(m_c - M),
+// o = sum o_c e^(m_c - M) / L.
+__global__ void k_attn_combine(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
+                               const int32_t* __restrict__ d_pos, int n_chunks, int hd, float* __restrict__ out) {
+  const int j = blockIdx.x;
+  const int used = (*d_pos + 1 + kAttnChunk - 1) / kAttnChunk;
+  float M = -INFINITY;
+  for (int c = 0; c < used; c++) M = fmaxf(M, part_ml[int64_t(j) * n_chunks + c].x);
+  for (int d = threadIdx.x; d < hd; d += blockDim.x) {
+    float L = 0.f, o = 0.f;
+    for (int c = 0; c < used; c++) {
+      const float2 ml = part_ml[int64_t(j) * n_chunks + c];
+      const float w = expf(ml.x - M);
+      L += ml.y * w;
+      o += part_o[(int64_t(j) * n_chunks + c) * hd + d] * w;
+    }
+    out[int64_t(j) * hd + d] = o / L;
+  }
+}
+
+__device__ __forceinline__ void top2_merge(float b2, int i2, float s2, float& b, int& bi, float& s) {
+  if (i2 == 0x7fffffff) return;
+  if (b2 > b || (b2 == b && i2 < bi)) {
+    s = fmaxf(s2, b);
+    b = b2;
+    bi = i2;
+  } else {
+    s = fmaxf(s, b2);
+  }
+}
+
+// Greedy choice over the per-CTA top-2 summaries of the output GEMV (ties to the
+// lowest id), then the step's bookkeeping: next input token, history, position.
+__global__ void k_argmax(const float4* __restrict__ top2, int n, int32_t* d_pos, int32_t* d_token,
+                         int32_t* d_next, float* d_margin, int32_t* d_hist, int max_ctx, int vocab) {
+  __shared__ float sb[256], ss[256];
+  __shared__ int si[256];
+  float b = -INFINITY, s = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const float4 v = top2[i];
+    top2_merge(v.x, __float_as_int(v.y), v.z, b, bi, s);
+  }
+  sb[threadIdx.x] = b;
+  ss[threadIdx.x] = s;
+  si[threadIdx.x] = bi;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int t = 1; t < blockDim.x; t++) top2_merge(sb[t], si[t], ss[t], b, bi, s);
+    if (bi < 0 || bi >= vocab) bi = 0;     // no finite logit at all: keep the id in range
+    const int p = *d_pos;
+    *d_next = bi;
+    *d_margin = b - s;
+    if (p < max_ctx) d_hist[p] = bi;
+    *d_token = bi;
+    *d_pos = p + 1;
+  }
+}
+
+// f16 N(0,1) prefill; counter index of (t, kv head g, d) is (t*n_kv + g)*hd + d.
+__global__ void k_kv_prefill(__half* kv, int n_layers, int n_kv, int max_ctx, int hd, int n_ctx, uint64_t seed) {
+  const int64_t per = int64_t(n_ctx) * n_kv * hd;
+  const int64_t total = int64_t(n_layers) * 2 * per;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t lk = i / per, r = i % per;    // lk = layer*2 + kv
+    const int64_t t = r / (int64_t(n_kv) * hd);
+    const int g = int((r / hd) % n_kv), d = int(r % hd);
+    const float z = __fmul_rn(gen_normal(seed, kUidKv + uint32_t(lk), uint64_t(r)), 1.0f);
+    kv[((lk * n_kv + g) * max_ctx + t) * hd + d] = __float2half_rn(z);
+  }
+}
+
+// ------------------------------------------------------------------ model --
+
+struct Layer {
+  uint8_t* dev = nullptr;    // device blob (resident layers)
+  uint8_t* host = nullptr;   // page-locked host blob (streamed layers)
+  size_t bytes = 0;          // padded blob bytes
+  size_t off[7] = {};        // per-role offset inside the blob
+  int64_t rows[7] = {}, cols[7] = {};
+  int type[7] = {};
+  nt_qtensor view[7];        // what nt_model_tensor hands out
+};
+
+struct Prof {
+  struct Rec {
+    int kind;
+    double bytes;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> pool;
+  size_t used = 0;
+  cudaEvent_t ev() {
+    if (used == pool.size()) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+      pool.push_back(e);
+    }
+    return pool[used++];
+  }
+  ~Prof() {
+    for (auto e : pool) cudaEventDestroy(e);
+  }
+};
+
+}  // namespace nt
+
+struct nt_model {
+  nt_config c{};
+  std::vector<nt::Layer> layers;
+  nt_qtensor embd, output;
+  __half* kv = nullptr;
+  float *x = nullptr, *q = nullptr, *att = nullptr, *u = nullptr, *logits = nullptr;
+  float* part_o = nullptr;
+  float2* part_ml = nullptr;
+  float2* rope = nullptr;
+  float4* top2 = nullptr;
+  int32_t* small = nullptr;          // pos, token, next, margin(float bits)
+  int32_t* hist = nullptr;           // produced ids by position
+  int32_t* h_io = nullptr;           // pinned host mirror of small
+  int n_chunks = 0;
+  cudaStream_t stream = nullptr, copy_stream = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int out_grid = 0;
+  int32_t pos = 0;
+  int n_resident = 0;
+  uint8_t* staging[2] = {nullptr, nullptr};
+  cudaEvent_t ev_copy_done[2] = {}, ev_compute_done[2] = {};
+  std::vector<cudaEvent_t> ev_cs, ev_ce, ev_ls, ev_le;
+  cudaEvent_t ev_step0 = nullptr, ev_step1 = nullptr;
+  nt_stats stats{};
+  size_t dev_bytes = 0, dev_limit = 0;
+  std::vector<void*> dev_allocs;
+};
+
+namespace nt {
+
+static int32_t* d_pos(nt_model* m) { return m->small + 0; }
+static int32_t* d_token(nt_model* m) { return m->small + 1; }
+static int32_t* d_next(nt_model* m) { return m->small + 2; }
+static float* d_margin(nt_model* m) { return reinterpret_cast<float*>(m->small + 3); }
+
+static cudaError_t dev_alloc(nt_model* m, void** p, size_t bytes) {
+  if (m->dev_limit && m->dev_bytes + bytes > m->dev_limit) return cudaErrorMemoryAllocation;
+  cudaError_t e = cudaMalloc(p, bytes ? bytes : 1);
+  if (e == cudaSuccess) {
+    m->dev_bytes += bytes;
+    m->dev_allocs.push_back(*p);
+  }
+  return e;
+}
+
+static void dev_free(nt_model* m, void* p) {
+  if (!p) return;
+  for (size_t i = 0; i < m->dev_allocs.size(); i++)
+    if (m->dev_allocs[i] == p) {
+      m->dev_allocs.erase(m->dev_allocs.begin() + long(i));
+      break;
+    }
+  cudaFree(p);
+}
+
+static QMat view_at(const Layer& L, int role, uint8_t* base) {
+  QMat q;
+  q.type = L.type[role];
+  q.rows = L.rows[role];
+  q.cols = L.cols[role];
+  layout_streams(q, base + L.off[role]);
+  return q;
+}
+
+static int64_t kv_layer_elems(const nt_config& c) { return int64_t(c.n_kv_heads) * c.max_ctx * c.head_dim; }
+static __half* k_cache(nt_model* m, int l) { return m->kv + (int64_t(l) * 2 + 0) * kv_layer_elems(m->c); }
+static __half* v_cache(nt_model* m, int l) { return m->kv + (int64_t(l) * 2 + 1) * kv_layer_elems(m->c); }
+
+static double qbytes(const QMat& q) { return double(stream_sizes(q.type, q.rows, q.cols).total()); }
+
+// Launch helper: optional event pair around each launch for nt_profile_steps.
+struct Launcher {
+  Prof* prof = nullptr;
+  cudaStream_t s = nullptr;
+  template <class F>
+  cudaError_t run(int kind, double bytes, F&& f) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (prof) {
+      a = prof->ev();
+      b = prof->ev();
+      if (!a || !b) return cudaErrorMemoryAllocation;
+      cudaError_t e = cudaEventRecord(a, s);
+      if (e != cudaSuccess) return e;
+    }
+    cudaError_t e = f();
+    if (e != cudaSuccess) return e;
+    if (prof) {
+      e = cudaEventRecord(b, s);
+      if (e != cudaSuccess) return e;
+      prof->recs.push_back({kind, bytes, a, b});
+    }
+    return cudaSuccess;
+  }
+};
+
+static cudaError_t enqueue_layer(nt_model* m, int l, uint8_t* base, Launcher& L, bool pdl) {
+  const nt_config& c = m->c;
+  const Layer& ly = m->layers[size_t(l)];
+  const int hd = c.head_dim, G = c.n_heads / c.n_kv_heads;
+  const int qd = c.n_heads * hd, kd = c.n_kv_heads * hd;
+  cudaStream_t s = L.s;
+  cudaError_t e;
+
+  // RMSNorm -> Q|K|V -> RoPE -> cache
+  GemvArgs a;
+  a.x = m->x;
+  a.norm = 1;
+  a.eps = c.rms_eps;
+  a.epi.y = m->q;
+  a.epi.q_rows = qd;
+  a.epi.k_rows = kd;
+  a.epi.head_dim = hd;
+  a.epi.pos = d_pos(m);
+  a.epi.rope = m->rope;
+  a.epi.k_cache = k_cache(m, l);
+  a.epi.v_cache = v_cache(m, l);
+  a.epi.max_ctx = c.max_ctx;
+  a.seg[0] = view_at(ly, NT_ROLE_Q, base);
+  a.seg[1] = view_at(ly, NT_ROLE_K, base);
+  if (c.t_v == c.t_q) {
+    a.seg[2] = view_at(ly, NT_ROLE_V, base);
+    a.nseg = 3;
+    const double by = qbytes(a.seg[0]) + qbytes(a.seg[1]) + qbytes(a.seg[2]) + 4.0 * (c.hidden + qd) + 4.0 * kd;
+    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(a, EPI_QKV, s, pdl, nullptr); }))) return e;
+  } else {
+    a.nseg = 2;
+    double by = qbytes(a.seg[0]) + qbytes(a.seg[1]) + 4.0 * (c.hidden + qd) + 2.0 * kd;
+    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(a, EPI_QKV, s, pdl, nullptr); }))) return e;
+    GemvArgs b = a;
+    b.seg[0] = view_at(ly, NT_ROLE_V, base);
+    b.nseg = 1;
+    b.epi.row_base = qd + kd;
+    by = qbytes(b.seg[0]) + 4.0 * c.hidden + 2.0 * kd;
+    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(b, EPI_QKV, s, pdl, nullptr); }))) return e;
+  }
+
+  // split-context GQA attention over positions 0..pos
+  {
+    const int n_used = m->pos + 1;   // host mirror (exact for profiled and streamed steps)
+    const double by = 2.0 * 2.0 * double(c.n_kv_heads) * n_used * hd + 8.0 * qd;
+    const size_t smem = size_t(2 * kAttnChunk * (hd + 8)) * 2 + size_t(G * hd + G * kAttnChunk) * 4;
+    const float scale = 1.0f / sqrtf(float(hd));
+    dim3 grid(unsigned(c.n_kv_heads), unsigned(m->n_chunks));
+    e = L.run(NT_KC_ATTN, by, [&] {
+      if (hd == 128)
+        k_attn<128><<<grid, kAttnThreads, smem, s>>>(m->q, k_cache(m, l), v_cache(m, l), c.max_ctx, d_pos(m), G,
+                                                     scale, m->part_o, m->part_ml, m->n_chunks);
+      else
+        k_attn<64><<<grid, kAttnThreads, smem, s>>>(m->q, k_cache(m, l), v_cache(m, l), c.max_ctx, d_pos(m), G,
+                                                    scale, m->part_o, m->part_ml, m->n_chunks);
+      return cudaGetLastError();
+    });
+    if (e) return e;
+    e = L.run(NT_KC_ATTN, 0.0, [&] {
+      k_attn_combine<<<unsigned(c.n_heads), unsigned(hd), 0, s>>>(m->part_o, m->part_ml, d_pos(m), m->n_chunks, hd,
+                                                                   m->att);
+      return cudaGetLastError();
+    });
+    if (e) return e;
+  }
+
+  // O + residual
+  {
+    GemvArgs o;
+    o.seg[0] = view_at(ly, NT_ROLE_O, base);
+    o.x = m->att;
+    o.epi.y = m->x;
+    const double by = qbytes(o.seg[0]) + 4.0 * qd + 8.0 * c.hidden;
+    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(o, EPI_ADD, s, pdl, nullptr); }))) return e;
+  }
+  // RMSNorm -> gate|up -> SwiGLU
+  {
+    GemvArgs gu;
+    gu.seg[0] = view_at(ly, NT_ROLE_GATE, base);
+    gu.seg[1] = view_at(ly, NT_ROLE_UP, base);
+    gu.nseg = 2;
+    gu.interleave = 1;
+    gu.x = m->x;
+    gu.norm = 1;
+    gu.eps = c.rms_eps;
+    gu.epi.y = m->u;
+    const double by = qbytes(gu.seg[0]) + qbytes(gu.seg[1]) + 4.0 * c.hidden + 4.0 * c.ffn_dim;
+    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(gu, EPI_SWIGLU, s, pdl, nullptr); }))) return e;
+  }
+  // down + residual
+  {
+    GemvArgs dn;
+    dn.seg[0] = view_at(ly, NT_ROLE_DOWN, base);
+    dn.x = m->u;
+    dn.epi.y = m->x;
+    const double by = qbytes(dn.seg[0]) + 4.0 * c.ffn_dim + 8.0 * c.hidden;
+    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(dn, EPI_ADD, s, pdl, nullptr); }))) return e;
+  }
+  return cudaSuccess;
+}
+
+static cudaError_t enqueue_head(nt_model* m, Launcher& L) {
+  const nt_config& c = m->c;
+  cudaStream_t s = L.s;
+  GemvArgs a;
+  a.seg[0] = m->output.m;
+  a.x = m->x;
+  a.norm = 1;
+  a.eps = c.rms_eps;
+  a.epi.y = m->logits;
+  a.epi.top2 = m->top2;
+  const double by = qbytes(a.seg[0]) + 4.0 * c.hidden + 4.0 * c.vocab;
+  cudaError_t e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(a, EPI_LOGITS, s, false, &m->out_grid); });
+  if (e) return e;
+  return L.run(NT_KC_OTHER, 0.0, [&] {
+    k_argmax<<<1, 256, 0, s>>>(m->top2, m->out_grid, d_pos(m), d_token(m), d_next(m), d_margin(m), m->hist,
+                               c.max_ctx, c.vocab);
+    return cudaGetLastError();
+  });
+}
+
+static cudaError_t enqueue_embed(nt_model* m, Launcher& L) {
+  return L.run(NT_KC_OTHER, 0.0, [&] {
+    k_embed<<<unsigned((m->c.hidden + 255) / 256), 256, 0, L.s>>>(m->embd.m, d_token(m), m->x);
+    return cudaGetLastError();
+  });
+}
+
+// Whole step for a model whose layers are all resident.
+static cudaError_t enqueue_resident(nt_model* m, Launcher& L, bool pdl) {
+  cudaError_t e = enqueue_embed(m, L);
+  for (int l = 0; l < m->c.n_layers && !e; l++) e = enqueue_layer(m, l, m->layers[size_t(l)].dev, L, pdl);
+  if (!e) e = enqueue_head(m, L);
+  return e;
+}
+
+// Whole step with layers [n_resident, n_layers) copied through the staging buffers.
+static cudaError_t enqueue_streamed(nt_model* m, Launcher& L) {
+  const int nl = m->c.n_layers, nr = m->n_resident;
+  cudaStream_t s = L.s, cs = m->copy_stream;
+  cudaError_t e;
+  auto issue_copy = [&](int l) -> cudaError_t {
+    const int b = (l - nr) & 1;
+    cudaError_t er = cudaStreamWaitEvent(cs, m->ev_compute_done[b], 0);
+    if (!er) er = cudaEventRecord(m->ev_cs[size_t(l)], cs);
+    if (!er) er = cudaMemcpyAsync(m->staging[b], m->layers[size_t(l)].host, m->layers[size_t(l)].bytes,
+                                  cudaMemcpyHostToDevice, cs);
+    if (!er) er = cudaEventRecord(m->ev_ce[size_t(l)], cs);
+    if (!er) er = cudaEventRecord(m->ev_copy_done[b], cs);
+    return er;
+  };
+  for (int l = nr; l < nl && l < nr + 2; l++)
+    if ((e = issue_copy(l))) return e;
+  if ((e = enqueue_embed(m, L))) return e;
+  for (int l = 0; l < nl; l++) {
+    const bool streamed = l >= nr;
+    const int b = (l - nr) & 1;
+    uint8_t* base = streamed ? m->staging[b] : m->layers[size_t(l)].dev;
+    if (streamed && (e = cudaStreamWaitEvent(s, m->ev_copy_done[b], 0))) return e;
+    if ((e = cudaEventRecord(m->ev_ls[size_t(l)], s))) return e;
+    if ((e = enqueue_layer(m, l, base, L, false))) return e;
+    if ((e = cudaEventRecord(m->ev_le[size_t(l)], s))) return e;
+    if (streamed) {
+      if ((e = cudaEventRecord(m->ev_compute_done[b], s))) return e;
+      if (l + 2 < nl && (e = issue_copy(l + 2))) return e;
+    }
+  }
+  return enqueue_head(m, L);
+}
+
+static double watchdog_ms() {
+  const char* v = getenv("NT_WATCHDOG_MS");
+  return v ? atof(v) : 120000.0;
+}
+
+// Waits for an event with a host-side time limit (NT_E_TIMEOUT when it expires).
+static nt_status wait_event(cudaEvent_t ev, const char* what) {
+  const auto t0 = std::chrono::steady_clock::now();
+  const double limit = watchdog_ms();
+  for (;;) {
+    cudaError_t e = cudaEventQuery(ev);
+    if (e == cudaSuccess) return NT_OK;
+    if (e != cudaErrorNotReady) return cuda_fail(e, what);
+    const double ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+    if (ms > limit) return fail(NT_E_TIMEOUT, std::string(what) + ": device did not finish within the watchdog limit");
+    std::this_thread::sleep_for(std::chrono::microseconds(ms < 5.0 ? 2 : 200));
+  }
+}
+
+static void drop_graph(nt_model* m) {
+  if (m->exec) cudaGraphExecDestroy(m->exec);
+  if (m->graph) cudaGraphDestroy(m->graph);
+  m->exec = nullptr;
+  m->graph = nullptr;
+}
+
+static nt_status ensure_graph(nt_model* m) {
+  if (m->exec) return NT_OK;
+  Launcher L;
+  L.s = m->stream;
+  NT_CUDA(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal));
+  cudaError_t e = enqueue_resident(m, L, true);
+  cudaGraph_t g = nullptr;
+  cudaError_t e2 = cudaStreamEndCapture(m->stream, &g);
+  if (e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    return cuda_fail(e, "decode step capture");
+  }
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaStreamEndCapture");
+  m->graph = g;
+  e = cudaGraphInstantiate(&m->exec, g, 0);
+  if (e != cudaSuccess) {
+    drop_graph(m);
+    return cuda_fail(e, "cudaGraphInstantiate");
+  }
+  return NT_OK;
+}
+
+static void free_model(nt_model* m) {
+  if (!m) return;
+  if (m->stream) cudaStreamSynchronize(m->stream);
+  if (m->copy_stream) cudaStreamSynchronize(m->copy_stream);
+  drop_graph(m);
+  for (auto& L : m->layers)
+    if (L.host) cudaFreeHost(L.host);
+  for (void* p : m->dev_allocs) cudaFree(p);
+  m->dev_allocs.clear();
+  if (m->h_io) cudaFreeHost(m->h_io);
+  for (int b = 0; b < 2; b++) {
+    if (m->ev_copy_done[b]) cudaEventDestroy(m->ev_copy_done[b]);
+    if (m->ev_compute_done[b]) cudaEventDestroy(m->ev_compute_done[b]);
+  }
+  for (auto* v : {&m->ev_cs, &m->ev_ce, &m->ev_ls, &m->ev_le})
+    for (auto e : *v) cudaEventDestroy(e);
+  if (m->ev_step0) cudaEventDestroy(m->ev_step0);
+  if (m->ev_step1) cudaEventDestroy(m->ev_step1);
+  if (m->stream) cudaStreamDestroy(m->stream);
+  if (m->copy_stream) cudaStreamDestroy(m->copy_stream);
+  delete m;
+}
+
+static nt_status validate(const nt_config* c) {
+  if (c->n_layers < 0 || c->hidden <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 ||
+      c->ffn_dim <= 0 || c->vocab <= 0 || c->max_ctx <= 0)
+    return fail(NT_E_INVAL, "nt_model_create: sizes must be positive");
+  if (c->n_heads % c->n_kv_heads) return fail(NT_E_INVAL, "nt_model_create: n_heads must be a multiple of n_kv_heads");
+  if (c->head_dim != 64 && c->head_dim != 128) return fail(NT_E_UNSUPPORTED, "nt_model_create: head_dim must be 64 or 128");
+  if (c->n_heads / c->n_kv_heads > 16) return fail(NT_E_UNSUPPORTED, "nt_model_create: more than 16 query heads per kv head");
+  const nt_qtype ts[9] = {c->t_embd, c->t_q, c->t_k, c->t_v, c->t_o, c->t_gate, c->t_up, c->t_down, c->t_out};
+  for (nt_qtype t : ts) {
+    if (t == NT_F32 || t == NT_F16) return fail(NT_E_UNSUPPORTED, "nt_model_create: F32/F16 weights are not implemented");
+    if (!supported_weight_type(t)) return fail(NT_E_INVAL, "nt_model_create: unknown weight type");
+  }
+  if (c->t_q != c->t_k) return fail(NT_E_UNSUPPORTED, "nt_model_create: q and k must share a format");
+  if (c->t_gate != c->t_up) return fail(NT_E_UNSUPPORTED, "nt_model_create: gate and up must share a format");
+  const int64_t h = c->hidden, qd = int64_t(c->n_heads) * c->head_dim, f = c->ffn_dim;
+  auto ok = [](nt_qtype t, int64_t cols) { return cols % block_elems(t) == 0 && cols <= 32768 && cols % 32 == 0; };
+  if (!ok(c->t_embd, h) || !ok(c->t_out, h) || !ok(c->t_q, h) || !ok(c->t_v, h) || !ok(c->t_gate, h) ||
+      !ok(c->t_o, qd) || !ok(c->t_down, f))
+    return fail(NT_E_INVAL, "nt_model_create: a column count is not a multiple of its format's block (or > 32768)");
+  if (int64_t(c->vocab) * h >= (int64_t(1) << 40)) return fail(NT_E_INVAL, "nt_model_create: vocab too large");
+  if (c->n_layers * 16 + 16 >= 0x100000) return fail(NT_E_INVAL, "nt_model_create: too many layers");
+  return NT_OK;
+}
+
+}  // namespace nt
+
+using namespace nt;
+
+extern "C" {
+
+nt_status nt_model_create(const nt_config* cfg, nt_model** out) {
+  if (!cfg || !out) return fail(NT_E_INVAL, "nt_model_create: NULL argument");
+  nt_status st = validate(cfg);
+  if (st) return st;
+  nt_model* m = new (std::nothrow) nt_model();
+  if (!m) return fail(NT_E_NOMEM, "nt_model_create: host allocation failed");
+  m->c = *cfg;
+  const nt_config& c = m->c;
+  if (const char* lim = getenv("NT_DEVICE_BYTES_LIMIT")) m->dev_limit = size_t(strtoull(lim, nullptr, 10));
+  cudaError_t e;
+#define NT_TRY(call, what)            \
+  do {                                \
+    e = (call);                       \
+    if (e != cudaSuccess) {           \
+      nt_status s_ = cuda_fail(e, what); \
+      free_model(m);                  \
+      return s_;                      \
+    }                                 \
+  } while (0)
+  NT_TRY(cudaStreamCreateWithFlags(&m->stream, cudaStreamNonBlocking), "cudaStreamCreate");
+  NT_TRY(cudaStreamCreateWithFlags(&m->copy_stream, cudaStreamNonBlocking), "cudaStreamCreate");
+  for (int b = 0; b < 2; b++) {
+    NT_TRY(cudaEventCreateWithFlags(&m->ev_copy_done[b], cudaEventDisableTiming), "cudaEventCreate");
+    NT_TRY(cudaEventCreateWithFlags(&m->ev_compute_done[b], cudaEventDisableTiming), "cudaEventCreate");
+  }
+  NT_TRY(cudaEventCreate(&m->ev_step0), "cudaEventCreate");
+  NT_TRY(cudaEventCreate(&m->ev_step1), "cudaEventCreate");
+  for (auto* v : {&m->ev_cs, &m->ev_ce, &m->ev_ls, &m->ev_le}) {
+    v->resize(size_t(c.n_layers));
+    for (auto& ev : *v) NT_TRY(cudaEventCreate(&ev), "cudaEventCreate");
+  }
+
+  const int64_t h = c.hidden, hd = c.head_dim, qd = int64_t(c.n_heads) * hd, kd = int64_t(c.n_kv_heads) * hd;
+  // weights
+  m->layers.resize(size_t(c.n_layers));
+  const nt_qtype types[7] = {c.t_q, c.t_k, c.t_v, c.t_o, c.t_gate, c.t_up, c.t_down};
+  const int64_t rows[7] = {qd, kd, kd, h, c.ffn_dim, c.ffn_dim, h};
+  const int64_t colsv[7] = {h, h, h, qd, h, h, c.ffn_dim};
+  for (int l = 0; l < c.n_layers; l++) {
+    Layer& L = m->layers[size_t(l)];
+    size_t off = 0;
+    for (int r = 0; r < 7; r++) {
+      L.type[r] = types[r];
+      L.rows[r] = rows[r];
+      L.cols[r] = colsv[r];
+      L.off[r] = off;
+      off += stream_sizes(types[r], rows[r], colsv[r]).padded_total();
+    }
+    L.bytes = off;
+    NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&L.dev), L.bytes), "nt_model_create: layer allocation");
+    for (int r = 0; r < 7; r++) {
+      nt_qtensor& v = L.view[r];
+      v.m = view_at(L, r, L.dev);
+      v.nbytes = stream_sizes(types[r], rows[r], colsv[r]).total();
+      NT_TRY(launch_generate(v.m, c.seed, uint32_t(l * 16 + r), c.init_std, m->stream), "generate layer");
+    }
+  }
+  auto make_big = [&](nt_qtensor& t, nt_qtype ty, uint32_t uid) -> cudaError_t {
+    t.m.type = ty;
+    t.m.rows = c.vocab;
+    t.m.cols = h;
+    StreamSizes ss = stream_sizes(ty, c.vocab, h);
+    t.nbytes = ss.total();
+    cudaError_t er = dev_alloc(m, reinterpret_cast<void**>(&t.base), ss.padded_total());
+    if (er) return er;
+    layout_streams(t.m, t.base);
+    return launch_generate(t.m, c.seed, uid, c.init_std, m->stream);
+  };
+  NT_TRY(make_big(m->embd, c.t_embd, kUidEmbd), "nt_model_create: token_embd");
+  NT_TRY(make_big(m->output, c.t_out, kUidOutput), "nt_model_create: output");
+
+  // cache, activations, partials
+  const size_t kv_elems = size_t(c.n_layers) * 2 * size_t(kv_layer_elems(c));
+  NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->kv), kv_elems * 2), "nt_model_create: KV cache");
+  NT_TRY(cudaMemsetAsync(m->kv, 0, kv_elems * 2, m->stream), "cudaMemset");
+  m->n_chunks = int((c.max_ctx + kAttnChunk - 1) / kAttnChunk);
+  NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->x), size_t(h) * 4), "alloc x");
+  NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->q), size_t(qd) * 4), "alloc q");
+  NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->att), size_t(qd) * 4), "alloc att");
+  NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->u), size_t(c.ffn_dim) * 4), "alloc u");
+  NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->logits), size_t(c.vocab) * 4), "alloc logits");
+  NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->part_o), size_t(qd) * m->n_chunks * 4), "alloc partials");
+  NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->part_ml), size_t(c.n_heads) * m->n_chunks * 8), "alloc partials");
+  NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->top2), size_t(kMaxGemvGrid) * 16), "alloc top2");
+  NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->small), 16 * 4), "alloc small");
+  NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->hist), size_t(c.max_ctx) * 4), "alloc hist");
+  NT_TRY(cudaMemsetAsync(m->small, 0, 16 * 4, m->stream), "cudaMemset");
+  NT_TRY(cudaMemsetAsync(m->hist, 0xff, size_t(c.max_ctx) * 4, m->stream), "cudaMemset");
+  NT_TRY(cudaHostAlloc(reinterpret_cast<void**>(&m->h_io), 16 * 4, cudaHostAllocDefault), "cudaHostAlloc");
+  // RoPE table in double: angle p * theta^(-2i/head_dim)
+  {
+    NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->rope), size_t(c.max_ctx) * (hd / 2) * 8), "alloc rope");
+    std::vector<float2> tab(size_t(c.max_ctx) * size_t(hd / 2));
+    for (int p = 0; p < c.max_ctx; p++)
+      for (int i = 0; i < hd / 2; i++) {
+        const double ang = double(p) * std::pow(double(c.rope_theta), -2.0 * i / double(hd));
+        tab[size_t(p) * (hd / 2) + i] = make_float2(float(std::cos(ang)), float(std::sin(ang)));
+      }
+    NT_TRY(cudaMemcpyAsync(m->rope, tab.data(), tab.size() * 8, cudaMemcpyHostToDevice, m->stream), "rope upload");
+    NT_TRY(cudaStreamSynchronize(m->stream), "nt_model_create");
+  }
+  m->n_resident = c.n_layers;
+  m->stats.n_resident = c.n_layers;
+#undef NT_TRY
+  *out = m;
+  return NT_OK;
+}
+
+void nt_model_destroy(nt_model* m) { free_model(m); }
+
+static nt_status set_pos(nt_model* m, int32_t p) {
+  m->h_io[0] = p;
+  NT_CUDA(cudaMemcpyAsync(d_pos(m), m->h_io, 4, cudaMemcpyHostToDevice, m->stream));
+  NT_CUDA(cudaStreamSynchronize(m->stream));
+  m->pos = p;
+  return NT_OK;
+}
+
+nt_status nt_kv_reset(nt_model* m) {
+  if (!m) return fail(NT_E_INVAL, "nt_kv_reset: model is NULL");
+  m->stats.steps = 0;
+  return set_pos(m, 0);
+}
+
+nt_status nt_kv_prefill(nt_model* m, int32_t n_ctx, uint64_t seed) {
+  if (!m) return fail(NT_E_INVAL, "nt_kv_prefill: model is NULL");
+  if (n_ctx < 0 || n_ctx > m->c.max_ctx) return fail(NT_E_INVAL, "nt_kv_prefill: n_ctx outside [0, max_ctx]");
+  if (n_ctx > 0 && m->c.n_layers > 0) {
+    const nt_config& c = m->c;
+    k_kv_prefill<<<152 * 16, 256, 0, m->stream>>>(m->kv, c.n_layers, c.n_kv_heads, c.max_ctx, c.head_dim, n_ctx, seed);
+    NT_CUDA(cudaGetLastError());
+  }
+  return set_pos(m, n_ctx);
+}
+
+nt_status nt_decode_step(nt_model* m, int32_t token, int32_t* next_token, float* logits_host, float* top2_margin) {
+  if (!m || !next_token) return fail(NT_E_INVAL, "nt_decode_step: NULL argument");
+  if (token < 0 || token >= m->c.vocab) return fail(NT_E_INVAL, "nt_decode_step: token outside [0, vocab)");
+  if (m->pos >= m->c.max_ctx) return fail(NT_E_INVAL, "nt_decode_step: position reached max_ctx");
+  const bool streamed = m->n_resident < m->c.n_layers;
+  if (!streamed) {
+    nt_status st = ensure_graph(m);
+    if (st) return st;
+  }
+  m->h_io[1] = token;
+  NT_CUDA(cudaMemcpyAsync(d_token(m), m->h_io + 1, 4, cudaMemcpyHostToDevice, m->stream));
+  NT_CUDA(cudaEventRecord(m->ev_step0, m->stream));
+  if (streamed) {
+    Launcher L;
+    L.s = m->stream;
+    cudaError_t e = enqueue_streamed(m, L);
+    if (e) return cuda_fail(e, "nt_decode_step: streamed step");
+  } else {
+    NT_CUDA(cudaGraphLaunch(m->exec, m->stream));
+  }
+  NT_CUDA(cudaEventRecord(m->ev_step1, m->stream));
+  NT_CUDA(cudaMemcpyAsync(m->h_io + 2, d_next(m), 8, cudaMemcpyDeviceToHost, m->stream));
+  if (logits_host)
+    NT_CUDA(cudaMemcpyAsync(logits_host, m->logits, size_t(m->c.vocab) * 4, cudaMemcpyDeviceToHost, m->stream));
+  cudaEvent_t done = m->ev_step1;
+  nt_status st = wait_event(done, "nt_decode_step");
+  if (st) return st;
+  NT_CUDA(cudaStreamSynchronize(m->stream));
+  float ms = 0.f;
+  NT_CUDA(cudaEventElapsedTime(&ms, m->ev_step0, m->ev_step1));
+  m->stats.last_step_ms = ms;
+  m->stats.steps++;
+  if (streamed) {
+    double h2d = 0, cms = 0, bytes = 0;
+    for (int l = 0; l < m->c.n_layers; l++) {
+      float t = 0.f;
+      NT_CUDA(cudaEventElapsedTime(&t, m->ev_ls[size_t(l)], m->ev_le[size_t(l)]));
+      cms += t;
+      if (l >= m->n_resident) {
+        NT_CUDA(cudaEventElapsedTime(&t, m->ev_cs[size_t(l)], m->ev_ce[size_t(l)]));
+        h2d += t;
+        bytes += double(m->layers[size_t(l)].bytes);
+      }
+    }
+    m->stats.h2d_ms = h2d;
+    m->stats.h2d_bytes = bytes;
+    m->stats.compute_ms = cms;
+    const double mn = h2d < cms ? h2d : cms;
+    double ov = mn > 0 ? (h2d + cms - ms) / mn : 0.0;
+    m->stats.overlap = ov < 0 ? 0 : (ov > 1 ? 1 : ov);
+  } else {
+    m->stats.h2d_ms = m->stats.h2d_bytes = m->stats.overlap = 0;
+    m->stats.compute_ms = ms;
+  }
+  m->pos++;
+  *next_token = m->h_io[2];
+  if (top2_margin) memcpy(top2_margin, m->h_io + 3, 4);
+  return NT_OK;
+}
+
+nt_status nt_decode_run(nt_model* m, int32_t token, int32_t n_steps, void* stream) {
+  if (!m) return fail(NT_E_INVAL, "nt_decode_run: model is NULL");
+  if (n_steps < 0 || token < 0 || token >= m->c.vocab) return fail(NT_E_INVAL, "nt_decode_run: bad token or n_steps");
+  if (m->pos + n_steps > m->c.max_ctx) return fail(NT_E_INVAL, "nt_decode_run: would pass max_ctx");
+  if (m->n_resident < m->c.n_layers) return fail(NT_E_STATE, "nt_decode_run: model has streamed layers");
+  nt_status st = ensure_graph(m);
+  if (st) return st;
+  cudaStream_t us = static_cast<cudaStream_t>(stream);
+  NT_CUDA(cudaEventRecord(m->ev_step0, us));
+  NT_CUDA(cudaStreamWaitEvent(m->stream, m->ev_step0, 0));
+  m->h_io[1] = token;
+  NT_CUDA(cudaMemcpyAsync(d_token(m), m->h_io + 1, 4, cudaMemcpyHostToDevice, m->stream));
+  for (int i = 0; i < n_steps; i++) NT_CUDA(cudaGraphLaunch(m->exec, m->stream));
+  NT_CUDA(cudaEventRecord(m->ev_step1, m->stream));
+  NT_CUDA(cudaStreamWaitEvent(us, m->ev_step1, 0));
+  m->pos += n_steps;
+  m->stats.steps += n_steps;
+  return NT_OK;
+}
+
+nt_status nt_get_tokens(nt_model* m, int32_t t0, int32_t n, int32_t* host_out) {
+  if (!m || !host_out) return fail(NT_E_INVAL, "nt_get_tokens: NULL argument");
+  if (t0 < 0 || n < 0 || t0 + n > m->c.max_ctx) return fail(NT_E_INVAL, "nt_get_tokens: range");
+  NT_CUDA(cudaStreamSynchronize(m->stream));
+  NT_CUDA(cudaMemcpy(host_out, m->hist + t0, size_t(n) * 4, cudaMemcpyDeviceToHost));
+  return NT_OK;
+}
+
+nt_status nt_kv_export(nt_model* m, int32_t layer, int32_t kv, int32_t kv_head, int32_t t0, int32_t n,
+                       uint16_t* host_out) {
+  if (!m || !host_out) return fail(NT_E_INVAL, "nt_kv_export: NULL argument");
+  const nt_config& c = m->c;
+  if (layer < 0 || layer >= c.n_layers || kv < 0 || kv > 1 || kv_head < 0 || kv_head >= c.n_kv_heads || t0 < 0 ||
+      n < 0 || t0 + n > c.max_ctx)
+    return fail(NT_E_INVAL, "nt_kv_export: index out of range");
+  NT_CUDA(cudaStreamSynchronize(m->stream));
+  const __half* src = (kv ? v_cache(m, layer) : k_cache(m, layer)) + (int64_t(kv_head) * c.max_ctx + t0) * c.head_dim;
+  NT_CUDA(cudaMemcpy(host_out, src, size_t(n) * c.head_dim * 2, cudaMemcpyDeviceToHost));
+  return NT_OK;
+}
+
+nt_status nt_stream_layers(nt_model* m, int32_t n_resident, int32_t n_staging) {
+  if (!m) return fail(NT_E_INVAL, "nt_stream_layers: model is NULL");
+  if (n_staging != 2) return fail(NT_E_UNSUPPORTED, "nt_stream_layers: n_staging must be 2 (double buffering)");
+  if (n_resident < 0 || n_resident > m->c.n_layers) return fail(NT_E_INVAL, "nt_stream_layers: n_resident range");
+  NT_CUDA(cudaStreamSynchronize(m->stream));
+  NT_CUDA(cudaStreamSynchronize(m->copy_stream));
+  drop_graph(m);
+  size_t max_bytes = 0;
+  for (int l = 0; l < m->c.n_layers; l++) {
+    Layer& L = m->layers[size_t(l)];
+    const bool want_dev = l < n_resident;
+    if (want_dev && !L.dev) {
+      cudaError_t e = dev_alloc(m, reinterpret_cast<void**>(&L.dev), L.bytes);
+      if (e) return cuda_fail(e, "nt_stream_layers: device allocation");
+      NT_CUDA(cudaMemcpy(L.dev, L.host, L.bytes, cudaMemcpyHostToDevice));
+      cudaFreeHost(L.host);
+      L.host = nullptr;
+    } else if (!want_dev && !L.host) {
+      cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&L.host), L.bytes, cudaHostAllocDefault);
+      if (e) return cuda_fail(e, "nt_stream_layers: cudaHostAlloc (page-locked tier)");
+      NT_CUDA(cudaMemcpy(L.host, L.dev, L.bytes, cudaMemcpyDeviceToHost));
+      m->dev_bytes -= L.bytes;
+      dev_free(m, L.dev);
+      L.dev = nullptr;
+    }
+    for (int r = 0; r < 7; r++) {
+      L.view[r].m = view_at(L, r, L.dev ? L.dev : L.host);
+      L.view[r].on_host = L.dev ? 0 : 1;
+    }
+    if (!want_dev && L.bytes > max_bytes) max_bytes = L.bytes;
+  }
+  for (int b = 0; b < 2; b++) {
+    if (m->staging[b]) {
+      m->dev_bytes -= 0;
+      dev_free(m, m->staging[b]);
+      m->staging[b] = nullptr;
+    }
+    if (max_bytes) {
+      cudaError_t e = dev_alloc(m, reinterpret_cast<void**>(&m->staging[b]), max_bytes);
+      if (e) return cuda_fail(e, "nt_stream_layers: staging buffer");
+    }
+  }
+  m->n_resident = n_resident;
+  m->stats.n_resident = n_resident;
+  return NT_OK;
+}
+
+nt_status nt_get_stats(const nt_model* m, nt_stats* out) {
+  if (!m || !out) return fail(NT_E_INVAL, "nt_get_stats: NULL argument");
+  *out = m->stats;
+  out->pos = m->pos;
+  int64_t wb = int64_t(m->output.nbytes) + int64_t(m->embd.m.cols) * 0;
+  for (const auto& L : m->layers)
+    for (int r = 0; r < 7; r++) wb += int64_t(L.view[r].nbytes);
+  out->weight_bytes = wb;
+  out->kv_bytes_per_pos = int64_t(m->c.n_layers) * 2 * m->c.n_kv_heads * m->c.head_dim * 2;
+  return NT_OK;
+}
+
+nt_status nt_profile_steps(nt_model* m, int32_t token, int32_t n_steps, nt_kernel_times* out) {
+  if (!m || !out) return fail(NT_E_INVAL, "nt_profile_steps: NULL argument");
+  if (token < 0 || token >= m->c.vocab || n_steps < 1) return fail(NT_E_INVAL, "nt_profile_steps: bad token or n_steps");
+  if (m->pos + n_steps > m->c.max_ctx) return fail(NT_E_INVAL, "nt_profile_steps: would pass max_ctx");
+  if (m->n_resident < m->c.n_layers) return fail(NT_E_STATE, "nt_profile_steps: model has streamed layers");
+  nt_kernel_times t{};
+  double wall = 0;
+  m->h_io[1] = token;
+  NT_CUDA(cudaMemcpyAsync(d_token(m), m->h_io + 1, 4, cudaMemcpyHostToDevice, m->stream));
+  for (int i = 0; i < n_steps; i++) {
+    Prof prof;
+    Launcher L;
+    L.s = m->stream;
+    L.prof = &prof;
+    NT_CUDA(cudaEventRecord(m->ev_step0, m->stream));
+    cudaError_t e = enqueue_resident(m, L, false);
+    if (e) return cuda_fail(e, "nt_profile_steps");
+    NT_CUDA(cudaEventRecord(m->ev_step1, m->stream));
+    nt_status st = wait_event(m->ev_step1, "nt_profile_steps");
+    if (st) return st;
+    float ms;
+    NT_CUDA(cudaEventElapsedTime(&ms, m->ev_step0, m->ev_step1));
+    wall += ms;
+    for (auto& r : prof.recs) {
+      NT_CUDA(cudaEventElapsedTime(&ms, r.a, r.b));
+      t.launches[r.kind]++;
+      t.ms[r.kind] += ms;
+      t.bytes[r.kind] += r.bytes;
+    }
+    m->pos++;
+    m->stats.steps++;
+  }
+  t.step_ms = wall / n_steps;
+  *out = t;
+  return NT_OK;
+}
+
+nt_status nt_model_tensor(const nt_model* m, int32_t layer, int32_t role, const nt_qtensor** out) {
+  if (!m || !out) return fail(NT_E_INVAL, "nt_model_tensor: NULL argument");
+  if (role == NT_ROLE_EMBD) { *out = &m->embd; return NT_OK; }
+  if (role == NT_ROLE_OUTPUT) { *out = &m->output; return NT_OK; }
+  if (layer < 0 || layer >= m->c.n_layers || role < 0 || role > 6) return fail(NT_E_INVAL, "nt_model_tensor: index");
+  *out = &m->layers[size_t(layer)].view[role];
+  return NT_OK;
+}
+
+}  // extern "C"

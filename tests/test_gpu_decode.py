@@ -1,0 +1,222 @@
+"""GPU: the decode step through nt_decode_step against the oracle (teacher-forced)."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from gpu_util import ensure_built, rel_l2, torch_cuda
+
+pytestmark = pytest.mark.gpu
+MAX_ABS, REL_L2, MARGIN = 1e-2, 5e-3, 1e-2
+
+
+@pytest.fixture(scope="module")
+def nt():
+    torch_cuda()
+    ensure_built()
+    from quantized_decode_dequant_gb300 import nt as _nt
+    return _nt
+
+
+@pytest.fixture(scope="module")
+def W():
+    from quantized_decode_dequant_gb300 import workloads
+    return workloads
+
+
+def _check_step(gl, gnx, ol, onx, omg, where):
+    err_abs = float(np.abs(gl.astype(np.float64) - ol).max())
+    err_rel = rel_l2(gl, ol)
+    assert err_abs <= MAX_ABS and err_rel <= REL_L2, (where, err_abs, err_rel)
+    if omg > MARGIN:
+        assert gnx == onx, (where, gnx, onx, omg)
+    return err_abs, err_rel
+
+
+def test_tiny_teacher_forced_64_steps(nt, W):
+    m = nt.nt_model_create(nt.make_config(**W.TINY, seed=0))
+    om = oracle.Model(oracle.ModelSpec(**W.TINY, seed=0))
+    try:
+        toks = oracle.tokens(0, W.TINY_STEPS, W.TINY["vocab"])
+        gl = np.empty(W.TINY["vocab"], np.float32)
+        worst = 0.0
+        for i, t in enumerate(toks):
+            gnx = nt.nt_decode_step(m, t, gl)
+            ol, onx, omg = om.decode_step(t)
+            worst = max(worst, _check_step(gl, gnx, ol, onx, omg, i)[0])
+        # the cache holds every step's K and V, RoPE'd, in f16
+        hd = W.TINY["head_dim"]
+        for (l, kv, g, t) in [(0, 0, 0, 0), (1, 1, 1, 63), (0, 0, 1, 31), (1, 1, 0, 5)]:
+            got = nt.nt_kv_export(m, l, kv, g, t, 1, hd)[0].view(np.float16).astype(np.float64)
+            want = np.array([om.kv_get(l, kv, g, t, d) for d in range(hd)], np.uint16).view(np.float16)
+            np.testing.assert_allclose(got, want.astype(np.float64), rtol=2e-3, atol=1e-4)
+        st = nt.nt_get_stats(m)
+        assert st.pos == W.TINY_STEPS and st.steps == W.TINY_STEPS
+        with pytest.raises(nt.NtError) as ei:
+            nt.nt_decode_step(m, 0)
+        assert ei.value.status == nt.NT_E_INVAL    # position reached max_ctx
+    finally:
+        nt.nt_model_destroy(m)
+
+
+def test_tiny_mixed_formats_teacher_forced(nt, W):
+    spec = dict(W.TINY, **W.Q4_K_M)
+    m = nt.nt_model_create(nt.make_config(**spec, seed=4))
+    om = oracle.Model(oracle.ModelSpec(**spec, seed=4))
+    try:
+        gl = np.empty(spec["vocab"], np.float32)
+        for i, t in enumerate(oracle.tokens(4, 12, spec["vocab"])):
+            gnx = nt.nt_decode_step(m, t, gl)
+            ol, onx, omg = om.decode_step(t)
+            _check_step(gl, gnx, ol, onx, omg, i)
+    finally:
+        nt.nt_model_destroy(m)
+
+
+def test_kv_prefill_bit_exact(nt, W):
+    m = nt.nt_model_create(nt.make_config(**W.TINY, seed=0))
+    om = oracle.Model(oracle.ModelSpec(**W.TINY, seed=0))
+    try:
+        nt.nt_kv_prefill(m, 40, 2)
+        om.kv_prefill(40, 2)
+        hd = W.TINY["head_dim"]
+        for (l, kv, g) in [(0, 0, 0), (1, 1, 1), (0, 1, 1)]:
+            got = nt.nt_kv_export(m, l, kv, g, 0, 40, hd)
+            want = np.array([[om.kv_get(l, kv, g, t, d) for d in range(hd)] for t in range(40)], np.uint16)
+            np.testing.assert_array_equal(got, want)
+        # decoding on top of the prefilled cache
+        gl = np.empty(W.TINY["vocab"], np.float32)
+        for i, t in enumerate(oracle.tokens(3, 5, W.TINY["vocab"])):
+            gnx = nt.nt_decode_step(m, t, gl)
+            ol, onx, omg = om.decode_step(t)
+            _check_step(gl, gnx, ol, onx, omg, i)
+    finally:
+        nt.nt_model_destroy(m)
+
+
+def test_device_loop_matches_host_loop_and_profile(nt, W):
+    cfg = nt.make_config(**W.TINY, seed=0)
+    a, b = nt.nt_model_create(cfg), nt.nt_model_create(cfg)
+    try:
+        tok = 17
+        seq = []
+        t = tok
+        for _ in range(10):
+            t = nt.nt_decode_step(a, t)
+            seq.append(t)
+        nt.nt_decode_run(b, tok, 10)
+        np.testing.assert_array_equal(nt.nt_get_tokens(b, 0, 10), seq)
+        nt.nt_kv_reset(b)
+        kt = nt.nt_profile_steps(b, tok, 3)
+        assert kt.launches[nt.KC_GEMV] == 3 * (4 * W.TINY["n_layers"] + 1)
+        assert kt.launches[nt.KC_ATTN] == 3 * 2 * W.TINY["n_layers"]
+        assert kt.ms[nt.KC_GEMV] > 0 and kt.step_ms > 0
+        np.testing.assert_array_equal(nt.nt_get_tokens(b, 0, 3), seq[:3])
+    finally:
+        nt.nt_model_destroy(a)
+        nt.nt_model_destroy(b)
+
+
+def test_streamed_layers_bitwise_equal_resident(nt, W):
+    spec = dict(W.TINY, n_layers=5)
+    cfg = nt.make_config(**spec, seed=6)
+    a, b = nt.nt_model_create(cfg), nt.nt_model_create(cfg)
+    try:
+        nt.nt_stream_layers(b, 2, 2)
+        la = np.empty(spec["vocab"], np.float32)
+        lb = np.empty(spec["vocab"], np.float32)
+        t = 5
+        for _ in range(6):
+            na = nt.nt_decode_step(a, t, la)
+            nb = nt.nt_decode_step(b, t, lb)
+            np.testing.assert_array_equal(la.view(np.uint32), lb.view(np.uint32))
+            assert na == nb
+            t = na
+        st = nt.nt_get_stats(b)
+        assert st.n_resident == 2 and st.h2d_bytes > 0 and st.h2d_ms > 0
+        assert 0.0 <= st.overlap <= 1.0
+        # a streamed tensor still exports, but cannot be used in place
+        tq = nt.nt_model_tensor(b, 4, "q")
+        from gpu_util import blocks
+        qk, bb = blocks("q8_0")
+        got = nt.nt_qtensor_export(tq, 0, 2, qk, bb, spec["hidden"])
+        want = oracle.qtensor_rows("q8_0", 512, 512, 6, oracle.uid_layer(4, "q"), 0.02, row0=0, nrows=2)
+        np.testing.assert_array_equal(got, want)
+        with pytest.raises(nt.NtError) as ei:
+            nt.nt_gemv_q(tq, 0, 0)
+        assert ei.value.status in (nt.NT_E_STATE, nt.NT_E_INVAL)
+        # back to fully resident
+        nt.nt_stream_layers(b, spec["n_layers"], 2)
+        na = nt.nt_decode_step(a, t, la)
+        nb = nt.nt_decode_step(b, t, lb)
+        np.testing.assert_array_equal(la.view(np.uint32), lb.view(np.uint32))
+    finally:
+        nt.nt_model_destroy(a)
+        nt.nt_model_destroy(b)
+
+
+def test_argument_and_resource_errors(nt, W):
+    with pytest.raises(nt.NtError) as ei:
+        nt.nt_model_create(nt.make_config(**dict(W.TINY, n_kv_heads=3)))
+    assert ei.value.status == nt.NT_E_INVAL
+    m = nt.nt_model_create(nt.make_config(**W.TINY))
+    try:
+        with pytest.raises(nt.NtError) as ei:
+            nt.nt_decode_step(m, W.TINY["vocab"])
+        assert ei.value.status == nt.NT_E_INVAL
+        with pytest.raises(nt.NtError):
+            nt.nt_kv_prefill(m, W.TINY["max_ctx"] + 1, 0)
+        with pytest.raises(nt.NtError) as ei:
+            nt.nt_stream_layers(m, 1, 3)
+        assert ei.value.status == nt.NT_E_UNSUPPORTED
+    finally:
+        nt.nt_model_destroy(m)
+    os.environ["NT_DEVICE_BYTES_LIMIT"] = str(1 << 20)
+    try:
+        with pytest.raises(nt.NtError) as ei:
+            nt.nt_model_create(nt.make_config(**W.TINY))
+        assert ei.value.status == nt.NT_E_NOMEM
+    finally:
+        del os.environ["NT_DEVICE_BYTES_LIMIT"]
+
+
+def test_llama8b_q8_0_teacher_forced(nt, W):
+    """8B shape at full size: prefilled context 512, prompt token, GPU's own greedy tokens fed to both."""
+    spec = W.LLAMA_8B_Q8_0
+    nthreads = os.cpu_count() or 8
+    m = nt.nt_model_create(nt.make_config(**spec, seed=W.SEED_WEIGHTS))
+    try:
+        nt.nt_kv_prefill(m, W.LLAMA_8B_CTX, W.SEED_KV)
+        om = oracle.Model(oracle.ModelSpec(**spec, seed=W.SEED_WEIGHTS), nthreads=nthreads)
+        om.kv_prefill(W.LLAMA_8B_CTX, W.SEED_KV)
+        gl = np.empty(spec["vocab"], np.float32)
+        tok = oracle.token(W.SEED_PROMPT, oracle.UID_TOKENS, 0, spec["vocab"])
+        for i in range(int(os.environ.get("NT_8B_STEPS", "3"))):
+            gnx = nt.nt_decode_step(m, tok, gl)
+            ol, onx, omg = om.decode_step(tok)
+            _check_step(gl, gnx, ol, onx, omg, i)
+            tok = gnx
+    finally:
+        nt.nt_model_destroy(m)
+
+
+@pytest.mark.slow
+@pytest.mark.skipif(os.environ.get("NT_RUN_SLOW") != "1", reason="70B oracle takes minutes per step; NT_RUN_SLOW=1")
+def test_llama70b_q4_k_m_teacher_forced(nt, W):
+    spec = W.LLAMA_70B_Q4_K_M
+    m = nt.nt_model_create(nt.make_config(**spec, seed=W.SEED_WEIGHTS))
+    try:
+        nt.nt_kv_prefill(m, W.LLAMA_70B_Q4_K_M_CTX, W.SEED_KV)
+        om = oracle.Model(oracle.ModelSpec(**spec, seed=W.SEED_WEIGHTS), lazy=True, nthreads=os.cpu_count() or 8)
+        om.kv_prefill(W.LLAMA_70B_Q4_K_M_CTX, W.SEED_KV)
+        gl = np.empty(spec["vocab"], np.float32)
+        tok = oracle.token(W.SEED_PROMPT, oracle.UID_TOKENS, 0, spec["vocab"])
+        for i in range(int(os.environ.get("NT_70B_STEPS", "2"))):
+            gnx = nt.nt_decode_step(m, tok, gl)
+            ol, onx, omg = om.decode_step(tok)
+            e = _check_step(gl, gnx, ol, onx, omg, i)
+            print(f"70B step {i}: max-abs {e[0]:.3e} rel-L2 {e[1]:.3e} margin {omg:.3e}")
+            tok = gnx
+    finally:
+        nt.nt_model_destroy(m)
