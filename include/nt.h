@@ -208,6 +208,29 @@ nt_status nt_dequant(const nt_qtensor* t, int64_t row0, int64_t nrows, float* de
  * dev_x and dev_y must not overlap and must be 16-byte aligned. */
 nt_status nt_gemv_q(const nt_qtensor* t, const float* dev_x, float* dev_y, void* stream);
 
+/* ------------------------------------------------ allocation-free variant -- */
+
+/* y = W x as nt_gemv_q, then the index of the largest y (ties to the lowest
+ * row) into dev_index and the gap between the largest and second-largest y
+ * into dev_margin (both device pointers, 4-byte aligned; dev_index is -1 when
+ * no y is finite).  The pages have no counterpart: this entry point exists for
+ * callers that cannot allocate device memory on this path, such as embedders
+ * whose device memory is all reserved by their own allocator, or latency-bound
+ * loops that cannot afford the implicit synchronisation of cudaMalloc/cudaFree.
+ * It allocates nothing: the per-CTA partial results of the selection live in a
+ * file-scope device array of 1024 x 16 bytes (16 KiB) that every GPU loading
+ * this library holds until the process exits.  The first call on a device, with
+ * that device current, looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call shares the array and overwrites what it reads, so nothing needs
+ * clearing, but calls that overlap on the GPU (for example on two streams at
+ * once) race on it: serialise them.  Asynchronous on stream.
+ * Errors: nt_gemv_q's argument rules; NT_E_INVAL for more than 2^31 - 2 rows;
+ * NT_E_UNSUPPORTED for more than 28672 columns or a device with more than 256
+ * SMs (the array then cannot hold one summary per CTA). */
+nt_status nt_gemv_argmax_noalloc(const nt_qtensor* t, const float* dev_x, float* dev_y, int32_t* dev_index,
+                                 float* dev_margin, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -82,6 +82,7 @@ _SIGS = {
     "nt_qtensor_export": (C.c_int, [_vp, _i64, _i64, _vp, C.c_size_t]),
     "nt_dequant": (C.c_int, [_vp, _i64, _i64, _vp, _vp]),
     "nt_gemv_q": (C.c_int, [_vp, _vp, _vp, _vp]),
+    "nt_gemv_argmax_noalloc": (C.c_int, [_vp, _vp, _vp, _vp, _vp, _vp]),
 }
 
 
@@ -243,3 +244,9 @@ def nt_dequant(t: int, row0: int, nrows: int, dev_out: int, stream=None) -> None
 
 def nt_gemv_q(t: int, dev_x: int, dev_y: int, stream=None) -> None:
     _check(lib().nt_gemv_q(t, dev_x, dev_y, _stream(stream)), "nt_gemv_q")
+
+
+def nt_gemv_argmax_noalloc(t: int, dev_x: int, dev_y: int, dev_index: int, dev_margin: int, stream=None) -> None:
+    """y = W x plus greedy index and top-2 margin on the device; allocates no device memory."""
+    _check(lib().nt_gemv_argmax_noalloc(t, dev_x, dev_y, dev_index, dev_margin, _stream(stream)),
+           "nt_gemv_argmax_noalloc")
