@@ -225,9 +225,9 @@ nt_status nt_gemv_q(const nt_qtensor* t, const float* dev_x, float* dev_y, void*
  * Every call shares the array and overwrites what it reads, so nothing needs
  * clearing, but calls that overlap on the GPU (for example on two streams at
  * once) race on it: serialise them.  Asynchronous on stream.
+ * The GEMV launch is capped at 1024 CTAs, one summary slot each.
  * Errors: nt_gemv_q's argument rules; NT_E_INVAL for more than 2^31 - 2 rows;
- * NT_E_UNSUPPORTED for more than 28672 columns or a device with more than 256
- * SMs (the array then cannot hold one summary per CTA). */
+ * NT_E_UNSUPPORTED for more than 28672 columns. */
 nt_status nt_gemv_argmax_noalloc(const nt_qtensor* t, const float* dev_x, float* dev_y, int32_t* dev_index,
                                  float* dev_margin, void* stream);
 

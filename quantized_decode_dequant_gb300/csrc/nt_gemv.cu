@@ -1,6 +1,8 @@
 // nt_gemv.cu -- launch-shape selection for the fused dequantize-GEMV and the
 // nt_gemv_q entry point.
-#include "nt_gemv.cuh"
+#include <cstdlib>
+
+#include "nt_gemv_pipe.cuh"
 
 namespace nt {
 
@@ -10,22 +12,57 @@ int64_t gemv_logical_rows(const GemvArgs& a) {
   return n;
 }
 
-cudaError_t launch_gemv(const GemvArgs& a, int epi, cudaStream_t s, bool pdl, int* grid_used) {
+// Chooses the kernel and its shape: the shared-memory pipeline when the column
+// count allows whole aligned scale copies, with as many ring stages as the
+// shared memory left after x holds (at most 8); matrices too wide for x and a
+// ring in one CTA, with a linear epilogue, are split into column windows that
+// successive launches accumulate.  Otherwise the register-path kernel.
+cudaError_t launch_gemv(const GemvArgs& a_in, int epi, cudaStream_t s, bool pdl, int* grid_used) {
+  GemvArgs a = a_in;
   const int64_t cols = a.seg[0].cols;
-  if (cols <= 0 || cols % 32 || a.nseg < 1 || a.nseg > 3) return cudaErrorInvalidValue;
+  if (cols <= 0 || cols % 32 || cols > 32768 || a.nseg < 1 || a.nseg > 3) return cudaErrorInvalidValue;
   for (int i = 1; i < a.nseg; i++)
     if (a.seg[i].type != a.seg[0].type || a.seg[i].cols != cols) return cudaErrorInvalidValue;
-  const int U = gemv_units_per_thread(cols);
-  const int tr = gemv_tr(cols, U);
-  if (tr > gemv_max_threads(U)) return cudaErrorInvalidValue;
-  int groups = gemv_max_threads(U) / tr;
-  if (groups < 1) groups = 1;
-  const int threads = tr * groups;
-  switch (a.seg[0].type) {
-    case NT_Q8_0: return launch_gemv_q8_0(a, epi, threads, tr, U, s, pdl, grid_used);
-    case NT_Q4_0: return launch_gemv_q4_0(a, epi, threads, tr, U, s, pdl, grid_used);
-    case NT_Q4_K: return launch_gemv_q4_k(a, epi, threads, tr, U, s, pdl, grid_used);
-    case NT_Q6_K: return launch_gemv_q6_k(a, epi, threads, tr, U, s, pdl, grid_used);
+  if (a.max_grid <= 0 || a.max_grid > kMaxGemvGrid) a.max_grid = kMaxGemvGrid;
+  const int fmt = a.seg[0].type;
+  const int64_t nrows = gemv_logical_rows(a);
+  const int R = nrows >= 16384 ? 4 : 2;
+  const int64_t align = fmt == NT_Q6_K ? 512 : 256;
+  static const bool force_register_path = getenv("NT_GEMV_REGISTER_PATH") != nullptr;
+  if (cols % align == 0 && !force_register_path) {
+    int parts = 1;
+    if (epi == EPI_STORE || epi == EPI_ADD)
+      while (pipe_x_bytes(cols / parts) > 140 * 1024 && (cols / parts) % (2 * align) == 0) parts *= 2;
+    const int64_t w = cols / parts;
+    const size_t xb = pipe_x_bytes(w);
+    const size_t budget = xb < size_t(kPipeMaxSmem) ? size_t(kPipeMaxSmem) - xb : 0;
+    int S = int(budget / (size_t(kPipeWarps) * R * pipe_row_bytes(fmt)));
+    if (S > 8) S = 8;
+    if (S >= 2) {
+      for (int p = 0; p < parts; p++) {
+        a.col0 = p * w;
+        a.ncols = w;
+        const int e_p = p == 0 ? epi : EPI_ADD;
+        cudaError_t e;
+        switch (fmt) {
+          case NT_Q8_0: e = launch_gemv_pipe_q8_0(a, e_p, R, S, s, pdl, grid_used); break;
+          case NT_Q4_0: e = launch_gemv_pipe_q4_0(a, e_p, R, S, s, pdl, grid_used); break;
+          case NT_Q4_K: e = launch_gemv_pipe_q4_k(a, e_p, R, S, s, pdl, grid_used); break;
+          case NT_Q6_K: e = launch_gemv_pipe_q6_k(a, e_p, R, S, s, pdl, grid_used); break;
+          default: e = cudaErrorInvalidValue;
+        }
+        if (e != cudaSuccess) return e;
+      }
+      return cudaSuccess;
+    }
+  }
+  a.col0 = 0;
+  a.ncols = cols;
+  switch (fmt) {
+    case NT_Q8_0: return launch_gemv_q8_0(a, epi, R, s, pdl, grid_used);
+    case NT_Q4_0: return launch_gemv_q4_0(a, epi, R, s, pdl, grid_used);
+    case NT_Q4_K: return launch_gemv_q4_k(a, epi, R, s, pdl, grid_used);
+    case NT_Q6_K: return launch_gemv_q6_k(a, epi, R, s, pdl, grid_used);
   }
   return cudaErrorInvalidValue;
 }

@@ -1,220 +1,232 @@
 // nt_gemv.cuh -- fused dequantize-GEMV, y = W x at batch 1 (hada "Architektur und
-// Codestruktur": "cuda/: GEMV-... Kernel"; the step's cost is these weight reads).
+// Codestruktur": "cuda/: GEMV-... Kernel"; the decode step's cost is these weight reads).
 //
-// Work split.  A thread owns U "units" of 32 consecutive columns and keeps the
-// matching 32*U activations in registers for the whole launch, so x is read
-// from shared memory once per CTA and every weight byte is fetched exactly once
-// with 128-bit non-allocating loads.  Tr threads cover one row (the split over
-// K inside a row group); G = blockDim/Tr groups per CTA work on different rows.
-// Each group handles R = 4 rows per iteration: a thread issues the loads of all
-// four rows before any arithmetic, dequantizes in registers and accumulates in
-// fp32; a transposed warp reduction then leaves one sum per row per warp and
-// the group's warps are summed through shared memory.  Row groups are dealt
-// round-robin over all (CTA, group) slots of a one-wave grid.
+// This header holds the per-format decode arithmetic and the register-path
+// kernel, used for column counts the shared-memory pipeline (nt_gemv_pipe.cuh)
+// does not take.  Work split: a CTA stages x once in shared memory
+// (RMS-normalised when asked, pre-scaled or permuted for the format's decode,
+// padded so 16-byte reads of consecutive lanes hit distinct banks) and then
+// every warp works alone: it owns groups of R consecutive rows, its lanes split
+// the columns into "units" (16 columns for Q8_0, 32 for the 4/6-bit formats;
+// lane l takes units l, l+32, ...), and each unit's codes are fetched with one
+// 128-bit non-allocating load per row.  The loads of the next unit (or of the
+// next row group's first unit) are issued before the current unit is decoded.
+// No barrier is taken in the loop; a transposed warp reduction ends each row
+// group and the epilogue runs on the lanes that hold the row sums.  Row groups
+// are dealt round-robin over all warps of a one-wave grid.  Weights do not
+// depend on the previous kernel, so the first loads are issued before
+// griddepcontrol.wait (programmatic dependent launch).
 //
-// Dequantization arithmetic (exact per element, scale applied per unit):
-//  - 8-bit codes: the byte (sign bit flipped) is placed under the exponent of
-//    2^23 with one byte permute, and 2^23 + 128 subtracted: the code q exactly.
-//  - 4-bit codes: nibble i of a 16-bit half is masked in place (value q*16^i)
-//    under the exponent of 2^23 and 2^23 (+ offset*16^i) subtracted; the
-//    activation it multiplies was pre-scaled by 16^-i when x was loaded.
-//  - Q4_K: sum_c (d sc q_c - dmin m) x_c = d sc sum q_c x_c - dmin m sum x_c,
-//    with sum x_c per unit computed once per CTA.
+// Decode arithmetic (exact per element; the scales are applied once per unit,
+// fp32 accumulation, packed f32x2 FMA):
+//  - Q8_0: byte b (sign bit flipped) is placed under the exponent of 2^23 by a
+//    byte permute; subtracting 2^23 + 128 gives the code q exactly.
+//  - Q4_0 / Q4_K: nibble i of a 16-bit half is masked in place (value q*16^i)
+//    under the exponent of 2^23; subtracting 2^23 (+ 8*16^i for Q4_0) gives
+//    (q - off)*16^i exactly and x was pre-scaled by 16^-i when staged.
+//    Q4_K: sum_c (d sc q_c - dmin m) x_c = d sc sum q_c x_c - dmin m sum x_c,
+//    with sum x_c per unit staged once per CTA.
+//  - Q6_K: the low nibbles of the even (odd) elements of a code word are
+//    masked (shifted) into bytes, the two high bits OR-ed in from the device's
+//    high-bit word, each byte placed under 2^23 and 2^23 + 32 subtracted;
+//    x is staged in the matching even/odd order.
 #pragma once
 
 #include "nt_internal.cuh"
 
 namespace nt {
 
-constexpr int kMaxThreads = 512;
-// rows per group iteration: 4 when a thread owns one 32-column unit, 2 when it owns two
-template <int U> struct RowsPer { static constexpr int value = U == 1 ? 4 : 2; };
-template <int U> struct ThreadsMax { static constexpr int value = U == 1 ? 512 : 448; };
+constexpr int kThreads = 512;   // 16 warps per CTA
+constexpr int kXPad = 4;        // floats of padding after each unit's x in shared memory
 
-__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+__device__ __forceinline__ uint4 ldg16(const void* p) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
   return v;
 }
-__device__ __forceinline__ uint2 ldg_stream8(const void* p) {
+__device__ __forceinline__ uint2 ldg8(const void* p) {
   uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
 }
-__device__ __forceinline__ uint32_t ldg_u16(const void* p) {
+__device__ __forceinline__ uint32_t ldg2(const void* p) {
   unsigned short v;
-  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  asm("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
   return v;
 }
-
 __device__ __forceinline__ float h2f_bits(uint32_t b) { return __half2float(__ushort_as_half((unsigned short)b)); }
+__device__ __forceinline__ float bits_f(uint32_t b) { return __uint_as_float(b); }
 
-// (q - off) * 16^i exactly, from the nibble already masked in place at bits [4i, 4i+4)
-template <int I, int OFF>
-__device__ __forceinline__ float nib_val(uint32_t masked) {
-  return __int_as_float(int(masked | 0x4B000000u)) - (8388608.0f + float(OFF) * float(1 << (4 * I)));
-}
+constexpr uint32_t kMagicBits = 0x4B000000u;   // 2^23
+constexpr float kMagic = 8388608.0f;
 
 // ------------------------------------------------------------ formats --
 
-// Per-(row, unit) register payload and its dot product with the unit's
-// activations xs[32] (pre-scaled as the format requires) and their sum.
-template <int FMT> struct Unit;
+template <int FMT> struct Fmt;
 
-template <> struct Unit<NT_Q8_0> {
-  uint4 a, b;
-  uint32_t d;
-  static constexpr bool kScaledX = false;
-  __device__ __forceinline__ void load(const QMat& m, int64_t lr, int unit) {
-    const uint8_t* q = m.q + lr * m.cols + int64_t(unit) * 32;
-    a = ldg_stream16(q);
-    b = ldg_stream16(q + 16);
-    d = ldg_u16(m.d + lr * (m.cols / 32) + unit);
-  }
-  __device__ __forceinline__ float dot(const float* xs, float /*xsum*/) const {
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    float s0 = 0.f, s1 = 0.f;
+// 16 int8 codes of one 16-byte vector against x[0..15]
+__device__ __forceinline__ float q8_dot16(uint4 c, const float4* xs) {
+  const float2 off = make_float2(-(kMagic + 128.0f), -(kMagic + 128.0f));
+  float2 acc = make_float2(0.f, 0.f);
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-    for (int k = 0; k < 8; k++) {
-      const uint32_t u = w[k] ^ 0x80808080u;
-#pragma unroll
-      for (int i = 0; i < 4; i++) {
-        const float q = __int_as_float(int(__byte_perm(u, 0x4B000000u, 0x7440u | i))) - 8388736.0f;
-        if (i & 1) s1 = fmaf(q, xs[4 * k + i], s1);
-        else s0 = fmaf(q, xs[4 * k + i], s0);
-      }
-    }
-    return h2f_bits(d) * (s0 + s1);
+  for (int k = 0; k < 4; k++) {
+    const uint32_t u = w[k] ^ 0x80808080u;
+    const float4 x = xs[k];
+    const float2 q01 = __fadd2_rn(make_float2(bits_f(__byte_perm(u, kMagicBits, 0x7440u)),
+                                              bits_f(__byte_perm(u, kMagicBits, 0x7441u))), off);
+    const float2 q23 = __fadd2_rn(make_float2(bits_f(__byte_perm(u, kMagicBits, 0x7442u)),
+                                              bits_f(__byte_perm(u, kMagicBits, 0x7443u))), off);
+    acc = __ffma2_rn(q01, make_float2(x.x, x.y), acc);
+    acc = __ffma2_rn(q23, make_float2(x.z, x.w), acc);
   }
+  return acc.x + acc.y;
+}
+
+template <> struct Fmt<NT_Q8_0> {
+  static constexpr int kCols = 16;
+  static constexpr bool kXSum = false;
+  struct Pay {
+    uint4 c;
+    uint32_t d;
+  };
+  __device__ static void load(Pay& p, const QMat& m, int64_t e) {   // e: flat index of the unit's first element
+    p.c = ldg16(m.q + e);
+    p.d = ldg2(m.d + (e >> 5));
+  }
+  // x staged in natural order
+  __device__ static int xpos(int c) { return c; }
+  __device__ static float xscale(int) { return 1.0f; }
+  __device__ static float dot(const Pay& p, const float4* xs, float) { return h2f_bits(p.d) * q8_dot16(p.c, xs); }
 };
 
-// 8 nibbles of one word against x[0..7] (scaled by 16^-(i%4)); offset subtracted per code
+// 8 nibbles of one word against x[0..7] (pre-scaled by 16^-(i%4)); OFF subtracted per code
 template <int OFF>
-__device__ __forceinline__ void nib8(uint32_t w, const float* x, float& s0, float& s1) {
+__device__ __forceinline__ float2 nib8(uint32_t w, float4 xa, float4 xb, float2 acc) {
+  const float2 o01 = make_float2(-(kMagic + float(OFF)), -(kMagic + float(OFF) * 16.0f));
+  const float2 o23 = make_float2(-(kMagic + float(OFF) * 256.0f), -(kMagic + float(OFF) * 4096.0f));
   const uint32_t h = w >> 16;
-  s0 = fmaf(nib_val<0, OFF>(w & 0xFu), x[0], s0);
-  s1 = fmaf(nib_val<1, OFF>(w & 0xF0u), x[1], s1);
-  s0 = fmaf(nib_val<2, OFF>(w & 0xF00u), x[2], s0);
-  s1 = fmaf(nib_val<3, OFF>(w & 0xF000u), x[3], s1);
-  s0 = fmaf(nib_val<0, OFF>(h & 0xFu), x[4], s0);
-  s1 = fmaf(nib_val<1, OFF>(h & 0xF0u), x[5], s1);
-  s0 = fmaf(nib_val<2, OFF>(h & 0xF00u), x[6], s0);
-  s1 = fmaf(nib_val<3, OFF>(h & 0xF000u), x[7], s1);
+  const float2 a = __fadd2_rn(make_float2(bits_f((w & 0xFu) | kMagicBits), bits_f((w & 0xF0u) | kMagicBits)), o01);
+  const float2 b = __fadd2_rn(make_float2(bits_f((w & 0xF00u) | kMagicBits), bits_f((w & 0xF000u) | kMagicBits)), o23);
+  const float2 c = __fadd2_rn(make_float2(bits_f((h & 0xFu) | kMagicBits), bits_f((h & 0xF0u) | kMagicBits)), o01);
+  const float2 d = __fadd2_rn(make_float2(bits_f((h & 0xF00u) | kMagicBits), bits_f((h & 0xF000u) | kMagicBits)), o23);
+  acc = __ffma2_rn(a, make_float2(xa.x, xa.y), acc);
+  acc = __ffma2_rn(b, make_float2(xa.z, xa.w), acc);
+  acc = __ffma2_rn(c, make_float2(xb.x, xb.y), acc);
+  acc = __ffma2_rn(d, make_float2(xb.z, xb.w), acc);
+  return acc;
 }
 
-template <> struct Unit<NT_Q4_0> {
-  uint4 a;
-  uint32_t d;
-  static constexpr bool kScaledX = true;
-  __device__ __forceinline__ void load(const QMat& m, int64_t lr, int unit) {
-    a = ldg_stream16(m.q + (lr * m.cols + int64_t(unit) * 32) / 2);
-    d = ldg_u16(m.d + lr * (m.cols / 32) + unit);
+__device__ __forceinline__ float nib_xscale(int c) {
+  const int i = c & 3;
+  return i == 0 ? 1.f : (i == 1 ? 0.0625f : (i == 2 ? 0.00390625f : 0.000244140625f));
+}
+
+template <> struct Fmt<NT_Q4_0> {
+  static constexpr int kCols = 32;
+  static constexpr bool kXSum = false;
+  struct Pay {
+    uint4 c;
+    uint32_t d;
+  };
+  __device__ static void load(Pay& p, const QMat& m, int64_t e) {
+    p.c = ldg16(m.q + (e >> 1));
+    p.d = ldg2(m.d + (e >> 5));
   }
-  __device__ __forceinline__ float dot(const float* xs, float /*xsum*/) const {
-    float s0 = 0.f, s1 = 0.f;
-    nib8<8>(a.x, xs, s0, s1);
-    nib8<8>(a.y, xs + 8, s0, s1);
-    nib8<8>(a.z, xs + 16, s0, s1);
-    nib8<8>(a.w, xs + 24, s0, s1);
-    return h2f_bits(d) * (s0 + s1);
+  __device__ static int xpos(int c) { return c; }
+  __device__ static float xscale(int c) { return nib_xscale(c); }
+  __device__ static float dot(const Pay& p, const float4* xs, float) {
+    float2 acc = make_float2(0.f, 0.f);
+    acc = nib8<8>(p.c.x, xs[0], xs[1], acc);
+    acc = nib8<8>(p.c.y, xs[2], xs[3], acc);
+    acc = nib8<8>(p.c.z, xs[4], xs[5], acc);
+    acc = nib8<8>(p.c.w, xs[6], xs[7], acc);
+    return h2f_bits(p.d) * (acc.x + acc.y);
   }
 };
 
-template <> struct Unit<NT_Q4_K> {
-  uint4 a, meta;
-  int j;
-  static constexpr bool kScaledX = true;
-  __device__ __forceinline__ void load(const QMat& m, int64_t lr, int unit) {
-    a = ldg_stream16(m.q + (lr * m.cols + int64_t(unit) * 32) / 2);
-    meta = __ldg(reinterpret_cast<const uint4*>(m.meta + (lr * (m.cols / 256) + unit / 8) * 16));
-    j = unit & 7;
+template <> struct Fmt<NT_Q4_K> {
+  static constexpr int kCols = 32;
+  static constexpr bool kXSum = true;
+  struct Pay {
+    uint4 c, meta;
+    int j;
+  };
+  __device__ static void load(Pay& p, const QMat& m, int64_t e) {
+    p.c = ldg16(m.q + (e >> 1));
+    p.meta = __ldg(reinterpret_cast<const uint4*>(m.meta + (e >> 8) * 16));
+    p.j = int(e >> 5) & 7;
   }
-  __device__ __forceinline__ float dot(const float* xs, float xsum) const {
-    float s0 = 0.f, s1 = 0.f;
-    nib8<0>(a.x, xs, s0, s1);
-    nib8<0>(a.y, xs + 8, s0, s1);
-    nib8<0>(a.z, xs + 16, s0, s1);
-    nib8<0>(a.w, xs + 24, s0, s1);
+  __device__ static int xpos(int c) { return c; }
+  __device__ static float xscale(int c) { return nib_xscale(c); }
+  __device__ static float dot(const Pay& p, const float4* xs, float xsum) {
+    float2 acc = make_float2(0.f, 0.f);
+    acc = nib8<0>(p.c.x, xs[0], xs[1], acc);
+    acc = nib8<0>(p.c.y, xs[2], xs[3], acc);
+    acc = nib8<0>(p.c.z, xs[4], xs[5], acc);
+    acc = nib8<0>(p.c.w, xs[6], xs[7], acc);
     // 6-bit fields: sc_j at bit 6j, m_j at bit 6(8+j) of the 96-bit stream (meta.y, meta.z, meta.w)
-    const uint64_t lo = uint64_t(meta.y) | (uint64_t(meta.z) << 32);
-    const uint32_t sc = uint32_t(lo >> (6 * j)) & 63u;
-    const int mb = 48 + 6 * j;
-    const uint32_t mm = mb >= 64 ? (meta.w >> (mb - 64)) & 63u
-                                 : uint32_t((lo >> mb) | (uint64_t(meta.w) << (64 - mb))) & 63u;
-    const float a_ = h2f_bits(meta.x & 0xFFFFu) * float(sc);
-    const float b_ = h2f_bits(meta.x >> 16) * float(mm);
-    return a_ * (s0 + s1) - b_ * xsum;
+    const uint64_t lo = uint64_t(p.meta.y) | (uint64_t(p.meta.z) << 32);
+    const uint32_t sc = uint32_t(lo >> (6 * p.j)) & 63u;
+    const int mb = 48 + 6 * p.j;
+    const uint32_t mm = mb >= 64 ? (p.meta.w >> (mb - 64)) & 63u
+                                 : uint32_t((lo >> mb) | (uint64_t(p.meta.w) << (64 - mb))) & 63u;
+    const float a = h2f_bits(p.meta.x & 0xFFFFu) * float(sc);
+    const float b = h2f_bits(p.meta.x >> 16) * float(mm);
+    return a * (acc.x + acc.y) - b * xsum;
   }
 };
 
-template <> struct Unit<NT_Q6_K> {
-  uint4 a;
-  uint2 h;
-  uint32_t sc, d;
-  static constexpr bool kScaledX = true;
-  __device__ __forceinline__ void load(const QMat& m, int64_t lr, int unit) {
-    const int64_t e = lr * m.cols + int64_t(unit) * 32;
-    a = ldg_stream16(m.q + e / 2);
-    h = ldg_stream8(m.qh + e / 4);
-    sc = ldg_u16(m.meta + e / 16);
-    d = ldg_u16(m.d + e / 256);
+template <> struct Fmt<NT_Q6_K> {
+  static constexpr int kCols = 32;
+  static constexpr bool kXSum = false;
+  struct Pay {
+    uint4 c;
+    uint2 h;
+    uint32_t sc, d;
+  };
+  __device__ static void load(Pay& p, const QMat& m, int64_t e) {
+    p.c = ldg16(m.q + (e >> 1));
+    p.h = ldg8(m.qh + (e >> 2));
+    p.sc = ldg2(m.meta + (e >> 4));
+    p.d = ldg2(m.d + (e >> 8));
   }
-  // word w (elements 8k..8k+7) with the high bits h16 (element 8k+i at bits 2i)
-  __device__ __forceinline__ static void six8(uint32_t w, uint32_t h16, const float* x, float& s0, float& s1) {
-    const uint32_t wh = w >> 16, hh = h16 >> 8;
-    s0 = fmaf(nib_val<0, 32>((w & 0xFu) | ((h16 << 4) & 0x30u)), x[0], s0);
-    s1 = fmaf(nib_val<1, 32>((w & 0xF0u) | ((h16 << 6) & 0x300u)), x[1], s1);
-    s0 = fmaf(nib_val<2, 32>((w & 0xF00u) | ((h16 << 8) & 0x3000u)), x[2], s0);
-    s1 = fmaf(nib_val<3, 32>((w & 0xF000u) | ((h16 << 10) & 0x30000u)), x[3], s1);
-    s0 = fmaf(nib_val<0, 32>((wh & 0xFu) | ((hh << 4) & 0x30u)), x[4], s0);
-    s1 = fmaf(nib_val<1, 32>((wh & 0xF0u) | ((hh << 6) & 0x300u)), x[5], s1);
-    s0 = fmaf(nib_val<2, 32>((wh & 0xF00u) | ((hh << 8) & 0x3000u)), x[6], s0);
-    s1 = fmaf(nib_val<3, 32>((wh & 0xF000u) | ((hh << 10) & 0x30000u)), x[7], s1);
+  // within each group of 8 columns x is staged as [0,2,4,6,1,3,5,7]
+  __device__ static int xpos(int c) { return (c & ~7) | ((c & 1) ? 4 + ((c & 7) >> 1) : ((c & 7) >> 1)); }
+  __device__ static float xscale(int) { return 1.0f; }
+  // four 6-bit codes (one per byte) minus 32, against x[0..3]
+  __device__ static float2 bytes4(uint32_t q, float4 x, float2 acc) {
+    const float2 off = make_float2(-(kMagic + 32.0f), -(kMagic + 32.0f));
+    const float2 a = __fadd2_rn(make_float2(bits_f(__byte_perm(q, kMagicBits, 0x7440u)),
+                                            bits_f(__byte_perm(q, kMagicBits, 0x7441u))), off);
+    const float2 b = __fadd2_rn(make_float2(bits_f(__byte_perm(q, kMagicBits, 0x7442u)),
+                                            bits_f(__byte_perm(q, kMagicBits, 0x7443u))), off);
+    acc = __ffma2_rn(a, make_float2(x.x, x.y), acc);
+    return __ffma2_rn(b, make_float2(x.z, x.w), acc);
   }
-  __device__ __forceinline__ float dot(const float* xs, float /*xsum*/) const {
-    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-    six8(a.x, h.x & 0xFFFFu, xs, a0, a1);
-    six8(a.y, h.x >> 16, xs + 8, a0, a1);
-    six8(a.z, h.y & 0xFFFFu, xs + 16, b0, b1);
-    six8(a.w, h.y >> 16, xs + 24, b0, b1);
-    const float dd = h2f_bits(d);
-    const float sc0 = float(int8_t(sc & 0xFF)), sc1 = float(int8_t(sc >> 8));
-    return dd * (sc0 * (a0 + a1) + sc1 * (b0 + b1));
+  __device__ static float dot(const Pay& p, const float4* xs, float) {
+    // device high-bit word G (one per 16 elements): byte j holds, for code words
+    // W (elements 0..7) and W' (elements 8..15), hi(W,2j) at bits 4-5,
+    // hi(W',2j) at bits 6-7, hi(W,2j+1) at bits 0-1, hi(W',2j+1) at bits 2-3
+    const uint32_t M = 0x30303030u, L = 0x0F0F0F0Fu;
+    float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+    const uint32_t g0 = p.h.x, g1 = p.h.y;
+    a0 = bytes4((p.c.x & L) | (g0 & M), xs[0], a0);
+    a0 = bytes4(((p.c.x >> 4) & L) | ((g0 << 4) & M), xs[1], a0);
+    a0 = bytes4((p.c.y & L) | ((g0 >> 2) & M), xs[2], a0);
+    a0 = bytes4(((p.c.y >> 4) & L) | ((g0 << 2) & M), xs[3], a0);
+    a1 = bytes4((p.c.z & L) | (g1 & M), xs[4], a1);
+    a1 = bytes4(((p.c.z >> 4) & L) | ((g1 << 4) & M), xs[5], a1);
+    a1 = bytes4((p.c.w & L) | ((g1 >> 2) & M), xs[6], a1);
+    a1 = bytes4(((p.c.w >> 4) & L) | ((g1 << 2) & M), xs[7], a1);
+    const float sc0 = float(int8_t(p.sc & 0xFF)), sc1 = float(int8_t(p.sc >> 8));
+    return h2f_bits(p.d) * (sc0 * (a0.x + a0.y) + sc1 * (a1.x + a1.y));
   }
 };
 
-// --------------------------------------------------------------- kernel --
-
-struct RowRef {
-  int seg;
-  int64_t lr;
-};
-
-__device__ __forceinline__ RowRef map_row(const GemvArgs& a, int64_t row) {
-  RowRef r;
-  if (a.interleave) {
-    r.seg = int(row & 1);
-    r.lr = row >> 1;
-    return r;
-  }
-  r.seg = 0;
-  r.lr = row;
-  if (a.nseg > 1 && r.lr >= a.seg[0].rows) {
-    r.lr -= a.seg[0].rows;
-    r.seg = 1;
-    if (a.nseg > 2 && r.lr >= a.seg[1].rows) {
-      r.lr -= a.seg[1].rows;
-      r.seg = 2;
-    }
-  }
-  return r;
-}
-
-__device__ __forceinline__ const QMat& seg_ref(const GemvArgs& a, int s) {
-  return s == 0 ? a.seg[0] : (s == 1 ? a.seg[1] : a.seg[2]);
-}
+// --------------------------------------------------------------- helpers --
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
@@ -228,269 +240,312 @@ __device__ __forceinline__ void top2_push(float v, int i, float& b, int& bi, flo
     s = fmaxf(s, v);
   }
 }
+__device__ __forceinline__ void top2_merge(float b2, int i2, float s2, float& b, int& bi, float& s) {
+  if (i2 == 0x7fffffff) return;
+  top2_push(b2, i2, b, bi, s);
+  s = fmaxf(s, s2);
+}
 
-template <int FMT, int U, int EPI>
-__global__ void __launch_bounds__(ThreadsMax<U>::value, 1)
-    k_gemv(const __grid_constant__ GemvArgs a, const int64_t nrows, const int tr) {
-  constexpr int kRows = RowsPer<U>::value;
+// logical row -> (segment, row inside the segment)
+__device__ __forceinline__ void map_row(const GemvArgs& a, int64_t row, int& seg, int64_t& lr) {
+  if (a.interleave) {
+    seg = int(row & 1);
+    lr = row >> 1;
+    return;
+  }
+  seg = 0;
+  lr = row;
+  if (a.nseg > 1 && lr >= a.seg[0].rows) {
+    lr -= a.seg[0].rows;
+    seg = 1;
+    if (a.nseg > 2 && lr >= a.seg[1].rows) {
+      lr -= a.seg[1].rows;
+      seg = 2;
+    }
+  }
+}
+
+// Transposed warp reduction of R per-lane partial sums: afterwards lane l holds
+// the warp total of row l / (32 / R).
+template <int R>
+__device__ __forceinline__ float warp_reduce_rows(const float (&acc)[R], int lane) {
+  float k;
+  const bool up = lane & 16;
+  if (R == 4) {
+    float k0 = up ? acc[2 % R] : acc[0], k1 = up ? acc[3 % R] : acc[1 % R];
+    const float s0 = up ? acc[0] : acc[2 % R], s1 = up ? acc[1 % R] : acc[3 % R];
+    k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+    k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+    const bool up2 = lane & 8;
+    k = up2 ? k1 : k0;
+    k += __shfl_xor_sync(0xffffffffu, up2 ? k0 : k1, 8);
+  } else {
+    k = up ? acc[1 % R] : acc[0];
+    k += __shfl_xor_sync(0xffffffffu, up ? acc[0] : acc[1 % R], 16);
+    k += __shfl_xor_sync(0xffffffffu, k, 8);
+  }
+  k += __shfl_xor_sync(0xffffffffu, k, 4);
+  k += __shfl_xor_sync(0xffffffffu, k, 2);
+  k += __shfl_xor_sync(0xffffffffu, k, 1);
+  return k;
+}
+
+// Epilogue of one finished row group: k is this lane's reduced row sum (valid
+// on lanes l % (32/R) == 0), rows grp*R + l/(32/R).  All lanes must call it.
+template <int R, int EPI>
+__device__ __forceinline__ void epilogue(const GemvArgs& a, int64_t grp, int64_t nrows, int lane, float k,
+                                         float& best, int& best_i, float& second) {
+  constexpr int LPR = 32 / R;
+  const int rr = lane / LPR;
+  const int64_t row = grp * R + rr;
+  const bool holder = (lane % LPR) == 0 && row < nrows;
+  // pair epilogues need rows 2i and 2i+1: the odd row's sum moves onto the even holder
+  const float other = __shfl_down_sync(0xffffffffu, k, LPR);
+  if (!holder) return;
+  if (EPI == EPI_STORE) {
+    a.epi.y[row] = k;
+  } else if (EPI == EPI_ADD) {
+    a.epi.y[row] += k;
+  } else if (EPI == EPI_LOGITS) {
+    a.epi.y[row] = k;
+    top2_push(k, int(row), best, best_i, second);
+  } else if ((rr & 1) == 0) {
+    const float v0 = k, v1 = other;
+    if (EPI == EPI_SWIGLU) {
+      a.epi.y[row >> 1] = silu(v0) * v1;
+    } else {  // EPI_QKV: RoPE on q and k pairs, f16 store of k and v at the current position
+      const int L = a.epi.row_base + int(row);
+      const int hd = a.epi.head_dim;
+      const int p = *a.epi.pos;
+      if (L < a.epi.q_rows + a.epi.k_rows) {
+        const int d = L % hd;
+        const float2 cs = a.epi.rope[int64_t(p) * (hd / 2) + d / 2];
+        const float r0 = v0 * cs.x - v1 * cs.y;
+        const float r1 = v0 * cs.y + v1 * cs.x;
+        if (L < a.epi.q_rows) {
+          a.epi.y[L] = r0;
+          a.epi.y[L + 1] = r1;
+        } else {
+          const int kr = L - a.epi.q_rows;
+          __half* dst = a.epi.k_cache + (int64_t(kr / hd) * a.epi.max_ctx + p) * hd + d;
+          dst[0] = __float2half_rn(r0);
+          dst[1] = __float2half_rn(r1);
+        }
+      } else {
+        const int vr = L - a.epi.q_rows - a.epi.k_rows;
+        const int d = vr % hd;
+        __half* dst = a.epi.v_cache + (int64_t(vr / hd) * a.epi.max_ctx + p) * hd + d;
+        dst[0] = __float2half_rn(v0);
+        dst[1] = __float2half_rn(v1);
+      }
+    }
+  }
+}
+
+// CTA-wide top-2 of the rows this CTA finished, written to top2[blockIdx.x].
+template <int NW>
+__device__ __forceinline__ void cta_top2(const GemvArgs& a, float best, int best_i, float second) {
+  __shared__ float s_b[NW], s_s[NW];
+  __shared__ int s_i[NW];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, second, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, best_i, o);
+    top2_merge(b2, i2, s2, best, best_i, second);
+  }
+  if (lane == 0) {
+    s_b[warp] = best;
+    s_s[warp] = second;
+    s_i[warp] = best_i;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = -INFINITY, s = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int w = 0; w < NW; w++) top2_merge(s_b[w], s_i[w], s_s[w], b, bi, s);
+    a.epi.top2[blockIdx.x] = make_float4(b, __int_as_float(bi), s, 0.f);
+  }
+}
+
+// ------------------------------------------------------ register-path kernel --
+
+template <int FMT, int R>
+struct Group {
+  typename Fmt<FMT>::Pay pay[R];
+  int seg[R];
+  int64_t e[R];     // flat element index of the row start (row-in-segment * cols)
+  bool live[R];
+};
+
+template <int FMT, int R>
+__device__ __forceinline__ void group_setup(const GemvArgs& a, int64_t grp, int64_t nrows, int64_t cols,
+                                            Group<FMT, R>& g) {
+#pragma unroll
+  for (int r = 0; r < R; r++) {
+    const int64_t row = grp * R + r;
+    g.live[r] = row < nrows;
+    int s = 0;
+    int64_t lr = 0;
+    if (g.live[r]) map_row(a, row, s, lr);
+    g.seg[r] = s;
+    g.e[r] = lr * cols;
+  }
+}
+
+template <int FMT, int R>
+__device__ __forceinline__ void group_load(const GemvArgs& a, Group<FMT, R>& g, int unit) {
+#pragma unroll
+  for (int r = 0; r < R; r++)
+    if (g.live[r]) Fmt<FMT>::load(g.pay[r], a.seg[g.seg[r]], g.e[r] + int64_t(unit) * Fmt<FMT>::kCols);
+}
+
+template <int FMT, int R, int EPI>
+__global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvArgs a, const int64_t nrows) {
+  using F = Fmt<FMT>;
+  constexpr int C = F::kCols, US = C + kXPad;    // unit columns, unit stride in shared memory
   extern __shared__ float4 smem4[];
-  float* xsh = reinterpret_cast<float*>(smem4);                      // [cols]
+  float* xsh = reinterpret_cast<float*>(smem4);
   const int64_t cols = a.seg[0].cols;
-  float* red = xsh + cols;                                           // [2][warps][kRows]
-  __shared__ float s_norm[32];
+  const int units = int(cols / C);
+  float* xsum = xsh + units * US;                // per 32-column unit (Q4_K)
+  __shared__ float s_red[kThreads / 32];
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nwarps = blockDim.x >> 5;
-  const int groups = blockDim.x / tr;
-  const int g = tid / tr;                 // row group of this thread
-  const int gt = tid - g * tr;            // thread within the group
-  const int wpg = tr >> 5;                // warps per group
-  const int units = int(cols / 32);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int64_t ngroups = (nrows + R - 1) / R;
+  const int64_t stride = int64_t(gridDim.x) * nw;
+  const int kiters = (units + 31) / 32;
+  int64_t grp = int64_t(blockIdx.x) * nw + warp;
 
-  // weights never depend on the previous kernel: only x (and the epilogue's
-  // outputs) do, so wait for the producer grid here, before touching them
+  // first loads before waiting for the producer of x
+  Group<FMT, R> cur;
+  if (grp < ngroups) {
+    group_setup<FMT, R>(a, grp, nrows, cols, cur);
+    if (lane < units) group_load<FMT, R>(a, cur, lane);
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // ---- stage x (and the RMSNorm scale) ------------------------------------
+  // ---- stage x ---------------------------------------------------------------
   {
-    const float4* x4 = reinterpret_cast<const float4*>(a.x);
     float ss = 0.f;
-    for (int i = tid; i < cols / 4; i += blockDim.x) {
-      float4 v = x4[i];
-      smem4[i] = v;
-      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    for (int c = tid; c < cols; c += blockDim.x) {
+      const float v = a.x[c];
+      ss += v * v;
+      xsh[(c / C) * US + F::xpos(c % C)] = v;
     }
+    float scale = 1.0f;
     if (a.norm) {
 #pragma unroll
       for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) s_norm[warp] = ss;
+      if (lane == 0) s_red[warp] = ss;
+      __syncthreads();
+      float t = 0.f;
+      for (int w = 0; w < nw; w++) t += s_red[w];
+      scale = rsqrtf(t / float(cols) + a.eps);
     }
     __syncthreads();
-  }
-  float scale = 1.0f;
-  if (a.norm) {
-    float t = 0.f;
-    for (int w = 0; w < nwarps; w++) t += s_norm[w];
-    scale = rsqrtf(t / float(cols) + a.eps);
-  }
-
-  float xs[U][32];
-  float xsum[U];
-  bool uact[U];
+    if (a.norm || F::kXSum || FMT != NT_Q8_0) {
+      // scale (norm, nibble position) in place; per-unit sums of the normalised x
+      for (int u = warp; u < units; u += nw) {
+        float v = 0.f;
+        if (lane < C) {
+          const int p = u * US + F::xpos(lane);
+          v = xsh[p] * scale;
+          xsh[p] = v * F::xscale(lane);
+        }
+        if (F::kXSum) {
 #pragma unroll
-  for (int u = 0; u < U; u++) {
-    const int unit = gt * U + u;
-    uact[u] = unit < units;
-    xsum[u] = 0.f;
-#pragma unroll
-    for (int c = 0; c < 32; c++) {
-      float v = uact[u] ? xsh[unit * 32 + c] * scale : 0.f;
-      xsum[u] += v;
-      if (Unit<FMT>::kScaledX) {
-        const int i = c & 3;   // nibble position within its 16-bit half
-        v *= (i == 0 ? 1.f : (i == 1 ? 0.0625f : (i == 2 ? 0.00390625f : 0.000244140625f)));
+          for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0) xsum[u] = v;
+        }
       }
-      xs[u][c] = v;
+      __syncthreads();
     }
   }
-
-  // ---- rows ----------------------------------------------------------------
-  const int64_t ngroups_rows = (nrows + kRows - 1) / kRows;
-  const int64_t slots = int64_t(gridDim.x) * groups;
-  const int64_t iters = (ngroups_rows + slots - 1) / slots;
-  const int64_t slot = int64_t(blockIdx.x) * groups + g;
 
   float best = -INFINITY, second = -INFINITY;
   int best_i = 0x7fffffff;
 
-  for (int64_t it = 0; it < iters; it++) {
-    const int64_t rg = slot + it * slots;
-    const int64_t r0 = rg * kRows;
-    Unit<FMT> ld[kRows][U];
-    bool ract[kRows];
+  for (; grp < ngroups; grp += stride) {
+    float acc[R];
 #pragma unroll
-    for (int rr = 0; rr < kRows; rr++) {
-      const int64_t row = r0 + rr;
-      ract[rr] = rg < ngroups_rows && row < nrows;
-      if (ract[rr]) {
-        const RowRef ref = map_row(a, row);
-        const QMat& m = seg_ref(a, ref.seg);
-#pragma unroll
-        for (int u = 0; u < U; u++)
-          if (uact[u]) ld[rr][u].load(m, ref.lr, gt * U + u);
+    for (int r = 0; r < R; r++) acc[r] = 0.f;
+    for (int it = 0; it < kiters; it++) {
+      const int u = it * 32 + lane;
+      // prefetch: next unit of this group, or the first unit of the next group
+      Group<FMT, R> nxt;
+      bool have_next = false;
+      if (it + 1 < kiters) {
+        nxt = cur;
+        if (u + 32 < units) group_load<FMT, R>(a, nxt, u + 32);
+        have_next = true;
+      } else if (grp + stride < ngroups) {
+        group_setup<FMT, R>(a, grp + stride, nrows, cols, nxt);
+        if (lane < units) group_load<FMT, R>(a, nxt, lane);
+        have_next = true;
       }
-    }
-    float acc[kRows];
+      if (u < units) {
+        const float4* xs = reinterpret_cast<const float4*>(xsh + u * US);
+        const float xu = F::kXSum ? xsum[u] : 0.f;
 #pragma unroll
-    for (int rr = 0; rr < kRows; rr++) {
-      acc[rr] = 0.f;
-#pragma unroll
-      for (int u = 0; u < U; u++)
-        if (ract[rr] && uact[u]) acc[rr] += ld[rr][u].dot(xs[u], xsum[u]);
-    }
-    // transposed warp reduction: after it lane l holds the warp sum of row l / (32 / kRows)
-    {
-      float k;
-      if (kRows == 4) {
-        const bool up = lane & 16;
-        float k0 = up ? acc[2 % kRows] : acc[0], k1 = up ? acc[3 % kRows] : acc[1 % kRows];
-        const float s0 = up ? acc[0] : acc[2 % kRows], s1 = up ? acc[1 % kRows] : acc[3 % kRows];
-        k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
-        k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
-        const bool up2 = lane & 8;
-        k = up2 ? k1 : k0;
-        const float s = up2 ? k0 : k1;
-        k += __shfl_xor_sync(0xffffffffu, s, 8);
-      } else {
-        const bool up = lane & 16;
-        k = up ? acc[1 % kRows] : acc[0];
-        const float s = up ? acc[0] : acc[1 % kRows];
-        k += __shfl_xor_sync(0xffffffffu, s, 16);
-        k += __shfl_xor_sync(0xffffffffu, k, 8);
+        for (int r = 0; r < R; r++)
+          if (cur.live[r]) acc[r] += F::dot(cur.pay[r], xs, xu);
       }
-      k += __shfl_xor_sync(0xffffffffu, k, 4);
-      k += __shfl_xor_sync(0xffffffffu, k, 2);
-      k += __shfl_xor_sync(0xffffffffu, k, 1);
-      constexpr int lanes_per_row = 32 / kRows;
-      if ((lane & (lanes_per_row - 1)) == 0) red[((it & 1) * nwarps + warp) * kRows + lane / lanes_per_row] = k;
+      if (have_next) cur = nxt;
     }
-    __syncthreads();
-    // epilogue: thread t < groups*kRows finishes row (t % kRows) of group t / kRows
-    if (tid < 64) {   // whole warps: groups * kRows <= 64 epilogue threads
-      const int eg = tid / kRows, rr = tid % kRows;
-      const int64_t rge = int64_t(blockIdx.x) * groups + eg + it * slots;
-      const int64_t row = rge * kRows + rr;
-      const bool mine = tid < groups * kRows;
-      float v = 0.f;
-      if (mine)
-        for (int w = 0; w < wpg; w++) v += red[((it & 1) * nwarps + eg * wpg + w) * kRows + rr];
-      const bool live = mine && rge < ngroups_rows && row < nrows;
-      if (EPI == EPI_STORE) {
-        if (live) a.epi.y[row] = v;
-      } else if (EPI == EPI_ADD) {
-        if (live) a.epi.y[row] += v;
-      } else if (EPI == EPI_LOGITS) {
-        if (live) {
-          a.epi.y[row] = v;
-          top2_push(v, int(row), best, best_i, second);
-        }
-      } else {
-        // pair epilogues: rows (2i, 2i+1) sit in the same group, adjacent lanes
-        const float other = __shfl_xor_sync(0xffffffffu, v, 1);
-        if (live && (rr & 1) == 0) {
-          const float v0 = v, v1 = other;
-          if (EPI == EPI_SWIGLU) {
-            a.epi.y[row >> 1] = silu(v0) * v1;
-          } else {  // EPI_QKV
-            const int L = a.epi.row_base + int(row);
-            const int hd = a.epi.head_dim;
-            const int p = *a.epi.pos;
-            if (L < a.epi.q_rows + a.epi.k_rows) {
-              const int d = L % hd;
-              const float2 cs = a.epi.rope[int64_t(p) * (hd / 2) + d / 2];
-              const float r0v = v0 * cs.x - v1 * cs.y;
-              const float r1v = v0 * cs.y + v1 * cs.x;
-              if (L < a.epi.q_rows) {
-                a.epi.y[L] = r0v;
-                a.epi.y[L + 1] = r1v;
-              } else {
-                const int kr = L - a.epi.q_rows;
-                __half* dst = a.epi.k_cache + (int64_t(kr / hd) * a.epi.max_ctx + p) * hd + d;
-                dst[0] = __float2half_rn(r0v);
-                dst[1] = __float2half_rn(r1v);
-              }
-            } else {
-              const int vr = L - a.epi.q_rows - a.epi.k_rows;
-              const int d = vr % hd;
-              __half* dst = a.epi.v_cache + (int64_t(vr / hd) * a.epi.max_ctx + p) * hd + d;
-              dst[0] = __float2half_rn(v0);
-              dst[1] = __float2half_rn(v1);
-            }
-          }
-        }
-      }
-    }
+    const float k = warp_reduce_rows<R>(acc, lane);
+    epilogue<R, EPI>(a, grp, nrows, lane, k, best, best_i, second);
   }
 
   asm volatile("griddepcontrol.launch_dependents;");
-
-  if (EPI == EPI_LOGITS) {
-    // CTA-wide top-2 over the epilogue threads (at most 32 * kRows... all < 64)
-    __shared__ float s_b[64], s_s[64];
-    __shared__ int s_i[64];
-    __syncthreads();
-    if (tid < groups * kRows) {
-      s_b[tid] = best;
-      s_s[tid] = second;
-      s_i[tid] = best_i;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float b = -INFINITY, s = -INFINITY;
-      int bi = 0x7fffffff;
-      for (int t = 0; t < groups * kRows; t++) {
-        if (s_i[t] == 0x7fffffff) continue;
-        top2_push(s_b[t], s_i[t], b, bi, s);
-        s = fmaxf(s, s_s[t]);
-      }
-      a.epi.top2[blockIdx.x] = make_float4(b, __int_as_float(bi), s, 0.f);
-    }
-  }
+  if (EPI == EPI_LOGITS) cta_top2<kThreads / 32>(a, best, best_i, second);
 }
 
-// Threads per row group for a given column count: ceil(units / U) rounded up to a warp.
-inline int gemv_tr(int64_t cols, int U) {
-  const int64_t units = cols / 32;
-  int64_t t = (units + U - 1) / U;
-  t = (t + 31) / 32 * 32;
-  return int(t);
+inline size_t gemv_smem(int fmt, int64_t cols) {
+  const int C = fmt == NT_Q8_0 ? 16 : 32;
+  return size_t(cols / C) * (C + kXPad) * 4 + size_t(cols / 32) * 4;
 }
 
-inline int gemv_units_per_thread(int64_t cols) { return cols / 32 > kMaxThreads ? 2 : 1; }
-inline int gemv_max_threads(int U) { return U == 1 ? ThreadsMax<1>::value : ThreadsMax<2>::value; }
-inline int gemv_rows_per_iter(int U) { return U == 1 ? RowsPer<1>::value : RowsPer<2>::value; }
-
-inline size_t gemv_smem(int64_t cols, int threads, int U) {
-  return size_t(cols) * 4 + size_t(2 * (threads / 32) * gemv_rows_per_iter(U)) * 4;
+// One-wave grid: SMs x resident CTAs, capped by the work and by a.max_grid.
+inline int64_t one_wave_grid(int sms, int occ, int64_t groups, int warps_per_cta, int max_grid) {
+  int64_t grid = int64_t(sms) * occ;
+  const int64_t need = (groups + warps_per_cta - 1) / warps_per_cta;
+  if (grid > need) grid = need;
+  if (grid > max_grid) grid = max_grid;
+  if (grid < 1) grid = 1;
+  return grid;
 }
 
-template <int FMT, int U, int EPI>
-cudaError_t launch_gemv_t(const GemvArgs& a, int threads, int tr, cudaStream_t s, bool pdl, int* grid_used) {
+template <int FMT, int R, int EPI>
+cudaError_t launch_gemv_t(const GemvArgs& a, cudaStream_t s, bool pdl, int* grid_used) {
   const int64_t nrows = gemv_logical_rows(a);
-  const size_t smem = gemv_smem(a.seg[0].cols, threads, U);
-  constexpr int kRows = RowsPer<U>::value;
-  auto kern = k_gemv<FMT, U, EPI>;
+  const size_t smem = gemv_smem(FMT, a.seg[0].cols);
+  auto kern = k_gemv<FMT, R, EPI>;
   static int s_sms = 0;
-  static int s_occ_threads = 0, s_occ = 0;
-  static size_t s_occ_smem = 0;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-  }
+  static size_t s_occ_smem = ~size_t(0);
+  static int s_occ = 0;
   if (!s_sms) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&s_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-  }
-  if (s_occ_threads != threads || s_occ_smem != smem) {
-    int occ = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
-    s_occ = occ < 1 ? 1 : occ;
-    s_occ_threads = threads;
+  }
+  if (s_occ_smem != smem) {
+    int occ = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) return cudaErrorInvalidConfiguration;
+    s_occ = occ;
     s_occ_smem = smem;
   }
-  const int groups = threads / tr;
-  const int64_t row_groups = (nrows + kRows - 1) / kRows;
-  int64_t grid = int64_t(s_sms) * s_occ;
-  const int64_t need = (row_groups + groups - 1) / groups;
-  if (grid > need) grid = need;
-  if (grid < 1) grid = 1;
+  const int64_t grid = one_wave_grid(s_sms, s_occ, (nrows + R - 1) / R, kThreads / 32, a.max_grid);
   if (grid_used) *grid_used = int(grid);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid));
-  cfg.blockDim = dim3(unsigned(threads));
+  cfg.blockDim = dim3(unsigned(kThreads));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -498,22 +553,21 @@ cudaError_t launch_gemv_t(const GemvArgs& a, int threads, int tr, cudaStream_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, a, nrows, tr);
+  return cudaLaunchKernelEx(&cfg, kern, a, nrows);
 }
 
 template <int FMT>
-cudaError_t launch_gemv_fmt(const GemvArgs& a, int epi, int threads, int tr, int U, cudaStream_t s, bool pdl,
-                            int* grid_used) {
-#define NT_EPI_CASES(UU)                                                                              \
-  switch (epi) {                                                                                      \
-    case EPI_STORE: return launch_gemv_t<FMT, UU, EPI_STORE>(a, threads, tr, s, pdl, grid_used);      \
-    case EPI_ADD: return launch_gemv_t<FMT, UU, EPI_ADD>(a, threads, tr, s, pdl, grid_used);          \
-    case EPI_QKV: return launch_gemv_t<FMT, UU, EPI_QKV>(a, threads, tr, s, pdl, grid_used);          \
-    case EPI_SWIGLU: return launch_gemv_t<FMT, UU, EPI_SWIGLU>(a, threads, tr, s, pdl, grid_used);    \
-    case EPI_LOGITS: return launch_gemv_t<FMT, UU, EPI_LOGITS>(a, threads, tr, s, pdl, grid_used);    \
+cudaError_t launch_gemv_fmt(const GemvArgs& a, int epi, int R, cudaStream_t s, bool pdl, int* grid_used) {
+#define NT_EPI_CASES(RR)                                                                   \
+  switch (epi) {                                                                           \
+    case EPI_STORE: return launch_gemv_t<FMT, RR, EPI_STORE>(a, s, pdl, grid_used);        \
+    case EPI_ADD: return launch_gemv_t<FMT, RR, EPI_ADD>(a, s, pdl, grid_used);            \
+    case EPI_QKV: return launch_gemv_t<FMT, RR, EPI_QKV>(a, s, pdl, grid_used);            \
+    case EPI_SWIGLU: return launch_gemv_t<FMT, RR, EPI_SWIGLU>(a, s, pdl, grid_used);      \
+    case EPI_LOGITS: return launch_gemv_t<FMT, RR, EPI_LOGITS>(a, s, pdl, grid_used);      \
   }
-  if (U == 1) {
-    NT_EPI_CASES(1)
+  if (R == 4) {
+    NT_EPI_CASES(4)
   } else {
     NT_EPI_CASES(2)
   }
@@ -522,7 +576,7 @@ cudaError_t launch_gemv_fmt(const GemvArgs& a, int epi, int threads, int tr, int
 }
 
 #define NT_DECLARE_GEMV(NAME) \
-  cudaError_t NAME(const GemvArgs& a, int epi, int threads, int tr, int U, cudaStream_t s, bool pdl, int* grid_used);
+  cudaError_t NAME(const GemvArgs& a, int epi, int R, cudaStream_t s, bool pdl, int* grid_used);
 NT_DECLARE_GEMV(launch_gemv_q8_0)
 NT_DECLARE_GEMV(launch_gemv_q4_0)
 NT_DECLARE_GEMV(launch_gemv_q4_k)

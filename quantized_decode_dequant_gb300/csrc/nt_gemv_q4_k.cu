@@ -1,9 +1,12 @@
-// nt_gemv_q4_k.cu -- instantiation of the fused dequantize-GEMV for Q4_K weights.
-#include "nt_gemv.cuh"
+// nt_gemv_q4_k.cu -- instantiations of the fused dequantize-GEMV for Q4_K weights.
+#include "nt_gemv_pipe.cuh"
 
 namespace nt {
-cudaError_t launch_gemv_q4_k(const GemvArgs& a, int epi, int threads, int tr, int U, cudaStream_t s, bool pdl,
-                             int* grid_used) {
-  return launch_gemv_fmt<NT_Q4_K>(a, epi, threads, tr, U, s, pdl, grid_used);
+cudaError_t launch_gemv_q4_k(const GemvArgs& a, int epi, int R, cudaStream_t s, bool pdl, int* grid_used) {
+  return launch_gemv_fmt<NT_Q4_K>(a, epi, R, s, pdl, grid_used);
+}
+cudaError_t launch_gemv_pipe_q4_k(const GemvArgs& a, int epi, int R, int S, cudaStream_t s, bool pdl,
+                                  int* grid_used) {
+  return launch_gemv_pipe_fmt<NT_Q4_K>(a, epi, R, S, s, pdl, grid_used);
 }
 }  // namespace nt

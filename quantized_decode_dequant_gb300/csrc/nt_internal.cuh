@@ -50,8 +50,11 @@ inline bool supported_weight_type(int t) { return block_elems(t) != 0; }
 //                                                d = f16 per 32 elements
 //   Q4_K: q  = 4-bit codes as Q4_0               meta = 16 B per 256 elements:
 //         f16 d | f16 dmin | 12 B of 6-bit sc_0..7, m_0..7 (LSB first)
-//   Q6_K: q  = low 4 bits as Q4_0, qh = high 2 bits (element k at byte k/4,
-//         bits 2*(k%4)), meta = int8 sc per 16 elements, d = f16 per 256
+//   Q6_K: q  = low 4 bits as Q4_0; qh = high 2 bits, 8 bytes per 32 elements
+//         as two little-endian words G_0 (elements 0..15) and G_1 (16..31);
+//         within G_p, element 8w+i of the unit (w = 2p + s, i = 2j + o) sits at
+//         bit 8j + (o ? 0 : 4) + (s ? 2 : 0); meta = int8 sc per 16 elements,
+//         d = f16 per 256.  (The canonical export order is rebuilt on the host.)
 struct QMat {
   int32_t type = 0;
   int64_t rows = 0, cols = 0;
@@ -107,6 +110,8 @@ struct GemvArgs {
   const float* x = nullptr;      // input [cols]
   int32_t norm = 0;              // 1: x <- x * rsqrt(mean(x^2) + eps) before the product
   float eps = 1e-5f;
+  int64_t col0 = 0, ncols = 0;   // column window [col0, col0 + ncols) (set by launch_gemv)
+  int32_t max_grid = 0;          // upper bound on CTAs (0: kMaxGemvGrid)
   EpiArgs epi;
 };
 
@@ -142,6 +147,17 @@ __device__ __forceinline__ float gen_normal(uint64_t seed, uint32_t uid, uint64_
 // fp32 formulas: Q8_0 d*q, Q4_0 d*(q-8), Q4_K fma(d*sc, q, -(dmin*m)), Q6_K (d*sc)*(q-32).
 __device__ __forceinline__ int nib_at(const uint8_t* q, int64_t e) { return (q[e >> 1] >> ((e & 1) * 4)) & 15; }
 
+// Two high bits of element e of a Q6_K tensor in the device layout (see QMat).
+__host__ __device__ __forceinline__ int q6_hi_shift(int k) {   // k = e % 32
+  const int w = k >> 3, i = k & 7;
+  return 8 * (i >> 1) + ((i & 1) ? 0 : 4) + ((w & 1) ? 2 : 0);
+}
+__device__ __forceinline__ int q6_hi(const uint8_t* qh, int64_t e) {
+  const int k = int(e & 31);
+  const uint32_t g = *reinterpret_cast<const uint32_t*>(qh + ((e - k) >> 2) + 4 * (k >> 4));
+  return int(g >> q6_hi_shift(k)) & 3;
+}
+
 __device__ __forceinline__ float dequant_elem(const QMat& m, int64_t e) {
   switch (m.type) {
     case NT_Q8_0:
@@ -167,7 +183,7 @@ __device__ __forceinline__ float dequant_elem(const QMat& m, int64_t e) {
       return __fmaf_rn(a, float(nib_at(m.q, e)), -b);
     }
     case NT_Q6_K: {
-      const int q = nib_at(m.q, e) | (((m.qh[e >> 2] >> (2 * (e & 3))) & 3) << 4);
+      const int q = nib_at(m.q, e) | (q6_hi(m.qh, e) << 4);
       const float a = __fmul_rn(__half2float(m.d[e / 256]), float(int8_t(m.meta[e / 16])));
       return __fmul_rn(a, float(q - 32));
     }

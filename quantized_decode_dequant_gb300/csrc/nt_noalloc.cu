@@ -13,8 +13,8 @@
 
 namespace nt {
 
-// Maximum number of CTAs whose summaries the array holds.  The GEMV runs at
-// most 4 CTAs per SM (>= 448 threads each), so devices with up to 256 SMs fit.
+// Maximum number of CTAs whose summaries the array holds; the GEMV launch is
+// capped to it.
 constexpr int kNoAllocMaxCtas = 1024;
 
 // 1024 x 16 B = 16 KiB per device.  Shared by every call: each call's GEMV
@@ -99,12 +99,8 @@ extern "C" nt_status nt_gemv_argmax_noalloc(const nt_qtensor* t, const float* de
   float4* scratch = nullptr;
   nt_status st = noalloc_scratch(&scratch);
   if (st) return st;
-  int dev = 0, sms = 0;
-  NT_CUDA(cudaGetDevice(&dev));
-  NT_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  if (sms * 4 > kNoAllocMaxCtas)
-    return fail(NT_E_UNSUPPORTED, "nt_gemv_argmax_noalloc: device has more than 256 SMs (scratch holds 1024 CTAs)");
   GemvArgs a;
+  a.max_grid = kNoAllocMaxCtas;
   a.seg[0] = t->m;
   a.nseg = 1;
   a.x = dev_x;

@@ -178,15 +178,18 @@ __global__ void __launch_bounds__(256) k_generate(QMat m, uint64_t seed, uint32_
     const float d = __half2float(dh);
     const int sc = d == 0.0f ? 0 : clampi(rnd(__fdiv_rn(s, d)), 0, 127);
     const float a = __fmul_rn(d, float(sc));
-    uint32_t lo = 0u, hi = 0u;
+    // lane l holds elements 8(l%4)..8(l%4)+7 of a 32-element unit: code word l%4
+    const int wi = lane & 3;
+    uint32_t lo = 0u, g = 0u;
 #pragma unroll
     for (int k = 0; k < 8; k++) {
       int q = a == 0.0f ? 32 : clampi(rnd(__fdiv_rn(w[k], a)) + 32, 0, 63);
       lo |= uint32_t(q & 15) << (4 * k);
-      hi |= uint32_t(q >> 4) << (2 * k);
+      g |= uint32_t(q >> 4) << q6_hi_shift(8 * wi + k);
     }
+    g |= __shfl_xor_sync(0xffffffffu, g, 1);   // code words 2p and 2p+1 share high-bit word G_p
     *reinterpret_cast<uint32_t*>(m.q + ebase / 2) = lo;
-    *reinterpret_cast<uint16_t*>(m.qh + ebase / 4) = uint16_t(hi);
+    if ((wi & 1) == 0) *reinterpret_cast<uint32_t*>(m.qh + (ebase - 8 * wi) / 4 + 4 * (wi >> 1)) = g;
     if ((lane & 1) == 0) m.meta[ebase / 16] = uint8_t(int8_t(sc));
     if (lane == 0) m.d[ebase / 256] = dh;
   }
@@ -264,12 +267,22 @@ static nt_status export_rows(const nt_qtensor* t, int64_t row0, int64_t nrows, u
         memcpy(out, &meta[b * 16], 16);
         memcpy(out + 16, &q[e / 2], 128);
         break;
-      case NT_Q6_K:
+      case NT_Q6_K: {
         memcpy(out, &q[e / 2], 128);
-        memcpy(out + 128, &qh[e / 4], 64);
+        // canonical high bits: element k of the block at byte k/4, bits 2(k%4)
+        uint8_t* cqh = out + 128;
+        memset(cqh, 0, 64);
+        for (int k = 0; k < 256; k++) {
+          const int64_t ue = e + (k & ~31);            // first element of k's 32-element unit
+          const int kk = k & 31;
+          const uint8_t* gp = &qh[ue / 4 + 4 * (kk >> 4)];
+          const uint32_t g = uint32_t(gp[0]) | (uint32_t(gp[1]) << 8) | (uint32_t(gp[2]) << 16) | (uint32_t(gp[3]) << 24);
+          const int hi = int(g >> q6_hi_shift(kk)) & 3;
+          cqh[k >> 2] |= uint8_t(hi << (2 * (k & 3)));
+        }
         memcpy(out + 192, &meta[e / 16], 16);
         memcpy(out + 208, &d[b * 2], 2);
-        break;
+      } break;
     }
   }
   return NT_OK;
