@@ -27,7 +27,7 @@ cudaError_t launch_gemv(const GemvArgs& a_in, int epi, cudaStream_t s, bool pdl,
   const int fmt = a.seg[0].type;
   const int64_t nrows = gemv_logical_rows(a);
   const int R = nrows >= 16384 ? 4 : 2;
-  const int64_t align = fmt == NT_Q6_K ? 512 : 256;
+  const int64_t align = 1024;   // whole 32-unit tiles for the pipeline
   static const bool force_register_path = getenv("NT_GEMV_REGISTER_PATH") != nullptr;
   if (cols % align == 0 && !force_register_path) {
     int parts = 1;

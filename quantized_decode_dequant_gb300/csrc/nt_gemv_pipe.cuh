@@ -1,23 +1,39 @@
 // nt_gemv_pipe.cuh -- the fused dequantize-GEMV with weights staged through a
-// per-warp shared-memory ring by asynchronous copies.
+// per-warp shared-memory ring by asynchronous copies, decoded with integer dot
+// products.
 //
-// Same work split and decode arithmetic as nt_gemv.cuh (warps own groups of R
-// rows, lanes own 32-column units, x staged once per CTA), but the codes and
-// scales of each (row group, 32-unit column tile) are copied global -> shared
-// with cp.async (16-byte LDGSTS, L2-only) S-1 tiles ahead of the one being
-// decoded.  Bytes in flight per warp are (S-1) * R * (row tile bytes) with no
-// register cost, which is what a bandwidth-bound GEMV needs to cover DRAM
-// latency; the only waits are cp.async.wait_group on the warp's own copies
-// plus __syncwarp for the scale bytes other lanes copied.
+// Work split (as nt_gemv.cuh): warps own groups of R rows, lanes own 32-column
+// units, x is staged once per CTA.  The codes and scales of each (row group,
+// 32-unit column tile) are copied global -> shared with cp.async (16-byte
+// LDGSTS, L2-only) S-1 tiles ahead of the tile being decoded, so every warp
+// keeps (S-1) * R row tiles in flight without spending registers on them; the
+// only waits are cp.async.wait_group on the warp's own copies plus __syncwarp
+// for the scale bytes other lanes copied.
+//
+// Arithmetic.  Each 32-column block of x is carried as 16-bit fixed point: an
+// fp32 scale sx = max|x|/32512 and integers t_c = round(x_c/sx) split as
+// t = 256 h + l with h, l int8.  The codes are exact small integers, so
+// sum_c q_c t_c = 256 sum q h + sum q l is computed exactly with DP4A (four
+// int8 products per instruction) and only the per-block combination with the
+// fp16 scales is floating point, accumulated in fp32.  The offsets of the
+// formats use the staged block sums T = sum t:
+//   Q8_0  d sx S,                       S = 256 Sh + Sl
+//   Q4_0  d sx (S - 8 T)
+//   Q4_K  sx (d sc S - dmin m T)
+//   Q6_K  d sx (sc_0 (S_0 - 32 T_0) + sc_1 (S_1 - 32 T_1))  (two 16-element halves)
+// The only approximation beyond fp32 is x's rounding to 16 bits per block
+// (|error| <= sx/2, i.e. 2^-16 of the block's largest |x|).  Nibble codes are
+// spread to bytes by masking even and odd nibbles (x staged in the matching
+// [0,2,4,6 | 1,3,5,7] order per 8 columns); Q6_K codes get their two high
+// bits OR-ed in from the device's high-bit words.
 //
 // Row tile layout in shared memory (one row, 32 units):
 //   Q8_0  32 x 32 B codes | 32 x f16 d                                  1088 B
 //   Q4_0  32 x 16 B codes | 32 x f16 d                                   576 B
 //   Q4_K  32 x 16 B codes | 4 x 16 B superblock headers                  576 B
 //   Q6_K  32 x 16 B low codes | 32 x 8 B high-bit words | 32 x 2 B sc | 4 x f16 d (16 B slot)   848 B
-// Requires the window width (and start) to be a multiple of 256 columns (512
-// for Q6_K) so every scale piece is a whole number of aligned 16-byte (4-byte
-// for Q6_K d) copies.
+// Requires the window width and start to be multiples of 1024 columns, so every
+// tile is whole and every scale piece an aligned 16-byte (4-byte for Q6_K d) copy.
 #pragma once
 
 #include "nt_gemv.cuh"
@@ -26,6 +42,7 @@ namespace nt {
 
 constexpr int kPipeWarps = 8;                 // 256 threads per CTA
 constexpr int kPipeMaxSmem = 221 * 1024;      // dynamic shared memory a CTA may ask for
+constexpr int kXUnit = 80;                    // staged x per 32 columns: h[32] | l[32] | sx, T0, T1, pad
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -54,191 +71,322 @@ __device__ __forceinline__ void cp_wait_dyn(int n) {
   }
 }
 
+// One staged x block in registers.
+struct XBlock {
+  int h[8], l[8];   // int8 halves, four per word, in the format's element order
+  float sx;         // block scale
+  int t0, t1;       // sums of t over elements 0..15 and 16..31
+};
+
+__device__ __forceinline__ void load_xblock(const uint8_t* p, XBlock& x) {
+  const uint4 h0 = *reinterpret_cast<const uint4*>(p), h1 = *reinterpret_cast<const uint4*>(p + 16);
+  const uint4 l0 = *reinterpret_cast<const uint4*>(p + 32), l1 = *reinterpret_cast<const uint4*>(p + 48);
+  const uint4 m = *reinterpret_cast<const uint4*>(p + 64);
+  x.h[0] = h0.x; x.h[1] = h0.y; x.h[2] = h0.z; x.h[3] = h0.w;
+  x.h[4] = h1.x; x.h[5] = h1.y; x.h[6] = h1.z; x.h[7] = h1.w;
+  x.l[0] = l0.x; x.l[1] = l0.y; x.l[2] = l0.z; x.l[3] = l0.w;
+  x.l[4] = l1.x; x.l[5] = l1.y; x.l[6] = l1.z; x.l[7] = l1.w;
+  x.sx = __uint_as_float(m.x);
+  x.t0 = int(m.y);
+  x.t1 = int(m.z);
+}
+
+// sum over words [W0, W1) of (codes . x) as 256 * (codes . h) + (codes . l)
+template <int W0, int W1>
+__device__ __forceinline__ int idot(const int (&c)[8], const XBlock& x) {
+  int ah0 = 0, ah1 = 0, al0 = 0, al1 = 0;
+#pragma unroll
+  for (int k = W0; k < W1; k += 2) {
+    ah0 = __dp4a(c[k], x.h[k], ah0);
+    al0 = __dp4a(c[k], x.l[k], al0);
+    ah1 = __dp4a(c[k + 1], x.h[k + 1], ah1);
+    al1 = __dp4a(c[k + 1], x.l[k + 1], al1);
+  }
+  return (ah0 + ah1) * 256 + (al0 + al1);
+}
+
+// even and odd nibbles of each code word as bytes: words 2k (elements 8k+0,2,4,6) and 2k+1 (8k+1,3,5,7)
+__device__ __forceinline__ void nibble_bytes(const uint4 w, int (&c)[8]) {
+  const uint32_t L = 0x0F0F0F0Fu;
+  c[0] = int(w.x & L); c[1] = int((w.x >> 4) & L);
+  c[2] = int(w.y & L); c[3] = int((w.y >> 4) & L);
+  c[4] = int(w.z & L); c[5] = int((w.z >> 4) & L);
+  c[6] = int(w.w & L); c[7] = int((w.w >> 4) & L);
+}
+
 template <int FMT> struct Pipe;
 
 template <> struct Pipe<NT_Q8_0> {
-  static constexpr int RB = 32 * 32 + 64;
-  static constexpr bool kXSum = false;
-  // e_row: flat element index of the row's first column in the window; u0: first unit of the tile
-  __device__ static void issue(const QMat& m, int64_t e_row, int u0, int nu, uint32_t dst, int lane) {
-    if (lane < nu) {
-      const uint8_t* src = m.q + e_row + int64_t(u0 + lane) * 32;
-      cp16(dst + lane * 32, src);
-      cp16(dst + lane * 32 + 16, src + 16);
-    }
-    if (lane < nu / 8)
-      cp16(dst + 1024 + lane * 16, reinterpret_cast<const uint8_t*>(m.d + (e_row >> 5) + u0) + lane * 16);
+  static constexpr int CB = 32, RB = 32 * 32 + 64;
+  __device__ static int xbyte(int c) { return c; }   // natural order
+  // e0: flat index of the tile's first element in this row; the lane copies its unit's codes
+  __device__ static void issue_codes(const QMat& m, int64_t e0, int lane, uint32_t dst) {
+    const uint8_t* src = m.q + e0 + lane * 32;
+    cp16(dst, src);
+    cp16(dst + 16, src + 16);
   }
-  __device__ static float dot(const uint8_t* blk, int lane, const float4* xs, float) {
+  static constexpr int NP = 4;   // 16-byte pieces of scales per row of a tile
+  __device__ static const void* aux_src(const QMat& m, int64_t e0, int i, int& off) {
+    off = 1024 + i * 16;
+    return reinterpret_cast<const uint8_t*>(m.d + (e0 >> 5)) + i * 16;
+  }
+  __device__ static float dot(const uint8_t* blk, int lane, const XBlock& x) {
     const uint4 c0 = *reinterpret_cast<const uint4*>(blk + lane * 32);
     const uint4 c1 = *reinterpret_cast<const uint4*>(blk + lane * 32 + 16);
-    const uint32_t d = *reinterpret_cast<const uint16_t*>(blk + 1024 + lane * 2);
-    return h2f_bits(d) * (q8_dot16(c0, xs) + q8_dot16(c1, xs + 4));
+    const int c[8] = {int(c0.x), int(c0.y), int(c0.z), int(c0.w), int(c1.x), int(c1.y), int(c1.z), int(c1.w)};
+    const float d = h2f_bits(*reinterpret_cast<const uint16_t*>(blk + 1024 + lane * 2));
+    return (d * x.sx) * float(idot<0, 8>(c, x));
   }
-  __device__ static int xpos(int c) { return c; }
-  __device__ static float xscale(int) { return 1.0f; }
 };
 
+__device__ __forceinline__ int nibble_xbyte(int c) { return (c & ~7) + ((c & 1) << 2) + ((c & 7) >> 1); }
+
 template <> struct Pipe<NT_Q4_0> {
-  static constexpr int RB = 32 * 16 + 64;
-  static constexpr bool kXSum = false;
-  __device__ static void issue(const QMat& m, int64_t e_row, int u0, int nu, uint32_t dst, int lane) {
-    if (lane < nu) cp16(dst + lane * 16, m.q + ((e_row + int64_t(u0 + lane) * 32) >> 1));
-    if (lane < nu / 8)
-      cp16(dst + 512 + lane * 16, reinterpret_cast<const uint8_t*>(m.d + (e_row >> 5) + u0) + lane * 16);
+  static constexpr int CB = 16, RB = 32 * 16 + 64;
+  __device__ static int xbyte(int c) { return nibble_xbyte(c); }
+  __device__ static void issue_codes(const QMat& m, int64_t e0, int lane, uint32_t dst) {
+    cp16(dst, m.q + (e0 >> 1) + lane * 16);
   }
-  __device__ static float dot(const uint8_t* blk, int lane, const float4* xs, float) {
-    Fmt<NT_Q4_0>::Pay p;
-    p.c = *reinterpret_cast<const uint4*>(blk + lane * 16);
-    p.d = *reinterpret_cast<const uint16_t*>(blk + 512 + lane * 2);
-    return Fmt<NT_Q4_0>::dot(p, xs, 0.f);
+  static constexpr int NP = 4;
+  __device__ static const void* aux_src(const QMat& m, int64_t e0, int i, int& off) {
+    off = 512 + i * 16;
+    return reinterpret_cast<const uint8_t*>(m.d + (e0 >> 5)) + i * 16;
   }
-  __device__ static int xpos(int c) { return c; }
-  __device__ static float xscale(int c) { return nib_xscale(c); }
+  __device__ static float dot(const uint8_t* blk, int lane, const XBlock& x) {
+    int c[8];
+    nibble_bytes(*reinterpret_cast<const uint4*>(blk + lane * 16), c);
+    const float d = h2f_bits(*reinterpret_cast<const uint16_t*>(blk + 512 + lane * 2));
+    return (d * x.sx) * float(idot<0, 8>(c, x) - 8 * (x.t0 + x.t1));
+  }
 };
 
 template <> struct Pipe<NT_Q4_K> {
-  static constexpr int RB = 32 * 16 + 64;
-  static constexpr bool kXSum = true;
-  __device__ static void issue(const QMat& m, int64_t e_row, int u0, int nu, uint32_t dst, int lane) {
-    if (lane < nu) cp16(dst + lane * 16, m.q + ((e_row + int64_t(u0 + lane) * 32) >> 1));
-    if (lane < nu / 8) cp16(dst + 512 + lane * 16, m.meta + ((e_row >> 8) + u0 / 8 + lane) * 16);
+  static constexpr int CB = 16, RB = 32 * 16 + 64;
+  __device__ static int xbyte(int c) { return nibble_xbyte(c); }
+  __device__ static void issue_codes(const QMat& m, int64_t e0, int lane, uint32_t dst) {
+    cp16(dst, m.q + (e0 >> 1) + lane * 16);
   }
-  __device__ static float dot(const uint8_t* blk, int lane, const float4* xs, float xsum) {
-    Fmt<NT_Q4_K>::Pay p;
-    p.c = *reinterpret_cast<const uint4*>(blk + lane * 16);
-    p.meta = *reinterpret_cast<const uint4*>(blk + 512 + (lane >> 3) * 16);
-    p.j = lane & 7;
-    return Fmt<NT_Q4_K>::dot(p, xs, xsum);
+  static constexpr int NP = 4;
+  __device__ static const void* aux_src(const QMat& m, int64_t e0, int i, int& off) {
+    off = 512 + i * 16;
+    return m.meta + ((e0 >> 8) + i) * 16;
   }
-  __device__ static int xpos(int c) { return c; }
-  __device__ static float xscale(int c) { return nib_xscale(c); }
+  __device__ static float dot(const uint8_t* blk, int lane, const XBlock& x) {
+    int c[8];
+    nibble_bytes(*reinterpret_cast<const uint4*>(blk + lane * 16), c);
+    const uint4 meta = *reinterpret_cast<const uint4*>(blk + 512 + (lane >> 3) * 16);
+    const int j = lane & 7;
+    // 6-bit fields: sc_j at bit 6j, m_j at bit 6(8+j) of the 96-bit stream (meta.y, meta.z, meta.w)
+    const uint64_t lo = uint64_t(meta.y) | (uint64_t(meta.z) << 32);
+    const uint32_t sc = uint32_t(lo >> (6 * j)) & 63u;
+    const int mb = 48 + 6 * j;
+    const uint32_t mm = mb >= 64 ? (meta.w >> (mb - 64)) & 63u
+                                 : uint32_t((lo >> mb) | (uint64_t(meta.w) << (64 - mb))) & 63u;
+    const float a = h2f_bits(meta.x & 0xFFFFu) * float(sc);
+    const float b = h2f_bits(meta.x >> 16) * float(mm);
+    return x.sx * (a * float(idot<0, 8>(c, x)) - b * float(x.t0 + x.t1));
+  }
 };
 
 template <> struct Pipe<NT_Q6_K> {
-  static constexpr int RB = 32 * 16 + 256 + 64 + 16;
-  static constexpr bool kXSum = false;
-  __device__ static void issue(const QMat& m, int64_t e_row, int u0, int nu, uint32_t dst, int lane) {
-    const int64_t e0 = e_row + int64_t(u0) * 32;   // first element of the tile
-    if (lane < nu) cp16(dst + lane * 16, m.q + ((e0 + int64_t(lane) * 32) >> 1));
-    if (lane < nu / 2) cp16(dst + 512 + lane * 16, m.qh + (e0 >> 2) + lane * 16);
-    if (lane < nu / 8) cp16(dst + 768 + lane * 16, m.meta + (e0 >> 4) + lane * 16);
-    if (lane < nu / 16) cp4(dst + 832 + lane * 4, reinterpret_cast<const uint8_t*>(m.d + (e0 >> 8)) + lane * 4);
+  static constexpr int CB = 16, RB = 32 * 16 + 256 + 64 + 16;
+  __device__ static int xbyte(int c) { return nibble_xbyte(c); }
+  __device__ static void issue_codes(const QMat& m, int64_t e0, int lane, uint32_t dst) {
+    cp16(dst, m.q + (e0 >> 1) + lane * 16);
   }
-  __device__ static float dot(const uint8_t* blk, int lane, const float4* xs, float) {
-    Fmt<NT_Q6_K>::Pay p;
-    p.c = *reinterpret_cast<const uint4*>(blk + lane * 16);
-    p.h = *reinterpret_cast<const uint2*>(blk + 512 + lane * 8);
-    p.sc = *reinterpret_cast<const uint16_t*>(blk + 768 + lane * 2);
-    p.d = *reinterpret_cast<const uint16_t*>(blk + 832 + (lane >> 3) * 2);
-    return Fmt<NT_Q6_K>::dot(p, xs, 0.f);
+  // 16 pieces of high-bit words (16 B = 2 units), then 4 of sub-block scales (16 B = 8 units)
+  static constexpr int NP = 20;
+  __device__ static const void* aux_src(const QMat& m, int64_t e0, int i, int& off) {
+    if (i < 16) {
+      off = 512 + i * 16;
+      return m.qh + (e0 >> 2) + i * 16;
+    }
+    off = 768 + (i - 16) * 16;
+    return m.meta + (e0 >> 4) + (i - 16) * 16;
   }
-  __device__ static int xpos(int c) { return Fmt<NT_Q6_K>::xpos(c); }
-  __device__ static float xscale(int) { return 1.0f; }
+  __device__ static float dot(const uint8_t* blk, int lane, const XBlock& x) {
+    const uint4 w = *reinterpret_cast<const uint4*>(blk + lane * 16);
+    const uint2 g = *reinterpret_cast<const uint2*>(blk + 512 + lane * 8);
+    const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(blk + 768 + lane * 2);
+    const float d = h2f_bits(*reinterpret_cast<const uint16_t*>(blk + 832 + (lane >> 3) * 2));
+    // device high-bit word G (one per 16 elements): byte j holds, for code words
+    // W (elements 0..7) and W' (elements 8..15), hi(W,2j) at bits 4-5,
+    // hi(W',2j) at bits 6-7, hi(W,2j+1) at bits 0-1, hi(W',2j+1) at bits 2-3
+    const uint32_t M = 0x30303030u, L = 0x0F0F0F0Fu;
+    const int c[8] = {int((w.x & L) | (g.x & M)),        int(((w.x >> 4) & L) | ((g.x << 4) & M)),
+                      int((w.y & L) | ((g.x >> 2) & M)), int(((w.y >> 4) & L) | ((g.x << 2) & M)),
+                      int((w.z & L) | (g.y & M)),        int(((w.z >> 4) & L) | ((g.y << 4) & M)),
+                      int((w.w & L) | ((g.y >> 2) & M)), int(((w.w >> 4) & L) | ((g.y << 2) & M))};
+    const int s0 = idot<0, 4>(c, x) - 32 * x.t0;
+    const int s1 = idot<4, 8>(c, x) - 32 * x.t1;
+    const float sc0 = float(int8_t(sc2 & 0xFF)), sc1 = float(int8_t(sc2 >> 8));
+    return (d * x.sx) * (sc0 * float(s0) + sc1 * float(s1));
+  }
 };
 
-// Rows of one group as seen by the copy issuer.
+// Rows of one group as seen by the copy issuer (R is small; indexed with constants or selects).
 template <int R>
 struct GroupRows {
   int seg[R];
   int64_t e[R];
-  bool live[R];
+  int nlive;   // rows [0, nlive) of the group exist
 };
 
 template <int R>
 __device__ __forceinline__ void rows_setup(const GemvArgs& a, int64_t grp, int64_t nrows, GroupRows<R>& g) {
+  g.nlive = int(nrows - grp * R < R ? nrows - grp * R : R);
 #pragma unroll
   for (int r = 0; r < R; r++) {
-    const int64_t row = grp * R + r;
-    g.live[r] = row < nrows;
     int s = 0;
     int64_t lr = 0;
-    if (g.live[r]) map_row(a, row, s, lr);
+    if (r < g.nlive) map_row(a, grp * R + r, s, lr);
     g.seg[r] = s;
     g.e[r] = lr * a.seg[0].cols + a.col0;
   }
+}
+
+template <int R>
+__device__ __forceinline__ int64_t pick(const int64_t (&v)[R], int r) {
+  int64_t out = v[0];
+#pragma unroll
+  for (int i = 1; i < R; i++) out = r == i ? v[i] : out;
+  return out;
+}
+template <int R>
+__device__ __forceinline__ int pick(const int (&v)[R], int r) {
+  int out = v[0];
+#pragma unroll
+  for (int i = 1; i < R; i++) out = r == i ? v[i] : out;
+  return out;
 }
 
 template <int FMT, int R, int EPI>
 __global__ void __launch_bounds__(kPipeWarps * 32) k_gemv_pipe(const __grid_constant__ GemvArgs a,
                                                               const int64_t nrows, const int S) {
   using P = Pipe<FMT>;
-  constexpr int US = 32 + kXPad;                  // x floats per unit in shared memory
   constexpr int nw = kPipeWarps;
   extern __shared__ float4 smem4[];
-  const int64_t cols = a.ncols;                   // window width
+  const int64_t cols = a.ncols;                   // window width, a multiple of 1024
   const int units = int(cols / 32);
-  float* xsh = reinterpret_cast<float*>(smem4);
-  float* xsum = xsh + units * US;
-  uint8_t* ring = reinterpret_cast<uint8_t*>(xsum + ((units + 3) & ~3));
+  const int kiters = units / 32;
+  uint8_t* xq = reinterpret_cast<uint8_t*>(smem4);          // units x kXUnit
+  uint8_t* ring = xq + size_t(units) * kXUnit;
   __shared__ float s_red[kPipeWarps];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t ngroups = (nrows + R - 1) / R;
   const int64_t stride = int64_t(gridDim.x) * nw;
-  const int kiters = (units + 31) / 32;
   uint8_t* wring = ring + size_t(warp) * S * R * P::RB;
   const uint32_t wring_s = smem_addr(wring);
 
-  // tile t of this warp = (its k-th row group, column tile it), t = k * kiters + it
+  // this warp's tiles, in order: its row groups g0, g0 + stride, ..., each in kiters column tiles
   const int64_t g0 = int64_t(blockIdx.x) * nw + warp;
   const int64_t my_groups = g0 < ngroups ? (ngroups - 1 - g0) / stride + 1 : 0;
   const int64_t ntiles = my_groups * kiters;
 
-  // copy issuer state (runs S-1 tiles ahead)
-  int64_t t_issue = 0;
+  // copy issuer: runs S-1 tiles ahead of the decoder, with its own cursor
+  int64_t i_grp = g0, i_left = ntiles;
+  int i_it = 0, i_slot = 0;
   GroupRows<R> ig;
-  auto issue_tile = [&](int64_t t) {
-    if (t < ntiles) {
-      const int64_t k = t / kiters;
-      const int it = int(t - k * kiters);
-      if (it == 0) rows_setup<R>(a, g0 + k * stride, nrows, ig);
-      const int u0 = it * 32;
-      const int nu = min(32, units - u0);
-      const uint32_t dst = wring_s + uint32_t((t % S) * R * P::RB);
+  auto issue_next = [&]() {
+    if (i_left > 0) {
+      if (i_it == 0) rows_setup<R>(a, i_grp, nrows, ig);
+      const uint32_t dst = wring_s + uint32_t(i_slot * R * P::RB);
+      const int64_t toff = int64_t(i_it) * 1024;          // first element of the tile in the row window
 #pragma unroll
       for (int r = 0; r < R; r++)
-        if (ig.live[r]) P::issue(a.seg[ig.seg[r]], ig.e[r], u0, nu, dst + r * P::RB, lane);
+        if (r < ig.nlive) P::issue_codes(a.seg[ig.seg[r]], ig.e[r] + toff, lane, dst + r * P::RB + lane * P::CB);
+#pragma unroll
+      for (int p0 = 0; p0 < R * P::NP; p0 += 32) {
+        const int p = p0 + lane;
+        const int r = p / P::NP, i = p % P::NP;
+        if (p < R * P::NP && r < ig.nlive) {
+          int off;
+          const void* src = P::aux_src(a.seg[pick<R>(ig.seg, r)], pick<R>(ig.e, r) + toff, i, off);
+          cp16(dst + r * P::RB + off, src);
+        }
+      }
+      if (FMT == NT_Q6_K) {   // f16 d per 256 columns: two 4-byte pieces per row
+        const int r = lane >> 1, i = lane & 1;
+        if (lane < 2 * R && r < ig.nlive) {
+          const int64_t e0 = pick<R>(ig.e, r) + toff;
+          cp4(dst + r * P::RB + 832 + i * 4,
+              reinterpret_cast<const uint8_t*>(a.seg[pick<R>(ig.seg, r)].d + (e0 >> 8)) + i * 4);
+        }
+      }
+      --i_left;
+      if (++i_slot == S) i_slot = 0;
+      if (++i_it == kiters) {
+        i_it = 0;
+        i_grp += stride;
+      }
     }
     cp_commit();   // one group per tile, empty past the end, so the wait_group counts stay aligned
   };
 
   // prologue: the first S-1 tiles before waiting for the producer of x
-  for (; t_issue < S - 1; t_issue++) issue_tile(t_issue);
+  for (int t = 0; t < S - 1; t++) issue_next();
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // ---- stage x ---------------------------------------------------------------
+  // ---- stage x: 16-bit fixed point per 32-column block, and the RMS scale ----
+  // Chunks of 8192 columns: every thread issues its eight float4 loads before
+  // using any, so a chunk costs one memory latency.  Eight consecutive threads
+  // hold one 32-column block (one float4 each).
+  float scale = 1.0f;
   {
-    const float* xg = a.x + a.col0;
+    const float4* x4 = reinterpret_cast<const float4*>(a.x + a.col0);
+    const int64_t n4 = cols / 4;
     float ss = 0.f;
-    for (int c = tid; c < cols; c += blockDim.x) {
-      const float v = xg[c];
-      ss += v * v;
-      xsh[(c >> 5) * US + P::xpos(c & 31)] = v;
+    for (int64_t f0 = 0; f0 < n4; f0 += 8 * kPipeWarps * 32) {
+      float4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        const int64_t f = f0 + tid + i * (kPipeWarps * 32);
+        v[i] = f < n4 ? x4[f] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        const int64_t f = f0 + tid + i * (kPipeWarps * 32);
+        ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+        float amax = fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w)));
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float inv = amax > 0.f ? 32512.0f / amax : 0.f;
+        const float vv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        const int c0 = int(f & 7) * 4;                       // first column of this float4 in its block
+        uint8_t* blk = xq + size_t(f >> 3) * kXUnit;
+        int tsum = 0;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+          int t = __float2int_rn(vv[j] * inv);
+          t = max(-32512, min(32512, t));
+          const int h = (t + 128) >> 8;
+          tsum += t;
+          if (f < n4) {
+            blk[P::xbyte(c0 + j)] = uint8_t(int8_t(h));
+            blk[32 + P::xbyte(c0 + j)] = uint8_t(int8_t(t - 256 * h));
+          }
+        }
+        int t0 = c0 < 16 ? tsum : 0, t1 = c0 < 16 ? 0 : tsum;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+          t0 += __shfl_xor_sync(0xffffffffu, t0, o);
+          t1 += __shfl_xor_sync(0xffffffffu, t1, o);
+        }
+        if (f < n4 && c0 == 0)
+          *reinterpret_cast<uint4*>(blk + 64) = make_uint4(__float_as_uint(amax / 32512.0f), uint32_t(t0), uint32_t(t1), 0u);
+      }
     }
-    float scale = 1.0f;
     if (a.norm) {
 #pragma unroll
       for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       if (lane == 0) s_red[warp] = ss;
-      __syncthreads();
+    }
+    __syncthreads();
+    if (a.norm) {
       float t = 0.f;
       for (int w = 0; w < nw; w++) t += s_red[w];
       scale = rsqrtf(t / float(cols) + a.eps);
-    }
-    __syncthreads();
-    if (a.norm || P::kXSum || FMT != NT_Q8_0) {
-      for (int u = warp; u < units; u += nw) {
-        const int p = u * US + P::xpos(lane);
-        float v = xsh[p] * scale;
-        xsh[p] = v * P::xscale(lane);
-        if (P::kXSum) {
-#pragma unroll
-          for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-          if (lane == 0) xsum[u] = v;
-        }
-      }
-      __syncthreads();
     }
   }
 
@@ -248,27 +396,31 @@ __global__ void __launch_bounds__(kPipeWarps * 32) k_gemv_pipe(const __grid_cons
 #pragma unroll
   for (int r = 0; r < R; r++) acc[r] = 0.f;
 
+  int64_t c_grp = g0;
+  int c_it = 0, c_slot = 0;
+  int nlive = int(nrows - c_grp * R < R ? nrows - c_grp * R : R);
   for (int64_t t = 0; t < ntiles; t++) {
-    cp_wait_dyn(S - 2);   // this lane's copies of tile t have landed
-    __syncwarp();         // ... and every lane's (scales are copied by a few lanes); slot t-1 is free
-    issue_tile(t_issue++);
-    const int64_t k = t / kiters;
-    const int it = int(t - k * kiters);
-    const int64_t grp = g0 + k * stride;
-    const int u = it * 32 + lane;
-    if (u < units) {
-      const uint8_t* blk = wring + (t % S) * R * P::RB;
-      const float4* xs = reinterpret_cast<const float4*>(xsh + u * US);
-      const float xu = P::kXSum ? xsum[u] : 0.f;
+    cp_wait_dyn(S - 2);   // this lane's copies of the tile have landed
+    __syncwarp();         // ... and every lane's (scales are copied by a few lanes); the previous slot is free
+    issue_next();
+    XBlock xb;
+    load_xblock(xq + size_t(c_it * 32 + lane) * kXUnit, xb);
+    const uint8_t* blk = wring + c_slot * R * P::RB;
 #pragma unroll
-      for (int r = 0; r < R; r++)
-        if (grp * R + r < nrows) acc[r] += P::dot(blk + r * P::RB, lane, xs, xu);
-    }
-    if (it != kiters - 1) continue;
-    const float kk = warp_reduce_rows<R>(acc, lane);
+    for (int r = 0; r < R; r++)
+      if (r < nlive) acc[r] += P::dot(blk + r * P::RB, lane, xb);
+    if (++c_slot == S) c_slot = 0;
+    if (++c_it < kiters) continue;
+
+    // ---- row group done: transposed warp reduction, epilogue ----------------
+    c_it = 0;
+    float kk = warp_reduce_rows<R>(acc, lane);
 #pragma unroll
     for (int r = 0; r < R; r++) acc[r] = 0.f;
-    epilogue<R, EPI>(a, grp, nrows, lane, kk, best, best_i, second);
+    kk *= scale;
+    epilogue<R, EPI>(a, c_grp, nrows, lane, kk, best, best_i, second);
+    c_grp += stride;
+    nlive = int(nrows - c_grp * R < R ? nrows - c_grp * R : R);
   }
   cp_wait<0>();
 
@@ -276,10 +428,7 @@ __global__ void __launch_bounds__(kPipeWarps * 32) k_gemv_pipe(const __grid_cons
   if (EPI == EPI_LOGITS) cta_top2<kPipeWarps>(a, best, best_i, second);
 }
 
-inline size_t pipe_x_bytes(int64_t cols) {
-  const int64_t units = cols / 32;
-  return size_t(units) * (32 + kXPad) * 4 + size_t((units + 3) & ~3) * 4;
-}
+inline size_t pipe_x_bytes(int64_t cols) { return size_t(cols / 32) * kXUnit; }
 inline int pipe_row_bytes(int fmt) {
   switch (fmt) {
     case NT_Q8_0: return Pipe<NT_Q8_0>::RB;

@@ -41,7 +41,9 @@ def test_gemv_matches_oracle(nt, fmt, rows, cols):
         assert np.isfinite(got).all()
         err = rel_l2(got, want)
         assert err < TOL, err
-        assert err < 1e-5, f"fp32 accumulation should be far inside the tolerance: {err}"
+        # activations are carried as 16-bit fixed point per 32-column block (error <= 2^-16 of the
+        # block's largest |x|): expected relative L2 ~2e-5, far inside the tolerance
+        assert err < 1e-4, f"should be far inside the tolerance: {err}"
         # determinism: a second launch gives the same bits
         np.testing.assert_array_equal(_gemv(nt, t, x, rows), got)
     finally:
