@@ -36,6 +36,16 @@ constexpr uint32_t kUidEmbd = 0x100000u, kUidOutput = 0x100001u, kUidKv = 0x2000
 
 // ---------------------------------------------------------------- kernels --
 
+__device__ __forceinline__ uint32_t attn_smem(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void attn_cp16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void attn_cp_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
 __global__ void k_embed(const QMat e, const int32_t* __restrict__ d_token, float* __restrict__ x) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= e.cols) return;
@@ -69,12 +79,15 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const float* __restrict__
   const __half* kb = kc + (int64_t(g) * max_ctx + t0) * HD;
   const __half* vb = vc + (int64_t(g) * max_ctx + t0) * HD;
   constexpr int VPR = HD / 8;
+  // every copy of the chunk issued before any is waited for: one memory latency
+  const uint32_t ks = attn_smem(Ks), vs = attn_smem(Vs), qss = attn_smem(qs);
   for (int i = tid; i < cnt * VPR; i += blockDim.x) {
     const int r = i / VPR, c = i % VPR;
-    *reinterpret_cast<uint4*>(Ks + r * KP + c * 8) = __ldg(reinterpret_cast<const uint4*>(kb + r * HD + c * 8));
-    *reinterpret_cast<uint4*>(Vs + r * KP + c * 8) = __ldg(reinterpret_cast<const uint4*>(vb + r * HD + c * 8));
+    attn_cp16(ks + uint32_t(r * KP + c * 8) * 2, kb + r * HD + c * 8);
+    attn_cp16(vs + uint32_t(r * KP + c * 8) * 2, vb + r * HD + c * 8);
   }
-  for (int i = tid; i < G * HD; i += blockDim.x) qs[i] = q[int64_t(g) * G * HD + i];
+  for (int i = tid; i < G * HD / 4; i += blockDim.x) attn_cp16(qss + i * 16, q + int64_t(g) * G * HD + i * 4);
+  attn_cp_wait_all();
   __syncthreads();
   for (int i = tid; i < G * C; i += blockDim.x) {
     const int h = i / C, c = i % C;
@@ -125,23 +138,53 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const float* __restrict__
 }
 
 // Merges the chunks of query head j: M = max m_c, L = sum l_c e^(m_c - M),
-// o = sum o_c e^(m_c - M) / L.
-__global__ void k_attn_combine(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
-                               const int32_t* __restrict__ d_pos, int n_chunks, int hd, float* __restrict__ out) {
-  const int j = blockIdx.x;
+// o = sum o_c e^(m_c - M) / L.  The four warps split the chunks (each lane
+// holds HD/32 dimensions, read as one vector) and all of a warp's chunk loads
+// are issued together; the warps' sums meet in shared memory.
+template <int HD>
+__global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ part_o,
+                                                      const float2* __restrict__ part_ml,
+                                                      const int32_t* __restrict__ d_pos, int n_chunks,
+                                                      float* __restrict__ out) {
+  constexpr int V = HD / 32;            // dims per lane
+  __shared__ float s_o[4][HD];
+  __shared__ float s_l[4], s_m[4];
+  const int j = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int used = (*d_pos + 1 + kAttnChunk - 1) / kAttnChunk;
+  const float2* ml = part_ml + int64_t(j) * n_chunks;
   float M = -INFINITY;
-  for (int c = 0; c < used; c++) M = fmaxf(M, part_ml[int64_t(j) * n_chunks + c].x);
-  for (int d = threadIdx.x; d < hd; d += blockDim.x) {
-    float L = 0.f, o = 0.f;
-    for (int c = 0; c < used; c++) {
-      const float2 ml = part_ml[int64_t(j) * n_chunks + c];
-      const float w = expf(ml.x - M);
-      L += ml.y * w;
-      o += part_o[(int64_t(j) * n_chunks + c) * hd + d] * w;
+  for (int c = tid; c < used; c += 128) M = fmaxf(M, ml[c].x);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) s_m[warp] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(s_m[0], s_m[1]), fmaxf(s_m[2], s_m[3]));
+  float acc[V], L = 0.f;
+#pragma unroll
+  for (int v = 0; v < V; v++) acc[v] = 0.f;
+#pragma unroll 8
+  for (int c = warp; c < used; c += 4) {
+    const float2 m = ml[c];
+    const float* po = part_o + (int64_t(j) * n_chunks + c) * HD + lane * V;
+    float val[V];
+    if (V == 4) {
+      const float4 t = *reinterpret_cast<const float4*>(po);
+      val[0] = t.x; val[1 % V] = t.y; val[2 % V] = t.z; val[3 % V] = t.w;
+    } else {
+      const float2 t = *reinterpret_cast<const float2*>(po);
+      val[0] = t.x; val[1 % V] = t.y;
     }
-    out[int64_t(j) * hd + d] = o / L;
+    const float w = expf(m.x - M);
+    L += m.y * w;
+#pragma unroll
+    for (int v = 0; v < V; v++) acc[v] += val[v] * w;
   }
+#pragma unroll
+  for (int v = 0; v < V; v++) s_o[warp][lane * V + v] = acc[v];
+  if (lane == 0) s_l[warp] = L;
+  __syncthreads();
+  for (int d = tid; d < HD; d += 128)
+    out[int64_t(j) * HD + d] = (s_o[0][d] + s_o[1][d] + s_o[2][d] + s_o[3][d]) / (s_l[0] + s_l[1] + s_l[2] + s_l[3]);
 }
 
 __device__ __forceinline__ void top2_merge(float b2, int i2, float s2, float& b, int& bi, float& s) {
@@ -387,8 +430,10 @@ static cudaError_t enqueue_layer(nt_model* m, int l, uint8_t* base, Launcher& L,
     });
     if (e) return e;
     e = L.run(NT_KC_ATTN, 0.0, [&] {
-      k_attn_combine<<<unsigned(c.n_heads), unsigned(hd), 0, s>>>(m->part_o, m->part_ml, d_pos(m), m->n_chunks, hd,
-                                                                   m->att);
+      if (hd == 128)
+        k_attn_combine<128><<<unsigned(c.n_heads), 128, 0, s>>>(m->part_o, m->part_ml, d_pos(m), m->n_chunks, m->att);
+      else
+        k_attn_combine<64><<<unsigned(c.n_heads), 128, 0, s>>>(m->part_o, m->part_ml, d_pos(m), m->n_chunks, m->att);
       return cudaGetLastError();
     });
     if (e) return e;

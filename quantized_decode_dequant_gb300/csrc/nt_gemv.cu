@@ -35,8 +35,15 @@ cudaError_t launch_gemv(const GemvArgs& a_in, int epi, cudaStream_t s, bool pdl,
       while (pipe_x_bytes(cols / parts) > 140 * 1024 && (cols / parts) % (2 * align) == 0) parts *= 2;
     const int64_t w = cols / parts;
     const size_t xb = pipe_x_bytes(w);
-    const size_t budget = xb < size_t(kPipeMaxSmem) ? size_t(kPipeMaxSmem) - xb : 0;
-    int S = int(budget / (size_t(kPipeWarps) * R * pipe_row_bytes(fmt)));
+    const size_t ring_stage = size_t(kPipeWarps) * R * pipe_row_bytes(fmt);
+    // ring depth: what fits beside x in half an SM's shared memory (two CTAs per SM),
+    // else what fits in the whole of it
+    size_t budget = xb < size_t(kPipeSmemTarget) ? size_t(kPipeSmemTarget) - xb : 0;
+    int S = int(budget / ring_stage);
+    if (S < 2) {
+      budget = xb < size_t(kPipeMaxSmem) ? size_t(kPipeMaxSmem) - xb : 0;
+      S = int(budget / ring_stage);
+    }
     if (S > 8) S = 8;
     if (S >= 2) {
       for (int p = 0; p < parts; p++) {

@@ -42,6 +42,7 @@ namespace nt {
 
 constexpr int kPipeWarps = 8;                 // 256 threads per CTA
 constexpr int kPipeMaxSmem = 221 * 1024;      // dynamic shared memory a CTA may ask for
+constexpr int kPipeSmemTarget = 110 * 1024;   // per CTA, so two CTAs fit on an SM
 constexpr int kXUnit = 80;                    // staged x per 32 columns: h[32] | l[32] | sx, T0, T1, pad
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -396,6 +397,10 @@ __global__ void __launch_bounds__(kPipeWarps * 32) k_gemv_pipe(const __grid_cons
 #pragma unroll
   for (int r = 0; r < R; r++) acc[r] = 0.f;
 
+  // the next kernel may start its own weight prefetch on SMs this grid frees;
+  // it waits for this grid to finish before it reads anything this grid writes
+  asm volatile("griddepcontrol.launch_dependents;");
+
   int64_t c_grp = g0;
   int c_it = 0, c_slot = 0;
   int nlive = int(nrows - c_grp * R < R ? nrows - c_grp * R : R);
@@ -423,8 +428,6 @@ __global__ void __launch_bounds__(kPipeWarps * 32) k_gemv_pipe(const __grid_cons
     nlive = int(nrows - c_grp * R < R ? nrows - c_grp * R : R);
   }
   cp_wait<0>();
-
-  asm volatile("griddepcontrol.launch_dependents;");
   if (EPI == EPI_LOGITS) cta_top2<kPipeWarps>(a, best, best_i, second);
 }
 
