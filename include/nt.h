@@ -203,9 +203,14 @@ nt_status nt_qtensor_export(const nt_qtensor* t, int64_t row0, int64_t nrows, vo
  * formulas (Q4_K as one fused multiply-add: fma(d*sc, q, -(dmin*m))). */
 nt_status nt_dequant(const nt_qtensor* t, int64_t row0, int64_t nrows, float* dev_out, void* stream);
 
-/* y = W x (hada "cuda/: GEMV-...-Kernel"): dev_x fp32[cols], dev_y fp32[rows],
- * fp32 accumulation of the dequantized products.  Asynchronous on stream.
- * dev_x and dev_y must not overlap and must be 16-byte aligned. */
+/* y = W x (hada "cuda/: GEMV-...-Kernel"): dev_x fp32[cols], dev_y fp32[rows].
+ * Codes are multiplied exactly in integers against x carried as 16-bit fixed
+ * point per 32-column block (error at most 2^-16 of the block's largest |x|);
+ * per-block results are scaled and accumulated in fp32.  Asynchronous on
+ * stream; launched with programmatic dependent launch, so it may start (and
+ * read W) before the previous kernel on the stream ends, but reads x and
+ * writes y only after it.  dev_x and dev_y must not overlap and must be
+ * 16-byte aligned. */
 nt_status nt_gemv_q(const nt_qtensor* t, const float* dev_x, float* dev_y, void* stream);
 
 /* ------------------------------------------------ allocation-free variant -- */

@@ -92,7 +92,9 @@ extern "C" nt_status nt_gemv_q(const nt_qtensor* t, const float* dev_x, float* d
   a.nseg = 1;
   a.x = dev_x;
   a.epi.y = dev_y;
-  cudaError_t e = launch_gemv(a, EPI_STORE, static_cast<cudaStream_t>(stream), false, nullptr);
+  // programmatic dependent launch: the kernel reads only the (never rewritten)
+  // weight codes before waiting for the previous kernel in the stream to finish
+  cudaError_t e = launch_gemv(a, EPI_STORE, static_cast<cudaStream_t>(stream), true, nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "nt_gemv_q");
   return NT_OK;
 }
