@@ -58,19 +58,23 @@ __global__ void k_embed(const QMat e, const int32_t* __restrict__ d_token, float
 // G = n_heads/n_kv_heads query heads that share g against the chunk's keys,
 // chunk-local softmax statistics (max, sum of exp) and the unnormalised
 // exp-weighted sum of the chunk's values.  Keys and values are read once per
-// kv head for the whole query group.
-template <int HD>
+// kv head for the whole query group.  Scores: threads 2c and 2c+1 hold the two
+// halves of key c in registers and score it against every head (q read as
+// broadcast float4s); P V: thread d accumulates dimension d of all G heads,
+// reading four weights of a head at a time.
+template <int HD, int G>
 __global__ void __launch_bounds__(kAttnThreads) k_attn(const float* __restrict__ q, const __half* __restrict__ kc,
                                                        const __half* __restrict__ vc, int max_ctx,
-                                                       const int32_t* __restrict__ d_pos, int G, float scale,
+                                                       const int32_t* __restrict__ d_pos, float scale,
                                                        float* __restrict__ part_o, float2* __restrict__ part_ml,
                                                        int n_chunks) {
   constexpr int C = kAttnChunk, KP = HD + 8;   // padded rows: 16-byte reads of 8 rows hit distinct banks
+  static_assert(C * 2 == kAttnThreads, "two threads per cached position");
   extern __shared__ uint4 smem_u4[];
   __half* Ks = reinterpret_cast<__half*>(smem_u4);
   __half* Vs = Ks + C * KP;
   float* qs = reinterpret_cast<float*>(Vs + C * KP);
-  float* S = qs + G * HD;
+  float* S = qs + G * HD;                      // [G][C]
   const int g = blockIdx.x, chunk = blockIdx.y, tid = threadIdx.x;
   const int n = *d_pos + 1;                    // positions 0..pos are attended (current one stored first)
   const int t0 = chunk * C;
@@ -89,31 +93,41 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const float* __restrict__
   for (int i = tid; i < G * HD / 4; i += blockDim.x) attn_cp16(qss + i * 16, q + int64_t(g) * G * HD + i * 4);
   attn_cp_wait_all();
   __syncthreads();
-  for (int i = tid; i < G * C; i += blockDim.x) {
-    const int h = i / C, c = i % C;
-    float s = -INFINITY;
-    if (c < cnt) {
-      const __half* kr = Ks + c * KP;
-      const float* qh = qs + h * HD;
-      float acc = 0.f;
-#pragma unroll 4
-      for (int d = 0; d < HD; d += 8) {
-        const uint4 kv = *reinterpret_cast<const uint4*>(kr + d);
-        const __half2* k2 = reinterpret_cast<const __half2*>(&kv);
+
+  // ---- scores ---------------------------------------------------------------
+  {
+    constexpr int HH = HD / 2;                 // dims per thread
+    const int c = tid >> 1, half = tid & 1;
+    float2 kf[HH / 2];
+    const uint4* kr = reinterpret_cast<const uint4*>(Ks + c * KP + half * HH);
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-          const float2 f = __half22float2(k2[j]);
-          acc = fmaf(qh[d + 2 * j], f.x, acc);
-          acc = fmaf(qh[d + 2 * j + 1], f.y, acc);
-        }
-      }
-      s = acc * scale;
+    for (int i = 0; i < HH / 8; i++) {
+      const uint4 v = kr[i];
+      const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+      for (int j = 0; j < 4; j++) kf[i * 4 + j] = __half22float2(h2[j]);
     }
-    S[i] = s;
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+      const float4* qh = reinterpret_cast<const float4*>(qs + h * HD + half * HH);
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < HH / 4; i++) {
+        const float4 qv = qh[i];
+        acc = fmaf(qv.x, kf[2 * i].x, acc);
+        acc = fmaf(qv.y, kf[2 * i].y, acc);
+        acc = fmaf(qv.z, kf[2 * i + 1].x, acc);
+        acc = fmaf(qv.w, kf[2 * i + 1].y, acc);
+      }
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      if (half == 0) S[h * C + c] = c < cnt ? acc * scale : -INFINITY;
+    }
   }
   __syncthreads();
+
+  // ---- chunk softmax statistics (max, sum of exp), weights in place ---------
   const int warp = tid >> 5, lane = tid & 31;
-  for (int h = warp; h < G; h += blockDim.x / 32) {
+  for (int h = warp; h < G; h += kAttnThreads / 32) {
     float mx = -INFINITY;
     for (int c = lane; c < C; c += 32) mx = fmaxf(mx, S[h * C + c]);
 #pragma unroll
@@ -129,11 +143,25 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const float* __restrict__
     if (lane == 0) part_ml[int64_t(g * G + h) * n_chunks + chunk] = make_float2(mx, l);
   }
   __syncthreads();
-  for (int i = tid; i < G * HD; i += blockDim.x) {
-    const int h = i / HD, d = i % HD;
-    float acc = 0.f;
-    for (int c = 0; c < cnt; c++) acc = fmaf(S[h * C + c], __half2float(Vs[c * KP + d]), acc);
-    part_o[(int64_t(g * G + h) * n_chunks + chunk) * HD + d] = acc;
+
+  // ---- P V --------------------------------------------------------------------
+  if (tid < HD) {
+    const int d = tid;
+    float acc[G];
+#pragma unroll
+    for (int h = 0; h < G; h++) acc[h] = 0.f;
+    for (int c = 0; c < cnt; c += 4) {        // weights past cnt are 0; rows past cnt are finite smem
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; j++) v[j] = c + j < cnt ? __half2float(Vs[(c + j) * KP + d]) : 0.f;
+#pragma unroll
+      for (int h = 0; h < G; h++) {
+        const float4 w = *reinterpret_cast<const float4*>(S + h * C + c);
+        acc[h] = fmaf(w.x, v[0], fmaf(w.y, v[1], fmaf(w.z, v[2], fmaf(w.w, v[3], acc[h]))));
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < G; h++) part_o[(int64_t(g * G + h) * n_chunks + chunk) * HD + d] = acc[h];
   }
 }
 
@@ -371,6 +399,39 @@ struct Launcher {
   }
 };
 
+template <int HD, int G>
+static cudaError_t launch_attn_t(dim3 grid, size_t smem, cudaStream_t s, const float* q, const __half* kc,
+                                 const __half* vc, int max_ctx, const int32_t* pos, float scale, float* po,
+                                 float2* pml, int n_chunks) {
+  auto kern = k_attn<HD, G>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<grid, kAttnThreads, smem, s>>>(q, kc, vc, max_ctx, pos, scale, po, pml, n_chunks);
+  return cudaGetLastError();
+}
+
+static cudaError_t launch_attn(int hd, int G, dim3 grid, size_t smem, cudaStream_t s, const float* q,
+                               const __half* kc, const __half* vc, int max_ctx, const int32_t* pos, float scale,
+                               float* po, float2* pml, int n_chunks) {
+#define NT_ATTN_G(HD)                                                                                    \
+  switch (G) {                                                                                           \
+    case 1: return launch_attn_t<HD, 1>(grid, smem, s, q, kc, vc, max_ctx, pos, scale, po, pml, n_chunks);   \
+    case 2: return launch_attn_t<HD, 2>(grid, smem, s, q, kc, vc, max_ctx, pos, scale, po, pml, n_chunks);   \
+    case 4: return launch_attn_t<HD, 4>(grid, smem, s, q, kc, vc, max_ctx, pos, scale, po, pml, n_chunks);   \
+    case 8: return launch_attn_t<HD, 8>(grid, smem, s, q, kc, vc, max_ctx, pos, scale, po, pml, n_chunks);   \
+    case 16: return launch_attn_t<HD, 16>(grid, smem, s, q, kc, vc, max_ctx, pos, scale, po, pml, n_chunks); \
+  }
+  if (hd == 128) {
+    NT_ATTN_G(128)
+  } else {
+    NT_ATTN_G(64)
+  }
+#undef NT_ATTN_G
+  return cudaErrorInvalidValue;
+}
+
 static cudaError_t enqueue_layer(nt_model* m, int l, uint8_t* base, Launcher& L, bool pdl) {
   const nt_config& c = m->c;
   const Layer& ly = m->layers[size_t(l)];
@@ -420,13 +481,8 @@ static cudaError_t enqueue_layer(nt_model* m, int l, uint8_t* base, Launcher& L,
     const float scale = 1.0f / sqrtf(float(hd));
     dim3 grid(unsigned(c.n_kv_heads), unsigned(m->n_chunks));
     e = L.run(NT_KC_ATTN, by, [&] {
-      if (hd == 128)
-        k_attn<128><<<grid, kAttnThreads, smem, s>>>(m->q, k_cache(m, l), v_cache(m, l), c.max_ctx, d_pos(m), G,
-                                                     scale, m->part_o, m->part_ml, m->n_chunks);
-      else
-        k_attn<64><<<grid, kAttnThreads, smem, s>>>(m->q, k_cache(m, l), v_cache(m, l), c.max_ctx, d_pos(m), G,
-                                                    scale, m->part_o, m->part_ml, m->n_chunks);
-      return cudaGetLastError();
+      return launch_attn(hd, G, grid, smem, s, m->q, k_cache(m, l), v_cache(m, l), c.max_ctx, d_pos(m), scale,
+                         m->part_o, m->part_ml, m->n_chunks);
     });
     if (e) return e;
     e = L.run(NT_KC_ATTN, 0.0, [&] {
@@ -620,7 +676,11 @@ static nt_status validate(const nt_config* c) {
     return fail(NT_E_INVAL, "nt_model_create: sizes must be positive");
   if (c->n_heads % c->n_kv_heads) return fail(NT_E_INVAL, "nt_model_create: n_heads must be a multiple of n_kv_heads");
   if (c->head_dim != 64 && c->head_dim != 128) return fail(NT_E_UNSUPPORTED, "nt_model_create: head_dim must be 64 or 128");
-  if (c->n_heads / c->n_kv_heads > 16) return fail(NT_E_UNSUPPORTED, "nt_model_create: more than 16 query heads per kv head");
+  {
+    const int G = c->n_heads / c->n_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
+      return fail(NT_E_UNSUPPORTED, "nt_model_create: query heads per kv head must be 1, 2, 4, 8 or 16");
+  }
   const nt_qtype ts[9] = {c->t_embd, c->t_q, c->t_k, c->t_v, c->t_o, c->t_gate, c->t_up, c->t_down, c->t_out};
   for (nt_qtype t : ts) {
     if (t == NT_F32 || t == NT_F16) return fail(NT_E_UNSUPPORTED, "nt_model_create: F32/F16 weights are not implemented");

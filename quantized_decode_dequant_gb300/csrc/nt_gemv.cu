@@ -26,7 +26,7 @@ cudaError_t launch_gemv(const GemvArgs& a_in, int epi, cudaStream_t s, bool pdl,
   if (a.max_grid <= 0 || a.max_grid > kMaxGemvGrid) a.max_grid = kMaxGemvGrid;
   const int fmt = a.seg[0].type;
   const int64_t nrows = gemv_logical_rows(a);
-  const int R = nrows >= 16384 ? 4 : 2;
+  int R = nrows >= 16384 ? 4 : 2;
   const int64_t align = 1024;   // whole 32-unit tiles for the pipeline
   static const bool force_register_path = getenv("NT_GEMV_REGISTER_PATH") != nullptr;
   if (cols % align == 0 && !force_register_path) {
@@ -35,6 +35,11 @@ cudaError_t launch_gemv(const GemvArgs& a_in, int epi, cudaStream_t s, bool pdl,
       while (pipe_x_bytes(cols / parts) > 140 * 1024 && (cols / parts) % (2 * align) == 0) parts *= 2;
     const int64_t w = cols / parts;
     const size_t xb = pipe_x_bytes(w);
+    // four rows per warp share each x read, but only if the ring still holds at least
+    // four stages (three tiles in flight) in half an SM's shared memory
+    if (R == 4 && xb < size_t(kPipeSmemTarget) &&
+        (size_t(kPipeSmemTarget) - xb) / (size_t(kPipeWarps) * 4 * pipe_row_bytes(fmt)) < 4)
+      R = 2;
     const size_t ring_stage = size_t(kPipeWarps) * R * pipe_row_bytes(fmt);
     // ring depth: what fits beside x in half an SM's shared memory (two CTAs per SM),
     // else what fits in the whole of it

@@ -59,19 +59,6 @@ template <int N>
 __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-// wait_group takes an immediate; the ring depth is at most 8 (so n <= 6)
-__device__ __forceinline__ void cp_wait_dyn(int n) {
-  switch (n) {
-    case 0: cp_wait<0>(); break;
-    case 1: cp_wait<1>(); break;
-    case 2: cp_wait<2>(); break;
-    case 3: cp_wait<3>(); break;
-    case 4: cp_wait<4>(); break;
-    case 5: cp_wait<5>(); break;
-    default: cp_wait<6>(); break;
-  }
-}
-
 // One staged x block in registers.
 struct XBlock {
   int h[8], l[8];   // int8 halves, four per word, in the format's element order
@@ -120,16 +107,15 @@ template <int FMT> struct Pipe;
 template <> struct Pipe<NT_Q8_0> {
   static constexpr int CB = 32, RB = 32 * 32 + 64;
   __device__ static int xbyte(int c) { return c; }   // natural order
-  // e0: flat index of the tile's first element in this row; the lane copies its unit's codes
-  __device__ static void issue_codes(const QMat& m, int64_t e0, int lane, uint32_t dst) {
-    const uint8_t* src = m.q + e0 + lane * 32;
-    cp16(dst, src);
-    cp16(dst + 16, src + 16);
-  }
-  static constexpr int NP = 4;   // 16-byte pieces of scales per row of a tile
-  __device__ static const void* aux_src(const QMat& m, int64_t e0, int i, int& off) {
+  // copy plan per row: code bytes per tile, then scale pieces (source, smem offset, bytes per tile, size)
+  static constexpr int CODE_STRIDE = 1024, NPT = 4;
+  __device__ static const uint8_t* code_base(const QMat& m, int64_t e_row) { return m.q + e_row; }
+  __device__ static void piece(const QMat& m, int64_t e_row, int i, const uint8_t*& src, int& off, int& stride,
+                               int& size) {
+    src = reinterpret_cast<const uint8_t*>(m.d + (e_row >> 5)) + i * 16;
     off = 1024 + i * 16;
-    return reinterpret_cast<const uint8_t*>(m.d + (e0 >> 5)) + i * 16;
+    stride = 64;
+    size = 16;
   }
   __device__ static float dot(const uint8_t* blk, int lane, const XBlock& x) {
     const uint4 c0 = *reinterpret_cast<const uint4*>(blk + lane * 32);
@@ -145,13 +131,14 @@ __device__ __forceinline__ int nibble_xbyte(int c) { return (c & ~7) + ((c & 1) 
 template <> struct Pipe<NT_Q4_0> {
   static constexpr int CB = 16, RB = 32 * 16 + 64;
   __device__ static int xbyte(int c) { return nibble_xbyte(c); }
-  __device__ static void issue_codes(const QMat& m, int64_t e0, int lane, uint32_t dst) {
-    cp16(dst, m.q + (e0 >> 1) + lane * 16);
-  }
-  static constexpr int NP = 4;
-  __device__ static const void* aux_src(const QMat& m, int64_t e0, int i, int& off) {
+  static constexpr int CODE_STRIDE = 512, NPT = 4;
+  __device__ static const uint8_t* code_base(const QMat& m, int64_t e_row) { return m.q + (e_row >> 1); }
+  __device__ static void piece(const QMat& m, int64_t e_row, int i, const uint8_t*& src, int& off, int& stride,
+                               int& size) {
+    src = reinterpret_cast<const uint8_t*>(m.d + (e_row >> 5)) + i * 16;
     off = 512 + i * 16;
-    return reinterpret_cast<const uint8_t*>(m.d + (e0 >> 5)) + i * 16;
+    stride = 64;
+    size = 16;
   }
   __device__ static float dot(const uint8_t* blk, int lane, const XBlock& x) {
     int c[8];
@@ -164,13 +151,14 @@ template <> struct Pipe<NT_Q4_0> {
 template <> struct Pipe<NT_Q4_K> {
   static constexpr int CB = 16, RB = 32 * 16 + 64;
   __device__ static int xbyte(int c) { return nibble_xbyte(c); }
-  __device__ static void issue_codes(const QMat& m, int64_t e0, int lane, uint32_t dst) {
-    cp16(dst, m.q + (e0 >> 1) + lane * 16);
-  }
-  static constexpr int NP = 4;
-  __device__ static const void* aux_src(const QMat& m, int64_t e0, int i, int& off) {
+  static constexpr int CODE_STRIDE = 512, NPT = 4;
+  __device__ static const uint8_t* code_base(const QMat& m, int64_t e_row) { return m.q + (e_row >> 1); }
+  __device__ static void piece(const QMat& m, int64_t e_row, int i, const uint8_t*& src, int& off, int& stride,
+                               int& size) {
+    src = m.meta + (e_row >> 8) * 16 + i * 16;
     off = 512 + i * 16;
-    return m.meta + ((e0 >> 8) + i) * 16;
+    stride = 64;
+    size = 16;
   }
   __device__ static float dot(const uint8_t* blk, int lane, const XBlock& x) {
     int c[8];
@@ -192,18 +180,27 @@ template <> struct Pipe<NT_Q4_K> {
 template <> struct Pipe<NT_Q6_K> {
   static constexpr int CB = 16, RB = 32 * 16 + 256 + 64 + 16;
   __device__ static int xbyte(int c) { return nibble_xbyte(c); }
-  __device__ static void issue_codes(const QMat& m, int64_t e0, int lane, uint32_t dst) {
-    cp16(dst, m.q + (e0 >> 1) + lane * 16);
-  }
-  // 16 pieces of high-bit words (16 B = 2 units), then 4 of sub-block scales (16 B = 8 units)
-  static constexpr int NP = 20;
-  __device__ static const void* aux_src(const QMat& m, int64_t e0, int i, int& off) {
+  // 16 pieces of high-bit words, 4 of sub-block scales, 2 four-byte pieces of d
+  static constexpr int CODE_STRIDE = 512, NPT = 22;
+  __device__ static const uint8_t* code_base(const QMat& m, int64_t e_row) { return m.q + (e_row >> 1); }
+  __device__ static void piece(const QMat& m, int64_t e_row, int i, const uint8_t*& src, int& off, int& stride,
+                               int& size) {
     if (i < 16) {
+      src = m.qh + (e_row >> 2) + i * 16;
       off = 512 + i * 16;
-      return m.qh + (e0 >> 2) + i * 16;
+      stride = 256;
+      size = 16;
+    } else if (i < 20) {
+      src = m.meta + (e_row >> 4) + (i - 16) * 16;
+      off = 768 + (i - 16) * 16;
+      stride = 64;
+      size = 16;
+    } else {
+      src = reinterpret_cast<const uint8_t*>(m.d + (e_row >> 8)) + (i - 20) * 4;
+      off = 832 + (i - 20) * 4;
+      stride = 8;
+      size = 4;
     }
-    off = 768 + (i - 16) * 16;
-    return m.meta + (e0 >> 4) + (i - 16) * 16;
   }
   __device__ static float dot(const uint8_t* blk, int lane, const XBlock& x) {
     const uint4 w = *reinterpret_cast<const uint4*>(blk + lane * 16);
@@ -225,45 +222,60 @@ template <> struct Pipe<NT_Q6_K> {
   }
 };
 
-// Rows of one group as seen by the copy issuer (R is small; indexed with constants or selects).
-template <int R>
-struct GroupRows {
-  int seg[R];
-  int64_t e[R];
-  int nlive;   // rows [0, nlive) of the group exist
+// This lane's share of the copies of one row group, set up once per group:
+// its code vector of each row, and up to NA scale pieces.  Tile it of the
+// group then copies from (source + it * stride).
+template <int FMT, int R>
+struct GroupCopies {
+  static constexpr int NA = (R * Pipe<FMT>::NPT + 31) / 32;
+  const uint8_t* code[R];
+  const uint8_t* src[NA];
+  int off[NA], stride[NA], size[NA];
+  int nlive;
 };
 
-template <int R>
-__device__ __forceinline__ void rows_setup(const GemvArgs& a, int64_t grp, int64_t nrows, GroupRows<R>& g) {
+template <int FMT, int R>
+__device__ __forceinline__ void group_copies(const GemvArgs& a, int64_t grp, int64_t nrows, int lane,
+                                             GroupCopies<FMT, R>& g) {
+  using P = Pipe<FMT>;
   g.nlive = int(nrows - grp * R < R ? nrows - grp * R : R);
+  int seg[R];
+  int64_t e[R];
 #pragma unroll
   for (int r = 0; r < R; r++) {
-    int s = 0;
+    int sg = 0;
     int64_t lr = 0;
-    if (r < g.nlive) map_row(a, grp * R + r, s, lr);
-    g.seg[r] = s;
-    g.e[r] = lr * a.seg[0].cols + a.col0;
+    if (r < g.nlive) map_row(a, grp * R + r, sg, lr);
+    seg[r] = sg;
+    e[r] = lr * a.seg[0].cols + a.col0;
+    g.code[r] = P::code_base(a.seg[sg], e[r]) + lane * P::CB;
+  }
+#pragma unroll
+  for (int k = 0; k < GroupCopies<FMT, R>::NA; k++) {
+    const int p = lane + 32 * k;
+    const int r = p / P::NPT, i = p - (p / P::NPT) * P::NPT;
+    g.size[k] = 0;
+    g.src[k] = nullptr;
+    g.off[k] = 0;
+    g.stride[k] = 0;
+    if (p < R * P::NPT && r < g.nlive) {
+      int sg = seg[0];
+      int64_t er = e[0];
+#pragma unroll
+      for (int rr = 1; rr < R; rr++)
+        if (r == rr) {
+          sg = seg[rr];
+          er = e[rr];
+        }
+      P::piece(a.seg[sg], er, i, g.src[k], g.off[k], g.stride[k], g.size[k]);
+      g.off[k] += r * P::RB;
+    }
   }
 }
 
-template <int R>
-__device__ __forceinline__ int64_t pick(const int64_t (&v)[R], int r) {
-  int64_t out = v[0];
-#pragma unroll
-  for (int i = 1; i < R; i++) out = r == i ? v[i] : out;
-  return out;
-}
-template <int R>
-__device__ __forceinline__ int pick(const int (&v)[R], int r) {
-  int out = v[0];
-#pragma unroll
-  for (int i = 1; i < R; i++) out = r == i ? v[i] : out;
-  return out;
-}
-
-template <int FMT, int R, int EPI>
+template <int FMT, int R, int S, int EPI>
 __global__ void __launch_bounds__(kPipeWarps * 32) k_gemv_pipe(const __grid_constant__ GemvArgs a,
-                                                              const int64_t nrows, const int S) {
+                                                              const int64_t nrows) {
   using P = Pipe<FMT>;
   constexpr int nw = kPipeWarps;
   extern __shared__ float4 smem4[];
@@ -288,32 +300,22 @@ __global__ void __launch_bounds__(kPipeWarps * 32) k_gemv_pipe(const __grid_cons
   // copy issuer: runs S-1 tiles ahead of the decoder, with its own cursor
   int64_t i_grp = g0, i_left = ntiles;
   int i_it = 0, i_slot = 0;
-  GroupRows<R> ig;
+  GroupCopies<FMT, R> gc;
   auto issue_next = [&]() {
     if (i_left > 0) {
-      if (i_it == 0) rows_setup<R>(a, i_grp, nrows, ig);
+      if (i_it == 0) group_copies<FMT, R>(a, i_grp, nrows, lane, gc);
       const uint32_t dst = wring_s + uint32_t(i_slot * R * P::RB);
-      const int64_t toff = int64_t(i_it) * 1024;          // first element of the tile in the row window
+      const int64_t ct = int64_t(i_it) * P::CODE_STRIDE;
 #pragma unroll
       for (int r = 0; r < R; r++)
-        if (r < ig.nlive) P::issue_codes(a.seg[ig.seg[r]], ig.e[r] + toff, lane, dst + r * P::RB + lane * P::CB);
+        if (r < gc.nlive) {
+          cp16(dst + r * P::RB + lane * P::CB, gc.code[r] + ct);
+          if (P::CB == 32) cp16(dst + r * P::RB + lane * P::CB + 16, gc.code[r] + ct + 16);
+        }
 #pragma unroll
-      for (int p0 = 0; p0 < R * P::NP; p0 += 32) {
-        const int p = p0 + lane;
-        const int r = p / P::NP, i = p % P::NP;
-        if (p < R * P::NP && r < ig.nlive) {
-          int off;
-          const void* src = P::aux_src(a.seg[pick<R>(ig.seg, r)], pick<R>(ig.e, r) + toff, i, off);
-          cp16(dst + r * P::RB + off, src);
-        }
-      }
-      if (FMT == NT_Q6_K) {   // f16 d per 256 columns: two 4-byte pieces per row
-        const int r = lane >> 1, i = lane & 1;
-        if (lane < 2 * R && r < ig.nlive) {
-          const int64_t e0 = pick<R>(ig.e, r) + toff;
-          cp4(dst + r * P::RB + 832 + i * 4,
-              reinterpret_cast<const uint8_t*>(a.seg[pick<R>(ig.seg, r)].d + (e0 >> 8)) + i * 4);
-        }
+      for (int k = 0; k < GroupCopies<FMT, R>::NA; k++) {
+        if (gc.size[k] == 16) cp16(dst + gc.off[k], gc.src[k] + int64_t(i_it) * gc.stride[k]);
+        else if (gc.size[k] == 4) cp4(dst + gc.off[k], gc.src[k] + int64_t(i_it) * gc.stride[k]);
       }
       --i_left;
       if (++i_slot == S) i_slot = 0;
@@ -326,6 +328,7 @@ __global__ void __launch_bounds__(kPipeWarps * 32) k_gemv_pipe(const __grid_cons
   };
 
   // prologue: the first S-1 tiles before waiting for the producer of x
+#pragma unroll
   for (int t = 0; t < S - 1; t++) issue_next();
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(kPipeWarps * 32) k_gemv_pipe(const __grid_cons
   int c_it = 0, c_slot = 0;
   int nlive = int(nrows - c_grp * R < R ? nrows - c_grp * R : R);
   for (int64_t t = 0; t < ntiles; t++) {
-    cp_wait_dyn(S - 2);   // this lane's copies of the tile have landed
+    cp_wait<S - 2>();     // this lane's copies of the tile have landed
     __syncwarp();         // ... and every lane's (scales are copied by a few lanes); the previous slot is free
     issue_next();
     XBlock xb;
@@ -441,12 +444,12 @@ inline int pipe_row_bytes(int fmt) {
   }
 }
 
-template <int FMT, int R, int EPI>
-cudaError_t launch_gemv_pipe_t(const GemvArgs& a, int S, cudaStream_t s, bool pdl, int* grid_used) {
+template <int FMT, int R, int S, int EPI>
+cudaError_t launch_gemv_pipe_t(const GemvArgs& a, cudaStream_t s, bool pdl, int* grid_used) {
   const int64_t nrows = gemv_logical_rows(a);
   const size_t smem = pipe_x_bytes(a.ncols) + size_t(kPipeWarps) * S * R * Pipe<FMT>::RB;
   if (smem > size_t(kPipeMaxSmem)) return cudaErrorInvalidValue;
-  auto kern = k_gemv_pipe<FMT, R, EPI>;
+  auto kern = k_gemv_pipe<FMT, R, S, EPI>;
   static int s_sms = 0;
   static size_t s_occ_smem = ~size_t(0);
   static int s_occ = 0;
@@ -478,27 +481,33 @@ cudaError_t launch_gemv_pipe_t(const GemvArgs& a, int S, cudaStream_t s, bool pd
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, a, nrows, S);
+  return cudaLaunchKernelEx(&cfg, kern, a, nrows);
 }
 
+template <int FMT, int R, int S>
+cudaError_t launch_gemv_pipe_rs(const GemvArgs& a, int epi, cudaStream_t s, bool pdl, int* grid_used) {
+  switch (epi) {
+    case EPI_STORE: return launch_gemv_pipe_t<FMT, R, S, EPI_STORE>(a, s, pdl, grid_used);
+    case EPI_ADD: return launch_gemv_pipe_t<FMT, R, S, EPI_ADD>(a, s, pdl, grid_used);
+    case EPI_QKV: return launch_gemv_pipe_t<FMT, R, S, EPI_QKV>(a, s, pdl, grid_used);
+    case EPI_SWIGLU: return launch_gemv_pipe_t<FMT, R, S, EPI_SWIGLU>(a, s, pdl, grid_used);
+    case EPI_LOGITS: return launch_gemv_pipe_t<FMT, R, S, EPI_LOGITS>(a, s, pdl, grid_used);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// S is rounded down to 2, 4 or 8 ring stages
 template <int FMT>
 cudaError_t launch_gemv_pipe_fmt(const GemvArgs& a, int epi, int R, int S, cudaStream_t s, bool pdl,
                                  int* grid_used) {
-#define NT_EPI_CASES(RR)                                                                       \
-  switch (epi) {                                                                               \
-    case EPI_STORE: return launch_gemv_pipe_t<FMT, RR, EPI_STORE>(a, S, s, pdl, grid_used);    \
-    case EPI_ADD: return launch_gemv_pipe_t<FMT, RR, EPI_ADD>(a, S, s, pdl, grid_used);        \
-    case EPI_QKV: return launch_gemv_pipe_t<FMT, RR, EPI_QKV>(a, S, s, pdl, grid_used);        \
-    case EPI_SWIGLU: return launch_gemv_pipe_t<FMT, RR, EPI_SWIGLU>(a, S, s, pdl, grid_used);  \
-    case EPI_LOGITS: return launch_gemv_pipe_t<FMT, RR, EPI_LOGITS>(a, S, s, pdl, grid_used);  \
-  }
   if (R == 4) {
-    NT_EPI_CASES(4)
-  } else {
-    NT_EPI_CASES(2)
+    if (S >= 8) return launch_gemv_pipe_rs<FMT, 4, 8>(a, epi, s, pdl, grid_used);
+    if (S >= 4) return launch_gemv_pipe_rs<FMT, 4, 4>(a, epi, s, pdl, grid_used);
+    return launch_gemv_pipe_rs<FMT, 4, 2>(a, epi, s, pdl, grid_used);
   }
-#undef NT_EPI_CASES
-  return cudaErrorInvalidValue;
+  if (S >= 8) return launch_gemv_pipe_rs<FMT, 2, 8>(a, epi, s, pdl, grid_used);
+  if (S >= 4) return launch_gemv_pipe_rs<FMT, 2, 4>(a, epi, s, pdl, grid_used);
+  return launch_gemv_pipe_rs<FMT, 2, 2>(a, epi, s, pdl, grid_used);
 }
 
 #define NT_DECLARE_GEMV_PIPE(NAME) \
