@@ -178,21 +178,24 @@ def job_throughput(units_per_rank: int, world: int, max_seconds: float) -> float
 
 # ------------------------------------------------------------ CPU baseline --
 
-def cpu_baseline(wl, sample_steps: int = 2, threads: int | None = None) -> dict:
+def cpu_baseline(wl, min_seconds: float = 10.0, max_steps: int = 64, threads: int | None = None) -> dict:
     """The oracle on the host cores, on a sample of the workload: the same
-    architecture truncated to one layer, decoded from the same prefilled context;
-    its per-token time is scaled to the full model by weight + KV bytes."""
+    architecture truncated to one layer, decoded from the same prefilled context
+    for about `min_seconds` (at least 2 steps, at most `max_steps`); its
+    per-token time is scaled to the full model by weight + KV bytes."""
     import oracle
     from quantized_decode_dequant_gb300 import workloads as W
     spec = dict(wl["spec"])
     threads = threads or os.cpu_count() or 1
-    sample = dict(spec, n_layers=1, max_ctx=wl["ctx"] + sample_steps + 1)
+    sample = dict(spec, n_layers=1, max_ctx=wl["ctx"] + max_steps + 1)
     m = oracle.Model(oracle.ModelSpec(**sample, seed=W.SEED_WEIGHTS), nthreads=threads)
     m.kv_prefill(wl["ctx"], W.SEED_KV)
     tok = oracle.token(W.SEED_PROMPT, oracle.UID_TOKENS, 0, spec["vocab"])
     t0 = time.perf_counter()
-    for _ in range(sample_steps):
+    sample_steps = 0
+    while sample_steps < max_steps and (sample_steps < 2 or time.perf_counter() - t0 < min_seconds):
         _, tok, _ = m.decode_step(tok)
+        sample_steps += 1
     dt = (time.perf_counter() - t0) / sample_steps
     m.close()
     full = W.weight_bytes(spec) + W.kv_bytes(spec, wl["ctx"])
