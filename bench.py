@@ -49,6 +49,8 @@ def parse_args(argv=None):
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--profile-gemv", nargs=4, metavar=("FMT", "ROWS", "COLS", "LAUNCHES"))
+    p.add_argument("--layers", type=int, default=None,
+                   help="profiling aid: the workload's shapes with this many layers (not a bench line)")
     return p.parse_args(argv)
 
 
@@ -238,6 +240,20 @@ def run_reference(args, wl, rank, world, dist):
     print(json.dumps(line), flush=True)
 
 
+def per_kernel_launches(spec) -> int:
+    """Kernels of one step on the per-kernel launch path: embedding, per layer the
+    QKV GEMV (two when v has its own format), attention, O, gate/up and down
+    GEMVs, then the output GEMV and the argmax."""
+    split_v = spec.get("t_v", "q8_0") != spec.get("t_q", "q8_0")
+    return 1 + spec["n_layers"] * (5 + int(split_v)) + 2
+
+
+def step_traffic(wl, step_bytes):
+    """DRAM bytes of one step-kernel launch from the committed ncu capture of the
+    same workload, or None when none is recorded for it."""
+    return None
+
+
 # ------------------------------------------------------------------ GEMV --
 
 def gemv_sweep(nt, torch, peak_gbs: float, l2_bytes: int) -> list[dict]:
@@ -387,30 +403,47 @@ def run_ours(args, wl, rank, world, local, dist):
         e2e = {"value": job_throughput(args.steps, world, e2e_sec), "unit": "tok/s",
                "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 8}
 
-        # ---- per-kernel-class device times (event pair around every launch)
+        # ---- per-class device times: event pairs around every launch, or the
+        # step kernel's per-phase clock stamps (one launch per step)
         roofline = None
         kt = None
         kernel_classes = None
+        stats = nt.nt_get_stats(m)
+        step_bytes = stats.weight_bytes + stats.kv_bytes_per_pos * (wl["ctx"] + args.steps / 2)
         if not streamed:
             reset()
             n_prof = max(4, min(args.steps, 32))
             kt = nt.nt_profile_steps(m, tok0, n_prof)
-            g_ms = kt.ms[nt.KC_GEMV] / kt.launches[nt.KC_GEMV]
-            g_bytes = kt.bytes[nt.KC_GEMV] / kt.launches[nt.KC_GEMV]
-            achieved = g_bytes / (g_ms * 1e-3) / 1e9
-            roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                        "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
-                        "kernel": "k_gemv (fused dequant-GEMV, all launches of a step)",
-                        "peak_source": peaks["source"],
-                        "bytes_per_launch": round(g_bytes), "launches_per_step": kt.launches[nt.KC_GEMV] // n_prof,
-                        "us_per_launch": round(g_ms * 1e3, 3)}
-            kernel_classes = {name: {"launches_per_step": kt.launches[c] // n_prof,
-                                     "ms_per_step": round(kt.ms[c] / n_prof, 4)}
+            step_kernel = kt.kernel_launches == n_prof
+            if step_kernel:
+                # the whole step is one kernel: its launch duration is the timed step
+                achieved = step_bytes / (ms_per_step * 1e-3) / 1e9
+                roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                            "traffic": step_traffic(wl, step_bytes),
+                            "kernel": "k_step (persistent decode step: all GEMVs, attention, argmax)",
+                            "peak_source": peaks["source"], "bytes_per_launch": round(step_bytes),
+                            "launches_per_step": 1, "us_per_launch": round(ms_per_step * 1e3, 3),
+                            "timing": "CUDA events around the timed greedy loop on the launching stream"}
+            else:
+                g_ms = kt.ms[nt.KC_GEMV] / kt.launches[nt.KC_GEMV]
+                g_bytes = kt.bytes[nt.KC_GEMV] / kt.launches[nt.KC_GEMV]
+                achieved = g_bytes / (g_ms * 1e-3) / 1e9
+                roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                            "kernel": "k_gemv (fused dequant-GEMV, all launches of a step)",
+                            "peak_source": peaks["source"],
+                            "bytes_per_launch": round(g_bytes), "launches_per_step": kt.launches[nt.KC_GEMV] // n_prof,
+                            "us_per_launch": round(g_ms * 1e3, 3)}
+            unit = "phases_per_step" if step_kernel else "launches_per_step"
+            kernel_classes = {name: {unit: kt.launches[c] // n_prof,
+                                     "ms_per_step": round(kt.ms[c] / n_prof, 4),
+                                     "GB_s": round(kt.bytes[c] / (kt.ms[c] * 1e-3) / 1e9, 1) if kt.ms[c] else None}
                               for name, c in (("gemv", nt.KC_GEMV), ("attention", nt.KC_ATTN),
                                               ("other", nt.KC_OTHER))}
             kernel_classes["profiled_step_ms"] = round(kt.step_ms, 4)
-        stats = nt.nt_get_stats(m)
-        step_bytes = stats.weight_bytes + stats.kv_bytes_per_pos * (wl["ctx"] + args.steps / 2)
+            kernel_classes["source"] = ("step kernel: SM clock of CTA 0 at every grid barrier" if step_kernel
+                                        else "CUDA event pair around every launch")
         step_roofline = {"bytes_per_step": step_bytes,
                          "achieved_GB_s": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
                          "frac": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
@@ -438,7 +471,8 @@ def run_ours(args, wl, rank, world, local, dist):
                        "parallelism": "replicas only" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (weights > 4x L2), no flush"},
             "roofline": roofline, "step_roofline": step_roofline, "kernel_classes": kernel_classes, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": None if kt is None else int(sum(kt.launches) // max(1, n_prof) * args.steps),
+            "gpu_launches": int(kt.kernel_launches // max(1, n_prof) * args.steps) if kt is not None
+            else per_kernel_launches(wl["spec"]) * args.steps,
             "clocks": clocks.summary(), "first_tokens": tokens}
     if h2d_stats:
         line["streaming"] = h2d_stats
@@ -461,6 +495,9 @@ def main(argv=None):
     args = parse_args(argv)
     rank, world, local, dist = dist_setup()
     wl = workload(args.workload)
+    if args.layers is not None:
+        wl = dict(wl, spec=dict(wl["spec"], n_layers=args.layers),
+                  label=wl["label"] + f" (profiling case: {args.layers} layers)", vs=None)
     try:
         if args.impl == "reference":
             run_reference(args, wl, rank, world, dist)

@@ -107,6 +107,7 @@ typedef struct {
   double ms[NT_KC_COUNT];          /* summed event-to-event time of the launches */
   double bytes[NT_KC_COUNT];       /* summed algorithmic bytes of the launches   */
   double step_ms;                  /* mean wall time of a profiled step          */
+  int64_t kernel_launches;         /* kernels launched over the profiled steps   */
 } nt_kernel_times;
 
 /* Message of the last failure on this thread ("" if none).  Never NULL. */
@@ -139,14 +140,22 @@ nt_status nt_kv_prefill(nt_model* m, int32_t n_ctx, uint64_t seed);
  * token: input id in [0, vocab).  next_token (host, required): the argmax.
  * logits_host (nullable): vocab floats.  top2_margin (nullable): top-1 minus
  * top-2 logit.  Synchronous.  Position becomes p+1.
- * NT_E_INVAL: token out of range or p == max_ctx. */
+ * A resident model runs the step as a CUDA graph of per-kernel launches.  With
+ * the environment variable NT_STEP_KERNEL=1, a model whose layers are all
+ * resident, whose GEMV widths are multiples of 1024 and whose format mix, head
+ * size and query group have a persistent step kernel (Q8_0 throughout with 4
+ * query heads per kv head; Q4_K_M with 8) runs the step as that one cooperative
+ * kernel instead; results are bitwise the same.
+ * NT_E_INVAL: token out of range or p == max_ctx.  NT_E_TIMEOUT: a wait of the
+ * step kernel ran past one second (the step is abandoned, the position does not
+ * advance) or the host watchdog expired. */
 nt_status nt_decode_step(nt_model* m, int32_t token, int32_t* next_token, float* logits_host,
                          float* top2_margin);
 
 /* n_steps greedy steps that feed each argmax back as the next input on the
  * device, starting from token; asynchronous on stream (the model's own
  * stream waits for it).  The produced ids are kept on the device
- * (nt_get_tokens).  Layer-streamed models are not supported here
+ * (nt_get_tokens, which reports NT_E_TIMEOUT if a step was abandoned).  Layer-streamed models are not supported here
  * (NT_E_STATE); use nt_decode_step. */
 nt_status nt_decode_run(nt_model* m, int32_t token, int32_t n_steps, void* stream);
 
@@ -170,9 +179,11 @@ nt_status nt_stream_layers(nt_model* m, int32_t n_resident, int32_t n_staging);
 
 nt_status nt_get_stats(const nt_model* m, nt_stats* out);
 
-/* Runs n_steps decode steps (from token, feeding back argmax) with a CUDA
- * event pair around every kernel launch on the model's stream and returns
- * per-class totals.  For measurement only; not graph-captured. */
+/* Runs n_steps decode steps (from token, feeding back argmax) and returns
+ * per-class device times.  Per-kernel launches: a CUDA event pair around every
+ * launch (not graph-captured).  Step kernel: the SM clock of CTA 0 at every
+ * grid barrier, scaled to the event-timed duration of the launch; a "launch"
+ * of a class is then one phase.  For measurement only. */
 nt_status nt_profile_steps(nt_model* m, int32_t token, int32_t n_steps, nt_kernel_times* out);
 
 /* Pointer to a weight tensor of the model (owned by the model).  For a

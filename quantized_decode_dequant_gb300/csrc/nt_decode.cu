@@ -26,25 +26,13 @@
 #include <thread>
 #include <vector>
 
-#include "nt_internal.cuh"
+#include "nt_step.cuh"
 
 namespace nt {
 
-constexpr int kAttnChunk = 64;      // cached positions per attention CTA
-constexpr int kAttnThreads = 128;
 constexpr uint32_t kUidEmbd = 0x100000u, kUidOutput = 0x100001u, kUidKv = 0x200000u;
 
 // ---------------------------------------------------------------- kernels --
-
-__device__ __forceinline__ uint32_t attn_smem(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void attn_cp16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void attn_cp_wait_all() {
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-}
 
 __global__ void k_embed(const QMat e, const int32_t* __restrict__ d_token, float* __restrict__ x) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -54,176 +42,16 @@ __global__ void k_embed(const QMat e, const int32_t* __restrict__ d_token, float
   x[i] = dequant_elem(e, tok * e.cols + i);
 }
 
-// One CTA per (kv head g, chunk of kAttnChunk cached positions): scores of the
-// G = n_heads/n_kv_heads query heads that share g against the chunk's keys,
-// chunk-local softmax statistics (max, sum of exp) and the unnormalised
-// exp-weighted sum of the chunk's values.  Keys and values are read once per
-// kv head for the whole query group.  Scores: threads 2c and 2c+1 hold the two
-// halves of key c in registers and score it against every head (q read as
-// broadcast float4s); P V: thread d accumulates dimension d of all G heads,
-// reading four weights of a head at a time.
+// One CTA (one attention group) per (kv head, chunk); chunks past the current
+// position have nothing to do.
 template <int HD, int G>
-__global__ void __launch_bounds__(kAttnThreads) k_attn(const float* __restrict__ q, const __half* __restrict__ kc,
-                                                       const __half* __restrict__ vc, int max_ctx,
-                                                       const int32_t* __restrict__ d_pos, float scale,
-                                                       float* __restrict__ part_o, float2* __restrict__ part_ml,
-                                                       int n_chunks) {
-  constexpr int C = kAttnChunk, KP = HD + 8;   // padded rows: 16-byte reads of 8 rows hit distinct banks
-  static_assert(C * 2 == kAttnThreads, "two threads per cached position");
+__global__ void __launch_bounds__(kAttnThreads) k_attn(const __grid_constant__ AttnArgs a,
+                                                       const int32_t* __restrict__ d_pos) {
   extern __shared__ uint4 smem_u4[];
-  __half* Ks = reinterpret_cast<__half*>(smem_u4);
-  __half* Vs = Ks + C * KP;
-  float* qs = reinterpret_cast<float*>(Vs + C * KP);
-  float* S = qs + G * HD;                      // [G][C]
-  const int g = blockIdx.x, chunk = blockIdx.y, tid = threadIdx.x;
-  const int n = *d_pos + 1;                    // positions 0..pos are attended (current one stored first)
-  const int t0 = chunk * C;
-  if (t0 >= n) return;
-  const int cnt = min(C, n - t0);
-  const __half* kb = kc + (int64_t(g) * max_ctx + t0) * HD;
-  const __half* vb = vc + (int64_t(g) * max_ctx + t0) * HD;
-  constexpr int VPR = HD / 8;
-  // every copy of the chunk issued before any is waited for: one memory latency
-  const uint32_t ks = attn_smem(Ks), vs = attn_smem(Vs), qss = attn_smem(qs);
-  for (int i = tid; i < cnt * VPR; i += blockDim.x) {
-    const int r = i / VPR, c = i % VPR;
-    attn_cp16(ks + uint32_t(r * KP + c * 8) * 2, kb + r * HD + c * 8);
-    attn_cp16(vs + uint32_t(r * KP + c * 8) * 2, vb + r * HD + c * 8);
-  }
-  for (int i = tid; i < G * HD / 4; i += blockDim.x) attn_cp16(qss + i * 16, q + int64_t(g) * G * HD + i * 4);
-  attn_cp_wait_all();
-  __syncthreads();
-
-  // ---- scores ---------------------------------------------------------------
-  {
-    constexpr int HH = HD / 2;                 // dims per thread
-    const int c = tid >> 1, half = tid & 1;
-    float2 kf[HH / 2];
-    const uint4* kr = reinterpret_cast<const uint4*>(Ks + c * KP + half * HH);
-#pragma unroll
-    for (int i = 0; i < HH / 8; i++) {
-      const uint4 v = kr[i];
-      const __half2* h2 = reinterpret_cast<const __half2*>(&v);
-#pragma unroll
-      for (int j = 0; j < 4; j++) kf[i * 4 + j] = __half22float2(h2[j]);
-    }
-#pragma unroll
-    for (int h = 0; h < G; h++) {
-      const float4* qh = reinterpret_cast<const float4*>(qs + h * HD + half * HH);
-      float acc = 0.f;
-#pragma unroll
-      for (int i = 0; i < HH / 4; i++) {
-        const float4 qv = qh[i];
-        acc = fmaf(qv.x, kf[2 * i].x, acc);
-        acc = fmaf(qv.y, kf[2 * i].y, acc);
-        acc = fmaf(qv.z, kf[2 * i + 1].x, acc);
-        acc = fmaf(qv.w, kf[2 * i + 1].y, acc);
-      }
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      if (half == 0) S[h * C + c] = c < cnt ? acc * scale : -INFINITY;
-    }
-  }
-  __syncthreads();
-
-  // ---- chunk softmax statistics (max, sum of exp), weights in place ---------
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int h = warp; h < G; h += kAttnThreads / 32) {
-    float mx = -INFINITY;
-    for (int c = lane; c < C; c += 32) mx = fmaxf(mx, S[h * C + c]);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float l = 0.f;
-    for (int c = lane; c < C; c += 32) {
-      const float e = c < cnt ? expf(S[h * C + c] - mx) : 0.f;
-      S[h * C + c] = e;
-      l += e;
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    if (lane == 0) part_ml[int64_t(g * G + h) * n_chunks + chunk] = make_float2(mx, l);
-  }
-  __syncthreads();
-
-  // ---- P V --------------------------------------------------------------------
-  if (tid < HD) {
-    const int d = tid;
-    float acc[G];
-#pragma unroll
-    for (int h = 0; h < G; h++) acc[h] = 0.f;
-    for (int c = 0; c < cnt; c += 4) {        // weights past cnt are 0; rows past cnt are finite smem
-      float v[4];
-#pragma unroll
-      for (int j = 0; j < 4; j++) v[j] = c + j < cnt ? __half2float(Vs[(c + j) * KP + d]) : 0.f;
-#pragma unroll
-      for (int h = 0; h < G; h++) {
-        const float4 w = *reinterpret_cast<const float4*>(S + h * C + c);
-        acc[h] = fmaf(w.x, v[0], fmaf(w.y, v[1], fmaf(w.z, v[2], fmaf(w.w, v[3], acc[h]))));
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < G; h++) part_o[(int64_t(g * G + h) * n_chunks + chunk) * HD + d] = acc[h];
-  }
-}
-
-// Merges the chunks of query head j: M = max m_c, L = sum l_c e^(m_c - M),
-// o = sum o_c e^(m_c - M) / L.  The four warps split the chunks (each lane
-// holds HD/32 dimensions, read as one vector) and all of a warp's chunk loads
-// are issued together; the warps' sums meet in shared memory.
-template <int HD>
-__global__ void __launch_bounds__(128) k_attn_combine(const float* __restrict__ part_o,
-                                                      const float2* __restrict__ part_ml,
-                                                      const int32_t* __restrict__ d_pos, int n_chunks,
-                                                      float* __restrict__ out) {
-  constexpr int V = HD / 32;            // dims per lane
-  __shared__ float s_o[4][HD];
-  __shared__ float s_l[4], s_m[4];
-  const int j = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int used = (*d_pos + 1 + kAttnChunk - 1) / kAttnChunk;
-  const float2* ml = part_ml + int64_t(j) * n_chunks;
-  float M = -INFINITY;
-  for (int c = tid; c < used; c += 128) M = fmaxf(M, ml[c].x);
-#pragma unroll
-  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) s_m[warp] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(s_m[0], s_m[1]), fmaxf(s_m[2], s_m[3]));
-  float acc[V], L = 0.f;
-#pragma unroll
-  for (int v = 0; v < V; v++) acc[v] = 0.f;
-#pragma unroll 8
-  for (int c = warp; c < used; c += 4) {
-    const float2 m = ml[c];
-    const float* po = part_o + (int64_t(j) * n_chunks + c) * HD + lane * V;
-    float val[V];
-    if (V == 4) {
-      const float4 t = *reinterpret_cast<const float4*>(po);
-      val[0] = t.x; val[1 % V] = t.y; val[2 % V] = t.z; val[3 % V] = t.w;
-    } else {
-      const float2 t = *reinterpret_cast<const float2*>(po);
-      val[0] = t.x; val[1 % V] = t.y;
-    }
-    const float w = expf(m.x - M);
-    L += m.y * w;
-#pragma unroll
-    for (int v = 0; v < V; v++) acc[v] += val[v] * w;
-  }
-#pragma unroll
-  for (int v = 0; v < V; v++) s_o[warp][lane * V + v] = acc[v];
-  if (lane == 0) s_l[warp] = L;
-  __syncthreads();
-  for (int d = tid; d < HD; d += 128)
-    out[int64_t(j) * HD + d] = (s_o[0][d] + s_o[1][d] + s_o[2][d] + s_o[3][d]) / (s_l[0] + s_l[1] + s_l[2] + s_l[3]);
-}
-
-__device__ __forceinline__ void top2_merge(float b2, int i2, float s2, float& b, int& bi, float& s) {
-  if (i2 == 0x7fffffff) return;
-  if (b2 > b || (b2 == b && i2 < bi)) {
-    s = fmaxf(s2, b);
-    b = b2;
-    bi = i2;
-  } else {
-    s = fmaxf(s, b2);
-  }
+  const int n = __ldcg(d_pos) + 1;
+  const int used = (n + a.chunk - 1) / a.chunk;
+  if (int(blockIdx.y) >= used) return;
+  attn_item<HD, G>(a, blockIdx.x, blockIdx.y, n, used, reinterpret_cast<uint8_t*>(smem_u4), false);
 }
 
 // Greedy choice over the per-CTA top-2 summaries of the output GEMV (ties to the
@@ -313,7 +141,14 @@ struct nt_model {
   float2* part_ml = nullptr;
   float2* rope = nullptr;
   float4* top2 = nullptr;
-  int32_t* small = nullptr;          // pos, token, next, margin(float bits)
+  unsigned* tickets = nullptr;       // attention: finished chunks per kv head
+  unsigned* bar = nullptr;           // step kernel: grid barrier state
+  nt::StepGemv* step_tab = nullptr;  // step kernel: GEMV table (device)
+  nt::StepPlan plan{};
+  nt::StepArgs step{};
+  size_t step_smem = 0;
+  int step_state = 0;                // 0 unknown, 1 ready, -1 not applicable
+  int32_t* small = nullptr;          // pos, token, next, margin(float bits), error word
   int32_t* hist = nullptr;           // produced ids by position
   int32_t* h_io = nullptr;           // pinned host mirror of small
   int n_chunks = 0;
@@ -400,28 +235,25 @@ struct Launcher {
 };
 
 template <int HD, int G>
-static cudaError_t launch_attn_t(dim3 grid, size_t smem, cudaStream_t s, const float* q, const __half* kc,
-                                 const __half* vc, int max_ctx, const int32_t* pos, float scale, float* po,
-                                 float2* pml, int n_chunks) {
+static cudaError_t launch_attn_t(dim3 grid, cudaStream_t s, const AttnArgs& a, const int32_t* pos) {
   auto kern = k_attn<HD, G>;
+  const size_t smem = attn_item_smem(HD, G, a.chunk);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
   }
-  kern<<<grid, kAttnThreads, smem, s>>>(q, kc, vc, max_ctx, pos, scale, po, pml, n_chunks);
+  kern<<<grid, kAttnThreads, smem, s>>>(a, pos);
   return cudaGetLastError();
 }
 
-static cudaError_t launch_attn(int hd, int G, dim3 grid, size_t smem, cudaStream_t s, const float* q,
-                               const __half* kc, const __half* vc, int max_ctx, const int32_t* pos, float scale,
-                               float* po, float2* pml, int n_chunks) {
-#define NT_ATTN_G(HD)                                                                                    \
-  switch (G) {                                                                                           \
-    case 1: return launch_attn_t<HD, 1>(grid, smem, s, q, kc, vc, max_ctx, pos, scale, po, pml, n_chunks);   \
-    case 2: return launch_attn_t<HD, 2>(grid, smem, s, q, kc, vc, max_ctx, pos, scale, po, pml, n_chunks);   \
-    case 4: return launch_attn_t<HD, 4>(grid, smem, s, q, kc, vc, max_ctx, pos, scale, po, pml, n_chunks);   \
-    case 8: return launch_attn_t<HD, 8>(grid, smem, s, q, kc, vc, max_ctx, pos, scale, po, pml, n_chunks);   \
-    case 16: return launch_attn_t<HD, 16>(grid, smem, s, q, kc, vc, max_ctx, pos, scale, po, pml, n_chunks); \
+static cudaError_t launch_attn(int hd, int G, dim3 grid, cudaStream_t s, const AttnArgs& a, const int32_t* pos) {
+#define NT_ATTN_G(HD)                                                  \
+  switch (G) {                                                         \
+    case 1: return launch_attn_t<HD, 1>(grid, s, a, pos);              \
+    case 2: return launch_attn_t<HD, 2>(grid, s, a, pos);              \
+    case 4: return launch_attn_t<HD, 4>(grid, s, a, pos);              \
+    case 8: return launch_attn_t<HD, 8>(grid, s, a, pos);              \
+    case 16: return launch_attn_t<HD, 16>(grid, s, a, pos);            \
   }
   if (hd == 128) {
     NT_ATTN_G(128)
@@ -432,16 +264,36 @@ static cudaError_t launch_attn(int hd, int G, dim3 grid, size_t smem, cudaStream
   return cudaErrorInvalidValue;
 }
 
-static cudaError_t enqueue_layer(nt_model* m, int l, uint8_t* base, Launcher& L, bool pdl) {
+static AttnArgs attn_args(nt_model* m, int l) {
+  AttnArgs a;
+  a.q = m->q;
+  a.kc = k_cache(m, l);
+  a.vc = v_cache(m, l);
+  a.max_ctx = m->c.max_ctx;
+  a.chunk = attn_chunk_len(m->c.max_ctx);
+  a.scale = 1.0f / sqrtf(float(m->c.head_dim));
+  a.part_o = m->part_o;
+  a.part_ml = m->part_ml;
+  a.n_chunks = m->n_chunks;
+  a.tickets = m->tickets;
+  a.out = m->att;
+  return a;
+}
+
+// The GEMVs of layer l with its weights at base: QK (QKV when v shares the
+// format; then v_split is false and `v` unused), V, O, gate/up, down.
+struct LayerGemvs {
+  GemvArgs qk, v, o, gu, down;
+  bool v_split = false;
+};
+
+static LayerGemvs layer_gemvs(nt_model* m, int l, uint8_t* base) {
   const nt_config& c = m->c;
   const Layer& ly = m->layers[size_t(l)];
-  const int hd = c.head_dim, G = c.n_heads / c.n_kv_heads;
-  const int qd = c.n_heads * hd, kd = c.n_kv_heads * hd;
-  cudaStream_t s = L.s;
-  cudaError_t e;
-
+  const int hd = c.head_dim, qd = c.n_heads * hd, kd = c.n_kv_heads * hd;
+  LayerGemvs g;
   // RMSNorm -> Q|K|V -> RoPE -> cache
-  GemvArgs a;
+  GemvArgs& a = g.qk;
   a.x = m->x;
   a.norm = 1;
   a.eps = c.rms_eps;
@@ -459,88 +311,93 @@ static cudaError_t enqueue_layer(nt_model* m, int l, uint8_t* base, Launcher& L,
   if (c.t_v == c.t_q) {
     a.seg[2] = view_at(ly, NT_ROLE_V, base);
     a.nseg = 3;
-    const double by = qbytes(a.seg[0]) + qbytes(a.seg[1]) + qbytes(a.seg[2]) + 4.0 * (c.hidden + qd) + 4.0 * kd;
-    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(a, EPI_QKV, s, pdl, nullptr); }))) return e;
   } else {
     a.nseg = 2;
-    double by = qbytes(a.seg[0]) + qbytes(a.seg[1]) + 4.0 * (c.hidden + qd) + 2.0 * kd;
-    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(a, EPI_QKV, s, pdl, nullptr); }))) return e;
-    GemvArgs b = a;
-    b.seg[0] = view_at(ly, NT_ROLE_V, base);
-    b.nseg = 1;
-    b.epi.row_base = qd + kd;
-    by = qbytes(b.seg[0]) + 4.0 * c.hidden + 2.0 * kd;
-    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(b, EPI_QKV, s, pdl, nullptr); }))) return e;
+    g.v = a;
+    g.v.seg[0] = view_at(ly, NT_ROLE_V, base);
+    g.v.nseg = 1;
+    g.v.epi.row_base = qd + kd;
+    g.v_split = true;
+  }
+  // O + residual
+  g.o.seg[0] = view_at(ly, NT_ROLE_O, base);
+  g.o.x = m->att;
+  g.o.epi.y = m->x;
+  // RMSNorm -> gate|up (rows interleaved) -> SwiGLU
+  g.gu.seg[0] = view_at(ly, NT_ROLE_GATE, base);
+  g.gu.seg[1] = view_at(ly, NT_ROLE_UP, base);
+  g.gu.nseg = 2;
+  g.gu.interleave = 1;
+  g.gu.x = m->x;
+  g.gu.norm = 1;
+  g.gu.eps = c.rms_eps;
+  g.gu.epi.y = m->u;
+  // down + residual
+  g.down.seg[0] = view_at(ly, NT_ROLE_DOWN, base);
+  g.down.x = m->u;
+  g.down.epi.y = m->x;
+  return g;
+}
+
+static GemvArgs head_gemv(nt_model* m) {
+  GemvArgs a;
+  a.seg[0] = m->output.m;
+  a.x = m->x;
+  a.norm = 1;
+  a.eps = m->c.rms_eps;
+  a.epi.y = m->logits;
+  a.epi.top2 = m->top2;
+  return a;
+}
+
+static double gemv_bytes(const GemvArgs& a, double out_bytes) {
+  double b = 0;
+  for (int i = 0; i < a.nseg; i++) b += qbytes(a.seg[i]);
+  return b + 4.0 * double(a.seg[0].cols) + out_bytes;
+}
+
+static cudaError_t enqueue_layer(nt_model* m, int l, uint8_t* base, Launcher& L, bool pdl) {
+  const nt_config& c = m->c;
+  const int hd = c.head_dim, G = c.n_heads / c.n_kv_heads;
+  const int qd = c.n_heads * hd, kd = c.n_kv_heads * hd;
+  cudaStream_t s = L.s;
+  cudaError_t e;
+  const LayerGemvs g = layer_gemvs(m, l, base);
+
+  if (!g.v_split) {
+    const double by = gemv_bytes(g.qk, 4.0 * qd + 4.0 * kd);
+    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(g.qk, EPI_QKV, s, pdl, nullptr); }))) return e;
+  } else {
+    double by = gemv_bytes(g.qk, 4.0 * qd + 2.0 * kd);
+    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(g.qk, EPI_QKV, s, pdl, nullptr); }))) return e;
+    by = gemv_bytes(g.v, 2.0 * kd);
+    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(g.v, EPI_QKV, s, pdl, nullptr); }))) return e;
   }
 
-  // split-context GQA attention over positions 0..pos
+  // split-context GQA attention over positions 0..pos, merged by the last chunk's CTA
   {
     const int n_used = m->pos + 1;   // host mirror (exact for profiled and streamed steps)
     const double by = 2.0 * 2.0 * double(c.n_kv_heads) * n_used * hd + 8.0 * qd;
-    const size_t smem = size_t(2 * kAttnChunk * (hd + 8)) * 2 + size_t(G * hd + G * kAttnChunk) * 4;
-    const float scale = 1.0f / sqrtf(float(hd));
     dim3 grid(unsigned(c.n_kv_heads), unsigned(m->n_chunks));
-    e = L.run(NT_KC_ATTN, by, [&] {
-      return launch_attn(hd, G, grid, smem, s, m->q, k_cache(m, l), v_cache(m, l), c.max_ctx, d_pos(m), scale,
-                         m->part_o, m->part_ml, m->n_chunks);
-    });
-    if (e) return e;
-    e = L.run(NT_KC_ATTN, 0.0, [&] {
-      if (hd == 128)
-        k_attn_combine<128><<<unsigned(c.n_heads), 128, 0, s>>>(m->part_o, m->part_ml, d_pos(m), m->n_chunks, m->att);
-      else
-        k_attn_combine<64><<<unsigned(c.n_heads), 128, 0, s>>>(m->part_o, m->part_ml, d_pos(m), m->n_chunks, m->att);
-      return cudaGetLastError();
-    });
+    const AttnArgs aa = attn_args(m, l);
+    e = L.run(NT_KC_ATTN, by, [&] { return launch_attn(hd, G, grid, s, aa, d_pos(m)); });
     if (e) return e;
   }
 
-  // O + residual
-  {
-    GemvArgs o;
-    o.seg[0] = view_at(ly, NT_ROLE_O, base);
-    o.x = m->att;
-    o.epi.y = m->x;
-    const double by = qbytes(o.seg[0]) + 4.0 * qd + 8.0 * c.hidden;
-    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(o, EPI_ADD, s, pdl, nullptr); }))) return e;
-  }
-  // RMSNorm -> gate|up -> SwiGLU
-  {
-    GemvArgs gu;
-    gu.seg[0] = view_at(ly, NT_ROLE_GATE, base);
-    gu.seg[1] = view_at(ly, NT_ROLE_UP, base);
-    gu.nseg = 2;
-    gu.interleave = 1;
-    gu.x = m->x;
-    gu.norm = 1;
-    gu.eps = c.rms_eps;
-    gu.epi.y = m->u;
-    const double by = qbytes(gu.seg[0]) + qbytes(gu.seg[1]) + 4.0 * c.hidden + 4.0 * c.ffn_dim;
-    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(gu, EPI_SWIGLU, s, pdl, nullptr); }))) return e;
-  }
-  // down + residual
-  {
-    GemvArgs dn;
-    dn.seg[0] = view_at(ly, NT_ROLE_DOWN, base);
-    dn.x = m->u;
-    dn.epi.y = m->x;
-    const double by = qbytes(dn.seg[0]) + 4.0 * c.ffn_dim + 8.0 * c.hidden;
-    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(dn, EPI_ADD, s, pdl, nullptr); }))) return e;
-  }
+  double by = gemv_bytes(g.o, 8.0 * c.hidden);
+  if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(g.o, EPI_ADD, s, pdl, nullptr); }))) return e;
+  by = gemv_bytes(g.gu, 4.0 * c.ffn_dim);
+  if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(g.gu, EPI_SWIGLU, s, pdl, nullptr); }))) return e;
+  by = gemv_bytes(g.down, 8.0 * c.hidden);
+  if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(g.down, EPI_ADD, s, pdl, nullptr); }))) return e;
   return cudaSuccess;
 }
 
 static cudaError_t enqueue_head(nt_model* m, Launcher& L) {
   const nt_config& c = m->c;
   cudaStream_t s = L.s;
-  GemvArgs a;
-  a.seg[0] = m->output.m;
-  a.x = m->x;
-  a.norm = 1;
-  a.eps = c.rms_eps;
-  a.epi.y = m->logits;
-  a.epi.top2 = m->top2;
-  const double by = qbytes(a.seg[0]) + 4.0 * c.hidden + 4.0 * c.vocab;
+  const GemvArgs a = head_gemv(m);
+  const double by = gemv_bytes(a, 4.0 * c.vocab);
   cudaError_t e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(a, EPI_LOGITS, s, false, &m->out_grid); });
   if (e) return e;
   return L.run(NT_KC_OTHER, 0.0, [&] {
@@ -645,6 +502,129 @@ static nt_status ensure_graph(nt_model* m) {
     return cuda_fail(e, "cudaGraphInstantiate");
   }
   return NT_OK;
+}
+
+// ------------------------------------------------------------ step kernel --
+
+// The persistent step kernel is opt-in (NT_STEP_KERNEL=1): on GB300 the
+// graph of per-kernel launches is faster today.
+static bool step_kernel_enabled() {
+  const char* v = getenv("NT_STEP_KERNEL");
+  return v && strcmp(v, "1") == 0;
+}
+
+static void fill_step_gemv(StepGemv& d, const GemvArgs& a) {
+  d.a = a;
+  d.a.col0 = 0;
+  d.a.ncols = a.seg[0].cols;
+  d.a.max_grid = kMaxGemvGrid;
+  d.nrows = gemv_logical_rows(a);
+}
+
+// Decides (once per residency layout) whether the step runs as the persistent
+// kernel, and if so builds its GEMV table in device memory.
+static nt_status prepare_step(nt_model* m) {
+  if (m->step_state) return NT_OK;
+  m->step_state = -1;
+  const nt_config& c = m->c;
+  if (!step_kernel_enabled() || m->n_resident < c.n_layers) return NT_OK;
+  const int64_t qd = int64_t(c.n_heads) * c.head_dim;
+  if (c.hidden % 1024 || qd % 1024 || c.ffn_dim % 1024 || c.n_kv_heads > kStepMaxTiles) return NT_OK;
+  StepPlan p;
+  p.f_qk = c.t_q;
+  p.f_v = c.t_v;
+  p.f_o = c.t_o;
+  p.f_gu = c.t_gate;
+  p.f_d = c.t_down;
+  p.f_out = c.t_out;
+  p.hd = c.head_dim;
+  p.G = c.n_heads / c.n_kv_heads;
+  int dev = 0, coop = 0;
+  NT_CUDA(cudaGetDevice(&dev));
+  NT_CUDA(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev));
+  if (!coop) return NT_OK;
+  int64_t max_cols = c.hidden > qd ? c.hidden : qd;
+  if (c.ffn_dim > max_cols) max_cols = c.ffn_dim;
+  size_t ring_off = 0;
+  const size_t smem = step_smem(p, max_cols, attn_chunk_len(c.max_ctx), &ring_off);
+  bool fits = false;
+  const cudaError_t fe = step_fits(p, smem, &fits);
+  if (fe == cudaErrorNotSupported) return NT_OK;   // no instantiation for this plan
+  if (fe != cudaSuccess) return cuda_fail(fe, "nt_decode_step: step kernel attributes");
+  if (!fits) return NT_OK;
+
+  // layer 0's GEMVs and the head; layer l reads its weights delta_l bytes further on
+  std::vector<StepGemv> tab(SG_PER_LAYER + 1);
+  std::vector<int64_t> delta(size_t(c.n_layers));
+  if (c.n_layers > 0) {
+    const LayerGemvs g = layer_gemvs(m, 0, m->layers[0].dev);
+    fill_step_gemv(tab[SG_QK], g.qk);
+    if (g.v_split) fill_step_gemv(tab[SG_V], g.v);
+    fill_step_gemv(tab[SG_O], g.o);
+    fill_step_gemv(tab[SG_GU], g.gu);
+    fill_step_gemv(tab[SG_DOWN], g.down);
+    for (int l = 0; l < c.n_layers; l++)
+      delta[size_t(l)] = int64_t(m->layers[size_t(l)].dev - m->layers[0].dev);
+  }
+  fill_step_gemv(tab[SG_PER_LAYER], head_gemv(m));
+  if (m->step_tab) dev_free(m, m->step_tab);
+  m->step_tab = nullptr;
+  const size_t tab_bytes = tab.size() * sizeof(StepGemv), delta_bytes = delta.size() * 8;
+  NT_CUDA(dev_alloc(m, reinterpret_cast<void**>(&m->step_tab), tab_bytes + delta_bytes + 8));
+  NT_CUDA(cudaMemcpy(m->step_tab, tab.data(), tab_bytes, cudaMemcpyHostToDevice));
+  int64_t* d_delta = reinterpret_cast<int64_t*>(reinterpret_cast<uint8_t*>(m->step_tab) + tab_bytes);
+  if (delta_bytes) NT_CUDA(cudaMemcpy(d_delta, delta.data(), delta_bytes, cudaMemcpyHostToDevice));
+
+  StepArgs& a = m->step;
+  a = StepArgs();
+  a.gemv = m->step_tab;
+  a.layer_delta = d_delta;
+  a.n_layers = c.n_layers;
+  a.split_v = c.t_v != c.t_q;
+  a.embd = m->embd.m;
+  a.x = m->x;
+  a.hidden = c.hidden;
+  a.attn = attn_args(m, 0);
+  a.kv = m->kv;
+  a.kv_layer_elems = kv_layer_elems(c);
+  a.n_kv = c.n_kv_heads;
+  a.attn_qd = int(qd);
+  a.attn_kd = c.n_kv_heads * c.head_dim;
+  a.top2 = m->top2;
+  a.small = m->small;
+  a.hist = m->hist;
+  a.max_ctx = c.max_ctx;
+  a.vocab = c.vocab;
+  a.bar = m->bar;
+  a.ring_off = uint32_t(ring_off);
+  // fault injection for tests: a barrier base that the arrivals never reach,
+  // so the step's grid barrier runs into its time limit
+  if (const char* off = getenv("NT_STEP_BARRIER_OFFSET")) {
+    const unsigned base = unsigned(strtoul(off, nullptr, 10));
+    NT_CUDA(cudaMemcpy(m->bar + 1, &base, 4, cudaMemcpyHostToDevice));
+  }
+  m->plan = p;
+  m->step_smem = smem;
+  m->step_state = 1;
+  return NT_OK;
+}
+
+static int step_barriers(const nt_model* m) { return 2 + 5 * m->c.n_layers; }
+
+static cudaError_t launch_step_model(nt_model* m, cudaStream_t s, long long* stamps) {
+  StepArgs a = m->step;
+  a.stamps = stamps;
+  return launch_step(m->plan, a, m->step_smem, s);
+}
+
+// After an abandoned step: clear the error word and the barrier state.
+static void reset_step_error(nt_model* m) {
+  cudaMemsetAsync(m->bar, 0, SYNC_WORDS * 4, m->stream);
+  m->h_io[0] = m->pos;   // the abandoned step may have advanced the device position
+  cudaMemcpyAsync(d_pos(m), m->h_io, 4, cudaMemcpyHostToDevice, m->stream);
+  cudaMemsetAsync(m->tickets, 0, size_t(m->c.n_kv_heads) * 4, m->stream);
+  cudaMemsetAsync(m->small + 4, 0, 4, m->stream);
+  cudaStreamSynchronize(m->stream);
 }
 
 static void free_model(nt_model* m) {
@@ -779,7 +759,7 @@ nt_status nt_model_create(const nt_config* cfg, nt_model** out) {
   const size_t kv_elems = size_t(c.n_layers) * 2 * size_t(kv_layer_elems(c));
   NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->kv), kv_elems * 2), "nt_model_create: KV cache");
   NT_TRY(cudaMemsetAsync(m->kv, 0, kv_elems * 2, m->stream), "cudaMemset");
-  m->n_chunks = int((c.max_ctx + kAttnChunk - 1) / kAttnChunk);
+  m->n_chunks = int((c.max_ctx + attn_chunk_len(c.max_ctx) - 1) / attn_chunk_len(c.max_ctx));
   NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->x), size_t(h) * 4), "alloc x");
   NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->q), size_t(qd) * 4), "alloc q");
   NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->att), size_t(qd) * 4), "alloc att");
@@ -788,6 +768,10 @@ nt_status nt_model_create(const nt_config* cfg, nt_model** out) {
   NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->part_o), size_t(qd) * m->n_chunks * 4), "alloc partials");
   NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->part_ml), size_t(c.n_heads) * m->n_chunks * 8), "alloc partials");
   NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->top2), size_t(kMaxGemvGrid) * 16), "alloc top2");
+  NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->tickets), size_t(c.n_kv_heads) * 4), "alloc tickets");
+  NT_TRY(cudaMemsetAsync(m->tickets, 0, size_t(c.n_kv_heads) * 4, m->stream), "cudaMemset");
+  NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->bar), SYNC_WORDS * 4), "alloc step sync state");
+  NT_TRY(cudaMemsetAsync(m->bar, 0, SYNC_WORDS * 4, m->stream), "cudaMemset");
   NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->small), 16 * 4), "alloc small");
   NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->hist), size_t(c.max_ctx) * 4), "alloc hist");
   NT_TRY(cudaMemsetAsync(m->small, 0, 16 * 4, m->stream), "cudaMemset");
@@ -844,7 +828,10 @@ nt_status nt_decode_step(nt_model* m, int32_t token, int32_t* next_token, float*
   if (token < 0 || token >= m->c.vocab) return fail(NT_E_INVAL, "nt_decode_step: token outside [0, vocab)");
   if (m->pos >= m->c.max_ctx) return fail(NT_E_INVAL, "nt_decode_step: position reached max_ctx");
   const bool streamed = m->n_resident < m->c.n_layers;
-  if (!streamed) {
+  nt_status st0 = prepare_step(m);
+  if (st0) return st0;
+  const bool step_kernel = m->step_state == 1;
+  if (!streamed && !step_kernel) {
     nt_status st = ensure_graph(m);
     if (st) return st;
   }
@@ -856,17 +843,25 @@ nt_status nt_decode_step(nt_model* m, int32_t token, int32_t* next_token, float*
     L.s = m->stream;
     cudaError_t e = enqueue_streamed(m, L);
     if (e) return cuda_fail(e, "nt_decode_step: streamed step");
+  } else if (step_kernel) {
+    cudaError_t e = launch_step_model(m, m->stream, nullptr);
+    if (e) return cuda_fail(e, "nt_decode_step: step kernel");
   } else {
     NT_CUDA(cudaGraphLaunch(m->exec, m->stream));
   }
   NT_CUDA(cudaEventRecord(m->ev_step1, m->stream));
-  NT_CUDA(cudaMemcpyAsync(m->h_io + 2, d_next(m), 8, cudaMemcpyDeviceToHost, m->stream));
+  // next id, margin and the error word
+  NT_CUDA(cudaMemcpyAsync(m->h_io + 2, d_next(m), 12, cudaMemcpyDeviceToHost, m->stream));
   if (logits_host)
     NT_CUDA(cudaMemcpyAsync(logits_host, m->logits, size_t(m->c.vocab) * 4, cudaMemcpyDeviceToHost, m->stream));
   cudaEvent_t done = m->ev_step1;
   nt_status st = wait_event(done, "nt_decode_step");
   if (st) return st;
   NT_CUDA(cudaStreamSynchronize(m->stream));
+  if (m->h_io[4]) {
+    reset_step_error(m);
+    return fail(NT_E_TIMEOUT, "nt_decode_step: a grid barrier of the step kernel timed out; step abandoned");
+  }
   float ms = 0.f;
   NT_CUDA(cudaEventElapsedTime(&ms, m->ev_step0, m->ev_step1));
   m->stats.last_step_ms = ms;
@@ -904,14 +899,23 @@ nt_status nt_decode_run(nt_model* m, int32_t token, int32_t n_steps, void* strea
   if (n_steps < 0 || token < 0 || token >= m->c.vocab) return fail(NT_E_INVAL, "nt_decode_run: bad token or n_steps");
   if (m->pos + n_steps > m->c.max_ctx) return fail(NT_E_INVAL, "nt_decode_run: would pass max_ctx");
   if (m->n_resident < m->c.n_layers) return fail(NT_E_STATE, "nt_decode_run: model has streamed layers");
-  nt_status st = ensure_graph(m);
+  nt_status st = prepare_step(m);
   if (st) return st;
+  const bool step_kernel = m->step_state == 1;
+  if (!step_kernel && (st = ensure_graph(m))) return st;
   cudaStream_t us = static_cast<cudaStream_t>(stream);
   NT_CUDA(cudaEventRecord(m->ev_step0, us));
   NT_CUDA(cudaStreamWaitEvent(m->stream, m->ev_step0, 0));
   m->h_io[1] = token;
   NT_CUDA(cudaMemcpyAsync(d_token(m), m->h_io + 1, 4, cudaMemcpyHostToDevice, m->stream));
-  for (int i = 0; i < n_steps; i++) NT_CUDA(cudaGraphLaunch(m->exec, m->stream));
+  for (int i = 0; i < n_steps; i++) {
+    if (step_kernel) {
+      cudaError_t e = launch_step_model(m, m->stream, nullptr);
+      if (e) return cuda_fail(e, "nt_decode_run: step kernel");
+    } else {
+      NT_CUDA(cudaGraphLaunch(m->exec, m->stream));
+    }
+  }
   NT_CUDA(cudaEventRecord(m->ev_step1, m->stream));
   NT_CUDA(cudaStreamWaitEvent(us, m->ev_step1, 0));
   m->pos += n_steps;
@@ -923,6 +927,15 @@ nt_status nt_get_tokens(nt_model* m, int32_t t0, int32_t n, int32_t* host_out) {
   if (!m || !host_out) return fail(NT_E_INVAL, "nt_get_tokens: NULL argument");
   if (t0 < 0 || n < 0 || t0 + n > m->c.max_ctx) return fail(NT_E_INVAL, "nt_get_tokens: range");
   NT_CUDA(cudaStreamSynchronize(m->stream));
+  int32_t err = 0;
+  NT_CUDA(cudaMemcpy(&err, m->small + 4, 4, cudaMemcpyDeviceToHost));
+  if (err) {
+    reset_step_error(m);
+    int32_t pos = 0;   // abandoned steps did not advance the device position
+    NT_CUDA(cudaMemcpy(&pos, d_pos(m), 4, cudaMemcpyDeviceToHost));
+    m->pos = pos;
+    return fail(NT_E_TIMEOUT, "nt_get_tokens: a step of an earlier nt_decode_run was abandoned (grid barrier timeout)");
+  }
   NT_CUDA(cudaMemcpy(host_out, m->hist + t0, size_t(n) * 4, cudaMemcpyDeviceToHost));
   return NT_OK;
 }
@@ -947,6 +960,7 @@ nt_status nt_stream_layers(nt_model* m, int32_t n_resident, int32_t n_staging) {
   NT_CUDA(cudaStreamSynchronize(m->stream));
   NT_CUDA(cudaStreamSynchronize(m->copy_stream));
   drop_graph(m);
+  m->step_state = 0;
   size_t max_bytes = 0;
   for (int l = 0; l < m->c.n_layers; l++) {
     Layer& L = m->layers[size_t(l)];
@@ -1008,6 +1022,72 @@ nt_status nt_profile_steps(nt_model* m, int32_t token, int32_t n_steps, nt_kerne
   double wall = 0;
   m->h_io[1] = token;
   NT_CUDA(cudaMemcpyAsync(d_token(m), m->h_io + 1, 4, cudaMemcpyHostToDevice, m->stream));
+  nt_status st0 = prepare_step(m);
+  if (st0) return st0;
+  if (m->step_state == 1) {
+    // one launch per step; CTA 0's SM clock at every barrier splits it into phases
+    const nt_config& c = m->c;
+    const int nb = step_barriers(m);
+    long long* d_stamps = nullptr;
+    NT_CUDA(cudaMalloc(&d_stamps, size_t(nb + 2) * 8));
+    std::vector<long long> h(size_t(nb + 2));
+    const int hd = c.head_dim, qd = c.n_heads * hd, kd = c.n_kv_heads * hd;
+    nt_status st = NT_OK;
+    for (int i = 0; i < n_steps && !st; i++) {
+      cudaError_t e = cudaEventRecord(m->ev_step0, m->stream);
+      if (!e) e = launch_step_model(m, m->stream, d_stamps);
+      if (!e) e = cudaEventRecord(m->ev_step1, m->stream);
+      if (e) {
+        st = cuda_fail(e, "nt_profile_steps: step kernel");
+        break;
+      }
+      if ((st = wait_event(m->ev_step1, "nt_profile_steps"))) break;
+      float ms = 0.f;
+      e = cudaEventElapsedTime(&ms, m->ev_step0, m->ev_step1);
+      if (!e) e = cudaMemcpy(h.data(), d_stamps, h.size() * 8, cudaMemcpyDeviceToHost);
+      if (!e) e = cudaMemcpy(m->h_io + 4, m->small + 4, 4, cudaMemcpyDeviceToHost);
+      if (e) {
+        st = cuda_fail(e, "nt_profile_steps");
+        break;
+      }
+      if (m->h_io[4]) {
+        reset_step_error(m);
+        st = fail(NT_E_TIMEOUT, "nt_profile_steps: a grid barrier of the step kernel timed out");
+        break;
+      }
+      wall += ms;
+      const double cyc = double(h[size_t(nb + 1)] - h[0]);
+      const double ms_per_cyc = cyc > 0 ? ms / cyc : 0.0;
+      auto add = [&](int kind, int k0, double bytes) {   // phase between stamps k0 and k0+1
+        t.launches[kind]++;
+        t.ms[kind] += double(h[size_t(k0 + 1)] - h[size_t(k0)]) * ms_per_cyc;
+        t.bytes[kind] += bytes;
+      };
+      const int n_used = m->pos + 1;
+      add(NT_KC_OTHER, 0, 0.0);
+      for (int l = 0; l < c.n_layers; l++) {
+        const LayerGemvs g = layer_gemvs(m, l, m->layers[size_t(l)].dev);
+        const int k = 1 + 5 * l;
+        double qkv = g.v_split ? gemv_bytes(g.qk, 4.0 * qd + 2.0 * kd) + gemv_bytes(g.v, 2.0 * kd)
+                               : gemv_bytes(g.qk, 4.0 * qd + 4.0 * kd);
+        add(NT_KC_GEMV, k, qkv);
+        add(NT_KC_ATTN, k + 1, 2.0 * 2.0 * double(c.n_kv_heads) * n_used * hd + 8.0 * qd);
+        add(NT_KC_GEMV, k + 2, gemv_bytes(g.o, 8.0 * c.hidden));
+        add(NT_KC_GEMV, k + 3, gemv_bytes(g.gu, 4.0 * c.ffn_dim));
+        add(NT_KC_GEMV, k + 4, gemv_bytes(g.down, 8.0 * c.hidden));
+      }
+      add(NT_KC_GEMV, nb - 1, gemv_bytes(head_gemv(m), 4.0 * c.vocab));
+      add(NT_KC_OTHER, nb, 0.0);
+      t.kernel_launches++;
+      m->pos++;
+      m->stats.steps++;
+    }
+    cudaFree(d_stamps);
+    if (st) return st;
+    t.step_ms = wall / n_steps;
+    *out = t;
+    return NT_OK;
+  }
   for (int i = 0; i < n_steps; i++) {
     Prof prof;
     Launcher L;
@@ -1024,6 +1104,7 @@ nt_status nt_profile_steps(nt_model* m, int32_t token, int32_t n_steps, nt_kerne
     wall += ms;
     for (auto& r : prof.recs) {
       NT_CUDA(cudaEventElapsedTime(&ms, r.a, r.b));
+      t.kernel_launches++;
       t.launches[r.kind]++;
       t.ms[r.kind] += ms;
       t.bytes[r.kind] += r.bytes;

@@ -305,23 +305,23 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, int64_t grp, int64_t
   if (EPI == EPI_STORE) {
     a.epi.y[row] = k;
   } else if (EPI == EPI_ADD) {
-    a.epi.y[row] += k;
+    a.epi.y[row] = __fadd_rn(__ldcg(a.epi.y + row), k);
   } else if (EPI == EPI_LOGITS) {
     a.epi.y[row] = k;
     top2_push(k, int(row), best, best_i, second);
   } else if ((rr & 1) == 0) {
     const float v0 = k, v1 = other;
     if (EPI == EPI_SWIGLU) {
-      a.epi.y[row >> 1] = silu(v0) * v1;
+      a.epi.y[row >> 1] = __fmul_rn(silu(v0), v1);
     } else {  // EPI_QKV: RoPE on q and k pairs, f16 store of k and v at the current position
       const int L = a.epi.row_base + int(row);
       const int hd = a.epi.head_dim;
-      const int p = *a.epi.pos;
+      const int p = __ldcg(a.epi.pos);
       if (L < a.epi.q_rows + a.epi.k_rows) {
         const int d = L % hd;
         const float2 cs = a.epi.rope[int64_t(p) * (hd / 2) + d / 2];
-        const float r0 = v0 * cs.x - v1 * cs.y;
-        const float r1 = v0 * cs.y + v1 * cs.x;
+        const float r0 = __fmaf_rn(v0, cs.x, -__fmul_rn(v1, cs.y));
+        const float r1 = __fmaf_rn(v0, cs.y, __fmul_rn(v1, cs.x));
         if (L < a.epi.q_rows) {
           a.epi.y[L] = r0;
           a.epi.y[L + 1] = r1;
@@ -344,7 +344,7 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, int64_t grp, int64_t
 
 // CTA-wide top-2 of the rows this CTA finished, written to top2[blockIdx.x].
 template <int NW>
-__device__ __forceinline__ void cta_top2(const GemvArgs& a, float best, int best_i, float second) {
+__device__ __forceinline__ void cta_top2(const GemvArgs& a, int cta, float best, int best_i, float second) {
   __shared__ float s_b[NW], s_s[NW];
   __shared__ int s_i[NW];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -365,7 +365,7 @@ __device__ __forceinline__ void cta_top2(const GemvArgs& a, float best, int best
     float b = -INFINITY, s = -INFINITY;
     int bi = 0x7fffffff;
     for (int w = 0; w < NW; w++) top2_merge(s_b[w], s_i[w], s_s[w], b, bi, s);
-    a.epi.top2[blockIdx.x] = make_float4(b, __int_as_float(bi), s, 0.f);
+    a.epi.top2[cta] = make_float4(b, __int_as_float(bi), s, 0.f);
   }
 }
 
@@ -499,7 +499,7 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const __grid_constant__ GemvA
   }
 
   asm volatile("griddepcontrol.launch_dependents;");
-  if (EPI == EPI_LOGITS) cta_top2<kThreads / 32>(a, best, best_i, second);
+  if (EPI == EPI_LOGITS) cta_top2<kThreads / 32>(a, blockIdx.x, best, best_i, second);
 }
 
 inline size_t gemv_smem(int fmt, int64_t cols) {

@@ -43,7 +43,7 @@ namespace nt {
 constexpr int kPipeWarps = 8;                 // 256 threads per CTA
 constexpr int kPipeMaxSmem = 221 * 1024;      // dynamic shared memory a CTA may ask for
 constexpr int kPipeSmemTarget = 110 * 1024;   // per CTA, so two CTAs fit on an SM
-constexpr int kXUnit = 80;                    // staged x per 32 columns: h[32] | l[32] | sx, T0, T1, pad
+constexpr int kXUnit = 80;                    // staged x per 32 columns: h[32] | l[32] | sx, T0, T1, sum of squares
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -122,7 +122,7 @@ template <> struct Pipe<NT_Q8_0> {
     const uint4 c1 = *reinterpret_cast<const uint4*>(blk + lane * 32 + 16);
     const int c[8] = {int(c0.x), int(c0.y), int(c0.z), int(c0.w), int(c1.x), int(c1.y), int(c1.z), int(c1.w)};
     const float d = h2f_bits(*reinterpret_cast<const uint16_t*>(blk + 1024 + lane * 2));
-    return (d * x.sx) * float(idot<0, 8>(c, x));
+    return __fmul_rn(__fmul_rn(d, x.sx), __int2float_rn(idot<0, 8>(c, x)));
   }
 };
 
@@ -144,7 +144,7 @@ template <> struct Pipe<NT_Q4_0> {
     int c[8];
     nibble_bytes(*reinterpret_cast<const uint4*>(blk + lane * 16), c);
     const float d = h2f_bits(*reinterpret_cast<const uint16_t*>(blk + 512 + lane * 2));
-    return (d * x.sx) * float(idot<0, 8>(c, x) - 8 * (x.t0 + x.t1));
+    return __fmul_rn(__fmul_rn(d, x.sx), __int2float_rn(idot<0, 8>(c, x) - 8 * (x.t0 + x.t1)));
   }
 };
 
@@ -171,9 +171,9 @@ template <> struct Pipe<NT_Q4_K> {
     const int mb = 48 + 6 * j;
     const uint32_t mm = mb >= 64 ? (meta.w >> (mb - 64)) & 63u
                                  : uint32_t((lo >> mb) | (uint64_t(meta.w) << (64 - mb))) & 63u;
-    const float a = h2f_bits(meta.x & 0xFFFFu) * float(sc);
-    const float b = h2f_bits(meta.x >> 16) * float(mm);
-    return x.sx * (a * float(idot<0, 8>(c, x)) - b * float(x.t0 + x.t1));
+    const float a = __fmul_rn(h2f_bits(meta.x & 0xFFFFu), float(sc));
+    const float b = __fmul_rn(h2f_bits(meta.x >> 16), float(mm));
+    return __fmul_rn(x.sx, __fmaf_rn(a, __int2float_rn(idot<0, 8>(c, x)), -__fmul_rn(b, __int2float_rn(x.t0 + x.t1))));
   }
 };
 
@@ -218,7 +218,7 @@ template <> struct Pipe<NT_Q6_K> {
     const int s0 = idot<0, 4>(c, x) - 32 * x.t0;
     const int s1 = idot<4, 8>(c, x) - 32 * x.t1;
     const float sc0 = float(int8_t(sc2 & 0xFF)), sc1 = float(int8_t(sc2 >> 8));
-    return (d * x.sx) * (sc0 * float(s0) + sc1 * float(s1));
+    return __fmul_rn(__fmul_rn(d, x.sx), __fmaf_rn(sc0, __int2float_rn(s0), __fmul_rn(sc1, __int2float_rn(s1))));
   }
 };
 
@@ -273,150 +273,220 @@ __device__ __forceinline__ void group_copies(const GemvArgs& a, int64_t grp, int
   }
 }
 
-template <int FMT, int R, int S, int EPI>
-__global__ void __launch_bounds__(kPipeWarps * 32) k_gemv_pipe(const __grid_constant__ GemvArgs a,
-                                                              const int64_t nrows) {
-  using P = Pipe<FMT>;
-  constexpr int nw = kPipeWarps;
-  extern __shared__ float4 smem4[];
-  const int64_t cols = a.ncols;                   // window width, a multiple of 1024
-  const int units = int(cols / 32);
-  const int kiters = units / 32;
-  uint8_t* xq = reinterpret_cast<uint8_t*>(smem4);          // units x kXUnit
-  uint8_t* ring = xq + size_t(units) * kXUnit;
-  __shared__ float s_red[kPipeWarps];
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// Tiles of one warp: its row groups g0, g0 + stride, ... (g0 = warp * ncta + cta,
+// so consecutive groups land on different CTAs and every SM gets an equal
+// share), each in kiters column tiles.
+struct WarpTiles {
+  int64_t g0, stride, ntiles;
+};
+__device__ __forceinline__ WarpTiles warp_tiles(int64_t nrows, int R, int kiters, int warp, int nw, int cta,
+                                                int ncta) {
+  WarpTiles w;
   const int64_t ngroups = (nrows + R - 1) / R;
-  const int64_t stride = int64_t(gridDim.x) * nw;
-  uint8_t* wring = ring + size_t(warp) * S * R * P::RB;
-  const uint32_t wring_s = smem_addr(wring);
+  w.g0 = int64_t(warp) * ncta + cta;
+  w.stride = int64_t(ncta) * nw;
+  w.ntiles = w.g0 < ngroups ? ((ngroups - 1 - w.g0) / w.stride + 1) * kiters : 0;
+  return w;
+}
 
-  // this warp's tiles, in order: its row groups g0, g0 + stride, ..., each in kiters column tiles
-  const int64_t g0 = int64_t(blockIdx.x) * nw + warp;
-  const int64_t my_groups = g0 < ngroups ? (ngroups - 1 - g0) / stride + 1 : 0;
-  const int64_t ntiles = my_groups * kiters;
-
-  // copy issuer: runs S-1 tiles ahead of the decoder, with its own cursor
-  int64_t i_grp = g0, i_left = ntiles;
-  int i_it = 0, i_slot = 0;
+// Copy cursor of one warp over its tiles: issues (or, to resume after a
+// prologue issued elsewhere, only steps over) the cp.async copies of one tile.
+template <int FMT, int R, int S>
+struct PipeCursor {
+  int64_t grp, left, stride;
+  int it, slot, kiters;
   GroupCopies<FMT, R> gc;
-  auto issue_next = [&]() {
-    if (i_left > 0) {
-      if (i_it == 0) group_copies<FMT, R>(a, i_grp, nrows, lane, gc);
-      const uint32_t dst = wring_s + uint32_t(i_slot * R * P::RB);
-      const int64_t ct = int64_t(i_it) * P::CODE_STRIDE;
-#pragma unroll
-      for (int r = 0; r < R; r++)
-        if (r < gc.nlive) {
-          cp16(dst + r * P::RB + lane * P::CB, gc.code[r] + ct);
-          if (P::CB == 32) cp16(dst + r * P::RB + lane * P::CB + 16, gc.code[r] + ct + 16);
-        }
-#pragma unroll
-      for (int k = 0; k < GroupCopies<FMT, R>::NA; k++) {
-        if (gc.size[k] == 16) cp16(dst + gc.off[k], gc.src[k] + int64_t(i_it) * gc.stride[k]);
-        else if (gc.size[k] == 4) cp4(dst + gc.off[k], gc.src[k] + int64_t(i_it) * gc.stride[k]);
-      }
-      --i_left;
-      if (++i_slot == S) i_slot = 0;
-      if (++i_it == kiters) {
-        i_it = 0;
-        i_grp += stride;
-      }
-    }
-    cp_commit();   // one group per tile, empty past the end, so the wait_group counts stay aligned
-  };
 
-  // prologue: the first S-1 tiles before waiting for the producer of x
-#pragma unroll
-  for (int t = 0; t < S - 1; t++) issue_next();
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
-  // ---- stage x: 16-bit fixed point per 32-column block, and the RMS scale ----
-  // Chunks of 8192 columns: every thread issues its eight float4 loads before
-  // using any, so a chunk costs one memory latency.  Eight consecutive threads
-  // hold one 32-column block (one float4 each).
-  float scale = 1.0f;
-  {
-    const float4* x4 = reinterpret_cast<const float4*>(a.x + a.col0);
-    const int64_t n4 = cols / 4;
-    float ss = 0.f;
-    for (int64_t f0 = 0; f0 < n4; f0 += 8 * kPipeWarps * 32) {
-      float4 v[8];
-#pragma unroll
-      for (int i = 0; i < 8; i++) {
-        const int64_t f = f0 + tid + i * (kPipeWarps * 32);
-        v[i] = f < n4 ? x4[f] : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; i++) {
-        const int64_t f = f0 + tid + i * (kPipeWarps * 32);
-        ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
-        float amax = fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w)));
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float inv = amax > 0.f ? 32512.0f / amax : 0.f;
-        const float vv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-        const int c0 = int(f & 7) * 4;                       // first column of this float4 in its block
-        uint8_t* blk = xq + size_t(f >> 3) * kXUnit;
-        int tsum = 0;
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-          int t = __float2int_rn(vv[j] * inv);
-          t = max(-32512, min(32512, t));
-          const int h = (t + 128) >> 8;
-          tsum += t;
-          if (f < n4) {
-            blk[P::xbyte(c0 + j)] = uint8_t(int8_t(h));
-            blk[32 + P::xbyte(c0 + j)] = uint8_t(int8_t(t - 256 * h));
-          }
-        }
-        int t0 = c0 < 16 ? tsum : 0, t1 = c0 < 16 ? 0 : tsum;
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
-          t0 += __shfl_xor_sync(0xffffffffu, t0, o);
-          t1 += __shfl_xor_sync(0xffffffffu, t1, o);
-        }
-        if (f < n4 && c0 == 0)
-          *reinterpret_cast<uint4*>(blk + 64) = make_uint4(__float_as_uint(amax / 32512.0f), uint32_t(t0), uint32_t(t1), 0u);
-      }
-    }
-    if (a.norm) {
-#pragma unroll
-      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) s_red[warp] = ss;
-    }
-    __syncthreads();
-    if (a.norm) {
-      float t = 0.f;
-      for (int w = 0; w < nw; w++) t += s_red[w];
-      scale = rsqrtf(t / float(cols) + a.eps);
-    }
+  __device__ __forceinline__ void init(const WarpTiles& w, int kiters_) {
+    grp = w.g0;
+    left = w.ntiles;
+    stride = w.stride;
+    it = 0;
+    slot = 0;
+    kiters = kiters_;
   }
+  template <bool ISSUE>
+  __device__ __forceinline__ void step(const GemvArgs& a, int64_t nrows, int lane, uint32_t wring_s) {
+    using P = Pipe<FMT>;
+    if (left > 0) {
+      if (it == 0) group_copies<FMT, R>(a, grp, nrows, lane, gc);
+      if (ISSUE) {
+        const uint32_t dst = wring_s + uint32_t(slot * R * P::RB);
+        const int64_t ct = int64_t(it) * P::CODE_STRIDE;
+#pragma unroll
+        for (int r = 0; r < R; r++)
+          if (r < gc.nlive) {
+            cp16(dst + r * P::RB + lane * P::CB, gc.code[r] + ct);
+            if (P::CB == 32) cp16(dst + r * P::RB + lane * P::CB + 16, gc.code[r] + ct + 16);
+          }
+#pragma unroll
+        for (int k = 0; k < GroupCopies<FMT, R>::NA; k++) {
+          if (gc.size[k] == 16) cp16(dst + gc.off[k], gc.src[k] + int64_t(it) * gc.stride[k]);
+          else if (gc.size[k] == 4) cp4(dst + gc.off[k], gc.src[k] + int64_t(it) * gc.stride[k]);
+        }
+      }
+      --left;
+      if (++slot == S) slot = 0;
+      if (++it == kiters) {
+        it = 0;
+        grp += stride;
+      }
+    }
+    if (ISSUE) cp_commit();   // one group per tile, empty past the end, so the wait_group counts stay aligned
+  }
+};
+
+template <int FMT, int R, int S>
+__host__ __device__ constexpr size_t pipe_ring_bytes(int nw) {
+  return size_t(nw) * S * R * Pipe<FMT>::RB;
+}
+
+// Ring bytes of one warp: SLICE when given (a fixed per-warp slice shared by
+// GEMVs of several formats), else exactly S tiles of R rows.
+template <int FMT, int R, int S, int SLICE>
+__host__ __device__ constexpr size_t pipe_slice() {
+  return SLICE ? size_t(SLICE) : size_t(S) * R * Pipe<FMT>::RB;
+}
+
+// First S-1 tiles of the calling warp.  Reads only weights, so it may run
+// before the producer of x has finished, and (with per-warp slices) while
+// other warps of the CTA still work on an earlier GEMV.
+template <int FMT, int R, int S, int NW, int SLICE = 0>
+__device__ __forceinline__ void pipe_prologue(const GemvArgs& a, int64_t nrows, int cta, int ncta, uint8_t* ring) {
+  static_assert(SLICE == 0 || size_t(S) * R * Pipe<FMT>::RB <= size_t(SLICE), "ring slice too small");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const WarpTiles w = warp_tiles(nrows, R, int(a.ncols / 1024), warp, NW, cta, ncta);
+  const uint32_t wring_s = smem_addr(ring + size_t(warp) * pipe_slice<FMT, R, S, SLICE>());
+  PipeCursor<FMT, R, S> c;
+  c.init(w, int(a.ncols / 1024));
+#pragma unroll 1
+  for (int t = 0; t < S - 1; t++) c.template step<true>(a, nrows, lane, wring_s);
+}
+
+// Stages the 32-column blocks of 1024-column tile k of x (the window starting at
+// x) as 16-bit fixed point: lane u of the calling warp owns block u, so every
+// block is converted the same way whichever warp or kernel stages it.  Per
+// block: sx = max|x|/32512, t = round(x/sx) split as 256 h + l, the sums T0, T1
+// of t over elements 0..15 and 16..31, and the sum of squares in element order.
+template <int FMT>
+__device__ __forceinline__ void stage_tile(const float* x, int k, uint8_t* xq) {
+  using P = Pipe<FMT>;
+  const int lane = threadIdx.x & 31;
+  const int blk = k * 32 + lane;
+  const float4* src = reinterpret_cast<const float4*>(x + size_t(blk) * 32);
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    const float4 f = __ldcg(src + i);
+    v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+  }
+  float amax = 0.f, sq = __fmul_rn(v[0], v[0]);
+#pragma unroll
+  for (int j = 0; j < 32; j++) amax = fmaxf(amax, fabsf(v[j]));
+#pragma unroll
+  for (int j = 1; j < 32; j++) sq = __fmaf_rn(v[j], v[j], sq);
+  const float inv = amax > 0.f ? 32512.0f / amax : 0.f;
+  uint32_t hw[8] = {0, 0, 0, 0, 0, 0, 0, 0}, lw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  int t0 = 0, t1 = 0;
+#pragma unroll
+  for (int j = 0; j < 32; j++) {
+    int t = __float2int_rn(v[j] * inv);
+    t = max(-32512, min(32512, t));
+    const int h = (t + 128) >> 8;
+    if (j < 16) t0 += t; else t1 += t;
+    const int b = P::xbyte(j);
+    hw[b >> 2] |= uint32_t(uint8_t(int8_t(h))) << (8 * (b & 3));
+    lw[b >> 2] |= uint32_t(uint8_t(int8_t(t - 256 * h))) << (8 * (b & 3));
+  }
+  uint4* dst = reinterpret_cast<uint4*>(xq + size_t(blk) * kXUnit);
+  dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+  dst[2] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  dst[3] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+  dst[4] = make_uint4(__float_as_uint(amax / 32512.0f), uint32_t(t0), uint32_t(t1), __float_as_uint(sq));
+}
+
+// RMSNorm factor rsqrt(mean(x^2) + eps) from the staged per-block squares,
+// summed by one warp's lanes in a fixed order (1 without norm).
+__device__ __forceinline__ float x_scale(const GemvArgs& a, const uint8_t* xq) {
+  if (!a.norm) return 1.0f;
+  const int lane = threadIdx.x & 31;
+  const int units = int(a.ncols / 32);
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  for (int b = lane; b < units; b += 128) {
+    s0 = __fadd_rn(s0, *reinterpret_cast<const float*>(xq + size_t(b) * kXUnit + 76));
+    if (b + 32 < units) s1 = __fadd_rn(s1, *reinterpret_cast<const float*>(xq + size_t(b + 32) * kXUnit + 76));
+    if (b + 64 < units) s2 = __fadd_rn(s2, *reinterpret_cast<const float*>(xq + size_t(b + 64) * kXUnit + 76));
+    if (b + 96 < units) s3 = __fadd_rn(s3, *reinterpret_cast<const float*>(xq + size_t(b + 96) * kXUnit + 76));
+  }
+  float t = __fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3));
+#pragma unroll
+  for (int o = 16; o; o >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, o));
+  return rsqrtf(t / float(a.ncols) + a.eps);
+}
+
+// Whole window staged up front by the CTA's NW warps (tile k by warp k % NW).
+template <int FMT, int NW>
+__device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xq) {
+  const int warp = threadIdx.x >> 5, kt = int(a.ncols / 1024);
+  for (int k = warp; k < kt; k += NW) stage_tile<FMT>(a.x + a.col0, k, xq);
+  __syncthreads();
+}
+
+// Hooks of the GEMV body for a caller that staged all of x before the loop.
+struct StagedHooks {
+  static constexpr bool kAllStaged = true;
+  template <int FMT>
+  __device__ __forceinline__ void tile(const GemvArgs&, uint8_t*, int) {}
+  __device__ __forceinline__ void group_done(const GemvArgs&, int64_t, int) {}
+};
+
+// The GEMV of this CTA's share after its prologue: the tile loop (resuming the
+// copy cursor S-1 tiles in), row-group epilogues and, for EPI_LOGITS, the CTA's
+// top-2 summary in a.epi.top2[cta].  With StagedHooks x is already staged and
+// `scale` holds the RMS factor; otherwise the hooks stage tile k before its
+// first use (H::tile) and the factor is formed at the first epilogue, and each
+// finished row group is reported (H::group_done).  Every thread of the CTA must
+// call it (EPI_LOGITS ends with a CTA barrier).
+template <int FMT, int R, int S, int EPI, int NW, int SLICE, class H>
+__device__ __forceinline__ void pipe_loop(const GemvArgs& a, int64_t nrows, int cta, int ncta, uint8_t* xq,
+                                          uint8_t* ring, float scale, H& hooks) {
+  using P = Pipe<FMT>;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int kiters = int(a.ncols / 1024);
+  const WarpTiles w = warp_tiles(nrows, R, kiters, warp, NW, cta, ncta);
+  uint8_t* wring = ring + size_t(warp) * pipe_slice<FMT, R, S, SLICE>();
+  const uint32_t wring_s = smem_addr(wring);
+  PipeCursor<FMT, R, S> cur;
+  cur.init(w, kiters);
+#pragma unroll 1
+  for (int t = 0; t < S - 1; t++) cur.template step<false>(a, nrows, lane, wring_s);
 
   float best = -INFINITY, second = -INFINITY;
   int best_i = 0x7fffffff;
   float acc[R];
 #pragma unroll
   for (int r = 0; r < R; r++) acc[r] = 0.f;
+  int known = H::kAllStaged ? kiters : 0;   // tiles [0, known) are staged
+  bool have_scale = H::kAllStaged;
 
-  // the next kernel may start its own weight prefetch on SMs this grid frees;
-  // it waits for this grid to finish before it reads anything this grid writes
-  asm volatile("griddepcontrol.launch_dependents;");
-
-  int64_t c_grp = g0;
+  int64_t c_grp = w.g0;
   int c_it = 0, c_slot = 0;
   int nlive = int(nrows - c_grp * R < R ? nrows - c_grp * R : R);
-  for (int64_t t = 0; t < ntiles; t++) {
+  for (int64_t t = 0; t < w.ntiles; t++) {
     cp_wait<S - 2>();     // this lane's copies of the tile have landed
     __syncwarp();         // ... and every lane's (scales are copied by a few lanes); the previous slot is free
-    issue_next();
+    cur.template step<true>(a, nrows, lane, wring_s);
+    if (!H::kAllStaged && c_it >= known) {
+      hooks.template tile<FMT>(a, xq, c_it);
+      known = c_it + 1;
+    }
     XBlock xb;
     load_xblock(xq + size_t(c_it * 32 + lane) * kXUnit, xb);
     const uint8_t* blk = wring + c_slot * R * P::RB;
 #pragma unroll
     for (int r = 0; r < R; r++)
-      if (r < nlive) acc[r] += P::dot(blk + r * P::RB, lane, xb);
+      if (r < nlive) acc[r] = __fadd_rn(acc[r], P::dot(blk + r * P::RB, lane, xb));
     if (++c_slot == S) c_slot = 0;
     if (++c_it < kiters) continue;
 
@@ -425,13 +495,46 @@ __global__ void __launch_bounds__(kPipeWarps * 32) k_gemv_pipe(const __grid_cons
     float kk = warp_reduce_rows<R>(acc, lane);
 #pragma unroll
     for (int r = 0; r < R; r++) acc[r] = 0.f;
-    kk *= scale;
+    if (!have_scale) {
+      scale = x_scale(a, xq);
+      have_scale = true;
+    }
+    kk = __fmul_rn(kk, scale);
     epilogue<R, EPI>(a, c_grp, nrows, lane, kk, best, best_i, second);
-    c_grp += stride;
+    hooks.group_done(a, c_grp, nlive);
+    c_grp += w.stride;
     nlive = int(nrows - c_grp * R < R ? nrows - c_grp * R : R);
   }
   cp_wait<0>();
-  if (EPI == EPI_LOGITS) cta_top2<kPipeWarps>(a, best, best_i, second);
+  __syncwarp();
+  if (EPI == EPI_LOGITS) cta_top2<NW>(a, cta, best, best_i, second);
+}
+
+// The per-launch body: stage all of x, then the loop.  TRIGGER: signal
+// programmatic dependents after staging.
+template <int FMT, int R, int S, int EPI, int NW, bool TRIGGER, int SLICE = 0>
+__device__ __forceinline__ void pipe_body(const GemvArgs& a, int64_t nrows, int cta, int ncta, uint8_t* xq,
+                                          uint8_t* ring) {
+  stage_x<FMT, NW>(a, xq);
+  const float scale = x_scale(a, xq);
+  if (TRIGGER) {
+    // the next kernel may start its own weight prefetch on SMs this grid frees;
+    // it waits for this grid to finish before it reads anything this grid writes
+    asm volatile("griddepcontrol.launch_dependents;");
+  }
+  StagedHooks h;
+  pipe_loop<FMT, R, S, EPI, NW, SLICE>(a, nrows, cta, ncta, xq, ring, scale, h);
+}
+
+template <int FMT, int R, int S, int EPI>
+__global__ void __launch_bounds__(kPipeWarps * 32) k_gemv_pipe(const __grid_constant__ GemvArgs a,
+                                                              const int64_t nrows) {
+  extern __shared__ float4 smem4[];
+  uint8_t* xq = reinterpret_cast<uint8_t*>(smem4);
+  uint8_t* ring = xq + size_t(a.ncols / 32) * kXUnit;
+  pipe_prologue<FMT, R, S, kPipeWarps>(a, nrows, blockIdx.x, gridDim.x, ring);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pipe_body<FMT, R, S, EPI, kPipeWarps, true>(a, nrows, blockIdx.x, gridDim.x, xq, ring);
 }
 
 inline size_t pipe_x_bytes(int64_t cols) { return size_t(cols / 32) * kXUnit; }
@@ -469,7 +572,12 @@ cudaError_t launch_gemv_pipe_t(const GemvArgs& a, cudaStream_t s, bool pdl, int*
     s_occ = occ;
     s_occ_smem = smem;
   }
-  const int64_t grid = one_wave_grid(s_sms, s_occ, (nrows + R - 1) / R, kPipeWarps, a.max_grid);
+  // one wave; groups are spread warp-major over all CTAs (see warp_tiles)
+  int64_t grid = int64_t(s_sms) * s_occ;
+  const int64_t groups = (nrows + R - 1) / R;
+  if (grid > groups) grid = groups;
+  if (grid > a.max_grid) grid = a.max_grid;
+  if (grid < 1) grid = 1;
   if (grid_used) *grid_used = int(grid);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid));

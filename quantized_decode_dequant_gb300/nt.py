@@ -56,7 +56,7 @@ class nt_stats(C.Structure):
 
 class nt_kernel_times(C.Structure):
     _fields_ = [("launches", C.c_int64 * 3), ("ms", C.c_double * 3), ("bytes", C.c_double * 3),
-                ("step_ms", C.c_double)]
+                ("step_ms", C.c_double), ("kernel_launches", C.c_int64)]
 
 
 _lib = None

@@ -110,7 +110,8 @@ def test_device_loop_matches_host_loop_and_profile(nt, W):
         nt.nt_kv_reset(b)
         kt = nt.nt_profile_steps(b, tok, 3)
         assert kt.launches[nt.KC_GEMV] == 3 * (4 * W.TINY["n_layers"] + 1)
-        assert kt.launches[nt.KC_ATTN] == 3 * 2 * W.TINY["n_layers"]
+        assert kt.launches[nt.KC_ATTN] == 3 * W.TINY["n_layers"]
+        assert kt.kernel_launches == 3 * (5 * W.TINY["n_layers"] + 3)
         assert kt.ms[nt.KC_GEMV] > 0 and kt.step_ms > 0
         np.testing.assert_array_equal(nt.nt_get_tokens(b, 0, 3), seq[:3])
     finally:
