@@ -12,11 +12,28 @@ int64_t gemv_logical_rows(const GemvArgs& a) {
   return n;
 }
 
-// Chooses the kernel and its shape: the shared-memory pipeline when the column
-// count allows whole aligned scale copies, with as many ring stages as the
-// shared memory left after x holds (at most 8); matrices too wide for x and a
-// ring in one CTA, with a linear epilogue, are split into column windows that
-// successive launches accumulate.  Otherwise the register-path kernel.
+// CTAs per SM the 8-warp layout is sized for (its x staging and ring split the
+// SM's shared memory evenly); NT_GEMV_CTAS_PER_SM (1..4) overrides.
+static int pipe_ctas_per_sm() {
+  static const int v = [] {
+    const char* e = getenv("NT_GEMV_CTAS_PER_SM");
+    const int n = e ? atoi(e) : 2;
+    return n >= 1 && n <= 4 ? n : 2;
+  }();
+  return v;
+}
+
+// Layout of the pipeline: 0 automatic, 8 (8-warp CTAs) or 16 (one 16-warp CTA
+// per SM), from NT_GEMV_WARPS.
+static int pipe_layout() {
+  static const int v = [] {
+    const char* e = getenv("NT_GEMV_WARPS");
+    const int n = e ? atoi(e) : 0;
+    return n == 8 || n == 16 ? n : 0;
+  }();
+  return v;
+}
+
 cudaError_t launch_gemv(const GemvArgs& a_in, int epi, cudaStream_t s, bool pdl, int* grid_used) {
   GemvArgs a = a_in;
   const int64_t cols = a.seg[0].cols;
@@ -35,21 +52,38 @@ cudaError_t launch_gemv(const GemvArgs& a_in, int epi, cudaStream_t s, bool pdl,
       while (pipe_x_bytes(cols / parts) > 140 * 1024 && (cols / parts) % (2 * align) == 0) parts *= 2;
     const int64_t w = cols / parts;
     const size_t xb = pipe_x_bytes(w);
+    const size_t target = size_t(kPipeSmPerSm) / size_t(pipe_ctas_per_sm()) - 2048;
     // four rows per warp share each x read, but only if the ring still holds at least
-    // four stages (three tiles in flight) in half an SM's shared memory
-    if (R == 4 && xb < size_t(kPipeSmemTarget) &&
-        (size_t(kPipeSmemTarget) - xb) / (size_t(kPipeWarps) * 4 * pipe_row_bytes(fmt)) < 4)
-      R = 2;
-    const size_t ring_stage = size_t(kPipeWarps) * R * pipe_row_bytes(fmt);
-    // ring depth: what fits beside x in half an SM's shared memory (two CTAs per SM),
-    // else what fits in the whole of it
-    size_t budget = xb < size_t(kPipeSmemTarget) ? size_t(kPipeSmemTarget) - xb : 0;
+    // four stages (three tiles in flight)
+    if (R == 4 && xb < target && (target - xb) / (size_t(8) * 4 * pipe_row_bytes(fmt)) < 4) R = 2;
+    const size_t ring_stage = size_t(8) * R * pipe_row_bytes(fmt);
+    // ring depth: what fits beside x at the chosen CTAs per SM, else in a whole SM
+    size_t budget = xb < target ? target - xb : 0;
     int S = int(budget / ring_stage);
     if (S < 2) {
       budget = xb < size_t(kPipeMaxSmem) ? size_t(kPipeMaxSmem) - xb : 0;
       S = int(budget / ring_stage);
     }
-    if (S > 8) S = 8;
+    // rounded down to the instantiated depths (see launch_gemv_pipe_fmt)
+    if (R == 4) S = S >= 4 ? 4 : S;
+    else S = S >= 8 ? 8 : (S >= 6 ? 6 : S);
+    // the 16-warp layout stages x once per SM and gives the ring the rest of it
+    const size_t ring16 = xb < size_t(kPipeMaxSmem) ? size_t(kPipeMaxSmem) - xb : 0;
+    int S16 = int(ring16 / (size_t(16) * 2 * pipe_row_bytes(fmt)));
+    S16 = S16 >= 6 ? 6 : (S16 >= 4 ? 4 : S16);
+    int NW = 8;
+    if (pipe_layout() == 16 && S16 >= 3) {
+      NW = 16;
+      R = 2;
+      S = S16;
+    } else if (pipe_layout() == 0 && S16 >= 3 && !(R == 4 && (fmt == NT_Q4_0 || fmt == NT_Q4_K))) {
+      // measured on GB300: one 16-warp CTA per SM (x staged once, the deeper ring) is
+      // faster for every shape except 4-bit formats with enough rows for four rows
+      // per warp, where the two 8-warp CTAs share each x read over four rows
+      NW = 16;
+      R = 2;
+      S = S16;
+    }
     if (S >= 2) {
       for (int p = 0; p < parts; p++) {
         a.col0 = p * w;
@@ -57,10 +91,10 @@ cudaError_t launch_gemv(const GemvArgs& a_in, int epi, cudaStream_t s, bool pdl,
         const int e_p = p == 0 ? epi : EPI_ADD;
         cudaError_t e;
         switch (fmt) {
-          case NT_Q8_0: e = launch_gemv_pipe_q8_0(a, e_p, R, S, s, pdl, grid_used); break;
-          case NT_Q4_0: e = launch_gemv_pipe_q4_0(a, e_p, R, S, s, pdl, grid_used); break;
-          case NT_Q4_K: e = launch_gemv_pipe_q4_k(a, e_p, R, S, s, pdl, grid_used); break;
-          case NT_Q6_K: e = launch_gemv_pipe_q6_k(a, e_p, R, S, s, pdl, grid_used); break;
+          case NT_Q8_0: e = launch_gemv_pipe_q8_0(a, e_p, R, S, NW, s, pdl, grid_used); break;
+          case NT_Q4_0: e = launch_gemv_pipe_q4_0(a, e_p, R, S, NW, s, pdl, grid_used); break;
+          case NT_Q4_K: e = launch_gemv_pipe_q4_k(a, e_p, R, S, NW, s, pdl, grid_used); break;
+          case NT_Q6_K: e = launch_gemv_pipe_q6_k(a, e_p, R, S, NW, s, pdl, grid_used); break;
           default: e = cudaErrorInvalidValue;
         }
         if (e != cudaSuccess) return e;

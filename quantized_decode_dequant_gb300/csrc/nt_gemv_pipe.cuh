@@ -42,7 +42,7 @@ namespace nt {
 
 constexpr int kPipeWarps = 8;                 // 256 threads per CTA
 constexpr int kPipeMaxSmem = 221 * 1024;      // dynamic shared memory a CTA may ask for
-constexpr int kPipeSmemTarget = 110 * 1024;   // per CTA, so two CTAs fit on an SM
+constexpr int kPipeSmPerSm = 228 * 1024;      // shared memory of an SM (each resident CTA also reserves 1 KB)
 constexpr int kXUnit = 80;                    // staged x per 32 columns: h[32] | l[32] | sx, T0, T1, sum of squares
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -108,7 +108,7 @@ template <> struct Pipe<NT_Q8_0> {
   static constexpr int CB = 32, RB = 32 * 32 + 64;
   __device__ static int xbyte(int c) { return c; }   // natural order
   // copy plan per row: code bytes per tile, then scale pieces (source, smem offset, bytes per tile, size)
-  static constexpr int CODE_STRIDE = 1024, NPT = 4;
+  static constexpr int CODE_STRIDE = 1024, NPA = 4, NPB = 0;
   __device__ static const uint8_t* code_base(const QMat& m, int64_t e_row) { return m.q + e_row; }
   __device__ static void piece(const QMat& m, int64_t e_row, int i, const uint8_t*& src, int& off, int& stride,
                                int& size) {
@@ -131,7 +131,7 @@ __device__ __forceinline__ int nibble_xbyte(int c) { return (c & ~7) + ((c & 1) 
 template <> struct Pipe<NT_Q4_0> {
   static constexpr int CB = 16, RB = 32 * 16 + 64;
   __device__ static int xbyte(int c) { return nibble_xbyte(c); }
-  static constexpr int CODE_STRIDE = 512, NPT = 4;
+  static constexpr int CODE_STRIDE = 512, NPA = 4, NPB = 0;
   __device__ static const uint8_t* code_base(const QMat& m, int64_t e_row) { return m.q + (e_row >> 1); }
   __device__ static void piece(const QMat& m, int64_t e_row, int i, const uint8_t*& src, int& off, int& stride,
                                int& size) {
@@ -151,7 +151,7 @@ template <> struct Pipe<NT_Q4_0> {
 template <> struct Pipe<NT_Q4_K> {
   static constexpr int CB = 16, RB = 32 * 16 + 64;
   __device__ static int xbyte(int c) { return nibble_xbyte(c); }
-  static constexpr int CODE_STRIDE = 512, NPT = 4;
+  static constexpr int CODE_STRIDE = 512, NPA = 4, NPB = 0;
   __device__ static const uint8_t* code_base(const QMat& m, int64_t e_row) { return m.q + (e_row >> 1); }
   __device__ static void piece(const QMat& m, int64_t e_row, int i, const uint8_t*& src, int& off, int& stride,
                                int& size) {
@@ -180,8 +180,8 @@ template <> struct Pipe<NT_Q4_K> {
 template <> struct Pipe<NT_Q6_K> {
   static constexpr int CB = 16, RB = 32 * 16 + 256 + 64 + 16;
   __device__ static int xbyte(int c) { return nibble_xbyte(c); }
-  // 16 pieces of high-bit words, 4 of sub-block scales, 2 four-byte pieces of d
-  static constexpr int CODE_STRIDE = 512, NPT = 22;
+  // 16 pieces of high-bit words and 4 of sub-block scales (16 bytes), 2 four-byte pieces of d
+  static constexpr int CODE_STRIDE = 512, NPA = 20, NPB = 2;
   __device__ static const uint8_t* code_base(const QMat& m, int64_t e_row) { return m.q + (e_row >> 1); }
   __device__ static void piece(const QMat& m, int64_t e_row, int i, const uint8_t*& src, int& off, int& stride,
                                int& size) {
@@ -222,43 +222,85 @@ template <> struct Pipe<NT_Q6_K> {
   }
 };
 
-// This lane's share of the copies of one row group, set up once per group:
-// its code vector of each row, and up to NA scale pieces.  Tile it of the
-// group then copies from (source + it * stride).
-template <int FMT, int R>
-struct GroupCopies {
-  static constexpr int NA = (R * Pipe<FMT>::NPT + 31) / 32;
-  const uint8_t* code[R];
-  const uint8_t* src[NA];
-  int off[NA], stride[NA], size[NA];
-  int nlive;
-};
+__device__ __forceinline__ void cp16z(uint32_t dst, const void* src, uint32_t n) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
 
-template <int FMT, int R>
-__device__ __forceinline__ void group_copies(const GemvArgs& a, int64_t grp, int64_t nrows, int lane,
-                                             GroupCopies<FMT, R>& g) {
+// Tiles of one warp: its row groups g0, g0 + stride, ... (g0 = warp * ncta + cta,
+// so consecutive groups land on different CTAs and every SM gets an equal
+// share), each in kiters column tiles.
+struct WarpTiles {
+  int64_t g0, stride;
+  int ntiles;
+};
+__device__ __forceinline__ WarpTiles warp_tiles(int64_t nrows, int R, int kiters, int warp, int nw, int cta,
+                                                int ncta) {
+  WarpTiles w;
+  const int64_t ngroups = (nrows + R - 1) / R;
+  w.g0 = int64_t(warp) * ncta + cta;
+  w.stride = int64_t(ncta) * nw;
+  w.ntiles = w.g0 < ngroups ? int((ngroups - 1 - w.g0) / w.stride + 1) * kiters : 0;
+  return w;
+}
+
+// Copy cursor of one warp over its tiles.  Every lane issues the same copies
+// for every tile, so there are no divergent branches: its 16 (or 32) code bytes
+// of each of the R rows (a row past the matrix copies zero bytes, src-size 0,
+// from a valid address, so its products are zero) and its share of the rows'
+// scale pieces (16-byte pieces, and 4-byte ones for Q6_K's d; a lane without a
+// piece of its own repeats one of row 0's).  Sources advance by a fixed stride
+// per tile; the per-lane plan is rebuilt at each new row group.
+template <int FMT, int R, int S>
+struct PipeCursor {
   using P = Pipe<FMT>;
-  g.nlive = int(nrows - grp * R < R ? nrows - grp * R : R);
-  int seg[R];
-  int64_t e[R];
-#pragma unroll
-  for (int r = 0; r < R; r++) {
-    int sg = 0;
-    int64_t lr = 0;
-    if (r < g.nlive) map_row(a, grp * R + r, sg, lr);
-    seg[r] = sg;
-    e[r] = lr * a.seg[0].cols + a.col0;
-    g.code[r] = P::code_base(a.seg[sg], e[r]) + lane * P::CB;
+  static constexpr int NA = (R * P::NPA + 31) / 32;
+  static constexpr int NB = P::NPB ? (R * P::NPB + 31) / 32 : 1;
+  const uint8_t* code[R];
+  uint32_t csz[R];
+  const uint8_t* asrc[NA];
+  uint32_t aoff[NA];
+  int astr[NA];
+  const uint8_t* bsrc[NB];
+  uint32_t boff[NB];
+  int bstr[NB];
+  int64_t grp, stride;
+  int left, it, kiters;
+  uint32_t dst, ring0, ring_end;
+
+  __device__ __forceinline__ void init(const WarpTiles& w, int kiters_, uint32_t wring_s) {
+    grp = w.g0;
+    stride = w.stride;
+    left = w.ntiles;
+    it = 0;
+    kiters = kiters_;
+    ring0 = dst = wring_s;
+    ring_end = wring_s + uint32_t(S * R * P::RB);
   }
+
+  __device__ __forceinline__ void setup(const GemvArgs& a, int64_t nrows, int lane) {
+    const int nlive = int(nrows - grp * R < R ? nrows - grp * R : R);
+    int seg[R];
+    int64_t e[R];
 #pragma unroll
-  for (int k = 0; k < GroupCopies<FMT, R>::NA; k++) {
-    const int p = lane + 32 * k;
-    const int r = p / P::NPT, i = p - (p / P::NPT) * P::NPT;
-    g.size[k] = 0;
-    g.src[k] = nullptr;
-    g.off[k] = 0;
-    g.stride[k] = 0;
-    if (p < R * P::NPT && r < g.nlive) {
+    for (int r = 0; r < R; r++) {
+      int sg = 0;
+      int64_t lr = 0;
+      map_row(a, grp * R + (r < nlive ? r : 0), sg, lr);
+      seg[r] = sg;
+      e[r] = lr * a.seg[0].cols + a.col0;
+      code[r] = P::code_base(a.seg[sg], e[r]) + lane * P::CB;
+      csz[r] = r < nlive ? 16u : 0u;
+    }
+    // piece slot k of this lane: piece p = lane + 32k of the group's R rows; a slot
+    // past the live pieces repeats piece p mod NP of row 0 (same bytes to the same place)
+#pragma unroll
+    for (int k = 0; k < NA; k++) {
+      const int p = lane + 32 * k;
+      int r = p / P::NPA, i = p - r * P::NPA;
+      if (!(p < R * P::NPA && r < nlive)) {
+        r = 0;
+        i = p % P::NPA;
+      }
       int sg = seg[0];
       int64_t er = e[0];
 #pragma unroll
@@ -267,66 +309,70 @@ __device__ __forceinline__ void group_copies(const GemvArgs& a, int64_t grp, int
           sg = seg[rr];
           er = e[rr];
         }
-      P::piece(a.seg[sg], er, i, g.src[k], g.off[k], g.stride[k], g.size[k]);
-      g.off[k] += r * P::RB;
+      const uint8_t* src;
+      int off, str, size;
+      P::piece(a.seg[sg], er, i, src, off, str, size);
+      asrc[k] = src;
+      aoff[k] = uint32_t(off + r * P::RB);
+      astr[k] = str;
+    }
+    if (P::NPB) {
+      constexpr int npb = P::NPB ? P::NPB : 1;
+#pragma unroll
+      for (int k = 0; k < NB; k++) {
+        const int p = lane + 32 * k;
+        int r = p / npb, i = p - r * npb;
+        if (!(p < R * P::NPB && r < nlive)) {
+          r = 0;
+          i = p % npb;
+        }
+        int sg = seg[0];
+        int64_t er = e[0];
+#pragma unroll
+        for (int rr = 1; rr < R; rr++)
+          if (r == rr) {
+            sg = seg[rr];
+            er = e[rr];
+          }
+        const uint8_t* src;
+        int off, str, size;
+        P::piece(a.seg[sg], er, P::NPA + i, src, off, str, size);
+        bsrc[k] = src;
+        boff[k] = uint32_t(off + r * P::RB);
+        bstr[k] = str;
+      }
     }
   }
-}
 
-// Tiles of one warp: its row groups g0, g0 + stride, ... (g0 = warp * ncta + cta,
-// so consecutive groups land on different CTAs and every SM gets an equal
-// share), each in kiters column tiles.
-struct WarpTiles {
-  int64_t g0, stride, ntiles;
-};
-__device__ __forceinline__ WarpTiles warp_tiles(int64_t nrows, int R, int kiters, int warp, int nw, int cta,
-                                                int ncta) {
-  WarpTiles w;
-  const int64_t ngroups = (nrows + R - 1) / R;
-  w.g0 = int64_t(warp) * ncta + cta;
-  w.stride = int64_t(ncta) * nw;
-  w.ntiles = w.g0 < ngroups ? ((ngroups - 1 - w.g0) / w.stride + 1) * kiters : 0;
-  return w;
-}
-
-// Copy cursor of one warp over its tiles: issues (or, to resume after a
-// prologue issued elsewhere, only steps over) the cp.async copies of one tile.
-template <int FMT, int R, int S>
-struct PipeCursor {
-  int64_t grp, left, stride;
-  int it, slot, kiters;
-  GroupCopies<FMT, R> gc;
-
-  __device__ __forceinline__ void init(const WarpTiles& w, int kiters_) {
-    grp = w.g0;
-    left = w.ntiles;
-    stride = w.stride;
-    it = 0;
-    slot = 0;
-    kiters = kiters_;
-  }
   template <bool ISSUE>
-  __device__ __forceinline__ void step(const GemvArgs& a, int64_t nrows, int lane, uint32_t wring_s) {
-    using P = Pipe<FMT>;
+  __device__ __forceinline__ void step(const GemvArgs& a, int64_t nrows, int lane) {
     if (left > 0) {
-      if (it == 0) group_copies<FMT, R>(a, grp, nrows, lane, gc);
+      if (it == 0) setup(a, nrows, lane);
       if (ISSUE) {
-        const uint32_t dst = wring_s + uint32_t(slot * R * P::RB);
-        const int64_t ct = int64_t(it) * P::CODE_STRIDE;
 #pragma unroll
-        for (int r = 0; r < R; r++)
-          if (r < gc.nlive) {
-            cp16(dst + r * P::RB + lane * P::CB, gc.code[r] + ct);
-            if (P::CB == 32) cp16(dst + r * P::RB + lane * P::CB + 16, gc.code[r] + ct + 16);
-          }
+        for (int r = 0; r < R; r++) {
+          const uint32_t d = dst + uint32_t(r * P::RB + lane * P::CB);
+          cp16z(d, code[r], csz[r]);
+          if (P::CB == 32) cp16z(d + 16, code[r] + 16, csz[r]);
+        }
 #pragma unroll
-        for (int k = 0; k < GroupCopies<FMT, R>::NA; k++) {
-          if (gc.size[k] == 16) cp16(dst + gc.off[k], gc.src[k] + int64_t(it) * gc.stride[k]);
-          else if (gc.size[k] == 4) cp4(dst + gc.off[k], gc.src[k] + int64_t(it) * gc.stride[k]);
+        for (int k = 0; k < NA; k++) cp16(dst + aoff[k], asrc[k]);
+        if (P::NPB) {
+#pragma unroll
+          for (int k = 0; k < NB; k++) cp4(dst + boff[k], bsrc[k]);
         }
       }
+#pragma unroll
+      for (int r = 0; r < R; r++) code[r] += P::CODE_STRIDE;
+#pragma unroll
+      for (int k = 0; k < NA; k++) asrc[k] += astr[k];
+      if (P::NPB) {
+#pragma unroll
+        for (int k = 0; k < NB; k++) bsrc[k] += bstr[k];
+      }
+      dst += uint32_t(R * P::RB);
+      if (dst == ring_end) dst = ring0;
       --left;
-      if (++slot == S) slot = 0;
       if (++it == kiters) {
         it = 0;
         grp += stride;
@@ -358,9 +404,9 @@ __device__ __forceinline__ void pipe_prologue(const GemvArgs& a, int64_t nrows, 
   const WarpTiles w = warp_tiles(nrows, R, int(a.ncols / 1024), warp, NW, cta, ncta);
   const uint32_t wring_s = smem_addr(ring + size_t(warp) * pipe_slice<FMT, R, S, SLICE>());
   PipeCursor<FMT, R, S> c;
-  c.init(w, int(a.ncols / 1024));
+  c.init(w, int(a.ncols / 1024), wring_s);
 #pragma unroll 1
-  for (int t = 0; t < S - 1; t++) c.template step<true>(a, nrows, lane, wring_s);
+  for (int t = 0; t < S - 1; t++) c.template step<true>(a, nrows, lane);
 }
 
 // Stages the 32-column blocks of 1024-column tile k of x (the window starting at
@@ -456,11 +502,10 @@ __device__ __forceinline__ void pipe_loop(const GemvArgs& a, int64_t nrows, int 
   const int kiters = int(a.ncols / 1024);
   const WarpTiles w = warp_tiles(nrows, R, kiters, warp, NW, cta, ncta);
   uint8_t* wring = ring + size_t(warp) * pipe_slice<FMT, R, S, SLICE>();
-  const uint32_t wring_s = smem_addr(wring);
   PipeCursor<FMT, R, S> cur;
-  cur.init(w, kiters);
+  cur.init(w, kiters, smem_addr(wring));
 #pragma unroll 1
-  for (int t = 0; t < S - 1; t++) cur.template step<false>(a, nrows, lane, wring_s);
+  for (int t = 0; t < S - 1; t++) cur.template step<false>(a, nrows, lane);
 
   float best = -INFINITY, second = -INFINITY;
   int best_i = 0x7fffffff;
@@ -471,27 +516,31 @@ __device__ __forceinline__ void pipe_loop(const GemvArgs& a, int64_t nrows, int 
   bool have_scale = H::kAllStaged;
 
   int64_t c_grp = w.g0;
-  int c_it = 0, c_slot = 0;
-  int nlive = int(nrows - c_grp * R < R ? nrows - c_grp * R : R);
-  for (int64_t t = 0; t < w.ntiles; t++) {
+  int c_it = 0;
+  const uint8_t* rd = wring;                               // slot of the tile being decoded
+  const uint8_t* const rd_end = wring + S * R * P::RB;
+  const uint8_t* xp = xq + size_t(lane) * kXUnit;          // this lane's x block of the tile
+#pragma unroll 1
+  for (int t = 0; t < w.ntiles; t++) {
     cp_wait<S - 2>();     // this lane's copies of the tile have landed
     __syncwarp();         // ... and every lane's (scales are copied by a few lanes); the previous slot is free
-    cur.template step<true>(a, nrows, lane, wring_s);
+    cur.template step<true>(a, nrows, lane);
     if (!H::kAllStaged && c_it >= known) {
       hooks.template tile<FMT>(a, xq, c_it);
       known = c_it + 1;
     }
     XBlock xb;
-    load_xblock(xq + size_t(c_it * 32 + lane) * kXUnit, xb);
-    const uint8_t* blk = wring + c_slot * R * P::RB;
+    load_xblock(xp, xb);
+    xp += 32 * kXUnit;
 #pragma unroll
-    for (int r = 0; r < R; r++)
-      if (r < nlive) acc[r] = __fadd_rn(acc[r], P::dot(blk + r * P::RB, lane, xb));
-    if (++c_slot == S) c_slot = 0;
+    for (int r = 0; r < R; r++) acc[r] = __fadd_rn(acc[r], P::dot(rd + r * P::RB, lane, xb));   // dead rows read zeros
+    rd += R * P::RB;
+    if (rd == rd_end) rd = wring;
     if (++c_it < kiters) continue;
 
     // ---- row group done: transposed warp reduction, epilogue ----------------
     c_it = 0;
+    xp = xq + size_t(lane) * kXUnit;
     float kk = warp_reduce_rows<R>(acc, lane);
 #pragma unroll
     for (int r = 0; r < R; r++) acc[r] = 0.f;
@@ -501,9 +550,8 @@ __device__ __forceinline__ void pipe_loop(const GemvArgs& a, int64_t nrows, int 
     }
     kk = __fmul_rn(kk, scale);
     epilogue<R, EPI>(a, c_grp, nrows, lane, kk, best, best_i, second);
-    hooks.group_done(a, c_grp, nlive);
+    hooks.group_done(a, c_grp, int(nrows - c_grp * R < R ? nrows - c_grp * R : R));
     c_grp += w.stride;
-    nlive = int(nrows - c_grp * R < R ? nrows - c_grp * R : R);
   }
   cp_wait<0>();
   __syncwarp();
@@ -526,15 +574,14 @@ __device__ __forceinline__ void pipe_body(const GemvArgs& a, int64_t nrows, int 
   pipe_loop<FMT, R, S, EPI, NW, SLICE>(a, nrows, cta, ncta, xq, ring, scale, h);
 }
 
-template <int FMT, int R, int S, int EPI>
-__global__ void __launch_bounds__(kPipeWarps * 32) k_gemv_pipe(const __grid_constant__ GemvArgs a,
-                                                              const int64_t nrows) {
+template <int FMT, int R, int S, int EPI, int NW>
+__global__ void __launch_bounds__(NW * 32) k_gemv_pipe(const __grid_constant__ GemvArgs a, const int64_t nrows) {
   extern __shared__ float4 smem4[];
   uint8_t* xq = reinterpret_cast<uint8_t*>(smem4);
   uint8_t* ring = xq + size_t(a.ncols / 32) * kXUnit;
-  pipe_prologue<FMT, R, S, kPipeWarps>(a, nrows, blockIdx.x, gridDim.x, ring);
+  pipe_prologue<FMT, R, S, NW>(a, nrows, blockIdx.x, gridDim.x, ring);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  pipe_body<FMT, R, S, EPI, kPipeWarps, true>(a, nrows, blockIdx.x, gridDim.x, xq, ring);
+  pipe_body<FMT, R, S, EPI, NW, true>(a, nrows, blockIdx.x, gridDim.x, xq, ring);
 }
 
 inline size_t pipe_x_bytes(int64_t cols) { return size_t(cols / 32) * kXUnit; }
@@ -547,12 +594,12 @@ inline int pipe_row_bytes(int fmt) {
   }
 }
 
-template <int FMT, int R, int S, int EPI>
+template <int FMT, int R, int S, int EPI, int NW>
 cudaError_t launch_gemv_pipe_t(const GemvArgs& a, cudaStream_t s, bool pdl, int* grid_used) {
   const int64_t nrows = gemv_logical_rows(a);
-  const size_t smem = pipe_x_bytes(a.ncols) + size_t(kPipeWarps) * S * R * Pipe<FMT>::RB;
+  const size_t smem = pipe_x_bytes(a.ncols) + size_t(NW) * S * R * Pipe<FMT>::RB;
   if (smem > size_t(kPipeMaxSmem)) return cudaErrorInvalidValue;
-  auto kern = k_gemv_pipe<FMT, R, S, EPI>;
+  auto kern = k_gemv_pipe<FMT, R, S, EPI, NW>;
   static int s_sms = 0;
   static size_t s_occ_smem = ~size_t(0);
   static int s_occ = 0;
@@ -566,22 +613,25 @@ cudaError_t launch_gemv_pipe_t(const GemvArgs& a, cudaStream_t s, bool pdl, int*
   }
   if (s_occ_smem != smem) {
     int occ = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kPipeWarps * 32, smem);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NW * 32, smem);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
     s_occ = occ;
     s_occ_smem = smem;
   }
-  // one wave; groups are spread warp-major over all CTAs (see warp_tiles)
+  // one wave, no more CTAs than the work fills (but at least one per SM while
+  // there are groups for it); groups are spread warp-major over the CTAs
   int64_t grid = int64_t(s_sms) * s_occ;
   const int64_t groups = (nrows + R - 1) / R;
-  if (grid > groups) grid = groups;
+  int64_t want = (groups + NW - 1) / NW;
+  if (want < s_sms) want = groups < s_sms ? groups : s_sms;
+  if (grid > want) grid = want;
   if (grid > a.max_grid) grid = a.max_grid;
   if (grid < 1) grid = 1;
   if (grid_used) *grid_used = int(grid);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid));
-  cfg.blockDim = dim3(unsigned(kPipeWarps * 32));
+  cfg.blockDim = dim3(unsigned(NW * 32));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -592,34 +642,42 @@ cudaError_t launch_gemv_pipe_t(const GemvArgs& a, cudaStream_t s, bool pdl, int*
   return cudaLaunchKernelEx(&cfg, kern, a, nrows);
 }
 
-template <int FMT, int R, int S>
+template <int FMT, int R, int S, int NW>
 cudaError_t launch_gemv_pipe_rs(const GemvArgs& a, int epi, cudaStream_t s, bool pdl, int* grid_used) {
   switch (epi) {
-    case EPI_STORE: return launch_gemv_pipe_t<FMT, R, S, EPI_STORE>(a, s, pdl, grid_used);
-    case EPI_ADD: return launch_gemv_pipe_t<FMT, R, S, EPI_ADD>(a, s, pdl, grid_used);
-    case EPI_QKV: return launch_gemv_pipe_t<FMT, R, S, EPI_QKV>(a, s, pdl, grid_used);
-    case EPI_SWIGLU: return launch_gemv_pipe_t<FMT, R, S, EPI_SWIGLU>(a, s, pdl, grid_used);
-    case EPI_LOGITS: return launch_gemv_pipe_t<FMT, R, S, EPI_LOGITS>(a, s, pdl, grid_used);
+    case EPI_STORE: return launch_gemv_pipe_t<FMT, R, S, EPI_STORE, NW>(a, s, pdl, grid_used);
+    case EPI_ADD: return launch_gemv_pipe_t<FMT, R, S, EPI_ADD, NW>(a, s, pdl, grid_used);
+    case EPI_QKV: return launch_gemv_pipe_t<FMT, R, S, EPI_QKV, NW>(a, s, pdl, grid_used);
+    case EPI_SWIGLU: return launch_gemv_pipe_t<FMT, R, S, EPI_SWIGLU, NW>(a, s, pdl, grid_used);
+    case EPI_LOGITS: return launch_gemv_pipe_t<FMT, R, S, EPI_LOGITS, NW>(a, s, pdl, grid_used);
   }
   return cudaErrorInvalidValue;
 }
 
-// S is rounded down to 2, 4 or 8 ring stages
+// Instantiated shapes: 8 warps per CTA with S in {2, 3, 4, 6, 8} (R = 2) or
+// {2, 4} (R = 4); 16 warps per CTA (one CTA per SM) with S in {3, 4, 6} (R = 2).
+// S is rounded down to the nearest instantiated depth.
 template <int FMT>
-cudaError_t launch_gemv_pipe_fmt(const GemvArgs& a, int epi, int R, int S, cudaStream_t s, bool pdl,
+cudaError_t launch_gemv_pipe_fmt(const GemvArgs& a, int epi, int R, int S, int NW, cudaStream_t s, bool pdl,
                                  int* grid_used) {
-  if (R == 4) {
-    if (S >= 8) return launch_gemv_pipe_rs<FMT, 4, 8>(a, epi, s, pdl, grid_used);
-    if (S >= 4) return launch_gemv_pipe_rs<FMT, 4, 4>(a, epi, s, pdl, grid_used);
-    return launch_gemv_pipe_rs<FMT, 4, 2>(a, epi, s, pdl, grid_used);
+  if (NW == 16) {
+    if (S >= 6) return launch_gemv_pipe_rs<FMT, 2, 6, 16>(a, epi, s, pdl, grid_used);
+    if (S >= 4) return launch_gemv_pipe_rs<FMT, 2, 4, 16>(a, epi, s, pdl, grid_used);
+    return launch_gemv_pipe_rs<FMT, 2, 3, 16>(a, epi, s, pdl, grid_used);
   }
-  if (S >= 8) return launch_gemv_pipe_rs<FMT, 2, 8>(a, epi, s, pdl, grid_used);
-  if (S >= 4) return launch_gemv_pipe_rs<FMT, 2, 4>(a, epi, s, pdl, grid_used);
-  return launch_gemv_pipe_rs<FMT, 2, 2>(a, epi, s, pdl, grid_used);
+  if (R == 4) {
+    if (S >= 4) return launch_gemv_pipe_rs<FMT, 4, 4, 8>(a, epi, s, pdl, grid_used);
+    return launch_gemv_pipe_rs<FMT, 4, 2, 8>(a, epi, s, pdl, grid_used);
+  }
+  if (S >= 8) return launch_gemv_pipe_rs<FMT, 2, 8, 8>(a, epi, s, pdl, grid_used);
+  if (S >= 6) return launch_gemv_pipe_rs<FMT, 2, 6, 8>(a, epi, s, pdl, grid_used);
+  if (S >= 4) return launch_gemv_pipe_rs<FMT, 2, 4, 8>(a, epi, s, pdl, grid_used);
+  if (S >= 3) return launch_gemv_pipe_rs<FMT, 2, 3, 8>(a, epi, s, pdl, grid_used);
+  return launch_gemv_pipe_rs<FMT, 2, 2, 8>(a, epi, s, pdl, grid_used);
 }
 
 #define NT_DECLARE_GEMV_PIPE(NAME) \
-  cudaError_t NAME(const GemvArgs& a, int epi, int R, int S, cudaStream_t s, bool pdl, int* grid_used);
+  cudaError_t NAME(const GemvArgs& a, int epi, int R, int S, int NW, cudaStream_t s, bool pdl, int* grid_used);
 NT_DECLARE_GEMV_PIPE(launch_gemv_pipe_q8_0)
 NT_DECLARE_GEMV_PIPE(launch_gemv_pipe_q4_0)
 NT_DECLARE_GEMV_PIPE(launch_gemv_pipe_q4_k)
