@@ -42,16 +42,24 @@ __global__ void k_embed(const QMat e, const int32_t* __restrict__ d_token, float
   x[i] = dequant_elem(e, tok * e.cols + i);
 }
 
-// One CTA (one attention group) per (kv head, chunk); chunks past the current
-// position have nothing to do.
+// One CTA per (kv head, chunk); chunks past the current position have nothing
+// to do.  Launched as a programmatic dependent of the QKV GEMV: the rows cached
+// by earlier steps (and the position, written by the previous step's argmax)
+// are final before that GEMV starts, so they are copied before waiting for it;
+// q and the current position's K and V only after.
 template <int HD, int G>
 __global__ void __launch_bounds__(kAttnThreads) k_attn(const __grid_constant__ AttnArgs a,
                                                        const int32_t* __restrict__ d_pos) {
   extern __shared__ uint4 smem_u4[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(smem_u4);
   const int n = __ldcg(d_pos) + 1;
   const int used = (n + a.chunk - 1) / a.chunk;
+  // the O projection may start its weight prefetch; it waits for this grid before reading its output
+  asm volatile("griddepcontrol.launch_dependents;");
   if (int(blockIdx.y) >= used) return;
-  attn_item<HD, G>(a, blockIdx.x, blockIdx.y, n, used, reinterpret_cast<uint8_t*>(smem_u4), false);
+  attn_prefetch<HD>(a, blockIdx.x, blockIdx.y, n - 1, sm);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  attn_item<HD, G>(a, blockIdx.x, blockIdx.y, n, used, sm, true);
 }
 
 // Greedy choice over the per-CTA top-2 summaries of the output GEMV (ties to the
@@ -235,25 +243,35 @@ struct Launcher {
 };
 
 template <int HD, int G>
-static cudaError_t launch_attn_t(dim3 grid, cudaStream_t s, const AttnArgs& a, const int32_t* pos) {
+static cudaError_t launch_attn_t(dim3 grid, cudaStream_t s, const AttnArgs& a, const int32_t* pos, bool pdl) {
   auto kern = k_attn<HD, G>;
   const size_t smem = attn_item_smem(HD, G, a.chunk);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
   }
-  kern<<<grid, kAttnThreads, smem, s>>>(a, pos);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a, pos);
 }
 
-static cudaError_t launch_attn(int hd, int G, dim3 grid, cudaStream_t s, const AttnArgs& a, const int32_t* pos) {
+static cudaError_t launch_attn(int hd, int G, dim3 grid, cudaStream_t s, const AttnArgs& a, const int32_t* pos,
+                               bool pdl) {
 #define NT_ATTN_G(HD)                                                  \
   switch (G) {                                                         \
-    case 1: return launch_attn_t<HD, 1>(grid, s, a, pos);              \
-    case 2: return launch_attn_t<HD, 2>(grid, s, a, pos);              \
-    case 4: return launch_attn_t<HD, 4>(grid, s, a, pos);              \
-    case 8: return launch_attn_t<HD, 8>(grid, s, a, pos);              \
-    case 16: return launch_attn_t<HD, 16>(grid, s, a, pos);            \
+    case 1: return launch_attn_t<HD, 1>(grid, s, a, pos, pdl);         \
+    case 2: return launch_attn_t<HD, 2>(grid, s, a, pos, pdl);         \
+    case 4: return launch_attn_t<HD, 4>(grid, s, a, pos, pdl);         \
+    case 8: return launch_attn_t<HD, 8>(grid, s, a, pos, pdl);         \
+    case 16: return launch_attn_t<HD, 16>(grid, s, a, pos, pdl);       \
   }
   if (hd == 128) {
     NT_ATTN_G(128)
@@ -380,7 +398,7 @@ static cudaError_t enqueue_layer(nt_model* m, int l, uint8_t* base, Launcher& L,
     const double by = 2.0 * 2.0 * double(c.n_kv_heads) * n_used * hd + 8.0 * qd;
     dim3 grid(unsigned(c.n_kv_heads), unsigned(m->n_chunks));
     const AttnArgs aa = attn_args(m, l);
-    e = L.run(NT_KC_ATTN, by, [&] { return launch_attn(hd, G, grid, s, aa, d_pos(m)); });
+    e = L.run(NT_KC_ATTN, by, [&] { return launch_attn(hd, G, grid, s, aa, d_pos(m), pdl); });
     if (e) return e;
   }
 
@@ -393,12 +411,12 @@ static cudaError_t enqueue_layer(nt_model* m, int l, uint8_t* base, Launcher& L,
   return cudaSuccess;
 }
 
-static cudaError_t enqueue_head(nt_model* m, Launcher& L) {
+static cudaError_t enqueue_head(nt_model* m, Launcher& L, bool pdl) {
   const nt_config& c = m->c;
   cudaStream_t s = L.s;
   const GemvArgs a = head_gemv(m);
   const double by = gemv_bytes(a, 4.0 * c.vocab);
-  cudaError_t e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(a, EPI_LOGITS, s, false, &m->out_grid); });
+  cudaError_t e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(a, EPI_LOGITS, s, pdl, &m->out_grid); });
   if (e) return e;
   return L.run(NT_KC_OTHER, 0.0, [&] {
     k_argmax<<<1, 256, 0, s>>>(m->top2, m->out_grid, d_pos(m), d_token(m), d_next(m), d_margin(m), m->hist,
@@ -418,7 +436,7 @@ static cudaError_t enqueue_embed(nt_model* m, Launcher& L) {
 static cudaError_t enqueue_resident(nt_model* m, Launcher& L, bool pdl) {
   cudaError_t e = enqueue_embed(m, L);
   for (int l = 0; l < m->c.n_layers && !e; l++) e = enqueue_layer(m, l, m->layers[size_t(l)].dev, L, pdl);
-  if (!e) e = enqueue_head(m, L);
+  if (!e) e = enqueue_head(m, L, pdl);
   return e;
 }
 
@@ -453,7 +471,7 @@ static cudaError_t enqueue_streamed(nt_model* m, Launcher& L) {
       if (l + 2 < nl && (e = issue_copy(l + 2))) return e;
     }
   }
-  return enqueue_head(m, L);
+  return enqueue_head(m, L, false);
 }
 
 static double watchdog_ms() {
