@@ -409,47 +409,57 @@ __device__ __forceinline__ void pipe_prologue(const GemvArgs& a, int64_t nrows, 
   for (int t = 0; t < S - 1; t++) c.template step<true>(a, nrows, lane);
 }
 
-// Stages the 32-column blocks of 1024-column tile k of x (the window starting at
-// x) as 16-bit fixed point: lane u of the calling warp owns block u, so every
-// block is converted the same way whichever warp or kernel stages it.  Per
-// block: sx = max|x|/32512, t = round(x/sx) split as 256 h + l, the sums T0, T1
-// of t over elements 0..15 and 16..31, and the sum of squares in element order.
+// Stages eight 32-column blocks of x (columns [256 p, 256 p + 256) of the
+// window starting at x) as 16-bit fixed point, four lanes of the calling warp
+// per block, eight consecutive elements per lane.  Per block: sx = max|x|/32512,
+// t = round(x/sx) split as 256 h + l, the sums T0, T1 of t over elements 0..15
+// and 16..31, and the sum of squares (each lane's eight in element order, then
+// the four lanes as (l0 + l1) + (l2 + l3)); every kernel stages the same way.
 template <int FMT>
-__device__ __forceinline__ void stage_tile(const float* x, int k, uint8_t* xq) {
+__device__ __forceinline__ void stage_pass(const float* x, int p, uint8_t* xq) {
   using P = Pipe<FMT>;
-  const int lane = threadIdx.x & 31;
-  const int blk = k * 32 + lane;
-  const float4* src = reinterpret_cast<const float4*>(x + size_t(blk) * 32);
-  float v[32];
-#pragma unroll
-  for (int i = 0; i < 8; i++) {
-    const float4 f = __ldcg(src + i);
-    v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
-  }
+  const int lane = threadIdx.x & 31, q = lane & 3;          // q: eighth of the block
+  const int blk = p * 8 + (lane >> 2);
+  const float4* src = reinterpret_cast<const float4*>(x + size_t(blk) * 32 + q * 8);
+  const float4 f0 = __ldcg(src), f1 = __ldcg(src + 1);
+  const float v[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
   float amax = 0.f, sq = __fmul_rn(v[0], v[0]);
 #pragma unroll
-  for (int j = 0; j < 32; j++) amax = fmaxf(amax, fabsf(v[j]));
+  for (int j = 0; j < 8; j++) amax = fmaxf(amax, fabsf(v[j]));
 #pragma unroll
-  for (int j = 1; j < 32; j++) sq = __fmaf_rn(v[j], v[j], sq);
+  for (int j = 1; j < 8; j++) sq = __fmaf_rn(v[j], v[j], sq);
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, 1));   // (l0 + l1), (l2 + l3)
+  sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, 2));   // then their sum
   const float inv = amax > 0.f ? 32512.0f / amax : 0.f;
-  uint32_t hw[8] = {0, 0, 0, 0, 0, 0, 0, 0}, lw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  int t0 = 0, t1 = 0;
+  uint32_t hw[2] = {0, 0}, lw[2] = {0, 0};
+  int ts = 0;
 #pragma unroll
-  for (int j = 0; j < 32; j++) {
-    int t = __float2int_rn(v[j] * inv);
+  for (int j = 0; j < 8; j++) {
+    int t = __float2int_rn(__fmul_rn(v[j], inv));
     t = max(-32512, min(32512, t));
     const int h = (t + 128) >> 8;
-    if (j < 16) t0 += t; else t1 += t;
-    const int b = P::xbyte(j);
+    ts += t;
+    const int b = P::xbyte(j);   // position inside this lane's eight bytes (the 8-group order)
     hw[b >> 2] |= uint32_t(uint8_t(int8_t(h))) << (8 * (b & 3));
     lw[b >> 2] |= uint32_t(uint8_t(int8_t(t - 256 * h))) << (8 * (b & 3));
   }
-  uint4* dst = reinterpret_cast<uint4*>(xq + size_t(blk) * kXUnit);
-  dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-  dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-  dst[2] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-  dst[3] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-  dst[4] = make_uint4(__float_as_uint(amax / 32512.0f), uint32_t(t0), uint32_t(t1), __float_as_uint(sq));
+  const int t01 = ts + __shfl_xor_sync(0xffffffffu, ts, 1);   // lanes q = 0,1: elements 0..15; q = 2,3: 16..31
+  const int t_hi = __shfl_xor_sync(0xffffffffu, t01, 2);
+  uint8_t* dst = xq + size_t(blk) * kXUnit;
+  *reinterpret_cast<uint2*>(dst + q * 8) = make_uint2(hw[0], hw[1]);
+  *reinterpret_cast<uint2*>(dst + 32 + q * 8) = make_uint2(lw[0], lw[1]);
+  if (q == 0)
+    *reinterpret_cast<uint4*>(dst + 64) =
+        make_uint4(__float_as_uint(amax / 32512.0f), uint32_t(t01), uint32_t(t_hi), __float_as_uint(sq));
+}
+
+// Stages 1024-column tile k of x (four passes) by the calling warp.
+template <int FMT>
+__device__ __forceinline__ void stage_tile(const float* x, int k, uint8_t* xq) {
+#pragma unroll
+  for (int i = 0; i < 4; i++) stage_pass<FMT>(x, k * 4 + i, xq);
 }
 
 // RMSNorm factor rsqrt(mean(x^2) + eps) from the staged per-block squares,
@@ -471,11 +481,11 @@ __device__ __forceinline__ float x_scale(const GemvArgs& a, const uint8_t* xq) {
   return rsqrtf(t / float(a.ncols) + a.eps);
 }
 
-// Whole window staged up front by the CTA's NW warps (tile k by warp k % NW).
+// Whole window staged up front by the CTA's NW warps (256-column pass p by warp p % NW).
 template <int FMT, int NW>
 __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xq) {
-  const int warp = threadIdx.x >> 5, kt = int(a.ncols / 1024);
-  for (int k = warp; k < kt; k += NW) stage_tile<FMT>(a.x + a.col0, k, xq);
+  const int warp = threadIdx.x >> 5, np = int(a.ncols / 256);
+  for (int p = warp; p < np; p += NW) stage_pass<FMT>(a.x + a.col0, p, xq);
   __syncthreads();
 }
 
