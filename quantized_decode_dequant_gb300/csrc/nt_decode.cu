@@ -385,11 +385,9 @@ static cudaError_t enqueue_layer(nt_model* m, int l, uint8_t* base, Launcher& L,
   if (!g.v_split) {
     const double by = gemv_bytes(g.qk, 4.0 * qd + 4.0 * kd);
     if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(g.qk, EPI_QKV, s, pdl, nullptr); }))) return e;
-  } else {
-    double by = gemv_bytes(g.qk, 4.0 * qd + 2.0 * kd);
-    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(g.qk, EPI_QKV, s, pdl, nullptr); }))) return e;
-    by = gemv_bytes(g.v, 2.0 * kd);
-    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(g.v, EPI_QKV, s, pdl, nullptr); }))) return e;
+  } else {   // v in its own format: one launch for both where a kernel exists for the pair
+    const double by = gemv_bytes(g.qk, 4.0 * qd + 2.0 * kd) + gemv_bytes(g.v, 2.0 * kd) - 4.0 * c.hidden;
+    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_pair(g.qk, g.v, EPI_QKV, s, pdl); }))) return e;
   }
 
   // split-context GQA attention over positions 0..pos, merged by the last chunk's CTA

@@ -397,16 +397,20 @@ __host__ __device__ constexpr size_t pipe_slice() {
 // First S-1 tiles of the calling warp.  Reads only weights, so it may run
 // before the producer of x has finished, and (with per-warp slices) while
 // other warps of the CTA still work on an earlier GEMV.
-template <int FMT, int R, int S, int NW, int SLICE = 0>
-__device__ __forceinline__ void pipe_prologue(const GemvArgs& a, int64_t nrows, int cta, int ncta, uint8_t* ring) {
+template <int FMT, int R, int S, int SLICE = 0>
+__device__ __forceinline__ void pipe_prologue_w(const GemvArgs& a, int64_t nrows, const WarpTiles& w, uint8_t* ring) {
   static_assert(SLICE == 0 || size_t(S) * R * Pipe<FMT>::RB <= size_t(SLICE), "ring slice too small");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const WarpTiles w = warp_tiles(nrows, R, int(a.ncols / 1024), warp, NW, cta, ncta);
   const uint32_t wring_s = smem_addr(ring + size_t(warp) * pipe_slice<FMT, R, S, SLICE>());
   PipeCursor<FMT, R, S> c;
   c.init(w, int(a.ncols / 1024), wring_s);
 #pragma unroll 1
   for (int t = 0; t < S - 1; t++) c.template step<true>(a, nrows, lane);
+}
+template <int FMT, int R, int S, int NW, int SLICE = 0>
+__device__ __forceinline__ void pipe_prologue(const GemvArgs& a, int64_t nrows, int cta, int ncta, uint8_t* ring) {
+  const WarpTiles w = warp_tiles(nrows, R, int(a.ncols / 1024), threadIdx.x >> 5, NW, cta, ncta);
+  pipe_prologue_w<FMT, R, S, SLICE>(a, nrows, w, ring);
 }
 
 // Stages eight 32-column blocks of x (columns [256 p, 256 p + 256) of the
@@ -505,12 +509,11 @@ struct StagedHooks {
 // finished row group is reported (H::group_done).  Every thread of the CTA must
 // call it (EPI_LOGITS ends with a CTA barrier).
 template <int FMT, int R, int S, int EPI, int NW, int SLICE, class H>
-__device__ __forceinline__ void pipe_loop(const GemvArgs& a, int64_t nrows, int cta, int ncta, uint8_t* xq,
-                                          uint8_t* ring, float scale, H& hooks) {
+__device__ __forceinline__ void pipe_loop_w(const GemvArgs& a, int64_t nrows, const WarpTiles& w, int cta,
+                                            uint8_t* xq, uint8_t* ring, float scale, H& hooks) {
   using P = Pipe<FMT>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int kiters = int(a.ncols / 1024);
-  const WarpTiles w = warp_tiles(nrows, R, kiters, warp, NW, cta, ncta);
   uint8_t* wring = ring + size_t(warp) * pipe_slice<FMT, R, S, SLICE>();
   PipeCursor<FMT, R, S> cur;
   cur.init(w, kiters, smem_addr(wring));
@@ -568,6 +571,13 @@ __device__ __forceinline__ void pipe_loop(const GemvArgs& a, int64_t nrows, int 
   if (EPI == EPI_LOGITS) cta_top2<NW>(a, cta, best, best_i, second);
 }
 
+template <int FMT, int R, int S, int EPI, int NW, int SLICE, class H>
+__device__ __forceinline__ void pipe_loop(const GemvArgs& a, int64_t nrows, int cta, int ncta, uint8_t* xq,
+                                          uint8_t* ring, float scale, H& hooks) {
+  const WarpTiles w = warp_tiles(nrows, R, int(a.ncols / 1024), threadIdx.x >> 5, NW, cta, ncta);
+  pipe_loop_w<FMT, R, S, EPI, NW, SLICE>(a, nrows, w, cta, xq, ring, scale, hooks);
+}
+
 // The per-launch body: stage all of x, then the loop.  TRIGGER: signal
 // programmatic dependents after staging.
 template <int FMT, int R, int S, int EPI, int NW, bool TRIGGER, int SLICE = 0>
@@ -592,6 +602,46 @@ __global__ void __launch_bounds__(NW * 32) k_gemv_pipe(const __grid_constant__ G
   pipe_prologue<FMT, R, S, NW>(a, nrows, blockIdx.x, gridDim.x, ring);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   pipe_body<FMT, R, S, EPI, NW, true>(a, nrows, blockIdx.x, gridDim.x, xq, ring);
+}
+
+// Two GEMVs over the same x in one launch: rows [0, n1) of a1 in format F1 and
+// rows [0, n2) of a2 in F2 (both 4-bit-nibble formats, so one staged x serves
+// both).  The group indices of the two run on as one range over the warps, a1's
+// first; each warp works through its a1 groups, then its a2 groups, with each
+// format's own ring depth in one per-warp slice.  Used for a Q4_K Q/K GEMV with
+// a Q6_K V GEMV.
+template <int F1, int F2, int S1, int S2, int EPI, int NW>
+__global__ void __launch_bounds__(NW * 32) k_gemv_pipe2(const __grid_constant__ GemvArgs a1,
+                                                       const __grid_constant__ GemvArgs a2, const int64_t n1,
+                                                       const int64_t n2) {
+  static_assert(F1 != NT_Q8_0 && F2 != NT_Q8_0, "one staged x: nibble formats only");
+  constexpr int R = 2;
+  constexpr int SLICE = int(pipe_slice<F1, R, S1, 0>() > pipe_slice<F2, R, S2, 0>() ? pipe_slice<F1, R, S1, 0>()
+                                                                                     : pipe_slice<F2, R, S2, 0>());
+  extern __shared__ float4 smem4[];
+  uint8_t* xq = reinterpret_cast<uint8_t*>(smem4);
+  uint8_t* ring = xq + size_t(a1.ncols / 32) * kXUnit;
+  const int warp = threadIdx.x >> 5, kiters = int(a1.ncols / 1024);
+  const int64_t G1 = (n1 + R - 1) / R, G = G1 + (n2 + R - 1) / R;
+  WarpTiles w1, w2;
+  w1.g0 = int64_t(warp) * gridDim.x + blockIdx.x;
+  w1.stride = int64_t(gridDim.x) * NW;
+  const int64_t c1 = w1.g0 < G1 ? (G1 - 1 - w1.g0) / w1.stride + 1 : 0;
+  w1.ntiles = int(c1) * kiters;
+  const int64_t g2 = w1.g0 + c1 * w1.stride;            // first combined index past a1
+  w2.g0 = g2 - G1;
+  w2.stride = w1.stride;
+  w2.ntiles = g2 < G ? int((G - 1 - g2) / w2.stride + 1) * kiters : 0;
+  if (w1.ntiles) pipe_prologue_w<F1, R, S1, SLICE>(a1, n1, w1, ring);
+  else pipe_prologue_w<F2, R, S2, SLICE>(a2, n2, w2, ring);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  stage_x<F1, NW>(a1, xq);
+  const float scale = x_scale(a1, xq);
+  asm volatile("griddepcontrol.launch_dependents;");
+  StagedHooks h;
+  pipe_loop_w<F1, R, S1, EPI, NW, SLICE>(a1, n1, w1, blockIdx.x, xq, ring, scale, h);
+  if (w1.ntiles && w2.ntiles) pipe_prologue_w<F2, R, S2, SLICE>(a2, n2, w2, ring);
+  pipe_loop_w<F2, R, S2, EPI, NW, SLICE>(a2, n2, w2, blockIdx.x, xq, ring, scale, h);
 }
 
 inline size_t pipe_x_bytes(int64_t cols) { return size_t(cols / 32) * kXUnit; }
@@ -684,6 +734,43 @@ cudaError_t launch_gemv_pipe_fmt(const GemvArgs& a, int epi, int R, int S, int N
   if (S >= 4) return launch_gemv_pipe_rs<FMT, 2, 4, 8>(a, epi, s, pdl, grid_used);
   if (S >= 3) return launch_gemv_pipe_rs<FMT, 2, 3, 8>(a, epi, s, pdl, grid_used);
   return launch_gemv_pipe_rs<FMT, 2, 2, 8>(a, epi, s, pdl, grid_used);
+}
+
+// Q4_K rows of a1 and Q6_K rows of a2 over one x (see k_gemv_pipe2), 16 warps
+// per CTA, one CTA per SM, the ring depths that fit beside x.
+template <int EPI>
+cudaError_t launch_gemv_pipe2_q4k_q6k(const GemvArgs& a1, const GemvArgs& a2, cudaStream_t s, bool pdl) {
+  constexpr int NW = 16, S1 = 8, S2 = 6;
+  auto kern = k_gemv_pipe2<NT_Q4_K, NT_Q6_K, S1, S2, EPI, NW>;
+  constexpr size_t slice = pipe_slice<NT_Q4_K, 2, S1, 0>() > pipe_slice<NT_Q6_K, 2, S2, 0>()
+                               ? pipe_slice<NT_Q4_K, 2, S1, 0>()
+                               : pipe_slice<NT_Q6_K, 2, S2, 0>();
+  const size_t smem = pipe_x_bytes(a1.ncols) + size_t(NW) * slice;
+  if (smem > size_t(kPipeMaxSmem) || a1.ncols != a2.ncols || a1.col0 || a2.col0) return cudaErrorInvalidValue;
+  static int s_sms = 0;
+  if (!s_sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&s_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeMaxSmem);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t n1 = gemv_logical_rows(a1), n2 = gemv_logical_rows(a2);
+  const int64_t groups = (n1 + 1) / 2 + (n2 + 1) / 2;
+  int64_t grid = (groups + NW - 1) / NW;
+  if (grid < s_sms) grid = groups < s_sms ? groups : s_sms;
+  if (grid > s_sms) grid = s_sms;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(unsigned(NW * 32));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a1, a2, n1, n2);
 }
 
 #define NT_DECLARE_GEMV_PIPE(NAME) \

@@ -119,6 +119,9 @@ int64_t gemv_logical_rows(const GemvArgs& a);
 constexpr int kMaxGemvGrid = 152 * 8;   // upper bound of CTAs in one GEMV launch (partial buffers)
 // grid_used (nullable) receives the number of CTAs launched.
 cudaError_t launch_gemv(const GemvArgs& a, int epi, cudaStream_t s, bool pdl, int* grid_used);
+// Two GEMVs over the same x in one launch where a kernel exists for the pair
+// (a Q4_K a1 with a Q6_K a2, whole 1024-column tiles); else two launch_gemv calls.
+cudaError_t launch_gemv_pair(const GemvArgs& a1, const GemvArgs& a2, int epi, cudaStream_t s, bool pdl);
 
 // ------------------------------------------------------------ generator --
 // SplitMix64 output function (Steele, Lea, Flood, OOPSLA 2014) on the counter
