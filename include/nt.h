@@ -186,6 +186,17 @@ nt_status nt_get_stats(const nt_model* m, nt_stats* out);
  * of a class is then one phase.  For measurement only. */
 nt_status nt_profile_steps(nt_model* m, int32_t token, int32_t n_steps, nt_kernel_times* out);
 
+/* Times the step's GEMV launches on their own: one CUDA graph of a step's GEMV
+ * launches (per layer QKV, O, gate/up, down, then the output head) as the step
+ * issues them (programmatic dependent launches back to back), replayed n_reps
+ * times between CUDA events on the model's stream.  Returns the mean device
+ * time per GEMV launch, the mean algorithmic bytes per launch and the launches
+ * per step.  The GEMVs read and overwrite the model's activations and the K/V
+ * row at the current position: prefill or reset the cache afterwards.
+ * Resident models only (NT_E_STATE otherwise).  For measurement only. */
+nt_status nt_profile_gemvs(nt_model* m, int32_t n_reps, double* ms_per_launch, double* bytes_per_launch,
+                           int32_t* launches_per_step);
+
 /* Pointer to a weight tensor of the model (owned by the model).  For a
  * streamed layer the tensor refers to host memory: nt_qtensor_export works,
  * nt_gemv_q and nt_dequant return NT_E_STATE. */

@@ -387,7 +387,7 @@ static cudaError_t enqueue_layer(nt_model* m, int l, uint8_t* base, Launcher& L,
     if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(g.qk, EPI_QKV, s, pdl, nullptr); }))) return e;
   } else {   // v in its own format: one launch for both where a kernel exists for the pair
     const double by = gemv_bytes(g.qk, 4.0 * qd + 2.0 * kd) + gemv_bytes(g.v, 2.0 * kd) - 4.0 * c.hidden;
-    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_pair(g.qk, g.v, EPI_QKV, s, pdl); }))) return e;
+    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_pair(g.qk, g.v, EPI_QKV, s, pdl, nullptr); }))) return e;
   }
 
   // split-context GQA attention over positions 0..pos, merged by the last chunk's CTA
@@ -1130,6 +1130,77 @@ nt_status nt_profile_steps(nt_model* m, int32_t token, int32_t n_steps, nt_kerne
   }
   t.step_ms = wall / n_steps;
   *out = t;
+  return NT_OK;
+}
+
+nt_status nt_profile_gemvs(nt_model* m, int32_t n_reps, double* ms_per_launch, double* bytes_per_launch,
+                           int32_t* launches_per_step) {
+  if (!m || !ms_per_launch || !bytes_per_launch || !launches_per_step)
+    return fail(NT_E_INVAL, "nt_profile_gemvs: NULL argument");
+  if (n_reps < 1) return fail(NT_E_INVAL, "nt_profile_gemvs: n_reps < 1");
+  if (m->n_resident < m->c.n_layers) return fail(NT_E_STATE, "nt_profile_gemvs: model has streamed layers");
+  if (m->pos >= m->c.max_ctx) return fail(NT_E_INVAL, "nt_profile_gemvs: position reached max_ctx");
+  const nt_config& c = m->c;
+  const int hd = c.head_dim, qd = c.n_heads * hd, kd = c.n_kv_heads * hd;
+  cudaStream_t s = m->stream;
+  double bytes = 0;
+  int n = 0;
+  // the step's GEMV launches, in order, programmatic dependent launches as in the step graph
+  auto enqueue = [&]() -> cudaError_t {
+    bytes = 0;
+    n = 0;
+    cudaError_t e;
+    for (int l = 0; l < c.n_layers; l++) {
+      const LayerGemvs g = layer_gemvs(m, l, m->layers[size_t(l)].dev);
+      if (!g.v_split) {
+        if ((e = launch_gemv(g.qk, EPI_QKV, s, true, nullptr))) return e;
+        bytes += gemv_bytes(g.qk, 4.0 * qd + 4.0 * kd);
+      } else {
+        int nl = 0;
+        if ((e = launch_gemv_pair(g.qk, g.v, EPI_QKV, s, true, &nl))) return e;
+        bytes += gemv_bytes(g.qk, 4.0 * qd + 2.0 * kd) + gemv_bytes(g.v, 2.0 * kd) - 4.0 * c.hidden;
+        n += nl - 1;
+      }
+      if ((e = launch_gemv(g.o, EPI_ADD, s, true, nullptr))) return e;
+      if ((e = launch_gemv(g.gu, EPI_SWIGLU, s, true, nullptr))) return e;
+      if ((e = launch_gemv(g.down, EPI_ADD, s, true, nullptr))) return e;
+      bytes += gemv_bytes(g.o, 8.0 * c.hidden) + gemv_bytes(g.gu, 4.0 * c.ffn_dim) + gemv_bytes(g.down, 8.0 * c.hidden);
+      n += 4;
+    }
+    const GemvArgs h = head_gemv(m);
+    if ((e = launch_gemv(h, EPI_LOGITS, s, true, &m->out_grid))) return e;
+    bytes += gemv_bytes(h, 4.0 * c.vocab);
+    return cudaSuccess;
+  };
+  n = 0;
+  NT_CUDA(cudaStreamSynchronize(s));
+  NT_CUDA(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+  cudaError_t e = enqueue();
+  cudaGraph_t g = nullptr;
+  cudaError_t e2 = cudaStreamEndCapture(s, &g);
+  if (e || e2) {
+    if (g) cudaGraphDestroy(g);
+    return cuda_fail(e ? e : e2, "nt_profile_gemvs: capture");
+  }
+  const int launches = n + 1;
+  cudaGraphExec_t ex = nullptr;
+  e = cudaGraphInstantiate(&ex, g, 0);
+  cudaGraphDestroy(g);
+  if (e) return cuda_fail(e, "nt_profile_gemvs: instantiate");
+  nt_status st = NT_OK;
+  e = cudaGraphLaunch(ex, s);   // warm-up
+  if (!e) e = cudaEventRecord(m->ev_step0, s);
+  for (int i = 0; i < n_reps && !e; i++) e = cudaGraphLaunch(ex, s);
+  if (!e) e = cudaEventRecord(m->ev_step1, s);
+  if (e) st = cuda_fail(e, "nt_profile_gemvs: launch");
+  if (!st) st = wait_event(m->ev_step1, "nt_profile_gemvs");
+  float ms = 0.f;
+  if (!st && (e = cudaEventElapsedTime(&ms, m->ev_step0, m->ev_step1))) st = cuda_fail(e, "nt_profile_gemvs");
+  cudaGraphExecDestroy(ex);
+  if (st) return st;
+  *ms_per_launch = double(ms) / (double(n_reps) * launches);
+  *bytes_per_launch = bytes / launches;
+  *launches_per_step = launches;
   return NT_OK;
 }
 

@@ -113,7 +113,8 @@ cudaError_t launch_gemv(const GemvArgs& a_in, int epi, cudaStream_t s, bool pdl,
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_gemv_pair(const GemvArgs& a1_in, const GemvArgs& a2_in, int epi, cudaStream_t s, bool pdl) {
+cudaError_t launch_gemv_pair(const GemvArgs& a1_in, const GemvArgs& a2_in, int epi, cudaStream_t s, bool pdl,
+                             int* launches) {
   static const bool force_register_path = getenv("NT_GEMV_REGISTER_PATH") != nullptr;
   const int64_t cols = a1_in.seg[0].cols;
   bool pair = !force_register_path && epi == EPI_QKV && a1_in.seg[0].type == NT_Q4_K && a2_in.seg[0].type == NT_Q6_K &&
@@ -124,8 +125,10 @@ cudaError_t launch_gemv_pair(const GemvArgs& a1_in, const GemvArgs& a2_in, int e
     GemvArgs a1 = a1_in, a2 = a2_in;
     a1.col0 = a2.col0 = 0;
     a1.ncols = a2.ncols = cols;
+    if (launches) *launches = 1;
     return launch_gemv_pipe2_q4k_q6k<EPI_QKV>(a1, a2, s, pdl);
   }
+  if (launches) *launches = 2;
   cudaError_t e = launch_gemv(a1_in, epi, s, pdl, nullptr);
   if (e == cudaSuccess) e = launch_gemv(a2_in, epi, s, pdl, nullptr);
   return e;

@@ -121,7 +121,9 @@ constexpr int kMaxGemvGrid = 152 * 8;   // upper bound of CTAs in one GEMV launc
 cudaError_t launch_gemv(const GemvArgs& a, int epi, cudaStream_t s, bool pdl, int* grid_used);
 // Two GEMVs over the same x in one launch where a kernel exists for the pair
 // (a Q4_K a1 with a Q6_K a2, whole 1024-column tiles); else two launch_gemv calls.
-cudaError_t launch_gemv_pair(const GemvArgs& a1, const GemvArgs& a2, int epi, cudaStream_t s, bool pdl);
+// launches (nullable) receives 1 or 2.
+cudaError_t launch_gemv_pair(const GemvArgs& a1, const GemvArgs& a2, int epi, cudaStream_t s, bool pdl,
+                             int* launches);
 
 // ------------------------------------------------------------ generator --
 // SplitMix64 output function (Steele, Lea, Flood, OOPSLA 2014) on the counter

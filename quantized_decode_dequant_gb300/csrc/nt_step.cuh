@@ -182,6 +182,15 @@ struct StepHooks {
     }
   }
 
+  // At the start of a GEMV: warp w claims and stages tiles w, w + 16, ... as their
+  // inputs become ready, so the tiles are staged in parallel rather than in the
+  // order the first row group reaches them.
+  template <int FMT>
+  __device__ __forceinline__ void prestage(const GemvArgs& a, uint8_t* xq) {
+    const int kt = int(a.ncols / 1024);
+    for (int k = threadIdx.x >> 5; k < kt; k += kStepWarps) tile<FMT>(a, xq, k);
+  }
+
   __device__ __forceinline__ void group_done(const GemvArgs& a, int64_t grp, int nlive) {
     if (kind == SIG_NONE) return;
     __syncwarp();   // the epilogue's stores of every lane before lane 0's release
@@ -229,6 +238,7 @@ __device__ __noinline__ void step_prologue(const StepGemv& g, uint8_t* ring) {
 }
 template <int FMT, int EPI>
 __device__ __noinline__ void step_gemv(const StepGemv& g, uint8_t* xq, uint8_t* ring, StepHooks& h) {
+  h.template prestage<FMT>(g.a, xq);
   pipe_loop<FMT, 2, StepRing<FMT>::S, EPI, kStepWarps, kStepSlice>(g.a, g.nrows, blockIdx.x, gridDim.x, xq, ring,
                                                                    1.0f, h);
 }

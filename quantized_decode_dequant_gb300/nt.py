@@ -74,6 +74,7 @@ _SIGS = {
     "nt_stream_layers": (C.c_int, [_vp, _i32, _i32]),
     "nt_get_stats": (C.c_int, [_vp, C.POINTER(nt_stats)]),
     "nt_profile_steps": (C.c_int, [_vp, _i32, _i32, C.POINTER(nt_kernel_times)]),
+    "nt_profile_gemvs": (C.c_int, [_vp, _i32, C.POINTER(C.c_double), C.POINTER(C.c_double), C.POINTER(_i32)]),
     "nt_model_tensor": (C.c_int, [_vp, _i32, _i32, C.POINTER(C.c_void_p)]),
     "nt_qtensor_create": (C.c_int, [C.c_int, _i64, _i64, _u64, C.c_uint32, C.c_float, C.POINTER(C.c_void_p)]),
     "nt_qtensor_destroy": (None, [_vp]),
@@ -204,6 +205,13 @@ def nt_profile_steps(m: int, token: int, n_steps: int) -> nt_kernel_times:
     t = nt_kernel_times()
     _check(lib().nt_profile_steps(m, token, n_steps, C.byref(t)), "nt_profile_steps")
     return t
+
+
+def nt_profile_gemvs(m: int, n_reps: int) -> tuple[float, float, int]:
+    """(ms per GEMV launch, algorithmic bytes per launch, GEMV launches per step)."""
+    ms, by, n = C.c_double(), C.c_double(), C.c_int32()
+    _check(lib().nt_profile_gemvs(m, n_reps, C.byref(ms), C.byref(by), C.byref(n)), "nt_profile_gemvs")
+    return ms.value, by.value, n.value
 
 
 def nt_model_tensor(m: int, layer: int, role) -> int:
