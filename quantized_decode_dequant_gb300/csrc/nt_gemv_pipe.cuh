@@ -44,6 +44,10 @@ constexpr int kPipeWarps = 8;                 // 256 threads per CTA
 constexpr int kPipeMaxSmem = 221 * 1024;      // dynamic shared memory a CTA may ask for
 constexpr int kPipeSmPerSm = 228 * 1024;      // shared memory of an SM (each resident CTA also reserves 1 KB)
 constexpr int kXUnit = 80;                    // staged x per 32 columns: h[32] | l[32] | sx, T0, T1, sum of squares
+// Before the producer of x is done only the first kPipeEarly tiles of a warp's
+// ring are copied: the x loads of the staging that follows would otherwise queue
+// behind a whole ring of weight copies; the rest is issued once x is staged.
+constexpr int kPipeEarly = 2;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -397,15 +401,24 @@ __host__ __device__ constexpr size_t pipe_slice() {
 // First S-1 tiles of the calling warp.  Reads only weights, so it may run
 // before the producer of x has finished, and (with per-warp slices) while
 // other warps of the CTA still work on an earlier GEMV.
+// Copies of the calling warp's tiles [from, to) (to <= S - 1): the first S - 1
+// tiles are in flight when the tile loop starts.
 template <int FMT, int R, int S, int SLICE = 0>
-__device__ __forceinline__ void pipe_prologue_w(const GemvArgs& a, int64_t nrows, const WarpTiles& w, uint8_t* ring) {
+__device__ __forceinline__ void pipe_issue_w(const GemvArgs& a, int64_t nrows, const WarpTiles& w, uint8_t* ring,
+                                             int from, int to) {
   static_assert(SLICE == 0 || size_t(S) * R * Pipe<FMT>::RB <= size_t(SLICE), "ring slice too small");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t wring_s = smem_addr(ring + size_t(warp) * pipe_slice<FMT, R, S, SLICE>());
   PipeCursor<FMT, R, S> c;
   c.init(w, int(a.ncols / 1024), wring_s);
 #pragma unroll 1
-  for (int t = 0; t < S - 1; t++) c.template step<true>(a, nrows, lane);
+  for (int t = 0; t < from; t++) c.template step<false>(a, nrows, lane);
+#pragma unroll 1
+  for (int t = from; t < to; t++) c.template step<true>(a, nrows, lane);
+}
+template <int FMT, int R, int S, int SLICE = 0>
+__device__ __forceinline__ void pipe_prologue_w(const GemvArgs& a, int64_t nrows, const WarpTiles& w, uint8_t* ring) {
+  pipe_issue_w<FMT, R, S, SLICE>(a, nrows, w, ring, 0, S - 1);
 }
 template <int FMT, int R, int S, int NW, int SLICE = 0>
 __device__ __forceinline__ void pipe_prologue(const GemvArgs& a, int64_t nrows, int cta, int ncta, uint8_t* ring) {
@@ -420,12 +433,10 @@ __device__ __forceinline__ void pipe_prologue(const GemvArgs& a, int64_t nrows, 
 // and 16..31, and the sum of squares (each lane's eight in element order, then
 // the four lanes as (l0 + l1) + (l2 + l3)); every kernel stages the same way.
 template <int FMT>
-__device__ __forceinline__ void stage_pass(const float* x, int p, uint8_t* xq) {
+__device__ __forceinline__ void stage_convert(float4 f0, float4 f1, int p, uint8_t* xq) {
   using P = Pipe<FMT>;
   const int lane = threadIdx.x & 31, q = lane & 3;          // q: eighth of the block
   const int blk = p * 8 + (lane >> 2);
-  const float4* src = reinterpret_cast<const float4*>(x + size_t(blk) * 32 + q * 8);
-  const float4 f0 = __ldcg(src), f1 = __ldcg(src + 1);
   const float v[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
   float amax = 0.f, sq = __fmul_rn(v[0], v[0]);
 #pragma unroll
@@ -459,6 +470,19 @@ __device__ __forceinline__ void stage_pass(const float* x, int p, uint8_t* xq) {
         make_uint4(__float_as_uint(amax / 32512.0f), uint32_t(t01), uint32_t(t_hi), __float_as_uint(sq));
 }
 
+// Stages eight 32-column blocks of x (columns [256 p, 256 p + 256) of the
+// window starting at x) as 16-bit fixed point, four lanes of the calling warp
+// per block, eight consecutive elements per lane.  Per block: sx = max|x|/32512,
+// t = round(x/sx) split as 256 h + l, the sums T0, T1 of t over elements 0..15
+// and 16..31, and the sum of squares (each lane's eight in element order, then
+// the four lanes as (l0 + l1) + (l2 + l3)); every kernel stages the same way.
+template <int FMT>
+__device__ __forceinline__ void stage_pass(const float* x, int p, uint8_t* xq) {
+  const int lane = threadIdx.x & 31;
+  const float4* src = reinterpret_cast<const float4*>(x + size_t(p) * 256 + lane * 8);
+  stage_convert<FMT>(__ldcg(src), __ldcg(src + 1), p, xq);
+}
+
 // Stages 1024-column tile k of x (four passes) by the calling warp.
 template <int FMT>
 __device__ __forceinline__ void stage_tile(const float* x, int k, uint8_t* xq) {
@@ -485,11 +509,28 @@ __device__ __forceinline__ float x_scale(const GemvArgs& a, const uint8_t* xq) {
   return rsqrtf(t / float(a.ncols) + a.eps);
 }
 
-// Whole window staged up front by the CTA's NW warps (256-column pass p by warp p % NW).
+// Whole window staged up front by the CTA's NW warps (256-column pass p by warp
+// p % NW); each warp loads up to four of its passes before converting any, so
+// the staging costs one memory latency.
 template <int FMT, int NW>
 __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xq) {
-  const int warp = threadIdx.x >> 5, np = int(a.ncols / 256);
-  for (int p = warp; p < np; p += NW) stage_pass<FMT>(a.x + a.col0, p, xq);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, np = int(a.ncols / 256);
+  const float* x = a.x + a.col0;
+  for (int p0 = warp; p0 < np; p0 += 4 * NW) {
+    float4 f[4][2];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const int p = p0 + i * NW;
+      if (p < np) {
+        const float4* src = reinterpret_cast<const float4*>(x + size_t(p) * 256 + lane * 8);
+        f[i][0] = __ldcg(src);
+        f[i][1] = __ldcg(src + 1);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+      if (p0 + i * NW < np) stage_convert<FMT>(f[i][0], f[i][1], p0 + i * NW, xq);
+  }
   __syncthreads();
 }
 
@@ -595,13 +636,23 @@ __device__ __forceinline__ void pipe_body(const GemvArgs& a, int64_t nrows, int 
 }
 
 template <int FMT, int R, int S, int EPI, int NW>
-__global__ void __launch_bounds__(NW * 32) k_gemv_pipe(const __grid_constant__ GemvArgs a, const int64_t nrows) {
+__global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe(const __grid_constant__ GemvArgs a,
+                                                                const int64_t nrows) {
+  constexpr int E = S - 1 < kPipeEarly ? S - 1 : kPipeEarly;
   extern __shared__ float4 smem4[];
   uint8_t* xq = reinterpret_cast<uint8_t*>(smem4);
   uint8_t* ring = xq + size_t(a.ncols / 32) * kXUnit;
-  pipe_prologue<FMT, R, S, NW>(a, nrows, blockIdx.x, gridDim.x, ring);
+  const WarpTiles w = warp_tiles(nrows, R, int(a.ncols / 1024), threadIdx.x >> 5, NW, blockIdx.x, gridDim.x);
+  pipe_issue_w<FMT, R, S>(a, nrows, w, ring, 0, E);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  pipe_body<FMT, R, S, EPI, NW, true>(a, nrows, blockIdx.x, gridDim.x, xq, ring);
+  stage_x<FMT, NW>(a, xq);
+  if (E < S - 1) pipe_issue_w<FMT, R, S>(a, nrows, w, ring, E, S - 1);
+  const float scale = x_scale(a, xq);
+  // the next kernel may start its own weight prefetch on SMs this grid frees;
+  // it waits for this grid to finish before it reads anything this grid writes
+  asm volatile("griddepcontrol.launch_dependents;");
+  StagedHooks h;
+  pipe_loop_w<FMT, R, S, EPI, NW, 0>(a, nrows, w, blockIdx.x, xq, ring, scale, h);
 }
 
 // Two GEMVs over the same x in one launch: rows [0, n1) of a1 in format F1 and
@@ -611,7 +662,7 @@ __global__ void __launch_bounds__(NW * 32) k_gemv_pipe(const __grid_constant__ G
 // format's own ring depth in one per-warp slice.  Used for a Q4_K Q/K GEMV with
 // a Q6_K V GEMV.
 template <int F1, int F2, int S1, int S2, int EPI, int NW>
-__global__ void __launch_bounds__(NW * 32) k_gemv_pipe2(const __grid_constant__ GemvArgs a1,
+__global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe2(const __grid_constant__ GemvArgs a1,
                                                        const __grid_constant__ GemvArgs a2, const int64_t n1,
                                                        const int64_t n2) {
   static_assert(F1 != NT_Q8_0 && F2 != NT_Q8_0, "one staged x: nibble formats only");
@@ -632,10 +683,13 @@ __global__ void __launch_bounds__(NW * 32) k_gemv_pipe2(const __grid_constant__ 
   w2.g0 = g2 - G1;
   w2.stride = w1.stride;
   w2.ntiles = g2 < G ? int((G - 1 - g2) / w2.stride + 1) * kiters : 0;
-  if (w1.ntiles) pipe_prologue_w<F1, R, S1, SLICE>(a1, n1, w1, ring);
-  else pipe_prologue_w<F2, R, S2, SLICE>(a2, n2, w2, ring);
+  constexpr int E1 = S1 - 1 < kPipeEarly ? S1 - 1 : kPipeEarly, E2 = S2 - 1 < kPipeEarly ? S2 - 1 : kPipeEarly;
+  if (w1.ntiles) pipe_issue_w<F1, R, S1, SLICE>(a1, n1, w1, ring, 0, E1);
+  else pipe_issue_w<F2, R, S2, SLICE>(a2, n2, w2, ring, 0, E2);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   stage_x<F1, NW>(a1, xq);
+  if (w1.ntiles) pipe_issue_w<F1, R, S1, SLICE>(a1, n1, w1, ring, E1, S1 - 1);
+  else pipe_issue_w<F2, R, S2, SLICE>(a2, n2, w2, ring, E2, S2 - 1);
   const float scale = x_scale(a1, xq);
   asm volatile("griddepcontrol.launch_dependents;");
   StagedHooks h;
