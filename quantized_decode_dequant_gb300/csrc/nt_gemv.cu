@@ -23,6 +23,16 @@ static int pipe_ctas_per_sm() {
   return v;
 }
 
+// Warps per CTA for 4-bit formats with four rows per warp: 16 (one CTA per SM,
+// measured slightly faster on GB300) unless NT_GEMV_R4_WARPS=8.
+static int pipe_r4_warps() {
+  static const int v = [] {
+    const char* e = getenv("NT_GEMV_R4_WARPS");
+    return e && atoi(e) == 8 ? 8 : 16;
+  }();
+  return v;
+}
+
 // Layout of the pipeline: 0 automatic, 8 (8-warp CTAs) or 16 (one 16-warp CTA
 // per SM), from NT_GEMV_WARPS.
 static int pipe_layout() {
@@ -70,16 +80,22 @@ cudaError_t launch_gemv(const GemvArgs& a_in, int epi, cudaStream_t s, bool pdl,
     // the 16-warp layout stages x once per SM and gives the ring the rest of it
     const size_t ring16 = xb < size_t(kPipeMaxSmem) ? size_t(kPipeMaxSmem) - xb : 0;
     int S16 = int(ring16 / (size_t(16) * 2 * pipe_row_bytes(fmt)));
-    S16 = S16 >= 6 ? 6 : (S16 >= 4 ? 4 : S16);
+    S16 = S16 >= 8 ? 8 : (S16 >= 6 ? 6 : (S16 >= 4 ? 4 : S16));
+    int S16r4 = int(ring16 / (size_t(16) * 4 * pipe_row_bytes(fmt)));
+    S16r4 = S16r4 >= 4 ? 4 : S16r4;
+    const bool four_bit_tall = R == 4 && (fmt == NT_Q4_0 || fmt == NT_Q4_K);
     int NW = 8;
     if (pipe_layout() == 16 && S16 >= 3) {
       NW = 16;
       R = 2;
       S = S16;
-    } else if (pipe_layout() == 0 && S16 >= 3 && !(R == 4 && (fmt == NT_Q4_0 || fmt == NT_Q4_K))) {
+    } else if (pipe_layout() == 0 && four_bit_tall && pipe_r4_warps() == 16 && S16r4 >= 3) {
+      NW = 16;
+      S = S16r4;
+    } else if (pipe_layout() == 0 && S16 >= 3 && !four_bit_tall) {
       // measured on GB300: one 16-warp CTA per SM (x staged once, the deeper ring) is
-      // faster for every shape except 4-bit formats with enough rows for four rows
-      // per warp, where the two 8-warp CTAs share each x read over four rows
+      // faster than two 8-warp CTAs for every shape; 4-bit formats with enough rows
+      // keep four rows per warp (each x read shared over four rows)
       NW = 16;
       R = 2;
       S = S16;

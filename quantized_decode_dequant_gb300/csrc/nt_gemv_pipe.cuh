@@ -769,12 +769,17 @@ cudaError_t launch_gemv_pipe_rs(const GemvArgs& a, int epi, cudaStream_t s, bool
 }
 
 // Instantiated shapes: 8 warps per CTA with S in {2, 3, 4, 6, 8} (R = 2) or
-// {2, 4} (R = 4); 16 warps per CTA (one CTA per SM) with S in {3, 4, 6} (R = 2).
-// S is rounded down to the nearest instantiated depth.
+// {2, 4} (R = 4); 16 warps per CTA (one CTA per SM) with S in {3, 4, 6, 8}
+// (R = 2) or {3, 4} (R = 4).  S is rounded down to the nearest instantiated depth.
 template <int FMT>
 cudaError_t launch_gemv_pipe_fmt(const GemvArgs& a, int epi, int R, int S, int NW, cudaStream_t s, bool pdl,
                                  int* grid_used) {
   if (NW == 16) {
+    if (R == 4) {
+      if (S >= 4) return launch_gemv_pipe_rs<FMT, 4, 4, 16>(a, epi, s, pdl, grid_used);
+      return launch_gemv_pipe_rs<FMT, 4, 3, 16>(a, epi, s, pdl, grid_used);
+    }
+    if (S >= 8) return launch_gemv_pipe_rs<FMT, 2, 8, 16>(a, epi, s, pdl, grid_used);
     if (S >= 6) return launch_gemv_pipe_rs<FMT, 2, 6, 16>(a, epi, s, pdl, grid_used);
     if (S >= 4) return launch_gemv_pipe_rs<FMT, 2, 4, 16>(a, epi, s, pdl, grid_used);
     return launch_gemv_pipe_rs<FMT, 2, 3, 16>(a, epi, s, pdl, grid_used);
