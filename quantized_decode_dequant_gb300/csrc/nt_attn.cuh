@@ -11,6 +11,8 @@
 // M = max m_c, o = sum o_c e^(m_c - M) / sum l_c e^(m_c - M).
 #pragma once
 
+#include <cstdlib>
+
 #include "nt_internal.cuh"
 
 namespace nt {
@@ -19,8 +21,15 @@ constexpr int kAttnThreads = 512;
 constexpr int kAttnMaxChunk = 256;
 
 // Cached positions per item: as short as keeps the items of a full context
-// within about one per SM (at most 256).
-inline int attn_chunk_len(int max_ctx) { return max_ctx <= 1024 ? 64 : (max_ctx <= 2048 ? 128 : 256); }
+// within about one per SM (at most 256); NT_ATTN_CHUNK (64, 128 or 256)
+// overrides.  Fixed per model: every path of a model splits the same way.
+inline int attn_chunk_len(int max_ctx) {
+  if (const char* e = getenv("NT_ATTN_CHUNK")) {
+    const int c = atoi(e);
+    if (c == 64 || c == 128 || c == 256) return c;
+  }
+  return max_ctx <= 1024 ? 64 : (max_ctx <= 2048 ? 128 : 256);
+}
 
 struct AttnArgs {
   const float* q = nullptr;         // [n_heads][hd], RoPE applied
@@ -136,18 +145,18 @@ __device__ __forceinline__ void attn_combine_head(const AttnArgs& a, int j, int 
   }
 }
 
-// One item by the whole CTA.  n = cached positions attended (pos + 1; the
-// current one is already stored), used = ceil(n / C) items of kv head g exist.
-// Scores: threads 2c and 2c+1 hold the two halves of key c in registers and
-// score it against every head (q read as broadcast float4s).  P V: the CTA's
+// One item by the whole CTA (C = a.chunk, a compile-time copy).  n = cached
+// positions attended (pos + 1; the current one is already stored), used =
+// ceil(n / C) items of kv head g exist.  Scores: threads 2c and 2c+1 hold the
+// two halves of key c in registers and score it against every head (q read as
+// broadcast float4s).  P V: the CTA's
 // threads are kAttnThreads/HD position slices x HD dimensions; slice s sums its
 // contiguous share of the chunk for all G heads, and the slices are added in
 // order.  Every thread of the CTA must call it.
-template <int HD, int G>
+template <int HD, int G, int C>
 __device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, int n, int used, uint8_t* sm,
                                           bool prefetched) {
   constexpr int KP = HD + 8, NS = kAttnThreads / HD;
-  const int C = a.chunk;
   __half* Ks = reinterpret_cast<__half*>(sm);
   __half* Vs = Ks + C * KP;
   float* qs = reinterpret_cast<float*>(Vs + C * KP);
@@ -167,14 +176,15 @@ __device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, i
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
   __syncthreads();
 
-  // ---- scores ---------------------------------------------------------------
+  // ---- scores: two threads per key (measured faster than spreading a key over
+  // more threads when C < 256), each half of its dimensions ----
   if (t < 2 * C) {
-    constexpr int HH = HD / 2;                 // dims per thread
-    const int c = t >> 1, half = t & 1;
-    float2 kf[HH / 2];
-    const uint4* kr = reinterpret_cast<const uint4*>(Ks + c * KP + half * HH);
+    constexpr int TPK = 2, DPT = HD / TPK;
+    const int c = t / TPK, part = t % TPK;
+    float2 kf[DPT / 2];
+    const uint4* kr = reinterpret_cast<const uint4*>(Ks + c * KP + part * DPT);
 #pragma unroll
-    for (int i = 0; i < HH / 8; i++) {
+    for (int i = 0; i < DPT / 8; i++) {
       const uint4 v = kr[i];
       const __half2* h2 = reinterpret_cast<const __half2*>(&v);
 #pragma unroll
@@ -182,18 +192,19 @@ __device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, i
     }
 #pragma unroll
     for (int h = 0; h < G; h++) {
-      const float4* qh = reinterpret_cast<const float4*>(qs + h * HD + half * HH);
+      const float4* qh = reinterpret_cast<const float4*>(qs + h * HD + part * DPT);
       float acc = 0.f;
 #pragma unroll
-      for (int i = 0; i < HH / 4; i++) {
+      for (int i = 0; i < DPT / 4; i++) {
         const float4 qv = qh[i];
         acc = __fmaf_rn(qv.x, kf[2 * i].x, acc);
         acc = __fmaf_rn(qv.y, kf[2 * i].y, acc);
         acc = __fmaf_rn(qv.z, kf[2 * i + 1].x, acc);
         acc = __fmaf_rn(qv.w, kf[2 * i + 1].y, acc);
       }
-      acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, 1));
-      if (half == 0) S[h * C + c] = c < cnt ? __fmul_rn(acc, a.scale) : -INFINITY;
+#pragma unroll
+      for (int o = 1; o < TPK; o <<= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+      if (part == 0) S[h * C + c] = c < cnt ? __fmul_rn(acc, a.scale) : -INFINITY;
     }
   }
   __syncthreads();

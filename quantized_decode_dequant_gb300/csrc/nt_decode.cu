@@ -47,7 +47,7 @@ __global__ void k_embed(const QMat e, const int32_t* __restrict__ d_token, float
 // by earlier steps (and the position, written by the previous step's argmax)
 // are final before that GEMV starts, so they are copied before waiting for it;
 // q and the current position's K and V only after.
-template <int HD, int G>
+template <int HD, int G, int C>
 __global__ void __launch_bounds__(kAttnThreads) k_attn(const __grid_constant__ AttnArgs a,
                                                        const int32_t* __restrict__ d_pos) {
   extern __shared__ uint4 smem_u4[];
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const __grid_constant__ A
   if (int(blockIdx.y) >= used) return;
   attn_prefetch<HD>(a, blockIdx.x, blockIdx.y, n - 1, sm);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  attn_item<HD, G>(a, blockIdx.x, blockIdx.y, n, used, sm, true);
+  attn_item<HD, G, C>(a, blockIdx.x, blockIdx.y, n, used, sm, true);
 }
 
 // Greedy choice over the per-CTA top-2 summaries of the output GEMV (ties to the
@@ -244,7 +244,7 @@ struct Launcher {
 
 template <int HD, int G>
 static cudaError_t launch_attn_t(dim3 grid, cudaStream_t s, const AttnArgs& a, const int32_t* pos, bool pdl) {
-  auto kern = k_attn<HD, G>;
+  auto kern = a.chunk == 64 ? k_attn<HD, G, 64> : (a.chunk == 128 ? k_attn<HD, G, 128> : k_attn<HD, G, 256>);
   const size_t smem = attn_item_smem(HD, G, a.chunk);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));

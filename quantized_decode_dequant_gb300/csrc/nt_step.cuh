@@ -258,7 +258,10 @@ __device__ __noinline__ void step_attention(const AttnArgs& aa, int n_kv, int n_
     attn_prefetch<HD>(aa, g, chunk, n_ctx - 1, sm);
     if (threadIdx.x == 0) wait_count(kv_ready + g, kv_target, err);
     __syncthreads();
-    if (attn_item<HD, G>(aa, g, chunk, n_ctx, used, sm, true)) {
+    const bool merged = aa.chunk == 64    ? attn_item<HD, G, 64>(aa, g, chunk, n_ctx, used, sm, true)
+                        : aa.chunk == 128 ? attn_item<HD, G, 128>(aa, g, chunk, n_ctx, used, sm, true)
+                                          : attn_item<HD, G, 256>(aa, g, chunk, n_ctx, used, sm, true);
+    if (merged) {
       __syncthreads();   // every head of kv head g merged
       if (threadIdx.x == 0) {
         __threadfence();
