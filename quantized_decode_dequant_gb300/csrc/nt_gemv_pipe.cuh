@@ -511,12 +511,18 @@ __device__ __forceinline__ float x_scale(const GemvArgs& a, const uint8_t* xq) {
 
 // Whole window staged up front by the CTA's NW warps (256-column pass p by warp
 // p % NW); each warp loads up to four of its passes before converting any, so
-// the staging costs one memory latency.
-template <int FMT, int NW>
-__device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xq) {
+// the staging costs one memory latency.  between() runs after the first loads
+// are issued and before they are used (the caller issues weight copies there,
+// behind the x loads).
+struct NoOp {
+  __device__ __forceinline__ void operator()() const {}
+};
+template <int FMT, int NW, class F = NoOp>
+__device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xq, F between = F()) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, np = int(a.ncols / 256);
   const float* x = a.x + a.col0;
-  for (int p0 = warp; p0 < np; p0 += 4 * NW) {
+  bool first = true;
+  for (int p0 = warp; p0 < np || first; p0 += 4 * NW) {
     float4 f[4][2];
 #pragma unroll
     for (int i = 0; i < 4; i++) {
@@ -526,6 +532,10 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xq) {
         f[i][0] = __ldcg(src);
         f[i][1] = __ldcg(src + 1);
       }
+    }
+    if (first) {
+      between();
+      first = false;
     }
 #pragma unroll
     for (int i = 0; i < 4; i++)
@@ -645,8 +655,9 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe(const __grid_con
   const WarpTiles w = warp_tiles(nrows, R, int(a.ncols / 1024), threadIdx.x >> 5, NW, blockIdx.x, gridDim.x);
   pipe_issue_w<FMT, R, S>(a, nrows, w, ring, 0, E);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  stage_x<FMT, NW>(a, xq);
-  if (E < S - 1) pipe_issue_w<FMT, R, S>(a, nrows, w, ring, E, S - 1);
+  stage_x<FMT, NW>(a, xq, [&] {
+    if (E < S - 1) pipe_issue_w<FMT, R, S>(a, nrows, w, ring, E, S - 1);
+  });
   const float scale = x_scale(a, xq);
   // the next kernel may start its own weight prefetch on SMs this grid frees;
   // it waits for this grid to finish before it reads anything this grid writes
@@ -687,9 +698,10 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe2(const __grid_co
   if (w1.ntiles) pipe_issue_w<F1, R, S1, SLICE>(a1, n1, w1, ring, 0, E1);
   else pipe_issue_w<F2, R, S2, SLICE>(a2, n2, w2, ring, 0, E2);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  stage_x<F1, NW>(a1, xq);
-  if (w1.ntiles) pipe_issue_w<F1, R, S1, SLICE>(a1, n1, w1, ring, E1, S1 - 1);
-  else pipe_issue_w<F2, R, S2, SLICE>(a2, n2, w2, ring, E2, S2 - 1);
+  stage_x<F1, NW>(a1, xq, [&] {
+    if (w1.ntiles) pipe_issue_w<F1, R, S1, SLICE>(a1, n1, w1, ring, E1, S1 - 1);
+    else pipe_issue_w<F2, R, S2, SLICE>(a2, n2, w2, ring, E2, S2 - 1);
+  });
   const float scale = x_scale(a1, xq);
   asm volatile("griddepcontrol.launch_dependents;");
   StagedHooks h;
