@@ -121,12 +121,19 @@ template <> struct Pipe<NT_Q8_0> {
     stride = 64;
     size = 16;
   }
-  __device__ static float dot(const uint8_t* blk, int lane, const XBlock& x) {
-    const uint4 c0 = *reinterpret_cast<const uint4*>(blk + lane * 32);
-    const uint4 c1 = *reinterpret_cast<const uint4*>(blk + lane * 32 + 16);
-    const int c[8] = {int(c0.x), int(c0.y), int(c0.z), int(c0.w), int(c1.x), int(c1.y), int(c1.z), int(c1.w)};
-    const float d = h2f_bits(*reinterpret_cast<const uint16_t*>(blk + 1024 + lane * 2));
-    return __fmul_rn(__fmul_rn(d, x.sx), __int2float_rn(idot<0, 8>(c, x)));
+  struct Frag {
+    uint4 c0, c1;
+    uint32_t d;
+  };
+  __device__ static void load(const uint8_t* blk, int lane, Frag& f) {
+    f.c0 = *reinterpret_cast<const uint4*>(blk + lane * 32);
+    f.c1 = *reinterpret_cast<const uint4*>(blk + lane * 32 + 16);
+    f.d = *reinterpret_cast<const uint16_t*>(blk + 1024 + lane * 2);
+  }
+  __device__ static float compute(const Frag& f, int lane, const XBlock& x) {
+    const int c[8] = {int(f.c0.x), int(f.c0.y), int(f.c0.z), int(f.c0.w),
+                      int(f.c1.x), int(f.c1.y), int(f.c1.z), int(f.c1.w)};
+    return __fmul_rn(__fmul_rn(h2f_bits(f.d), x.sx), __int2float_rn(idot<0, 8>(c, x)));
   }
 };
 
@@ -144,11 +151,18 @@ template <> struct Pipe<NT_Q4_0> {
     stride = 64;
     size = 16;
   }
-  __device__ static float dot(const uint8_t* blk, int lane, const XBlock& x) {
+  struct Frag {
+    uint4 w;
+    uint32_t d;
+  };
+  __device__ static void load(const uint8_t* blk, int lane, Frag& f) {
+    f.w = *reinterpret_cast<const uint4*>(blk + lane * 16);
+    f.d = *reinterpret_cast<const uint16_t*>(blk + 512 + lane * 2);
+  }
+  __device__ static float compute(const Frag& f, int lane, const XBlock& x) {
     int c[8];
-    nibble_bytes(*reinterpret_cast<const uint4*>(blk + lane * 16), c);
-    const float d = h2f_bits(*reinterpret_cast<const uint16_t*>(blk + 512 + lane * 2));
-    return __fmul_rn(__fmul_rn(d, x.sx), __int2float_rn(idot<0, 8>(c, x) - 8 * (x.t0 + x.t1)));
+    nibble_bytes(f.w, c);
+    return __fmul_rn(__fmul_rn(h2f_bits(f.d), x.sx), __int2float_rn(idot<0, 8>(c, x) - 8 * (x.t0 + x.t1)));
   }
 };
 
@@ -164,10 +178,17 @@ template <> struct Pipe<NT_Q4_K> {
     stride = 64;
     size = 16;
   }
-  __device__ static float dot(const uint8_t* blk, int lane, const XBlock& x) {
+  struct Frag {
+    uint4 w, meta;
+  };
+  __device__ static void load(const uint8_t* blk, int lane, Frag& f) {
+    f.w = *reinterpret_cast<const uint4*>(blk + lane * 16);
+    f.meta = *reinterpret_cast<const uint4*>(blk + 512 + (lane >> 3) * 16);
+  }
+  __device__ static float compute(const Frag& f, int lane, const XBlock& x) {
     int c[8];
-    nibble_bytes(*reinterpret_cast<const uint4*>(blk + lane * 16), c);
-    const uint4 meta = *reinterpret_cast<const uint4*>(blk + 512 + (lane >> 3) * 16);
+    nibble_bytes(f.w, c);
+    const uint4 meta = f.meta;
     const int j = lane & 7;
     // 6-bit fields: sc_j at bit 6j, m_j at bit 6(8+j) of the 96-bit stream (meta.y, meta.z, meta.w)
     const uint64_t lo = uint64_t(meta.y) | (uint64_t(meta.z) << 32);
@@ -206,11 +227,22 @@ template <> struct Pipe<NT_Q6_K> {
       size = 4;
     }
   }
-  __device__ static float dot(const uint8_t* blk, int lane, const XBlock& x) {
-    const uint4 w = *reinterpret_cast<const uint4*>(blk + lane * 16);
-    const uint2 g = *reinterpret_cast<const uint2*>(blk + 512 + lane * 8);
-    const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(blk + 768 + lane * 2);
-    const float d = h2f_bits(*reinterpret_cast<const uint16_t*>(blk + 832 + (lane >> 3) * 2));
+  struct Frag {
+    uint4 w;
+    uint2 g;
+    uint32_t sc2, db;
+  };
+  __device__ static void load(const uint8_t* blk, int lane, Frag& f) {
+    f.w = *reinterpret_cast<const uint4*>(blk + lane * 16);
+    f.g = *reinterpret_cast<const uint2*>(blk + 512 + lane * 8);
+    f.sc2 = *reinterpret_cast<const uint16_t*>(blk + 768 + lane * 2);
+    f.db = *reinterpret_cast<const uint16_t*>(blk + 832 + (lane >> 3) * 2);
+  }
+  __device__ static float compute(const Frag& f, int lane, const XBlock& x) {
+    const uint4 w = f.w;
+    const uint2 g = f.g;
+    const uint32_t sc2 = f.sc2;
+    const float d = h2f_bits(f.db);
     // device high-bit word G (one per 16 elements): byte j holds, for code words
     // W (elements 0..7) and W' (elements 8..15), hi(W,2j) at bits 4-5,
     // hi(W',2j) at bits 6-7, hi(W,2j+1) at bits 0-1, hi(W',2j+1) at bits 2-3
@@ -245,6 +277,14 @@ __device__ __forceinline__ WarpTiles warp_tiles(int64_t nrows, int R, int kiters
   w.stride = int64_t(ncta) * nw;
   w.ntiles = w.g0 < ngroups ? int((ngroups - 1 - w.g0) / w.stride + 1) * kiters : 0;
   return w;
+}
+
+// Dot product of one row unit straight from shared memory.
+template <int FMT>
+__device__ __forceinline__ float pipe_dot(const uint8_t* blk, int lane, const XBlock& x) {
+  typename Pipe<FMT>::Frag f;
+  Pipe<FMT>::load(blk, lane, f);
+  return Pipe<FMT>::compute(f, lane, x);
 }
 
 // Copy cursor of one warp over its tiles.  Every lane issues the same copies
@@ -584,6 +624,48 @@ __device__ __forceinline__ void pipe_loop_w(const GemvArgs& a, int64_t nrows, co
   const uint8_t* rd = wring;                               // slot of the tile being decoded
   const uint8_t* const rd_end = wring + S * R * P::RB;
   const uint8_t* xp = xq + size_t(lane) * kXUnit;          // this lane's x block of the tile
+  if constexpr (H::kAllStaged && S >= 3) {
+    // Operands one tile ahead: the next tile's codes, scales and x block are read
+    // from shared memory while the cursor issues copies, before they are used.
+    typename P::Frag fr[R];
+    XBlock xb;
+    if (w.ntiles > 0) {
+      cp_wait<S - 2>();   // tile 0 has landed
+      __syncwarp();
+#pragma unroll
+      for (int r = 0; r < R; r++) P::load(rd + r * P::RB, lane, fr[r]);
+      load_xblock(xp, xb);
+    }
+#pragma unroll 1
+    for (int t = 0; t < w.ntiles; t++) {
+#pragma unroll
+      for (int r = 0; r < R; r++) acc[r] = __fadd_rn(acc[r], P::compute(fr[r], lane, xb));   // dead rows read zeros
+      rd += R * P::RB;
+      if (rd == rd_end) rd = wring;
+      xp += 32 * kXUnit;
+      if (++c_it == kiters) {
+        // ---- row group done: transposed warp reduction, epilogue ------------
+        c_it = 0;
+        xp = xq + size_t(lane) * kXUnit;
+        float kk = warp_reduce_rows<R>(acc, lane);
+#pragma unroll
+        for (int r = 0; r < R; r++) acc[r] = 0.f;
+        kk = __fmul_rn(kk, scale);
+        epilogue<R, EPI>(a, c_grp, nrows, lane, kk, best, best_i, second);
+        c_grp += w.stride;
+      }
+      cp_wait<S - 3>();   // tile t + 1 has landed
+      __syncwarp();       // ... every lane's copies; the slot of tile t - 1 is free
+#pragma unroll
+      for (int r = 0; r < R; r++) P::load(rd + r * P::RB, lane, fr[r]);
+      load_xblock(xp, xb);
+      cur.template step<true>(a, nrows, lane);   // tile t + S - 1
+    }
+    cp_wait<0>();
+    __syncwarp();
+    if (EPI == EPI_LOGITS) cta_top2<NW>(a, cta, best, best_i, second);
+    return;
+  }
 #pragma unroll 1
   for (int t = 0; t < w.ntiles; t++) {
     cp_wait<S - 2>();     // this lane's copies of the tile have landed
@@ -597,7 +679,7 @@ __device__ __forceinline__ void pipe_loop_w(const GemvArgs& a, int64_t nrows, co
     load_xblock(xp, xb);
     xp += 32 * kXUnit;
 #pragma unroll
-    for (int r = 0; r < R; r++) acc[r] = __fadd_rn(acc[r], P::dot(rd + r * P::RB, lane, xb));   // dead rows read zeros
+    for (int r = 0; r < R; r++) acc[r] = __fadd_rn(acc[r], pipe_dot<FMT>(rd + r * P::RB, lane, xb));   // dead rows read zeros
     rd += R * P::RB;
     if (rd == rd_end) rd = wring;
     if (++c_it < kiters) continue;
