@@ -177,6 +177,26 @@ nt_status nt_kv_export(nt_model* m, int32_t layer, int32_t kv, int32_t kv_head, 
  * n_layers brings every layer back to the device. */
 nt_status nt_stream_layers(nt_model* m, int32_t n_resident, int32_t n_staging);
 
+/* Tier placement ("Tier A" VRAM-resident layers, the rest streamed from pinned
+ * RAM): how many layers of a model with configuration cfg fit in budget_bytes of
+ * device memory next to everything else the model keeps there -- the token
+ * embedding and output tensors, the K/V cache for max_ctx positions, the
+ * activations and partials, and two staging buffers of one layer each when any
+ * layer streams.  All layers have the same size, so the resident ones are the
+ * first n.  Pure host arithmetic on the configuration (no device work).
+ * n_resident (required) receives n in [0, n_layers]; device_bytes (nullable)
+ * the device bytes of that placement; layer_bytes (nullable) the bytes of one
+ * layer.  NT_E_INVAL: invalid configuration or negative budget.
+ * NT_E_NOMEM: not even the non-layer allocations fit (n_resident is set to 0). */
+nt_status nt_plan_residency(const nt_config* cfg, int64_t budget_bytes, int32_t* n_resident, int64_t* device_bytes,
+                            int64_t* layer_bytes);
+
+/* nt_stream_layers with the placement nt_plan_residency gives for the device
+ * memory this model could use now: the driver's free memory plus what the
+ * model already holds, minus margin_bytes.  n_resident_out (nullable) receives
+ * the placement. */
+nt_status nt_auto_residency(nt_model* m, int64_t margin_bytes, int32_t* n_resident_out);
+
 nt_status nt_get_stats(const nt_model* m, nt_stats* out);
 
 /* Runs n_steps decode steps (from token, feeding back argmax) and returns

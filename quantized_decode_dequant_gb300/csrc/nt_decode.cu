@@ -1017,6 +1017,29 @@ nt_status nt_stream_layers(nt_model* m, int32_t n_resident, int32_t n_staging) {
   return NT_OK;
 }
 
+// Device bytes of one layer blob and of everything else a model allocates (see
+// nt_model_create), both with the 256-byte stream padding.
+static void model_bytes(const nt_config& c, int64_t* layer, int64_t* fixed) {
+  const int64_t h = c.hidden, hd = c.head_dim, qd = int64_t(c.n_heads) * hd, kd = int64_t(c.n_kv_heads) * hd;
+  const nt_qtype types[7] = {c.t_q, c.t_k, c.t_v, c.t_o, c.t_gate, c.t_up, c.t_down};
+  const int64_t rows[7] = {qd, kd, kd, h, c.ffn_dim, c.ffn_dim, h};
+  const int64_t colsv[7] = {h, h, h, qd, h, h, c.ffn_dim};
+  int64_t lb = 0;
+  for (int r = 0; r < 7; r++) lb += int64_t(stream_sizes(types[r], rows[r], colsv[r]).padded_total());
+  const int chunk = attn_chunk_len(c.max_ctx);
+  const int64_t n_chunks = (c.max_ctx + chunk - 1) / chunk;
+  int64_t f = int64_t(stream_sizes(c.t_embd, c.vocab, h).padded_total()) +
+              int64_t(stream_sizes(c.t_out, c.vocab, h).padded_total());
+  f += int64_t(c.n_layers) * 2 * kd * c.max_ctx * 2;                      // K/V cache
+  f += 4 * (h + 2 * qd + c.ffn_dim + c.vocab);                            // x, q, att, u, logits
+  f += qd * n_chunks * 4 + int64_t(c.n_heads) * n_chunks * 8;              // attention partials
+  f += int64_t(kMaxGemvGrid) * 16 + int64_t(c.n_kv_heads) * 4 + SYNC_WORDS * 4 + 16 * 4;
+  f += int64_t(c.max_ctx) * 4 + int64_t(c.max_ctx) * (hd / 2) * 8;        // token history, RoPE table
+  f += int64_t(c.n_layers) * 256 * 16;                                    // allocation rounding
+  *layer = lb;
+  *fixed = f;
+}
+
 nt_status nt_get_stats(const nt_model* m, nt_stats* out) {
   if (!m || !out) return fail(NT_E_INVAL, "nt_get_stats: NULL argument");
   *out = m->stats;
@@ -1201,6 +1224,49 @@ nt_status nt_profile_gemvs(nt_model* m, int32_t n_reps, double* ms_per_launch, d
   *ms_per_launch = double(ms) / (double(n_reps) * launches);
   *bytes_per_launch = bytes / launches;
   *launches_per_step = launches;
+  return NT_OK;
+}
+
+nt_status nt_plan_residency(const nt_config* cfg, int64_t budget_bytes, int32_t* n_resident, int64_t* device_bytes,
+                            int64_t* layer_bytes) {
+  if (!cfg || !n_resident) return fail(NT_E_INVAL, "nt_plan_residency: NULL argument");
+  if (budget_bytes < 0) return fail(NT_E_INVAL, "nt_plan_residency: negative budget");
+  nt_status st = validate(cfg);
+  if (st) return st;
+  int64_t layer = 0, fixed = 0;
+  model_bytes(*cfg, &layer, &fixed);
+  const int L = cfg->n_layers;
+  *n_resident = 0;
+  if (layer_bytes) *layer_bytes = layer;
+  int n;
+  if (fixed + int64_t(L) * layer <= budget_bytes) {
+    n = L;   // everything resident: no staging buffers
+  } else {
+    const int64_t room = budget_bytes - fixed - 2 * layer;
+    if (room < 0) {
+      if (device_bytes) *device_bytes = fixed + 2 * layer;
+      return fail(NT_E_NOMEM, "nt_plan_residency: the non-layer allocations and staging buffers exceed the budget");
+    }
+    n = int(room / layer);
+    if (n >= L) n = L - 1;
+  }
+  *n_resident = n;
+  if (device_bytes) *device_bytes = fixed + int64_t(n) * layer + (n < L ? 2 * layer : 0);
+  return NT_OK;
+}
+
+nt_status nt_auto_residency(nt_model* m, int64_t margin_bytes, int32_t* n_resident_out) {
+  if (!m) return fail(NT_E_INVAL, "nt_auto_residency: model is NULL");
+  if (margin_bytes < 0) return fail(NT_E_INVAL, "nt_auto_residency: negative margin");
+  NT_CUDA(cudaStreamSynchronize(m->stream));
+  size_t free_b = 0, total_b = 0;
+  NT_CUDA(cudaMemGetInfo(&free_b, &total_b));
+  const int64_t budget = int64_t(free_b) + int64_t(m->dev_bytes) - margin_bytes;
+  int32_t n = 0;
+  nt_status st = nt_plan_residency(&m->c, budget > 0 ? budget : 0, &n, nullptr, nullptr);
+  if (st) return st;
+  if ((st = nt_stream_layers(m, n, 2))) return st;
+  if (n_resident_out) *n_resident_out = n;
   return NT_OK;
 }
 

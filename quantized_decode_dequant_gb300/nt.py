@@ -75,6 +75,8 @@ _SIGS = {
     "nt_get_stats": (C.c_int, [_vp, C.POINTER(nt_stats)]),
     "nt_profile_steps": (C.c_int, [_vp, _i32, _i32, C.POINTER(nt_kernel_times)]),
     "nt_profile_gemvs": (C.c_int, [_vp, _i32, C.POINTER(C.c_double), C.POINTER(C.c_double), C.POINTER(_i32)]),
+    "nt_plan_residency": (C.c_int, [C.POINTER(nt_config), _i64, C.POINTER(_i32), C.POINTER(_i64), C.POINTER(_i64)]),
+    "nt_auto_residency": (C.c_int, [_vp, _i64, C.POINTER(_i32)]),
     "nt_model_tensor": (C.c_int, [_vp, _i32, _i32, C.POINTER(C.c_void_p)]),
     "nt_qtensor_create": (C.c_int, [C.c_int, _i64, _i64, _u64, C.c_uint32, C.c_float, C.POINTER(C.c_void_p)]),
     "nt_qtensor_destroy": (None, [_vp]),
@@ -212,6 +214,20 @@ def nt_profile_gemvs(m: int, n_reps: int) -> tuple[float, float, int]:
     ms, by, n = C.c_double(), C.c_double(), C.c_int32()
     _check(lib().nt_profile_gemvs(m, n_reps, C.byref(ms), C.byref(by), C.byref(n)), "nt_profile_gemvs")
     return ms.value, by.value, n.value
+
+
+def nt_plan_residency(cfg, budget_bytes: int) -> tuple[int, int, int]:
+    """(layers resident, device bytes of that placement, bytes of one layer) for a budget."""
+    n, dev, lay = C.c_int32(), C.c_int64(), C.c_int64()
+    _check(lib().nt_plan_residency(C.byref(cfg), budget_bytes, C.byref(n), C.byref(dev), C.byref(lay)),
+           "nt_plan_residency")
+    return n.value, dev.value, lay.value
+
+
+def nt_auto_residency(m: int, margin_bytes: int = 1 << 30) -> int:
+    n = C.c_int32()
+    _check(lib().nt_auto_residency(m, margin_bytes, C.byref(n)), "nt_auto_residency")
+    return n.value
 
 
 def nt_model_tensor(m: int, layer: int, role) -> int:

@@ -221,3 +221,31 @@ def test_llama70b_q4_k_m_teacher_forced(nt, W):
             tok = gnx
     finally:
         nt.nt_model_destroy(m)
+
+
+def test_auto_residency_places_layers_and_decodes_the_same(nt, W):
+    """nt_auto_residency keeps a model that fits resident; with a margin that
+    leaves room for only a few layers it streams the rest, bit for bit the same."""
+    import torch
+    spec = dict(W.TINY, n_layers=6)
+    cfg = nt.make_config(**spec, seed=8)
+    a, b = nt.nt_model_create(cfg), nt.nt_model_create(cfg)
+    try:
+        assert nt.nt_auto_residency(a, 1 << 30) == spec["n_layers"]
+        _, dev_all, lay = nt.nt_plan_residency(cfg, 1 << 50)
+        fixed = dev_all - spec["n_layers"] * lay
+        free, _ = torch.cuda.mem_get_info()
+        margin = free + dev_all - (fixed + 5 * lay)          # about three layers resident
+        n = nt.nt_auto_residency(b, margin)
+        assert 1 <= n < spec["n_layers"]
+        assert nt.nt_get_stats(b).n_resident == n
+        la, lb = np.empty(spec["vocab"], np.float32), np.empty(spec["vocab"], np.float32)
+        t = 9
+        for _ in range(4):
+            na, nb = nt.nt_decode_step(a, t, la), nt.nt_decode_step(b, t, lb)
+            np.testing.assert_array_equal(la.view(np.uint32), lb.view(np.uint32))
+            assert na == nb
+            t = na
+    finally:
+        nt.nt_model_destroy(a)
+        nt.nt_model_destroy(b)
