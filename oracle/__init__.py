@@ -95,6 +95,11 @@ def lib():
         L.orc_decode_step.argtypes = [C.c_void_p, C.c_int32, f64p, C.POINTER(C.c_int32), f64p]
         L.orc_kv_get.restype = C.c_uint16
         L.orc_kv_get.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int]
+        L.orc_set_layer_skip.argtypes = [C.c_void_p, u8p]
+        L.orc_layer_cos.argtypes = [C.c_void_p, f64p]
+        L.orc_hidden.argtypes = [C.c_void_p, f64p]
+        L.orc_cosine.restype = C.c_double
+        L.orc_cosine.argtypes = [f64p, f64p, C.c_int64]
         _lib = L
     return _lib
 
@@ -231,6 +236,29 @@ def attend(q: np.ndarray, k_f16: np.ndarray, v_f16: np.ndarray) -> np.ndarray:
     return out
 
 
+def cosine(a: np.ndarray, b: np.ndarray) -> float:
+    """Cosine similarity of two vectors in fp64 (0 when either is zero)."""
+    a = np.ascontiguousarray(a, np.float64)
+    b = np.ascontiguousarray(b, np.float64)
+    return float(lib().orc_cosine(_p(a, C.c_double), _p(b, C.c_double), a.size))
+
+
+def plan_layer_skip(cos, threshold: float, max_skip: int = 0) -> np.ndarray:
+    """Which layers to skip from their calibrated similarities ([hotdry]
+    "性能数据与瓶颈分析": layers whose similarity is at or above the threshold,
+    0.98 there, are skipped).  Reading: every layer with cos >= threshold; when
+    max_skip > 0 and more qualify, the max_skip most similar ones (ties: lower
+    layer first).  Returns a uint8 mask."""
+    cand = [(-float(c), l) for l, c in enumerate(cos) if float(c) >= threshold]
+    cand.sort()
+    if max_skip > 0:
+        cand = cand[:max_skip]
+    mask = np.zeros(len(cos), np.uint8)
+    for _, l in cand:
+        mask[l] = 1
+    return mask
+
+
 def argmax(x: np.ndarray) -> tuple[int, float]:
     x = np.ascontiguousarray(x, np.float64)
     m = C.c_double()
@@ -328,3 +356,25 @@ class Model:
         if rc:
             raise RuntimeError(f"orc_decode_step failed ({rc})")
         return lg, int(nx.value), float(mg.value)
+
+    def set_layer_skip(self, mask):
+        """Skips the layers whose mask entry is nonzero (None: none)."""
+        if mask is None:
+            lib().orc_set_layer_skip(self._h, None)
+            return
+        m = np.ascontiguousarray(np.asarray(mask).astype(np.uint8))
+        assert m.size == self.spec.n_layers
+        if lib().orc_set_layer_skip(self._h, _p(m, C.c_uint8)):
+            raise MemoryError("orc_set_layer_skip")
+
+    def layer_cos(self) -> np.ndarray:
+        """Per layer, last step: cosine between the residual stream entering and leaving it."""
+        out = np.empty(self.spec.n_layers, np.float64)
+        lib().orc_layer_cos(self._h, _p(out, C.c_double))
+        return out
+
+    def hidden(self) -> np.ndarray:
+        """Last step: the residual stream after the last layer."""
+        out = np.empty(self.spec.hidden, np.float64)
+        lib().orc_hidden(self._h, _p(out, C.c_double))
+        return out

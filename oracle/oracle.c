@@ -499,6 +499,9 @@ struct orc_model {
   uint8_t** layer;       /* [n_layers][7] tensors (NULL entries when lazy)                           */
   uint16_t* kv;          /* [n_layers][2][n_kv_heads][max_ctx][head_dim] binary16                    */
   int32_t pos;
+  uint8_t* skip;         /* [n_layers]: 1 = layer skipped (NULL: none)                               */
+  double* layer_cos;     /* [n_layers]: cosine between the residual entering and leaving each layer  */
+  double* hidden;        /* [hidden]: residual stream after the last layer, last step                */
 };
 
 static void role_shape(const orc_config* c, int role, int64_t* rows, int64_t* cols, int* qt) {
@@ -540,7 +543,9 @@ orc_model* orc_model_create(const orc_config* cfg) {
   m->layer = (uint8_t**)calloc((size_t)c->n_layers * 7, sizeof(uint8_t*));
   size_t kvn = (size_t)c->n_layers * 2 * c->n_kv_heads * (size_t)c->max_ctx * c->head_dim;
   m->kv = (uint16_t*)calloc(kvn > 0 ? kvn : 1, sizeof(uint16_t));
-  if (!m->layer || !m->kv) { orc_model_destroy(m); return NULL; }
+  m->layer_cos = (double*)calloc((size_t)(c->n_layers > 0 ? c->n_layers : 1), sizeof(double));
+  m->hidden = (double*)calloc((size_t)c->hidden, sizeof(double));
+  if (!m->layer || !m->kv || !m->layer_cos || !m->hidden) { orc_model_destroy(m); return NULL; }
   if (!c->lazy) {
     m->embd = gen_tensor(c, c->t_embd, c->vocab, c->hidden, ORC_UID_EMBD);
     m->output = gen_tensor(c, c->t_out, c->vocab, c->hidden, ORC_UID_OUTPUT);
@@ -562,7 +567,45 @@ void orc_model_destroy(orc_model* m) {
   free(m->embd);
   free(m->output);
   free(m->kv);
+  free(m->skip);
+  free(m->layer_cos);
+  free(m->hidden);
   free(m);
+}
+
+/* Layer skip ([hada] "Hauptfunktionen": layers skipped by cosine similarity;
+ * [hotdry] "性能数据与瓶颈分析": similarity between layer outputs is computed
+ * beforehand and layers above the threshold are skipped at inference).  Reading:
+ * a skipped layer is not evaluated at all -- the residual stream passes through
+ * unchanged and no K/V row is written for it. */
+int orc_set_layer_skip(orc_model* m, const uint8_t* mask) {
+  if (!mask) {
+    free(m->skip);
+    m->skip = NULL;
+    return 0;
+  }
+  if (!m->skip) m->skip = (uint8_t*)malloc((size_t)(m->c.n_layers > 0 ? m->c.n_layers : 1));
+  if (!m->skip) return -2;
+  for (int l = 0; l < m->c.n_layers; l++) m->skip[l] = mask[l] ? 1 : 0;
+  return 0;
+}
+
+void orc_layer_cos(const orc_model* m, double* out) {
+  memcpy(out, m->layer_cos, sizeof(double) * (size_t)m->c.n_layers);
+}
+
+void orc_hidden(const orc_model* m, double* out) { memcpy(out, m->hidden, sizeof(double) * (size_t)m->c.hidden); }
+
+/* cos(a, b) = sum a_i b_i / (sqrt(sum a_i^2) sqrt(sum b_i^2)); 0 when either is the zero vector. */
+double orc_cosine(const double* a, const double* b, int64_t n) {
+  double ab = 0, aa = 0, bb = 0;
+  for (int64_t i = 0; i < n; i++) {
+    ab += a[i] * b[i];
+    aa += a[i] * a[i];
+    bb += b[i] * b[i];
+  }
+  if (aa == 0 || bb == 0) return 0;
+  return ab / (sqrt(aa) * sqrt(bb));
 }
 
 int32_t orc_pos(const orc_model* m) { return m->pos; }
@@ -631,12 +674,13 @@ int orc_decode_step(orc_model* m, int32_t token, double* logits, int32_t* next, 
   double *t = (double*)malloc(sizeof(double) * (h > f ? h : f));
   double *g = (double*)malloc(sizeof(double) * f), *u = (double*)malloc(sizeof(double) * f);
   double *lg = (double*)malloc(sizeof(double) * c->vocab);
+  double *x_in = (double*)malloc(sizeof(double) * h);
   float* row = (float*)malloc(sizeof(float) * h);
   uint16_t *kc = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(pos + 1) * hd);
   uint16_t *vc = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(pos + 1) * hd);
   uint8_t* er = (uint8_t*)malloc((size_t)row_bytes(c->t_embd, h));
   int rc = 0;
-  if (!x || !xn || !q || !k || !v || !o || !t || !g || !u || !lg || !row || !kc || !vc || !er) { rc = -2; goto done; }
+  if (!x || !xn || !q || !k || !v || !o || !t || !g || !u || !lg || !x_in || !row || !kc || !vc || !er) { rc = -2; goto done; }
 
   /* embedding row */
   if (m->embd) memcpy(er, m->embd + (int64_t)token * row_bytes(c->t_embd, h), (size_t)row_bytes(c->t_embd, h));
@@ -645,6 +689,11 @@ int orc_decode_step(orc_model* m, int32_t token, double* logits, int32_t* next, 
   for (int64_t i = 0; i < h; i++) x[i] = (double)row[i];
 
   for (int l = 0; l < c->n_layers; l++) {
+    if (m->skip && m->skip[l]) {
+      m->layer_cos[l] = 1.0;
+      continue;
+    }
+    memcpy(x_in, x, sizeof(double) * h);
     orc_rmsnorm(x, h, c->rms_eps, xn);
     if ((rc = gemv_role(m, l, ORC_ROLE_Q, xn, q))) goto done;
     if ((rc = gemv_role(m, l, ORC_ROLE_K, xn, k))) goto done;
@@ -674,7 +723,9 @@ int orc_decode_step(orc_model* m, int32_t token, double* logits, int32_t* next, 
     for (int64_t i = 0; i < f; i++) u[i] = orc_silu(g[i]) * u[i];
     if ((rc = gemv_role(m, l, ORC_ROLE_DOWN, u, t))) goto done;
     for (int64_t i = 0; i < h; i++) x[i] += t[i];
+    m->layer_cos[l] = orc_cosine(x_in, x, h);
   }
+  memcpy(m->hidden, x, sizeof(double) * h);
   orc_rmsnorm(x, h, c->rms_eps, xn);
   {
     uint8_t* w = m->output;
@@ -694,7 +745,7 @@ int orc_decode_step(orc_model* m, int32_t token, double* logits, int32_t* next, 
   }
   m->pos = (int32_t)(pos + 1);
 done:
-  free(x); free(xn); free(q); free(k); free(v); free(o); free(t); free(g); free(u); free(lg);
+  free(x); free(x_in); free(xn); free(q); free(k); free(v); free(o); free(t); free(g); free(u); free(lg);
   free(row); free(kc); free(vc); free(er);
   return rc;
 }

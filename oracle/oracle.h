@@ -103,6 +103,13 @@ int32_t    orc_pos(const orc_model* m);
 void       orc_set_threads(orc_model* m, int32_t nthreads);
 /* logits (vocab doubles, nullable), next token, top-2 margin (nullable) */
 int        orc_decode_step(orc_model* m, int32_t token, double* logits, int32_t* next, double* margin);
+/* Layer skip: mask[l] != 0 skips layer l (no arithmetic, no K/V row); NULL clears. */
+int        orc_set_layer_skip(orc_model* m, const uint8_t* mask);
+/* last step: cosine similarity between the residual entering and leaving each layer (1 when skipped) */
+void       orc_layer_cos(const orc_model* m, double* out);
+/* last step: residual stream after the last layer (before the output norm) */
+void       orc_hidden(const orc_model* m, double* out);
+double     orc_cosine(const double* a, const double* b, int64_t n);
 /* read one cached f16 value (for tests) */
 uint16_t   orc_kv_get(const orc_model* m, int layer, int kv, int kv_head, int t, int d);
 

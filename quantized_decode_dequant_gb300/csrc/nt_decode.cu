@@ -172,7 +172,7 @@ struct nt_model {
   cudaEvent_t ev_step0 = nullptr, ev_step1 = nullptr;
   nt_stats stats{};
   size_t dev_bytes = 0, dev_limit = 0;
-  std::vector<void*> dev_allocs;
+  std::vector<std::pair<void*, size_t>> dev_allocs;   // live device allocations and their sizes
 };
 
 namespace nt {
@@ -187,7 +187,7 @@ static cudaError_t dev_alloc(nt_model* m, void** p, size_t bytes) {
   cudaError_t e = cudaMalloc(p, bytes ? bytes : 1);
   if (e == cudaSuccess) {
     m->dev_bytes += bytes;
-    m->dev_allocs.push_back(*p);
+    m->dev_allocs.emplace_back(*p, bytes);
   }
   return e;
 }
@@ -195,7 +195,8 @@ static cudaError_t dev_alloc(nt_model* m, void** p, size_t bytes) {
 static void dev_free(nt_model* m, void* p) {
   if (!p) return;
   for (size_t i = 0; i < m->dev_allocs.size(); i++)
-    if (m->dev_allocs[i] == p) {
+    if (m->dev_allocs[i].first == p) {
+      m->dev_bytes -= m->dev_allocs[i].second;
       m->dev_allocs.erase(m->dev_allocs.begin() + long(i));
       break;
     }
@@ -650,7 +651,7 @@ static void free_model(nt_model* m) {
   drop_graph(m);
   for (auto& L : m->layers)
     if (L.host) cudaFreeHost(L.host);
-  for (void* p : m->dev_allocs) cudaFree(p);
+  for (auto& a : m->dev_allocs) cudaFree(a.first);
   m->dev_allocs.clear();
   if (m->h_io) cudaFreeHost(m->h_io);
   for (int b = 0; b < 2; b++) {
@@ -991,7 +992,6 @@ nt_status nt_stream_layers(nt_model* m, int32_t n_resident, int32_t n_staging) {
       cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&L.host), L.bytes, cudaHostAllocDefault);
       if (e) return cuda_fail(e, "nt_stream_layers: cudaHostAlloc (page-locked tier)");
       NT_CUDA(cudaMemcpy(L.host, L.dev, L.bytes, cudaMemcpyDeviceToHost));
-      m->dev_bytes -= L.bytes;
       dev_free(m, L.dev);
       L.dev = nullptr;
     }
@@ -1003,7 +1003,6 @@ nt_status nt_stream_layers(nt_model* m, int32_t n_resident, int32_t n_staging) {
   }
   for (int b = 0; b < 2; b++) {
     if (m->staging[b]) {
-      m->dev_bytes -= 0;
       dev_free(m, m->staging[b]);
       m->staging[b] = nullptr;
     }

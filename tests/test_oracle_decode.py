@@ -116,3 +116,68 @@ def test_decode_deterministic_lazy_equals_resident_and_position_limit():
     c = oracle.Model(spec)
     l1, _, _ = c.decode_step(toks[0])
     np.testing.assert_array_equal(l0, l1)
+
+
+# ---- layer skip (cosine similarity between the residual entering and leaving a layer)
+
+def test_cosine_closed_forms():
+    a = np.array([3.0, 4.0])
+    assert oracle.cosine(a, np.array([4.0, 3.0])) == pytest.approx(24 / 25, abs=1e-15)
+    assert oracle.cosine(np.array([1.0, 0.0]), np.array([0.0, 2.0])) == 0.0
+    assert oracle.cosine(a, 2.5 * a) == pytest.approx(1.0, abs=1e-15)
+    assert oracle.cosine(a, -a) == pytest.approx(-1.0, abs=1e-15)
+    assert oracle.cosine(a, np.zeros(2)) == 0.0
+    # 45 degrees: (1, 0) against (1, 1)
+    assert oracle.cosine(np.array([1.0, 0.0]), np.array([1.0, 1.0])) == pytest.approx(np.sqrt(0.5), abs=1e-15)
+
+
+def test_skipping_the_last_layers_equals_a_shallower_model():
+    deep, shallow = oracle.Model(_spec(n_layers=3)), oracle.Model(_spec(n_layers=1))
+    deep.set_layer_skip([0, 1, 1])
+    for t in oracle.tokens(4, 3, TINY["vocab"]):
+        ld, nd, md = deep.decode_step(t)
+        ls, ns, ms = shallow.decode_step(t)
+        np.testing.assert_array_equal(ld, ls)
+        assert (nd, md) == (ns, ms)
+        np.testing.assert_array_equal(deep.hidden(), shallow.hidden())
+    # skipped layers write no K/V row and report similarity 1
+    assert all(deep.kv_get(l, kv, g, 2, d) == 0 for l in (1, 2) for kv in (0, 1) for g in (0, 1) for d in (0, 63))
+    assert deep.kv_get(0, 0, 0, 2, 0) == shallow.kv_get(0, 0, 0, 2, 0)
+    np.testing.assert_array_equal(deep.layer_cos()[1:], [1.0, 1.0])
+    # skipping every layer is the zero-layer model
+    every, none = oracle.Model(_spec(n_layers=2)), oracle.Model(_spec(n_layers=0))
+    every.set_layer_skip([1, 1])
+    np.testing.assert_array_equal(every.decode_step(9)[0], none.decode_step(9)[0])
+    # clearing the mask restores the full model
+    full, cleared = oracle.Model(_spec()), oracle.Model(_spec())
+    cleared.set_layer_skip([1, 0])
+    cleared.set_layer_skip(None)
+    np.testing.assert_array_equal(full.decode_step(3)[0], cleared.decode_step(3)[0])
+
+
+def test_layer_similarity_is_the_cosine_of_consecutive_residuals():
+    # layer L-1's similarity compares the residuals after L-1 and after L layers,
+    # which the (L-1)- and L-layer models give independently
+    toks = oracle.tokens(6, 3, TINY["vocab"])
+    models = [oracle.Model(_spec(n_layers=n)) for n in (1, 2, 3)]
+    for t in toks:
+        for m in models:
+            m.decode_step(t)
+    h = [_embed(_spec(), toks[-1])] + [m.hidden() for m in models]
+    for n in (1, 2, 3):
+        cos = models[n - 1].layer_cos()
+        assert cos[n - 1] == pytest.approx(oracle.cosine(h[n - 1], h[n]), abs=1e-15)
+    # the one-layer step at position 0 worked out from its parts above
+    m = oracle.Model(_spec(n_layers=1))
+    m.decode_step(toks[0])
+    x0 = _embed(_spec(), toks[0])
+    assert m.layer_cos()[0] == pytest.approx(oracle.cosine(x0, m.hidden()), abs=1e-15)
+    assert -1.0 <= m.layer_cos()[0] <= 1.0
+
+
+def test_skip_plan_threshold_and_cap():
+    cos = [0.5, 0.99, 0.97, 0.98, 0.995, 0.99]
+    np.testing.assert_array_equal(oracle.plan_layer_skip(cos, 0.98), [0, 1, 0, 1, 1, 1])
+    np.testing.assert_array_equal(oracle.plan_layer_skip(cos, 0.98, max_skip=2), [0, 1, 0, 0, 1, 0])  # tie: lower layer
+    np.testing.assert_array_equal(oracle.plan_layer_skip(cos, 0.999), [0] * 6)
+    np.testing.assert_array_equal(oracle.plan_layer_skip(cos, -1.0, max_skip=1), [0, 0, 0, 0, 1, 0])
