@@ -18,9 +18,9 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
-QTYPES = {"f32": 0, "f16": 1, "q8_0": 2, "q4_0": 3, "q4_k": 4, "q6_k": 5}
-BLOCK_ELEMS = {"f32": 1, "f16": 1, "q8_0": 32, "q4_0": 32, "q4_k": 256, "q6_k": 256}
-BLOCK_BYTES = {"f32": 4, "f16": 2, "q8_0": 34, "q4_0": 18, "q4_k": 144, "q6_k": 210}
+QTYPES = {"f32": 0, "f16": 1, "q8_0": 2, "q4_0": 3, "q4_k": 4, "q6_k": 5, "q5_k": 6}
+BLOCK_ELEMS = {"f32": 1, "f16": 1, "q8_0": 32, "q4_0": 32, "q4_k": 256, "q6_k": 256, "q5_k": 256}
+BLOCK_BYTES = {"f32": 4, "f16": 2, "q8_0": 34, "q4_0": 18, "q4_k": 144, "q6_k": 210, "q5_k": 176}
 
 UID_EMBD = 0x100000
 UID_OUTPUT = 0x100001

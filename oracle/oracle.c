@@ -21,7 +21,7 @@ int orc_block_elems(int qtype) {
   switch (qtype) {
     case ORC_F32: case ORC_F16: return 1;
     case ORC_Q8_0: case ORC_Q4_0: return 32;
-    case ORC_Q4_K: case ORC_Q6_K: return 256;
+    case ORC_Q4_K: case ORC_Q5_K: case ORC_Q6_K: return 256;
   }
   return 0;
 }
@@ -34,6 +34,7 @@ int orc_block_bytes(int qtype) {
     case ORC_Q4_0: return 18;   /* f16 d | u8 qs[16]                          */
     case ORC_Q4_K: return 144;  /* f16 d | f16 dmin | 12 B scales | u8 qs[128] */
     case ORC_Q6_K: return 210;  /* u8 ql[128] | u8 qh[64] | int8 sc[16] | f16 d */
+    case ORC_Q5_K: return 176;  /* f16 d | f16 dmin | 12 B scales | u8 qh[32] | u8 qs[128] */
   }
   return 0;
 }
@@ -153,6 +154,16 @@ static int get_q6(const uint8_t* ql, const uint8_t* qh, int k) {
   return get_nib(ql, k) | (((qh[k >> 2] >> (2 * (k & 3))) & 3) << 4);
 }
 
+/* Q5_K codes: low 4 bits as the 4-bit layout in qs[128]; the fifth bit of
+ * element k in qh[k/8] at bit k%8. */
+static void put_q5(uint8_t* qs, uint8_t* qh, int k, int q) {
+  put_nib(qs, k, q & 0x0F);
+  qh[k >> 3] = (uint8_t)((qh[k >> 3] & ~(1u << (k & 7))) | (((q >> 4) & 1) << (k & 7)));
+}
+static int get_q5(const uint8_t* qs, const uint8_t* qh, int k) {
+  return get_nib(qs, k) | (((qh[k >> 3] >> (k & 7)) & 1) << 4);
+}
+
 /* Q8_0: d32 = absmax/127, d = f16(d32), q = clamp(round(w/d32), -127, 127). */
 static void quant_q8_0(const float* w, uint8_t* blk) {
   float amax = 0.0f;
@@ -217,6 +228,46 @@ static void quant_q4_k(const float* w, uint8_t* blk) {
   }
 }
 
+/* Q5_K: the Q4_K rule with 32 levels: per 32-element sub-block j: lo = min(0, min w),
+ * hi = max w, s_j = (hi - lo)/31, m*_j = -lo; d = f16(max s / 63),
+ * dmin = f16(max m* / 63); sc_j = clamp(round(s_j/d), 0, 63),
+ * m_j = clamp(round(m*_j/dmin), 0, 63); q = clamp(round((w + dmin*m_j) / (d*sc_j)), 0, 31),
+ * 0 where d*sc_j = 0. */
+static void quant_q5_k(const float* w, uint8_t* blk) {
+  float s[8], ms[8], smax = 0.0f, mmax = 0.0f;
+  for (int j = 0; j < 8; j++) {
+    float lo = 0.0f, hi = w[32 * j];
+    for (int k = 0; k < 32; k++) {
+      lo = fminf(lo, w[32 * j + k]);
+      hi = fmaxf(hi, w[32 * j + k]);
+    }
+    s[j] = (hi - lo) / 31.0f;
+    ms[j] = -lo;
+    smax = fmaxf(smax, s[j]);
+    mmax = fmaxf(mmax, ms[j]);
+  }
+  uint16_t dh = f2h(smax / 63.0f), mh = f2h(mmax / 63.0f);
+  float d = h2f(dh), dmin = h2f(mh);
+  put16(blk, dh);
+  put16(blk + 2, mh);
+  memset(blk + 4, 0, 12 + 32 + 128);
+  int sc[8], mm[8];
+  for (int j = 0; j < 8; j++) {
+    sc[j] = (d == 0.0f) ? 0 : clampi(rnd(s[j] / d), 0, 63);
+    mm[j] = (dmin == 0.0f) ? 0 : clampi(rnd(ms[j] / dmin), 0, 63);
+    put6(blk + 4, j, sc[j]);
+    put6(blk + 4, 8 + j, mm[j]);
+  }
+  for (int j = 0; j < 8; j++) {
+    float a = d * (float)sc[j];
+    float b = dmin * (float)mm[j];
+    for (int k = 0; k < 32; k++) {
+      int q = (a == 0.0f) ? 0 : clampi(rnd((w[32 * j + k] + b) / a), 0, 31);
+      put_q5(blk + 48, blk + 16, 32 * j + k, q);
+    }
+  }
+}
+
 /* Q6_K: per 16-element sub-block j: s_j = absmax/31; d = f16(max s / 127);
  * sc_j = clamp(round(s_j/d), 0, 127); q = clamp(round(w/(d*sc_j)) + 32, 0, 63),
  * 32 where d*sc_j = 0. */
@@ -259,6 +310,7 @@ int orc_quantize_row(int qtype, const float* w, int64_t n, uint8_t* blocks) {
       case ORC_Q4_0: quant_q4_0(wb, ob); break;
       case ORC_Q4_K: quant_q4_k(wb, ob); break;
       case ORC_Q6_K: quant_q6_k(wb, ob); break;
+      case ORC_Q5_K: quant_q5_k(wb, ob); break;
     }
   }
   return 0;
@@ -268,6 +320,7 @@ int orc_quantize_row(int qtype, const float* w, int64_t n, uint8_t* blocks) {
  *   Q8_0  w = d * q
  *   Q4_0  w = d * (q - 8)
  *   Q4_K  w = fma(d*sc, q, -(dmin*m))     (a single fused multiply-add)
+ *   Q5_K  w = fma(d*sc, q, -(dmin*m))     (as Q4_K, q in 0..31)
  *   Q6_K  w = (d*sc) * (q - 32)                                              */
 int orc_dequant_row(int qtype, const uint8_t* blocks, int64_t n, float* w) {
   int qk = orc_block_elems(qtype), bb = orc_block_bytes(qtype);
@@ -293,6 +346,15 @@ int orc_dequant_row(int qtype, const uint8_t* blocks, int64_t n, float* w) {
           float bm = dmin * (float)get6(blk + 4, 8 + j);
           for (int k = 0; k < 32; k++)
             wb[32 * j + k] = fmaf(a, (float)get_nib(blk + 16, 32 * j + k), -bm);
+        }
+      } break;
+      case ORC_Q5_K: {
+        float d = h2f(get16(blk)), dmin = h2f(get16(blk + 2));
+        for (int j = 0; j < 8; j++) {
+          float a = d * (float)get6(blk + 4, j);
+          float bm = dmin * (float)get6(blk + 4, 8 + j);
+          for (int k = 0; k < 32; k++)
+            wb[32 * j + k] = fmaf(a, (float)get_q5(blk + 48, blk + 16, 32 * j + k), -bm);
         }
       } break;
       case ORC_Q6_K: {

@@ -34,7 +34,7 @@ extern "C" {
 #endif
 
 /* Format codes used by the oracle (its own numbering). */
-enum { ORC_F32 = 0, ORC_F16 = 1, ORC_Q8_0 = 2, ORC_Q4_0 = 3, ORC_Q4_K = 4, ORC_Q6_K = 5 };
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_Q8_0 = 2, ORC_Q4_0 = 3, ORC_Q4_K = 4, ORC_Q6_K = 5, ORC_Q5_K = 6 };
 
 /* Elements per block and bytes per block of each quantized format. */
 int orc_block_elems(int qtype);

@@ -7,10 +7,10 @@ import numpy as np
 import pytest
 
 import oracle
-from blockspec import pack_q4_0, pack_q4_k, pack_q6_k, pack_q8_0
+from blockspec import pack_q4_0, pack_q4_k, pack_q5_k, pack_q6_k, pack_q8_0
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-FORMATS = ["q8_0", "q4_0", "q4_k", "q6_k"]
+FORMATS = ["q8_0", "q4_0", "q4_k", "q6_k", "q5_k"]
 
 
 # ---------------------------------------------------------------- dequant --
@@ -41,6 +41,20 @@ def test_dequant_q4_k_uniform_scale_gives_3q_minus_1():
     q = [k % 16 for k in range(256)]
     w = oracle.dequant_row("q4_k", np.frombuffer(pack_q4_k(1.0, 0.5, [3] * 8, [2] * 8, q), np.uint8), 256)
     np.testing.assert_array_equal(w, 3 * np.array(q, np.float32) - 1)
+
+
+def test_dequant_q5_k_hand_block():
+    # d = 1, dmin = 0.5, sub-block j: sc = j+1, m = 2j  ->  w = (j+1) q - j, q in 0..31
+    sc = [j + 1 for j in range(8)]
+    m = [2 * j for j in range(8)]
+    q = [(k * 7) % 32 for k in range(256)]
+    w = oracle.dequant_row("q5_k", np.frombuffer(pack_q5_k(1.0, 0.5, sc, m, q), np.uint8), 256)
+    want = [(k // 32 + 1) * q[k] - k // 32 for k in range(256)]
+    np.testing.assert_array_equal(w, np.array(want, np.float32))
+    # uniform sc = 3, m = 2: 3q - 1 for q = 0..31 (the fifth bit carries 16)
+    q2 = [k % 32 for k in range(256)]
+    w2 = oracle.dequant_row("q5_k", np.frombuffer(pack_q5_k(1.0, 0.5, [3] * 8, [2] * 8, q2), np.uint8), 256)
+    np.testing.assert_array_equal(w2, 3 * np.array(q2, np.float32) - 1)
 
 
 def test_dequant_q6_k_hand_block():
@@ -88,6 +102,18 @@ def test_quantize_q4_k_exact_grid_roundtrip():
     np.testing.assert_array_equal(oracle.dequant_row("q4_k", np.frombuffer(got, np.uint8), 256), w)
 
 
+def test_quantize_q5_k_exact_grid_roundtrip():
+    # as the Q4_K case with q = 0..31 present in every sub-block: lo = -m_j 2^-9,
+    # s_j = 31 sc_j 2^-8 / 31 = sc_j 2^-8, d = 2^-8, dmin = 2^-9
+    sc = [63 - 7 * j for j in range(8)]
+    m = [9 * j for j in range(8)]
+    q = [(k * 13 + j) % 32 for j in range(8) for k in range(32)]
+    w = np.array([-m[k // 32] * 2.0**-9 + q[k] * sc[k // 32] * 2.0**-8 for k in range(256)], np.float32)
+    got = oracle.quantize_row("q5_k", w).tobytes()
+    assert got == pack_q5_k(2.0**-8, 2.0**-9, sc, m, q)
+    np.testing.assert_array_equal(oracle.dequant_row("q5_k", np.frombuffer(got, np.uint8), 256), w)
+
+
 def test_quantize_q6_k_exact_grid_roundtrip():
     # amax_j = 31 sc_j 2^-10 -> s_j = sc_j 2^-10; max sc = 127 -> d = 2^-10.
     sc = [127 - 8 * j for j in range(16)]
@@ -126,6 +152,12 @@ def _block_bound(fmt, wb):
         d, dmin = _f16(s.max() / 63), _f16((-lo).max() / 63)
         # half a step plus the shift of the grid from rounding sc and m
         return (s + d / 2).max() / 2 + 15 * d / 2 + dmin / 2
+    if fmt == "q5_k":
+        sub = wb.reshape(8, 32)
+        lo = np.minimum(0, sub.min(1))
+        s = (sub.max(1) - lo) / 31
+        d, dmin = _f16(s.max() / 63), _f16((-lo).max() / 63)
+        return (s + d / 2).max() / 2 + 31 * d / 2 + dmin / 2
     if fmt == "q6_k":
         sub = wb.reshape(16, 16)
         s = np.abs(sub).max(1) / 31
@@ -148,7 +180,7 @@ def test_roundtrip_error_within_rule_bound(fmt):
         assert err[sl].max() <= bound, (fmt, i, err[sl].max(), bound)
     # and the typical error is a fraction of one step (uniform rounding error)
     rel = np.sqrt(np.mean(err**2)) / np.sqrt(np.mean(w.astype(np.float64) ** 2))
-    assert rel < {"q8_0": 0.012, "q4_0": 0.2, "q4_k": 0.12, "q6_k": 0.05}[fmt], rel
+    assert rel < {"q8_0": 0.012, "q4_0": 0.2, "q4_k": 0.12, "q6_k": 0.05, "q5_k": 0.06}[fmt], rel
 
 
 def test_q8_0_absmax_element_maps_to_127():
@@ -166,6 +198,22 @@ def test_q4_k_all_positive_sub_block_has_zero_min():
     bits = int.from_bytes(bytes(b[4:16]), "little")
     assert all(((bits >> (6 * (8 + j))) & 63) == 0 for j in range(8))
     assert b[2] == 0 and b[3] == 0            # dmin = f16(0)
+
+
+def test_q5_k_fifth_bit_and_all_positive_min():
+    # an all-positive sub-block has m = 0 (dmin = 0); its largest element takes code 31
+    w = np.abs(oracle.gen_normal(2, 6, 0, 256, 0.02))
+    b = oracle.quantize_row("q5_k", w)
+    bits = int.from_bytes(bytes(b[4:16]), "little")
+    assert all(((bits >> (6 * (8 + j))) & 63) == 0 for j in range(8))
+    assert b[2] == 0 and b[3] == 0
+    qh, qs = bytes(b[16:48]), bytes(b[48:176])
+    code = [((qs[k // 2] >> (4 * (k % 2))) & 15) | (((qh[k // 8] >> (k % 8)) & 1) << 4) for k in range(256)]
+    for j in range(8):
+        sub = w[32 * j:32 * j + 32]
+        assert code[32 * j + int(np.argmax(sub))] >= 30      # top of the 0..31 grid (sc is rounded)
+    # every code uses 0..31 and both halves of the grid occur (the fifth bit is used)
+    assert max(code) <= 31 and any(c >= 16 for c in code) and any(c < 16 for c in code)
 
 
 def test_qtensor_rows_is_rowwise_generate_then_quantize():
@@ -194,6 +242,13 @@ def _rand_dyadic_block(fmt, rng):
         vals = [Fraction(sc[k // 32] * q[k]) * Fraction(2) ** e - Fraction(m[k // 32]) * Fraction(2) ** em
                 for k in range(256)]
         return pack_q4_k(2.0**e, 2.0**em, sc, m, q), vals
+    if fmt == "q5_k":
+        e, em = int(rng.integers(-8, -2)), int(rng.integers(-8, -2))
+        sc = rng.integers(0, 64, 8).tolist(); m = rng.integers(0, 64, 8).tolist()
+        q = rng.integers(0, 32, 256).tolist()
+        vals = [Fraction(sc[k // 32] * q[k]) * Fraction(2) ** e - Fraction(m[k // 32]) * Fraction(2) ** em
+                for k in range(256)]
+        return pack_q5_k(2.0**e, 2.0**em, sc, m, q), vals
     e = int(rng.integers(-10, -4)); sc = rng.integers(-128, 128, 16).tolist(); q = rng.integers(0, 64, 256).tolist()
     return pack_q6_k(2.0**e, sc, q), [Fraction(sc[k // 16] * (q[k] - 32)) * Fraction(2) ** e for k in range(256)]
 
