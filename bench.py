@@ -49,6 +49,9 @@ def parse_args(argv=None):
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--profile-gemv", nargs=4, metavar=("FMT", "ROWS", "COLS", "LAUNCHES"))
+    p.add_argument("--layer-skip", type=int, default=0, metavar="MAX",
+                   help="calibrate per-layer similarity, then skip up to MAX layers at or above --skip-threshold")
+    p.add_argument("--skip-threshold", type=float, default=0.98)
     p.add_argument("--layers", type=int, default=None,
                    help="profiling aid: the workload's shapes with this many layers (not a bench line)")
     return p.parse_args(argv)
@@ -366,6 +369,10 @@ def run_ours(args, wl, rank, world, local, dist):
             else:
                 nt.nt_kv_reset(m)
 
+        skip_info = None
+        if args.layer_skip > 0:
+            skip_info = calibrate_skip(nt, m, reset, tok0, spec, args.layer_skip, args.skip_threshold)
+
         # ---- warm-up
         reset()
         if streamed:
@@ -432,6 +439,10 @@ def run_ours(args, wl, rank, world, local, dist):
         kernel_classes = None
         stats = nt.nt_get_stats(m)
         step_bytes = stats.weight_bytes + stats.kv_bytes_per_pos * (wl["ctx"] + args.steps / 2)
+        if skip_info:   # skipped layers' weights and cache are not read
+            frac_kv = 1.0 - skip_info["n_skipped"] / spec["n_layers"]
+            step_bytes = (stats.weight_bytes - skip_info["weight_bytes_saved_per_token"]
+                          + stats.kv_bytes_per_pos * frac_kv * (wl["ctx"] + args.steps / 2))
         if not streamed:
             reset()
             n_prof = max(4, min(args.steps, 32))
@@ -501,10 +512,37 @@ def run_ours(args, wl, rank, world, local, dist):
             "clocks": clocks.summary(), "first_tokens": tokens}
     if h2d_stats:
         line["streaming"] = h2d_stats
+    if skip_info:
+        line["layer_skip"] = skip_info
     if sweep:
         line["gemv_sweep"] = sweep
         line["gemv_sweep_min_frac"] = min(s["frac"] for s in sweep)
     print(json.dumps(line), flush=True)
+
+
+def calibrate_skip(nt, m, reset, tok0, spec, max_skip: int, threshold: float, steps: int = 4) -> dict:
+    """Per-layer cosine between the residual entering and leaving each layer,
+    averaged over a few greedy steps from the prompt token, then the skip plan
+    (layers at or above the threshold, at most max_skip) applied to the model."""
+    import numpy as np
+
+    from quantized_decode_dequant_gb300 import workloads as W
+    reset()
+    cos = np.zeros(spec["n_layers"])
+    t = tok0
+    for _ in range(steps):
+        t, c = nt.nt_layer_similarity(m, t)
+        cos += c
+    cos /= steps
+    mask = nt.nt_plan_layer_skip(cos, threshold, max_skip)
+    nt.nt_set_layer_skip(m, mask)
+    layer_bytes = W.weight_bytes(dict(spec, n_layers=1)) - W.weight_bytes(dict(spec, n_layers=0))
+    skipped = [int(i) for i in np.flatnonzero(mask)]
+    return {"threshold": threshold, "max_skip": max_skip, "calibration_steps": steps, "n_skipped": len(skipped),
+            "skipped_layers": skipped, "layers_at_or_above_threshold": int((cos >= threshold).sum()),
+            "cos_min_max": [round(float(cos.min()), 5), round(float(cos.max()), 5)],
+            "weight_bytes_saved_per_token": layer_bytes * len(skipped),
+            "note": "mechanism and bytes only: output quality cannot be judged on random weights"}
 
 
 def _prompt_token(vocab: int) -> int:

@@ -46,7 +46,7 @@ typedef enum {
 } nt_status;
 
 /* Weight formats ("Quantisierungsformate Q4_0, Q8_0, Q4_K_M, Q5_K, Q6_K, F16
- * und F32", hada "Überblick").  Q5_K, F16 and F32 weights are not implemented
+ * und F32", hada "Überblick").  F16 and F32 weights are not implemented
  * (NT_E_UNSUPPORTED); F16 is used only for the KV cache.
  * Canonical block bytes (little-endian), the export format:
  *   Q8_0  32 weights, 34 B:  f16 d | int8 q[32]                  w = d*q
@@ -58,9 +58,12 @@ typedef enum {
  *   Q6_K  256 weights, 210 B: u8 ql[128] (low 4 bits, as Q4_0) | u8 qh[64]
  *         (high 2 bits of element k in byte k/4 at bits 2*(k%4)) | int8 sc[16] | f16 d
  *                                                               w = d*sc_j*(q-32)
+ *   Q5_K  256 weights, 176 B: f16 d | f16 dmin | 12 B of 6-bit fields as Q4_K |
+ *         u8 qh[32] (fifth bit of element k in byte k/8 at bit k%8) | u8 qs[128]
+ *         (low 4 bits, as Q4_0), q in 0..31              w = d*sc_j*q - dmin*m_j
  * On the device each tensor is held as separate 16-byte-aligned streams
  * (codes, scales) with the same byte count. */
-typedef enum { NT_F32 = 0, NT_F16 = 1, NT_Q8_0 = 2, NT_Q4_0 = 3, NT_Q4_K = 4, NT_Q6_K = 5 } nt_qtype;
+typedef enum { NT_F32 = 0, NT_F16 = 1, NT_Q8_0 = 2, NT_Q4_0 = 3, NT_Q4_K = 4, NT_Q6_K = 5, NT_Q5_K = 6 } nt_qtype;
 
 /* Tensor roles inside a layer, and the two model-level matrices. */
 enum {
@@ -196,6 +199,34 @@ nt_status nt_plan_residency(const nt_config* cfg, int64_t budget_bytes, int32_t*
  * model already holds, minus margin_bytes.  n_resident_out (nullable) receives
  * the placement. */
 nt_status nt_auto_residency(nt_model* m, int64_t margin_bytes, int32_t* n_resident_out);
+
+/* ---- layer skip (hada "Hauptfunktionen": layer skip by cosine similarity;
+ * hotdry "性能数据与瓶颈分析": the similarity between layer outputs is
+ * computed beforehand and layers at or above the threshold, 0.98 there, are
+ * skipped at inference) ----
+ *
+ * nt_layer_similarity runs one decode step exactly like nt_decode_step (same
+ * result, position advanced by one, every layer evaluated whatever the skip
+ * mask) and also writes cos_out[l], l < n_layers: the cosine similarity
+ * between the residual stream entering layer l and leaving it, accumulated in
+ * fp64 from the fp32 activations.  cos_out is host memory owned by the caller;
+ * next_token as in nt_decode_step.  Works for resident and streamed models. */
+nt_status nt_layer_similarity(nt_model* m, int32_t token, int32_t* next_token, double* cos_out);
+
+/* Sets the layers later steps skip: mask[l] != 0 (n_layers bytes of host
+ * memory, copied) skips layer l -- its weights are neither read nor copied from
+ * the host tier, its K/V row is not written, and the residual stream passes
+ * through unchanged.  mask = NULL evaluates every layer again.  Applies to
+ * nt_decode_step, nt_decode_run and nt_profile_steps (the persistent step
+ * kernel is not used while any layer is skipped). */
+nt_status nt_set_layer_skip(nt_model* m, const uint8_t* mask);
+
+/* Host arithmetic: mask_out[l] = 1 for every layer with cos[l] >= threshold;
+ * when max_skip > 0 and more qualify, only the max_skip most similar ones
+ * (ties: lower layer first).  n_skipped (nullable) receives the count.
+ * NT_E_INVAL on NULL arrays or n_layers < 0. */
+nt_status nt_plan_layer_skip(const double* cos, int32_t n_layers, double threshold, int32_t max_skip,
+                             uint8_t* mask_out, int32_t* n_skipped);
 
 nt_status nt_get_stats(const nt_model* m, nt_stats* out);
 

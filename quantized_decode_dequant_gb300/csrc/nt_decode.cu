@@ -19,6 +19,7 @@
 // host memory; each step copies layer l into staging buffer (l - n_resident) % 2
 // on a copy stream while layer l-1 computes; the copy into a buffer waits for
 // the compute that last read it.
+#include <algorithm>
 #include <chrono>
 #include <cmath>
 #include <cstdlib>
@@ -91,6 +92,42 @@ __global__ void k_argmax(const float4* __restrict__ top2, int n, int32_t* d_pos,
 }
 
 // f16 N(0,1) prefill; counter index of (t, kv head g, d) is (t*n_kv + g)*hd + d.
+// cos[l] = <a, b> / (|a| |b|) for a = hs[l], b = hs[l + 1] (0 when either is zero):
+// one CTA per layer, fp64 partial sums in a fixed order.
+__global__ void __launch_bounds__(256) k_layer_cos(const float* __restrict__ hs, int n, double* __restrict__ cos) {
+  const float* a = hs + size_t(blockIdx.x) * n;
+  const float* b = a + n;
+  double ab = 0, aa = 0, bb = 0;
+  for (int i = threadIdx.x; i < n; i += 256) {
+    const double u = a[i], v = b[i];
+    ab = fma(u, v, ab);
+    aa = fma(u, u, aa);
+    bb = fma(v, v, bb);
+  }
+  __shared__ double red[3][8];
+  for (int o = 16; o; o >>= 1) {
+    ab += __shfl_xor_sync(0xffffffffu, ab, o);
+    aa += __shfl_xor_sync(0xffffffffu, aa, o);
+    bb += __shfl_xor_sync(0xffffffffu, bb, o);
+  }
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    red[0][w] = ab;
+    red[1][w] = aa;
+    red[2][w] = bb;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double s0 = 0, s1 = 0, s2 = 0;
+    for (int i = 0; i < 8; i++) {
+      s0 += red[0][i];
+      s1 += red[1][i];
+      s2 += red[2][i];
+    }
+    cos[blockIdx.x] = (s1 == 0 || s2 == 0) ? 0.0 : s0 / (sqrt(s1) * sqrt(s2));
+  }
+}
+
 __global__ void k_kv_prefill(__half* kv, int n_layers, int n_kv, int max_ctx, int hd, int n_ctx, uint64_t seed) {
   const int64_t per = int64_t(n_ctx) * n_kv * hd;
   const int64_t total = int64_t(n_layers) * 2 * per;
@@ -171,6 +208,10 @@ struct nt_model {
   std::vector<cudaEvent_t> ev_cs, ev_ce, ev_ls, ev_le;
   cudaEvent_t ev_step0 = nullptr, ev_step1 = nullptr;
   nt_stats stats{};
+  std::vector<uint8_t> skip;         // per layer: 1 = skipped (empty: none)
+  std::vector<uint8_t> ran;          // per layer: evaluated in the last streamed step
+  float* hs = nullptr;               // similarity step: residual before each layer and after the last
+  double* d_cos = nullptr;           // similarity step: per-layer cosine
   size_t dev_bytes = 0, dev_limit = 0;
   std::vector<std::pair<void*, size_t>> dev_allocs;   // live device allocations and their sizes
 };
@@ -215,6 +256,8 @@ static QMat view_at(const Layer& L, int role, uint8_t* base) {
 static int64_t kv_layer_elems(const nt_config& c) { return int64_t(c.n_kv_heads) * c.max_ctx * c.head_dim; }
 static __half* k_cache(nt_model* m, int l) { return m->kv + (int64_t(l) * 2 + 0) * kv_layer_elems(m->c); }
 static __half* v_cache(nt_model* m, int l) { return m->kv + (int64_t(l) * 2 + 1) * kv_layer_elems(m->c); }
+
+static bool skipped(const nt_model* m, int l) { return !m->skip.empty() && m->skip[size_t(l)]; }
 
 static double qbytes(const QMat& q) { return double(stream_sizes(q.type, q.rows, q.cols).total()); }
 
@@ -434,18 +477,30 @@ static cudaError_t enqueue_embed(nt_model* m, Launcher& L) {
 // Whole step for a model whose layers are all resident.
 static cudaError_t enqueue_resident(nt_model* m, Launcher& L, bool pdl) {
   cudaError_t e = enqueue_embed(m, L);
-  for (int l = 0; l < m->c.n_layers && !e; l++) e = enqueue_layer(m, l, m->layers[size_t(l)].dev, L, pdl);
+  for (int l = 0; l < m->c.n_layers && !e; l++)
+    if (!skipped(m, l)) e = enqueue_layer(m, l, m->layers[size_t(l)].dev, L, pdl);
   if (!e) e = enqueue_head(m, L, pdl);
   return e;
 }
 
-// Whole step with layers [n_resident, n_layers) copied through the staging buffers.
-static cudaError_t enqueue_streamed(nt_model* m, Launcher& L) {
+// Whole step with layers [n_resident, n_layers) copied through the staging
+// buffers (with none streamed it is the resident step without PDL).  Skipped
+// layers are neither copied nor run; the staging buffers alternate over the
+// streamed layers that do run.  With hs set (similarity step) every layer runs
+// and the residual is copied to hs[l] before layer l and to hs[n_layers] after
+// the last.
+static cudaError_t enqueue_streamed(nt_model* m, Launcher& L, float* hs) {
   const int nl = m->c.n_layers, nr = m->n_resident;
+  const size_t xbytes = size_t(m->c.hidden) * 4;
   cudaStream_t s = L.s, cs = m->copy_stream;
   cudaError_t e;
-  auto issue_copy = [&](int l) -> cudaError_t {
-    const int b = (l - nr) & 1;
+  m->ran.assign(size_t(nl), 0);
+  for (int l = 0; l < nl; l++) m->ran[size_t(l)] = (hs || !skipped(m, l)) ? 1 : 0;
+  std::vector<int> sl;   // streamed layers that run, in order; sl[k] uses buffer k % 2
+  for (int l = nr; l < nl; l++)
+    if (m->ran[size_t(l)]) sl.push_back(l);
+  auto issue_copy = [&](size_t k) -> cudaError_t {
+    const int l = sl[k], b = int(k & 1);
     cudaError_t er = cudaStreamWaitEvent(cs, m->ev_compute_done[b], 0);
     if (!er) er = cudaEventRecord(m->ev_cs[size_t(l)], cs);
     if (!er) er = cudaMemcpyAsync(m->staging[b], m->layers[size_t(l)].host, m->layers[size_t(l)].bytes,
@@ -454,20 +509,32 @@ static cudaError_t enqueue_streamed(nt_model* m, Launcher& L) {
     if (!er) er = cudaEventRecord(m->ev_copy_done[b], cs);
     return er;
   };
-  for (int l = nr; l < nl && l < nr + 2; l++)
-    if ((e = issue_copy(l))) return e;
+  for (size_t k = 0; k < sl.size() && k < 2; k++)
+    if ((e = issue_copy(k))) return e;
   if ((e = enqueue_embed(m, L))) return e;
+  size_t k = 0;
   for (int l = 0; l < nl; l++) {
+    if (!m->ran[size_t(l)]) continue;
     const bool streamed = l >= nr;
-    const int b = (l - nr) & 1;
+    const int b = int(k & 1);
     uint8_t* base = streamed ? m->staging[b] : m->layers[size_t(l)].dev;
+    if (hs && (e = cudaMemcpyAsync(hs + size_t(l) * m->c.hidden, m->x, xbytes, cudaMemcpyDeviceToDevice, s)))
+      return e;
     if (streamed && (e = cudaStreamWaitEvent(s, m->ev_copy_done[b], 0))) return e;
     if ((e = cudaEventRecord(m->ev_ls[size_t(l)], s))) return e;
     if ((e = enqueue_layer(m, l, base, L, false))) return e;
     if ((e = cudaEventRecord(m->ev_le[size_t(l)], s))) return e;
     if (streamed) {
       if ((e = cudaEventRecord(m->ev_compute_done[b], s))) return e;
-      if (l + 2 < nl && (e = issue_copy(l + 2))) return e;
+      if (k + 2 < sl.size() && (e = issue_copy(k + 2))) return e;
+      k++;
+    }
+  }
+  if (hs) {
+    if ((e = cudaMemcpyAsync(hs + size_t(nl) * m->c.hidden, m->x, xbytes, cudaMemcpyDeviceToDevice, s))) return e;
+    if (nl > 0) {
+      k_layer_cos<<<unsigned(nl), 256, 0, s>>>(hs, m->c.hidden, m->d_cos);
+      if ((e = cudaGetLastError())) return e;
     }
   }
   return enqueue_head(m, L, false);
@@ -545,6 +612,8 @@ static nt_status prepare_step(nt_model* m) {
   m->step_state = -1;
   const nt_config& c = m->c;
   if (!step_kernel_enabled() || m->n_resident < c.n_layers) return NT_OK;
+  for (int l = 0; l < c.n_layers; l++)
+    if (skipped(m, l)) return NT_OK;
   const int64_t qd = int64_t(c.n_heads) * c.head_dim;
   if (c.hidden % 1024 || qd % 1024 || c.ffn_dim % 1024 || c.n_kv_heads > kStepMaxTiles) return NT_OK;
   StepPlan p;
@@ -563,7 +632,7 @@ static nt_status prepare_step(nt_model* m) {
   int64_t max_cols = c.hidden > qd ? c.hidden : qd;
   if (c.ffn_dim > max_cols) max_cols = c.ffn_dim;
   size_t ring_off = 0;
-  const size_t smem = step_smem(p, max_cols, attn_chunk_len(c.max_ctx), &ring_off);
+  const size_t smem = step_smem(p, max_cols, c.hidden, attn_chunk_len(c.max_ctx), &ring_off);
   bool fits = false;
   const cudaError_t fe = step_fits(p, smem, &fits);
   if (fe == cudaErrorNotSupported) return NT_OK;   // no instantiation for this plan
@@ -840,29 +909,41 @@ nt_status nt_kv_prefill(nt_model* m, int32_t n_ctx, uint64_t seed) {
   return set_pos(m, n_ctx);
 }
 
-nt_status nt_decode_step(nt_model* m, int32_t token, int32_t* next_token, float* logits_host, float* top2_margin) {
-  if (!m || !next_token) return fail(NT_E_INVAL, "nt_decode_step: NULL argument");
-  if (token < 0 || token >= m->c.vocab) return fail(NT_E_INVAL, "nt_decode_step: token outside [0, vocab)");
-  if (m->pos >= m->c.max_ctx) return fail(NT_E_INVAL, "nt_decode_step: position reached max_ctx");
-  const bool streamed = m->n_resident < m->c.n_layers;
-  nt_status st0 = prepare_step(m);
-  if (st0) return st0;
-  const bool step_kernel = m->step_state == 1;
-  if (!streamed && !step_kernel) {
-    nt_status st = ensure_graph(m);
-    if (st) return st;
+// One synchronous decode step.  cos_out (similarity step): every layer runs on
+// the launch-by-launch path and the per-layer cosines are copied out.
+static nt_status run_step(nt_model* m, int32_t token, int32_t* next_token, float* logits_host, float* top2_margin,
+                          double* cos_out, const char* who) {
+  if (!m || !next_token) return fail(NT_E_INVAL, std::string(who) + ": NULL argument");
+  if (token < 0 || token >= m->c.vocab) return fail(NT_E_INVAL, std::string(who) + ": token outside [0, vocab)");
+  if (m->pos >= m->c.max_ctx) return fail(NT_E_INVAL, std::string(who) + ": position reached max_ctx");
+  const nt_config& c = m->c;
+  const bool streamed = m->n_resident < c.n_layers;
+  const bool calib = cos_out != nullptr;
+  if (calib && !m->hs) {
+    NT_CUDA(dev_alloc(m, reinterpret_cast<void**>(&m->hs), size_t(c.n_layers + 1) * c.hidden * 4));
+    NT_CUDA(dev_alloc(m, reinterpret_cast<void**>(&m->d_cos), size_t(c.n_layers > 0 ? c.n_layers : 1) * 8));
+  }
+  bool step_kernel = false;
+  if (!calib) {
+    nt_status st0 = prepare_step(m);
+    if (st0) return st0;
+    step_kernel = m->step_state == 1;
+    if (!streamed && !step_kernel) {
+      nt_status st = ensure_graph(m);
+      if (st) return st;
+    }
   }
   m->h_io[1] = token;
   NT_CUDA(cudaMemcpyAsync(d_token(m), m->h_io + 1, 4, cudaMemcpyHostToDevice, m->stream));
   NT_CUDA(cudaEventRecord(m->ev_step0, m->stream));
-  if (streamed) {
+  if (streamed || calib) {
     Launcher L;
     L.s = m->stream;
-    cudaError_t e = enqueue_streamed(m, L);
-    if (e) return cuda_fail(e, "nt_decode_step: streamed step");
+    cudaError_t e = enqueue_streamed(m, L, calib ? m->hs : nullptr);
+    if (e) return cuda_fail(e, (std::string(who) + ": launch-by-launch step").c_str());
   } else if (step_kernel) {
     cudaError_t e = launch_step_model(m, m->stream, nullptr);
-    if (e) return cuda_fail(e, "nt_decode_step: step kernel");
+    if (e) return cuda_fail(e, (std::string(who) + ": step kernel").c_str());
   } else {
     NT_CUDA(cudaGraphLaunch(m->exec, m->stream));
   }
@@ -870,22 +951,24 @@ nt_status nt_decode_step(nt_model* m, int32_t token, int32_t* next_token, float*
   // next id, margin and the error word
   NT_CUDA(cudaMemcpyAsync(m->h_io + 2, d_next(m), 12, cudaMemcpyDeviceToHost, m->stream));
   if (logits_host)
-    NT_CUDA(cudaMemcpyAsync(logits_host, m->logits, size_t(m->c.vocab) * 4, cudaMemcpyDeviceToHost, m->stream));
-  cudaEvent_t done = m->ev_step1;
-  nt_status st = wait_event(done, "nt_decode_step");
+    NT_CUDA(cudaMemcpyAsync(logits_host, m->logits, size_t(c.vocab) * 4, cudaMemcpyDeviceToHost, m->stream));
+  if (calib && c.n_layers > 0)
+    NT_CUDA(cudaMemcpyAsync(cos_out, m->d_cos, size_t(c.n_layers) * 8, cudaMemcpyDeviceToHost, m->stream));
+  nt_status st = wait_event(m->ev_step1, who);
   if (st) return st;
   NT_CUDA(cudaStreamSynchronize(m->stream));
   if (m->h_io[4]) {
     reset_step_error(m);
-    return fail(NT_E_TIMEOUT, "nt_decode_step: a grid barrier of the step kernel timed out; step abandoned");
+    return fail(NT_E_TIMEOUT, std::string(who) + ": a grid barrier of the step kernel timed out; step abandoned");
   }
   float ms = 0.f;
   NT_CUDA(cudaEventElapsedTime(&ms, m->ev_step0, m->ev_step1));
   m->stats.last_step_ms = ms;
   m->stats.steps++;
-  if (streamed) {
+  if (streamed || calib) {
     double h2d = 0, cms = 0, bytes = 0;
-    for (int l = 0; l < m->c.n_layers; l++) {
+    for (int l = 0; l < c.n_layers; l++) {
+      if (!m->ran[size_t(l)]) continue;
       float t = 0.f;
       NT_CUDA(cudaEventElapsedTime(&t, m->ev_ls[size_t(l)], m->ev_le[size_t(l)]));
       cms += t;
@@ -908,6 +991,44 @@ nt_status nt_decode_step(nt_model* m, int32_t token, int32_t* next_token, float*
   m->pos++;
   *next_token = m->h_io[2];
   if (top2_margin) memcpy(top2_margin, m->h_io + 3, 4);
+  return NT_OK;
+}
+
+nt_status nt_decode_step(nt_model* m, int32_t token, int32_t* next_token, float* logits_host, float* top2_margin) {
+  return run_step(m, token, next_token, logits_host, top2_margin, nullptr, "nt_decode_step");
+}
+
+nt_status nt_layer_similarity(nt_model* m, int32_t token, int32_t* next_token, double* cos_out) {
+  if (!cos_out) return fail(NT_E_INVAL, "nt_layer_similarity: NULL argument");
+  return run_step(m, token, next_token, nullptr, nullptr, cos_out, "nt_layer_similarity");
+}
+
+nt_status nt_set_layer_skip(nt_model* m, const uint8_t* mask) {
+  if (!m) return fail(NT_E_INVAL, "nt_set_layer_skip: model is NULL");
+  NT_CUDA(cudaStreamSynchronize(m->stream));
+  drop_graph(m);
+  m->step_state = 0;
+  m->skip.clear();
+  if (mask) {
+    m->skip.assign(size_t(m->c.n_layers), 0);
+    for (int l = 0; l < m->c.n_layers; l++) m->skip[size_t(l)] = mask[l] ? 1 : 0;
+  }
+  return NT_OK;
+}
+
+nt_status nt_plan_layer_skip(const double* cos, int32_t n_layers, double threshold, int32_t max_skip,
+                             uint8_t* mask_out, int32_t* n_skipped) {
+  if (n_layers < 0 || (n_layers > 0 && (!cos || !mask_out)))
+    return fail(NT_E_INVAL, "nt_plan_layer_skip: NULL array or negative n_layers");
+  std::vector<int> cand;
+  for (int l = 0; l < n_layers; l++)
+    if (cos[l] >= threshold) cand.push_back(l);
+  // most similar first, lower layer first among equals
+  std::stable_sort(cand.begin(), cand.end(), [&](int a, int b) { return cos[a] > cos[b]; });
+  if (max_skip > 0 && int(cand.size()) > max_skip) cand.resize(size_t(max_skip));
+  for (int l = 0; l < n_layers; l++) mask_out[l] = 0;
+  for (int l : cand) mask_out[l] = 1;
+  if (n_skipped) *n_skipped = int32_t(cand.size());
   return NT_OK;
 }
 

@@ -59,9 +59,9 @@ cudaError_t launch_gemv(const GemvArgs& a_in, int epi, cudaStream_t s, bool pdl,
   if (cols % align == 0 && !force_register_path) {
     int parts = 1;
     if (epi == EPI_STORE || epi == EPI_ADD)
-      while (pipe_x_bytes(cols / parts) > 140 * 1024 && (cols / parts) % (2 * align) == 0) parts *= 2;
+      while (pipe_x_bytes(cols / parts, epi) > 140 * 1024 && (cols / parts) % (2 * align) == 0) parts *= 2;
     const int64_t w = cols / parts;
-    const size_t xb = pipe_x_bytes(w);
+    const size_t xb = pipe_x_bytes(w, epi);
     const size_t target = size_t(kPipeSmPerSm) / size_t(pipe_ctas_per_sm()) - 2048;
     // four rows per warp share each x read, but only if the ring still holds at least
     // four stages (three tiles in flight)
@@ -83,7 +83,7 @@ cudaError_t launch_gemv(const GemvArgs& a_in, int epi, cudaStream_t s, bool pdl,
     S16 = S16 >= 8 ? 8 : (S16 >= 6 ? 6 : (S16 >= 4 ? 4 : S16));
     int S16r4 = int(ring16 / (size_t(16) * 4 * pipe_row_bytes(fmt)));
     S16r4 = S16r4 >= 4 ? 4 : S16r4;
-    const bool four_bit_tall = R == 4 && (fmt == NT_Q4_0 || fmt == NT_Q4_K);
+    const bool four_bit_tall = R == 4 && (fmt == NT_Q4_0 || fmt == NT_Q4_K || fmt == NT_Q5_K);
     int NW = 8;
     if (pipe_layout() == 16 && S16 >= 3) {
       NW = 16;
@@ -111,6 +111,7 @@ cudaError_t launch_gemv(const GemvArgs& a_in, int epi, cudaStream_t s, bool pdl,
           case NT_Q4_0: e = launch_gemv_pipe_q4_0(a, e_p, R, S, NW, s, pdl, grid_used); break;
           case NT_Q4_K: e = launch_gemv_pipe_q4_k(a, e_p, R, S, NW, s, pdl, grid_used); break;
           case NT_Q6_K: e = launch_gemv_pipe_q6_k(a, e_p, R, S, NW, s, pdl, grid_used); break;
+          case NT_Q5_K: e = launch_gemv_pipe_q5_k(a, e_p, R, S, NW, s, pdl, grid_used); break;
           default: e = cudaErrorInvalidValue;
         }
         if (e != cudaSuccess) return e;
@@ -125,6 +126,7 @@ cudaError_t launch_gemv(const GemvArgs& a_in, int epi, cudaStream_t s, bool pdl,
     case NT_Q4_0: return launch_gemv_q4_0(a, epi, R, s, pdl, grid_used);
     case NT_Q4_K: return launch_gemv_q4_k(a, epi, R, s, pdl, grid_used);
     case NT_Q6_K: return launch_gemv_q6_k(a, epi, R, s, pdl, grid_used);
+    case NT_Q5_K: return launch_gemv_q5_k(a, epi, R, s, pdl, grid_used);
   }
   return cudaErrorInvalidValue;
 }
@@ -134,7 +136,7 @@ cudaError_t launch_gemv_pair(const GemvArgs& a1_in, const GemvArgs& a2_in, int e
   static const bool force_register_path = getenv("NT_GEMV_REGISTER_PATH") != nullptr;
   const int64_t cols = a1_in.seg[0].cols;
   bool pair = !force_register_path && epi == EPI_QKV && a1_in.seg[0].type == NT_Q4_K && a2_in.seg[0].type == NT_Q6_K &&
-              a2_in.seg[0].cols == cols && cols % 1024 == 0 && pipe_x_bytes(cols) <= 56 * 1024;
+              a2_in.seg[0].cols == cols && cols % 1024 == 0 && pipe_x_bytes(cols, EPI_QKV) <= 56 * 1024;
   for (int i = 1; i < a1_in.nseg; i++) pair = pair && a1_in.seg[i].type == NT_Q4_K && a1_in.seg[i].cols == cols;
   pair = pair && a2_in.nseg == 1 && !a1_in.interleave && !a2_in.interleave;
   if (pair) {

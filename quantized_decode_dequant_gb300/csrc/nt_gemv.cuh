@@ -179,6 +179,55 @@ template <> struct Fmt<NT_Q4_K> {
   }
 };
 
+// Q5_K: code bytes built as for Q6_K (x staged [0,2,4,6,1,3,5,7] per 8 columns):
+// low nibble | fifth bit from the unit's word H at bit 4; Q4_K's scale and min.
+template <> struct Fmt<NT_Q5_K> {
+  static constexpr int kCols = 32;
+  static constexpr bool kXSum = true;
+  struct Pay {
+    uint4 c, meta;
+    uint32_t h;
+    int j;
+  };
+  __device__ static void load(Pay& p, const QMat& m, int64_t e) {
+    p.c = ldg16(m.q + (e >> 1));
+    p.h = __ldg(reinterpret_cast<const unsigned int*>(m.qh + (e >> 3)));
+    p.meta = __ldg(reinterpret_cast<const uint4*>(m.meta + (e >> 8) * 16));
+    p.j = int(e >> 5) & 7;
+  }
+  __device__ static int xpos(int c) { return (c & ~7) | ((c & 1) ? 4 + ((c & 7) >> 1) : ((c & 7) >> 1)); }
+  __device__ static float xscale(int) { return 1.0f; }
+  __device__ static float2 bytes4(uint32_t q, float4 x, float2 acc) {
+    const float2 off = make_float2(-kMagic, -kMagic);
+    const float2 a = __fadd2_rn(make_float2(bits_f(__byte_perm(q, kMagicBits, 0x7440u)),
+                                            bits_f(__byte_perm(q, kMagicBits, 0x7441u))), off);
+    const float2 b = __fadd2_rn(make_float2(bits_f(__byte_perm(q, kMagicBits, 0x7442u)),
+                                            bits_f(__byte_perm(q, kMagicBits, 0x7443u))), off);
+    acc = __ffma2_rn(a, make_float2(x.x, x.y), acc);
+    return __ffma2_rn(b, make_float2(x.z, x.w), acc);
+  }
+  __device__ static float dot(const Pay& p, const float4* xs, float xsum) {
+    const uint32_t L = 0x0F0F0F0Fu, M = 0x10101010u, H = p.h;
+    float2 acc = make_float2(0.f, 0.f);
+    acc = bytes4((p.c.x & L) | ((H << 4) & M), xs[0], acc);
+    acc = bytes4(((p.c.x >> 4) & L) | ((H << 3) & M), xs[1], acc);
+    acc = bytes4((p.c.y & L) | ((H << 2) & M), xs[2], acc);
+    acc = bytes4(((p.c.y >> 4) & L) | ((H << 1) & M), xs[3], acc);
+    acc = bytes4((p.c.z & L) | (H & M), xs[4], acc);
+    acc = bytes4(((p.c.z >> 4) & L) | ((H >> 1) & M), xs[5], acc);
+    acc = bytes4((p.c.w & L) | ((H >> 2) & M), xs[6], acc);
+    acc = bytes4(((p.c.w >> 4) & L) | ((H >> 3) & M), xs[7], acc);
+    const uint64_t lo = uint64_t(p.meta.y) | (uint64_t(p.meta.z) << 32);
+    const uint32_t sc = uint32_t(lo >> (6 * p.j)) & 63u;
+    const int mb = 48 + 6 * p.j;
+    const uint32_t mm = mb >= 64 ? (p.meta.w >> (mb - 64)) & 63u
+                                 : uint32_t((lo >> mb) | (uint64_t(p.meta.w) << (64 - mb))) & 63u;
+    const float a = h2f_bits(p.meta.x & 0xFFFFu) * float(sc);
+    const float b = h2f_bits(p.meta.x >> 16) * float(mm);
+    return a * (acc.x + acc.y) - b * xsum;
+  }
+};
+
 template <> struct Fmt<NT_Q6_K> {
   static constexpr int kCols = 32;
   static constexpr bool kXSum = false;
@@ -580,6 +629,7 @@ cudaError_t launch_gemv_fmt(const GemvArgs& a, int epi, int R, cudaStream_t s, b
 NT_DECLARE_GEMV(launch_gemv_q8_0)
 NT_DECLARE_GEMV(launch_gemv_q4_0)
 NT_DECLARE_GEMV(launch_gemv_q4_k)
+NT_DECLARE_GEMV(launch_gemv_q5_k)
 NT_DECLARE_GEMV(launch_gemv_q6_k)
 #undef NT_DECLARE_GEMV
 

@@ -36,6 +36,8 @@
 // tile is whole and every scale piece an aligned 16-byte (4-byte for Q6_K d) copy.
 #pragma once
 
+#include <type_traits>
+
 #include "nt_gemv.cuh"
 
 namespace nt {
@@ -43,7 +45,15 @@ namespace nt {
 constexpr int kPipeWarps = 8;                 // 256 threads per CTA
 constexpr int kPipeMaxSmem = 221 * 1024;      // dynamic shared memory a CTA may ask for
 constexpr int kPipeSmPerSm = 228 * 1024;      // shared memory of an SM (each resident CTA also reserves 1 KB)
-constexpr int kXUnit = 80;                    // staged x per 32 columns: h[32] | l[32] | sx, T0, T1, sum of squares
+// Staged x per 32 columns, in int8 slices of fixed point t = round(x/sx):
+// two slices (t = 256 h + l, |t| <= 32512): h[32] | l[32] | sx, T0, T1, sum of squares;
+// three slices (t = 4096 h + 16 m + l, |t| <= 520192, l in 0..15): h[32] | m[32] | l[32] | the same.
+// The Q/K/V GEMV takes three: its error reaches the logits through the softmax
+// over the whole context and dominates theirs with two; every other GEMV takes two.
+constexpr int kXUnit = 80;
+template <int XS>
+__host__ __device__ constexpr int x_unit() { return XS == 3 ? 112 : 80; }
+__host__ __device__ constexpr int x_slices(int epi) { return epi == EPI_QKV ? 3 : 2; }
 // Before the producer of x is done only the first kPipeEarly tiles of a warp's
 // ring are copied: the x loads of the staging that follows would otherwise queue
 // behind a whole ring of weight copies; the rest is issued once x is staged.
@@ -65,36 +75,50 @@ __device__ __forceinline__ void cp_wait() {
 }
 // One staged x block in registers.
 struct XBlock {
-  int h[8], l[8];   // int8 halves, four per word, in the format's element order
+  int h[8], m[8], l[8];   // int8 slices, four per word, in the format's element order (m: three slices only)
   float sx;         // block scale
   int t0, t1;       // sums of t over elements 0..15 and 16..31
 };
 
+template <int XS>
 __device__ __forceinline__ void load_xblock(const uint8_t* p, XBlock& x) {
-  const uint4 h0 = *reinterpret_cast<const uint4*>(p), h1 = *reinterpret_cast<const uint4*>(p + 16);
-  const uint4 l0 = *reinterpret_cast<const uint4*>(p + 32), l1 = *reinterpret_cast<const uint4*>(p + 48);
-  const uint4 m = *reinterpret_cast<const uint4*>(p + 64);
-  x.h[0] = h0.x; x.h[1] = h0.y; x.h[2] = h0.z; x.h[3] = h0.w;
-  x.h[4] = h1.x; x.h[5] = h1.y; x.h[6] = h1.z; x.h[7] = h1.w;
-  x.l[0] = l0.x; x.l[1] = l0.y; x.l[2] = l0.z; x.l[3] = l0.w;
-  x.l[4] = l1.x; x.l[5] = l1.y; x.l[6] = l1.z; x.l[7] = l1.w;
+  auto words = [](const uint8_t* q, int (&w)[8]) {
+    const uint4 a = *reinterpret_cast<const uint4*>(q), b = *reinterpret_cast<const uint4*>(q + 16);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  };
+  words(p, x.h);
+  if (XS == 3) words(p + 32, x.m);
+  words(p + 32 * (XS - 1), x.l);
+  const uint4 m = *reinterpret_cast<const uint4*>(p + 32 * XS);
   x.sx = __uint_as_float(m.x);
   x.t0 = int(m.y);
   x.t1 = int(m.z);
 }
 
-// sum over words [W0, W1) of (codes . x) as 256 * (codes . h) + (codes . l)
-template <int W0, int W1>
-__device__ __forceinline__ int idot(const int (&c)[8], const XBlock& x) {
-  int ah0 = 0, ah1 = 0, al0 = 0, al1 = 0;
+// Exact integer dot of codes and t: int with two slices, 64-bit with three
+// (4096 * (codes . h) can pass 2^31 for 8-bit codes).
+template <int XS>
+using xacc_t = typename std::conditional<XS == 3, long long, int>::type;
+__device__ __forceinline__ float xacc_f(int v) { return __int2float_rn(v); }
+__device__ __forceinline__ float xacc_f(long long v) { return __ll2float_rn(v); }
+
+// sum over words [W0, W1) of (codes . t): 256 (codes . h) + (codes . l), or
+// 4096 (codes . h) + 16 (codes . m) + (codes . l)
+template <int W0, int W1, int XS>
+__device__ __forceinline__ xacc_t<XS> idot(const int (&c)[8], const XBlock& x) {
+  int ah0 = 0, ah1 = 0, am0 = 0, am1 = 0, al0 = 0, al1 = 0;
 #pragma unroll
   for (int k = W0; k < W1; k += 2) {
     ah0 = __dp4a(c[k], x.h[k], ah0);
+    if (XS == 3) am0 = __dp4a(c[k], x.m[k], am0);
     al0 = __dp4a(c[k], x.l[k], al0);
     ah1 = __dp4a(c[k + 1], x.h[k + 1], ah1);
+    if (XS == 3) am1 = __dp4a(c[k + 1], x.m[k + 1], am1);
     al1 = __dp4a(c[k + 1], x.l[k + 1], al1);
   }
-  return (ah0 + ah1) * 256 + (al0 + al1);
+  if constexpr (XS == 3) return (long long)(ah0 + ah1) * 4096 + ((am0 + am1) * 16 + (al0 + al1));
+  else return (ah0 + ah1) * 256 + (al0 + al1);
 }
 
 // even and odd nibbles of each code word as bytes: words 2k (elements 8k+0,2,4,6) and 2k+1 (8k+1,3,5,7)
@@ -130,10 +154,11 @@ template <> struct Pipe<NT_Q8_0> {
     f.c1 = *reinterpret_cast<const uint4*>(blk + lane * 32 + 16);
     f.d = *reinterpret_cast<const uint16_t*>(blk + 1024 + lane * 2);
   }
+  template <int XS>
   __device__ static float compute(const Frag& f, int lane, const XBlock& x) {
     const int c[8] = {int(f.c0.x), int(f.c0.y), int(f.c0.z), int(f.c0.w),
                       int(f.c1.x), int(f.c1.y), int(f.c1.z), int(f.c1.w)};
-    return __fmul_rn(__fmul_rn(h2f_bits(f.d), x.sx), __int2float_rn(idot<0, 8>(c, x)));
+    return __fmul_rn(__fmul_rn(h2f_bits(f.d), x.sx), xacc_f(idot<0, 8, XS>(c, x)));
   }
 };
 
@@ -159,12 +184,29 @@ template <> struct Pipe<NT_Q4_0> {
     f.w = *reinterpret_cast<const uint4*>(blk + lane * 16);
     f.d = *reinterpret_cast<const uint16_t*>(blk + 512 + lane * 2);
   }
+  template <int XS>
   __device__ static float compute(const Frag& f, int lane, const XBlock& x) {
     int c[8];
     nibble_bytes(f.w, c);
-    return __fmul_rn(__fmul_rn(h2f_bits(f.d), x.sx), __int2float_rn(idot<0, 8>(c, x) - 8 * (x.t0 + x.t1)));
+    return __fmul_rn(__fmul_rn(h2f_bits(f.d), x.sx), xacc_f(idot<0, 8, XS>(c, x) - xacc_t<XS>(8) * (x.t0 + x.t1)));
   }
 };
+
+// One K-quant sub-block (Q4_K / Q5_K): sx * (d sc_j * sum q x - dmin m_j * sum x),
+// unit `lane` of the tile is sub-block j = lane % 8 of super-block lane / 8.
+template <int XS>
+__device__ __forceinline__ float kquant_unit(const uint4 meta, int lane, const int (&c)[8], const XBlock& x) {
+  const int j = lane & 7;
+  // 6-bit fields: sc_j at bit 6j, m_j at bit 6(8+j) of the 96-bit stream (meta.y, meta.z, meta.w)
+  const uint64_t lo = uint64_t(meta.y) | (uint64_t(meta.z) << 32);
+  const uint32_t sc = uint32_t(lo >> (6 * j)) & 63u;
+  const int mb = 48 + 6 * j;
+  const uint32_t mm = mb >= 64 ? (meta.w >> (mb - 64)) & 63u
+                               : uint32_t((lo >> mb) | (uint64_t(meta.w) << (64 - mb))) & 63u;
+  const float a = __fmul_rn(h2f_bits(meta.x & 0xFFFFu), float(sc));
+  const float b = __fmul_rn(h2f_bits(meta.x >> 16), float(mm));
+  return __fmul_rn(x.sx, __fmaf_rn(a, xacc_f(idot<0, 8, XS>(c, x)), -__fmul_rn(b, __int2float_rn(x.t0 + x.t1))));
+}
 
 template <> struct Pipe<NT_Q4_K> {
   static constexpr int CB = 16, RB = 32 * 16 + 64;
@@ -185,20 +227,58 @@ template <> struct Pipe<NT_Q4_K> {
     f.w = *reinterpret_cast<const uint4*>(blk + lane * 16);
     f.meta = *reinterpret_cast<const uint4*>(blk + 512 + (lane >> 3) * 16);
   }
+  template <int XS>
   __device__ static float compute(const Frag& f, int lane, const XBlock& x) {
     int c[8];
     nibble_bytes(f.w, c);
-    const uint4 meta = f.meta;
-    const int j = lane & 7;
-    // 6-bit fields: sc_j at bit 6j, m_j at bit 6(8+j) of the 96-bit stream (meta.y, meta.z, meta.w)
-    const uint64_t lo = uint64_t(meta.y) | (uint64_t(meta.z) << 32);
-    const uint32_t sc = uint32_t(lo >> (6 * j)) & 63u;
-    const int mb = 48 + 6 * j;
-    const uint32_t mm = mb >= 64 ? (meta.w >> (mb - 64)) & 63u
-                                 : uint32_t((lo >> mb) | (uint64_t(meta.w) << (64 - mb))) & 63u;
-    const float a = __fmul_rn(h2f_bits(meta.x & 0xFFFFu), float(sc));
-    const float b = __fmul_rn(h2f_bits(meta.x >> 16), float(mm));
-    return __fmul_rn(x.sx, __fmaf_rn(a, __int2float_rn(idot<0, 8>(c, x)), -__fmul_rn(b, __int2float_rn(x.t0 + x.t1))));
+    return kquant_unit<XS>(f.meta, lane, c, x);
+  }
+};
+
+// Q5_K: the Q4_K unit with a fifth code bit per element from the unit's word H
+// (byte i of H, bit v: code word v's byte i), OR-ed in at bit 4 of each byte.
+template <> struct Pipe<NT_Q5_K> {
+  static constexpr int CB = 16, RB = 32 * 16 + 128 + 64;
+  __device__ static int xbyte(int c) { return nibble_xbyte(c); }
+  // 8 pieces of fifth-bit words (128 bytes per row and tile), 4 of super-block meta
+  static constexpr int CODE_STRIDE = 512, NPA = 12, NPB = 0;
+  __device__ static const uint8_t* code_base(const QMat& m, int64_t e_row) { return m.q + (e_row >> 1); }
+  __device__ static void piece(const QMat& m, int64_t e_row, int i, const uint8_t*& src, int& off, int& stride,
+                               int& size) {
+    if (i < 8) {
+      src = m.qh + (e_row >> 3) + i * 16;
+      off = 512 + i * 16;
+      stride = 128;
+    } else {
+      src = m.meta + (e_row >> 8) * 16 + (i - 8) * 16;
+      off = 640 + (i - 8) * 16;
+      stride = 64;
+    }
+    size = 16;
+  }
+  struct Frag {
+    uint4 w, meta;
+    uint32_t h;
+  };
+  __device__ static void load(const uint8_t* blk, int lane, Frag& f) {
+    f.w = *reinterpret_cast<const uint4*>(blk + lane * 16);
+    f.h = *reinterpret_cast<const uint32_t*>(blk + 512 + lane * 4);
+    f.meta = *reinterpret_cast<const uint4*>(blk + 640 + (lane >> 3) * 16);
+  }
+  template <int XS>
+  __device__ static float compute(const Frag& f, int lane, const XBlock& x) {
+    int c[8];
+    nibble_bytes(f.w, c);
+    const uint32_t H = f.h, M = 0x10101010u;
+    c[0] |= int((H << 4) & M);
+    c[1] |= int((H << 3) & M);
+    c[2] |= int((H << 2) & M);
+    c[3] |= int((H << 1) & M);
+    c[4] |= int(H & M);
+    c[5] |= int((H >> 1) & M);
+    c[6] |= int((H >> 2) & M);
+    c[7] |= int((H >> 3) & M);
+    return kquant_unit<XS>(f.meta, lane, c, x);
   }
 };
 
@@ -238,6 +318,7 @@ template <> struct Pipe<NT_Q6_K> {
     f.sc2 = *reinterpret_cast<const uint16_t*>(blk + 768 + lane * 2);
     f.db = *reinterpret_cast<const uint16_t*>(blk + 832 + (lane >> 3) * 2);
   }
+  template <int XS>
   __device__ static float compute(const Frag& f, int lane, const XBlock& x) {
     const uint4 w = f.w;
     const uint2 g = f.g;
@@ -251,10 +332,10 @@ template <> struct Pipe<NT_Q6_K> {
                       int((w.y & L) | ((g.x >> 2) & M)), int(((w.y >> 4) & L) | ((g.x << 2) & M)),
                       int((w.z & L) | (g.y & M)),        int(((w.z >> 4) & L) | ((g.y << 4) & M)),
                       int((w.w & L) | ((g.y >> 2) & M)), int(((w.w >> 4) & L) | ((g.y << 2) & M))};
-    const int s0 = idot<0, 4>(c, x) - 32 * x.t0;
-    const int s1 = idot<4, 8>(c, x) - 32 * x.t1;
+    const xacc_t<XS> s0 = idot<0, 4, XS>(c, x) - xacc_t<XS>(32) * x.t0;
+    const xacc_t<XS> s1 = idot<4, 8, XS>(c, x) - xacc_t<XS>(32) * x.t1;
     const float sc0 = float(int8_t(sc2 & 0xFF)), sc1 = float(int8_t(sc2 >> 8));
-    return __fmul_rn(__fmul_rn(d, x.sx), __fmaf_rn(sc0, __int2float_rn(s0), __fmul_rn(sc1, __int2float_rn(s1))));
+    return __fmul_rn(__fmul_rn(d, x.sx), __fmaf_rn(sc0, xacc_f(s0), __fmul_rn(sc1, xacc_f(s1))));
   }
 };
 
@@ -280,11 +361,11 @@ __device__ __forceinline__ WarpTiles warp_tiles(int64_t nrows, int R, int kiters
 }
 
 // Dot product of one row unit straight from shared memory.
-template <int FMT>
+template <int FMT, int XS>
 __device__ __forceinline__ float pipe_dot(const uint8_t* blk, int lane, const XBlock& x) {
   typename Pipe<FMT>::Frag f;
   Pipe<FMT>::load(blk, lane, f);
-  return Pipe<FMT>::compute(f, lane, x);
+  return Pipe<FMT>::template compute<XS>(f, lane, x);
 }
 
 // Copy cursor of one warp over its tiles.  Every lane issues the same copies
@@ -466,13 +547,8 @@ __device__ __forceinline__ void pipe_prologue(const GemvArgs& a, int64_t nrows, 
   pipe_prologue_w<FMT, R, S, SLICE>(a, nrows, w, ring);
 }
 
-// Stages eight 32-column blocks of x (columns [256 p, 256 p + 256) of the
-// window starting at x) as 16-bit fixed point, four lanes of the calling warp
-// per block, eight consecutive elements per lane.  Per block: sx = max|x|/32512,
-// t = round(x/sx) split as 256 h + l, the sums T0, T1 of t over elements 0..15
-// and 16..31, and the sum of squares (each lane's eight in element order, then
-// the four lanes as (l0 + l1) + (l2 + l3)); every kernel stages the same way.
-template <int FMT>
+// Converts one lane's eight elements of a 32-column block (see stage_pass).
+template <int FMT, int XS>
 __device__ __forceinline__ void stage_convert(float4 f0, float4 f1, int p, uint8_t* xq) {
   using P = Pipe<FMT>;
   const int lane = threadIdx.x & 31, q = lane & 3;          // q: eighth of the block
@@ -487,61 +563,76 @@ __device__ __forceinline__ void stage_convert(float4 f0, float4 f1, int p, uint8
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
   sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, 1));   // (l0 + l1), (l2 + l3)
   sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, 2));   // then their sum
-  const float inv = amax > 0.f ? 32512.0f / amax : 0.f;
-  uint32_t hw[2] = {0, 0}, lw[2] = {0, 0};
+  constexpr int kT = XS == 3 ? 520192 : 32512;   // 127 * 4096, 127 * 256
+  const float inv = amax > 0.f ? float(kT) / amax : 0.f;
+  uint32_t hw[2] = {0, 0}, mw[2] = {0, 0}, lw[2] = {0, 0};
   int ts = 0;
 #pragma unroll
   for (int j = 0; j < 8; j++) {
     int t = __float2int_rn(__fmul_rn(v[j], inv));
-    t = max(-32512, min(32512, t));
-    const int h = (t + 128) >> 8;
+    t = max(-kT, min(kT, t));
     ts += t;
+    int h, m = 0, l;
+    if (XS == 3) {
+      h = (t + 2048) >> 12;            // |h| <= 127
+      const int r = t - 4096 * h;      // -2048 .. 2047
+      m = r >> 4;                      // -128 .. 127
+      l = r & 15;                      // 0 .. 15
+    } else {
+      h = (t + 128) >> 8;
+      l = t - 256 * h;
+    }
     const int b = P::xbyte(j);   // position inside this lane's eight bytes (the 8-group order)
     hw[b >> 2] |= uint32_t(uint8_t(int8_t(h))) << (8 * (b & 3));
-    lw[b >> 2] |= uint32_t(uint8_t(int8_t(t - 256 * h))) << (8 * (b & 3));
+    if (XS == 3) mw[b >> 2] |= uint32_t(uint8_t(int8_t(m))) << (8 * (b & 3));
+    lw[b >> 2] |= uint32_t(uint8_t(int8_t(l))) << (8 * (b & 3));
   }
   const int t01 = ts + __shfl_xor_sync(0xffffffffu, ts, 1);   // lanes q = 0,1: elements 0..15; q = 2,3: 16..31
   const int t_hi = __shfl_xor_sync(0xffffffffu, t01, 2);
-  uint8_t* dst = xq + size_t(blk) * kXUnit;
+  uint8_t* dst = xq + size_t(blk) * x_unit<XS>();
   *reinterpret_cast<uint2*>(dst + q * 8) = make_uint2(hw[0], hw[1]);
-  *reinterpret_cast<uint2*>(dst + 32 + q * 8) = make_uint2(lw[0], lw[1]);
+  if (XS == 3) *reinterpret_cast<uint2*>(dst + 32 + q * 8) = make_uint2(mw[0], mw[1]);
+  *reinterpret_cast<uint2*>(dst + 32 * (XS - 1) + q * 8) = make_uint2(lw[0], lw[1]);
   if (q == 0)
-    *reinterpret_cast<uint4*>(dst + 64) =
-        make_uint4(__float_as_uint(amax / 32512.0f), uint32_t(t01), uint32_t(t_hi), __float_as_uint(sq));
+    *reinterpret_cast<uint4*>(dst + 32 * XS) =
+        make_uint4(__float_as_uint(amax / float(kT)), uint32_t(t01), uint32_t(t_hi), __float_as_uint(sq));
 }
 
 // Stages eight 32-column blocks of x (columns [256 p, 256 p + 256) of the
-// window starting at x) as 16-bit fixed point, four lanes of the calling warp
-// per block, eight consecutive elements per lane.  Per block: sx = max|x|/32512,
-// t = round(x/sx) split as 256 h + l, the sums T0, T1 of t over elements 0..15
-// and 16..31, and the sum of squares (each lane's eight in element order, then
-// the four lanes as (l0 + l1) + (l2 + l3)); every kernel stages the same way.
-template <int FMT>
+// window starting at x) as fixed point in XS int8 slices, four lanes of the
+// calling warp per block, eight consecutive elements per lane.  Per block:
+// sx = max|x|/T (T = 32512 or 520192), t = round(x/sx) split into the slices,
+// the sums T0, T1 of t over elements 0..15 and 16..31, and the sum of squares
+// (each lane's eight in element order, then the four lanes as (l0 + l1) +
+// (l2 + l3)); every kernel stages the same way.
+template <int FMT, int XS>
 __device__ __forceinline__ void stage_pass(const float* x, int p, uint8_t* xq) {
   const int lane = threadIdx.x & 31;
   const float4* src = reinterpret_cast<const float4*>(x + size_t(p) * 256 + lane * 8);
-  stage_convert<FMT>(__ldcg(src), __ldcg(src + 1), p, xq);
+  stage_convert<FMT, XS>(__ldcg(src), __ldcg(src + 1), p, xq);
 }
 
 // Stages 1024-column tile k of x (four passes) by the calling warp.
-template <int FMT>
+template <int FMT, int XS>
 __device__ __forceinline__ void stage_tile(const float* x, int k, uint8_t* xq) {
 #pragma unroll
-  for (int i = 0; i < 4; i++) stage_pass<FMT>(x, k * 4 + i, xq);
+  for (int i = 0; i < 4; i++) stage_pass<FMT, XS>(x, k * 4 + i, xq);
 }
 
 // RMSNorm factor rsqrt(mean(x^2) + eps) from the staged per-block squares,
 // summed by one warp's lanes in a fixed order (1 without norm).
+template <int XS>
 __device__ __forceinline__ float x_scale(const GemvArgs& a, const uint8_t* xq) {
   if (!a.norm) return 1.0f;
   const int lane = threadIdx.x & 31;
   const int units = int(a.ncols / 32);
+  constexpr int U = x_unit<XS>(), SQ = 32 * XS + 12;
   float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
   for (int b = lane; b < units; b += 128) {
-    s0 = __fadd_rn(s0, *reinterpret_cast<const float*>(xq + size_t(b) * kXUnit + 76));
-    if (b + 32 < units) s1 = __fadd_rn(s1, *reinterpret_cast<const float*>(xq + size_t(b + 32) * kXUnit + 76));
-    if (b + 64 < units) s2 = __fadd_rn(s2, *reinterpret_cast<const float*>(xq + size_t(b + 64) * kXUnit + 76));
-    if (b + 96 < units) s3 = __fadd_rn(s3, *reinterpret_cast<const float*>(xq + size_t(b + 96) * kXUnit + 76));
+    s0 = __fadd_rn(s0, *reinterpret_cast<const float*>(xq + size_t(b) * U + SQ));
+    if (b + 32 < units) s1 = __fadd_rn(s1, *reinterpret_cast<const float*>(xq + size_t(b + 32) * U + SQ));
+    if (b + 64 < units) s2 = __fadd_rn(s2, *reinterpret_cast<const float*>(xq + size_t(b + 64) * U + SQ));
+    if (b + 96 < units) s3 = __fadd_rn(s3, *reinterpret_cast<const float*>(xq + size_t(b + 96) * U + SQ));
   }
   float t = __fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3));
 #pragma unroll
@@ -557,7 +648,7 @@ __device__ __forceinline__ float x_scale(const GemvArgs& a, const uint8_t* xq) {
 struct NoOp {
   __device__ __forceinline__ void operator()() const {}
 };
-template <int FMT, int NW, class F = NoOp>
+template <int FMT, int NW, int XS, class F = NoOp>
 __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xq, F between = F()) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, np = int(a.ncols / 256);
   const float* x = a.x + a.col0;
@@ -579,7 +670,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xq, F betwee
     }
 #pragma unroll
     for (int i = 0; i < 4; i++)
-      if (p0 + i * NW < np) stage_convert<FMT>(f[i][0], f[i][1], p0 + i * NW, xq);
+      if (p0 + i * NW < np) stage_convert<FMT, XS>(f[i][0], f[i][1], p0 + i * NW, xq);
   }
   __syncthreads();
 }
@@ -587,7 +678,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xq, F betwee
 // Hooks of the GEMV body for a caller that staged all of x before the loop.
 struct StagedHooks {
   static constexpr bool kAllStaged = true;
-  template <int FMT>
+  template <int FMT, int XS>
   __device__ __forceinline__ void tile(const GemvArgs&, uint8_t*, int) {}
   __device__ __forceinline__ void group_done(const GemvArgs&, int64_t, int) {}
 };
@@ -603,6 +694,7 @@ template <int FMT, int R, int S, int EPI, int NW, int SLICE, class H>
 __device__ __forceinline__ void pipe_loop_w(const GemvArgs& a, int64_t nrows, const WarpTiles& w, int cta,
                                             uint8_t* xq, uint8_t* ring, float scale, H& hooks) {
   using P = Pipe<FMT>;
+  constexpr int XS = x_slices(EPI), XU = x_unit<XS>();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int kiters = int(a.ncols / 1024);
   uint8_t* wring = ring + size_t(warp) * pipe_slice<FMT, R, S, SLICE>();
@@ -623,7 +715,7 @@ __device__ __forceinline__ void pipe_loop_w(const GemvArgs& a, int64_t nrows, co
   int c_it = 0;
   const uint8_t* rd = wring;                               // slot of the tile being decoded
   const uint8_t* const rd_end = wring + S * R * P::RB;
-  const uint8_t* xp = xq + size_t(lane) * kXUnit;          // this lane's x block of the tile
+  const uint8_t* xp = xq + size_t(lane) * XU;             // this lane's x block of the tile
   if constexpr (H::kAllStaged && S >= 3) {
     // Operands one tile ahead: the next tile's codes, scales and x block are read
     // from shared memory while the cursor issues copies, before they are used.
@@ -634,19 +726,19 @@ __device__ __forceinline__ void pipe_loop_w(const GemvArgs& a, int64_t nrows, co
       __syncwarp();
 #pragma unroll
       for (int r = 0; r < R; r++) P::load(rd + r * P::RB, lane, fr[r]);
-      load_xblock(xp, xb);
+      load_xblock<XS>(xp, xb);
     }
 #pragma unroll 1
     for (int t = 0; t < w.ntiles; t++) {
 #pragma unroll
-      for (int r = 0; r < R; r++) acc[r] = __fadd_rn(acc[r], P::compute(fr[r], lane, xb));   // dead rows read zeros
+      for (int r = 0; r < R; r++) acc[r] = __fadd_rn(acc[r], P::template compute<XS>(fr[r], lane, xb));   // dead rows read zeros
       rd += R * P::RB;
       if (rd == rd_end) rd = wring;
-      xp += 32 * kXUnit;
+      xp += 32 * XU;
       if (++c_it == kiters) {
         // ---- row group done: transposed warp reduction, epilogue ------------
         c_it = 0;
-        xp = xq + size_t(lane) * kXUnit;
+        xp = xq + size_t(lane) * XU;
         float kk = warp_reduce_rows<R>(acc, lane);
 #pragma unroll
         for (int r = 0; r < R; r++) acc[r] = 0.f;
@@ -658,7 +750,7 @@ __device__ __forceinline__ void pipe_loop_w(const GemvArgs& a, int64_t nrows, co
       __syncwarp();       // ... every lane's copies; the slot of tile t - 1 is free
 #pragma unroll
       for (int r = 0; r < R; r++) P::load(rd + r * P::RB, lane, fr[r]);
-      load_xblock(xp, xb);
+      load_xblock<XS>(xp, xb);
       cur.template step<true>(a, nrows, lane);   // tile t + S - 1
     }
     cp_wait<0>();
@@ -672,26 +764,26 @@ __device__ __forceinline__ void pipe_loop_w(const GemvArgs& a, int64_t nrows, co
     __syncwarp();         // ... and every lane's (scales are copied by a few lanes); the previous slot is free
     cur.template step<true>(a, nrows, lane);
     if (!H::kAllStaged && c_it >= known) {
-      hooks.template tile<FMT>(a, xq, c_it);
+      hooks.template tile<FMT, XS>(a, xq, c_it);
       known = c_it + 1;
     }
     XBlock xb;
-    load_xblock(xp, xb);
-    xp += 32 * kXUnit;
+    load_xblock<XS>(xp, xb);
+    xp += 32 * XU;
 #pragma unroll
-    for (int r = 0; r < R; r++) acc[r] = __fadd_rn(acc[r], pipe_dot<FMT>(rd + r * P::RB, lane, xb));   // dead rows read zeros
+    for (int r = 0; r < R; r++) acc[r] = __fadd_rn(acc[r], pipe_dot<FMT, XS>(rd + r * P::RB, lane, xb));   // dead rows read zeros
     rd += R * P::RB;
     if (rd == rd_end) rd = wring;
     if (++c_it < kiters) continue;
 
     // ---- row group done: transposed warp reduction, epilogue ----------------
     c_it = 0;
-    xp = xq + size_t(lane) * kXUnit;
+    xp = xq + size_t(lane) * XU;
     float kk = warp_reduce_rows<R>(acc, lane);
 #pragma unroll
     for (int r = 0; r < R; r++) acc[r] = 0.f;
     if (!have_scale) {
-      scale = x_scale(a, xq);
+      scale = x_scale<XS>(a, xq);
       have_scale = true;
     }
     kk = __fmul_rn(kk, scale);
@@ -716,8 +808,8 @@ __device__ __forceinline__ void pipe_loop(const GemvArgs& a, int64_t nrows, int 
 template <int FMT, int R, int S, int EPI, int NW, bool TRIGGER, int SLICE = 0>
 __device__ __forceinline__ void pipe_body(const GemvArgs& a, int64_t nrows, int cta, int ncta, uint8_t* xq,
                                           uint8_t* ring) {
-  stage_x<FMT, NW>(a, xq);
-  const float scale = x_scale(a, xq);
+  stage_x<FMT, NW, x_slices(EPI)>(a, xq);
+  const float scale = x_scale<x_slices(EPI)>(a, xq);
   if (TRIGGER) {
     // the next kernel may start its own weight prefetch on SMs this grid frees;
     // it waits for this grid to finish before it reads anything this grid writes
@@ -733,14 +825,15 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe(const __grid_con
   constexpr int E = S - 1 < kPipeEarly ? S - 1 : kPipeEarly;
   extern __shared__ float4 smem4[];
   uint8_t* xq = reinterpret_cast<uint8_t*>(smem4);
-  uint8_t* ring = xq + size_t(a.ncols / 32) * kXUnit;
+  constexpr int XS = x_slices(EPI);
+  uint8_t* ring = xq + size_t(a.ncols / 32) * x_unit<XS>();
   const WarpTiles w = warp_tiles(nrows, R, int(a.ncols / 1024), threadIdx.x >> 5, NW, blockIdx.x, gridDim.x);
   pipe_issue_w<FMT, R, S>(a, nrows, w, ring, 0, E);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  stage_x<FMT, NW>(a, xq, [&] {
+  stage_x<FMT, NW, XS>(a, xq, [&] {
     if (E < S - 1) pipe_issue_w<FMT, R, S>(a, nrows, w, ring, E, S - 1);
   });
-  const float scale = x_scale(a, xq);
+  const float scale = x_scale<XS>(a, xq);
   // the next kernel may start its own weight prefetch on SMs this grid frees;
   // it waits for this grid to finish before it reads anything this grid writes
   asm volatile("griddepcontrol.launch_dependents;");
@@ -764,7 +857,8 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe2(const __grid_co
                                                                                      : pipe_slice<F2, R, S2, 0>());
   extern __shared__ float4 smem4[];
   uint8_t* xq = reinterpret_cast<uint8_t*>(smem4);
-  uint8_t* ring = xq + size_t(a1.ncols / 32) * kXUnit;
+  constexpr int XS = x_slices(EPI);
+  uint8_t* ring = xq + size_t(a1.ncols / 32) * x_unit<XS>();
   const int warp = threadIdx.x >> 5, kiters = int(a1.ncols / 1024);
   const int64_t G1 = (n1 + R - 1) / R, G = G1 + (n2 + R - 1) / R;
   WarpTiles w1, w2;
@@ -780,11 +874,11 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe2(const __grid_co
   if (w1.ntiles) pipe_issue_w<F1, R, S1, SLICE>(a1, n1, w1, ring, 0, E1);
   else pipe_issue_w<F2, R, S2, SLICE>(a2, n2, w2, ring, 0, E2);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  stage_x<F1, NW>(a1, xq, [&] {
+  stage_x<F1, NW, XS>(a1, xq, [&] {
     if (w1.ntiles) pipe_issue_w<F1, R, S1, SLICE>(a1, n1, w1, ring, E1, S1 - 1);
     else pipe_issue_w<F2, R, S2, SLICE>(a2, n2, w2, ring, E2, S2 - 1);
   });
-  const float scale = x_scale(a1, xq);
+  const float scale = x_scale<XS>(a1, xq);
   asm volatile("griddepcontrol.launch_dependents;");
   StagedHooks h;
   pipe_loop_w<F1, R, S1, EPI, NW, SLICE>(a1, n1, w1, blockIdx.x, xq, ring, scale, h);
@@ -792,12 +886,15 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe2(const __grid_co
   pipe_loop_w<F2, R, S2, EPI, NW, SLICE>(a2, n2, w2, blockIdx.x, xq, ring, scale, h);
 }
 
-inline size_t pipe_x_bytes(int64_t cols) { return size_t(cols / 32) * kXUnit; }
+inline size_t pipe_x_bytes(int64_t cols, int epi) {
+  return size_t(cols / 32) * size_t(x_slices(epi) == 3 ? x_unit<3>() : x_unit<2>());
+}
 inline int pipe_row_bytes(int fmt) {
   switch (fmt) {
     case NT_Q8_0: return Pipe<NT_Q8_0>::RB;
     case NT_Q4_0: return Pipe<NT_Q4_0>::RB;
     case NT_Q4_K: return Pipe<NT_Q4_K>::RB;
+    case NT_Q5_K: return Pipe<NT_Q5_K>::RB;
     default: return Pipe<NT_Q6_K>::RB;
   }
 }
@@ -805,7 +902,7 @@ inline int pipe_row_bytes(int fmt) {
 template <int FMT, int R, int S, int EPI, int NW>
 cudaError_t launch_gemv_pipe_t(const GemvArgs& a, cudaStream_t s, bool pdl, int* grid_used) {
   const int64_t nrows = gemv_logical_rows(a);
-  const size_t smem = pipe_x_bytes(a.ncols) + size_t(NW) * S * R * Pipe<FMT>::RB;
+  const size_t smem = pipe_x_bytes(a.ncols, EPI) + size_t(NW) * S * R * Pipe<FMT>::RB;
   if (smem > size_t(kPipeMaxSmem)) return cudaErrorInvalidValue;
   auto kern = k_gemv_pipe<FMT, R, S, EPI, NW>;
   static int s_sms = 0;
@@ -898,7 +995,7 @@ cudaError_t launch_gemv_pipe2_q4k_q6k(const GemvArgs& a1, const GemvArgs& a2, cu
   constexpr size_t slice = pipe_slice<NT_Q4_K, 2, S1, 0>() > pipe_slice<NT_Q6_K, 2, S2, 0>()
                                ? pipe_slice<NT_Q4_K, 2, S1, 0>()
                                : pipe_slice<NT_Q6_K, 2, S2, 0>();
-  const size_t smem = pipe_x_bytes(a1.ncols) + size_t(NW) * slice;
+  const size_t smem = pipe_x_bytes(a1.ncols, EPI) + size_t(NW) * slice;
   if (smem > size_t(kPipeMaxSmem) || a1.ncols != a2.ncols || a1.col0 || a2.col0) return cudaErrorInvalidValue;
   static int s_sms = 0;
   if (!s_sms) {
@@ -931,6 +1028,7 @@ cudaError_t launch_gemv_pipe2_q4k_q6k(const GemvArgs& a1, const GemvArgs& a2, cu
 NT_DECLARE_GEMV_PIPE(launch_gemv_pipe_q8_0)
 NT_DECLARE_GEMV_PIPE(launch_gemv_pipe_q4_0)
 NT_DECLARE_GEMV_PIPE(launch_gemv_pipe_q4_k)
+NT_DECLARE_GEMV_PIPE(launch_gemv_pipe_q5_k)
 NT_DECLARE_GEMV_PIPE(launch_gemv_pipe_q6_k)
 #undef NT_DECLARE_GEMV_PIPE
 

@@ -1,0 +1,12 @@
+// nt_gemv_q5_k.cu -- instantiations of the fused dequantize-GEMV for Q5_K weights.
+#include "nt_gemv_pipe.cuh"
+
+namespace nt {
+cudaError_t launch_gemv_q5_k(const GemvArgs& a, int epi, int R, cudaStream_t s, bool pdl, int* grid_used) {
+  return launch_gemv_fmt<NT_Q5_K>(a, epi, R, s, pdl, grid_used);
+}
+cudaError_t launch_gemv_pipe_q5_k(const GemvArgs& a, int epi, int R, int S, int NW, cudaStream_t s, bool pdl,
+                                  int* grid_used) {
+  return launch_gemv_pipe_fmt<NT_Q5_K>(a, epi, R, S, NW, s, pdl, grid_used);
+}
+}  // namespace nt

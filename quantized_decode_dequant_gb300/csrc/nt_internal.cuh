@@ -28,7 +28,7 @@ nt_status cuda_fail(cudaError_t e, const char* what);
 inline int block_elems(int t) {
   switch (t) {
     case NT_Q8_0: case NT_Q4_0: return 32;
-    case NT_Q4_K: case NT_Q6_K: return 256;
+    case NT_Q4_K: case NT_Q6_K: case NT_Q5_K: return 256;
   }
   return 0;
 }
@@ -38,6 +38,7 @@ inline int block_bytes(int t) {
     case NT_Q4_0: return 18;
     case NT_Q4_K: return 144;
     case NT_Q6_K: return 210;
+    case NT_Q5_K: return 176;
   }
   return 0;
 }
@@ -55,6 +56,11 @@ inline bool supported_weight_type(int t) { return block_elems(t) != 0; }
 //         within G_p, element 8w+i of the unit (w = 2p + s, i = 2j + o) sits at
 //         bit 8j + (o ? 0 : 4) + (s ? 2 : 0); meta = int8 sc per 16 elements,
 //         d = f16 per 256.  (The canonical export order is rebuilt on the host.)
+//   Q5_K: q  = low 4 bits as Q4_0; qh = one little-endian word H per 32 elements:
+//         element 8w+2i+o of the unit (w < 4, i < 4, o < 2) has its fifth bit at
+//         bit 8i + 2w + o, i.e. byte i of H serves byte i of the eight code words
+//         v = 2w+o that the low/high nibbles of the unit's four words form;
+//         meta = 16 B per 256 elements as Q4_K.
 struct QMat {
   int32_t type = 0;
   int64_t rows = 0, cols = 0;
@@ -149,7 +155,8 @@ __device__ __forceinline__ float gen_normal(uint64_t seed, uint32_t uid, uint64_
 }
 
 // One dequantized weight (flat element index e), bit-exact under the formats'
-// fp32 formulas: Q8_0 d*q, Q4_0 d*(q-8), Q4_K fma(d*sc, q, -(dmin*m)), Q6_K (d*sc)*(q-32).
+// fp32 formulas: Q8_0 d*q, Q4_0 d*(q-8), Q4_K and Q5_K fma(d*sc, q, -(dmin*m)),
+// Q6_K (d*sc)*(q-32).
 __device__ __forceinline__ int nib_at(const uint8_t* q, int64_t e) { return (q[e >> 1] >> ((e & 1) * 4)) & 15; }
 
 // Two high bits of element e of a Q6_K tensor in the device layout (see QMat).
@@ -161,6 +168,27 @@ __device__ __forceinline__ int q6_hi(const uint8_t* qh, int64_t e) {
   const int k = int(e & 31);
   const uint32_t g = *reinterpret_cast<const uint32_t*>(qh + ((e - k) >> 2) + 4 * (k >> 4));
   return int(g >> q6_hi_shift(k)) & 3;
+}
+
+// Fifth bit of element e of a Q5_K tensor in the device layout (see QMat).
+__host__ __device__ __forceinline__ int q5_hi_bit(int k) {   // k = e % 32
+  return 8 * ((k & 7) >> 1) + 2 * (k >> 3) + (k & 1);
+}
+__device__ __forceinline__ int q5_hi(const uint8_t* qh, int64_t e) {
+  const int k = int(e & 31);
+  const uint32_t h = *reinterpret_cast<const uint32_t*>(qh + ((e - k) >> 3));
+  return int(h >> q5_hi_bit(k)) & 1;
+}
+
+// 6-bit field f (sc_j for f = j, m_j for f = 8 + j) at bits [6f, 6f+6) of the
+// 12 bytes after a K-quant super-block's d and dmin
+__device__ __forceinline__ int kquant_field(const uint8_t* meta, int f) {
+  int v = 0;
+  for (int b = 0; b < 6; b++) {
+    const int bit = 6 * f + b;
+    v |= ((meta[4 + (bit >> 3)] >> (bit & 7)) & 1) << b;
+  }
+  return v;
 }
 
 __device__ __forceinline__ float dequant_elem(const QMat& m, int64_t e) {
@@ -186,6 +214,15 @@ __device__ __forceinline__ float dequant_elem(const QMat& m, int64_t e) {
       const float a = __fmul_rn(d, float(field(j)));
       const float b = __fmul_rn(dmin, float(field(8 + j)));
       return __fmaf_rn(a, float(nib_at(m.q, e)), -b);
+    }
+    case NT_Q5_K: {
+      const uint8_t* meta = m.meta + (e / 256) * 16;
+      const float d = __half2float(__ushort_as_half(uint16_t(meta[0] | (meta[1] << 8))));
+      const float dmin = __half2float(__ushort_as_half(uint16_t(meta[2] | (meta[3] << 8))));
+      const int j = int((e % 256) / 32);
+      const float a = __fmul_rn(d, float(kquant_field(meta, j)));
+      const float b = __fmul_rn(dmin, float(kquant_field(meta, 8 + j)));
+      return __fmaf_rn(a, float(nib_at(m.q, e) | (q5_hi(m.qh, e) << 4)), -b);
     }
     case NT_Q6_K: {
       const int q = nib_at(m.q, e) | (q6_hi(m.qh, e) << 4);

@@ -53,6 +53,7 @@ StreamSizes stream_sizes(int type, int64_t rows, int64_t cols) {
     case NT_Q4_0: s.q = n / 2; s.d = n / 32 * 2; break;
     case NT_Q4_K: s.q = n / 2; s.meta = n / 256 * 16; break;
     case NT_Q6_K: s.q = n / 2; s.qh = n / 4; s.meta = n / 16; s.d = n / 256 * 2; break;
+    case NT_Q5_K: s.q = n / 2; s.qh = n / 8; s.meta = n / 256 * 16; break;
   }
   return s;
 }
@@ -114,7 +115,9 @@ __global__ void __launch_bounds__(256) k_generate(QMat m, uint64_t seed, uint32_
       *reinterpret_cast<uint32_t*>(m.q + ebase / 2) = wd;
     }
     if ((lane & 3) == 0) m.d[ebase / 32] = __float2half_rn(d32);
-  } else if (T == NT_Q4_K) {
+  } else if (T == NT_Q4_K || T == NT_Q5_K) {
+    constexpr float kLevels = T == NT_Q4_K ? 15.0f : 31.0f;
+    constexpr int kMaxQ = T == NT_Q4_K ? 15 : 31;
     float lo = 0.0f, hi = w[0];
 #pragma unroll
     for (int k = 0; k < 8; k++) { lo = fminf(lo, w[k]); hi = fmaxf(hi, w[k]); }
@@ -123,7 +126,7 @@ __global__ void __launch_bounds__(256) k_generate(QMat m, uint64_t seed, uint32_
       lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
       hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
     }
-    const float s = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+    const float s = __fdiv_rn(__fsub_rn(hi, lo), kLevels);
     const float ms = __fsub_rn(0.0f, lo);
     float smax = s, mmax = ms;
 #pragma unroll
@@ -137,13 +140,20 @@ __global__ void __launch_bounds__(256) k_generate(QMat m, uint64_t seed, uint32_
     const int sc = d == 0.0f ? 0 : clampi(rnd(__fdiv_rn(s, d)), 0, 63);
     const int mm = dmin == 0.0f ? 0 : clampi(rnd(__fdiv_rn(ms, dmin)), 0, 63);
     const float a = __fmul_rn(d, float(sc)), b = __fmul_rn(dmin, float(mm));
-    uint32_t wd = 0u;
+    uint32_t wd = 0u, hb = 0u;
+    const int wi = lane & 3;   // this lane's code word within the 32-element unit
 #pragma unroll
     for (int k = 0; k < 8; k++) {
-      int q = a == 0.0f ? 0 : clampi(rnd(__fdiv_rn(__fadd_rn(w[k], b), a)), 0, 15);
-      wd |= uint32_t(q) << (4 * k);
+      int q = a == 0.0f ? 0 : clampi(rnd(__fdiv_rn(__fadd_rn(w[k], b), a)), 0, kMaxQ);
+      wd |= uint32_t(q & 15) << (4 * k);
+      if (T == NT_Q5_K) hb |= uint32_t(q >> 4) << q5_hi_bit(8 * wi + k);
     }
     *reinterpret_cast<uint32_t*>(m.q + ebase / 2) = wd;
+    if (T == NT_Q5_K) {   // the unit's four lanes share one fifth-bit word
+      hb |= __shfl_xor_sync(0xffffffffu, hb, 1);
+      hb |= __shfl_xor_sync(0xffffffffu, hb, 2);
+      if (wi == 0) *reinterpret_cast<uint32_t*>(m.qh + ebase / 8) = hb;
+    }
     // 96-bit field stream: field f (sc_j for f = j, m_j for f = 8 + j) at bits [6f, 6f+6)
     uint64_t lo64 = 0, hi64 = 0;
 #pragma unroll
@@ -205,6 +215,7 @@ cudaError_t launch_generate(const QMat& m, uint64_t seed, uint32_t uid, float st
     case NT_Q4_0: k_generate<NT_Q4_0><<<grid, block, 0, s>>>(m, seed, uid, std); break;
     case NT_Q4_K: k_generate<NT_Q4_K><<<grid, block, 0, s>>>(m, seed, uid, std); break;
     case NT_Q6_K: k_generate<NT_Q6_K><<<grid, block, 0, s>>>(m, seed, uid, std); break;
+    case NT_Q5_K: k_generate<NT_Q5_K><<<grid, block, 0, s>>>(m, seed, uid, std); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -267,6 +278,18 @@ static nt_status export_rows(const nt_qtensor* t, int64_t row0, int64_t nrows, u
         memcpy(out, &meta[b * 16], 16);
         memcpy(out + 16, &q[e / 2], 128);
         break;
+      case NT_Q5_K: {
+        memcpy(out, &meta[b * 16], 16);
+        // canonical fifth bits: element k of the block at byte k/8, bit k%8
+        uint8_t* cqh = out + 16;
+        memset(cqh, 0, 32);
+        for (int k = 0; k < 256; k++) {
+          const uint8_t* hp = &qh[(e + (k & ~31)) / 8];
+          const uint32_t h = uint32_t(hp[0]) | (uint32_t(hp[1]) << 8) | (uint32_t(hp[2]) << 16) | (uint32_t(hp[3]) << 24);
+          cqh[k >> 3] |= uint8_t(((h >> q5_hi_bit(k & 31)) & 1) << (k & 7));
+        }
+        memcpy(out + 48, &q[e / 2], 128);
+      } break;
       case NT_Q6_K: {
         memcpy(out, &q[e / 2], 128);
         // canonical high bits: element k of the block at byte k/4, bits 2(k%4)

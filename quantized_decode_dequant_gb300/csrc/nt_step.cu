@@ -3,8 +3,11 @@
 
 namespace nt {
 
-size_t step_smem(const StepPlan& p, int64_t max_cols, int attn_chunk, size_t* ring_off) {
-  const size_t lo = (size_t(max_cols / 32) * kXUnit + 127) & ~size_t(127);
+size_t step_smem(const StepPlan& p, int64_t max_cols, int64_t qkv_cols, int attn_chunk, size_t* ring_off) {
+  // staged x of the widest GEMV input, or of the Q/K/V input with its three slices
+  size_t xb = pipe_x_bytes(max_cols, EPI_ADD);
+  if (pipe_x_bytes(qkv_cols, EPI_QKV) > xb) xb = pipe_x_bytes(qkv_cols, EPI_QKV);
+  const size_t lo = (xb + 127) & ~size_t(127);
   *ring_off = lo;
   const size_t gemv = lo + kStepRingBytes;
   const size_t attn = attn_item_smem(p.hd, p.G, attn_chunk);

@@ -147,7 +147,7 @@ struct StepHooks {
   unsigned tag = 0;
   volatile int32_t* err = nullptr;
 
-  template <int FMT>
+  template <int FMT, int XS>
   __device__ __forceinline__ void tile(const GemvArgs& a, uint8_t* xq, int k) {
     const int lane = threadIdx.x & 31;
     volatile unsigned* st = tstate + k;
@@ -161,7 +161,7 @@ struct StepHooks {
     if (mine) {
       if (lane == 0 && ready) wait_count(ready + k, target, err);
       __syncwarp();
-      stage_tile<FMT>(a.x + a.col0, k, xq);
+      stage_tile<FMT, XS>(a.x + a.col0, k, xq);
       __syncwarp();
       __threadfence_block();
       if (lane == 0) atomicExch(tstate + k, staged);
@@ -185,10 +185,10 @@ struct StepHooks {
   // At the start of a GEMV: warp w claims and stages tiles w, w + 16, ... as their
   // inputs become ready, so the tiles are staged in parallel rather than in the
   // order the first row group reaches them.
-  template <int FMT>
+  template <int FMT, int XS>
   __device__ __forceinline__ void prestage(const GemvArgs& a, uint8_t* xq) {
     const int kt = int(a.ncols / 1024);
-    for (int k = threadIdx.x >> 5; k < kt; k += kStepWarps) tile<FMT>(a, xq, k);
+    for (int k = threadIdx.x >> 5; k < kt; k += kStepWarps) tile<FMT, XS>(a, xq, k);
   }
 
   __device__ __forceinline__ void group_done(const GemvArgs& a, int64_t grp, int nlive) {
@@ -238,7 +238,7 @@ __device__ __noinline__ void step_prologue(const StepGemv& g, uint8_t* ring) {
 }
 template <int FMT, int EPI>
 __device__ __noinline__ void step_gemv(const StepGemv& g, uint8_t* xq, uint8_t* ring, StepHooks& h) {
-  h.template prestage<FMT>(g.a, xq);
+  h.template prestage<FMT, x_slices(EPI)>(g.a, xq);
   pipe_loop<FMT, 2, StepRing<FMT>::S, EPI, kStepWarps, kStepSlice>(g.a, g.nrows, blockIdx.x, gridDim.x, xq, ring,
                                                                    1.0f, h);
 }
@@ -543,7 +543,7 @@ struct StepPlan {
 // Dynamic shared memory of k_step for a plan: x staging of the widest GEMV then
 // the warps' ring slices, or an attention item if that is larger (the two are
 // never live at once).
-size_t step_smem(const StepPlan& p, int64_t max_cols, int attn_chunk, size_t* ring_off);
+size_t step_smem(const StepPlan& p, int64_t max_cols, int64_t qkv_cols, int attn_chunk, size_t* ring_off);
 
 // Launches k_step for the plan (cooperative, one CTA per SM); whether it fits
 // with `smem` bytes.  Both return cudaErrorNotSupported when no instantiation

@@ -21,7 +21,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "nt.h")
 
 NT_OK, NT_E_INVAL, NT_E_NOMEM, NT_E_CUDA, NT_E_TIMEOUT, NT_E_UNSUPPORTED, NT_E_STATE = range(7)
 STATUS_NAMES = ["NT_OK", "NT_E_INVAL", "NT_E_NOMEM", "NT_E_CUDA", "NT_E_TIMEOUT", "NT_E_UNSUPPORTED", "NT_E_STATE"]
-QTYPES = {"f32": 0, "f16": 1, "q8_0": 2, "q4_0": 3, "q4_k": 4, "q6_k": 5}
+QTYPES = {"f32": 0, "f16": 1, "q8_0": 2, "q4_0": 3, "q4_k": 4, "q6_k": 5, "q5_k": 6}
 ROLES = {"q": 0, "k": 1, "v": 2, "o": 3, "gate": 4, "up": 5, "down": 6, "embd": 16, "output": 17}
 KC_GEMV, KC_ATTN, KC_OTHER = 0, 1, 2
 
@@ -77,6 +77,10 @@ _SIGS = {
     "nt_profile_gemvs": (C.c_int, [_vp, _i32, C.POINTER(C.c_double), C.POINTER(C.c_double), C.POINTER(_i32)]),
     "nt_plan_residency": (C.c_int, [C.POINTER(nt_config), _i64, C.POINTER(_i32), C.POINTER(_i64), C.POINTER(_i64)]),
     "nt_auto_residency": (C.c_int, [_vp, _i64, C.POINTER(_i32)]),
+    "nt_layer_similarity": (C.c_int, [_vp, _i32, C.POINTER(_i32), C.POINTER(C.c_double)]),
+    "nt_set_layer_skip": (C.c_int, [_vp, C.POINTER(C.c_uint8)]),
+    "nt_plan_layer_skip": (C.c_int, [C.POINTER(C.c_double), _i32, C.c_double, _i32, C.POINTER(C.c_uint8),
+                                     C.POINTER(_i32)]),
     "nt_model_tensor": (C.c_int, [_vp, _i32, _i32, C.POINTER(C.c_void_p)]),
     "nt_qtensor_create": (C.c_int, [C.c_int, _i64, _i64, _u64, C.c_uint32, C.c_float, C.POINTER(C.c_void_p)]),
     "nt_qtensor_destroy": (None, [_vp]),
@@ -146,14 +150,24 @@ def make_config(*, n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn_dim, voc
 
 # ------------------------------------------------------------------- model --
 
+_n_layers: dict[int, int] = {}   # layer count of each live model handle
+
+
 def nt_model_create(cfg: nt_config) -> int:
     h = C.c_void_p()
     _check(lib().nt_model_create(C.byref(cfg), C.byref(h)), "nt_model_create")
+    _n_layers[h.value] = cfg.n_layers
     return h.value
 
 
 def nt_model_destroy(m: int) -> None:
+    _n_layers.pop(m, None)
     lib().nt_model_destroy(m)
+
+
+def stats_layers(m: int) -> int:
+    """Layer count of a model created through this module."""
+    return _n_layers[m]
 
 
 def nt_kv_reset(m: int) -> None:
@@ -228,6 +242,37 @@ def nt_auto_residency(m: int, margin_bytes: int = 1 << 30) -> int:
     n = C.c_int32()
     _check(lib().nt_auto_residency(m, margin_bytes, C.byref(n)), "nt_auto_residency")
     return n.value
+
+
+def nt_layer_similarity(m: int, token: int) -> tuple[int, np.ndarray]:
+    """One decode step that also returns the per-layer cosine between the residual entering and leaving it."""
+    n = stats_layers(m)
+    cos = np.empty(max(n, 1), np.float64)
+    nx = C.c_int32()
+    _check(lib().nt_layer_similarity(m, token, C.byref(nx), cos.ctypes.data_as(C.POINTER(C.c_double))),
+           "nt_layer_similarity")
+    return nx.value, cos[:n]
+
+
+def nt_set_layer_skip(m: int, mask) -> None:
+    """Skips the layers whose mask entry is nonzero (None: none)."""
+    if mask is None:
+        _check(lib().nt_set_layer_skip(m, None), "nt_set_layer_skip")
+        return
+    a = np.ascontiguousarray(np.asarray(mask).astype(np.uint8))
+    assert a.size == stats_layers(m)
+    _check(lib().nt_set_layer_skip(m, a.ctypes.data_as(C.POINTER(C.c_uint8))), "nt_set_layer_skip")
+
+
+def nt_plan_layer_skip(cos, threshold: float, max_skip: int = 0) -> np.ndarray:
+    """uint8 mask of the layers to skip for calibrated similarities (host arithmetic)."""
+    c = np.ascontiguousarray(np.asarray(cos, np.float64))
+    mask = np.zeros(max(c.size, 1), np.uint8)
+    n = C.c_int32()
+    _check(lib().nt_plan_layer_skip(c.ctypes.data_as(C.POINTER(C.c_double)), c.size, threshold, max_skip,
+                                    mask.ctypes.data_as(C.POINTER(C.c_uint8)), C.byref(n)), "nt_plan_layer_skip")
+    assert int(mask[:c.size].sum()) == n.value
+    return mask[:c.size]
 
 
 def nt_model_tensor(m: int, layer: int, role) -> int:

@@ -23,15 +23,17 @@ LLAMA_70B_Q4_K_M = dict(LLAMA_70B, max_ctx=4096 + 128, **Q4_K_M)
 LLAMA_70B_Q4_K_M_CTX, LLAMA_70B_Q4_K_M_STEPS = 4096, 128
 
 ALL_Q6_K = {k: "q6_k" for k in Q4_K_M}
+# Q5_K_M-style mix: attn_v, ffn_down and output in Q6_K, everything else Q5_K
+Q5_K_M = dict(Q4_K_M, **{k: "q5_k" for k, v in Q4_K_M.items() if v == "q4_k"})
 LLAMA_70B_Q6_K = dict(LLAMA_70B, max_ctx=1024 + 32, **ALL_Q6_K)
 LLAMA_70B_Q6_K_CTX, LLAMA_70B_Q6_K_STEPS, LLAMA_70B_Q6_K_RESIDENT = 1024, 32, 26
 
 # isolated dequant-GEMV sweep at 70B layer shapes (out x in)
 GEMV_SHAPES = [(8192, 8192), (1024, 8192), (28672, 8192), (8192, 28672), (128256, 8192)]
-GEMV_FORMATS = ["q4_0", "q8_0", "q4_k", "q6_k"]
+GEMV_FORMATS = ["q4_0", "q8_0", "q4_k", "q6_k", "q5_k"]
 
-BLOCK_ELEMS = {"q8_0": 32, "q4_0": 32, "q4_k": 256, "q6_k": 256}
-BLOCK_BYTES = {"q8_0": 34, "q4_0": 18, "q4_k": 144, "q6_k": 210}
+BLOCK_ELEMS = {"q8_0": 32, "q4_0": 32, "q4_k": 256, "q6_k": 256, "q5_k": 256}
+BLOCK_BYTES = {"q8_0": 34, "q4_0": 18, "q4_k": 144, "q6_k": 210, "q5_k": 176}
 
 
 def weight_bytes(spec: dict) -> int:

@@ -60,8 +60,14 @@ def test_tiny_teacher_forced_64_steps(nt, W):
         nt.nt_model_destroy(m)
 
 
-def test_tiny_mixed_formats_teacher_forced(nt, W):
-    spec = dict(W.TINY, **W.Q4_K_M)
+WIDE = dict(n_layers=2, hidden=1024, n_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=2048, vocab=4096, max_ctx=64)
+
+
+@pytest.mark.parametrize("mix,shape", [("q4_k_m", "tiny"), ("q5_k_m", "tiny"), ("q5_k_m", "wide"),
+                                       ("q4_k_m", "wide")])
+def test_tiny_mixed_formats_teacher_forced(nt, W, mix, shape):
+    """Mixed K-quant formats; 'wide' widths (multiples of 1024) take the shared-memory pipeline everywhere."""
+    spec = dict(W.TINY if shape == "tiny" else WIDE, **(W.Q4_K_M if mix == "q4_k_m" else W.Q5_K_M))
     m = nt.nt_model_create(nt.make_config(**spec, seed=4))
     om = oracle.Model(oracle.ModelSpec(**spec, seed=4))
     try:

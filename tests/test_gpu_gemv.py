@@ -7,7 +7,7 @@ from gpu_util import ensure_built, rel_l2, torch_cuda
 from inputs import activation
 
 pytestmark = pytest.mark.gpu
-FORMATS = ["q8_0", "q4_0", "q4_k", "q6_k"]
+FORMATS = ["q8_0", "q4_0", "q4_k", "q6_k", "q5_k"]
 TOL = 2e-3   # relative L2 against fp64 accumulation of the same dequantized weights
 
 

@@ -6,7 +6,7 @@ import oracle
 from gpu_util import blocks, ensure_built, torch_cuda
 
 pytestmark = pytest.mark.gpu
-FORMATS = ["q8_0", "q4_0", "q4_k", "q6_k"]
+FORMATS = ["q8_0", "q4_0", "q4_k", "q6_k", "q5_k"]
 
 
 @pytest.fixture(scope="module")

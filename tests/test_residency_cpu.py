@@ -22,6 +22,8 @@ def stream_bytes(fmt, rows, cols):
         parts = [e // 2, e // 32 * 2]
     elif fmt == "q4_k":
         parts = [e // 2, e // 256 * 16]
+    elif fmt == "q5_k":   # low nibbles, fifth-bit words, 16 B per 256
+        parts = [e // 2, e // 8, e // 256 * 16]
     else:  # q6_k: low nibbles, high-bit words, int8 scale per 16, f16 d per 256
         parts = [e // 2, e // 4, e // 16, e // 256 * 2]
     return sum(pad(p) for p in parts)
@@ -46,9 +48,9 @@ def lib():
     return nt
 
 
-@pytest.mark.parametrize("name", ["LLAMA_8B_Q8_0", "LLAMA_70B_Q4_K_M", "LLAMA_70B_Q6_K"])
+@pytest.mark.parametrize("name", ["LLAMA_8B_Q8_0", "LLAMA_70B_Q4_K_M", "LLAMA_70B_Q6_K", "LLAMA_70B_Q5_K_M"])
 def test_layer_bytes_match_the_stream_layout(lib, name):
-    spec = getattr(W, name)
+    spec = getattr(W, name) if name != "LLAMA_70B_Q5_K_M" else dict(W.LLAMA_70B, max_ctx=4224, **W.Q5_K_M)
     n, dev, lay = lib.nt_plan_residency(lib.make_config(**spec), 1 << 50)
     assert lay == layer_bytes(spec)
     assert n == spec["n_layers"]
