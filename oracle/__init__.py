@@ -96,6 +96,7 @@ def lib():
         L.orc_kv_get.restype = C.c_uint16
         L.orc_kv_get.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int]
         L.orc_set_layer_skip.argtypes = [C.c_void_p, u8p]
+        L.orc_set_pos.argtypes = [C.c_void_p, C.c_int32]
         L.orc_layer_cos.argtypes = [C.c_void_p, f64p]
         L.orc_hidden.argtypes = [C.c_void_p, f64p]
         L.orc_cosine.restype = C.c_double
@@ -378,3 +379,58 @@ class Model:
         out = np.empty(self.spec.hidden, np.float64)
         lib().orc_hidden(self._h, _p(out, C.c_double))
         return out
+
+    def set_pos(self, pos: int):
+        """Moves the position back (or forward) without touching the cache."""
+        if lib().orc_set_pos(self._h, pos):
+            raise ValueError(pos)
+
+
+def speculative_cycles(spec: ModelSpec, n_draft: int, k: int, token: int, n_cycles: int,
+                       prefill: tuple[int, int] | None = None, nthreads: int = 1):
+    """Self-speculative decoding ([hada] "Architektur und Codestruktur": the
+    VRAM-resident layers serve as the draft model, no extra model), from its
+    definition.  Per cycle at position p with input token t:
+      draft    d_1..d_k = greedy continuation of the model restricted to layers
+               [0, n_draft) and the output head, from t;
+      verify   y_i = the full model's greedy token at position p + i after
+               t, d_1..d_i (i < k);
+      accept   j = the length of the longest prefix with y_i == d_{i+1};
+               emitted: d_1..d_j, then y_j when j < k.
+    Returns [(emitted tokens, j), ...].  The emitted stream is the full model's
+    greedy stream; the draft only decides how many tokens a cycle yields."""
+    full = Model(spec, nthreads=nthreads)
+    draft = Model(spec, nthreads=nthreads)
+    draft.set_layer_skip([1 if l >= n_draft else 0 for l in range(spec.n_layers)])
+    try:
+        if prefill:
+            full.kv_prefill(*prefill)
+            draft.kv_prefill(*prefill)
+        out = []
+        t = token
+        for _ in range(n_cycles):
+            p = full.pos
+            d, tt = [], t
+            for _ in range(k):              # the draft's own greedy continuation
+                _, tt, _ = draft.decode_step(tt)
+                d.append(tt)
+            draft.set_pos(p)
+            y, tt = [], t
+            for i in range(k):              # the full model on t, d_1..d_{k-1}
+                _, yi, _ = full.decode_step(tt)
+                y.append(yi)
+                if yi != d[i]:
+                    break
+                tt = d[i]
+            j = len(y) if y[-1] == d[len(y) - 1] else len(y) - 1
+            emitted = d[:j] + ([y[j]] if j < k else [])
+            full.set_pos(p)
+            for e in [t] + emitted[:-1]:    # both models advance over the emitted prefix
+                full.decode_step(e)
+                draft.decode_step(e)
+            out.append((emitted, j))
+            t = emitted[-1]
+        return out
+    finally:
+        full.close()
+        draft.close()

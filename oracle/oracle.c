@@ -679,6 +679,13 @@ int orc_kv_reset(orc_model* m) {
   return 0;
 }
 
+/* Moves the position (rows at and past it are overwritten as decoding reaches them). */
+int orc_set_pos(orc_model* m, int32_t pos) {
+  if (pos < 0 || pos > m->c.max_ctx) return -1;
+  m->pos = pos;
+  return 0;
+}
+
 static size_t kv_index(const orc_config* c, int l, int kv, int kvh, int64_t t, int d) {
   return ((((size_t)l * 2 + kv) * c->n_kv_heads + kvh) * (size_t)c->max_ctx + (size_t)t) * c->head_dim + d;
 }

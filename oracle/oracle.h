@@ -98,6 +98,7 @@ enum { ORC_ROLE_Q = 0, ORC_ROLE_K, ORC_ROLE_V, ORC_ROLE_O, ORC_ROLE_GATE, ORC_RO
 orc_model* orc_model_create(const orc_config* cfg);
 void       orc_model_destroy(orc_model* m);
 int        orc_kv_reset(orc_model* m);
+int        orc_set_pos(orc_model* m, int32_t pos);
 int        orc_kv_prefill(orc_model* m, int32_t n_ctx, uint64_t seed);
 int32_t    orc_pos(const orc_model* m);
 void       orc_set_threads(orc_model* m, int32_t nthreads);

@@ -91,7 +91,6 @@ __global__ void k_argmax(const float4* __restrict__ top2, int n, int32_t* d_pos,
   }
 }
 
-// f16 N(0,1) prefill; counter index of (t, kv head g, d) is (t*n_kv + g)*hd + d.
 // cos[l] = <a, b> / (|a| |b|) for a = hs[l], b = hs[l + 1] (0 when either is zero):
 // one CTA per layer, fp64 partial sums in a fixed order.
 __global__ void __launch_bounds__(256) k_layer_cos(const float* __restrict__ hs, int n, double* __restrict__ cos) {
@@ -128,6 +127,7 @@ __global__ void __launch_bounds__(256) k_layer_cos(const float* __restrict__ hs,
   }
 }
 
+// f16 N(0,1) prefill; counter index of (t, kv head g, d) is (t*n_kv + g)*hd + d.
 __global__ void k_kv_prefill(__half* kv, int n_layers, int n_kv, int max_ctx, int hd, int n_ctx, uint64_t seed) {
   const int64_t per = int64_t(n_ctx) * n_kv * hd;
   const int64_t total = int64_t(n_layers) * 2 * per;

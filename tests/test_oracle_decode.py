@@ -181,3 +181,46 @@ def test_skip_plan_threshold_and_cap():
     np.testing.assert_array_equal(oracle.plan_layer_skip(cos, 0.98, max_skip=2), [0, 1, 0, 0, 1, 0])  # tie: lower layer
     np.testing.assert_array_equal(oracle.plan_layer_skip(cos, 0.999), [0] * 6)
     np.testing.assert_array_equal(oracle.plan_layer_skip(cos, -1.0, max_skip=1), [0, 0, 0, 0, 1, 0])
+
+
+# ---- self-speculative decoding (resident layers as the draft)
+
+def _greedy(spec, token, n, prefill=None):
+    m = oracle.Model(spec)
+    if prefill:
+        m.kv_prefill(*prefill)
+    out, t = [], token
+    for _ in range(n):
+        _, t, _ = m.decode_step(t)
+        out.append(t)
+    return out
+
+
+@pytest.mark.parametrize("n_draft,k", [(3, 4), (1, 4), (0, 3), (2, 1)])
+def test_speculative_stream_is_the_greedy_stream(n_draft, k):
+    spec = _spec(n_layers=3, vocab=512, max_ctx=48)
+    cycles = oracle.speculative_cycles(spec, n_draft, k, 7, 6, prefill=(5, 2))
+    stream = [t for emitted, _ in cycles for t in emitted]
+    assert stream == _greedy(spec, 7, len(stream), prefill=(5, 2))
+    for emitted, j in cycles:
+        assert 0 <= j <= k and len(emitted) == (j + 1 if j < k else k)
+    if n_draft == spec.n_layers:           # the draft is the full model: everything is accepted
+        assert all(j == k for _, j in cycles)
+    if k == 1:
+        assert all(len(e) == 1 for e, _ in cycles)
+
+
+def test_speculative_zero_layer_draft_acceptance_is_agreement_with_the_head():
+    # with n_draft = 0 the draft proposes argmax(head(norm(embedding(t)))): the
+    # first proposal is accepted exactly when the full model's next token equals it
+    spec = _spec(n_layers=2, vocab=256, max_ctx=32)
+    cycles = oracle.speculative_cycles(spec, 0, 2, 11, 5)
+    zero = oracle.Model(_spec(n_layers=0, vocab=256, max_ctx=32))
+    greedy = _greedy(spec, 11, sum(len(e) for e, _ in cycles))
+    pos, t = 0, 11
+    for emitted, j in cycles:
+        zero.set_pos(pos)
+        _, d1, _ = zero.decode_step(t)
+        assert (j >= 1) == (d1 == greedy[pos])
+        pos += len(emitted)
+        t = emitted[-1]
