@@ -52,6 +52,10 @@ def parse_args(argv=None):
     p.add_argument("--layer-skip", type=int, default=0, metavar="MAX",
                    help="calibrate per-layer similarity, then skip up to MAX layers at or above --skip-threshold")
     p.add_argument("--skip-threshold", type=float, default=0.98)
+    p.add_argument("--speculative", type=int, default=0, metavar="K",
+                   help="time self-speculative cycles of K draft tokens instead of plain steps")
+    p.add_argument("--draft-layers", type=int, default=None,
+                   help="draft model depth (default: the resident layers, else a quarter of the layers)")
     p.add_argument("--layers", type=int, default=None,
                    help="profiling aid: the workload's shapes with this many layers (not a bench line)")
     return p.parse_args(argv)
@@ -259,9 +263,9 @@ def step_traffic(wl, step_bytes):
 # DRAM bytes (read + write) per algorithmic byte of the GEMV kernel, from the ncu
 # capture summarised in profiles/k_gemv_pipe_q8_0_57344x4096.md, and the SHA-256 of
 # the kernel sources that capture was taken on: a changed kernel reports no traffic.
-GEMV_DRAM_PER_BYTE = (249.612032 + 3.821312) / (57344 * 4096 * 1.0625 + 4 * (57344 + 4096)) * 1e6
+GEMV_DRAM_PER_BYTE = (249.624320 + 3.564544) / (57344 * 4096 * 1.0625 + 4 * (57344 + 4096)) * 1e6
 GEMV_SOURCES = ("nt_gemv_pipe.cuh", "nt_gemv.cuh")
-GEMV_SOURCES_SHA256 = "660f4bfd33ef11d9f9d33fd611d8377be292ecd8175359da9bb7159ba558e03d"
+GEMV_SOURCES_SHA256 = "d65f5d76ce96e30cfff0cca3f779287c252a4407f07ce505f77f3d3452b007d0"
 
 
 def gemv_sources_sha256() -> str:
@@ -387,10 +391,32 @@ def run_ours(args, wl, rank, world, local, dist):
         reset()
         clocks = ClockSampler(local)
         h2d_stats = None
+        spec_stats = None
+        n_draft = args.draft_layers if args.draft_layers is not None else (
+            wl["resident"] if streamed else spec["n_layers"] // 4)
         with clocks:
             barrier(dist)
             torch.cuda.synchronize()
-            if streamed:
+            if args.speculative:
+                # cycles until `steps` tokens are emitted; each cycle copies the
+                # host-tier layers once for up to K tokens
+                t0 = time.perf_counter()
+                t, emitted, cycles, accepted, h2d_b = tok0, 0, 0, 0, 0.0
+                while emitted < args.steps:
+                    e, j = nt.nt_speculative_step(m, t, n_draft, args.speculative)
+                    t = e[-1]
+                    emitted += len(e)
+                    cycles += 1
+                    accepted += j
+                    h2d_b += nt.nt_get_stats(m).h2d_bytes
+                torch.cuda.synchronize()
+                sec = (time.perf_counter() - t0) * args.steps / emitted
+                spec_stats = {"k": args.speculative, "draft_layers": n_draft, "cycles": cycles,
+                              "tokens": emitted, "tokens_per_cycle": round(emitted / cycles, 3),
+                              "accepted_per_cycle": round(accepted / cycles, 3),
+                              "h2d_GB_per_token": round(h2d_b / emitted / 1e9, 3),
+                              "note": "acceptance is meaningless on random weights; the cycle cost is the measurement"}
+            elif streamed:
                 t0 = time.perf_counter()
                 t = tok0
                 h2d_b = h2d_ms = comp_ms = ov = 0.0
@@ -514,6 +540,8 @@ def run_ours(args, wl, rank, world, local, dist):
         line["streaming"] = h2d_stats
     if skip_info:
         line["layer_skip"] = skip_info
+    if spec_stats:
+        line["speculative"] = spec_stats
     if sweep:
         line["gemv_sweep"] = sweep
         line["gemv_sweep_min_frac"] = min(s["frac"] for s in sweep)

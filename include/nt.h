@@ -200,7 +200,7 @@ nt_status nt_plan_residency(const nt_config* cfg, int64_t budget_bytes, int32_t*
  * the placement. */
 nt_status nt_auto_residency(nt_model* m, int64_t margin_bytes, int32_t* n_resident_out);
 
-/* ---- layer skip (hada "Hauptfunktionen": layer skip by cosine similarity;
+/* ---- layer skip (hada "Leistung und Caching-Struktur": layer skip by cosine similarity;
  * hotdry "性能数据与瓶颈分析": the similarity between layer outputs is
  * computed beforehand and layers at or above the threshold, 0.98 there, are
  * skipped at inference) ----
@@ -227,6 +227,28 @@ nt_status nt_set_layer_skip(nt_model* m, const uint8_t* mask);
  * NT_E_INVAL on NULL arrays or n_layers < 0. */
 nt_status nt_plan_layer_skip(const double* cos, int32_t n_layers, double threshold, int32_t max_skip,
                              uint8_t* mask_out, int32_t* n_skipped);
+
+/* ---- self-speculative decoding (hada "Hauptfunktionen": the
+ * VRAM-resident layers serve as the draft model, no extra model) ----
+ *
+ * One cycle from the current position p with input token `token`:
+ *   draft   k greedy steps (1 <= k <= 8) of the model restricted to layers
+ *           [0, n_draft) and the output head: d_1..d_k;
+ *   verify  layers [n_draft, n_layers) and the head for token, d_1..d_{k-1} at
+ *           positions p..p+k-1, layer by layer, so a host-tier layer is copied
+ *           once per cycle rather than once per token; y_i is the full model's
+ *           greedy token after position p+i;
+ *   accept  j = the longest prefix with y_i == d_{i+1}; the emitted tokens are
+ *           d_1..d_j, then y_j when j < k.
+ * The emitted tokens are those nt_decode_step would produce from the same state,
+ * bit for bit (every token runs the same kernels on the same inputs; layers
+ * below n_draft are not recomputed, their K/V rows from the draft are the full
+ * model's).  out_tokens (host, >= k entries) receives them, *n_out their count
+ * (j + 1, or k when all are accepted), *n_accepted (nullable) j; the position
+ * advances by *n_out.  Layers the skip mask names are skipped in both passes.
+ * NT_E_INVAL: bad token, k or n_draft, or p + k > max_ctx. */
+nt_status nt_speculative_step(nt_model* m, int32_t token, int32_t n_draft, int32_t k, int32_t* out_tokens,
+                              int32_t* n_out, int32_t* n_accepted);
 
 nt_status nt_get_stats(const nt_model* m, nt_stats* out);
 

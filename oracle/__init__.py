@@ -388,7 +388,7 @@ class Model:
 
 def speculative_cycles(spec: ModelSpec, n_draft: int, k: int, token: int, n_cycles: int,
                        prefill: tuple[int, int] | None = None, nthreads: int = 1):
-    """Self-speculative decoding ([hada] "Architektur und Codestruktur": the
+    """Self-speculative decoding ([hada] "Hauptfunktionen": the
     VRAM-resident layers serve as the draft model, no extra model), from its
     definition.  Per cycle at position p with input token t:
       draft    d_1..d_k = greedy continuation of the model restricted to layers

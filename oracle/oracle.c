@@ -635,7 +635,7 @@ void orc_model_destroy(orc_model* m) {
   free(m);
 }
 
-/* Layer skip ([hada] "Hauptfunktionen": layers skipped by cosine similarity;
+/* Layer skip ([hada] "Leistung und Caching-Struktur": layers skipped by cosine similarity;
  * [hotdry] "性能数据与瓶颈分析": similarity between layer outputs is computed
  * beforehand and layers above the threshold are skipped at inference).  Reading:
  * a skipped layer is not evaluated at all -- the residual stream passes through

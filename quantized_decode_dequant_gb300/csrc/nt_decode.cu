@@ -195,7 +195,11 @@ struct nt_model {
   int step_state = 0;                // 0 unknown, 1 ready, -1 not applicable
   int32_t* small = nullptr;          // pos, token, next, margin(float bits), error word
   int32_t* hist = nullptr;           // produced ids by position
-  int32_t* h_io = nullptr;           // pinned host mirror of small
+  int32_t* h_io = nullptr;           // pinned host mirror of small; [32, 56): speculative step
+  float* sp_x = nullptr;             // speculative step: residual of each draft token after the draft layers
+  int32_t* sp_i = nullptr;           // speculative step: positions [0, 8), full-model tokens [8, 16), draft tokens [16, 24)
+  float* cur_x = nullptr;            // residual the enqueue helpers use (nullptr: x)
+  int32_t* cur_pos = nullptr;        // device position the enqueue helpers use (nullptr: the step's)
   int n_chunks = 0;
   cudaStream_t stream = nullptr, copy_stream = nullptr;
   cudaGraph_t graph = nullptr;
@@ -222,6 +226,10 @@ static int32_t* d_pos(nt_model* m) { return m->small + 0; }
 static int32_t* d_token(nt_model* m) { return m->small + 1; }
 static int32_t* d_next(nt_model* m) { return m->small + 2; }
 static float* d_margin(nt_model* m) { return reinterpret_cast<float*>(m->small + 3); }
+// Residual vector and device position of the token being enqueued: the step's
+// own, or one token of a speculative verification pass.
+static float* xres(nt_model* m) { return m->cur_x ? m->cur_x : m->x; }
+static int32_t* xpos(nt_model* m) { return m->cur_pos ? m->cur_pos : d_pos(m); }
 
 static cudaError_t dev_alloc(nt_model* m, void** p, size_t bytes) {
   if (m->dev_limit && m->dev_bytes + bytes > m->dev_limit) return cudaErrorMemoryAllocation;
@@ -356,14 +364,14 @@ static LayerGemvs layer_gemvs(nt_model* m, int l, uint8_t* base) {
   LayerGemvs g;
   // RMSNorm -> Q|K|V -> RoPE -> cache
   GemvArgs& a = g.qk;
-  a.x = m->x;
+  a.x = xres(m);
   a.norm = 1;
   a.eps = c.rms_eps;
   a.epi.y = m->q;
   a.epi.q_rows = qd;
   a.epi.k_rows = kd;
   a.epi.head_dim = hd;
-  a.epi.pos = d_pos(m);
+  a.epi.pos = xpos(m);
   a.epi.rope = m->rope;
   a.epi.k_cache = k_cache(m, l);
   a.epi.v_cache = v_cache(m, l);
@@ -384,27 +392,27 @@ static LayerGemvs layer_gemvs(nt_model* m, int l, uint8_t* base) {
   // O + residual
   g.o.seg[0] = view_at(ly, NT_ROLE_O, base);
   g.o.x = m->att;
-  g.o.epi.y = m->x;
+  g.o.epi.y = xres(m);
   // RMSNorm -> gate|up (rows interleaved) -> SwiGLU
   g.gu.seg[0] = view_at(ly, NT_ROLE_GATE, base);
   g.gu.seg[1] = view_at(ly, NT_ROLE_UP, base);
   g.gu.nseg = 2;
   g.gu.interleave = 1;
-  g.gu.x = m->x;
+  g.gu.x = xres(m);
   g.gu.norm = 1;
   g.gu.eps = c.rms_eps;
   g.gu.epi.y = m->u;
   // down + residual
   g.down.seg[0] = view_at(ly, NT_ROLE_DOWN, base);
   g.down.x = m->u;
-  g.down.epi.y = m->x;
+  g.down.epi.y = xres(m);
   return g;
 }
 
 static GemvArgs head_gemv(nt_model* m) {
   GemvArgs a;
   a.seg[0] = m->output.m;
-  a.x = m->x;
+  a.x = xres(m);
   a.norm = 1;
   a.eps = m->c.rms_eps;
   a.epi.y = m->logits;
@@ -440,7 +448,7 @@ static cudaError_t enqueue_layer(nt_model* m, int l, uint8_t* base, Launcher& L,
     const double by = 2.0 * 2.0 * double(c.n_kv_heads) * n_used * hd + 8.0 * qd;
     dim3 grid(unsigned(c.n_kv_heads), unsigned(m->n_chunks));
     const AttnArgs aa = attn_args(m, l);
-    e = L.run(NT_KC_ATTN, by, [&] { return launch_attn(hd, G, grid, s, aa, d_pos(m), pdl); });
+    e = L.run(NT_KC_ATTN, by, [&] { return launch_attn(hd, G, grid, s, aa, xpos(m), pdl); });
     if (e) return e;
   }
 
@@ -453,7 +461,9 @@ static cudaError_t enqueue_layer(nt_model* m, int l, uint8_t* base, Launcher& L,
   return cudaSuccess;
 }
 
-static cudaError_t enqueue_head(nt_model* m, Launcher& L, bool pdl) {
+// Output GEMV and greedy choice; next_out (device) receives the token instead
+// of the step's next-token word when given.
+static cudaError_t enqueue_head(nt_model* m, Launcher& L, bool pdl, int32_t* next_out = nullptr) {
   const nt_config& c = m->c;
   cudaStream_t s = L.s;
   const GemvArgs a = head_gemv(m);
@@ -461,8 +471,8 @@ static cudaError_t enqueue_head(nt_model* m, Launcher& L, bool pdl) {
   cudaError_t e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv(a, EPI_LOGITS, s, pdl, &m->out_grid); });
   if (e) return e;
   return L.run(NT_KC_OTHER, 0.0, [&] {
-    k_argmax<<<1, 256, 0, s>>>(m->top2, m->out_grid, d_pos(m), d_token(m), d_next(m), d_margin(m), m->hist,
-                               c.max_ctx, c.vocab);
+    k_argmax<<<1, 256, 0, s>>>(m->top2, m->out_grid, xpos(m), d_token(m), next_out ? next_out : d_next(m),
+                               d_margin(m), m->hist, c.max_ctx, c.vocab);
     return cudaGetLastError();
   });
 }
@@ -489,7 +499,7 @@ static cudaError_t enqueue_resident(nt_model* m, Launcher& L, bool pdl) {
 // streamed layers that do run.  With hs set (similarity step) every layer runs
 // and the residual is copied to hs[l] before layer l and to hs[n_layers] after
 // the last.
-static cudaError_t enqueue_streamed(nt_model* m, Launcher& L, float* hs) {
+static cudaError_t enqueue_streamed(nt_model* m, Launcher& L, float* hs, float* x_out = nullptr) {
   const int nl = m->c.n_layers, nr = m->n_resident;
   const size_t xbytes = size_t(m->c.hidden) * 4;
   cudaStream_t s = L.s, cs = m->copy_stream;
@@ -530,6 +540,7 @@ static cudaError_t enqueue_streamed(nt_model* m, Launcher& L, float* hs) {
       k++;
     }
   }
+  if (x_out && (e = cudaMemcpyAsync(x_out, m->x, xbytes, cudaMemcpyDeviceToDevice, s))) return e;
   if (hs) {
     if ((e = cudaMemcpyAsync(hs + size_t(nl) * m->c.hidden, m->x, xbytes, cudaMemcpyDeviceToDevice, s))) return e;
     if (nl > 0) {
@@ -862,7 +873,7 @@ nt_status nt_model_create(const nt_config* cfg, nt_model** out) {
   NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->hist), size_t(c.max_ctx) * 4), "alloc hist");
   NT_TRY(cudaMemsetAsync(m->small, 0, 16 * 4, m->stream), "cudaMemset");
   NT_TRY(cudaMemsetAsync(m->hist, 0xff, size_t(c.max_ctx) * 4, m->stream), "cudaMemset");
-  NT_TRY(cudaHostAlloc(reinterpret_cast<void**>(&m->h_io), 16 * 4, cudaHostAllocDefault), "cudaHostAlloc");
+  NT_TRY(cudaHostAlloc(reinterpret_cast<void**>(&m->h_io), 64 * 4, cudaHostAllocDefault), "cudaHostAlloc");
   // RoPE table in double: angle p * theta^(-2i/head_dim)
   {
     NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->rope), size_t(c.max_ctx) * (hd / 2) * 8), "alloc rope");
@@ -1013,6 +1024,146 @@ nt_status nt_set_layer_skip(nt_model* m, const uint8_t* mask) {
     m->skip.assign(size_t(m->c.n_layers), 0);
     for (int l = 0; l < m->c.n_layers; l++) m->skip[size_t(l)] = mask[l] ? 1 : 0;
   }
+  return NT_OK;
+}
+
+// Verification pass of a speculative cycle: layers [n_draft, n_layers) that the
+// skip mask keeps, layer by layer, each for the k draft tokens in order (token i
+// at position p + i from its residual after the draft layers); a host-tier layer
+// is copied once for all k.  Then the head for each token; token i's greedy
+// choice goes to sp_i[8 + i].  Returns the bytes copied from the host tier.
+static cudaError_t enqueue_verify(nt_model* m, Launcher& L, int n_draft, int k, double* h2d_bytes) {
+  const int nl = m->c.n_layers, nr = m->n_resident;
+  const size_t h = size_t(m->c.hidden);
+  cudaStream_t s = L.s, cs = m->copy_stream;
+  cudaError_t e;
+  std::vector<int> run, sl;
+  for (int l = n_draft; l < nl; l++)
+    if (!skipped(m, l)) {
+      run.push_back(l);
+      if (l >= nr) sl.push_back(l);
+    }
+  *h2d_bytes = 0;
+  auto issue_copy = [&](size_t j) -> cudaError_t {
+    const int l = sl[j], b = int(j & 1);
+    cudaError_t er = cudaStreamWaitEvent(cs, m->ev_compute_done[b], 0);
+    if (!er) er = cudaMemcpyAsync(m->staging[b], m->layers[size_t(l)].host, m->layers[size_t(l)].bytes,
+                                  cudaMemcpyHostToDevice, cs);
+    if (!er) er = cudaEventRecord(m->ev_copy_done[b], cs);
+    *h2d_bytes += double(m->layers[size_t(l)].bytes);
+    return er;
+  };
+  for (size_t j = 0; j < sl.size() && j < 2; j++)
+    if ((e = issue_copy(j))) return e;
+  size_t j = 0;
+  for (int l : run) {
+    const bool streamed = l >= nr;
+    const int b = int(j & 1);
+    uint8_t* base = streamed ? m->staging[b] : m->layers[size_t(l)].dev;
+    if (streamed && (e = cudaStreamWaitEvent(s, m->ev_copy_done[b], 0))) return e;
+    for (int i = 0; i < k && !e; i++) {
+      m->cur_x = m->sp_x + size_t(i) * h;
+      m->cur_pos = m->sp_i + i;
+      e = enqueue_layer(m, l, base, L, false);
+    }
+    m->cur_x = nullptr;
+    m->cur_pos = nullptr;
+    if (e) return e;
+    if (streamed) {
+      if ((e = cudaEventRecord(m->ev_compute_done[b], s))) return e;
+      if (j + 2 < sl.size() && (e = issue_copy(j + 2))) return e;
+      j++;
+    }
+  }
+  for (int i = 0; i < k && !e; i++) {
+    m->cur_x = m->sp_x + size_t(i) * h;
+    m->cur_pos = m->sp_i + i;
+    e = enqueue_head(m, L, false, m->sp_i + 8 + i);
+  }
+  m->cur_x = nullptr;
+  m->cur_pos = nullptr;
+  return e;
+}
+
+nt_status nt_speculative_step(nt_model* m, int32_t token, int32_t n_draft, int32_t k, int32_t* out_tokens,
+                              int32_t* n_out, int32_t* n_accepted) {
+  if (!m || !out_tokens || !n_out) return fail(NT_E_INVAL, "nt_speculative_step: NULL argument");
+  const nt_config& c = m->c;
+  if (token < 0 || token >= c.vocab) return fail(NT_E_INVAL, "nt_speculative_step: token outside [0, vocab)");
+  if (k < 1 || k > 8 || n_draft < 0 || n_draft > c.n_layers)
+    return fail(NT_E_INVAL, "nt_speculative_step: k outside [1, 8] or n_draft outside [0, n_layers]");
+  if (m->pos + k > c.max_ctx) return fail(NT_E_INVAL, "nt_speculative_step: the cycle would pass max_ctx");
+  const size_t h = size_t(c.hidden);
+  if (!m->sp_x) {
+    NT_CUDA(dev_alloc(m, reinterpret_cast<void**>(&m->sp_x), 8 * h * 4));
+    NT_CUDA(dev_alloc(m, reinterpret_cast<void**>(&m->sp_i), 32 * 4));
+  }
+  NT_CUDA(cudaStreamSynchronize(m->stream));
+  const int32_t p = m->pos;
+  int32_t* hs = m->h_io + 32;            // positions, full-model tokens, draft tokens
+  for (int i = 0; i < k; i++) hs[i] = p + i;
+  m->h_io[0] = p;
+  m->h_io[1] = token;
+  NT_CUDA(cudaMemcpyAsync(d_pos(m), m->h_io, 8, cudaMemcpyHostToDevice, m->stream));   // pos, token
+  NT_CUDA(cudaMemcpyAsync(m->sp_i, hs, 8 * 4, cudaMemcpyHostToDevice, m->stream));
+  NT_CUDA(cudaEventRecord(m->ev_step0, m->stream));
+
+  // draft: k greedy steps over the layers below n_draft (and the head); each
+  // token's residual after them is kept for the verification pass
+  const std::vector<uint8_t> user = m->skip;
+  std::vector<uint8_t> dmask(size_t(c.n_layers), 0);
+  for (int l = 0; l < c.n_layers; l++) dmask[size_t(l)] = (l >= n_draft || (!user.empty() && user[size_t(l)])) ? 1 : 0;
+  m->skip = dmask;
+  cudaError_t e = cudaSuccess;
+  double h2d = 0;
+  for (int i = 0; i < k && !e; i++) {
+    Launcher L;
+    L.s = m->stream;
+    e = enqueue_streamed(m, L, nullptr, m->sp_x + size_t(i) * h);
+    for (int l = 0; l < c.n_layers; l++)
+      if (m->ran[size_t(l)] && l >= m->n_resident) h2d += double(m->layers[size_t(l)].bytes);
+  }
+  m->skip = user;
+  if (e) return cuda_fail(e, "nt_speculative_step: draft");
+  // the draft's tokens d_1..d_k sit in the history at positions p..p+k-1
+  NT_CUDA(cudaMemcpyAsync(m->sp_i + 16, m->hist + p, size_t(k) * 4, cudaMemcpyDeviceToDevice, m->stream));
+  {
+    Launcher L;
+    L.s = m->stream;
+    double vb = 0;
+    e = enqueue_verify(m, L, n_draft, k, &vb);
+    if (e) return cuda_fail(e, "nt_speculative_step: verification");
+    h2d += vb;
+  }
+  NT_CUDA(cudaEventRecord(m->ev_step1, m->stream));
+  NT_CUDA(cudaMemcpyAsync(hs + 8, m->sp_i + 8, 16 * 4, cudaMemcpyDeviceToHost, m->stream));
+  nt_status st = wait_event(m->ev_step1, "nt_speculative_step");
+  if (st) return st;
+  NT_CUDA(cudaStreamSynchronize(m->stream));
+  const int32_t* y = hs + 8;
+  const int32_t* d = hs + 16;
+  int j = 0;
+  while (j < k && y[j] == d[j]) j++;
+  const int n = j < k ? j + 1 : k;
+  for (int i = 0; i < j; i++) out_tokens[i] = d[i];
+  if (j < k) out_tokens[j] = y[j];
+  // the history at p..p+n-1 already holds the full model's choices; position and
+  // next input move to the end of the emitted run
+  m->pos = p + n;
+  m->h_io[0] = m->pos;
+  m->h_io[1] = out_tokens[n - 1];
+  NT_CUDA(cudaMemcpyAsync(d_pos(m), m->h_io, 8, cudaMemcpyHostToDevice, m->stream));
+  NT_CUDA(cudaStreamSynchronize(m->stream));
+  float ms = 0.f;
+  NT_CUDA(cudaEventElapsedTime(&ms, m->ev_step0, m->ev_step1));
+  m->stats.last_step_ms = ms;
+  m->stats.steps += n;
+  m->stats.h2d_bytes = h2d;
+  m->stats.h2d_ms = 0;
+  m->stats.compute_ms = ms;
+  m->stats.overlap = 0;
+  *n_out = n;
+  if (n_accepted) *n_accepted = j;
   return NT_OK;
 }
 

@@ -79,6 +79,7 @@ _SIGS = {
     "nt_auto_residency": (C.c_int, [_vp, _i64, C.POINTER(_i32)]),
     "nt_layer_similarity": (C.c_int, [_vp, _i32, C.POINTER(_i32), C.POINTER(C.c_double)]),
     "nt_set_layer_skip": (C.c_int, [_vp, C.POINTER(C.c_uint8)]),
+    "nt_speculative_step": (C.c_int, [_vp, _i32, _i32, _i32, C.POINTER(_i32), C.POINTER(_i32), C.POINTER(_i32)]),
     "nt_plan_layer_skip": (C.c_int, [C.POINTER(C.c_double), _i32, C.c_double, _i32, C.POINTER(C.c_uint8),
                                      C.POINTER(_i32)]),
     "nt_model_tensor": (C.c_int, [_vp, _i32, _i32, C.POINTER(C.c_void_p)]),
@@ -262,6 +263,14 @@ def nt_set_layer_skip(m: int, mask) -> None:
     a = np.ascontiguousarray(np.asarray(mask).astype(np.uint8))
     assert a.size == stats_layers(m)
     _check(lib().nt_set_layer_skip(m, a.ctypes.data_as(C.POINTER(C.c_uint8))), "nt_set_layer_skip")
+
+
+def nt_speculative_step(m: int, token: int, n_draft: int, k: int) -> tuple[list[int], int]:
+    """One self-speculative cycle: (emitted tokens, accepted draft tokens)."""
+    out = (_i32 * 8)()
+    n, j = _i32(), _i32()
+    _check(lib().nt_speculative_step(m, token, n_draft, k, out, C.byref(n), C.byref(j)), "nt_speculative_step")
+    return [out[i] for i in range(n.value)], j.value
 
 
 def nt_plan_layer_skip(cos, threshold: float, max_skip: int = 0) -> np.ndarray:

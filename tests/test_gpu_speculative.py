@@ -1,0 +1,114 @@
+"""GPU: self-speculative decoding (resident layers as the draft) against plain
+greedy decoding on the device and against the oracle's cycle reference."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from gpu_util import ensure_built, torch_cuda
+
+pytestmark = pytest.mark.gpu
+MARGIN = 1e-2
+SPEC = dict(n_layers=3, hidden=512, n_heads=8, n_kv_heads=2, head_dim=64, ffn_dim=1536, vocab=512, max_ctx=96)
+
+
+@pytest.fixture(scope="module")
+def nt():
+    torch_cuda()
+    ensure_built()
+    from quantized_decode_dequant_gb300 import nt as _nt
+    return _nt
+
+
+def _greedy(nt, cfg, token, n, prefill):
+    m = nt.nt_model_create(cfg)
+    try:
+        nt.nt_kv_prefill(m, *prefill)
+        out, t = [], token
+        for _ in range(n):
+            t = nt.nt_decode_step(m, t)
+            out.append(t)
+        return out
+    finally:
+        nt.nt_model_destroy(m)
+
+
+def _cycles(nt, m, token, n_draft, k, n_cycles):
+    out, t = [], token
+    for _ in range(n_cycles):
+        emitted, j = nt.nt_speculative_step(m, t, n_draft, k)
+        out.append((emitted, j))
+        t = emitted[-1]
+    return out
+
+
+@pytest.mark.parametrize("n_draft,k,resident", [(3, 4, 3), (1, 4, 3), (1, 3, 1), (0, 2, 3), (2, 8, 2)])
+def test_speculative_stream_equals_greedy_and_the_oracle(nt, n_draft, k, resident):
+    cfg = nt.make_config(**SPEC, seed=12)
+    prefill = (20, 2)
+    m = nt.nt_model_create(cfg)
+    try:
+        nt.nt_kv_prefill(m, *prefill)
+        if resident < SPEC["n_layers"]:
+            nt.nt_stream_layers(m, resident, 2)
+        cycles = _cycles(nt, m, 9, n_draft, k, 6)
+        stream = [t for e, _ in cycles for t in e]
+        assert nt.nt_get_stats(m).pos == prefill[0] + len(stream)
+        for e, j in cycles:
+            assert 0 <= j <= k and len(e) == (j + 1 if j < k else k)
+        if n_draft == SPEC["n_layers"]:
+            assert all(j == k for _, j in cycles)
+        # bit-exact property: the emitted stream is the device's own greedy stream
+        assert stream == _greedy(nt, cfg, 9, len(stream), prefill)
+        # the history holds the emitted tokens, and plain decoding continues from the cycle's end
+        np.testing.assert_array_equal(nt.nt_get_tokens(m, prefill[0], len(stream)), stream)
+        nxt = nt.nt_decode_step(m, stream[-1])
+        assert nxt == _greedy(nt, cfg, 9, len(stream) + 1, prefill)[-1]
+    finally:
+        nt.nt_model_destroy(m)
+    # the oracle's cycles (exact while its greedy margins stay above the near-tie bar)
+    ospec = oracle.ModelSpec(**SPEC, seed=12)
+    want = oracle.speculative_cycles(ospec, n_draft, k, 9, 6, prefill=prefill, nthreads=os.cpu_count() or 8)
+    om = oracle.Model(ospec, nthreads=os.cpu_count() or 8)
+    om.kv_prefill(*prefill)
+    t, margins = 9, []
+    for _ in range(len(stream)):
+        _, t, mg = om.decode_step(t)
+        margins.append(mg)
+    om.close()
+    if min(margins) > MARGIN:
+        assert cycles == [(list(e), j) for e, j in want]
+
+
+def test_streamed_verification_copies_each_layer_once_per_cycle(nt):
+    cfg = nt.make_config(**dict(SPEC, n_layers=4), seed=3)
+    m = nt.nt_model_create(cfg)
+    try:
+        nt.nt_stream_layers(m, 1, 2)
+        t = 5
+        nt.nt_decode_step(m, t)
+        per_step = nt.nt_get_stats(m).h2d_bytes          # three streamed layers
+        nt.nt_kv_reset(m)
+        for k in (1, 4, 8):
+            e, _ = nt.nt_speculative_step(m, t, 1, k)
+            assert nt.nt_get_stats(m).h2d_bytes == per_step   # draft layers are resident: copies only in the verification
+            t = e[-1]
+    finally:
+        nt.nt_model_destroy(m)
+
+
+def test_speculative_argument_checks(nt):
+    m = nt.nt_model_create(nt.make_config(**dict(SPEC, max_ctx=8), seed=1))
+    try:
+        for args in [(0, 1, 0), (0, 1, 9), (0, 4, 2), (SPEC["vocab"], 1, 2), (0, -1, 2)]:
+            with pytest.raises(nt.NtError) as ei:
+                nt.nt_speculative_step(m, *args)
+            assert ei.value.status == nt.NT_E_INVAL
+        nt.nt_kv_prefill(m, 6, 2)
+        with pytest.raises(nt.NtError):
+            nt.nt_speculative_step(m, 0, 1, 3)      # 6 + 3 > max_ctx
+        e, _ = nt.nt_speculative_step(m, 0, 1, 2)
+        assert 1 <= len(e) <= 2
+    finally:
+        nt.nt_model_destroy(m)
