@@ -152,3 +152,23 @@ def test_streamed_skip_equals_resident_skip_and_copies_fewer_bytes(nt, W):
     finally:
         for m in (res, stm, full):
             nt.nt_model_destroy(m)
+
+
+def test_skipping_every_layer_is_the_zero_layer_model(nt):
+    every = nt.nt_model_create(nt.make_config(**dict(SPEC, n_layers=2), seed=5))
+    none = nt.nt_model_create(nt.make_config(**dict(SPEC, n_layers=0), seed=5))
+    try:
+        nt.nt_set_layer_skip(every, [1, 1])
+        le, ln = np.empty(SPEC["vocab"], np.float32), np.empty(SPEC["vocab"], np.float32)
+        t = 3
+        for _ in range(3):
+            ne, nn = nt.nt_decode_step(every, t, le), nt.nt_decode_step(none, t, ln)
+            np.testing.assert_array_equal(_bits(le), _bits(ln))
+            assert ne == nn
+            t = ne
+        # a speculative cycle whose draft is the whole (empty) remaining model accepts everything
+        e, j = nt.nt_speculative_step(every, t, 2, 3)
+        assert j == 3 and len(e) == 3
+    finally:
+        nt.nt_model_destroy(every)
+        nt.nt_model_destroy(none)
