@@ -1124,21 +1124,29 @@ nt_status nt_speculative_step(nt_model* m, int32_t token, int32_t n_draft, int32
       if (m->ran[size_t(l)] && l >= m->n_resident) h2d += double(m->layers[size_t(l)].bytes);
   }
   m->skip = user;
-  if (e) return cuda_fail(e, "nt_speculative_step: draft");
+  // on failure the draft may have moved the device position: put it back
+  auto resync = [&](nt_status st) {
+    m->h_io[0] = m->pos;
+    cudaMemcpyAsync(d_pos(m), m->h_io, 4, cudaMemcpyHostToDevice, m->stream);
+    cudaStreamSynchronize(m->stream);
+    return st;
+  };
+  if (e) return resync(cuda_fail(e, "nt_speculative_step: draft"));
   // the draft's tokens d_1..d_k sit in the history at positions p..p+k-1
-  NT_CUDA(cudaMemcpyAsync(m->sp_i + 16, m->hist + p, size_t(k) * 4, cudaMemcpyDeviceToDevice, m->stream));
+  e = cudaMemcpyAsync(m->sp_i + 16, m->hist + p, size_t(k) * 4, cudaMemcpyDeviceToDevice, m->stream);
+  if (e) return resync(cuda_fail(e, "nt_speculative_step: draft tokens"));
   {
     Launcher L;
     L.s = m->stream;
     double vb = 0;
     e = enqueue_verify(m, L, n_draft, k, &vb);
-    if (e) return cuda_fail(e, "nt_speculative_step: verification");
+    if (e) return resync(cuda_fail(e, "nt_speculative_step: verification"));
     h2d += vb;
   }
   NT_CUDA(cudaEventRecord(m->ev_step1, m->stream));
   NT_CUDA(cudaMemcpyAsync(hs + 8, m->sp_i + 8, 16 * 4, cudaMemcpyDeviceToHost, m->stream));
   nt_status st = wait_event(m->ev_step1, "nt_speculative_step");
-  if (st) return st;
+  if (st) return resync(st);
   NT_CUDA(cudaStreamSynchronize(m->stream));
   const int32_t* y = hs + 8;
   const int32_t* d = hs + 16;
