@@ -229,6 +229,38 @@ def test_llama70b_q4_k_m_teacher_forced(nt, W):
         nt.nt_model_destroy(m)
 
 
+@pytest.mark.slow
+@pytest.mark.skipif(os.environ.get("NT_RUN_SLOW") != "1", reason="70B oracle takes minutes per step; NT_RUN_SLOW=1")
+def test_llama70b_q6_k_streamed_teacher_forced_and_equal_to_resident(nt, W):
+    """70B all-Q6_K, 26 layers resident and 54 streamed: against the oracle, and bit for bit
+    against the same model held entirely in device memory."""
+    spec = W.LLAMA_70B_Q6_K
+    cfg = nt.make_config(**spec, seed=W.SEED_WEIGHTS)
+    stm, res = nt.nt_model_create(cfg), nt.nt_model_create(cfg)
+    try:
+        nt.nt_stream_layers(stm, W.LLAMA_70B_Q6_K_RESIDENT, 2)
+        for m in (stm, res):
+            nt.nt_kv_prefill(m, W.LLAMA_70B_Q6_K_CTX, W.SEED_KV)
+        om = oracle.Model(oracle.ModelSpec(**spec, seed=W.SEED_WEIGHTS), lazy=True, nthreads=os.cpu_count() or 8)
+        om.kv_prefill(W.LLAMA_70B_Q6_K_CTX, W.SEED_KV)
+        gl, rl = np.empty(spec["vocab"], np.float32), np.empty(spec["vocab"], np.float32)
+        tok = oracle.token(W.SEED_PROMPT, oracle.UID_TOKENS, 0, spec["vocab"])
+        for i in range(int(os.environ.get("NT_70B_STEPS", "2"))):
+            gnx = nt.nt_decode_step(stm, tok, gl)
+            rnx = nt.nt_decode_step(res, tok, rl)
+            np.testing.assert_array_equal(gl.view(np.uint32), rl.view(np.uint32))
+            assert gnx == rnx
+            assert nt.nt_get_stats(stm).h2d_bytes > 0
+            ol, onx, omg = om.decode_step(tok)
+            e = _check_step(gl, gnx, ol, onx, omg, i)
+            print(f"70B Q6_K streamed step {i}: max-abs {e[0]:.3e} rel-L2 {e[1]:.3e} margin {omg:.3e}")
+            tok = gnx
+        om.close()
+    finally:
+        nt.nt_model_destroy(stm)
+        nt.nt_model_destroy(res)
+
+
 def test_auto_residency_places_layers_and_decodes_the_same(nt, W):
     """nt_auto_residency keeps a model that fits resident; with a margin that
     leaves room for only a few layers it streams the rest, bit for bit the same."""
