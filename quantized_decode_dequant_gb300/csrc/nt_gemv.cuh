@@ -167,12 +167,8 @@ template <> struct Fmt<NT_Q4_K> {
     acc = nib8<0>(p.c.y, xs[2], xs[3], acc);
     acc = nib8<0>(p.c.z, xs[4], xs[5], acc);
     acc = nib8<0>(p.c.w, xs[6], xs[7], acc);
-    // 6-bit fields: sc_j at bit 6j, m_j at bit 6(8+j) of the 96-bit stream (meta.y, meta.z, meta.w)
-    const uint64_t lo = uint64_t(p.meta.y) | (uint64_t(p.meta.z) << 32);
-    const uint32_t sc = uint32_t(lo >> (6 * p.j)) & 63u;
-    const int mb = 48 + 6 * p.j;
-    const uint32_t mm = mb >= 64 ? (p.meta.w >> (mb - 64)) & 63u
-                                 : uint32_t((lo >> mb) | (uint64_t(p.meta.w) << (64 - mb))) & 63u;
+    uint32_t sc, mm;
+    kquant_scale_min(p.meta, p.j, sc, mm);
     const float a = h2f_bits(p.meta.x & 0xFFFFu) * float(sc);
     const float b = h2f_bits(p.meta.x >> 16) * float(mm);
     return a * (acc.x + acc.y) - b * xsum;
@@ -217,11 +213,8 @@ template <> struct Fmt<NT_Q5_K> {
     acc = bytes4(((p.c.z >> 4) & L) | ((H >> 1) & M), xs[5], acc);
     acc = bytes4((p.c.w & L) | ((H >> 2) & M), xs[6], acc);
     acc = bytes4(((p.c.w >> 4) & L) | ((H >> 3) & M), xs[7], acc);
-    const uint64_t lo = uint64_t(p.meta.y) | (uint64_t(p.meta.z) << 32);
-    const uint32_t sc = uint32_t(lo >> (6 * p.j)) & 63u;
-    const int mb = 48 + 6 * p.j;
-    const uint32_t mm = mb >= 64 ? (p.meta.w >> (mb - 64)) & 63u
-                                 : uint32_t((lo >> mb) | (uint64_t(p.meta.w) << (64 - mb))) & 63u;
+    uint32_t sc, mm;
+    kquant_scale_min(p.meta, p.j, sc, mm);
     const float a = h2f_bits(p.meta.x & 0xFFFFu) * float(sc);
     const float b = h2f_bits(p.meta.x >> 16) * float(mm);
     return a * (acc.x + acc.y) - b * xsum;

@@ -196,13 +196,8 @@ template <> struct Pipe<NT_Q4_0> {
 // unit `lane` of the tile is sub-block j = lane % 8 of super-block lane / 8.
 template <int XS>
 __device__ __forceinline__ float kquant_unit(const uint4 meta, int lane, const int (&c)[8], const XBlock& x) {
-  const int j = lane & 7;
-  // 6-bit fields: sc_j at bit 6j, m_j at bit 6(8+j) of the 96-bit stream (meta.y, meta.z, meta.w)
-  const uint64_t lo = uint64_t(meta.y) | (uint64_t(meta.z) << 32);
-  const uint32_t sc = uint32_t(lo >> (6 * j)) & 63u;
-  const int mb = 48 + 6 * j;
-  const uint32_t mm = mb >= 64 ? (meta.w >> (mb - 64)) & 63u
-                               : uint32_t((lo >> mb) | (uint64_t(meta.w) << (64 - mb))) & 63u;
+  uint32_t sc, mm;
+  kquant_scale_min(meta, lane & 7, sc, mm);
   const float a = __fmul_rn(h2f_bits(meta.x & 0xFFFFu), float(sc));
   const float b = __fmul_rn(h2f_bits(meta.x >> 16), float(mm));
   return __fmul_rn(x.sx, __fmaf_rn(a, xacc_f(idot<0, 8, XS>(c, x)), -__fmul_rn(b, __int2float_rn(x.t0 + x.t1))));

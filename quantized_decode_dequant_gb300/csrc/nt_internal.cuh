@@ -50,7 +50,10 @@ inline bool supported_weight_type(int t) { return block_elems(t) != 0; }
 //   Q4_0: q  = 4-bit codes, element k of a row at byte k/2 (low nibble for even k)
 //                                                d = f16 per 32 elements
 //   Q4_K: q  = 4-bit codes as Q4_0               meta = 16 B per 256 elements:
-//         f16 d | f16 dmin | 12 B of 6-bit sc_0..7, m_0..7 (LSB first)
+//         f16 d | f16 dmin | 8 B: byte j = sc_j | (m_j & 3) << 6 | 4 B: nibble j =
+//         m_j >> 2 (the canonical header packs the same sixteen 6-bit fields
+//         LSB-first; this arrangement gives each lane its sub-block's pair with a
+//         byte permute and three logic ops)
 //   Q6_K: q  = low 4 bits as Q4_0; qh = high 2 bits, 8 bytes per 32 elements
 //         as two little-endian words G_0 (elements 0..15) and G_1 (16..31);
 //         within G_p, element 8w+i of the unit (w = 2p + s, i = 2j + o) sits at
@@ -60,7 +63,7 @@ inline bool supported_weight_type(int t) { return block_elems(t) != 0; }
 //         element 8w+2i+o of the unit (w < 4, i < 4, o < 2) has its fifth bit at
 //         bit 8i + 2w + o, i.e. byte i of H serves byte i of the eight code words
 //         v = 2w+o that the low/high nibbles of the unit's four words form;
-//         meta = 16 B per 256 elements as Q4_K.
+//         meta = 16 B per 256 elements in Q4_K's device arrangement.
 struct QMat {
   int32_t type = 0;
   int64_t rows = 0, cols = 0;
@@ -180,15 +183,17 @@ __device__ __forceinline__ int q5_hi(const uint8_t* qh, int64_t e) {
   return int(h >> q5_hi_bit(k)) & 1;
 }
 
-// 6-bit field f (sc_j for f = j, m_j for f = 8 + j) at bits [6f, 6f+6) of the
-// 12 bytes after a K-quant super-block's d and dmin
-__device__ __forceinline__ int kquant_field(const uint8_t* meta, int f) {
-  int v = 0;
-  for (int b = 0; b < 6; b++) {
-    const int bit = 6 * f + b;
-    v |= ((meta[4 + (bit >> 3)] >> (bit & 7)) & 1) << b;
-  }
-  return v;
+// Scale sc_j and min m_j of sub-block j from a K-quant super-block header in
+// the device arrangement (words x: d, dmin; y, z: bytes sc_j | (m_j & 3) << 6;
+// w: nibbles m_j >> 2).
+__device__ __forceinline__ void kquant_scale_min(const uint4 meta, int j, uint32_t& sc, uint32_t& m) {
+  const uint32_t b = __byte_perm(meta.y, meta.z, uint32_t(j));   // byte j of y:z in the low byte
+  sc = b & 63u;
+  m = ((b >> 6) & 3u) | (((meta.w >> (4 * j)) & 15u) << 2);
+}
+__host__ __device__ __forceinline__ void kquant_scale_min_bytes(const uint8_t* meta, int j, int& sc, int& m) {
+  sc = meta[4 + j] & 63;
+  m = (meta[4 + j] >> 6) | (((meta[12 + (j >> 1)] >> (4 * (j & 1))) & 15) << 2);
 }
 
 __device__ __forceinline__ float dequant_elem(const QMat& m, int64_t e) {
@@ -201,27 +206,20 @@ __device__ __forceinline__ float dequant_elem(const QMat& m, int64_t e) {
       const uint8_t* meta = m.meta + (e / 256) * 16;
       const float d = __half2float(__ushort_as_half(uint16_t(meta[0] | (meta[1] << 8))));
       const float dmin = __half2float(__ushort_as_half(uint16_t(meta[2] | (meta[3] << 8))));
-      const int j = int((e % 256) / 32);
-      // 6-bit field f at bits [6f, 6f+6) of the 12 bytes meta[4..15]
-      auto field = [&](int f) -> int {
-        int v = 0;
-        for (int b = 0; b < 6; b++) {
-          const int bit = 6 * f + b;
-          v |= ((meta[4 + (bit >> 3)] >> (bit & 7)) & 1) << b;
-        }
-        return v;
-      };
-      const float a = __fmul_rn(d, float(field(j)));
-      const float b = __fmul_rn(dmin, float(field(8 + j)));
+      int sc, mm;
+      kquant_scale_min_bytes(meta, int((e % 256) / 32), sc, mm);
+      const float a = __fmul_rn(d, float(sc));
+      const float b = __fmul_rn(dmin, float(mm));
       return __fmaf_rn(a, float(nib_at(m.q, e)), -b);
     }
     case NT_Q5_K: {
       const uint8_t* meta = m.meta + (e / 256) * 16;
       const float d = __half2float(__ushort_as_half(uint16_t(meta[0] | (meta[1] << 8))));
       const float dmin = __half2float(__ushort_as_half(uint16_t(meta[2] | (meta[3] << 8))));
-      const int j = int((e % 256) / 32);
-      const float a = __fmul_rn(d, float(kquant_field(meta, j)));
-      const float b = __fmul_rn(dmin, float(kquant_field(meta, 8 + j)));
+      int sc, mm;
+      kquant_scale_min_bytes(meta, int((e % 256) / 32), sc, mm);
+      const float a = __fmul_rn(d, float(sc));
+      const float b = __fmul_rn(dmin, float(mm));
       return __fmaf_rn(a, float(nib_at(m.q, e) | (q5_hi(m.qh, e) << 4)), -b);
     }
     case NT_Q6_K: {

@@ -154,25 +154,21 @@ __global__ void __launch_bounds__(256) k_generate(QMat m, uint64_t seed, uint32_
       hb |= __shfl_xor_sync(0xffffffffu, hb, 2);
       if (wi == 0) *reinterpret_cast<uint32_t*>(m.qh + ebase / 8) = hb;
     }
-    // 96-bit field stream: field f (sc_j for f = j, m_j for f = 8 + j) at bits [6f, 6f+6)
-    uint64_t lo64 = 0, hi64 = 0;
+    // device header: bytes sc_j | (m_j & 3) << 6 (j = 0..7), then nibbles m_j >> 2
+    uint32_t yz[2] = {0u, 0u}, wn = 0u;
 #pragma unroll
     for (int j = 0; j < 8; j++) {
-      int scj = __shfl_sync(0xffffffffu, sc, 4 * j);
-      int mj = __shfl_sync(0xffffffffu, mm, 4 * j);
-      int f0 = j, f1 = 8 + j;
-      // a field never straddles bit 64 except f = 10 (bits 60..65)
-      if (6 * f0 + 6 <= 64) lo64 |= uint64_t(scj) << (6 * f0);
-      if (6 * f1 + 6 <= 64) lo64 |= uint64_t(mj) << (6 * f1);
-      else if (6 * f1 >= 64) hi64 |= uint64_t(mj) << (6 * f1 - 64);
-      else { lo64 |= uint64_t(mj) << (6 * f1); hi64 |= uint64_t(mj) >> (64 - 6 * f1); }
+      const uint32_t scj = uint32_t(__shfl_sync(0xffffffffu, sc, 4 * j));
+      const uint32_t mj = uint32_t(__shfl_sync(0xffffffffu, mm, 4 * j));
+      yz[j >> 2] |= (scj | ((mj & 3u) << 6)) << (8 * (j & 3));
+      wn |= (mj >> 2) << (4 * j);
     }
     if (lane == 0) {
       uint4 meta;
       meta.x = uint32_t(__half_as_ushort(dh)) | (uint32_t(__half_as_ushort(mh)) << 16);
-      meta.y = uint32_t(lo64);
-      meta.z = uint32_t(lo64 >> 32);
-      meta.w = uint32_t(hi64);
+      meta.y = yz[0];
+      meta.z = yz[1];
+      meta.w = wn;
       *reinterpret_cast<uint4*>(m.meta + (ebase / 256) * 16) = meta;
     }
   } else {  // NT_Q6_K
@@ -240,6 +236,22 @@ cudaError_t launch_dequant(const QMat& m, int64_t row0, int64_t nrows, float* ou
 
 // ---------------------------------------------------------------- export --
 
+// K-quant super-block header, device arrangement -> canonical bytes: d, dmin,
+// then the sixteen 6-bit fields sc_0..7, m_0..7 packed least-significant bit first.
+static void kquant_header_canonical(const uint8_t* dev, uint8_t* out) {
+  memcpy(out, dev, 4);
+  memset(out + 4, 0, 12);
+  for (int j = 0; j < 8; j++) {
+    int sc, m;
+    kquant_scale_min_bytes(dev, j, sc, m);
+    for (int f = 0; f < 2; f++) {
+      const int v = f ? m : sc, base = 6 * (j + 8 * f);
+      for (int bit = 0; bit < 6; bit++)
+        if ((v >> bit) & 1) out[4 + ((base + bit) >> 3)] |= uint8_t(1u << ((base + bit) & 7));
+    }
+  }
+}
+
 // Interleaves the device streams of rows [row0, row0+nrows) into canonical
 // block bytes on the host.
 static nt_status export_rows(const nt_qtensor* t, int64_t row0, int64_t nrows, uint8_t* dst) {
@@ -275,11 +287,11 @@ static nt_status export_rows(const nt_qtensor* t, int64_t row0, int64_t nrows, u
         memcpy(out + 2, &q[e / 2], 16);
         break;
       case NT_Q4_K:
-        memcpy(out, &meta[b * 16], 16);
+        kquant_header_canonical(&meta[b * 16], out);
         memcpy(out + 16, &q[e / 2], 128);
         break;
       case NT_Q5_K: {
-        memcpy(out, &meta[b * 16], 16);
+        kquant_header_canonical(&meta[b * 16], out);
         // canonical fifth bits: element k of the block at byte k/8, bit k%8
         uint8_t* cqh = out + 16;
         memset(cqh, 0, 32);
