@@ -49,7 +49,7 @@ struct AttnArgs {
 // distinct banks), q of the G heads, the G x C scores, the P V partial sums of
 // the kAttnThreads/hd position slices, a flag.
 __host__ __device__ constexpr size_t attn_item_smem(int hd, int G, int C) {
-  return size_t(2 * C * (hd + 8)) * 2 + size_t(G * hd + G * C) * 4 + size_t(kAttnThreads / hd) * G * hd * 4 + 16;
+  return size_t(2 * C * (hd + 8)) * 2 + size_t(G * hd + G * C) * 4 + size_t(2 * kAttnThreads / hd) * G * hd * 4 + 16;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -149,14 +149,15 @@ __device__ __forceinline__ void attn_combine_head(const AttnArgs& a, int j, int 
 // positions attended (pos + 1; the current one is already stored), used =
 // ceil(n / C) items of kv head g exist.  Scores: threads 2c and 2c+1 hold the
 // two halves of key c in registers and score it against every head (q read as
-// broadcast float4s).  P V: the CTA's
-// threads are kAttnThreads/HD position slices x HD dimensions; slice s sums its
-// contiguous share of the chunk for all G heads, and the slices are added in
-// order.  Every thread of the CTA must call it.
+// broadcast float4s; even and odd dimensions in the two lanes of packed f32x2
+// FMAs, added at the end).  P V: the CTA's threads are 2*kAttnThreads/HD
+// position slices x HD/2 dimension pairs (packed f32x2 FMAs on a pair); slice s
+// sums its contiguous share of the chunk for all G heads, and the slices are
+// added in order.  Every thread of the CTA must call it.
 template <int HD, int G, int C>
 __device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, int n, int used, uint8_t* sm,
                                           bool prefetched) {
-  constexpr int KP = HD + 8, NS = kAttnThreads / HD;
+  constexpr int KP = HD + 8, NS = 2 * kAttnThreads / HD;
   __half* Ks = reinterpret_cast<__half*>(sm);
   __half* Vs = Ks + C * KP;
   float* qs = reinterpret_cast<float*>(Vs + C * KP);
@@ -193,15 +194,14 @@ __device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, i
 #pragma unroll
     for (int h = 0; h < G; h++) {
       const float4* qh = reinterpret_cast<const float4*>(qs + h * HD + part * DPT);
-      float acc = 0.f;
+      float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int i = 0; i < DPT / 4; i++) {
         const float4 qv = qh[i];
-        acc = __fmaf_rn(qv.x, kf[2 * i].x, acc);
-        acc = __fmaf_rn(qv.y, kf[2 * i].y, acc);
-        acc = __fmaf_rn(qv.z, kf[2 * i + 1].x, acc);
-        acc = __fmaf_rn(qv.w, kf[2 * i + 1].y, acc);
+        acc2 = __ffma2_rn(make_float2(qv.x, qv.y), kf[2 * i], acc2);
+        acc2 = __ffma2_rn(make_float2(qv.z, qv.w), kf[2 * i + 1], acc2);
       }
+      float acc = __fadd_rn(acc2.x, acc2.y);
 #pragma unroll
       for (int o = 1; o < TPK; o <<= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
       if (part == 0) S[h * C + c] = c < cnt ? __fmul_rn(acc, a.scale) : -INFINITY;
@@ -227,26 +227,31 @@ __device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, i
   }
   __syncthreads();
 
-  // ---- P V: slice s of the positions, dimension d -------------------------------
+  // ---- P V: slice s of the positions, dimension pair (2dp, 2dp+1) -------------------
   {
-    const int d = t % HD, s = t / HD;
+    const int dp = t % (HD / 2), s = t / (HD / 2);
     const int span = C / NS;                   // positions per slice (a multiple of 4)
     const int c_lo = s * span, c_hi = min(c_lo + span, cnt);
-    float acc[G];
+    float2 acc[G];
 #pragma unroll
-    for (int h = 0; h < G; h++) acc[h] = 0.f;
+    for (int h = 0; h < G; h++) acc[h] = make_float2(0.f, 0.f);
     for (int c = c_lo; c < c_hi; c += 4) {     // weights past cnt are 0; rows past cnt are finite smem
-      float v[4];
+      float2 v[4];
 #pragma unroll
-      for (int j = 0; j < 4; j++) v[j] = c + j < cnt ? __half2float(Vs[(c + j) * KP + d]) : 0.f;
+      for (int j = 0; j < 4; j++)
+        v[j] = c + j < cnt ? __half22float2(*reinterpret_cast<const __half2*>(Vs + (c + j) * KP + 2 * dp))
+                           : make_float2(0.f, 0.f);
 #pragma unroll
       for (int h = 0; h < G; h++) {
         const float4 w = *reinterpret_cast<const float4*>(S + h * C + c);
-        acc[h] = __fmaf_rn(w.x, v[0], __fmaf_rn(w.y, v[1], __fmaf_rn(w.z, v[2], __fmaf_rn(w.w, v[3], acc[h]))));
+        acc[h] = __ffma2_rn(make_float2(w.w, w.w), v[3], acc[h]);
+        acc[h] = __ffma2_rn(make_float2(w.z, w.z), v[2], acc[h]);
+        acc[h] = __ffma2_rn(make_float2(w.y, w.y), v[1], acc[h]);
+        acc[h] = __ffma2_rn(make_float2(w.x, w.x), v[0], acc[h]);
       }
     }
 #pragma unroll
-    for (int h = 0; h < G; h++) P[(s * G + h) * HD + d] = acc[h];
+    for (int h = 0; h < G; h++) *reinterpret_cast<float2*>(P + (s * G + h) * HD + 2 * dp) = acc[h];
   }
   __syncthreads();
   for (int i = t; i < G * HD; i += kAttnThreads) {
