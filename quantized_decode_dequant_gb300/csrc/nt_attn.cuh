@@ -194,14 +194,16 @@ __device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, i
 #pragma unroll
     for (int h = 0; h < G; h++) {
       const float4* qh = reinterpret_cast<const float4*>(qs + h * HD + part * DPT);
-      float2 acc2 = make_float2(0.f, 0.f);
+      float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);   // two chains: dimensions 8i..8i+3, 8i+4..8i+7
 #pragma unroll
-      for (int i = 0; i < DPT / 4; i++) {
-        const float4 qv = qh[i];
-        acc2 = __ffma2_rn(make_float2(qv.x, qv.y), kf[2 * i], acc2);
-        acc2 = __ffma2_rn(make_float2(qv.z, qv.w), kf[2 * i + 1], acc2);
+      for (int i = 0; i < DPT / 4; i += 2) {
+        const float4 qv = qh[i], qw = qh[i + 1];
+        a0 = __ffma2_rn(make_float2(qv.x, qv.y), kf[2 * i], a0);
+        a1 = __ffma2_rn(make_float2(qw.x, qw.y), kf[2 * i + 2], a1);
+        a0 = __ffma2_rn(make_float2(qv.z, qv.w), kf[2 * i + 1], a0);
+        a1 = __ffma2_rn(make_float2(qw.z, qw.w), kf[2 * i + 3], a1);
       }
-      float acc = __fadd_rn(acc2.x, acc2.y);
+      float acc = __fadd_rn(__fadd_rn(a0.x, a0.y), __fadd_rn(a1.x, a1.y));
 #pragma unroll
       for (int o = 1; o < TPK; o <<= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
       if (part == 0) S[h * C + c] = c < cnt ? __fmul_rn(acc, a.scale) : -INFINITY;
