@@ -213,7 +213,29 @@ def cpu_baseline(wl, min_seconds: float = 10.0, max_steps: int = 64, threads: in
     return {"value": 1.0 / sec_per_tok, "unit": "tok/s", "cores": threads, "kind": "oracle",
             "sample": (f"{sample_steps} oracle decode steps of the same architecture truncated to 1 layer "
                        f"(ctx {wl['ctx']}), {dt:.2f} s/step, scaled to the full model by weight+KV bytes "
-                       f"({full / part:.1f}x)")}
+                       f"({full / part:.1f}x)"),
+            "gemv": oracle_gemv_rates()}
+
+
+def oracle_gemv_rates(rows_sample: int = 64) -> dict:
+    """The oracle's dequant-GEMV on one host core at the sweep's shapes: the
+    first `rows_sample` rows of each matrix (generated and quantized outside the
+    timed call), GB/s of weight bytes read."""
+    import numpy as np
+
+    import oracle
+    from quantized_decode_dequant_gb300 import workloads as W
+    out = {}
+    for fmt in W.GEMV_FORMATS:
+        for rows, cols in W.GEMV_SHAPES:
+            b = oracle.qtensor_rows(fmt, rows, cols, 0, 1, 0.02, row0=0, nrows=rows_sample, nthreads=4)
+            x = np.random.default_rng(1).standard_normal(cols).astype(np.float32)
+            t0 = time.perf_counter()
+            oracle.gemv(fmt, b, rows_sample, cols, x, nthreads=1)
+            dt = time.perf_counter() - t0
+            gb = rows_sample * cols // W.BLOCK_ELEMS[fmt] * W.BLOCK_BYTES[fmt] / 1e9
+            out[f"{fmt} {rows}x{cols}"] = round(gb / dt, 3)
+    return {"unit": "GB/s, 1 core", "sample": f"first {rows_sample} rows of each sweep shape", "rates": out}
 
 
 def run_reference(args, wl, rank, world, dist):
