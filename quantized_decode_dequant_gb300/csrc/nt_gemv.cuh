@@ -564,17 +564,11 @@ cudaError_t launch_gemv_t(const GemvArgs& a, cudaStream_t s, bool pdl, int* grid
   const int64_t nrows = gemv_logical_rows(a);
   const size_t smem = gemv_smem(FMT, a.seg[0].cols);
   auto kern = k_gemv<FMT, R, EPI>;
-  static int s_sms = 0;
-  static size_t s_occ_smem = ~size_t(0);
-  static int s_occ = 0;
-  if (!s_sms) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&s_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e != cudaSuccess) return e;
-  }
+  static const KernelSetup setup = kernel_setup(kern, 200 * 1024);
+  if (setup.err != cudaSuccess) return setup.err;
+  const int s_sms = setup.sms;
+  thread_local size_t s_occ_smem = ~size_t(0);   // occupancy of the last shared-memory size (per thread)
+  thread_local int s_occ = 0;
   if (s_occ_smem != smem) {
     int occ = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);

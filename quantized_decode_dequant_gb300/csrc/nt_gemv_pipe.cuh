@@ -900,17 +900,11 @@ cudaError_t launch_gemv_pipe_t(const GemvArgs& a, cudaStream_t s, bool pdl, int*
   const size_t smem = pipe_x_bytes(a.ncols, EPI) + size_t(NW) * S * R * Pipe<FMT>::RB;
   if (smem > size_t(kPipeMaxSmem)) return cudaErrorInvalidValue;
   auto kern = k_gemv_pipe<FMT, R, S, EPI, NW>;
-  static int s_sms = 0;
-  static size_t s_occ_smem = ~size_t(0);
-  static int s_occ = 0;
-  if (!s_sms) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&s_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeMaxSmem);
-    if (e != cudaSuccess) return e;
-  }
+  static const KernelSetup setup = kernel_setup(kern, kPipeMaxSmem);
+  if (setup.err != cudaSuccess) return setup.err;
+  const int s_sms = setup.sms;
+  thread_local size_t s_occ_smem = ~size_t(0);   // occupancy of the last shared-memory size (per thread)
+  thread_local int s_occ = 0;
   if (s_occ_smem != smem) {
     int occ = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NW * 32, smem);
@@ -992,14 +986,9 @@ cudaError_t launch_gemv_pipe2_q4k_q6k(const GemvArgs& a1, const GemvArgs& a2, cu
                                : pipe_slice<NT_Q6_K, 2, S2, 0>();
   const size_t smem = pipe_x_bytes(a1.ncols, EPI) + size_t(NW) * slice;
   if (smem > size_t(kPipeMaxSmem) || a1.ncols != a2.ncols || a1.col0 || a2.col0) return cudaErrorInvalidValue;
-  static int s_sms = 0;
-  if (!s_sms) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&s_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeMaxSmem);
-    if (e != cudaSuccess) return e;
-  }
+  static const KernelSetup setup = kernel_setup(kern, kPipeMaxSmem);
+  if (setup.err != cudaSuccess) return setup.err;
+  const int s_sms = setup.sms;
   const int64_t n1 = gemv_logical_rows(a1), n2 = gemv_logical_rows(a2);
   const int64_t groups = (n1 + 1) / 2 + (n2 + 1) / 2;
   int64_t grid = (groups + NW - 1) / NW;

@@ -235,6 +235,25 @@ __device__ __forceinline__ float dequant_elem(const QMat& m, int64_t e) {
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// One-time launch setup of a kernel (thread-safe: a function-local static
+// initialised once): the device's SM count and, for kernels that ask for more
+// than 48 KB, the dynamic shared-memory limit.  A concurrent first launch from
+// another thread waits for the setup instead of launching without the limit.
+struct KernelSetup {
+  int sms = 0;
+  cudaError_t err = cudaSuccess;
+};
+template <class K>
+inline KernelSetup kernel_setup(K kern, int max_dynamic_smem) {
+  KernelSetup k;
+  int dev = 0;
+  k.err = cudaGetDevice(&dev);
+  if (k.err == cudaSuccess) k.err = cudaDeviceGetAttribute(&k.sms, cudaDevAttrMultiProcessorCount, dev);
+  if (k.err == cudaSuccess && max_dynamic_smem > 0)
+    k.err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic_smem);
+  return k;
+}
+
 }  // namespace nt
 
 struct nt_qtensor {

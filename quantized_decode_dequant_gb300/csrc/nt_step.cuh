@@ -32,6 +32,8 @@
 // abandoned.  A launch that starts with the error word set does nothing.
 #pragma once
 
+#include <mutex>
+
 #include "nt_attn.cuh"
 #include "nt_gemv_pipe.cuh"
 
@@ -490,18 +492,18 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
 template <int F_QK, int F_V, int F_O, int F_GU, int F_D, int F_OUT, int HD, int G>
 cudaError_t launch_step_t(const StepArgs& a, size_t smem, cudaStream_t s) {
   auto kern = k_step<F_QK, F_V, F_O, F_GU, F_D, F_OUT, HD, G>;
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-  }
-  static size_t set_smem = 0;
-  if (set_smem < smem) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    set_smem = smem;
+  static const KernelSetup setup = kernel_setup(kern, 0);
+  if (setup.err != cudaSuccess) return setup.err;
+  const int sms = setup.sms;
+  {   // the kernel's shared-memory limit only grows, so a launch never finds it below its own request
+    static std::mutex mu;
+    static size_t set_smem = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (set_smem < smem) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+      if (e != cudaSuccess) return e;
+      set_smem = smem;
+    }
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(sms));

@@ -287,3 +287,36 @@ def test_auto_residency_places_layers_and_decodes_the_same(nt, W):
     finally:
         nt.nt_model_destroy(a)
         nt.nt_model_destroy(b)
+
+
+def test_two_models_in_two_threads_match_sequential_runs(nt, W):
+    """One model per host thread: concurrent steps (first launches included) give
+    the same logits as the same models stepped one after the other."""
+    import threading
+    specs = [dict(WIDE, **W.Q4_K_M), dict(WIDE, n_layers=3)]
+
+    def run(spec, seed, out):
+        m = nt.nt_model_create(nt.make_config(**spec, seed=seed))
+        try:
+            lg = np.empty(spec["vocab"], np.float32)
+            t, logs = 7, []
+            for _ in range(6):
+                t = nt.nt_decode_step(m, t, lg)
+                logs.append(lg.copy())
+            out.extend(logs)
+        finally:
+            nt.nt_model_destroy(m)
+
+    seq = [[], []]
+    for i, sp in enumerate(specs):
+        run(sp, 20 + i, seq[i])
+    par = [[], []]
+    th = [threading.Thread(target=run, args=(sp, 20 + i, par[i])) for i, sp in enumerate(specs)]
+    for x in th:
+        x.start()
+    for x in th:
+        x.join()
+    for i in range(2):
+        assert len(par[i]) == 6
+        for a, b in zip(seq[i], par[i]):
+            np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))

@@ -30,7 +30,7 @@ def _gemv(nt, t, x, rows):
 
 @pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("rows,cols", [(1, 256), (3, 512), (37, 1536), (1000, 4096), (77, 8192), (45, 14336),
-                                       (19, 28672)])
+                                       (19, 28672), (5, 32768), (2, 31744)])
 def test_gemv_matches_oracle(nt, fmt, rows, cols):
     t = nt.nt_qtensor_create(fmt, rows, cols, 3, 55, 0.02)
     try:
