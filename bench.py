@@ -285,9 +285,9 @@ def step_traffic(wl, step_bytes):
 # DRAM bytes (read + write) per algorithmic byte of the GEMV kernel, from the ncu
 # capture summarised in profiles/k_gemv_pipe_q8_0_57344x4096.md, and the SHA-256 of
 # the kernel sources that capture was taken on: a changed kernel reports no traffic.
-GEMV_DRAM_PER_BYTE = (249.624320 + 3.564544) / (57344 * 4096 * 1.0625 + 4 * (57344 + 4096)) * 1e6
+GEMV_DRAM_PER_BYTE = (249.623040 + 3.790336) / (57344 * 4096 * 1.0625 + 4 * (57344 + 4096)) * 1e6
 GEMV_SOURCES = ("nt_gemv_pipe.cuh", "nt_gemv.cuh")
-GEMV_SOURCES_SHA256 = "d65f5d76ce96e30cfff0cca3f779287c252a4407f07ce505f77f3d3452b007d0"
+GEMV_SOURCES_SHA256 = "a8bbdf30332938854bc53e1e385230532b8e489bc0d50e7fa851d7227503427a"
 
 
 def gemv_sources_sha256() -> str:

@@ -43,7 +43,7 @@ def _cycles(nt, m, token, n_draft, k, n_cycles):
     return out
 
 
-@pytest.mark.parametrize("n_draft,k,resident", [(3, 4, 3), (1, 4, 3), (1, 3, 1), (0, 2, 3), (2, 8, 2)])
+@pytest.mark.parametrize("n_draft,k,resident", [(3, 4, 3), (1, 4, 3), (1, 3, 1), (0, 2, 3), (2, 8, 2), (2, 3, 1)])
 def test_speculative_stream_equals_greedy_and_the_oracle(nt, n_draft, k, resident):
     cfg = nt.make_config(**SPEC, seed=12)
     prefill = (20, 2)
