@@ -52,6 +52,8 @@ def parse_args(argv=None):
     p.add_argument("--layer-skip", type=int, default=0, metavar="MAX",
                    help="calibrate per-layer similarity, then skip up to MAX layers at or above --skip-threshold")
     p.add_argument("--skip-threshold", type=float, default=0.98)
+    p.add_argument("--resident", type=int, default=None, metavar="N",
+                   help="keep layers [0, N) in device memory and stream the rest (0: every layer from the host tier)")
     p.add_argument("--speculative", type=int, default=0, metavar="K",
                    help="time self-speculative cycles of K draft tokens instead of plain steps")
     p.add_argument("--draft-layers", type=int, default=None,
@@ -611,6 +613,10 @@ def main(argv=None):
     if args.layers is not None:
         wl = dict(wl, spec=dict(wl["spec"], n_layers=args.layers),
                   label=wl["label"] + f" (profiling case: {args.layers} layers)", vs=None)
+    if args.resident is not None:
+        n = max(0, min(args.resident, wl["spec"]["n_layers"]))
+        wl = dict(wl, resident=n, vs=None,
+                  label=wl["label"] + f" ({n} layers resident, {wl['spec']['n_layers'] - n} streamed)")
     try:
         if args.impl == "reference":
             run_reference(args, wl, rank, world, dist)

@@ -493,6 +493,22 @@ static cudaError_t enqueue_resident(nt_model* m, Launcher& L, bool pdl) {
   return e;
 }
 
+// Copy of layer l's host blob into staging buffer b on the copy stream, once the
+// buffer's last reader (ev_compute_done[b]) is done; records ev_copy_done[b]
+// (and the layer's copy start/end events when `timed`).  One copy per layer:
+// splitting it over several copy streams was measured slower on GB300's
+// host link (168 GB/s with one stream, 148 with two, 115 with four).
+static cudaError_t issue_layer_copy(nt_model* m, int l, int b, bool timed) {
+  const Layer& ly = m->layers[size_t(l)];
+  cudaStream_t cs = m->copy_stream;
+  cudaError_t e = cudaStreamWaitEvent(cs, m->ev_compute_done[b], 0);
+  if (!e && timed) e = cudaEventRecord(m->ev_cs[size_t(l)], cs);
+  if (!e) e = cudaMemcpyAsync(m->staging[b], ly.host, ly.bytes, cudaMemcpyHostToDevice, cs);
+  if (!e && timed) e = cudaEventRecord(m->ev_ce[size_t(l)], cs);
+  if (!e) e = cudaEventRecord(m->ev_copy_done[b], cs);
+  return e;
+}
+
 // Whole step with layers [n_resident, n_layers) copied through the staging
 // buffers (with none streamed it is the resident step without PDL).  Skipped
 // layers are neither copied nor run; the staging buffers alternate over the
@@ -502,23 +518,14 @@ static cudaError_t enqueue_resident(nt_model* m, Launcher& L, bool pdl) {
 static cudaError_t enqueue_streamed(nt_model* m, Launcher& L, float* hs, float* x_out = nullptr) {
   const int nl = m->c.n_layers, nr = m->n_resident;
   const size_t xbytes = size_t(m->c.hidden) * 4;
-  cudaStream_t s = L.s, cs = m->copy_stream;
+  cudaStream_t s = L.s;
   cudaError_t e;
   m->ran.assign(size_t(nl), 0);
   for (int l = 0; l < nl; l++) m->ran[size_t(l)] = (hs || !skipped(m, l)) ? 1 : 0;
   std::vector<int> sl;   // streamed layers that run, in order; sl[k] uses buffer k % 2
   for (int l = nr; l < nl; l++)
     if (m->ran[size_t(l)]) sl.push_back(l);
-  auto issue_copy = [&](size_t k) -> cudaError_t {
-    const int l = sl[k], b = int(k & 1);
-    cudaError_t er = cudaStreamWaitEvent(cs, m->ev_compute_done[b], 0);
-    if (!er) er = cudaEventRecord(m->ev_cs[size_t(l)], cs);
-    if (!er) er = cudaMemcpyAsync(m->staging[b], m->layers[size_t(l)].host, m->layers[size_t(l)].bytes,
-                                  cudaMemcpyHostToDevice, cs);
-    if (!er) er = cudaEventRecord(m->ev_ce[size_t(l)], cs);
-    if (!er) er = cudaEventRecord(m->ev_copy_done[b], cs);
-    return er;
-  };
+  auto issue_copy = [&](size_t k) -> cudaError_t { return issue_layer_copy(m, sl[k], int(k & 1), true); };
   for (size_t k = 0; k < sl.size() && k < 2; k++)
     if ((e = issue_copy(k))) return e;
   if ((e = enqueue_embed(m, L))) return e;
@@ -1035,7 +1042,7 @@ nt_status nt_set_layer_skip(nt_model* m, const uint8_t* mask) {
 static cudaError_t enqueue_verify(nt_model* m, Launcher& L, int n_draft, int k, double* h2d_bytes) {
   const int nl = m->c.n_layers, nr = m->n_resident;
   const size_t h = size_t(m->c.hidden);
-  cudaStream_t s = L.s, cs = m->copy_stream;
+  cudaStream_t s = L.s;
   cudaError_t e;
   std::vector<int> run, sl;
   for (int l = n_draft; l < nl; l++)
@@ -1045,13 +1052,8 @@ static cudaError_t enqueue_verify(nt_model* m, Launcher& L, int n_draft, int k, 
     }
   *h2d_bytes = 0;
   auto issue_copy = [&](size_t j) -> cudaError_t {
-    const int l = sl[j], b = int(j & 1);
-    cudaError_t er = cudaStreamWaitEvent(cs, m->ev_compute_done[b], 0);
-    if (!er) er = cudaMemcpyAsync(m->staging[b], m->layers[size_t(l)].host, m->layers[size_t(l)].bytes,
-                                  cudaMemcpyHostToDevice, cs);
-    if (!er) er = cudaEventRecord(m->ev_copy_done[b], cs);
-    *h2d_bytes += double(m->layers[size_t(l)].bytes);
-    return er;
+    *h2d_bytes += double(m->layers[size_t(sl[j])].bytes);
+    return issue_layer_copy(m, sl[j], int(j & 1), false);
   };
   for (size_t j = 0; j < sl.size() && j < 2; j++)
     if ((e = issue_copy(j))) return e;

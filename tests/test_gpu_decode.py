@@ -125,12 +125,13 @@ def test_device_loop_matches_host_loop_and_profile(nt, W):
         nt.nt_model_destroy(b)
 
 
-def test_streamed_layers_bitwise_equal_resident(nt, W):
+@pytest.mark.parametrize("nr", [2, 0])   # 0: every layer in the page-locked host tier
+def test_streamed_layers_bitwise_equal_resident(nt, W, nr):
     spec = dict(W.TINY, n_layers=5)
     cfg = nt.make_config(**spec, seed=6)
     a, b = nt.nt_model_create(cfg), nt.nt_model_create(cfg)
     try:
-        nt.nt_stream_layers(b, 2, 2)
+        nt.nt_stream_layers(b, nr, 2)
         la = np.empty(spec["vocab"], np.float32)
         lb = np.empty(spec["vocab"], np.float32)
         t = 5
@@ -141,7 +142,7 @@ def test_streamed_layers_bitwise_equal_resident(nt, W):
             assert na == nb
             t = na
         st = nt.nt_get_stats(b)
-        assert st.n_resident == 2 and st.h2d_bytes > 0 and st.h2d_ms > 0
+        assert st.n_resident == nr and st.h2d_bytes > 0 and st.h2d_ms > 0
         assert 0.0 <= st.overlap <= 1.0
         # a streamed tensor still exports, but cannot be used in place
         tq = nt.nt_model_tensor(b, 4, "q")
