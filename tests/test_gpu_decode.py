@@ -200,11 +200,14 @@ def test_llama8b_q8_0_teacher_forced(nt, W):
         om.kv_prefill(W.LLAMA_8B_CTX, W.SEED_KV)
         gl = np.empty(spec["vocab"], np.float32)
         tok = oracle.token(W.SEED_PROMPT, oracle.UID_TOKENS, 0, spec["vocab"])
+        worst = (0.0, 0.0)
         for i in range(int(os.environ.get("NT_8B_STEPS", "3"))):
             gnx = nt.nt_decode_step(m, tok, gl)
             ol, onx, omg = om.decode_step(tok)
-            _check_step(gl, gnx, ol, onx, omg, i)
+            e = _check_step(gl, gnx, ol, onx, omg, i)
+            worst = (max(worst[0], e[0]), max(worst[1], e[1]))
             tok = gnx
+        print(f"8B worst over {i + 1} steps: max-abs {worst[0]:.3e} rel-L2 {worst[1]:.3e}")
     finally:
         nt.nt_model_destroy(m)
 
