@@ -53,7 +53,7 @@ cudaError_t launch_gemv(const GemvArgs& a_in, int epi, cudaStream_t s, bool pdl,
   if (a.max_grid <= 0 || a.max_grid > kMaxGemvGrid) a.max_grid = kMaxGemvGrid;
   const int fmt = a.seg[0].type;
   const int64_t nrows = gemv_logical_rows(a);
-  int R = nrows >= 16384 ? 4 : 2;
+  int R = nrows >= 8192 ? 4 : 2;   // four rows per warp for tall 4-bit matrices (measured from 8192 rows)
   const int64_t align = 1024;   // whole 32-unit tiles for the pipeline
   static const bool force_register_path = getenv("NT_GEMV_REGISTER_PATH") != nullptr;
   if (cols % align == 0 && !force_register_path) {
