@@ -573,7 +573,11 @@ static nt_status wait_event(cudaEvent_t ev, const char* what) {
     if (e != cudaErrorNotReady) return cuda_fail(e, what);
     const double ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
     if (ms > limit) return fail(NT_E_TIMEOUT, std::string(what) + ": device did not finish within the watchdog limit");
-    std::this_thread::sleep_for(std::chrono::microseconds(ms < 5.0 ? 2 : 200));
+    // a decode step takes milliseconds: poll without sleeping for the first 20 ms
+    // (a sleep of a few microseconds returns only after the timer slack, tens of
+    // microseconds, which a step would pay every token), then back off
+    if (ms < 20.0) std::this_thread::yield();
+    else std::this_thread::sleep_for(std::chrono::microseconds(200));
   }
 }
 
