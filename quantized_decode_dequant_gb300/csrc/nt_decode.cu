@@ -211,6 +211,7 @@ struct nt_model {
   cudaEvent_t ev_copy_done[2] = {}, ev_compute_done[2] = {};
   std::vector<cudaEvent_t> ev_cs, ev_ce, ev_ls, ev_le;
   cudaEvent_t ev_step0 = nullptr, ev_step1 = nullptr;
+  cudaEvent_t ev_io = nullptr;       // after a step's result copies to the host
   nt_stats stats{};
   std::vector<uint8_t> skip;         // per layer: 1 = skipped (empty: none)
   std::vector<uint8_t> ran;          // per layer: evaluated in the last streamed step
@@ -753,6 +754,7 @@ static void free_model(nt_model* m) {
     for (auto e : *v) cudaEventDestroy(e);
   if (m->ev_step0) cudaEventDestroy(m->ev_step0);
   if (m->ev_step1) cudaEventDestroy(m->ev_step1);
+  if (m->ev_io) cudaEventDestroy(m->ev_io);
   if (m->stream) cudaStreamDestroy(m->stream);
   if (m->copy_stream) cudaStreamDestroy(m->copy_stream);
   delete m;
@@ -819,6 +821,7 @@ nt_status nt_model_create(const nt_config* cfg, nt_model** out) {
   }
   NT_TRY(cudaEventCreate(&m->ev_step0), "cudaEventCreate");
   NT_TRY(cudaEventCreate(&m->ev_step1), "cudaEventCreate");
+  NT_TRY(cudaEventCreateWithFlags(&m->ev_io, cudaEventDisableTiming), "cudaEventCreate");
   for (auto* v : {&m->ev_cs, &m->ev_ce, &m->ev_ls, &m->ev_le}) {
     v->resize(size_t(c.n_layers));
     for (auto& ev : *v) NT_TRY(cudaEventCreate(&ev), "cudaEventCreate");
@@ -976,9 +979,9 @@ static nt_status run_step(nt_model* m, int32_t token, int32_t* next_token, float
     NT_CUDA(cudaMemcpyAsync(logits_host, m->logits, size_t(c.vocab) * 4, cudaMemcpyDeviceToHost, m->stream));
   if (calib && c.n_layers > 0)
     NT_CUDA(cudaMemcpyAsync(cos_out, m->d_cos, size_t(c.n_layers) * 8, cudaMemcpyDeviceToHost, m->stream));
-  nt_status st = wait_event(m->ev_step1, who);
+  NT_CUDA(cudaEventRecord(m->ev_io, m->stream));   // the step and its result copies
+  nt_status st = wait_event(m->ev_io, who);
   if (st) return st;
-  NT_CUDA(cudaStreamSynchronize(m->stream));
   if (m->h_io[4]) {
     reset_step_error(m);
     return fail(NT_E_TIMEOUT, std::string(who) + ": a grid barrier of the step kernel timed out; step abandoned");
