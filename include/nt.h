@@ -143,23 +143,17 @@ nt_status nt_kv_prefill(nt_model* m, int32_t n_ctx, uint64_t seed);
  * token: input id in [0, vocab).  next_token (host, required): the argmax.
  * logits_host (nullable): vocab floats.  top2_margin (nullable): top-1 minus
  * top-2 logit.  Synchronous.  Position becomes p+1.
- * A resident model runs the step as a CUDA graph of per-kernel launches.  With
- * the environment variable NT_STEP_KERNEL=1, a model whose layers are all
- * resident, whose GEMV widths are multiples of 1024 and whose format mix, head
- * size and query group have a persistent step kernel (Q8_0 throughout with 4
- * query heads per kv head; Q4_K_M with 8) runs the step as that one cooperative
- * kernel instead; results are bitwise the same.
- * NT_E_INVAL: token out of range or p == max_ctx.  NT_E_TIMEOUT: a wait of the
- * step kernel ran past one second (the step is abandoned, the position does not
- * advance) or the host watchdog expired. */
+ * A resident model runs the step as a CUDA graph of per-kernel launches.
+ * NT_E_INVAL: token out of range or p == max_ctx.  NT_E_TIMEOUT: the host
+ * watchdog (NT_WATCHDOG_MS, default 120 s) expired before the step finished. */
 nt_status nt_decode_step(nt_model* m, int32_t token, int32_t* next_token, float* logits_host,
                          float* top2_margin);
 
 /* n_steps greedy steps that feed each argmax back as the next input on the
  * device, starting from token; asynchronous on stream (the model's own
  * stream waits for it).  The produced ids are kept on the device
- * (nt_get_tokens, which reports NT_E_TIMEOUT if a step was abandoned).  Layer-streamed models are not supported here
- * (NT_E_STATE); use nt_decode_step. */
+ * (nt_get_tokens).  Layer-streamed models are not supported here (NT_E_STATE);
+ * use nt_decode_step. */
 nt_status nt_decode_run(nt_model* m, int32_t token, int32_t n_steps, void* stream);
 
 /* Copies the ids produced at positions [t0, t0+n) into host_out (n int32). */
@@ -217,8 +211,7 @@ nt_status nt_layer_similarity(nt_model* m, int32_t token, int32_t* next_token, d
  * memory, copied) skips layer l -- its weights are neither read nor copied from
  * the host tier, its K/V row is not written, and the residual stream passes
  * through unchanged.  mask = NULL evaluates every layer again.  Applies to
- * nt_decode_step, nt_decode_run and nt_profile_steps (the persistent step
- * kernel is not used while any layer is skipped). */
+ * nt_decode_step, nt_decode_run and nt_profile_steps. */
 nt_status nt_set_layer_skip(nt_model* m, const uint8_t* mask);
 
 /* Host arithmetic: mask_out[l] = 1 for every layer with cos[l] >= threshold;
@@ -253,10 +246,8 @@ nt_status nt_speculative_step(nt_model* m, int32_t token, int32_t n_draft, int32
 nt_status nt_get_stats(const nt_model* m, nt_stats* out);
 
 /* Runs n_steps decode steps (from token, feeding back argmax) and returns
- * per-class device times.  Per-kernel launches: a CUDA event pair around every
- * launch (not graph-captured).  Step kernel: the SM clock of CTA 0 at every
- * grid barrier, scaled to the event-timed duration of the launch; a "launch"
- * of a class is then one phase.  For measurement only. */
+ * per-class device times: a CUDA event pair around every launch (not
+ * graph-captured, no programmatic dependent launch).  For measurement only. */
 nt_status nt_profile_steps(nt_model* m, int32_t token, int32_t n_steps, nt_kernel_times* out);
 
 /* Times the step's GEMV launches on their own: one CUDA graph of a step's GEMV

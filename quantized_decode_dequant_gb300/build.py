@@ -17,8 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnt.so")
 SOURCES = ["nt_quant.cu", "nt_gemv.cu", "nt_gemv_q8_0.cu", "nt_gemv_q4_0.cu", "nt_gemv_q4_k.cu",
-           "nt_gemv_q6_k.cu", "nt_gemv_q5_k.cu", "nt_decode.cu", "nt_noalloc.cu", "nt_step.cu", "nt_step_q8_0.cu",
-           "nt_step_q4_k_m.cu"]
+           "nt_gemv_q6_k.cu", "nt_gemv_q5_k.cu", "nt_decode.cu", "nt_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
                 "-Xcompiler", "-Wall", "-diag-suppress", "177"]

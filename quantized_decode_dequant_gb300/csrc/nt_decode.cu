@@ -27,7 +27,8 @@
 #include <thread>
 #include <vector>
 
-#include "nt_step.cuh"
+#include "nt_attn.cuh"
+#include "nt_gemv_pipe.cuh"
 
 namespace nt {
 
@@ -187,13 +188,7 @@ struct nt_model {
   float2* rope = nullptr;
   float4* top2 = nullptr;
   unsigned* tickets = nullptr;       // attention: finished chunks per kv head
-  unsigned* bar = nullptr;           // step kernel: grid barrier state
-  nt::StepGemv* step_tab = nullptr;  // step kernel: GEMV table (device)
-  nt::StepPlan plan{};
-  nt::StepArgs step{};
-  size_t step_smem = 0;
-  int step_state = 0;                // 0 unknown, 1 ready, -1 not applicable
-  int32_t* small = nullptr;          // pos, token, next, margin(float bits), error word
+  int32_t* small = nullptr;          // pos, token, next, margin(float bits)
   int32_t* hist = nullptr;           // produced ids by position
   int32_t* h_io = nullptr;           // pinned host mirror of small; [32, 56): speculative step
   float* sp_x = nullptr;             // speculative step: residual of each draft token after the draft layers
@@ -611,131 +606,6 @@ static nt_status ensure_graph(nt_model* m) {
   return NT_OK;
 }
 
-// ------------------------------------------------------------ step kernel --
-
-// The persistent step kernel is opt-in (NT_STEP_KERNEL=1): on GB300 the
-// graph of per-kernel launches is faster today.
-static bool step_kernel_enabled() {
-  const char* v = getenv("NT_STEP_KERNEL");
-  return v && strcmp(v, "1") == 0;
-}
-
-static void fill_step_gemv(StepGemv& d, const GemvArgs& a) {
-  d.a = a;
-  d.a.col0 = 0;
-  d.a.ncols = a.seg[0].cols;
-  d.a.max_grid = kMaxGemvGrid;
-  d.nrows = gemv_logical_rows(a);
-}
-
-// Decides (once per residency layout) whether the step runs as the persistent
-// kernel, and if so builds its GEMV table in device memory.
-static nt_status prepare_step(nt_model* m) {
-  if (m->step_state) return NT_OK;
-  m->step_state = -1;
-  const nt_config& c = m->c;
-  if (!step_kernel_enabled() || m->n_resident < c.n_layers) return NT_OK;
-  for (int l = 0; l < c.n_layers; l++)
-    if (skipped(m, l)) return NT_OK;
-  const int64_t qd = int64_t(c.n_heads) * c.head_dim;
-  if (c.hidden % 1024 || qd % 1024 || c.ffn_dim % 1024 || c.n_kv_heads > kStepMaxTiles) return NT_OK;
-  StepPlan p;
-  p.f_qk = c.t_q;
-  p.f_v = c.t_v;
-  p.f_o = c.t_o;
-  p.f_gu = c.t_gate;
-  p.f_d = c.t_down;
-  p.f_out = c.t_out;
-  p.hd = c.head_dim;
-  p.G = c.n_heads / c.n_kv_heads;
-  int dev = 0, coop = 0;
-  NT_CUDA(cudaGetDevice(&dev));
-  NT_CUDA(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev));
-  if (!coop) return NT_OK;
-  int64_t max_cols = c.hidden > qd ? c.hidden : qd;
-  if (c.ffn_dim > max_cols) max_cols = c.ffn_dim;
-  size_t ring_off = 0;
-  const size_t smem = step_smem(p, max_cols, c.hidden, attn_chunk_len(c.max_ctx), &ring_off);
-  bool fits = false;
-  const cudaError_t fe = step_fits(p, smem, &fits);
-  if (fe == cudaErrorNotSupported) return NT_OK;   // no instantiation for this plan
-  if (fe != cudaSuccess) return cuda_fail(fe, "nt_decode_step: step kernel attributes");
-  if (!fits) return NT_OK;
-
-  // layer 0's GEMVs and the head; layer l reads its weights delta_l bytes further on
-  std::vector<StepGemv> tab(SG_PER_LAYER + 1);
-  std::vector<int64_t> delta(size_t(c.n_layers));
-  if (c.n_layers > 0) {
-    const LayerGemvs g = layer_gemvs(m, 0, m->layers[0].dev);
-    fill_step_gemv(tab[SG_QK], g.qk);
-    if (g.v_split) fill_step_gemv(tab[SG_V], g.v);
-    fill_step_gemv(tab[SG_O], g.o);
-    fill_step_gemv(tab[SG_GU], g.gu);
-    fill_step_gemv(tab[SG_DOWN], g.down);
-    for (int l = 0; l < c.n_layers; l++)
-      delta[size_t(l)] = int64_t(m->layers[size_t(l)].dev - m->layers[0].dev);
-  }
-  fill_step_gemv(tab[SG_PER_LAYER], head_gemv(m));
-  if (m->step_tab) dev_free(m, m->step_tab);
-  m->step_tab = nullptr;
-  const size_t tab_bytes = tab.size() * sizeof(StepGemv), delta_bytes = delta.size() * 8;
-  NT_CUDA(dev_alloc(m, reinterpret_cast<void**>(&m->step_tab), tab_bytes + delta_bytes + 8));
-  NT_CUDA(cudaMemcpy(m->step_tab, tab.data(), tab_bytes, cudaMemcpyHostToDevice));
-  int64_t* d_delta = reinterpret_cast<int64_t*>(reinterpret_cast<uint8_t*>(m->step_tab) + tab_bytes);
-  if (delta_bytes) NT_CUDA(cudaMemcpy(d_delta, delta.data(), delta_bytes, cudaMemcpyHostToDevice));
-
-  StepArgs& a = m->step;
-  a = StepArgs();
-  a.gemv = m->step_tab;
-  a.layer_delta = d_delta;
-  a.n_layers = c.n_layers;
-  a.split_v = c.t_v != c.t_q;
-  a.embd = m->embd.m;
-  a.x = m->x;
-  a.hidden = c.hidden;
-  a.attn = attn_args(m, 0);
-  a.kv = m->kv;
-  a.kv_layer_elems = kv_layer_elems(c);
-  a.n_kv = c.n_kv_heads;
-  a.attn_qd = int(qd);
-  a.attn_kd = c.n_kv_heads * c.head_dim;
-  a.top2 = m->top2;
-  a.small = m->small;
-  a.hist = m->hist;
-  a.max_ctx = c.max_ctx;
-  a.vocab = c.vocab;
-  a.bar = m->bar;
-  a.ring_off = uint32_t(ring_off);
-  // fault injection for tests: a barrier base that the arrivals never reach,
-  // so the step's grid barrier runs into its time limit
-  if (const char* off = getenv("NT_STEP_BARRIER_OFFSET")) {
-    const unsigned base = unsigned(strtoul(off, nullptr, 10));
-    NT_CUDA(cudaMemcpy(m->bar + 1, &base, 4, cudaMemcpyHostToDevice));
-  }
-  m->plan = p;
-  m->step_smem = smem;
-  m->step_state = 1;
-  return NT_OK;
-}
-
-static int step_barriers(const nt_model* m) { return 2 + 5 * m->c.n_layers; }
-
-static cudaError_t launch_step_model(nt_model* m, cudaStream_t s, long long* stamps) {
-  StepArgs a = m->step;
-  a.stamps = stamps;
-  return launch_step(m->plan, a, m->step_smem, s);
-}
-
-// After an abandoned step: clear the error word and the barrier state.
-static void reset_step_error(nt_model* m) {
-  cudaMemsetAsync(m->bar, 0, SYNC_WORDS * 4, m->stream);
-  m->h_io[0] = m->pos;   // the abandoned step may have advanced the device position
-  cudaMemcpyAsync(d_pos(m), m->h_io, 4, cudaMemcpyHostToDevice, m->stream);
-  cudaMemsetAsync(m->tickets, 0, size_t(m->c.n_kv_heads) * 4, m->stream);
-  cudaMemsetAsync(m->small + 4, 0, 4, m->stream);
-  cudaStreamSynchronize(m->stream);
-}
-
 static void free_model(nt_model* m) {
   if (!m) return;
   if (m->stream) cudaStreamSynchronize(m->stream);
@@ -881,8 +751,6 @@ nt_status nt_model_create(const nt_config* cfg, nt_model** out) {
   NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->top2), size_t(kMaxGemvGrid) * 16), "alloc top2");
   NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->tickets), size_t(c.n_kv_heads) * 4), "alloc tickets");
   NT_TRY(cudaMemsetAsync(m->tickets, 0, size_t(c.n_kv_heads) * 4, m->stream), "cudaMemset");
-  NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->bar), SYNC_WORDS * 4), "alloc step sync state");
-  NT_TRY(cudaMemsetAsync(m->bar, 0, SYNC_WORDS * 4, m->stream), "cudaMemset");
   NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->small), 16 * 4), "alloc small");
   NT_TRY(dev_alloc(m, reinterpret_cast<void**>(&m->hist), size_t(c.max_ctx) * 4), "alloc hist");
   NT_TRY(cudaMemsetAsync(m->small, 0, 16 * 4, m->stream), "cudaMemset");
@@ -948,15 +816,9 @@ static nt_status run_step(nt_model* m, int32_t token, int32_t* next_token, float
     NT_CUDA(dev_alloc(m, reinterpret_cast<void**>(&m->hs), size_t(c.n_layers + 1) * c.hidden * 4));
     NT_CUDA(dev_alloc(m, reinterpret_cast<void**>(&m->d_cos), size_t(c.n_layers > 0 ? c.n_layers : 1) * 8));
   }
-  bool step_kernel = false;
-  if (!calib) {
-    nt_status st0 = prepare_step(m);
-    if (st0) return st0;
-    step_kernel = m->step_state == 1;
-    if (!streamed && !step_kernel) {
-      nt_status st = ensure_graph(m);
-      if (st) return st;
-    }
+  if (!calib && !streamed) {
+    nt_status st = ensure_graph(m);
+    if (st) return st;
   }
   m->h_io[1] = token;
   NT_CUDA(cudaMemcpyAsync(d_token(m), m->h_io + 1, 4, cudaMemcpyHostToDevice, m->stream));
@@ -966,15 +828,12 @@ static nt_status run_step(nt_model* m, int32_t token, int32_t* next_token, float
     L.s = m->stream;
     cudaError_t e = enqueue_streamed(m, L, calib ? m->hs : nullptr);
     if (e) return cuda_fail(e, (std::string(who) + ": launch-by-launch step").c_str());
-  } else if (step_kernel) {
-    cudaError_t e = launch_step_model(m, m->stream, nullptr);
-    if (e) return cuda_fail(e, (std::string(who) + ": step kernel").c_str());
   } else {
     NT_CUDA(cudaGraphLaunch(m->exec, m->stream));
   }
   NT_CUDA(cudaEventRecord(m->ev_step1, m->stream));
-  // next id, margin and the error word
-  NT_CUDA(cudaMemcpyAsync(m->h_io + 2, d_next(m), 12, cudaMemcpyDeviceToHost, m->stream));
+  // next id and margin
+  NT_CUDA(cudaMemcpyAsync(m->h_io + 2, d_next(m), 8, cudaMemcpyDeviceToHost, m->stream));
   if (logits_host)
     NT_CUDA(cudaMemcpyAsync(logits_host, m->logits, size_t(c.vocab) * 4, cudaMemcpyDeviceToHost, m->stream));
   if (calib && c.n_layers > 0)
@@ -982,10 +841,6 @@ static nt_status run_step(nt_model* m, int32_t token, int32_t* next_token, float
   NT_CUDA(cudaEventRecord(m->ev_io, m->stream));   // the step and its result copies
   nt_status st = wait_event(m->ev_io, who);
   if (st) return st;
-  if (m->h_io[4]) {
-    reset_step_error(m);
-    return fail(NT_E_TIMEOUT, std::string(who) + ": a grid barrier of the step kernel timed out; step abandoned");
-  }
   float ms = 0.f;
   NT_CUDA(cudaEventElapsedTime(&ms, m->ev_step0, m->ev_step1));
   m->stats.last_step_ms = ms;
@@ -1032,7 +887,6 @@ nt_status nt_set_layer_skip(nt_model* m, const uint8_t* mask) {
   if (!m) return fail(NT_E_INVAL, "nt_set_layer_skip: model is NULL");
   NT_CUDA(cudaStreamSynchronize(m->stream));
   drop_graph(m);
-  m->step_state = 0;
   m->skip.clear();
   if (mask) {
     m->skip.assign(size_t(m->c.n_layers), 0);
@@ -1205,23 +1059,14 @@ nt_status nt_decode_run(nt_model* m, int32_t token, int32_t n_steps, void* strea
   if (n_steps < 0 || token < 0 || token >= m->c.vocab) return fail(NT_E_INVAL, "nt_decode_run: bad token or n_steps");
   if (m->pos + n_steps > m->c.max_ctx) return fail(NT_E_INVAL, "nt_decode_run: would pass max_ctx");
   if (m->n_resident < m->c.n_layers) return fail(NT_E_STATE, "nt_decode_run: model has streamed layers");
-  nt_status st = prepare_step(m);
+  nt_status st = ensure_graph(m);
   if (st) return st;
-  const bool step_kernel = m->step_state == 1;
-  if (!step_kernel && (st = ensure_graph(m))) return st;
   cudaStream_t us = static_cast<cudaStream_t>(stream);
   NT_CUDA(cudaEventRecord(m->ev_step0, us));
   NT_CUDA(cudaStreamWaitEvent(m->stream, m->ev_step0, 0));
   m->h_io[1] = token;
   NT_CUDA(cudaMemcpyAsync(d_token(m), m->h_io + 1, 4, cudaMemcpyHostToDevice, m->stream));
-  for (int i = 0; i < n_steps; i++) {
-    if (step_kernel) {
-      cudaError_t e = launch_step_model(m, m->stream, nullptr);
-      if (e) return cuda_fail(e, "nt_decode_run: step kernel");
-    } else {
-      NT_CUDA(cudaGraphLaunch(m->exec, m->stream));
-    }
-  }
+  for (int i = 0; i < n_steps; i++) NT_CUDA(cudaGraphLaunch(m->exec, m->stream));
   NT_CUDA(cudaEventRecord(m->ev_step1, m->stream));
   NT_CUDA(cudaStreamWaitEvent(us, m->ev_step1, 0));
   m->pos += n_steps;
@@ -1233,15 +1078,6 @@ nt_status nt_get_tokens(nt_model* m, int32_t t0, int32_t n, int32_t* host_out) {
   if (!m || !host_out) return fail(NT_E_INVAL, "nt_get_tokens: NULL argument");
   if (t0 < 0 || n < 0 || t0 + n > m->c.max_ctx) return fail(NT_E_INVAL, "nt_get_tokens: range");
   NT_CUDA(cudaStreamSynchronize(m->stream));
-  int32_t err = 0;
-  NT_CUDA(cudaMemcpy(&err, m->small + 4, 4, cudaMemcpyDeviceToHost));
-  if (err) {
-    reset_step_error(m);
-    int32_t pos = 0;   // abandoned steps did not advance the device position
-    NT_CUDA(cudaMemcpy(&pos, d_pos(m), 4, cudaMemcpyDeviceToHost));
-    m->pos = pos;
-    return fail(NT_E_TIMEOUT, "nt_get_tokens: a step of an earlier nt_decode_run was abandoned (grid barrier timeout)");
-  }
   NT_CUDA(cudaMemcpy(host_out, m->hist + t0, size_t(n) * 4, cudaMemcpyDeviceToHost));
   return NT_OK;
 }
@@ -1266,7 +1102,6 @@ nt_status nt_stream_layers(nt_model* m, int32_t n_resident, int32_t n_staging) {
   NT_CUDA(cudaStreamSynchronize(m->stream));
   NT_CUDA(cudaStreamSynchronize(m->copy_stream));
   drop_graph(m);
-  m->step_state = 0;
   size_t max_bytes = 0;
   for (int l = 0; l < m->c.n_layers; l++) {
     Layer& L = m->layers[size_t(l)];
@@ -1321,7 +1156,7 @@ static void model_bytes(const nt_config& c, int64_t* layer, int64_t* fixed) {
   f += int64_t(c.n_layers) * 2 * kd * c.max_ctx * 2;                      // K/V cache
   f += 4 * (h + 2 * qd + c.ffn_dim + c.vocab);                            // x, q, att, u, logits
   f += qd * n_chunks * 4 + int64_t(c.n_heads) * n_chunks * 8;              // attention partials
-  f += int64_t(kMaxGemvGrid) * 16 + int64_t(c.n_kv_heads) * 4 + SYNC_WORDS * 4 + 16 * 4;
+  f += int64_t(kMaxGemvGrid) * 16 + int64_t(c.n_kv_heads) * 4 + 16 * 4;
   f += int64_t(c.max_ctx) * 4 + int64_t(c.max_ctx) * (hd / 2) * 8;        // token history, RoPE table
   f += int64_t(c.n_layers) * 256 * 16;                                    // allocation rounding
   *layer = lb;
@@ -1349,72 +1184,6 @@ nt_status nt_profile_steps(nt_model* m, int32_t token, int32_t n_steps, nt_kerne
   double wall = 0;
   m->h_io[1] = token;
   NT_CUDA(cudaMemcpyAsync(d_token(m), m->h_io + 1, 4, cudaMemcpyHostToDevice, m->stream));
-  nt_status st0 = prepare_step(m);
-  if (st0) return st0;
-  if (m->step_state == 1) {
-    // one launch per step; CTA 0's SM clock at every barrier splits it into phases
-    const nt_config& c = m->c;
-    const int nb = step_barriers(m);
-    long long* d_stamps = nullptr;
-    NT_CUDA(cudaMalloc(&d_stamps, size_t(nb + 2) * 8));
-    std::vector<long long> h(size_t(nb + 2));
-    const int hd = c.head_dim, qd = c.n_heads * hd, kd = c.n_kv_heads * hd;
-    nt_status st = NT_OK;
-    for (int i = 0; i < n_steps && !st; i++) {
-      cudaError_t e = cudaEventRecord(m->ev_step0, m->stream);
-      if (!e) e = launch_step_model(m, m->stream, d_stamps);
-      if (!e) e = cudaEventRecord(m->ev_step1, m->stream);
-      if (e) {
-        st = cuda_fail(e, "nt_profile_steps: step kernel");
-        break;
-      }
-      if ((st = wait_event(m->ev_step1, "nt_profile_steps"))) break;
-      float ms = 0.f;
-      e = cudaEventElapsedTime(&ms, m->ev_step0, m->ev_step1);
-      if (!e) e = cudaMemcpy(h.data(), d_stamps, h.size() * 8, cudaMemcpyDeviceToHost);
-      if (!e) e = cudaMemcpy(m->h_io + 4, m->small + 4, 4, cudaMemcpyDeviceToHost);
-      if (e) {
-        st = cuda_fail(e, "nt_profile_steps");
-        break;
-      }
-      if (m->h_io[4]) {
-        reset_step_error(m);
-        st = fail(NT_E_TIMEOUT, "nt_profile_steps: a grid barrier of the step kernel timed out");
-        break;
-      }
-      wall += ms;
-      const double cyc = double(h[size_t(nb + 1)] - h[0]);
-      const double ms_per_cyc = cyc > 0 ? ms / cyc : 0.0;
-      auto add = [&](int kind, int k0, double bytes) {   // phase between stamps k0 and k0+1
-        t.launches[kind]++;
-        t.ms[kind] += double(h[size_t(k0 + 1)] - h[size_t(k0)]) * ms_per_cyc;
-        t.bytes[kind] += bytes;
-      };
-      const int n_used = m->pos + 1;
-      add(NT_KC_OTHER, 0, 0.0);
-      for (int l = 0; l < c.n_layers; l++) {
-        const LayerGemvs g = layer_gemvs(m, l, m->layers[size_t(l)].dev);
-        const int k = 1 + 5 * l;
-        double qkv = g.v_split ? gemv_bytes(g.qk, 4.0 * qd + 2.0 * kd) + gemv_bytes(g.v, 2.0 * kd)
-                               : gemv_bytes(g.qk, 4.0 * qd + 4.0 * kd);
-        add(NT_KC_GEMV, k, qkv);
-        add(NT_KC_ATTN, k + 1, 2.0 * 2.0 * double(c.n_kv_heads) * n_used * hd + 8.0 * qd);
-        add(NT_KC_GEMV, k + 2, gemv_bytes(g.o, 8.0 * c.hidden));
-        add(NT_KC_GEMV, k + 3, gemv_bytes(g.gu, 4.0 * c.ffn_dim));
-        add(NT_KC_GEMV, k + 4, gemv_bytes(g.down, 8.0 * c.hidden));
-      }
-      add(NT_KC_GEMV, nb - 1, gemv_bytes(head_gemv(m), 4.0 * c.vocab));
-      add(NT_KC_OTHER, nb, 0.0);
-      t.kernel_launches++;
-      m->pos++;
-      m->stats.steps++;
-    }
-    cudaFree(d_stamps);
-    if (st) return st;
-    t.step_ms = wall / n_steps;
-    *out = t;
-    return NT_OK;
-  }
   for (int i = 0; i < n_steps; i++) {
     Prof prof;
     Launcher L;
