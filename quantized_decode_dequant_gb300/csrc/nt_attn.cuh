@@ -1,35 +1,36 @@
-// nt_attn.cuh -- GQA decode attention over the f16 KV cache, as device
-// functions for one CTA of kAttnThreads threads, so the per-launch kernel and
-// the persistent step kernel run the same arithmetic.
+// nt_attn.cuh -- GQA decode attention over the f16 KV cache (hada "Hauptfunktionen":
+// GQA with a KV cache; "Architektur und Codestruktur": softmax kernel).
 //
-// Split context: item (kv head g, chunk c) scores the G = n_heads/n_kv_heads
-// query heads that share g against the chunk's C cached keys (C = 64, 128 or
-// 256, fixed per model by its maximum context), keeps the chunk's softmax
-// statistics (max m_c, sum of exp l_c) and the unnormalised exp-weighted sum o_c
-// of its values.  The CTA that finishes the last chunk of kv head g (an atomic
-// ticket per kv head) merges the chunks of g's heads, one warp per head:
-// M = max m_c, o = sum o_c e^(m_c - M) / sum l_c e^(m_c - M).
+// Split context: item (kv head g, chunk c) attends the G = n_heads/n_kv_heads
+// query heads that share g over the chunk's C cached positions.  It keeps the
+// chunk's softmax statistics (max m_c, sum of exponentials l_c) and the
+// unnormalised exp-weighted sum o_c of its values.  The CTA that finishes the
+// last chunk of kv head g (an atomic ticket per kv head) merges the chunks of
+// g's heads: M = max m_c, o = sum o_c e^(m_c - M) / sum l_c e^(m_c - M).
+//
+// The two contractions of an item are small dense products, run on the tensor
+// cores with mma.sync m16n8k16 (f16 operands, fp32 accumulation):
+//   scores  S[h][t] = q_h . K_t        A = q (query heads), B = K^T
+//   values  O[h][d] = sum_t P[h][t] V_t[d]   A = P, B = V
+// K and V are f16 already, so they enter exactly.  q and P are fp32; each is
+// split into two f16 terms, hi = f16(v) and lo = f16(v - hi), held as separate
+// rows of the A operand, and the two rows' products are added in fp32
+// afterwards: the operand keeps about 22 significant bits instead of 11.
+// With G <= 8 one 16-row tile holds hi (rows 0..G-1) and lo (rows 8..8+G-1);
+// with G = 16 two tiles hold hi and lo of all heads.
 #pragma once
-
-#include <cstdlib>
 
 #include "nt_internal.cuh"
 
 namespace nt {
 
-constexpr int kAttnThreads = 512;
-constexpr int kAttnMaxChunk = 256;
+constexpr int kAttnWarps = 8;
+constexpr int kAttnThreads = 32 * kAttnWarps;
 
-// Cached positions per item: as short as keeps the items of a full context
-// within about one per SM (at most 256); NT_ATTN_CHUNK (64, 128 or 256)
-// overrides.  Fixed per model: every path of a model splits the same way.
-inline int attn_chunk_len(int max_ctx) {
-  if (const char* e = getenv("NT_ATTN_CHUNK")) {
-    const int c = atoi(e);
-    if (c == 64 || c == 128 || c == 256) return c;
-  }
-  return max_ctx <= 1024 ? 64 : (max_ctx <= 2048 ? 128 : 256);
-}
+// Cached positions per item: 64 up to 1024 positions of maximum context, 128 up
+// to 2048, else 256 (about one item per SM for the longest contexts; the merge
+// then combines at most 17 chunks per head at 4096 positions).  Fixed per model.
+inline int attn_chunk_len(int max_ctx) { return max_ctx <= 1024 ? 64 : (max_ctx <= 2048 ? 128 : 256); }
 
 struct AttnArgs {
   const float* q = nullptr;         // [n_heads][hd], RoPE applied
@@ -45,12 +46,21 @@ struct AttnArgs {
   float* out = nullptr;             // [n_heads][hd]
 };
 
-// Shared memory of one item: K and V rows (padded: 16-byte reads of 8 rows hit
-// distinct banks), q of the G heads, the G x C scores, the P V partial sums of
-// the kAttnThreads/hd position slices, a flag.
-__host__ __device__ constexpr size_t attn_item_smem(int hd, int G, int C) {
-  return size_t(2 * C * (hd + 8)) * 2 + size_t(G * hd + G * C) * 4 + size_t(2 * kAttnThreads / hd) * G * hd * 4 + 16;
-}
+// Shared memory of one item.  K and V rows are padded by 16 bytes so that the
+// eight 16-byte rows one ldmatrix phase reads fall in distinct banks; P rows
+// likewise.
+template <int HD, int G, int C>
+struct AttnLayout {
+  static constexpr int KP = HD + 8;              // halves per padded K/V row
+  static constexpr int MT = G > 8 ? 2 : 1;       // 16-row tiles of the A operand
+  static constexpr int PP = C + 8;               // halves per padded P row
+  static constexpr size_t kK = 0;
+  static constexpr size_t kV = kK + size_t(C) * KP * 2;
+  static constexpr size_t kP = kV + size_t(C) * KP * 2;
+  static constexpr size_t kRed = kP + size_t(MT) * 16 * PP * 2;        // [2][warps][G] floats
+  static constexpr size_t kFlag = kRed + size_t(2) * kAttnWarps * G * 4;
+  static constexpr size_t kBytes = kFlag + 16;
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -58,30 +68,48 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ void attn_cp16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+// D += A B for one 16x8x16 tile (f16 operands, fp32 accumulators)
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// (hi, lo) f16 pair terms of two fp32 values, packed as two f16x2 words
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(__fsub_rn(x0, hf.x), __fsub_rn(x1, hf.y));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
 
 // Copies of rows [r0, r1) of the item's K and V (chunk-relative) into shared memory.
-template <int HD>
+template <int HD, int C>
 __device__ __forceinline__ void attn_copy_rows(const AttnArgs& a, int g, int t0, int r0, int r1, uint8_t* sm) {
   constexpr int KP = HD + 8, VPR = HD / 8;
   const __half* kb = a.kc + (int64_t(g) * a.max_ctx + t0) * HD;
   const __half* vb = a.vc + (int64_t(g) * a.max_ctx + t0) * HD;
-  const uint32_t ks = smem_u32(sm), vs = ks + uint32_t(a.chunk * KP) * 2;
+  const uint32_t ks = smem_u32(sm), vs = ks + uint32_t(C * KP) * 2;
   for (int i = r0 * VPR + int(threadIdx.x); i < r1 * VPR; i += kAttnThreads) {
     const int r = i / VPR, c = i % VPR;
     attn_cp16(ks + uint32_t(r * KP + c * 8) * 2, kb + r * HD + c * 8);
     attn_cp16(vs + uint32_t(r * KP + c * 8) * 2, vb + r * HD + c * 8);
   }
-}
-
-// Before the current position is known to be written: the item's rows of the
-// positions cached by earlier steps (t < pos).  attn_item(..., prefetched=true)
-// then copies only the rest.
-template <int HD>
-__device__ __forceinline__ void attn_prefetch(const AttnArgs& a, int g, int chunk, int pos, uint8_t* sm) {
-  const int t0 = chunk * a.chunk;
-  const int r1 = min(a.chunk, pos - t0);
-  if (r1 > 0) attn_copy_rows<HD>(a, g, t0, 0, r1, sm);
-  asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
 // Merge of the `used` chunks of query head j by one warp (lane holds HD/32
@@ -145,127 +173,226 @@ __device__ __forceinline__ void attn_combine_head(const AttnArgs& a, int j, int 
   }
 }
 
-// One item by the whole CTA (C = a.chunk, a compile-time copy).  n = cached
-// positions attended (pos + 1; the current one is already stored), used =
-// ceil(n / C) items of kv head g exist.  Scores: threads 2c and 2c+1 hold the
-// two halves of key c in registers and score it against every head (q read as
-// broadcast float4s; even and odd dimensions in the two lanes of packed f32x2
-// FMAs, added at the end).  P V: the CTA's threads are 2*kAttnThreads/HD
-// position slices x HD/2 dimension pairs (packed f32x2 FMAs on a pair); slice s
-// sums its contiguous share of the chunk for all G heads, and the slices are
-// added in order.  Every thread of the CTA must call it.
+
+// One item by the whole CTA: kv head g, chunk `chunk` of C positions; n =
+// positions attended (pos + 1: the current one is stored by now), used =
+// ceil(n / C) items of kv head g exist; rows [0, r_done) of the chunk are
+// already being copied (cp.async groups the CTA committed before).  Every
+// thread of the CTA must call it.  Returns true on the CTA that merged.
+//
+// Warp w scores key tiles w, w + 8, ... (8 keys each) against all heads; the
+// chunk maximum and sum per head go through shared memory; P (hi and lo rows)
+// is written to shared memory; warp w then forms output dimensions
+// [8 HD/64 w, 8 HD/64 (w+1)) over all keys.  Sums of the hi and lo rows, of the
+// per-warp softmax sums and of the k-steps run in a fixed order, so the result
+// does not depend on timing.
 template <int HD, int G, int C>
 __device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, int n, int used, uint8_t* sm,
-                                          bool prefetched) {
-  constexpr int KP = HD + 8, NS = 2 * kAttnThreads / HD;
-  __half* Ks = reinterpret_cast<__half*>(sm);
-  __half* Vs = Ks + C * KP;
-  float* qs = reinterpret_cast<float*>(Vs + C * KP);
-  float* S = qs + G * HD;                      // [G][C]
-  float* P = S + G * C;                        // [NS][G][HD]
-  int* flag = reinterpret_cast<int*>(P + NS * G * HD);
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int t0 = chunk * C;
-  const int cnt = min(C, n - t0);
-  const int pos = n - 1;
-  // every copy of the chunk issued before any is waited for: one memory latency
-  attn_copy_rows<HD>(a, g, t0, prefetched ? max(0, min(cnt, pos - t0)) : 0, cnt, sm);
+                                          int r_done) {
+  using Lay = AttnLayout<HD, G, C>;
+  constexpr int KP = Lay::KP, MT = Lay::MT, PP = Lay::PP, NW = kAttnWarps;
+  constexpr int KS = HD / 16;                          // k-steps of the scores (even)
+  constexpr int NTW = C / 8 / NW;                      // score tiles per warp
+  constexpr int NVW = HD / 8 / NW;                     // output tiles per warp (1 or 2)
+  constexpr int HPT = MT;                              // heads per thread: gi (and gi + 8)
+  static_assert(KS % 2 == 0 && NTW >= 1 && (NVW == 1 || NVW == 2) && C % 16 == 0, "attention tile shape");
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, gi = lane >> 2, tg = lane & 3;
+  const int t0 = chunk * C, cnt = min(C, n - t0);
+  const uint32_t ks = smem_u32(sm + Lay::kK), vs = smem_u32(sm + Lay::kV), ps = smem_u32(sm + Lay::kP);
+  float* red_max = reinterpret_cast<float*>(sm + Lay::kRed);
+  float* red_sum = red_max + NW * G;
+
+  // q of this thread's heads as hi/lo A fragments (loads first: the longest latency)
+  float2 qv[HPT][KS][2];
   {
-    const uint32_t qss = smem_u32(qs);
-    for (int i = t; i < G * HD / 4; i += kAttnThreads) attn_cp16(qss + i * 16, a.q + int64_t(g) * G * HD + i * 4);
-  }
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-  __syncthreads();
-
-  // ---- scores: two threads per key (measured faster than spreading a key over
-  // more threads when C < 256), each half of its dimensions ----
-  if (t < 2 * C) {
-    constexpr int TPK = 2, DPT = HD / TPK;
-    const int c = t / TPK, part = t % TPK;
-    float2 kf[DPT / 2];
-    const uint4* kr = reinterpret_cast<const uint4*>(Ks + c * KP + part * DPT);
+    const float* qb = a.q + int64_t(g) * G * HD;
 #pragma unroll
-    for (int i = 0; i < DPT / 8; i++) {
-      const uint4 v = kr[i];
-      const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+    for (int h = 0; h < HPT; h++) {
+      const int head = gi + 8 * h;
 #pragma unroll
-      for (int j = 0; j < 4; j++) kf[i * 4 + j] = __half22float2(h2[j]);
-    }
-#pragma unroll
-    for (int h = 0; h < G; h++) {
-      const float4* qh = reinterpret_cast<const float4*>(qs + h * HD + part * DPT);
-      float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);   // two chains: dimensions 8i..8i+3, 8i+4..8i+7
-#pragma unroll
-      for (int i = 0; i < DPT / 4; i += 2) {
-        const float4 qv = qh[i], qw = qh[i + 1];
-        a0 = __ffma2_rn(make_float2(qv.x, qv.y), kf[2 * i], a0);
-        a1 = __ffma2_rn(make_float2(qw.x, qw.y), kf[2 * i + 2], a1);
-        a0 = __ffma2_rn(make_float2(qv.z, qv.w), kf[2 * i + 1], a0);
-        a1 = __ffma2_rn(make_float2(qw.z, qw.w), kf[2 * i + 3], a1);
+      for (int kk = 0; kk < KS; kk++) {
+        if (head < G) {
+          qv[h][kk][0] = __ldcg(reinterpret_cast<const float2*>(qb + head * HD + kk * 16 + 2 * tg));
+          qv[h][kk][1] = __ldcg(reinterpret_cast<const float2*>(qb + head * HD + kk * 16 + 8 + 2 * tg));
+        } else {
+          qv[h][kk][0] = qv[h][kk][1] = make_float2(0.f, 0.f);
+        }
       }
-      float acc = __fadd_rn(__fadd_rn(a0.x, a0.y), __fadd_rn(a1.x, a1.y));
-#pragma unroll
-      for (int o = 1; o < TPK; o <<= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
-      if (part == 0) S[h * C + c] = c < cnt ? __fmul_rn(acc, a.scale) : -INFINITY;
     }
   }
+  // the rows not copied before the wait (the current position's)
+  attn_copy_rows<HD, C>(a, g, t0, r_done, cnt, sm);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  // V rows past cnt inside the last 16-key step enter P V with weight 0: make them finite
+  {
+    const int r1 = min(C, (cnt + 15) & ~15);
+    for (int i = cnt * (HD / 8) + t; i < r1 * (HD / 8); i += kAttnThreads) {
+      const int r = i / (HD / 8), c = i % (HD / 8);
+      *reinterpret_cast<uint4*>(sm + Lay::kV + size_t(r * KP + c * 8) * 2) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  uint32_t qa[MT][KS][4];
+#pragma unroll
+  for (int kk = 0; kk < KS; kk++) {
+    if (MT == 1) {   // rows gi (hi) and gi + 8 (lo) of one tile
+      split2(qv[0][kk][0].x, qv[0][kk][0].y, qa[0][kk][0], qa[0][kk][1]);
+      split2(qv[0][kk][1].x, qv[0][kk][1].y, qa[0][kk][2], qa[0][kk][3]);
+    } else {         // tile 0: hi of heads gi, gi + 8; tile 1: their lo
+      split2(qv[0][kk][0].x, qv[0][kk][0].y, qa[0][kk][0], qa[MT - 1][kk][0]);
+      split2(qv[HPT - 1][kk][0].x, qv[HPT - 1][kk][0].y, qa[0][kk][1], qa[MT - 1][kk][1]);
+      split2(qv[0][kk][1].x, qv[0][kk][1].y, qa[0][kk][2], qa[MT - 1][kk][2]);
+      split2(qv[HPT - 1][kk][1].x, qv[HPT - 1][kk][1].y, qa[0][kk][3], qa[MT - 1][kk][3]);
+    }
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
 
-  // ---- chunk softmax statistics (max, sum of exp), weights in place ---------
-  for (int h = warp; h < G; h += kAttnThreads / 32) {
+  // ---- scores of this warp's key tiles ---------------------------------------
+  const int nt_live = (cnt + 7) >> 3;
+  float s[HPT][NTW][2];
+#pragma unroll
+  for (int i = 0; i < NTW; i++) {
+    const int nt = warp + NW * i;
+    if (nt < nt_live) {   // warp-uniform
+      float acc[MT][4];
+#pragma unroll
+      for (int m = 0; m < MT; m++) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+      const uint32_t rowa = ks + uint32_t((nt * 8 + (lane & 7)) * KP + (lane >> 3) * 8) * 2;
+#pragma unroll
+      for (int kk = 0; kk < KS; kk += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(rowa + uint32_t(kk * 16) * 2, b0, b1, b2, b3);
+#pragma unroll
+        for (int m = 0; m < MT; m++) {
+          mma16816(acc[m], qa[m][kk], b0, b1);
+          mma16816(acc[m], qa[m][kk + 1], b2, b3);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 2; e++) {
+        const bool live = nt * 8 + 2 * tg + e < cnt;
+        const float v0 = MT == 1 ? __fadd_rn(acc[0][e], acc[0][e + 2]) : __fadd_rn(acc[0][e], acc[MT - 1][e]);
+        s[0][i][e] = live ? __fmul_rn(v0, a.scale) : -INFINITY;
+        if (HPT == 2) {
+          const float v1 = __fadd_rn(acc[0][e + 2], acc[MT - 1][e + 2]);
+          s[HPT - 1][i][e] = live ? __fmul_rn(v1, a.scale) : -INFINITY;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < HPT; h++) s[h][i][0] = s[h][i][1] = -INFINITY;
+    }
+  }
+  // per-warp maxima per head
+#pragma unroll
+  for (int h = 0; h < HPT; h++) {
     float mx = -INFINITY;
-    for (int c = lane; c < C; c += 32) mx = fmaxf(mx, S[h * C + c]);
 #pragma unroll
-    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float l = 0.f;
-    for (int c = lane; c < C; c += 32) {
-      const float e = c < cnt ? expf(S[h * C + c] - mx) : 0.f;
-      S[h * C + c] = e;
-      l = __fadd_rn(l, e);
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, o));
-    if (lane == 0) a.part_ml[int64_t(g * G + h) * a.n_chunks + chunk] = make_float2(mx, l);
+    for (int i = 0; i < NTW; i++) mx = fmaxf(mx, fmaxf(s[h][i][0], s[h][i][1]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const int head = gi + 8 * h;
+    if (tg == 0 && head < G) red_max[warp * G + head] = mx;
   }
   __syncthreads();
 
-  // ---- P V: slice s of the positions, dimension pair (2dp, 2dp+1) -------------------
+  // ---- exponentials against the chunk maximum; P rows to shared memory --------
+#pragma unroll
+  for (int h = 0; h < HPT; h++) {
+    const int head = gi + 8 * h;
+    float M = -INFINITY;
+    if (head < G) {
+#pragma unroll
+      for (int w = 0; w < NW; w++) M = fmaxf(M, red_max[w * G + head]);
+    }
+    float l = 0.f;
+#pragma unroll
+    for (int i = 0; i < NTW; i++) {
+      const int key = (warp + NW * i) * 8 + 2 * tg;
+      float p0 = 0.f, p1 = 0.f;
+      if (head < G) {
+        p0 = expf(s[h][i][0] - M);   // exp(-inf) = 0 past cnt
+        p1 = expf(s[h][i][1] - M);
+      }
+      l = __fadd_rn(l, __fadd_rn(p0, p1));
+      uint32_t hi, lo;
+      split2(p0, p1, hi, lo);
+      // MT == 1: row gi hi, row gi + 8 lo; MT == 2: rows head (hi) and 16 + head (lo)
+      const int rhi = MT == 1 ? gi : head, rlo = MT == 1 ? gi + 8 : 16 + head;
+      *reinterpret_cast<uint32_t*>(sm + Lay::kP + size_t(rhi * PP + key) * 2) = hi;
+      *reinterpret_cast<uint32_t*>(sm + Lay::kP + size_t(rlo * PP + key) * 2) = lo;
+    }
+    l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, 1));
+    l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, 2));
+    if (tg == 0 && head < G) red_sum[warp * G + head] = l;
+  }
+  __syncthreads();
+  if (t < G) {   // chunk statistics of head t, warps in order
+    float M = -INFINITY, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; w++) M = fmaxf(M, red_max[w * G + t]);
+#pragma unroll
+    for (int w = 0; w < NW; w++) L = __fadd_rn(L, red_sum[w * G + t]);
+    a.part_ml[int64_t(g * G + t) * a.n_chunks + chunk] = make_float2(M, L);
+  }
+
+  // ---- P V: this warp's output dimension tiles over the live key steps ---------
   {
-    const int dp = t % (HD / 2), s = t / (HD / 2);
-    const int span = C / NS;                   // positions per slice (a multiple of 4)
-    const int c_lo = s * span, c_hi = min(c_lo + span, cnt);
-    float2 acc[G];
+    const int kv_steps = (cnt + 15) >> 4;
+    float acc[MT][NVW][4];
 #pragma unroll
-    for (int h = 0; h < G; h++) acc[h] = make_float2(0.f, 0.f);
-    for (int c = c_lo; c < c_hi; c += 4) {     // weights past cnt are 0; rows past cnt are finite smem
-      float2 v[4];
+    for (int m = 0; m < MT; m++)
 #pragma unroll
-      for (int j = 0; j < 4; j++)
-        v[j] = c + j < cnt ? __half22float2(*reinterpret_cast<const __half2*>(Vs + (c + j) * KP + 2 * dp))
-                           : make_float2(0.f, 0.f);
+      for (int j = 0; j < NVW; j++) acc[m][j][0] = acc[m][j][1] = acc[m][j][2] = acc[m][j][3] = 0.f;
+    const int n0 = warp * NVW * 8;   // first output dimension of this warp
+    // A rows (lane & 7) + 8 ((lane >> 3) & 1), keys + 8 (lane >> 4); V rows likewise for .trans
+    const uint32_t pa = ps + uint32_t(((lane & 7) + 8 * ((lane >> 3) & 1)) * PP + 8 * (lane >> 4)) * 2;
+    // (with one dimension tile only lanes 0..15 address rows: keys 0..15 of the step)
+    const uint32_t va = vs + uint32_t(((lane & 7) + 8 * ((lane >> 3) & 1)) * KP + n0 + (NVW == 2 ? 8 * (lane >> 4) : 0)) * 2;
+#pragma unroll 4
+    for (int kv = 0; kv < kv_steps; kv++) {
+      uint32_t pf[MT][4];
 #pragma unroll
-      for (int h = 0; h < G; h++) {
-        const float4 w = *reinterpret_cast<const float4*>(S + h * C + c);
-        acc[h] = __ffma2_rn(make_float2(w.w, w.w), v[3], acc[h]);
-        acc[h] = __ffma2_rn(make_float2(w.z, w.z), v[2], acc[h]);
-        acc[h] = __ffma2_rn(make_float2(w.y, w.y), v[1], acc[h]);
-        acc[h] = __ffma2_rn(make_float2(w.x, w.x), v[0], acc[h]);
+      for (int m = 0; m < MT; m++)
+        ldsm_x4(pa + uint32_t(m * 16 * PP + kv * 16) * 2, pf[m][0], pf[m][1], pf[m][2], pf[m][3]);
+      if (NVW == 2) {   // two dimension tiles of one key step
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(va + uint32_t(kv * 16 * KP) * 2, b0, b1, b2, b3);
+#pragma unroll
+        for (int m = 0; m < MT; m++) {
+          mma16816(acc[m][0], pf[m], b0, b1);
+          mma16816(acc[m][NVW - 1], pf[m], b2, b3);
+        }
+      } else {          // one dimension tile
+        uint32_t b0, b1;
+        ldsm_x2_t(va + uint32_t(kv * 16 * KP) * 2, b0, b1);
+#pragma unroll
+        for (int m = 0; m < MT; m++) mma16816(acc[m][0], pf[m], b0, b1);
       }
     }
 #pragma unroll
-    for (int h = 0; h < G; h++) *reinterpret_cast<float2*>(P + (s * G + h) * HD + 2 * dp) = acc[h];
-  }
-  __syncthreads();
-  for (int i = t; i < G * HD; i += kAttnThreads) {
-    float o = P[i];
+    for (int h = 0; h < HPT; h++) {
+      const int head = gi + 8 * h;
+      if (head >= G) continue;
+      float* po = a.part_o + (int64_t(g * G + head) * a.n_chunks + chunk) * HD + n0 + 2 * tg;
 #pragma unroll
-    for (int s = 1; s < NS; s++) o = __fadd_rn(o, P[s * G * HD + i]);
-    const int h = i / HD, d = i % HD;
-    a.part_o[(int64_t(g * G + h) * a.n_chunks + chunk) * HD + d] = o;
+      for (int j = 0; j < NVW; j++) {
+        float o0, o1;
+        if (MT == 1) {
+          o0 = __fadd_rn(acc[0][j][0], acc[0][j][2]);
+          o1 = __fadd_rn(acc[0][j][1], acc[0][j][3]);
+        } else {
+          o0 = __fadd_rn(acc[0][j][2 * h], acc[MT - 1][j][2 * h]);
+          o1 = __fadd_rn(acc[0][j][2 * h + 1], acc[MT - 1][j][2 * h + 1]);
+        }
+        *reinterpret_cast<float2*>(po + 8 * j) = make_float2(o0, o1);
+      }
+    }
   }
 
   // ---- the CTA that finishes kv head g's last chunk merges its heads --------
   // (the CTA barrier orders every thread's partials before thread 0's fence)
+  int* flag = reinterpret_cast<int*>(sm + Lay::kFlag);
   __syncthreads();
   if (t == 0) {
     __threadfence();
@@ -274,10 +401,8 @@ __device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, i
     __threadfence();
   }
   __syncthreads();
-  const bool last = *flag;
-  __syncthreads();   // the flag slot is free again before any later item writes it
-  if (!last) return false;
-  for (int h = warp; h < G; h += kAttnThreads / 32) attn_combine_head<HD>(a, g * G + h, used, lane);
+  if (!*flag) return false;
+  for (int h = warp; h < G; h += NW) attn_combine_head<HD>(a, g * G + h, used, lane);
   if (t == 0) a.tickets[g] = 0u;
   return true;
 }

@@ -50,18 +50,21 @@ __global__ void k_embed(const QMat e, const int32_t* __restrict__ d_token, float
 // are final before that GEMV starts, so they are copied before waiting for it;
 // q and the current position's K and V only after.
 template <int HD, int G, int C>
-__global__ void __launch_bounds__(kAttnThreads) k_attn(const __grid_constant__ AttnArgs a,
+__global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const __grid_constant__ AttnArgs a,
                                                        const int32_t* __restrict__ d_pos) {
   extern __shared__ uint4 smem_u4[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(smem_u4);
   const int n = __ldcg(d_pos) + 1;
-  const int used = (n + a.chunk - 1) / a.chunk;
+  const int used = (n + C - 1) / C;
   // the O projection may start its weight prefetch; it waits for this grid before reading its output
   asm volatile("griddepcontrol.launch_dependents;");
   if (int(blockIdx.y) >= used) return;
-  attn_prefetch<HD>(a, blockIdx.x, blockIdx.y, n - 1, sm);
+  const int t0 = int(blockIdx.y) * C;
+  const int r_done = max(0, min(C, n - 1 - t0));   // rows of positions cached by earlier steps
+  attn_copy_rows<HD, C>(a, blockIdx.x, t0, 0, r_done, sm);
+  asm volatile("cp.async.commit_group;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  attn_item<HD, G, C>(a, blockIdx.x, blockIdx.y, n, used, sm, true);
+  attn_item<HD, G, C>(a, blockIdx.x, blockIdx.y, n, used, sm, r_done);
 }
 
 // Greedy choice over the per-CTA top-2 summaries of the output GEMV (ties to the
@@ -290,10 +293,16 @@ struct Launcher {
   }
 };
 
+constexpr size_t kAttnMinSmem = 116 * 1024;   // more than half of an SM's shared memory
+
 template <int HD, int G>
 static cudaError_t launch_attn_t(dim3 grid, cudaStream_t s, const AttnArgs& a, const int32_t* pos, bool pdl) {
   auto kern = a.chunk == 64 ? k_attn<HD, G, 64> : (a.chunk == 128 ? k_attn<HD, G, 128> : k_attn<HD, G, 256>);
-  const size_t smem = attn_item_smem(HD, G, a.chunk);
+  size_t smem = a.chunk == 64 ? AttnLayout<HD, G, 64>::kBytes
+                              : (a.chunk == 128 ? AttnLayout<HD, G, 128>::kBytes : AttnLayout<HD, G, 256>::kBytes);
+  // one item per SM: the block scheduler would otherwise pack several small items
+  // onto the first SMs the Q/K/V GEMV frees instead of spreading them
+  if (smem < kAttnMinSmem) smem = kAttnMinSmem;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;

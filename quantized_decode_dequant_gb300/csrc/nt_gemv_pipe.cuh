@@ -42,7 +42,7 @@
 
 namespace nt {
 
-constexpr int kPipeWarps = 8;                 // 256 threads per CTA
+constexpr int kPipeWarps = 16;                // 512 threads per CTA, one CTA per SM
 constexpr int kPipeMaxSmem = 221 * 1024;      // dynamic shared memory a CTA may ask for
 constexpr int kPipeSmPerSm = 228 * 1024;      // shared memory of an SM (each resident CTA also reserves 1 KB)
 // Staged x per 32 columns, in int8 slices of fixed point t = round(x/sx):
@@ -364,7 +364,7 @@ __device__ __forceinline__ float pipe_dot(const uint8_t* blk, int lane, const XB
 }
 
 // Copy cursor of one warp over its tiles.  Every lane issues the same copies
-// for every tile, so there are no divergent branches: its 16 (or 32) code bytes
+// for every tile, so there are no divergent branches: 16 (or twice 16) code bytes
 // of each of the R rows (a row past the matrix copies zero bytes, src-size 0,
 // from a valid address, so its products are zero) and its share of the rows'
 // scale pieces (16-byte pieces, and 4-byte ones for Q6_K's d; a lane without a
@@ -408,7 +408,7 @@ struct PipeCursor {
       map_row(a, grp * R + (r < nlive ? r : 0), sg, lr);
       seg[r] = sg;
       e[r] = lr * a.seg[0].cols + a.col0;
-      code[r] = P::code_base(a.seg[sg], e[r]) + lane * P::CB;
+      code[r] = P::code_base(a.seg[sg], e[r]) + lane * 16;
       csz[r] = r < nlive ? 16u : 0u;
     }
     // piece slot k of this lane: piece p = lane + 32k of the group's R rows; a slot
@@ -471,9 +471,12 @@ struct PipeCursor {
       if (ISSUE) {
 #pragma unroll
         for (int r = 0; r < R; r++) {
-          const uint32_t d = dst + uint32_t(r * P::RB + lane * P::CB);
+          // lane l copies bytes [16 l, 16 l + 16) of the row's codes (and, with 32
+          // code bytes per unit, [512 + 16 l, ...)): each copy instruction of the
+          // warp reads 512 contiguous bytes, whole 32-byte sectors
+          const uint32_t d = dst + uint32_t(r * P::RB + lane * 16);
           cp16z(d, code[r], csz[r]);
-          if (P::CB == 32) cp16z(d + 16, code[r] + 16, csz[r]);
+          if (P::CB == 32) cp16z(d + 512, code[r] + 512, csz[r]);
         }
 #pragma unroll
         for (int k = 0; k < NA; k++) cp16(dst + aoff[k], asrc[k]);
@@ -536,13 +539,12 @@ template <int FMT, int R, int S, int SLICE = 0>
 __device__ __forceinline__ void pipe_prologue_w(const GemvArgs& a, int64_t nrows, const WarpTiles& w, uint8_t* ring) {
   pipe_issue_w<FMT, R, S, SLICE>(a, nrows, w, ring, 0, S - 1);
 }
-template <int FMT, int R, int S, int NW, int SLICE = 0>
-__device__ __forceinline__ void pipe_prologue(const GemvArgs& a, int64_t nrows, int cta, int ncta, uint8_t* ring) {
-  const WarpTiles w = warp_tiles(nrows, R, int(a.ncols / 1024), threadIdx.x >> 5, NW, cta, ncta);
-  pipe_prologue_w<FMT, R, S, SLICE>(a, nrows, w, ring);
-}
-
-// Converts one lane's eight elements of a 32-column block (see stage_pass).
+// Converts one lane's eight elements of a 32-column block: columns
+// [256 p, 256 p + 256) of the window are eight blocks, four lanes per block,
+// eight consecutive elements per lane.  Per block: sx = max|x|/T (T = 32512 or
+// 520192), t = round(x/sx) split into the slices, the sums T0, T1 of t over
+// elements 0..15 and 16..31, and the sum of squares (each lane's eight in
+// element order, then the four lanes as (l0 + l1) + (l2 + l3)).
 template <int FMT, int XS>
 __device__ __forceinline__ void stage_convert(float4 f0, float4 f1, int p, uint8_t* xq) {
   using P = Pipe<FMT>;
@@ -591,27 +593,6 @@ __device__ __forceinline__ void stage_convert(float4 f0, float4 f1, int p, uint8
   if (q == 0)
     *reinterpret_cast<uint4*>(dst + 32 * XS) =
         make_uint4(__float_as_uint(amax / float(kT)), uint32_t(t01), uint32_t(t_hi), __float_as_uint(sq));
-}
-
-// Stages eight 32-column blocks of x (columns [256 p, 256 p + 256) of the
-// window starting at x) as fixed point in XS int8 slices, four lanes of the
-// calling warp per block, eight consecutive elements per lane.  Per block:
-// sx = max|x|/T (T = 32512 or 520192), t = round(x/sx) split into the slices,
-// the sums T0, T1 of t over elements 0..15 and 16..31, and the sum of squares
-// (each lane's eight in element order, then the four lanes as (l0 + l1) +
-// (l2 + l3)); every kernel stages the same way.
-template <int FMT, int XS>
-__device__ __forceinline__ void stage_pass(const float* x, int p, uint8_t* xq) {
-  const int lane = threadIdx.x & 31;
-  const float4* src = reinterpret_cast<const float4*>(x + size_t(p) * 256 + lane * 8);
-  stage_convert<FMT, XS>(__ldcg(src), __ldcg(src + 1), p, xq);
-}
-
-// Stages 1024-column tile k of x (four passes) by the calling warp.
-template <int FMT, int XS>
-__device__ __forceinline__ void stage_tile(const float* x, int k, uint8_t* xq) {
-#pragma unroll
-  for (int i = 0; i < 4; i++) stage_pass<FMT, XS>(x, k * 4 + i, xq);
 }
 
 // RMSNorm factor rsqrt(mean(x^2) + eps) from the staged per-block squares,
@@ -670,24 +651,18 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xq, F betwee
   __syncthreads();
 }
 
-// Hooks of the GEMV body for a caller that staged all of x before the loop.
-struct StagedHooks {
-  static constexpr bool kAllStaged = true;
-  template <int FMT, int XS>
-  __device__ __forceinline__ void tile(const GemvArgs&, uint8_t*, int) {}
-  __device__ __forceinline__ void group_done(const GemvArgs&, int64_t, int) {}
-};
-
-// The GEMV of this CTA's share after its prologue: the tile loop (resuming the
-// copy cursor S-1 tiles in), row-group epilogues and, for EPI_LOGITS, the CTA's
-// top-2 summary in a.epi.top2[cta].  With StagedHooks x is already staged and
-// `scale` holds the RMS factor; otherwise the hooks stage tile k before its
-// first use (H::tile) and the factor is formed at the first epilogue, and each
-// finished row group is reported (H::group_done).  Every thread of the CTA must
-// call it (EPI_LOGITS ends with a CTA barrier).
-template <int FMT, int R, int S, int EPI, int NW, int SLICE, class H>
+// The GEMV of the calling warp's groups after its first S-1 tiles were issued:
+// the tile loop (resuming the copy cursor S-1 tiles in), row-group epilogues
+// and, for EPI_LOGITS, the CTA's top-2 summary in a.epi.top2[cta].  x is staged
+// in xq and `scale` is the RMS factor.  Operands are read one tile ahead: the
+// next tile's codes, scales and x block come from shared memory while the
+// cursor issues copies, before they are used.  last: the launch's final loop
+// (it writes the EPI_LOGITS summary).  Every thread of the CTA must call it
+// (EPI_LOGITS ends with a CTA barrier).
+template <int FMT, int R, int S, int EPI, int NW, int SLICE>
 __device__ __forceinline__ void pipe_loop_w(const GemvArgs& a, int64_t nrows, const WarpTiles& w, int cta,
-                                            uint8_t* xq, uint8_t* ring, float scale, H& hooks) {
+                                            uint8_t* xq, uint8_t* ring, float scale, bool last = true) {
+  static_assert(S >= 3, "the loop keeps one tile's operands ahead");
   using P = Pipe<FMT>;
   constexpr int XS = x_slices(EPI), XU = x_unit<XS>();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -703,115 +678,48 @@ __device__ __forceinline__ void pipe_loop_w(const GemvArgs& a, int64_t nrows, co
   float acc[R];
 #pragma unroll
   for (int r = 0; r < R; r++) acc[r] = 0.f;
-  int known = H::kAllStaged ? kiters : 0;   // tiles [0, known) are staged
-  bool have_scale = H::kAllStaged;
-
   int64_t c_grp = w.g0;
   int c_it = 0;
   const uint8_t* rd = wring;                               // slot of the tile being decoded
   const uint8_t* const rd_end = wring + S * R * P::RB;
   const uint8_t* xp = xq + size_t(lane) * XU;             // this lane's x block of the tile
-  if constexpr (H::kAllStaged && S >= 3) {
-    // Operands one tile ahead: the next tile's codes, scales and x block are read
-    // from shared memory while the cursor issues copies, before they are used.
-    typename P::Frag fr[R];
-    XBlock xb;
-    if (w.ntiles > 0) {
-      cp_wait<S - 2>();   // tile 0 has landed
-      __syncwarp();
-#pragma unroll
-      for (int r = 0; r < R; r++) P::load(rd + r * P::RB, lane, fr[r]);
-      load_xblock<XS>(xp, xb);
-    }
-#pragma unroll 1
-    for (int t = 0; t < w.ntiles; t++) {
-#pragma unroll
-      for (int r = 0; r < R; r++) acc[r] = __fadd_rn(acc[r], P::template compute<XS>(fr[r], lane, xb));   // dead rows read zeros
-      rd += R * P::RB;
-      if (rd == rd_end) rd = wring;
-      xp += 32 * XU;
-      if (++c_it == kiters) {
-        // ---- row group done: transposed warp reduction, epilogue ------------
-        c_it = 0;
-        xp = xq + size_t(lane) * XU;
-        float kk = warp_reduce_rows<R>(acc, lane);
-#pragma unroll
-        for (int r = 0; r < R; r++) acc[r] = 0.f;
-        kk = __fmul_rn(kk, scale);
-        epilogue<R, EPI>(a, c_grp, nrows, lane, kk, best, best_i, second);
-        c_grp += w.stride;
-      }
-      cp_wait<S - 3>();   // tile t + 1 has landed
-      __syncwarp();       // ... every lane's copies; the slot of tile t - 1 is free
-#pragma unroll
-      for (int r = 0; r < R; r++) P::load(rd + r * P::RB, lane, fr[r]);
-      load_xblock<XS>(xp, xb);
-      cur.template step<true>(a, nrows, lane);   // tile t + S - 1
-    }
-    cp_wait<0>();
+  typename P::Frag fr[R];
+  XBlock xb;
+  if (w.ntiles > 0) {
+    cp_wait<S - 2>();   // tile 0 has landed
     __syncwarp();
-    if (EPI == EPI_LOGITS) cta_top2<NW>(a, cta, best, best_i, second);
-    return;
+#pragma unroll
+    for (int r = 0; r < R; r++) P::load(rd + r * P::RB, lane, fr[r]);
+    load_xblock<XS>(xp, xb);
   }
 #pragma unroll 1
   for (int t = 0; t < w.ntiles; t++) {
-    cp_wait<S - 2>();     // this lane's copies of the tile have landed
-    __syncwarp();         // ... and every lane's (scales are copied by a few lanes); the previous slot is free
-    cur.template step<true>(a, nrows, lane);
-    if (!H::kAllStaged && c_it >= known) {
-      hooks.template tile<FMT, XS>(a, xq, c_it);
-      known = c_it + 1;
-    }
-    XBlock xb;
-    load_xblock<XS>(xp, xb);
-    xp += 32 * XU;
 #pragma unroll
-    for (int r = 0; r < R; r++) acc[r] = __fadd_rn(acc[r], pipe_dot<FMT, XS>(rd + r * P::RB, lane, xb));   // dead rows read zeros
+    for (int r = 0; r < R; r++) acc[r] = __fadd_rn(acc[r], P::template compute<XS>(fr[r], lane, xb));   // dead rows read zeros
     rd += R * P::RB;
     if (rd == rd_end) rd = wring;
-    if (++c_it < kiters) continue;
-
-    // ---- row group done: transposed warp reduction, epilogue ----------------
-    c_it = 0;
-    xp = xq + size_t(lane) * XU;
-    float kk = warp_reduce_rows<R>(acc, lane);
+    xp += 32 * XU;
+    if (++c_it == kiters) {
+      // ---- row group done: transposed warp reduction, epilogue ------------
+      c_it = 0;
+      xp = xq + size_t(lane) * XU;
+      float kk = warp_reduce_rows<R>(acc, lane);
 #pragma unroll
-    for (int r = 0; r < R; r++) acc[r] = 0.f;
-    if (!have_scale) {
-      scale = x_scale<XS>(a, xq);
-      have_scale = true;
+      for (int r = 0; r < R; r++) acc[r] = 0.f;
+      kk = __fmul_rn(kk, scale);
+      epilogue<R, EPI>(a, c_grp, nrows, lane, kk, best, best_i, second);
+      c_grp += w.stride;
     }
-    kk = __fmul_rn(kk, scale);
-    epilogue<R, EPI>(a, c_grp, nrows, lane, kk, best, best_i, second);
-    hooks.group_done(a, c_grp, int(nrows - c_grp * R < R ? nrows - c_grp * R : R));
-    c_grp += w.stride;
+    cp_wait<S - 3>();   // tile t + 1 has landed
+    __syncwarp();       // ... every lane's copies; the slot of tile t - 1 is free
+#pragma unroll
+    for (int r = 0; r < R; r++) P::load(rd + r * P::RB, lane, fr[r]);
+    load_xblock<XS>(xp, xb);
+    cur.template step<true>(a, nrows, lane);   // tile t + S - 1
   }
   cp_wait<0>();
   __syncwarp();
-  if (EPI == EPI_LOGITS) cta_top2<NW>(a, cta, best, best_i, second);
-}
-
-template <int FMT, int R, int S, int EPI, int NW, int SLICE, class H>
-__device__ __forceinline__ void pipe_loop(const GemvArgs& a, int64_t nrows, int cta, int ncta, uint8_t* xq,
-                                          uint8_t* ring, float scale, H& hooks) {
-  const WarpTiles w = warp_tiles(nrows, R, int(a.ncols / 1024), threadIdx.x >> 5, NW, cta, ncta);
-  pipe_loop_w<FMT, R, S, EPI, NW, SLICE>(a, nrows, w, cta, xq, ring, scale, hooks);
-}
-
-// The per-launch body: stage all of x, then the loop.  TRIGGER: signal
-// programmatic dependents after staging.
-template <int FMT, int R, int S, int EPI, int NW, bool TRIGGER, int SLICE = 0>
-__device__ __forceinline__ void pipe_body(const GemvArgs& a, int64_t nrows, int cta, int ncta, uint8_t* xq,
-                                          uint8_t* ring) {
-  stage_x<FMT, NW, x_slices(EPI)>(a, xq);
-  const float scale = x_scale<x_slices(EPI)>(a, xq);
-  if (TRIGGER) {
-    // the next kernel may start its own weight prefetch on SMs this grid frees;
-    // it waits for this grid to finish before it reads anything this grid writes
-    asm volatile("griddepcontrol.launch_dependents;");
-  }
-  StagedHooks h;
-  pipe_loop<FMT, R, S, EPI, NW, SLICE>(a, nrows, cta, ncta, xq, ring, scale, h);
+  if (EPI == EPI_LOGITS && last) cta_top2<NW>(a, cta, best, best_i, second);
 }
 
 template <int FMT, int R, int S, int EPI, int NW>
@@ -832,8 +740,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe(const __grid_con
   // the next kernel may start its own weight prefetch on SMs this grid frees;
   // it waits for this grid to finish before it reads anything this grid writes
   asm volatile("griddepcontrol.launch_dependents;");
-  StagedHooks h;
-  pipe_loop_w<FMT, R, S, EPI, NW, 0>(a, nrows, w, blockIdx.x, xq, ring, scale, h);
+  pipe_loop_w<FMT, R, S, EPI, NW, 0>(a, nrows, w, blockIdx.x, xq, ring, scale);
 }
 
 // Two GEMVs over the same x in one launch: rows [0, n1) of a1 in format F1 and
@@ -875,10 +782,9 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe2(const __grid_co
   });
   const float scale = x_scale<XS>(a1, xq);
   asm volatile("griddepcontrol.launch_dependents;");
-  StagedHooks h;
-  pipe_loop_w<F1, R, S1, EPI, NW, SLICE>(a1, n1, w1, blockIdx.x, xq, ring, scale, h);
+  pipe_loop_w<F1, R, S1, EPI, NW, SLICE>(a1, n1, w1, blockIdx.x, xq, ring, scale, false);
   if (w1.ntiles && w2.ntiles) pipe_prologue_w<F2, R, S2, SLICE>(a2, n2, w2, ring);
-  pipe_loop_w<F2, R, S2, EPI, NW, SLICE>(a2, n2, w2, blockIdx.x, xq, ring, scale, h);
+  pipe_loop_w<F2, R, S2, EPI, NW, SLICE>(a2, n2, w2, blockIdx.x, xq, ring, scale);
 }
 
 inline size_t pipe_x_bytes(int64_t cols, int epi) {
@@ -948,38 +854,26 @@ cudaError_t launch_gemv_pipe_rs(const GemvArgs& a, int epi, cudaStream_t s, bool
   return cudaErrorInvalidValue;
 }
 
-// Instantiated shapes: 8 warps per CTA with S in {2, 3, 4, 6, 8} (R = 2) or
-// {2, 4} (R = 4); 16 warps per CTA (one CTA per SM) with S in {3, 4, 6, 8}
+// Instantiated shapes: 16 warps per CTA (one CTA per SM) with S in {3, 4, 6, 8}
 // (R = 2) or {3, 4} (R = 4).  S is rounded down to the nearest instantiated depth.
 template <int FMT>
-cudaError_t launch_gemv_pipe_fmt(const GemvArgs& a, int epi, int R, int S, int NW, cudaStream_t s, bool pdl,
+cudaError_t launch_gemv_pipe_fmt(const GemvArgs& a, int epi, int R, int S, cudaStream_t s, bool pdl,
                                  int* grid_used) {
-  if (NW == 16) {
-    if (R == 4) {
-      if (S >= 4) return launch_gemv_pipe_rs<FMT, 4, 4, 16>(a, epi, s, pdl, grid_used);
-      return launch_gemv_pipe_rs<FMT, 4, 3, 16>(a, epi, s, pdl, grid_used);
-    }
-    if (S >= 8) return launch_gemv_pipe_rs<FMT, 2, 8, 16>(a, epi, s, pdl, grid_used);
-    if (S >= 6) return launch_gemv_pipe_rs<FMT, 2, 6, 16>(a, epi, s, pdl, grid_used);
-    if (S >= 4) return launch_gemv_pipe_rs<FMT, 2, 4, 16>(a, epi, s, pdl, grid_used);
-    return launch_gemv_pipe_rs<FMT, 2, 3, 16>(a, epi, s, pdl, grid_used);
-  }
   if (R == 4) {
-    if (S >= 4) return launch_gemv_pipe_rs<FMT, 4, 4, 8>(a, epi, s, pdl, grid_used);
-    return launch_gemv_pipe_rs<FMT, 4, 2, 8>(a, epi, s, pdl, grid_used);
+    if (S >= 4) return launch_gemv_pipe_rs<FMT, 4, 4, kPipeWarps>(a, epi, s, pdl, grid_used);
+    return launch_gemv_pipe_rs<FMT, 4, 3, kPipeWarps>(a, epi, s, pdl, grid_used);
   }
-  if (S >= 8) return launch_gemv_pipe_rs<FMT, 2, 8, 8>(a, epi, s, pdl, grid_used);
-  if (S >= 6) return launch_gemv_pipe_rs<FMT, 2, 6, 8>(a, epi, s, pdl, grid_used);
-  if (S >= 4) return launch_gemv_pipe_rs<FMT, 2, 4, 8>(a, epi, s, pdl, grid_used);
-  if (S >= 3) return launch_gemv_pipe_rs<FMT, 2, 3, 8>(a, epi, s, pdl, grid_used);
-  return launch_gemv_pipe_rs<FMT, 2, 2, 8>(a, epi, s, pdl, grid_used);
+  if (S >= 8) return launch_gemv_pipe_rs<FMT, 2, 8, kPipeWarps>(a, epi, s, pdl, grid_used);
+  if (S >= 6) return launch_gemv_pipe_rs<FMT, 2, 6, kPipeWarps>(a, epi, s, pdl, grid_used);
+  if (S >= 4) return launch_gemv_pipe_rs<FMT, 2, 4, kPipeWarps>(a, epi, s, pdl, grid_used);
+  return launch_gemv_pipe_rs<FMT, 2, 3, kPipeWarps>(a, epi, s, pdl, grid_used);
 }
 
 // Q4_K rows of a1 and Q6_K rows of a2 over one x (see k_gemv_pipe2), 16 warps
 // per CTA, one CTA per SM, the ring depths that fit beside x.
 template <int EPI>
 cudaError_t launch_gemv_pipe2_q4k_q6k(const GemvArgs& a1, const GemvArgs& a2, cudaStream_t s, bool pdl) {
-  constexpr int NW = 16, S1 = 8, S2 = 6;
+  constexpr int NW = kPipeWarps, S1 = 8, S2 = 6;
   auto kern = k_gemv_pipe2<NT_Q4_K, NT_Q6_K, S1, S2, EPI, NW>;
   constexpr size_t slice = pipe_slice<NT_Q4_K, 2, S1, 0>() > pipe_slice<NT_Q6_K, 2, S2, 0>()
                                ? pipe_slice<NT_Q4_K, 2, S1, 0>()
@@ -1008,7 +902,7 @@ cudaError_t launch_gemv_pipe2_q4k_q6k(const GemvArgs& a1, const GemvArgs& a2, cu
 }
 
 #define NT_DECLARE_GEMV_PIPE(NAME) \
-  cudaError_t NAME(const GemvArgs& a, int epi, int R, int S, int NW, cudaStream_t s, bool pdl, int* grid_used);
+  cudaError_t NAME(const GemvArgs& a, int epi, int R, int S, cudaStream_t s, bool pdl, int* grid_used);
 NT_DECLARE_GEMV_PIPE(launch_gemv_pipe_q8_0)
 NT_DECLARE_GEMV_PIPE(launch_gemv_pipe_q4_0)
 NT_DECLARE_GEMV_PIPE(launch_gemv_pipe_q4_k)

@@ -5,8 +5,8 @@ namespace nt {
 cudaError_t launch_gemv_q5_k(const GemvArgs& a, int epi, int R, cudaStream_t s, bool pdl, int* grid_used) {
   return launch_gemv_fmt<NT_Q5_K>(a, epi, R, s, pdl, grid_used);
 }
-cudaError_t launch_gemv_pipe_q5_k(const GemvArgs& a, int epi, int R, int S, int NW, cudaStream_t s, bool pdl,
+cudaError_t launch_gemv_pipe_q5_k(const GemvArgs& a, int epi, int R, int S, cudaStream_t s, bool pdl,
                                   int* grid_used) {
-  return launch_gemv_pipe_fmt<NT_Q5_K>(a, epi, R, S, NW, s, pdl, grid_used);
+  return launch_gemv_pipe_fmt<NT_Q5_K>(a, epi, R, S, s, pdl, grid_used);
 }
 }  // namespace nt
