@@ -1,20 +1,26 @@
 """Benchmark of the batch-1 quantized Llama decode step on GB300.
 
-Default workload: Llama-3.1-8B-shaped model, Q8_0 weights (8.0 GB) resident in
-HBM, f16 KV cache prefilled to context 512, greedy decode.  One step = one
-decode step (every kernel of the hot path).  Prints one JSON line (rank 0).
+Default workload: Llama-3.1-70B-shaped model, Q4_K_M-style weight mix (45.7 GB
+of weights read per token) resident in HBM, f16 KV cache prefilled to context
+4096, greedy decode.  One step = one decode step (every kernel of the hot
+path).  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload llama8b_q8_0|llama70b_q4_k_m|llama70b_q6_k_streamed|tiny]
-                  [--no-sweep] [--no-cpu-baseline] [--profile-gemv FMT ROWS COLS LAUNCHES]
+                  [--workload llama70b_q4_k_m|llama8b_q8_0|llama70b_q6_k_streamed|tiny]
+                  [--no-sweep] [--no-extras] [--no-cpu-baseline] [--profile-gemv FMT ROWS COLS LAUNCHES]
 
 value: tokens/s over the K timed steps, device-timed (CUDA events on the
 launching stream around a device-resident greedy loop; inputs already in HBM).
 e2e: tokens/s through nt_decode_step with the token copied host->device and
-the result device->host every step.  Inputs (8 GB of weights) are larger than
-L2 (129 MB), so no flush is needed between steps.
---impl reference times the oracle (the C reference restatement) on the host
-cores on a bounded sample of the same workload.
+the result device->host every step.  Weights are far larger than L2 (129 MB),
+so no flush is needed between steps.
+After the main model is freed, rank 0 also measures (unless turned off): the
+isolated dequant-GEMV sweep at the 70B layer shapes in five formats, the 8B Q8_0
+decode step, and the 70B Q6_K step with 54 of 80 layers streamed from
+page-locked host memory.
+--impl reference times the oracle (the C restatement of the method) on one
+host core, each step one decode step of the same architecture truncated to one
+layer; tokens/s are projected to the whole model by weight+KV bytes.
 With N > 1 (torchrun) every rank runs an independent replica (the step does
 not shard); value = all ranks' tokens / max over ranks of the time.
 """
@@ -41,12 +47,13 @@ PAGES_8B_Q8_0_TOK_S = 48.9   # RTX 3090, Llama 8B Q8_0 (hada "Roadmap", Phase 1)
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=256)
+    p.add_argument("--steps", type=int, default=128)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="llama8b_q8_0",
+    p.add_argument("--workload", default="llama70b_q4_k_m",
                    choices=["llama8b_q8_0", "llama70b_q4_k_m", "llama70b_q6_k_streamed", "tiny"])
     p.add_argument("--no-sweep", action="store_true")
+    p.add_argument("--no-extras", action="store_true", help="skip the 8B and streamed-70B extra measurements")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--profile-gemv", nargs=4, metavar=("FMT", "ROWS", "COLS", "LAUNCHES"))
     p.add_argument("--layer-skip", type=int, default=0, metavar="MAX",
@@ -66,6 +73,10 @@ def parse_args(argv=None):
 # ---------------------------------------------------------------- workloads --
 
 def workload(name: str):
+    return dict(_workload(name), key=name)
+
+
+def _workload(name: str):
     from quantized_decode_dequant_gb300 import workloads as W
     if name == "llama8b_q8_0":
         return dict(spec=W.LLAMA_8B_Q8_0, ctx=W.LLAMA_8B_CTX, resident=None,
@@ -189,33 +200,54 @@ def job_throughput(units_per_rank: int, world: int, max_seconds: float) -> float
 
 # ------------------------------------------------------------ CPU baseline --
 
-def cpu_baseline(wl, min_seconds: float = 10.0, max_steps: int = 64, threads: int | None = None) -> dict:
-    """The oracle on the host cores, on a sample of the workload: the same
-    architecture truncated to one layer, decoded from the same prefilled context
-    for about `min_seconds` (at least 2 steps, at most `max_steps`); its
-    per-token time is scaled to the full model by weight + KV bytes."""
-    import oracle
-    from quantized_decode_dequant_gb300 import workloads as W
-    spec = dict(wl["spec"])
-    threads = threads or os.cpu_count() or 1
-    sample = dict(spec, n_layers=1, max_ctx=wl["ctx"] + max_steps + 1)
-    m = oracle.Model(oracle.ModelSpec(**sample, seed=W.SEED_WEIGHTS), nthreads=threads)
-    m.kv_prefill(wl["ctx"], W.SEED_KV)
-    tok = oracle.token(W.SEED_PROMPT, oracle.UID_TOKENS, 0, spec["vocab"])
-    t0 = time.perf_counter()
-    sample_steps = 0
-    while sample_steps < max_steps and (sample_steps < 2 or time.perf_counter() - t0 < min_seconds):
-        _, tok, _ = m.decode_step(tok)
-        sample_steps += 1
-    dt = (time.perf_counter() - t0) / sample_steps
-    m.close()
-    full = W.weight_bytes(spec) + W.kv_bytes(spec, wl["ctx"])
-    part = W.weight_bytes(sample) + W.kv_bytes(sample, wl["ctx"])
-    sec_per_tok = dt * full / part
-    return {"value": 1.0 / sec_per_tok, "unit": "tok/s", "cores": threads, "kind": "oracle",
-            "sample": (f"{sample_steps} oracle decode steps of the same architecture truncated to 1 layer "
-                       f"(ctx {wl['ctx']}), {dt:.2f} s/step, scaled to the full model by weight+KV bytes "
-                       f"({full / part:.1f}x)"),
+class OracleSample:
+    """The oracle on one layer of the workload: the same architecture truncated
+    to one decoder layer (plus the embedding and the output head), weights
+    generated and quantized with every host thread when it is built (outside
+    any timed region), KV cache prefilled to the workload's context, then timed
+    on ONE host thread -- the single-core baseline.  A full token's time is
+    projected from a sample step by weight+KV bytes (the oracle's time is
+    proportional to the bytes it dequantizes)."""
+
+    def __init__(self, wl, n_steps: int):
+        import oracle
+        from quantized_decode_dequant_gb300 import workloads as W
+        spec = dict(wl["spec"])
+        self.sample = dict(spec, n_layers=1, max_ctx=max(wl["ctx"], 1) + n_steps + 2)
+        self.model = oracle.Model(oracle.ModelSpec(**self.sample, seed=W.SEED_WEIGHTS),
+                                  nthreads=os.cpu_count() or 1)
+        self.model.set_threads(1)
+        if wl["ctx"] > 0:
+            self.model.kv_prefill(wl["ctx"], W.SEED_KV)
+        self.tok = oracle.token(W.SEED_PROMPT, oracle.UID_TOKENS, 0, spec["vocab"])
+        full = W.weight_bytes(spec) + W.kv_bytes(spec, wl["ctx"])
+        part = W.weight_bytes(self.sample) + W.kv_bytes(self.sample, wl["ctx"])
+        self.scale = full / part
+
+    def step(self) -> float:
+        t0 = time.perf_counter()
+        _, self.tok, _ = self.model.decode_step(self.tok)
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.model.close()
+
+
+def cpu_baseline(wl, n_steps: int = 3) -> dict:
+    """Single-core oracle on a bounded sample of the workload (OracleSample):
+    n_steps one-layer decode steps, each about 1-5 s on one core."""
+    smp = OracleSample(wl, n_steps)
+    try:
+        times = [smp.step() for _ in range(n_steps)]
+    finally:
+        smp.close()
+    dt = statistics.median(times)
+    return {"value": 1.0 / (dt * smp.scale), "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "sample": (f"{n_steps} oracle decode steps of the architecture truncated to 1 decoder layer "
+                       f"(ctx {wl['ctx']}, embedding and output head included) on one host thread: "
+                       f"median {dt:.3f} s per sample step, measured; value = 1 / (that x {smp.scale:.1f}), "
+                       f"the full model's weight+KV bytes over the sample's"),
+            "sample_s_per_step": round(dt, 4), "projection_factor": round(smp.scale, 2),
             "gemv": oracle_gemv_rates()}
 
 
@@ -241,55 +273,54 @@ def oracle_gemv_rates(rows_sample: int = 64) -> dict:
 
 
 def run_reference(args, wl, rank, world, dist):
+    """The oracle as the reference arm: W warm-up and K timed sample steps
+    (OracleSample, one host thread); ms_per_step is the measured time of a
+    sample step, value the projected whole-model tokens/s."""
     if rank != 0:
         return
-    import oracle
-    from quantized_decode_dequant_gb300 import workloads as W
-    spec = wl["spec"]
-    threads = os.cpu_count() or 1
-    sample = dict(spec, n_layers=1, max_ctx=wl["ctx"] + args.steps + args.warmup + 2)
-    m = oracle.Model(oracle.ModelSpec(**sample, seed=W.SEED_WEIGHTS), nthreads=threads)
-    m.kv_prefill(wl["ctx"], W.SEED_KV)
-    tok = oracle.token(W.SEED_PROMPT, oracle.UID_TOKENS, 0, spec["vocab"])
-    for _ in range(args.warmup):
-        _, tok, _ = m.decode_step(tok)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        _, tok, _ = m.decode_step(tok)
-    dt = (time.perf_counter() - t0) / args.steps
-    full = W.weight_bytes(spec) + W.kv_bytes(spec, wl["ctx"])
-    part = W.weight_bytes(sample) + W.kv_bytes(sample, wl["ctx"])
-    value = 1.0 / (dt * full / part)
+    smp = OracleSample(wl, args.steps + args.warmup)
+    try:
+        for _ in range(args.warmup):
+            smp.step()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            smp.step()
+        dt = (time.perf_counter() - t0) / args.steps
+    finally:
+        smp.close()
+    value = 1.0 / (dt * smp.scale)
+    sample = (f"each step: one oracle decode step of the architecture truncated to 1 decoder layer "
+              f"(ctx {wl['ctx']}, embedding and output head included) on one host thread, measured "
+              f"({dt * 1e3:.1f} ms); value = 1 / (step time x {smp.scale:.1f}), the full model's "
+              f"weight+KV bytes over the sample's")
     line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": dt * full / part * 1e3, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": wl["label"], "parallelism": "replicas only"},
-            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": threads, "kind": "oracle",
-                             "sample": (f"each step: one oracle decode step of the architecture truncated to "
-                                        f"1 layer, scaled to the full model by weight+KV bytes ({full / part:.1f}x)")},
+            "projection": {"measured_s_per_sample_step": dt, "factor": smp.scale,
+                           "projected_s_per_token": dt * smp.scale},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 def per_kernel_launches(spec) -> int:
     """Kernels of one step on the per-kernel launch path: embedding, per layer the
-    QKV GEMV (two when v has its own format), attention, O, gate/up and down
-    GEMVs, then the output GEMV and the argmax."""
-    split_v = spec.get("t_v", "q8_0") != spec.get("t_q", "q8_0")
-    return 1 + spec["n_layers"] * (5 + int(split_v)) + 2
+    QKV GEMV (two launches when v has its own format and no two-format kernel
+    takes the pair: a Q4_K q/k with a Q6_K v at widths of whole 1024-column
+    tiles is one launch), attention, O, gate/up and down GEMVs, then the output
+    GEMV and the argmax."""
+    tq, tv = spec.get("t_q", "q8_0"), spec.get("t_v", "q8_0")
+    pair = tq == "q4_k" and tv == "q6_k" and spec["hidden"] % 1024 == 0
+    return 1 + spec["n_layers"] * (5 + int(tq != tv and not pair)) + 2
 
 
-def step_traffic(wl, step_bytes):
-    """DRAM bytes of one step-kernel launch: no ncu capture of it is recorded."""
-    return None
-
-
-# DRAM bytes (read + write) per algorithmic byte of the GEMV kernel, from the ncu
-# capture summarised in profiles/k_gemv_pipe_q8_0_57344x4096.md, and the SHA-256 of
-# the kernel sources that capture was taken on: a changed kernel reports no traffic.
-GEMV_DRAM_PER_BYTE = (249.623040 + 3.790336) / (57344 * 4096 * 1.0625 + 4 * (57344 + 4096)) * 1e6
+# DRAM bytes (read + write) per algorithmic byte of the step's GEMV launches, per
+# workload, from the ncu captures summarised in profiles/, and the SHA-256 of the
+# kernel sources they were taken on: a changed kernel reports no traffic.
+GEMV_DRAM_PER_BYTE: dict[str, float] = {}
 GEMV_SOURCES = ("nt_gemv_pipe.cuh", "nt_gemv.cuh")
-GEMV_SOURCES_SHA256 = "a8bbdf30332938854bc53e1e385230532b8e489bc0d50e7fa851d7227503427a"
+GEMV_SOURCES_SHA256 = ""
 
 
 def gemv_sources_sha256() -> str:
@@ -301,10 +332,11 @@ def gemv_sources_sha256() -> str:
     return h.hexdigest()
 
 
-def gemv_traffic(bytes_per_launch: float):
-    if gemv_sources_sha256() != GEMV_SOURCES_SHA256:
+def gemv_traffic(bytes_per_launch: float, wl):
+    ratio = GEMV_DRAM_PER_BYTE.get(wl.get("key", ""))
+    if ratio is None or gemv_sources_sha256() != GEMV_SOURCES_SHA256:
         return None
-    return round(bytes_per_launch * GEMV_DRAM_PER_BYTE)
+    return round(bytes_per_launch * ratio)
 
 
 # ------------------------------------------------------------------ GEMV --
@@ -368,23 +400,23 @@ def profile_gemv(nt, torch, fmt: str, rows: int, cols: int, launches: int):
 
 # ------------------------------------------------------------------ ours --
 
-def run_ours(args, wl, rank, world, local, dist):
-    import torch
+DTYPE = ("weights as block codes; GEMV: codes x activations in 16-bit fixed point per 32-column block "
+         "(19-bit into the Q/K/V GEMV), exact int32 DP4A dot products, fp32 block scales and accumulation; "
+         "attention: f16 KV cache, f16 hi+lo tensor-core products with fp32 accumulation, fp32 softmax")
 
-    from quantized_decode_dequant_gb300 import nt, workloads as W
-    torch.cuda.set_device(local)
-    nt.lib()
-    if args.profile_gemv:
-        fmt, r, c, n = args.profile_gemv
-        profile_gemv(nt, torch, fmt, int(r), int(c), int(n))
-        return
-    spec = dict(wl["spec"], max_ctx=max_ctx_for(wl, args.steps, args.warmup))
-    cfg = nt.make_config(**spec, seed=W.SEED_WEIGHTS)
-    m = nt.nt_model_create(cfg)
-    peaks = measured_peaks()
-    props = torch.cuda.get_device_properties(local)
-    l2 = int(getattr(props, "L2_cache_size", 0) or 0) or (126 << 20)
+
+def measure(nt, torch, wl, steps: int, warmup: int, args, dist, world: int, local: int, peaks: dict,
+            primary: bool) -> dict:
+    """One model of workload wl: W warm-up steps, K timed steps (device-timed
+    greedy loop on the device for resident models; per-step nt_decode_step
+    calls, layer copies inside, for streamed ones), the same K steps end to end
+    through nt_decode_step, per-class device times and the roofline of the
+    step's GEMV launches.  The model is freed before it returns."""
+    from quantized_decode_dequant_gb300 import workloads as W
+    spec = dict(wl["spec"], max_ctx=max_ctx_for(wl, steps, warmup))
+    m = nt.nt_model_create(nt.make_config(**spec, seed=W.SEED_WEIGHTS))
     stream = torch.cuda.current_stream()
+    out = {}
     try:
         tok0 = _prompt_token(spec["vocab"])
         streamed = wl["resident"] is not None
@@ -398,35 +430,33 @@ def run_ours(args, wl, rank, world, local, dist):
                 nt.nt_kv_reset(m)
 
         skip_info = None
-        if args.layer_skip > 0:
+        if primary and args.layer_skip > 0:
             skip_info = calibrate_skip(nt, m, reset, tok0, spec, args.layer_skip, args.skip_threshold)
 
         # ---- warm-up
         reset()
         if streamed:
             t = tok0
-            for _ in range(args.warmup):
+            for _ in range(warmup):
                 t = nt.nt_decode_step(m, t)
         else:
-            nt.nt_decode_run(m, tok0, args.warmup, stream)
+            nt.nt_decode_run(m, tok0, warmup, stream)
         torch.cuda.synchronize()
 
-        # ---- timed: device-resident greedy loop (streamed: per-step calls, copies inside)
+        # ---- timed
         reset()
         clocks = ClockSampler(local)
-        h2d_stats = None
-        spec_stats = None
         n_draft = args.draft_layers if args.draft_layers is not None else (
             wl["resident"] if streamed else spec["n_layers"] // 4)
         with clocks:
             barrier(dist)
             torch.cuda.synchronize()
-            if args.speculative:
+            if primary and args.speculative:
                 # cycles until `steps` tokens are emitted; each cycle copies the
                 # host-tier layers once for up to K tokens
                 t0 = time.perf_counter()
                 t, emitted, cycles, accepted, h2d_b = tok0, 0, 0, 0, 0.0
-                while emitted < args.steps:
+                while emitted < steps:
                     e, j = nt.nt_speculative_step(m, t, n_draft, args.speculative)
                     t = e[-1]
                     emitted += len(e)
@@ -434,17 +464,18 @@ def run_ours(args, wl, rank, world, local, dist):
                     accepted += j
                     h2d_b += nt.nt_get_stats(m).h2d_bytes
                 torch.cuda.synchronize()
-                sec = (time.perf_counter() - t0) * args.steps / emitted
-                spec_stats = {"k": args.speculative, "draft_layers": n_draft, "cycles": cycles,
-                              "tokens": emitted, "tokens_per_cycle": round(emitted / cycles, 3),
-                              "accepted_per_cycle": round(accepted / cycles, 3),
-                              "h2d_GB_per_token": round(h2d_b / emitted / 1e9, 3),
-                              "note": "acceptance is meaningless on random weights; the cycle cost is the measurement"}
+                sec = (time.perf_counter() - t0) * steps / emitted
+                out["speculative"] = {"k": args.speculative, "draft_layers": n_draft, "cycles": cycles,
+                                      "tokens": emitted, "tokens_per_cycle": round(emitted / cycles, 3),
+                                      "accepted_per_cycle": round(accepted / cycles, 3),
+                                      "h2d_GB_per_token": round(h2d_b / emitted / 1e9, 3),
+                                      "note": "acceptance is meaningless on random weights; the cycle cost is "
+                                              "the measurement"}
             elif streamed:
                 t0 = time.perf_counter()
                 t = tok0
                 h2d_b = h2d_ms = comp_ms = ov = 0.0
-                for _ in range(args.steps):
+                for _ in range(steps):
                     t = nt.nt_decode_step(m, t)
                     st = nt.nt_get_stats(m)
                     h2d_b += st.h2d_bytes
@@ -453,119 +484,149 @@ def run_ours(args, wl, rank, world, local, dist):
                     ov += st.overlap
                 torch.cuda.synchronize()
                 sec = time.perf_counter() - t0
-                h2d_stats = {"h2d_GB_s": h2d_b / (h2d_ms * 1e-3) / 1e9 if h2d_ms else None,
-                             "h2d_GB_per_step": h2d_b / args.steps / 1e9, "overlap": ov / args.steps,
-                             "compute_ms_per_step": comp_ms / args.steps,
-                             "pcie_gen5_x16_nominal_GB_s": 64.0}
+                out["streaming"] = {
+                    "resident_layers": wl["resident"], "streamed_layers": spec["n_layers"] - wl["resident"],
+                    "h2d_GB_s": round(h2d_b / (h2d_ms * 1e-3) / 1e9, 1) if h2d_ms else None,
+                    "h2d_GB_per_step": round(h2d_b / steps / 1e9, 3), "overlap": round(ov / steps, 4),
+                    "compute_ms_per_step": round(comp_ms / steps, 3),
+                    "pcie_gen5_x16_nominal_GB_s": 64.0, "link": host_link(local),
+                    "h2d_timing": "copy-stream CUDA events around each layer's copy"}
             else:
                 ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 ev0.record(stream)
-                nt.nt_decode_run(m, tok0, args.steps, stream)
+                nt.nt_decode_run(m, tok0, steps, stream)
                 ev1.record(stream)
                 torch.cuda.synchronize()
                 sec = ev0.elapsed_time(ev1) * 1e-3
             barrier(dist)
         sec_max = reduce_max(dist, sec)
-        value = job_throughput(args.steps, world, sec_max)
-        ms_per_step = sec_max / args.steps * 1e3
-        tokens = None if streamed else nt.nt_get_tokens(m, wl["ctx"], min(args.steps, 8)).tolist()
+        out["value"] = job_throughput(steps, world, sec_max)
+        out["ms_per_step"] = sec_max / steps * 1e3
+        out["clocks"] = clocks.summary()
+        out["first_tokens"] = None if streamed else nt.nt_get_tokens(m, max(wl["ctx"], 0), min(steps, 8)).tolist()
 
-        # ---- e2e through the public call with host token in / result out every step
-        reset()
-        barrier(dist)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        t = tok0
-        for _ in range(args.steps):
-            t = nt.nt_decode_step(m, t)
-        e2e_sec = reduce_max(dist, time.perf_counter() - t0)
-        e2e = {"value": job_throughput(args.steps, world, e2e_sec), "unit": "tok/s",
-               "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 8}
+        # ---- e2e through the public call, host token in / result out every step
+        # (a streamed step already runs through nt_decode_step: its timed loop is the e2e one)
+        if streamed:
+            e2e_value = out["value"]
+        else:
+            reset()
+            barrier(dist)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            t = tok0
+            for _ in range(steps):
+                t = nt.nt_decode_step(m, t)
+            e2e_value = job_throughput(steps, world, reduce_max(dist, time.perf_counter() - t0))
+        out["e2e"] = {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 8}
 
-        # ---- per-class device times: event pairs around every launch, or the
-        # step kernel's per-phase clock stamps (one launch per step)
-        roofline = None
-        kt = None
-        kernel_classes = None
+        # ---- per-class device times (event pair around every launch) and the roofline
         stats = nt.nt_get_stats(m)
-        step_bytes = stats.weight_bytes + stats.kv_bytes_per_pos * (wl["ctx"] + args.steps / 2)
+        step_bytes = stats.weight_bytes + stats.kv_bytes_per_pos * (wl["ctx"] + steps / 2)
         if skip_info:   # skipped layers' weights and cache are not read
             frac_kv = 1.0 - skip_info["n_skipped"] / spec["n_layers"]
             step_bytes = (stats.weight_bytes - skip_info["weight_bytes_saved_per_token"]
-                          + stats.kv_bytes_per_pos * frac_kv * (wl["ctx"] + args.steps / 2))
+                          + stats.kv_bytes_per_pos * frac_kv * (wl["ctx"] + steps / 2))
+            out["layer_skip"] = skip_info
+        out["step_roofline"] = {"bytes_per_step": step_bytes,
+                                "achieved_GB_s": round(step_bytes / (out["ms_per_step"] * 1e-3) / 1e9, 1),
+                                "frac": round(step_bytes / (out["ms_per_step"] * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                                "peak_GB_s": peaks["hbm_gbs"]}
         if not streamed:
             reset()
-            n_prof = max(4, min(args.steps, 32))
+            n_prof = max(4, min(steps, 32))
             kt = nt.nt_profile_steps(m, tok0, n_prof)
-            step_kernel = kt.kernel_launches == n_prof
-            if step_kernel:
-                # the whole step is one kernel: its launch duration is the timed step
-                achieved = step_bytes / (ms_per_step * 1e-3) / 1e9
-                roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                            "traffic": step_traffic(wl, step_bytes),
-                            "kernel": "k_step (persistent decode step: all GEMVs, attention, argmax)",
-                            "peak_source": peaks["source"], "bytes_per_launch": round(step_bytes),
-                            "launches_per_step": 1, "us_per_launch": round(ms_per_step * 1e3, 3),
-                            "timing": "CUDA events around the timed greedy loop on the launching stream"}
-            else:
-                # the dominant kernel: the step's GEMV launches replayed on their own, back to back
-                reset()
-                g_ms, g_bytes, g_n = nt.nt_profile_gemvs(m, 8)
-                achieved = g_bytes / (g_ms * 1e-3) / 1e9
-                roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                            "traffic": gemv_traffic(g_bytes),
-                            "kernel": "k_gemv_pipe (fused dequant-GEMV: every GEMV launch of a step, "
-                                      "graph-replayed back to back with programmatic dependent launch)",
-                            "peak_source": peaks["source"], "bytes_per_launch": round(g_bytes),
-                            "launches_per_step": g_n, "us_per_launch": round(g_ms * 1e3, 3),
-                            "timing": "CUDA events around 8 replays of the GEMV graph on the launching stream"}
-            unit = "phases_per_step" if step_kernel else "launches_per_step"
-            kernel_classes = {name: {unit: kt.launches[c] // n_prof,
-                                     "ms_per_step": round(kt.ms[c] / n_prof, 4),
-                                     "GB_s": round(kt.bytes[c] / (kt.ms[c] * 1e-3) / 1e9, 1) if kt.ms[c] else None}
-                              for name, c in (("gemv", nt.KC_GEMV), ("attention", nt.KC_ATTN),
-                                              ("other", nt.KC_OTHER))}
-            kernel_classes["profiled_step_ms"] = round(kt.step_ms, 4)
-            kernel_classes["source"] = ("step kernel: SM clock of CTA 0 at every grid barrier" if step_kernel
-                                        else "CUDA event pair around every launch")
-        step_roofline = {"bytes_per_step": step_bytes,
-                         "achieved_GB_s": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
-                         "frac": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
-        sweep = None
-        if not args.no_sweep and rank == 0 and wl["spec"]["n_layers"] <= 32:
-            nt.nt_model_destroy(m)
-            m = None
-            sweep = gemv_sweep(nt, torch, peaks["hbm_gbs"], l2)
-        cpu = None
-        if rank == 0 and not args.no_cpu_baseline:
-            cpu = cpu_baseline(wl)
+            out["gpu_launches"] = int(kt.kernel_launches // n_prof * steps)
+            out["kernel_classes"] = {
+                name: {"launches_per_step": kt.launches[c] // n_prof, "ms_per_step": round(kt.ms[c] / n_prof, 4),
+                       "GB_s": round(kt.bytes[c] / (kt.ms[c] * 1e-3) / 1e9, 1) if kt.ms[c] else None}
+                for name, c in (("gemv", nt.KC_GEMV), ("attention", nt.KC_ATTN), ("other", nt.KC_OTHER))}
+            out["kernel_classes"]["profiled_step_ms"] = round(kt.step_ms, 4)
+            out["kernel_classes"]["source"] = "CUDA event pair around every launch (no overlap between launches)"
+            # the dominant kernel: the step's GEMV launches replayed on their own, back to back
+            reset()
+            g_ms, g_bytes, g_n = nt.nt_profile_gemvs(m, 8)
+            achieved = g_bytes / (g_ms * 1e-3) / 1e9
+            out["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                               "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                               "traffic": gemv_traffic(g_bytes, wl),
+                               "kernel": "k_gemv_pipe (fused dequant-GEMV: every GEMV launch of a step, "
+                                         "graph-replayed back to back with programmatic dependent launch)",
+                               "peak_source": peaks["source"], "bytes_per_launch": round(g_bytes),
+                               "launches_per_step": g_n, "us_per_launch": round(g_ms * 1e3, 3),
+                               "timing": "CUDA events around 8 replays of the GEMV graph on the launching stream"}
+        else:
+            out["gpu_launches"] = per_kernel_launches(wl["spec"]) * steps
     finally:
-        if m is not None:
-            nt.nt_model_destroy(m)
+        nt.nt_model_destroy(m)
+    return out
 
+
+def host_link(local: int) -> str:
+    """How the GPU reaches host memory: NVLink-C2C on Grace systems, else PCIe."""
+    try:
+        r = subprocess.run(["nvidia-smi", "-q", "-i", str(local)], capture_output=True, text=True, timeout=20)
+        txt = r.stdout
+    except (OSError, subprocess.SubprocessError):
+        return "unknown"
+    if "C2C" in txt or "c2c" in txt:
+        return "NVLink-C2C"
+    for line in txt.splitlines():
+        if "PCIe Generation" in line or "Link Width" in line:
+            return "PCIe"
+    return "unknown"
+
+
+def run_ours(args, wl, rank, world, local, dist):
+    import torch
+
+    from quantized_decode_dequant_gb300 import nt, workloads as W
+    torch.cuda.set_device(local)
+    nt.lib()
+    if args.profile_gemv:
+        fmt, r, c, n = args.profile_gemv
+        profile_gemv(nt, torch, fmt, int(r), int(c), int(n))
+        return
+    peaks = measured_peaks()
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 0) or (126 << 20)
+    main_m = measure(nt, torch, wl, args.steps, args.warmup, args, dist, world, local, peaks, primary=True)
+    sweep = cpu = None
+    extras = {}
+    if rank == 0:
+        if not args.no_sweep:
+            sweep = gemv_sweep(nt, torch, peaks["hbm_gbs"], l2)
+        plain = (args.layers is None and args.resident is None and not args.layer_skip and not args.speculative
+                 and args.workload == "llama70b_q4_k_m")
+        if plain and not args.no_extras:
+            for name, steps, warm in (("llama8b_q8_0", W.LLAMA_8B_STEPS, 5),
+                                      ("llama70b_q6_k_streamed", W.LLAMA_70B_Q6_K_STEPS, 3)):
+                x = measure(nt, torch, workload(name), steps, warm, args, None, 1, local, peaks, primary=False)
+                keep = ("value", "ms_per_step", "e2e", "step_roofline", "roofline", "streaming", "clocks")
+                extras[name] = dict({k: x[k] for k in keep if k in x}, unit="tok/s", steps=steps, warmup=warm,
+                                    workload=workload(name)["label"])
+        if not args.no_cpu_baseline:
+            cpu = cpu_baseline(wl)
     if rank != 0:
         return
+    value = main_m["value"]
     line = {"metric": METRIC, "value": round(value, 3), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": round(main_m["ms_per_step"], 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": round(value / wl["vs"], 3) if wl["vs"] else None,
-            "dtype": "q8_0/q4_k/q6_k weights, f32 math, f16 KV" if wl["spec"].get("t_q", "q8_0") != "q8_0"
-            else "q8_0 weights, f32 math, f16 KV",
+            "dtype": DTYPE,
             "data": "synthetic (seeded N(0,0.02) weights quantized on device; N(0,1) f16 KV prefill)",
             "config": {"workload": wl["label"], "model": "llama", "global_batch": 1, "seq_len": wl["ctx"],
                        "parallelism": "replicas only" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (weights > 4x L2), no flush"},
-            "roofline": roofline, "step_roofline": step_roofline, "kernel_classes": kernel_classes, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": int(kt.kernel_launches // max(1, n_prof) * args.steps) if kt is not None
-            else per_kernel_launches(wl["spec"]) * args.steps,
-            "clocks": clocks.summary(), "first_tokens": tokens}
-    if h2d_stats:
-        line["streaming"] = h2d_stats
-    if skip_info:
-        line["layer_skip"] = skip_info
-    if spec_stats:
-        line["speculative"] = spec_stats
+            "roofline": main_m.get("roofline"), "step_roofline": main_m["step_roofline"],
+            "kernel_classes": main_m.get("kernel_classes"), "cpu_baseline": cpu, "e2e": main_m["e2e"],
+            "gpu_launches": main_m["gpu_launches"], "clocks": main_m["clocks"],
+            "first_tokens": main_m["first_tokens"]}
+    for k in ("streaming", "layer_skip", "speculative"):
+        if k in main_m:
+            line[k] = main_m[k]
+    if extras:
+        line["extras"] = extras
     if sweep:
         line["gemv_sweep"] = sweep
         line["gemv_sweep_min_frac"] = min(s["frac"] for s in sweep)

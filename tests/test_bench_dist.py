@@ -80,3 +80,22 @@ def test_two_gloo_ranks_take_the_slowest_time(tmp_path):
         assert o["world"] == 2
         assert o["max"] == 4.0
         assert o["value"] == pytest.approx(64 * 2 / 4.0)
+
+
+def test_reference_arm_line_is_a_measured_single_core_sample(capsys):
+    """The reference arm times the oracle on one host thread: ms_per_step is the
+    measured time of one sample step (so ms_per_step x steps fits the run) and
+    value is that time projected to the whole model by weight+KV bytes."""
+    import time
+    args = bench.parse_args(["--impl", "reference", "--steps", "2", "--warmup", "1", "--workload", "tiny"])
+    t0 = time.perf_counter()
+    bench.run_reference(args, bench.workload("tiny"), 0, 1, None)
+    wall = time.perf_counter() - t0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["cpu_baseline"]["cores"] == 1
+    assert line["ms_per_step"] * line["steps"] / 1e3 <= wall
+    proj = line["projection"]
+    assert abs(proj["measured_s_per_sample_step"] * 1e3 - line["ms_per_step"]) < 1e-6
+    assert abs(line["value"] * proj["measured_s_per_sample_step"] * proj["factor"] - 1.0) < 1e-9
+    assert proj["factor"] > 1.0     # the tiny model's two layers, sampled with one
+    assert line["e2e"]["value"] == line["value"]

@@ -201,7 +201,7 @@ def test_llama8b_q8_0_teacher_forced(nt, W):
         gl = np.empty(spec["vocab"], np.float32)
         tok = oracle.token(W.SEED_PROMPT, oracle.UID_TOKENS, 0, spec["vocab"])
         worst = (0.0, 0.0)
-        for i in range(int(os.environ.get("NT_8B_STEPS", "3"))):
+        for i in range(int(os.environ.get("NT_8B_STEPS", "16"))):
             gnx = nt.nt_decode_step(m, tok, gl)
             ol, onx, omg = om.decode_step(tok)
             e = _check_step(gl, gnx, ol, onx, omg, i)
@@ -210,6 +210,67 @@ def test_llama8b_q8_0_teacher_forced(nt, W):
         print(f"8B worst over {i + 1} steps: max-abs {worst[0]:.3e} rel-L2 {worst[1]:.3e}")
     finally:
         nt.nt_model_destroy(m)
+
+
+def _teacher_forced(nt, m, om, spec, ctx, steps, W, where, also=None):
+    """Prefilled context ctx on both sides, the prompt token, then the GPU's own
+    greedy tokens fed to both; logits checked at every step.  also(m2): a second
+    device model stepped alongside that must give bit-identical logits."""
+    nt.nt_kv_prefill(m, ctx, W.SEED_KV)
+    om.kv_prefill(ctx, W.SEED_KV)
+    if also is not None:
+        nt.nt_kv_prefill(also, ctx, W.SEED_KV)
+    gl = np.empty(spec["vocab"], np.float32)
+    al = np.empty(spec["vocab"], np.float32)
+    tok = oracle.token(W.SEED_PROMPT, oracle.UID_TOKENS, 0, spec["vocab"])
+    worst = (0.0, 0.0)
+    for i in range(steps):
+        gnx = nt.nt_decode_step(m, tok, gl)
+        if also is not None:
+            anx = nt.nt_decode_step(also, tok, al)
+            np.testing.assert_array_equal(gl.view(np.uint32), al.view(np.uint32))
+            assert anx == gnx
+        ol, onx, omg = om.decode_step(tok)
+        e = _check_step(gl, gnx, ol, onx, omg, (where, i))
+        worst = (max(worst[0], e[0]), max(worst[1], e[1]))
+        tok = gnx
+    print(f"{where}: worst over {steps} steps max-abs {worst[0]:.3e} rel-L2 {worst[1]:.3e}")
+    return worst
+
+
+def test_llama70b_widths_q4_k_m_4_layers_ctx4096(nt, W):
+    """The 70B Q4_K_M workload's kernels at full width with 4 layers: 8192-wide
+    two-format Q/K/V launch (Q4_K q/k, Q6_K v), 64/8 heads attended over 4097+
+    cached positions in 256-position items, four-rows-per-warp Q4_K O and
+    gate/up, Q6_K down and 128256-row Q6_K head; ctx 4096, 4 teacher-forced steps."""
+    spec = dict(W.LLAMA_70B_Q4_K_M, n_layers=4)
+    m = nt.nt_model_create(nt.make_config(**spec, seed=W.SEED_WEIGHTS))
+    om = oracle.Model(oracle.ModelSpec(**spec, seed=W.SEED_WEIGHTS), nthreads=os.cpu_count() or 8)
+    try:
+        _teacher_forced(nt, m, om, spec, W.LLAMA_70B_Q4_K_M_CTX, 4, W, "70B-width Q4_K_M 4 layers")
+    finally:
+        om.close()
+        nt.nt_model_destroy(m)
+
+
+def test_llama70b_widths_q6_k_2_resident_2_streamed_ctx1024(nt, W):
+    """The streamed 70B Q6_K workload's path at full width with 4 layers, 2 of
+    them copied from page-locked host memory into the staging buffers every step
+    (so the pipeline GEMVs read staging buffers): against the oracle, and bit for
+    bit against the same model held resident; ctx 1024, 3 teacher-forced steps."""
+    spec = dict(W.LLAMA_70B_Q6_K, n_layers=4)
+    cfg = nt.make_config(**spec, seed=W.SEED_WEIGHTS)
+    stm, res = nt.nt_model_create(cfg), nt.nt_model_create(cfg)
+    om = oracle.Model(oracle.ModelSpec(**spec, seed=W.SEED_WEIGHTS), nthreads=os.cpu_count() or 8)
+    try:
+        nt.nt_stream_layers(stm, 2, 2)
+        _teacher_forced(nt, stm, om, spec, W.LLAMA_70B_Q6_K_CTX, 3, W, "70B-width Q6_K 2+2 streamed", also=res)
+        st = nt.nt_get_stats(stm)
+        assert st.n_resident == 2 and st.h2d_bytes > 0
+    finally:
+        om.close()
+        nt.nt_model_destroy(stm)
+        nt.nt_model_destroy(res)
 
 
 @pytest.mark.slow

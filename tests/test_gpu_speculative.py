@@ -67,7 +67,9 @@ def test_speculative_stream_equals_greedy_and_the_oracle(nt, n_draft, k, residen
         assert nxt == _greedy(nt, cfg, 9, len(stream) + 1, prefill)[-1]
     finally:
         nt.nt_model_destroy(m)
-    # the oracle's cycles (exact while its greedy margins stay above the near-tie bar)
+    # the oracle's cycles.  Cycles are exact only while every greedy margin is above
+    # the near-tie bar; seed 12 with this prefill and token keeps all of them above
+    # 0.02 for 50 steps (checked with the oracle), so the comparison always runs.
     ospec = oracle.ModelSpec(**SPEC, seed=12)
     want = oracle.speculative_cycles(ospec, n_draft, k, 9, 6, prefill=prefill, nthreads=os.cpu_count() or 8)
     om = oracle.Model(ospec, nthreads=os.cpu_count() or 8)
@@ -77,8 +79,8 @@ def test_speculative_stream_equals_greedy_and_the_oracle(nt, n_draft, k, residen
         _, t, mg = om.decode_step(t)
         margins.append(mg)
     om.close()
-    if min(margins) > MARGIN:
-        assert cycles == [(list(e), j) for e, j in want]
+    assert min(margins) > MARGIN, margins
+    assert cycles == [(list(e), j) for e, j in want]
 
 
 def test_streamed_verification_copies_each_layer_once_per_cycle(nt):
