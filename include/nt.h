@@ -302,9 +302,10 @@ nt_status nt_gemv_q(const nt_qtensor* t, const float* dev_x, float* dev_y, void*
 /* ------------------------------------------------ allocation-free variant -- */
 
 /* y = W x as nt_gemv_q, then the index of the largest y (ties to the lowest
- * row) into dev_index and the gap between the largest and second-largest y
- * into dev_margin (both device pointers, 4-byte aligned; dev_index is -1 when
- * no y is finite).  The pages have no counterpart: this entry point exists for
+ * row; NaN values are never selected) into dev_index and the gap between the
+ * largest and second-largest y into dev_margin (both device pointers, 4-byte
+ * aligned).  dev_index is -1 only when every y is NaN; dev_margin is +inf when
+ * a single y is not NaN, and NaN when the two largest are both +inf.  The pages have no counterpart: this entry point exists for
  * callers that cannot allocate device memory on this path, such as embedders
  * whose device memory is all reserved by their own allocator, or latency-bound
  * loops that cannot afford the implicit synchronisation of cudaMalloc/cudaFree.
@@ -312,7 +313,10 @@ nt_status nt_gemv_q(const nt_qtensor* t, const float* dev_x, float* dev_y, void*
  * file-scope device array of 1024 x 16 bytes (16 KiB) that every GPU loading
  * this library holds until the process exits.  The first call on a device, with
  * that device current, looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * (cudaGetSymbolAddress) and keeps it for the life of the process; make that
+ * first call before any stream capture, and make no call on a device after a
+ * cudaDeviceReset of it (the reset unloads the array and the kept address goes
+ * stale).
  * Every call shares the array and overwrites what it reads, so nothing needs
  * clearing, but calls that overlap on the GPU (for example on two streams at
  * once) race on it: serialise them.  Asynchronous on stream.

@@ -36,8 +36,6 @@
 // tile is whole and every scale piece an aligned 16-byte (4-byte for Q6_K d) copy.
 #pragma once
 
-#include <type_traits>
-
 #include "nt_gemv.cuh"
 
 namespace nt {
@@ -96,12 +94,14 @@ __device__ __forceinline__ void load_xblock(const uint8_t* p, XBlock& x) {
   x.t1 = int(m.z);
 }
 
-// Exact integer dot of codes and t: int with two slices, 64-bit with three
-// (4096 * (codes . h) can pass 2^31 for 8-bit codes).
+// Exact integer dot of codes and t over at most 32 elements, in int32 for both
+// slice counts: the largest sum is 32 x 127 x 520192 = 2,114,060,288 (8-bit codes,
+// three slices), and with |h| <= 127 the partial 4096 (codes . h) and the added
+// 16 (codes . m) + (codes . l) stay below 2^31 - 1 as well.  (A 64-bit sum would
+// convert to float on the FP64 pipe, which is narrow on this GPU.)
 template <int XS>
-using xacc_t = typename std::conditional<XS == 3, long long, int>::type;
+using xacc_t = int;
 __device__ __forceinline__ float xacc_f(int v) { return __int2float_rn(v); }
-__device__ __forceinline__ float xacc_f(long long v) { return __ll2float_rn(v); }
 
 // sum over words [W0, W1) of (codes . t): 256 (codes . h) + (codes . l), or
 // 4096 (codes . h) + 16 (codes . m) + (codes . l)
@@ -117,7 +117,7 @@ __device__ __forceinline__ xacc_t<XS> idot(const int (&c)[8], const XBlock& x) {
     if (XS == 3) am1 = __dp4a(c[k + 1], x.m[k + 1], am1);
     al1 = __dp4a(c[k + 1], x.l[k + 1], al1);
   }
-  if constexpr (XS == 3) return (long long)(ah0 + ah1) * 4096 + ((am0 + am1) * 16 + (al0 + al1));
+  if constexpr (XS == 3) return (ah0 + ah1) * 4096 + ((am0 + am1) * 16 + (al0 + al1));
   else return (ah0 + ah1) * 256 + (al0 + al1);
 }
 
@@ -339,8 +339,11 @@ __device__ __forceinline__ void cp16z(uint32_t dst, const void* src, uint32_t n)
 }
 
 // Tiles of one warp: its row groups g0, g0 + stride, ... (g0 = warp * ncta + cta,
-// so consecutive groups land on different CTAs and every SM gets an equal
-// share), each in kiters column tiles.
+// stride = ncta * NW, so consecutive groups land on different CTAs and every SM
+// gets an equal share), each in kiters column tiles.  (Measured on GB300:
+// cutting the groups into contiguous per-CTA shares split evenly over the warps
+// at tile granularity, pieces of a group added in shared memory, was slower at
+// every shape, even where whole groups leave a last round to a tenth of the warps.)
 struct WarpTiles {
   int64_t g0, stride;
   int ntiles;
@@ -369,7 +372,9 @@ __device__ __forceinline__ float pipe_dot(const uint8_t* blk, int lane, const XB
 // from a valid address, so its products are zero) and its share of the rows'
 // scale pieces (16-byte pieces, and 4-byte ones for Q6_K's d; a lane without a
 // piece of its own repeats one of row 0's).  Sources advance by a fixed stride
-// per tile; the per-lane plan is rebuilt at each new row group.
+// per tile; the per-lane plan is rebuilt at each new row group.  One cursor per
+// warp serves the whole launch: the copies issued before the dependency wait,
+// those issued during the x staging and those of the tile loop.
 template <int FMT, int R, int S>
 struct PipeCursor {
   using P = Pipe<FMT>;
@@ -385,6 +390,7 @@ struct PipeCursor {
   int bstr[NB];
   int64_t grp, stride;
   int left, it, kiters;
+  bool fresh;
   uint32_t dst, ring0, ring_end;
 
   __device__ __forceinline__ void init(const WarpTiles& w, int kiters_, uint32_t wring_s) {
@@ -393,6 +399,7 @@ struct PipeCursor {
     left = w.ntiles;
     it = 0;
     kiters = kiters_;
+    fresh = true;
     ring0 = dst = wring_s;
     ring_end = wring_s + uint32_t(S * R * P::RB);
   }
@@ -467,7 +474,10 @@ struct PipeCursor {
   template <bool ISSUE>
   __device__ __forceinline__ void step(const GemvArgs& a, int64_t nrows, int lane) {
     if (left > 0) {
-      if (it == 0) setup(a, nrows, lane);
+      if (fresh) {
+        setup(a, nrows, lane);
+        fresh = false;
+      }
       if (ISSUE) {
 #pragma unroll
         for (int r = 0; r < R; r++) {
@@ -499,6 +509,7 @@ struct PipeCursor {
       if (++it == kiters) {
         it = 0;
         grp += stride;
+        fresh = true;
       }
     }
     if (ISSUE) cp_commit();   // one group per tile, empty past the end, so the wait_group counts stay aligned
@@ -517,28 +528,14 @@ __host__ __device__ constexpr size_t pipe_slice() {
   return SLICE ? size_t(SLICE) : size_t(S) * R * Pipe<FMT>::RB;
 }
 
-// First S-1 tiles of the calling warp.  Reads only weights, so it may run
-// before the producer of x has finished, and (with per-warp slices) while
-// other warps of the CTA still work on an earlier GEMV.
-// Copies of the calling warp's tiles [from, to) (to <= S - 1): the first S - 1
-// tiles are in flight when the tile loop starts.
-template <int FMT, int R, int S, int SLICE = 0>
-__device__ __forceinline__ void pipe_issue_w(const GemvArgs& a, int64_t nrows, const WarpTiles& w, uint8_t* ring,
-                                             int from, int to) {
-  static_assert(SLICE == 0 || size_t(S) * R * Pipe<FMT>::RB <= size_t(SLICE), "ring slice too small");
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t wring_s = smem_addr(ring + size_t(warp) * pipe_slice<FMT, R, S, SLICE>());
-  PipeCursor<FMT, R, S> c;
-  c.init(w, int(a.ncols / 1024), wring_s);
+// Issues the copies of the cursor's next n tiles (one commit group each).
+template <class Cur>
+__device__ __forceinline__ void pipe_issue(Cur& cur, const GemvArgs& a, int64_t nrows, int n) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll 1
-  for (int t = 0; t < from; t++) c.template step<false>(a, nrows, lane);
-#pragma unroll 1
-  for (int t = from; t < to; t++) c.template step<true>(a, nrows, lane);
+  for (int t = 0; t < n; t++) cur.template step<true>(a, nrows, lane);
 }
-template <int FMT, int R, int S, int SLICE = 0>
-__device__ __forceinline__ void pipe_prologue_w(const GemvArgs& a, int64_t nrows, const WarpTiles& w, uint8_t* ring) {
-  pipe_issue_w<FMT, R, S, SLICE>(a, nrows, w, ring, 0, S - 1);
-}
+
 // Converts one lane's eight elements of a 32-column block: columns
 // [256 p, 256 p + 256) of the window are eight blocks, four lanes per block,
 // eight consecutive elements per lane.  Per block: sx = max|x|/T (T = 32512 or
@@ -651,30 +648,27 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xq, F betwee
   __syncthreads();
 }
 
-// The GEMV of the calling warp's groups after its first S-1 tiles were issued:
-// the tile loop (resuming the copy cursor S-1 tiles in), row-group epilogues
-// and, for EPI_LOGITS, the CTA's top-2 summary in a.epi.top2[cta].  x is staged
-// in xq and `scale` is the RMS factor.  Operands are read one tile ahead: the
-// next tile's codes, scales and x block come from shared memory while the
-// cursor issues copies, before they are used.  last: the launch's final loop
-// (it writes the EPI_LOGITS summary).  Every thread of the CTA must call it
-// (EPI_LOGITS ends with a CTA barrier).
-template <int FMT, int R, int S, int EPI, int NW, int SLICE>
-__device__ __forceinline__ void pipe_loop_w(const GemvArgs& a, int64_t nrows, const WarpTiles& w, int cta,
-                                            uint8_t* xq, uint8_t* ring, float scale, bool last = true) {
+// Running top-2 of the rows a warp finished (EPI_LOGITS).
+struct Top2 {
+  float best = -INFINITY, second = -INFINITY;
+  int best_i = 0x7fffffff;
+};
+
+// The GEMV of the calling warp's groups w: the tile loop and the row-group
+// epilogues.  cur is the warp's copy cursor with its first S-1 tiles issued
+// (ring slices at wring); x is staged in xq and `scale` is the RMS factor.
+// Operands are read one tile ahead: the next tile's codes, scales and x block
+// come from shared memory while the cursor issues copies, before they are used.
+template <int FMT, int R, int S, int EPI, int NW>
+__device__ __forceinline__ void pipe_loop_w(const GemvArgs& a, int64_t nrows, const WarpTiles& w, uint8_t* xq,
+                                            const uint8_t* wring, float scale, PipeCursor<FMT, R, S>& cur,
+                                            Top2& t2) {
   static_assert(S >= 3, "the loop keeps one tile's operands ahead");
   using P = Pipe<FMT>;
   constexpr int XS = x_slices(EPI), XU = x_unit<XS>();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int kiters = int(a.ncols / 1024);
-  uint8_t* wring = ring + size_t(warp) * pipe_slice<FMT, R, S, SLICE>();
-  PipeCursor<FMT, R, S> cur;
-  cur.init(w, kiters, smem_addr(wring));
-#pragma unroll 1
-  for (int t = 0; t < S - 1; t++) cur.template step<false>(a, nrows, lane);
-
-  float best = -INFINITY, second = -INFINITY;
-  int best_i = 0x7fffffff;
+  if (w.ntiles == 0) return;
   float acc[R];
 #pragma unroll
   for (int r = 0; r < R; r++) acc[r] = 0.f;
@@ -685,13 +679,11 @@ __device__ __forceinline__ void pipe_loop_w(const GemvArgs& a, int64_t nrows, co
   const uint8_t* xp = xq + size_t(lane) * XU;             // this lane's x block of the tile
   typename P::Frag fr[R];
   XBlock xb;
-  if (w.ntiles > 0) {
-    cp_wait<S - 2>();   // tile 0 has landed
-    __syncwarp();
+  cp_wait<S - 2>();   // tile 0 has landed
+  __syncwarp();
 #pragma unroll
-    for (int r = 0; r < R; r++) P::load(rd + r * P::RB, lane, fr[r]);
-    load_xblock<XS>(xp, xb);
-  }
+  for (int r = 0; r < R; r++) P::load(rd + r * P::RB, lane, fr[r]);
+  load_xblock<XS>(xp, xb);
 #pragma unroll 1
   for (int t = 0; t < w.ntiles; t++) {
 #pragma unroll
@@ -700,14 +692,14 @@ __device__ __forceinline__ void pipe_loop_w(const GemvArgs& a, int64_t nrows, co
     if (rd == rd_end) rd = wring;
     xp += 32 * XU;
     if (++c_it == kiters) {
-      // ---- row group done: transposed warp reduction, epilogue ------------
+      // ---- row group done: transposed warp reduction, epilogue --------------
       c_it = 0;
       xp = xq + size_t(lane) * XU;
       float kk = warp_reduce_rows<R>(acc, lane);
 #pragma unroll
       for (int r = 0; r < R; r++) acc[r] = 0.f;
       kk = __fmul_rn(kk, scale);
-      epilogue<R, EPI>(a, c_grp, nrows, lane, kk, best, best_i, second);
+      epilogue<R, EPI>(a, c_grp, nrows, lane, kk, t2.best, t2.best_i, t2.second);
       c_grp += w.stride;
     }
     cp_wait<S - 3>();   // tile t + 1 has landed
@@ -719,7 +711,6 @@ __device__ __forceinline__ void pipe_loop_w(const GemvArgs& a, int64_t nrows, co
   }
   cp_wait<0>();
   __syncwarp();
-  if (EPI == EPI_LOGITS && last) cta_top2<NW>(a, cta, best, best_i, second);
 }
 
 template <int FMT, int R, int S, int EPI, int NW>
@@ -730,17 +721,21 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe(const __grid_con
   uint8_t* xq = reinterpret_cast<uint8_t*>(smem4);
   constexpr int XS = x_slices(EPI);
   uint8_t* ring = xq + size_t(a.ncols / 32) * x_unit<XS>();
-  const WarpTiles w = warp_tiles(nrows, R, int(a.ncols / 1024), threadIdx.x >> 5, NW, blockIdx.x, gridDim.x);
-  pipe_issue_w<FMT, R, S>(a, nrows, w, ring, 0, E);
+  const int warp = threadIdx.x >> 5, kiters = int(a.ncols / 1024);
+  const WarpTiles w = warp_tiles(nrows, R, kiters, warp, NW, blockIdx.x, gridDim.x);
+  uint8_t* wring = ring + size_t(warp) * pipe_slice<FMT, R, S, 0>();
+  PipeCursor<FMT, R, S> cur;
+  cur.init(w, kiters, smem_addr(wring));
+  pipe_issue(cur, a, nrows, E);   // weights only: before the producer of x has finished
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  stage_x<FMT, NW, XS>(a, xq, [&] {
-    if (E < S - 1) pipe_issue_w<FMT, R, S>(a, nrows, w, ring, E, S - 1);
-  });
+  stage_x<FMT, NW, XS>(a, xq, [&] { pipe_issue(cur, a, nrows, S - 1 - E); });
   const float scale = x_scale<XS>(a, xq);
   // the next kernel may start its own weight prefetch on SMs this grid frees;
   // it waits for this grid to finish before it reads anything this grid writes
   asm volatile("griddepcontrol.launch_dependents;");
-  pipe_loop_w<FMT, R, S, EPI, NW, 0>(a, nrows, w, blockIdx.x, xq, ring, scale);
+  Top2 t2;
+  pipe_loop_w<FMT, R, S, EPI, NW>(a, nrows, w, xq, wring, scale, cur, t2);
+  if (EPI == EPI_LOGITS) cta_top2<NW>(a, blockIdx.x, t2.best, t2.best_i, t2.second);
 }
 
 // Two GEMVs over the same x in one launch: rows [0, n1) of a1 in format F1 and
@@ -772,19 +767,32 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe2(const __grid_co
   w2.g0 = g2 - G1;
   w2.stride = w1.stride;
   w2.ntiles = g2 < G ? int((G - 1 - g2) / w2.stride + 1) * kiters : 0;
+  uint8_t* wring = ring + size_t(warp) * SLICE;
+  PipeCursor<F1, R, S1> cur1;
+  PipeCursor<F2, R, S2> cur2;
   constexpr int E1 = S1 - 1 < kPipeEarly ? S1 - 1 : kPipeEarly, E2 = S2 - 1 < kPipeEarly ? S2 - 1 : kPipeEarly;
-  if (w1.ntiles) pipe_issue_w<F1, R, S1, SLICE>(a1, n1, w1, ring, 0, E1);
-  else pipe_issue_w<F2, R, S2, SLICE>(a2, n2, w2, ring, 0, E2);
+  if (w1.ntiles) {
+    cur1.init(w1, kiters, smem_addr(wring));
+    pipe_issue(cur1, a1, n1, E1);
+  } else {
+    cur2.init(w2, kiters, smem_addr(wring));
+    pipe_issue(cur2, a2, n2, E2);
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   stage_x<F1, NW, XS>(a1, xq, [&] {
-    if (w1.ntiles) pipe_issue_w<F1, R, S1, SLICE>(a1, n1, w1, ring, E1, S1 - 1);
-    else pipe_issue_w<F2, R, S2, SLICE>(a2, n2, w2, ring, E2, S2 - 1);
+    if (w1.ntiles) pipe_issue(cur1, a1, n1, S1 - 1 - E1);
+    else pipe_issue(cur2, a2, n2, S2 - 1 - E2);
   });
   const float scale = x_scale<XS>(a1, xq);
   asm volatile("griddepcontrol.launch_dependents;");
-  pipe_loop_w<F1, R, S1, EPI, NW, SLICE>(a1, n1, w1, blockIdx.x, xq, ring, scale, false);
-  if (w1.ntiles && w2.ntiles) pipe_prologue_w<F2, R, S2, SLICE>(a2, n2, w2, ring);
-  pipe_loop_w<F2, R, S2, EPI, NW, SLICE>(a2, n2, w2, blockIdx.x, xq, ring, scale);
+  Top2 t2;
+  pipe_loop_w<F1, R, S1, EPI, NW>(a1, n1, w1, xq, wring, scale, cur1, t2);
+  if (w1.ntiles && w2.ntiles) {   // the a2 groups start on a drained ring
+    cur2.init(w2, kiters, smem_addr(wring));
+    pipe_issue(cur2, a2, n2, S2 - 1);
+  }
+  pipe_loop_w<F2, R, S2, EPI, NW>(a2, n2, w2, xq, wring, scale, cur2, t2);
+  if (EPI == EPI_LOGITS) cta_top2<NW>(a1, blockIdx.x, t2.best, t2.best_i, t2.second);
 }
 
 inline size_t pipe_x_bytes(int64_t cols, int epi) {

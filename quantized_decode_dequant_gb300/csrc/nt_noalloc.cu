@@ -9,13 +9,15 @@
 // this array, which every GPU that loads the library holds until exit.
 #include <mutex>
 
-#include "nt_internal.cuh"
+#include "nt_gemv.cuh"
 
 namespace nt {
 
-// Maximum number of CTAs whose summaries the array holds; the GEMV launch is
-// capped to it.
+// Maximum number of CTAs whose summaries the array holds.  The GEMV launch is
+// capped to it: launch_gemv never starts more CTAs than GemvArgs::max_grid
+// (itself at most kMaxGemvGrid) on any of its paths.
 constexpr int kNoAllocMaxCtas = 1024;
+static_assert(kNoAllocMaxCtas <= kMaxGemvGrid, "max_grid must reach the GEMV launch unchanged");
 
 // 1024 x 16 B = 16 KiB per device.  Shared by every call: each call's GEMV
 // overwrites the first grid-size entries before the selection reads them, so
@@ -28,7 +30,8 @@ static float4* g_noalloc_addr[kNoAllocMaxDevices];   // device address of the ar
 
 // The array's device address for the current device.  In host code the array's
 // name is only a host-side stand-in, so it is resolved once per device with
-// that device current.
+// that device current, and kept for the life of the process: a cudaDeviceReset
+// (which unloads the module) makes the kept address stale.
 static nt_status noalloc_scratch(float4** out) {
   int dev = 0;
   NT_CUDA(cudaGetDevice(&dev));
@@ -44,19 +47,8 @@ static nt_status noalloc_scratch(float4** out) {
   return NT_OK;
 }
 
-__device__ __forceinline__ void noalloc_merge(float b2, int i2, float s2, float& b, int& bi, float& s) {
-  if (i2 == 0x7fffffff) return;
-  if (b2 > b || (b2 == b && i2 < bi)) {
-    s = fmaxf(s2, b);
-    b = b2;
-    bi = i2;
-  } else {
-    s = fmaxf(s, b2);
-  }
-}
-
-// Largest entry over the n per-CTA summaries (ties to the lowest row), and the
-// gap to the second largest.
+// Largest entry over the n per-CTA summaries (ties to the lowest row; NaN
+// entries are never selected), and the gap to the second largest.
 __global__ void k_noalloc_select(const float4* __restrict__ top2, int n, int32_t* out_index, float* out_margin) {
   __shared__ float sb[256], ss[256];
   __shared__ int si[256];
@@ -64,14 +56,14 @@ __global__ void k_noalloc_select(const float4* __restrict__ top2, int n, int32_t
   int bi = 0x7fffffff;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const float4 v = top2[i];
-    noalloc_merge(v.x, __float_as_int(v.y), v.z, b, bi, s);
+    top2_merge(v.x, __float_as_int(v.y), v.z, b, bi, s);
   }
   sb[threadIdx.x] = b;
   ss[threadIdx.x] = s;
   si[threadIdx.x] = bi;
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int t = 1; t < blockDim.x; t++) noalloc_merge(sb[t], si[t], ss[t], b, bi, s);
+    for (int t = 1; t < blockDim.x; t++) top2_merge(sb[t], si[t], ss[t], b, bi, s);
     *out_index = bi == 0x7fffffff ? -1 : bi;
     *out_margin = b - s;
   }
@@ -110,7 +102,6 @@ extern "C" nt_status nt_gemv_argmax_noalloc(const nt_qtensor* t, const float* de
   int grid = 0;
   cudaError_t e = launch_gemv(a, EPI_LOGITS, s, false, &grid);
   if (e != cudaSuccess) return cuda_fail(e, "nt_gemv_argmax_noalloc: GEMV");
-  if (grid > kNoAllocMaxCtas) return fail(NT_E_CUDA, "nt_gemv_argmax_noalloc: GEMV used more CTAs than the scratch holds");
   k_noalloc_select<<<1, 256, 0, s>>>(scratch, grid, dev_index, dev_margin);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "nt_gemv_argmax_noalloc: selection");

@@ -40,6 +40,32 @@ def test_noalloc_matches_gemv_entry_point_two_calls(fmt, rows, cols):
         nt.nt_qtensor_destroy(t)
 
 
+def test_noalloc_one_row_and_ties():
+    """One row: index 0 and an infinite margin.  x = 0 makes every y equal: the
+    lowest row wins the tie with margin 0 (on two calls in a row)."""
+    torch = torch_cuda()
+    ensure_built()
+    from quantized_decode_dequant_gb300 import nt
+    s = torch.cuda.current_stream()
+    for rows, cols, x_zero in ((1, 1024, False), (300, 1024, True), (5, 96, True)):
+        t = nt.nt_qtensor_create("q8_0", rows, cols, 0, 5, 0.02)
+        try:
+            x = torch.zeros(cols, device="cuda") if x_zero else torch.from_numpy(activation(cols, seed=3)).cuda()
+            y = torch.empty(rows, device="cuda")
+            idx = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+            margin = torch.full((1,), float("nan"), device="cuda")
+            for _ in range(2):
+                nt.nt_gemv_argmax_noalloc(t, x.data_ptr(), y.data_ptr(), idx.data_ptr(), margin.data_ptr(), s)
+                torch.cuda.synchronize()
+                assert int(idx.item()) == 0
+                if rows == 1:
+                    assert float(margin.item()) == float("inf")
+                else:
+                    assert float(margin.item()) == 0.0 and float(y.abs().max().item()) == 0.0
+        finally:
+            nt.nt_qtensor_destroy(t)
+
+
 def test_noalloc_rejects_bad_arguments():
     torch = torch_cuda()
     ensure_built()
