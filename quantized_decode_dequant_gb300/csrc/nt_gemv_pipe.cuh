@@ -66,6 +66,19 @@ __device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
+// the same, issued only when on != 0 (a predicated copy: no branch)
+__device__ __forceinline__ void cp16_if(uint32_t on, uint32_t dst, const void* src) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %2, 0;\n @p cp.async.cg.shared.global [%0], [%1], 16;\n}\n" ::"r"(dst),
+      "l"(src), "r"(on)
+      : "memory");
+}
+__device__ __forceinline__ void cp4_if(uint32_t on, uint32_t dst, const void* src) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %2, 0;\n @p cp.async.ca.shared.global [%0], [%1], 4;\n}\n" ::"r"(dst),
+      "l"(src), "r"(on)
+      : "memory");
+}
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_wait() {
@@ -370,8 +383,8 @@ __device__ __forceinline__ float pipe_dot(const uint8_t* blk, int lane, const XB
 // for every tile, so there are no divergent branches: 16 (or twice 16) code bytes
 // of each of the R rows (a row past the matrix copies zero bytes, src-size 0,
 // from a valid address, so its products are zero) and its share of the rows'
-// scale pieces (16-byte pieces, and 4-byte ones for Q6_K's d; a lane without a
-// piece of its own repeats one of row 0's).  Sources advance by a fixed stride
+// scale pieces (16-byte pieces, and 4-byte ones for Q6_K's d; a lane slot
+// without a piece of its own is a predicated-off copy).  Sources advance by a fixed stride
 // per tile; the per-lane plan is rebuilt at each new row group.  One cursor per
 // warp serves the whole launch: the copies issued before the dependency wait,
 // those issued during the x staging and those of the tile loop.
@@ -383,10 +396,10 @@ struct PipeCursor {
   const uint8_t* code[R];
   uint32_t csz[R];
   const uint8_t* asrc[NA];
-  uint32_t aoff[NA];
+  uint32_t aoff[NA], aon[NA];
   int astr[NA];
   const uint8_t* bsrc[NB];
-  uint32_t boff[NB];
+  uint32_t boff[NB], bon[NB];
   int bstr[NB];
   int64_t grp, stride;
   int left, it, kiters;
@@ -419,12 +432,13 @@ struct PipeCursor {
       csz[r] = r < nlive ? 16u : 0u;
     }
     // piece slot k of this lane: piece p = lane + 32k of the group's R rows; a slot
-    // past the live pieces repeats piece p mod NP of row 0 (same bytes to the same place)
+    // past the live pieces copies nothing (its plan points at a piece of row 0)
 #pragma unroll
     for (int k = 0; k < NA; k++) {
       const int p = lane + 32 * k;
       int r = p / P::NPA, i = p - r * P::NPA;
-      if (!(p < R * P::NPA && r < nlive)) {
+      aon[k] = p < R * P::NPA && r < nlive;
+      if (!aon[k]) {
         r = 0;
         i = p % P::NPA;
       }
@@ -449,7 +463,8 @@ struct PipeCursor {
       for (int k = 0; k < NB; k++) {
         const int p = lane + 32 * k;
         int r = p / npb, i = p - r * npb;
-        if (!(p < R * P::NPB && r < nlive)) {
+        bon[k] = p < R * P::NPB && r < nlive;
+        if (!bon[k]) {
           r = 0;
           i = p % npb;
         }
@@ -489,10 +504,10 @@ struct PipeCursor {
           if (P::CB == 32) cp16z(d + 512, code[r] + 512, csz[r]);
         }
 #pragma unroll
-        for (int k = 0; k < NA; k++) cp16(dst + aoff[k], asrc[k]);
+        for (int k = 0; k < NA; k++) cp16_if(aon[k], dst + aoff[k], asrc[k]);
         if (P::NPB) {
 #pragma unroll
-          for (int k = 0; k < NB; k++) cp4(dst + boff[k], bsrc[k]);
+          for (int k = 0; k < NB; k++) cp4_if(bon[k], dst + boff[k], bsrc[k]);
         }
       }
 #pragma unroll
@@ -740,24 +755,24 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe(const __grid_con
 
 // Two GEMVs over the same x in one launch: rows [0, n1) of a1 in format F1 and
 // rows [0, n2) of a2 in F2 (both 4-bit-nibble formats, so one staged x serves
-// both).  The group indices of the two run on as one range over the warps, a1's
-// first; each warp works through its a1 groups, then its a2 groups, with each
-// format's own ring depth in one per-warp slice.  Used for a Q4_K Q/K GEMV with
-// a Q6_K V GEMV.
-template <int F1, int F2, int S1, int S2, int EPI, int NW>
+// both).  The group indices of the two (R1 rows per a1 group, R2 per a2 group)
+// run on as one range over the warps, a1's first; each warp works through its
+// a1 groups, then its a2 groups, with each format's own ring depth in one
+// per-warp slice.  Used for a Q4_K Q/K GEMV (four rows per warp, each x read
+// shared by four rows) with a Q6_K V GEMV (two).
+template <int F1, int F2, int R1, int R2, int S1, int S2, int EPI, int NW>
 __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe2(const __grid_constant__ GemvArgs a1,
                                                        const __grid_constant__ GemvArgs a2, const int64_t n1,
                                                        const int64_t n2) {
   static_assert(F1 != NT_Q8_0 && F2 != NT_Q8_0, "one staged x: nibble formats only");
-  constexpr int R = 2;
-  constexpr int SLICE = int(pipe_slice<F1, R, S1, 0>() > pipe_slice<F2, R, S2, 0>() ? pipe_slice<F1, R, S1, 0>()
-                                                                                     : pipe_slice<F2, R, S2, 0>());
+  constexpr int SLICE = int(pipe_slice<F1, R1, S1, 0>() > pipe_slice<F2, R2, S2, 0>() ? pipe_slice<F1, R1, S1, 0>()
+                                                                                       : pipe_slice<F2, R2, S2, 0>());
   extern __shared__ float4 smem4[];
   uint8_t* xq = reinterpret_cast<uint8_t*>(smem4);
   constexpr int XS = x_slices(EPI);
   uint8_t* ring = xq + size_t(a1.ncols / 32) * x_unit<XS>();
   const int warp = threadIdx.x >> 5, kiters = int(a1.ncols / 1024);
-  const int64_t G1 = (n1 + R - 1) / R, G = G1 + (n2 + R - 1) / R;
+  const int64_t G1 = (n1 + R1 - 1) / R1, G = G1 + (n2 + R2 - 1) / R2;
   WarpTiles w1, w2;
   w1.g0 = int64_t(warp) * gridDim.x + blockIdx.x;
   w1.stride = int64_t(gridDim.x) * NW;
@@ -768,30 +783,22 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe2(const __grid_co
   w2.stride = w1.stride;
   w2.ntiles = g2 < G ? int((G - 1 - g2) / w2.stride + 1) * kiters : 0;
   uint8_t* wring = ring + size_t(warp) * SLICE;
-  PipeCursor<F1, R, S1> cur1;
-  PipeCursor<F2, R, S2> cur2;
-  constexpr int E1 = S1 - 1 < kPipeEarly ? S1 - 1 : kPipeEarly, E2 = S2 - 1 < kPipeEarly ? S2 - 1 : kPipeEarly;
-  if (w1.ntiles) {
-    cur1.init(w1, kiters, smem_addr(wring));
-    pipe_issue(cur1, a1, n1, E1);
-  } else {
-    cur2.init(w2, kiters, smem_addr(wring));
-    pipe_issue(cur2, a2, n2, E2);
-  }
+  // a1's copies from the start; a2's once the warp's a1 groups are done (on a
+  // drained ring; one cursor live at a time keeps the loops within the registers)
+  PipeCursor<F1, R1, S1> cur1;
+  constexpr int E1 = S1 - 1 < kPipeEarly ? S1 - 1 : kPipeEarly;
+  cur1.init(w1, kiters, smem_addr(wring));
+  pipe_issue(cur1, a1, n1, E1);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  stage_x<F1, NW, XS>(a1, xq, [&] {
-    if (w1.ntiles) pipe_issue(cur1, a1, n1, S1 - 1 - E1);
-    else pipe_issue(cur2, a2, n2, S2 - 1 - E2);
-  });
+  stage_x<F1, NW, XS>(a1, xq, [&] { pipe_issue(cur1, a1, n1, S1 - 1 - E1); });
   const float scale = x_scale<XS>(a1, xq);
   asm volatile("griddepcontrol.launch_dependents;");
   Top2 t2;
-  pipe_loop_w<F1, R, S1, EPI, NW>(a1, n1, w1, xq, wring, scale, cur1, t2);
-  if (w1.ntiles && w2.ntiles) {   // the a2 groups start on a drained ring
-    cur2.init(w2, kiters, smem_addr(wring));
-    pipe_issue(cur2, a2, n2, S2 - 1);
-  }
-  pipe_loop_w<F2, R, S2, EPI, NW>(a2, n2, w2, xq, wring, scale, cur2, t2);
+  pipe_loop_w<F1, R1, S1, EPI, NW>(a1, n1, w1, xq, wring, scale, cur1, t2);
+  PipeCursor<F2, R2, S2> cur2;
+  cur2.init(w2, kiters, smem_addr(wring));
+  pipe_issue(cur2, a2, n2, S2 - 1);
+  pipe_loop_w<F2, R2, S2, EPI, NW>(a2, n2, w2, xq, wring, scale, cur2, t2);
   if (EPI == EPI_LOGITS) cta_top2<NW>(a1, blockIdx.x, t2.best, t2.best_i, t2.second);
 }
 
@@ -881,18 +888,18 @@ cudaError_t launch_gemv_pipe_fmt(const GemvArgs& a, int epi, int R, int S, cudaS
 // per CTA, one CTA per SM, the ring depths that fit beside x.
 template <int EPI>
 cudaError_t launch_gemv_pipe2_q4k_q6k(const GemvArgs& a1, const GemvArgs& a2, cudaStream_t s, bool pdl) {
-  constexpr int NW = kPipeWarps, S1 = 8, S2 = 6;
-  auto kern = k_gemv_pipe2<NT_Q4_K, NT_Q6_K, S1, S2, EPI, NW>;
-  constexpr size_t slice = pipe_slice<NT_Q4_K, 2, S1, 0>() > pipe_slice<NT_Q6_K, 2, S2, 0>()
-                               ? pipe_slice<NT_Q4_K, 2, S1, 0>()
-                               : pipe_slice<NT_Q6_K, 2, S2, 0>();
+  constexpr int NW = kPipeWarps, R1 = 4, R2 = 2, S1 = 4, S2 = 6;
+  auto kern = k_gemv_pipe2<NT_Q4_K, NT_Q6_K, R1, R2, S1, S2, EPI, NW>;
+  constexpr size_t slice = pipe_slice<NT_Q4_K, R1, S1, 0>() > pipe_slice<NT_Q6_K, R2, S2, 0>()
+                               ? pipe_slice<NT_Q4_K, R1, S1, 0>()
+                               : pipe_slice<NT_Q6_K, R2, S2, 0>();
   const size_t smem = pipe_x_bytes(a1.ncols, EPI) + size_t(NW) * slice;
   if (smem > size_t(kPipeMaxSmem) || a1.ncols != a2.ncols || a1.col0 || a2.col0) return cudaErrorInvalidValue;
   static const KernelSetup setup = kernel_setup(kern, kPipeMaxSmem);
   if (setup.err != cudaSuccess) return setup.err;
   const int s_sms = setup.sms;
   const int64_t n1 = gemv_logical_rows(a1), n2 = gemv_logical_rows(a2);
-  const int64_t groups = (n1 + 1) / 2 + (n2 + 1) / 2;
+  const int64_t groups = (n1 + R1 - 1) / R1 + (n2 + R2 - 1) / R2;
   int64_t grid = (groups + NW - 1) / NW;
   if (grid < s_sms) grid = groups < s_sms ? groups : s_sms;
   if (grid > s_sms) grid = s_sms;
