@@ -27,17 +27,24 @@ namespace nt {
 constexpr int kAttnWarps = 8;
 constexpr int kAttnThreads = 32 * kAttnWarps;
 
-// Cached positions per item: 64 up to 1024 positions of maximum context, 128 up
-// to 2048, else 256 (about one item per SM for the longest contexts; the merge
-// then combines at most 17 chunks per head at 4096 positions).  Fixed per model.
-inline int attn_chunk_len(int max_ctx) { return max_ctx <= 1024 ? 64 : (max_ctx <= 2048 ? 128 : 256); }
+// Chunk length: the context is cut into at most 16 items per kv head up to 5120
+// positions (the merge reads every chunk's partials in one round of loads), at
+// least 32 positions each, a multiple of 16: C = max(32, 16 ceil(max_ctx / 256)),
+// at most 320.  The items a step uses split its positions evenly (see k_attn).
+// Fixed per model.
+inline int attn_chunk_len(int max_ctx) {
+  const int c = 16 * ((max_ctx + 255) / 256);
+  return c < 32 ? 32 : (c > 320 ? 320 : c);   // 320: the largest instantiated chunk (longer contexts: more items)
+}
+// Largest chunk a kernel instantiation holds (its shared-memory layout).
+inline int attn_chunk_max(int chunk) { return chunk <= 64 ? 64 : (chunk <= 128 ? 128 : (chunk <= 256 ? 256 : 320)); }
 
 struct AttnArgs {
   const float* q = nullptr;         // [n_heads][hd], RoPE applied
   const __half* kc = nullptr;       // this layer's K: [n_kv][max_ctx][hd]
   const __half* vc = nullptr;
   int max_ctx = 0;
-  int chunk = 64;                   // C
+  int chunk = 64;                   // C, a multiple of 16
   float scale = 1.f;                // 1/sqrt(hd)
   float* part_o = nullptr;          // [n_heads][n_chunks][hd]
   float2* part_ml = nullptr;        // [n_heads][n_chunks] (m_c, l_c)
@@ -46,17 +53,18 @@ struct AttnArgs {
   float* out = nullptr;             // [n_heads][hd]
 };
 
-// Shared memory of one item.  K and V rows are padded by 16 bytes so that the
-// eight 16-byte rows one ldmatrix phase reads fall in distinct banks; P rows
-// likewise.
-template <int HD, int G, int C>
+// Shared memory of one item (CM: the largest chunk).  K and V rows are padded
+// by 16 bytes so that the eight 16-byte rows one ldmatrix phase reads fall in
+// distinct banks; P rows likewise.  Then the softmax reductions and the merge
+// flag.
+template <int HD, int G, int CM>
 struct AttnLayout {
   static constexpr int KP = HD + 8;              // halves per padded K/V row
   static constexpr int MT = G > 8 ? 2 : 1;       // 16-row tiles of the A operand
-  static constexpr int PP = C + 8;               // halves per padded P row
+  static constexpr int PP = CM + 8;              // halves per padded P row
   static constexpr size_t kK = 0;
-  static constexpr size_t kV = kK + size_t(C) * KP * 2;
-  static constexpr size_t kP = kV + size_t(C) * KP * 2;
+  static constexpr size_t kV = kK + size_t(CM) * KP * 2;
+  static constexpr size_t kP = kV + size_t(CM) * KP * 2;
   static constexpr size_t kRed = kP + size_t(MT) * 16 * PP * 2;        // [2][warps][G] floats
   static constexpr size_t kFlag = kRed + size_t(2) * kAttnWarps * G * 4;
   static constexpr size_t kBytes = kFlag + 16;
@@ -98,13 +106,15 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// Copies of rows [r0, r1) of the item's K and V (chunk-relative) into shared memory.
-template <int HD, int C>
+// Copies of rows [r0, r1) of the item's K and V (chunk-relative) into shared
+// memory, 16 bytes per thread and copy.  (One bulk copy per row, by one warp,
+// measured almost twice as slow: 512 copies of 256 bytes queue up.)
+template <int HD, int CM>
 __device__ __forceinline__ void attn_copy_rows(const AttnArgs& a, int g, int t0, int r0, int r1, uint8_t* sm) {
   constexpr int KP = HD + 8, VPR = HD / 8;
   const __half* kb = a.kc + (int64_t(g) * a.max_ctx + t0) * HD;
   const __half* vb = a.vc + (int64_t(g) * a.max_ctx + t0) * HD;
-  const uint32_t ks = smem_u32(sm), vs = ks + uint32_t(C * KP) * 2;
+  const uint32_t ks = smem_u32(sm), vs = ks + uint32_t(CM * KP) * 2;
   for (int i = r0 * VPR + int(threadIdx.x); i < r1 * VPR; i += kAttnThreads) {
     const int r = i / VPR, c = i % VPR;
     attn_cp16(ks + uint32_t(r * KP + c * 8) * 2, kb + r * HD + c * 8);
@@ -113,52 +123,70 @@ __device__ __forceinline__ void attn_copy_rows(const AttnArgs& a, int g, int t0,
 }
 
 // Merge of the `used` chunks of query head j by one warp (lane holds HD/32
-// dimensions); chunk loads are issued eight at a time; sums run over c in
-// increasing order.
+// dimensions): M = max m_c, o = sum_c o_c e^(m_c - M) / sum_c l_c e^(m_c - M),
+// sums over c in increasing order.  Up to 32 chunks (every context up to 16 x 320
+// positions), the statistics of chunk `lane` and the partial outputs of 16
+// chunks at a time are loaded before any of them is used.
 template <int HD>
 __device__ __forceinline__ void attn_combine_head(const AttnArgs& a, int j, int used, int lane) {
-  constexpr int V = HD / 32;
+  constexpr int V = HD / 32, NB = 16;
   const float2* ml = a.part_ml + int64_t(j) * a.n_chunks;
-  float M = -INFINITY;
-  for (int c = lane; c < used; c += 32) M = fmaxf(M, __ldcg(ml + c).x);
-#pragma unroll
-  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float* pj = a.part_o + int64_t(j) * a.n_chunks * HD + lane * V;
   float acc[V];
 #pragma unroll
   for (int v = 0; v < V; v++) acc[v] = 0.f;
-  float L = 0.f;
-  const float* pj = a.part_o + int64_t(j) * a.n_chunks * HD + lane * V;
-  for (int c0 = 0; c0 < used; c0 += 32) {
-    const int c = c0 + lane;
-    float w = 0.f, lw = 0.f;
-    if (c < used) {
-      const float2 m = __ldcg(ml + c);
-      w = expf(m.x - M);
-      lw = __fmul_rn(m.y, w);
-    }
+  auto load_batch = [&](int c0, float (&t)[NB][V]) {
 #pragma unroll
-    for (int o = 16; o; o >>= 1) lw = __fadd_rn(lw, __shfl_xor_sync(0xffffffffu, lw, o));
-    L = __fadd_rn(L, lw);
-    const int n = min(32, used - c0);
-    for (int i0 = 0; i0 < n; i0 += 8) {
-      float t[8][V];
-#pragma unroll
-      for (int i = 0; i < 8; i++) {
-        if (i0 + i < n) {
-          const float* po = pj + int64_t(c0 + i0 + i) * HD;
-          if (V == 4) {
-            const float4 u = __ldcg(reinterpret_cast<const float4*>(po));
-            t[i][0] = u.x; t[i][1 % V] = u.y; t[i][2 % V] = u.z; t[i][3 % V] = u.w;
-          } else {
-            const float2 u = __ldcg(reinterpret_cast<const float2*>(po));
-            t[i][0] = u.x; t[i][1 % V] = u.y;
-          }
+    for (int i = 0; i < NB; i++) {
+      if (c0 + i < used) {
+        const float* po = pj + int64_t(c0 + i) * HD;
+        if (V == 4) {
+          const float4 u = __ldcg(reinterpret_cast<const float4*>(po));
+          t[i][0] = u.x; t[i][1 % V] = u.y; t[i][2 % V] = u.z; t[i][3 % V] = u.w;
+        } else {
+          const float2 u = __ldcg(reinterpret_cast<const float2*>(po));
+          t[i][0] = u.x; t[i][1 % V] = u.y;
         }
       }
+    }
+  };
+  float L = 0.f;
+  if (used <= 32) {
+    const float2 mv = lane < used ? __ldcg(ml + lane) : make_float2(-INFINITY, 0.f);
+    float t[NB][V];
+    load_batch(0, t);
+    float M = mv.x;
 #pragma unroll
-      for (int i = 0; i < 8; i++) {
-        const float wi = __shfl_sync(0xffffffffu, w, (i0 + i) & 31);
-        if (i0 + i < n) {
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w = lane < used ? expf(mv.x - M) : 0.f;
+    L = __fmul_rn(mv.y, w);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) L = __fadd_rn(L, __shfl_xor_sync(0xffffffffu, L, o));
+    for (int c0 = 0; c0 < used; c0 += NB) {
+      if (c0) load_batch(c0, t);
+#pragma unroll
+      for (int i = 0; i < NB; i++) {
+        const float wi = __shfl_sync(0xffffffffu, w, (c0 + i) & 31);
+        if (c0 + i < used) {
+#pragma unroll
+          for (int v = 0; v < V; v++) acc[v] = __fmaf_rn(t[i][v], wi, acc[v]);
+        }
+      }
+    }
+  } else {
+    float M = -INFINITY;
+    for (int c = lane; c < used; c += 32) M = fmaxf(M, __ldcg(ml + c).x);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int c0 = 0; c0 < used; c0 += NB) {
+      float t[NB][V];
+      load_batch(c0, t);
+#pragma unroll
+      for (int i = 0; i < NB; i++) {
+        if (c0 + i < used) {
+          const float2 m = __ldcg(ml + c0 + i);
+          const float wi = expf(m.x - M);
+          L = __fadd_rn(L, __fmul_rn(m.y, wi));
 #pragma unroll
           for (int v = 0; v < V; v++) acc[v] = __fmaf_rn(t[i][v], wi, acc[v]);
         }
@@ -173,7 +201,6 @@ __device__ __forceinline__ void attn_combine_head(const AttnArgs& a, int j, int 
   }
 }
 
-
 // One item by the whole CTA: kv head g, chunk `chunk` of C positions; n =
 // positions attended (pos + 1: the current one is stored by now), used =
 // ceil(n / C) items of kv head g exist; rows [0, r_done) of the chunk are
@@ -186,18 +213,17 @@ __device__ __forceinline__ void attn_combine_head(const AttnArgs& a, int j, int 
 // [8 HD/64 w, 8 HD/64 (w+1)) over all keys.  Sums of the hi and lo rows, of the
 // per-warp softmax sums and of the k-steps run in a fixed order, so the result
 // does not depend on timing.
-template <int HD, int G, int C>
-__device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, int n, int used, uint8_t* sm,
-                                          int r_done) {
-  using Lay = AttnLayout<HD, G, C>;
+template <int HD, int G, int CM>
+__device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, int t0, int cnt, int used,
+                                          uint8_t* sm, int r_done) {
+  using Lay = AttnLayout<HD, G, CM>;
   constexpr int KP = Lay::KP, MT = Lay::MT, PP = Lay::PP, NW = kAttnWarps;
   constexpr int KS = HD / 16;                          // k-steps of the scores (even)
-  constexpr int NTW = C / 8 / NW;                      // score tiles per warp
+  constexpr int NTW = CM / 8 / NW;                     // score tiles per warp
   constexpr int NVW = HD / 8 / NW;                     // output tiles per warp (1 or 2)
   constexpr int HPT = MT;                              // heads per thread: gi (and gi + 8)
-  static_assert(KS % 2 == 0 && NTW >= 1 && (NVW == 1 || NVW == 2) && C % 16 == 0, "attention tile shape");
+  static_assert(KS % 2 == 0 && NTW >= 1 && (NVW == 1 || NVW == 2) && CM % 64 == 0, "attention tile shape");
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31, gi = lane >> 2, tg = lane & 3;
-  const int t0 = chunk * C, cnt = min(C, n - t0);
   const uint32_t ks = smem_u32(sm + Lay::kK), vs = smem_u32(sm + Lay::kV), ps = smem_u32(sm + Lay::kP);
   float* red_max = reinterpret_cast<float*>(sm + Lay::kRed);
   float* red_sum = red_max + NW * G;
@@ -221,11 +247,11 @@ __device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, i
     }
   }
   // the rows not copied before the wait (the current position's)
-  attn_copy_rows<HD, C>(a, g, t0, r_done, cnt, sm);
+  attn_copy_rows<HD, CM>(a, g, t0, r_done, cnt, sm);
   asm volatile("cp.async.commit_group;" ::: "memory");
   // V rows past cnt inside the last 16-key step enter P V with weight 0: make them finite
   {
-    const int r1 = min(C, (cnt + 15) & ~15);
+    const int r1 = min(CM, (cnt + 15) & ~15);
     for (int i = cnt * (HD / 8) + t; i < r1 * (HD / 8); i += kAttnThreads) {
       const int r = i / (HD / 8), c = i % (HD / 8);
       *reinterpret_cast<uint4*>(sm + Lay::kV + size_t(r * KP + c * 8) * 2) = make_uint4(0u, 0u, 0u, 0u);

@@ -44,27 +44,30 @@ __global__ void k_embed(const QMat e, const int32_t* __restrict__ d_token, float
   x[i] = dequant_elem(e, tok * e.cols + i);
 }
 
-// One CTA per (kv head, chunk); chunks past the current position have nothing
-// to do.  Launched as a programmatic dependent of the QKV GEMV: the rows cached
-// by earlier steps (and the position, written by the previous step's argmax)
-// are final before that GEMV starts, so they are copied before waiting for it;
-// q and the current position's K and V only after.
-template <int HD, int G, int C>
+// One CTA per (kv head, chunk).  The n = pos + 1 positions of a step are split
+// into per = max(32, ceil(n / chunks of the grid)) <= C positions per item, the
+// last item taking the rest, over used = ceil(n / per) items of each kv head
+// (items past those have nothing to do).  Launched as a programmatic dependent of the QKV GEMV: the
+// rows cached by earlier steps (and the position, written by the previous
+// step's argmax) are final before that GEMV starts, so they are copied before
+// waiting for it; q and the current position's K and V only after.
+template <int HD, int G, int CM>
 __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const __grid_constant__ AttnArgs a,
-                                                       const int32_t* __restrict__ d_pos) {
+                                                          const int32_t* __restrict__ d_pos) {
   extern __shared__ uint4 smem_u4[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(smem_u4);
   const int n = __ldcg(d_pos) + 1;
-  const int used = (n + C - 1) / C;
+  const int per = max(32, (n + int(gridDim.y) - 1) / int(gridDim.y));   // positions per item, <= C
+  const int used = (n + per - 1) / per;
   // the O projection may start its weight prefetch; it waits for this grid before reading its output
   asm volatile("griddepcontrol.launch_dependents;");
   if (int(blockIdx.y) >= used) return;
-  const int t0 = int(blockIdx.y) * C;
-  const int r_done = max(0, min(C, n - 1 - t0));   // rows of positions cached by earlier steps
-  attn_copy_rows<HD, C>(a, blockIdx.x, t0, 0, r_done, sm);
+  const int t0 = int(blockIdx.y) * per, cnt = min(per, n - t0);
+  const int r_done = max(0, min(cnt, n - 1 - t0));          // rows of positions cached by earlier steps
+  attn_copy_rows<HD, CM>(a, blockIdx.x, t0, 0, r_done, sm);
   asm volatile("cp.async.commit_group;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  attn_item<HD, G, C>(a, blockIdx.x, blockIdx.y, n, used, sm, r_done);
+  attn_item<HD, G, CM>(a, blockIdx.x, blockIdx.y, t0, cnt, used, sm, r_done);
 }
 
 // Greedy choice over the per-CTA top-2 summaries of the output GEMV (ties to the
@@ -295,18 +298,15 @@ struct Launcher {
 
 constexpr size_t kAttnMinSmem = 116 * 1024;   // more than half of an SM's shared memory
 
-template <int HD, int G>
-static cudaError_t launch_attn_t(dim3 grid, cudaStream_t s, const AttnArgs& a, const int32_t* pos, bool pdl) {
-  auto kern = a.chunk == 64 ? k_attn<HD, G, 64> : (a.chunk == 128 ? k_attn<HD, G, 128> : k_attn<HD, G, 256>);
-  size_t smem = a.chunk == 64 ? AttnLayout<HD, G, 64>::kBytes
-                              : (a.chunk == 128 ? AttnLayout<HD, G, 128>::kBytes : AttnLayout<HD, G, 256>::kBytes);
+template <int HD, int G, int CM>
+static cudaError_t launch_attn_cm(dim3 grid, cudaStream_t s, const AttnArgs& a, const int32_t* pos, bool pdl) {
+  auto kern = k_attn<HD, G, CM>;
   // one item per SM: the block scheduler would otherwise pack several small items
   // onto the first SMs the Q/K/V GEMV frees instead of spreading them
+  size_t smem = AttnLayout<HD, G, CM>::kBytes;
   if (smem < kAttnMinSmem) smem = kAttnMinSmem;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-  }
+  static const KernelSetup setup = kernel_setup(kern, int(smem));
+  if (setup.err != cudaSuccess) return setup.err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kAttnThreads);
@@ -318,6 +318,17 @@ static cudaError_t launch_attn_t(dim3 grid, cudaStream_t s, const AttnArgs& a, c
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, a, pos);
+}
+
+template <int HD, int G>
+static cudaError_t launch_attn_t(dim3 grid, cudaStream_t s, const AttnArgs& a, const int32_t* pos, bool pdl) {
+  switch (attn_chunk_max(a.chunk)) {
+    case 64: return launch_attn_cm<HD, G, 64>(grid, s, a, pos, pdl);
+    case 128: return launch_attn_cm<HD, G, 128>(grid, s, a, pos, pdl);
+    case 256: return launch_attn_cm<HD, G, 256>(grid, s, a, pos, pdl);
+    case 320: return launch_attn_cm<HD, G, 320>(grid, s, a, pos, pdl);
+  }
+  return cudaErrorInvalidValue;
 }
 
 static cudaError_t launch_attn(int hd, int G, dim3 grid, cudaStream_t s, const AttnArgs& a, const int32_t* pos,
