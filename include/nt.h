@@ -101,6 +101,9 @@ typedef struct {
   double overlap;          /* (h2d_ms + compute_ms - last_step_ms) / min(...), in [0,1] */
   int64_t weight_bytes;    /* quantized weight bytes read per step                  */
   int64_t kv_bytes_per_pos;/* KV cache bytes read per cached position per step      */
+  double verify_weight_bytes; /* layer weight bytes the verification pass of the last
+                              nt_speculative_step read (each multi-token launch reads
+                              its weights once)                                      */
 } nt_stats;
 
 /* Per-kernel-class device times of profiled steps (nt_profile_steps). */
@@ -234,9 +237,11 @@ nt_status nt_plan_layer_skip(const double* cos, int32_t n_layers, double thresho
  *   accept  j = the longest prefix with y_i == d_{i+1}; the emitted tokens are
  *           d_1..d_j, then y_j when j < k.
  * The emitted tokens are those nt_decode_step would produce from the same state,
- * bit for bit (every token runs the same kernels on the same inputs; layers
+ * bit for bit (every token gets the same arithmetic on the same inputs; layers
  * below n_draft are not recomputed, their K/V rows from the draft are the full
- * model's).  out_tokens (host, >= k entries) receives them, *n_out their count
+ * model's).  The verification runs each layer's GEMVs for several tokens per
+ * launch (as nt_gemv_q_batch), so a resident layer's weights are read fewer than
+ * k times; nt_stats.verify_weight_bytes reports the bytes read.  out_tokens (host, >= k entries) receives them, *n_out their count
  * (j + 1, or k when all are accepted), *n_accepted (nullable) j; the position
  * advances by *n_out.  Layers the skip mask names are skipped in both passes.
  * NT_E_INVAL: bad token, k or n_draft, or p + k > max_ctx. */
@@ -298,6 +303,19 @@ nt_status nt_dequant(const nt_qtensor* t, int64_t row0, int64_t nrows, float* de
  * writes y only after it.  dev_x and dev_y must not overlap and must be
  * 16-byte aligned. */
 nt_status nt_gemv_q(const nt_qtensor* t, const float* dev_x, float* dev_y, void* stream);
+
+/* y_i = W x_i for k vectors (1 <= k <= 8) in as few launches as fit: the
+ * verification GEMV of self-speculative decoding (hada "Hauptfunktionen"), where
+ * k draft tokens go through the same weights.  Each launch stages the x of up to
+ * four tokens beside its weight ring and multiplies every weight tile it copies
+ * by each of them, so the weights are read once per launch instead of once per
+ * vector; where fewer than two x fit, one launch per vector.  Every y_i is bit for
+ * bit what nt_gemv_q(t, dev_x[i], dev_y[i]) writes.  dev_x and dev_y are host
+ * arrays of k device pointers (16-byte aligned; no y may overlap an x or another
+ * y).  launches (nullable, host) receives the number of launches.  Asynchronous
+ * on stream.  NT_E_INVAL: k outside [1, 8], NULL or misaligned vectors, overlaps. */
+nt_status nt_gemv_q_batch(const nt_qtensor* t, const float* const* dev_x, float* const* dev_y, int32_t k,
+                          int32_t* launches, void* stream);
 
 /* ------------------------------------------------ allocation-free variant -- */
 

@@ -198,6 +198,7 @@ struct nt_model {
   int32_t* hist = nullptr;           // produced ids by position
   int32_t* h_io = nullptr;           // pinned host mirror of small; [32, 56): speculative step
   float* sp_x = nullptr;             // speculative step: residual of each draft token after the draft layers
+  float *sp_q = nullptr, *sp_att = nullptr, *sp_u = nullptr;   // speculative step: per-token q, attention output, u
   int32_t* sp_i = nullptr;           // speculative step: positions [0, 8), full-model tokens [8, 16), draft tokens [16, 24)
   float* cur_x = nullptr;            // residual the enqueue helpers use (nullptr: x)
   int32_t* cur_pos = nullptr;        // device position the enqueue helpers use (nullptr: the step's)
@@ -916,10 +917,67 @@ nt_status nt_set_layer_skip(nt_model* m, const uint8_t* mask) {
 }
 
 // Verification pass of a speculative cycle: layers [n_draft, n_layers) that the
-// skip mask keeps, layer by layer, each for the k draft tokens in order (token i
-// at position p + i from its residual after the draft layers); a host-tier layer
-// is copied once for all k.  Then the head for each token; token i's greedy
+// skip mask keeps, layer by layer, each for the k draft tokens (token i at
+// position p + i from its residual after the draft layers, enqueue_layer_batch:
+// a layer's weights are read once per multi-token launch); a host-tier layer is
+// copied once for all k.  Then the head for each token; token i's greedy
 // choice goes to sp_i[8 + i].  Returns the bytes copied from the host tier.
+// Layer l (weights at base) for the k tokens of a verification pass: token i
+// enters with residual sp_x[i] at position sp_i[i].  Each GEMV runs once for
+// several tokens (launch_gemv_batch: the weights are read once per launch, with
+// each token's single-token arithmetic); attention runs once per token, token i
+// over positions [0, p + i], after every token's K/V row of the layer is stored.
+// Bit for bit the same as k enqueue_layer calls in token order.
+static cudaError_t enqueue_layer_batch(nt_model* m, int l, uint8_t* base, Launcher& L, int k) {
+  const nt_config& c = m->c;
+  const int hd = c.head_dim, G = c.n_heads / c.n_kv_heads;
+  const size_t qd = size_t(c.n_heads) * hd, kd = size_t(c.n_kv_heads) * hd, h = size_t(c.hidden);
+  const size_t F = size_t(c.ffn_dim);
+  cudaStream_t s = L.s;
+  cudaError_t e;
+  const LayerGemvs g = layer_gemvs(m, l, base);
+  BatchTok qkv[8], o[8], gu[8], dn[8];
+  int nq = 0, no = 0, ng = 0, nd = 0;   // launches of each GEMV (each reads the GEMV's weights once)
+  for (int i = 0; i < k; i++) {
+    float* xi = m->sp_x + size_t(i) * h;
+    qkv[i] = {xi, m->sp_q + size_t(i) * qd, m->sp_i + i};
+    o[i] = {m->sp_att + size_t(i) * qd, xi, nullptr};
+    gu[i] = {xi, m->sp_u + size_t(i) * F, nullptr};
+    dn[i] = {m->sp_u + size_t(i) * F, xi, nullptr};
+  }
+  if (!g.v_split) {
+    const double by = gemv_bytes(g.qk, 4.0 * qd + 4.0 * kd);
+    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_batch(g.qk, EPI_QKV, qkv, k, 0, s, false, &nq); }))) return e;
+  } else {
+    const double by = gemv_bytes(g.qk, 4.0 * qd + 2.0 * kd) + gemv_bytes(g.v, 2.0 * kd) - 4.0 * c.hidden;
+    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_pair_batch(g.qk, g.v, EPI_QKV, qkv, qkv, k, s, false, &nq); })))
+      return e;
+  }
+  for (int i = 0; i < k; i++) {
+    const int n_used = m->pos + i + 1;
+    const double by = 2.0 * 2.0 * double(c.n_kv_heads) * n_used * hd + 8.0 * qd;
+    dim3 grid(unsigned(c.n_kv_heads), unsigned(m->n_chunks));
+    AttnArgs aa = attn_args(m, l);
+    aa.q = m->sp_q + size_t(i) * qd;
+    aa.out = m->sp_att + size_t(i) * qd;
+    const int32_t* pos = m->sp_i + i;
+    if ((e = L.run(NT_KC_ATTN, by, [&] { return launch_attn(hd, G, grid, s, aa, pos, false); }))) return e;
+  }
+  double by = gemv_bytes(g.o, 8.0 * c.hidden);
+  if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_batch(g.o, EPI_ADD, o, k, 0, s, false, &no); }))) return e;
+  by = gemv_bytes(g.gu, 4.0 * c.ffn_dim);
+  if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_batch(g.gu, EPI_SWIGLU, gu, k, 0, s, false, &ng); }))) return e;
+  by = gemv_bytes(g.down, 8.0 * c.hidden);
+  if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_batch(g.down, EPI_ADD, dn, k, 0, s, false, &nd); }))) return e;
+  // weight bytes the layer's launches read
+  const Layer& ly = m->layers[size_t(l)];
+  double wb = 0;
+  const int nl_[7] = {nq, nq, nq, no, ng, ng, nd};
+  for (int r = 0; r < 7; r++) wb += double(nl_[r]) * qbytes(view_at(ly, r, base));
+  m->stats.verify_weight_bytes += wb;
+  return cudaSuccess;
+}
+
 static cudaError_t enqueue_verify(nt_model* m, Launcher& L, int n_draft, int k, double* h2d_bytes) {
   const int nl = m->c.n_layers, nr = m->n_resident;
   const size_t h = size_t(m->c.hidden);
@@ -944,14 +1002,7 @@ static cudaError_t enqueue_verify(nt_model* m, Launcher& L, int n_draft, int k, 
     const int b = int(j & 1);
     uint8_t* base = streamed ? m->staging[b] : m->layers[size_t(l)].dev;
     if (streamed && (e = cudaStreamWaitEvent(s, m->ev_copy_done[b], 0))) return e;
-    for (int i = 0; i < k && !e; i++) {
-      m->cur_x = m->sp_x + size_t(i) * h;
-      m->cur_pos = m->sp_i + i;
-      e = enqueue_layer(m, l, base, L, false);
-    }
-    m->cur_x = nullptr;
-    m->cur_pos = nullptr;
-    if (e) return e;
+    if ((e = enqueue_layer_batch(m, l, base, L, k))) return e;
     if (streamed) {
       if ((e = cudaEventRecord(m->ev_compute_done[b], s))) return e;
       if (j + 2 < sl.size() && (e = issue_copy(j + 2))) return e;
@@ -978,8 +1029,12 @@ nt_status nt_speculative_step(nt_model* m, int32_t token, int32_t n_draft, int32
   if (m->pos + k > c.max_ctx) return fail(NT_E_INVAL, "nt_speculative_step: the cycle would pass max_ctx");
   const size_t h = size_t(c.hidden);
   if (!m->sp_x) {
+    const size_t qd = size_t(c.n_heads) * c.head_dim;
     NT_CUDA(dev_alloc(m, reinterpret_cast<void**>(&m->sp_x), 8 * h * 4));
     NT_CUDA(dev_alloc(m, reinterpret_cast<void**>(&m->sp_i), 32 * 4));
+    NT_CUDA(dev_alloc(m, reinterpret_cast<void**>(&m->sp_q), 8 * qd * 4));
+    NT_CUDA(dev_alloc(m, reinterpret_cast<void**>(&m->sp_att), 8 * qd * 4));
+    NT_CUDA(dev_alloc(m, reinterpret_cast<void**>(&m->sp_u), 8 * size_t(c.ffn_dim) * 4));
   }
   NT_CUDA(cudaStreamSynchronize(m->stream));
   const int32_t p = m->pos;
@@ -1022,6 +1077,7 @@ nt_status nt_speculative_step(nt_model* m, int32_t token, int32_t n_draft, int32
     Launcher L;
     L.s = m->stream;
     double vb = 0;
+    m->stats.verify_weight_bytes = 0;
     e = enqueue_verify(m, L, n_draft, k, &vb);
     if (e) return resync(cuda_fail(e, "nt_speculative_step: verification"));
     h2d += vb;

@@ -334,9 +334,12 @@ __device__ __forceinline__ float warp_reduce_rows(const float (&acc)[R], int lan
 
 // Epilogue of one finished row group: k is this lane's reduced row sum (valid
 // on lanes l % (32/R) == 0), rows grp*R + l/(32/R).  All lanes must call it.
+// y and pos: the output and the position counter (a.epi.y and a.epi.pos, or one
+// token's of a multi-token launch).
 template <int R, int EPI>
-__device__ __forceinline__ void epilogue(const GemvArgs& a, int64_t grp, int64_t nrows, int lane, float k,
-                                         float& best, int& best_i, float& second) {
+__device__ __forceinline__ void epilogue_to(const GemvArgs& a, float* y, const int32_t* pos, int64_t grp,
+                                            int64_t nrows, int lane, float k, float& best, int& best_i,
+                                            float& second) {
   constexpr int LPR = 32 / R;
   const int rr = lane / LPR;
   const int64_t row = grp * R + rr;
@@ -345,28 +348,28 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, int64_t grp, int64_t
   const float other = __shfl_down_sync(0xffffffffu, k, LPR);
   if (!holder) return;
   if (EPI == EPI_STORE) {
-    a.epi.y[row] = k;
+    y[row] = k;
   } else if (EPI == EPI_ADD) {
-    a.epi.y[row] = __fadd_rn(__ldcg(a.epi.y + row), k);
+    y[row] = __fadd_rn(__ldcg(y + row), k);
   } else if (EPI == EPI_LOGITS) {
-    a.epi.y[row] = k;
+    y[row] = k;
     top2_push(k, int(row), best, best_i, second);
   } else if ((rr & 1) == 0) {
     const float v0 = k, v1 = other;
     if (EPI == EPI_SWIGLU) {
-      a.epi.y[row >> 1] = __fmul_rn(silu(v0), v1);
+      y[row >> 1] = __fmul_rn(silu(v0), v1);
     } else {  // EPI_QKV: RoPE on q and k pairs, f16 store of k and v at the current position
       const int L = a.epi.row_base + int(row);
       const int hd = a.epi.head_dim;
-      const int p = __ldcg(a.epi.pos);
+      const int p = __ldcg(pos);
       if (L < a.epi.q_rows + a.epi.k_rows) {
         const int d = L % hd;
         const float2 cs = a.epi.rope[int64_t(p) * (hd / 2) + d / 2];
         const float r0 = __fmaf_rn(v0, cs.x, -__fmul_rn(v1, cs.y));
         const float r1 = __fmaf_rn(v0, cs.y, __fmul_rn(v1, cs.x));
         if (L < a.epi.q_rows) {
-          a.epi.y[L] = r0;
-          a.epi.y[L + 1] = r1;
+          y[L] = r0;
+          y[L + 1] = r1;
         } else {
           const int kr = L - a.epi.q_rows;
           __half* dst = a.epi.k_cache + (int64_t(kr / hd) * a.epi.max_ctx + p) * hd + d;
@@ -382,6 +385,12 @@ __device__ __forceinline__ void epilogue(const GemvArgs& a, int64_t grp, int64_t
       }
     }
   }
+}
+
+template <int R, int EPI>
+__device__ __forceinline__ void epilogue(const GemvArgs& a, int64_t grp, int64_t nrows, int lane, float k,
+                                         float& best, int& best_i, float& second) {
+  epilogue_to<R, EPI>(a, a.epi.y, a.epi.pos, grp, nrows, lane, k, best, best_i, second);
 }
 
 // CTA-wide top-2 of the rows this CTA finished, written to top2[blockIdx.x].

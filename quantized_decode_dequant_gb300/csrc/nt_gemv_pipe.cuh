@@ -610,10 +610,10 @@ __device__ __forceinline__ void stage_convert(float4 f0, float4 f1, int p, uint8
 // RMSNorm factor rsqrt(mean(x^2) + eps) from the staged per-block squares,
 // summed by one warp's lanes in a fixed order (1 without norm).
 template <int XS>
-__device__ __forceinline__ float x_scale(const GemvArgs& a, const uint8_t* xq) {
-  if (!a.norm) return 1.0f;
+__device__ __forceinline__ float x_scale_n(int norm, int64_t ncols, float eps, const uint8_t* xq) {
+  if (!norm) return 1.0f;
   const int lane = threadIdx.x & 31;
-  const int units = int(a.ncols / 32);
+  const int units = int(ncols / 32);
   constexpr int U = x_unit<XS>(), SQ = 32 * XS + 12;
   float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
   for (int b = lane; b < units; b += 128) {
@@ -625,7 +625,11 @@ __device__ __forceinline__ float x_scale(const GemvArgs& a, const uint8_t* xq) {
   float t = __fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3));
 #pragma unroll
   for (int o = 16; o; o >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, o));
-  return rsqrtf(t / float(a.ncols) + a.eps);
+  return rsqrtf(t / float(ncols) + eps);
+}
+template <int XS>
+__device__ __forceinline__ float x_scale(const GemvArgs& a, const uint8_t* xq) {
+  return x_scale_n<XS>(a.norm, a.ncols, a.eps, xq);
 }
 
 // Whole window staged up front by the CTA's NW warps (256-column pass p by warp
@@ -636,10 +640,10 @@ __device__ __forceinline__ float x_scale(const GemvArgs& a, const uint8_t* xq) {
 struct NoOp {
   __device__ __forceinline__ void operator()() const {}
 };
-template <int FMT, int NW, int XS, class F = NoOp>
-__device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xq, F between = F()) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, np = int(a.ncols / 256);
-  const float* x = a.x + a.col0;
+// The same for the window x[0, ncols) into xq, without the closing barrier.
+template <int FMT, int NW, int XS, class F>
+__device__ __forceinline__ void stage_x_from(const float* x, int64_t ncols, uint8_t* xq, F between) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, np = int(ncols / 256);
   bool first = true;
   for (int p0 = warp; p0 < np || first; p0 += 4 * NW) {
     float4 f[4][2];
@@ -660,8 +664,14 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xq, F betwee
     for (int i = 0; i < 4; i++)
       if (p0 + i * NW < np) stage_convert<FMT, XS>(f[i][0], f[i][1], p0 + i * NW, xq);
   }
+}
+
+template <int FMT, int NW, int XS, class F = NoOp>
+__device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xq, F between = F()) {
+  stage_x_from<FMT, NW, XS>(a.x + a.col0, a.ncols, xq, between);
   __syncthreads();
 }
+
 
 // Running top-2 of the rows a warp finished (EPI_LOGITS).
 struct Top2 {
@@ -802,6 +812,108 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe2(const __grid_co
   if (EPI == EPI_LOGITS) cta_top2<NW>(a1, blockIdx.x, t2.best, t2.best_i, t2.second);
 }
 
+// ---- multi-token launches (the verification of a speculative cycle) ---------
+// One GEMV for up to kBatchMax tokens with the same weights: each warp's weight
+// tiles are copied once and multiplied by every token's staged x.  Every
+// token's result is bit for bit the single-token kernel's with the same R and
+// epilogue: the same x staging and RMS factor, the same per-lane tile order, the
+// same warp reduction and epilogue.
+constexpr int kBatchMax = 4;
+struct BatchTok {
+  const float* x = nullptr;      // the token's input
+  float* y = nullptr;            // the token's output (EPI_QKV: its q rows; EPI_ADD: its residual; EPI_SWIGLU: u)
+  const int32_t* pos = nullptr;  // the token's position counter (EPI_QKV)
+};
+struct GemvBatch {
+  BatchTok tok[kBatchMax];
+  int32_t n = 0;
+};
+
+template <int FMT, int R, int S, int EPI, int NW>
+__global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe_batch(const __grid_constant__ GemvArgs a,
+                                                                      const __grid_constant__ GemvBatch b,
+                                                                      const int64_t nrows) {
+  using P = Pipe<FMT>;
+  constexpr int E = S - 1 < kPipeEarly ? S - 1 : kPipeEarly;
+  constexpr int XS = x_slices(EPI), XU = x_unit<XS>();
+  extern __shared__ float4 smem4[];
+  uint8_t* xq = reinterpret_cast<uint8_t*>(smem4);
+  const size_t xbytes = size_t(a.ncols / 32) * XU;   // one token's staged x (a multiple of 16 bytes)
+  uint8_t* ring = xq + size_t(b.n) * xbytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, kiters = int(a.ncols / 1024);
+  const WarpTiles w = warp_tiles(nrows, R, kiters, warp, NW, blockIdx.x, gridDim.x);
+  uint8_t* wring = ring + size_t(warp) * pipe_slice<FMT, R, S, 0>();
+  PipeCursor<FMT, R, S> cur;
+  cur.init(w, kiters, smem_addr(wring));
+  pipe_issue(cur, a, nrows, E);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int j = 0; j < b.n; j++) {
+    if (j == 0) stage_x_from<FMT, NW, XS>(b.tok[0].x + a.col0, a.ncols, xq, [&] { pipe_issue(cur, a, nrows, S - 1 - E); });
+    else stage_x_from<FMT, NW, XS>(b.tok[j].x + a.col0, a.ncols, xq + size_t(j) * xbytes, NoOp());
+  }
+  __syncthreads();
+  float scale[kBatchMax];
+#pragma unroll
+  for (int j = 0; j < kBatchMax; j++) scale[j] = j < b.n ? x_scale_n<XS>(a.norm, a.ncols, a.eps, xq + size_t(j) * xbytes) : 1.f;
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (w.ntiles == 0) return;
+
+  float acc[kBatchMax][R];
+#pragma unroll
+  for (int j = 0; j < kBatchMax; j++)
+#pragma unroll
+    for (int r = 0; r < R; r++) acc[j][r] = 0.f;
+  float best = -INFINITY, second = -INFINITY;
+  int best_i = 0x7fffffff;
+  int64_t c_grp = w.g0;
+  int c_it = 0;
+  const uint8_t* rd = wring;
+  const uint8_t* const rd_end = wring + S * R * P::RB;
+  const uint8_t* xp = xq + size_t(lane) * XU;   // this lane's x block of the tile (token 0)
+  typename P::Frag fr[R];
+  cp_wait<S - 2>();
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < R; r++) P::load(rd + r * P::RB, lane, fr[r]);
+#pragma unroll 1
+  for (int t = 0; t < w.ntiles; t++) {
+#pragma unroll
+    for (int j = 0; j < kBatchMax; j++) {
+      if (j < b.n) {
+        XBlock xb;
+        load_xblock<XS>(xp + size_t(j) * xbytes, xb);
+#pragma unroll
+        for (int r = 0; r < R; r++) acc[j][r] = __fadd_rn(acc[j][r], P::template compute<XS>(fr[r], lane, xb));
+      }
+    }
+    rd += R * P::RB;
+    if (rd == rd_end) rd = wring;
+    xp += 32 * XU;
+    if (++c_it == kiters) {
+      c_it = 0;
+      xp = xq + size_t(lane) * XU;
+#pragma unroll
+      for (int j = 0; j < kBatchMax; j++) {
+        if (j < b.n) {
+          float kk = warp_reduce_rows<R>(acc[j], lane);
+          kk = __fmul_rn(kk, scale[j]);
+          epilogue_to<R, EPI>(a, b.tok[j].y, b.tok[j].pos, c_grp, nrows, lane, kk, best, best_i, second);
+        }
+#pragma unroll
+        for (int r = 0; r < R; r++) acc[j][r] = 0.f;
+      }
+      c_grp += w.stride;
+    }
+    cp_wait<S - 3>();
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < R; r++) P::load(rd + r * P::RB, lane, fr[r]);
+    cur.template step<true>(a, nrows, lane);
+  }
+  cp_wait<0>();
+  __syncwarp();
+}
+
 inline size_t pipe_x_bytes(int64_t cols, int epi) {
   return size_t(cols / 32) * size_t(x_slices(epi) == 3 ? x_unit<3>() : x_unit<2>());
 }
@@ -869,6 +981,57 @@ cudaError_t launch_gemv_pipe_rs(const GemvArgs& a, int epi, cudaStream_t s, bool
   return cudaErrorInvalidValue;
 }
 
+template <int FMT, int R, int S, int EPI>
+cudaError_t launch_gemv_batch_t(const GemvArgs& a, const GemvBatch& b, cudaStream_t s, bool pdl) {
+  constexpr int NW = kPipeWarps;
+  const int64_t nrows = gemv_logical_rows(a);
+  const size_t smem = size_t(b.n) * pipe_x_bytes(a.ncols, EPI) + size_t(NW) * S * R * Pipe<FMT>::RB;
+  if (smem > size_t(kPipeMaxSmem) || b.n < 1 || b.n > kBatchMax) return cudaErrorInvalidValue;
+  auto kern = k_gemv_pipe_batch<FMT, R, S, EPI, NW>;
+  static const KernelSetup setup = kernel_setup(kern, kPipeMaxSmem);
+  if (setup.err != cudaSuccess) return setup.err;
+  // the grid of the single-token launch: one CTA per SM (capped by the groups)
+  const int64_t groups = (nrows + R - 1) / R;
+  int64_t want = (groups + NW - 1) / NW;
+  if (want < setup.sms) want = groups < setup.sms ? groups : setup.sms;
+  int64_t grid = setup.sms;
+  if (grid > want) grid = want;
+  if (grid > a.max_grid) grid = a.max_grid;
+  if (grid < 1) grid = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(unsigned(NW * 32));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a, b, nrows);
+}
+
+// Multi-token launch of one format: R fixed by the caller (the single-token
+// launch's), ring depth 3 or 4 (what fits beside the n staged x).
+template <int FMT>
+cudaError_t launch_gemv_batch_fmt(const GemvArgs& a, int epi, int R, int S, const GemvBatch& b, cudaStream_t s,
+                                  bool pdl) {
+#define NT_BATCH_EPI(RR, SS)                                                                  \
+  switch (epi) {                                                                              \
+    case EPI_ADD: return launch_gemv_batch_t<FMT, RR, SS, EPI_ADD>(a, b, s, pdl);             \
+    case EPI_QKV: return launch_gemv_batch_t<FMT, RR, SS, EPI_QKV>(a, b, s, pdl);             \
+    case EPI_SWIGLU: return launch_gemv_batch_t<FMT, RR, SS, EPI_SWIGLU>(a, b, s, pdl);       \
+    case EPI_STORE: return launch_gemv_batch_t<FMT, RR, SS, EPI_STORE>(a, b, s, pdl);         \
+  }
+  if (R == 4) {
+    if (S >= 4) { NT_BATCH_EPI(4, 4) } else { NT_BATCH_EPI(4, 3) }
+  } else {
+    if (S >= 4) { NT_BATCH_EPI(2, 4) } else { NT_BATCH_EPI(2, 3) }
+  }
+#undef NT_BATCH_EPI
+  return cudaErrorInvalidValue;
+}
+
 // Instantiated shapes: 16 warps per CTA (one CTA per SM) with S in {3, 4, 6, 8}
 // (R = 2) or {3, 4} (R = 4).  S is rounded down to the nearest instantiated depth.
 // (A depth of 5, which fits beside the x of 8192 and 28672 columns, measured 1%
@@ -918,8 +1081,9 @@ cudaError_t launch_gemv_pipe2_q4k_q6k(const GemvArgs& a1, const GemvArgs& a2, cu
   return cudaLaunchKernelEx(&cfg, kern, a1, a2, n1, n2);
 }
 
-#define NT_DECLARE_GEMV_PIPE(NAME) \
-  cudaError_t NAME(const GemvArgs& a, int epi, int R, int S, cudaStream_t s, bool pdl, int* grid_used);
+#define NT_DECLARE_GEMV_PIPE(NAME)                                                                          \
+  cudaError_t NAME(const GemvArgs& a, int epi, int R, int S, cudaStream_t s, bool pdl, int* grid_used);        \
+  cudaError_t NAME##_batch(const GemvArgs& a, int epi, int R, int S, const GemvBatch& b, cudaStream_t s, bool pdl);
 NT_DECLARE_GEMV_PIPE(launch_gemv_pipe_q8_0)
 NT_DECLARE_GEMV_PIPE(launch_gemv_pipe_q4_0)
 NT_DECLARE_GEMV_PIPE(launch_gemv_pipe_q4_k)

@@ -133,6 +133,17 @@ cudaError_t launch_gemv(const GemvArgs& a, int epi, cudaStream_t s, bool pdl, in
 // launches (nullable) receives 1 or 2.
 cudaError_t launch_gemv_pair(const GemvArgs& a1, const GemvArgs& a2, int epi, cudaStream_t s, bool pdl,
                              int* launches);
+// Several tokens through one GEMV (see launch_gemv_batch in nt_gemv.cu): token i
+// reads toks[i].x and writes toks[i].y (its position: toks[i].pos), each with
+// the arithmetic of its own single-token launch.
+struct BatchTok;
+// launches (nullable) receives the number of launches (per token when they do
+// not fit two at a time).
+cudaError_t launch_gemv_batch(const GemvArgs& a, int epi, const BatchTok* toks, int k, int R_single, cudaStream_t s,
+                              bool pdl, int* launches);
+cudaError_t launch_gemv_pair_batch(const GemvArgs& a1, const GemvArgs& a2, int epi, const BatchTok* toks1,
+                                   const BatchTok* toks2, int k, cudaStream_t s, bool pdl, int* launches);
+bool pipe_shape(int fmt, int64_t nrows, int64_t cols, int epi, int& R, int& S);
 
 // ------------------------------------------------------------ generator --
 // SplitMix64 output function (Steele, Lea, Flood, OOPSLA 2014) on the counter

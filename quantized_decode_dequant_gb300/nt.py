@@ -51,7 +51,7 @@ class nt_stats(C.Structure):
     _fields_ = [("steps", C.c_int64), ("pos", C.c_int32), ("n_resident", C.c_int32),
                 ("last_step_ms", C.c_double), ("h2d_bytes", C.c_double), ("h2d_ms", C.c_double),
                 ("compute_ms", C.c_double), ("overlap", C.c_double), ("weight_bytes", C.c_int64),
-                ("kv_bytes_per_pos", C.c_int64)]
+                ("kv_bytes_per_pos", C.c_int64), ("verify_weight_bytes", C.c_double)]
 
 
 class nt_kernel_times(C.Structure):
@@ -90,6 +90,7 @@ _SIGS = {
     "nt_qtensor_export": (C.c_int, [_vp, _i64, _i64, _vp, C.c_size_t]),
     "nt_dequant": (C.c_int, [_vp, _i64, _i64, _vp, _vp]),
     "nt_gemv_q": (C.c_int, [_vp, _vp, _vp, _vp]),
+    "nt_gemv_q_batch": (C.c_int, [_vp, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), _i32, C.POINTER(_i32), _vp]),
     "nt_gemv_argmax_noalloc": (C.c_int, [_vp, _vp, _vp, _vp, _vp, _vp]),
 }
 
@@ -322,6 +323,16 @@ def nt_dequant(t: int, row0: int, nrows: int, dev_out: int, stream=None) -> None
 
 def nt_gemv_q(t: int, dev_x: int, dev_y: int, stream=None) -> None:
     _check(lib().nt_gemv_q(t, dev_x, dev_y, _stream(stream)), "nt_gemv_q")
+
+
+def nt_gemv_q_batch(t: int, dev_xs, dev_ys, stream=None) -> int:
+    """y_i = W x_i for the k device vectors dev_xs[i] -> dev_ys[i]; returns the launches used."""
+    k = len(dev_xs)
+    xs = (C.c_void_p * k)(*dev_xs)
+    ys = (C.c_void_p * k)(*dev_ys)
+    n = C.c_int32()
+    _check(lib().nt_gemv_q_batch(t, xs, ys, k, C.byref(n), _stream(stream)), "nt_gemv_q_batch")
+    return int(n.value)
 
 
 def nt_gemv_argmax_noalloc(t: int, dev_x: int, dev_y: int, dev_index: int, dev_margin: int, stream=None) -> None:

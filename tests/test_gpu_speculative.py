@@ -83,6 +83,40 @@ def test_speculative_stream_equals_greedy_and_the_oracle(nt, n_draft, k, residen
     assert cycles == [(list(e), j) for e, j in want]
 
 
+# widths of whole 1024-column tiles: the verification's GEMVs run several tokens
+# per launch; seed 54 keeps every greedy margin above 0.018 for 50 steps (checked
+# with the oracle), so the comparison with the oracle's cycles always runs
+WIDE = dict(n_layers=3, hidden=1024, n_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=2048, vocab=512, max_ctx=96)
+
+
+@pytest.mark.parametrize("n_draft,k,resident", [(1, 4, 3), (0, 8, 3), (2, 3, 1)])
+def test_multi_token_verification_equals_greedy_and_the_oracle(nt, n_draft, k, resident):
+    cfg = nt.make_config(**WIDE, seed=54)
+    prefill = (20, 2)
+    m = nt.nt_model_create(cfg)
+    try:
+        nt.nt_kv_prefill(m, *prefill)
+        if resident < WIDE["n_layers"]:
+            nt.nt_stream_layers(m, resident, 2)
+        cycles = []
+        t = 9
+        layer_bytes = sum(nt.nt_qtensor_info(nt.nt_model_tensor(m, 0, r))[3] for r in range(7))
+        for _ in range(4):
+            e, j = nt.nt_speculative_step(m, t, n_draft, k)
+            cycles.append((e, j))
+            t = e[-1]
+            # the verified layers' weights are read fewer than k times per cycle
+            vb = nt.nt_get_stats(m).verify_weight_bytes
+            assert 0 < vb < k * layer_bytes * (WIDE["n_layers"] - n_draft)
+        stream = [x for e, _ in cycles for x in e]
+        assert stream == _greedy(nt, cfg, 9, len(stream), prefill)
+    finally:
+        nt.nt_model_destroy(m)
+    ospec = oracle.ModelSpec(**WIDE, seed=54)
+    want = oracle.speculative_cycles(ospec, n_draft, k, 9, 4, prefill=prefill, nthreads=os.cpu_count() or 8)
+    assert cycles == [(list(e), j) for e, j in want]
+
+
 def test_streamed_verification_copies_each_layer_once_per_cycle(nt):
     cfg = nt.make_config(**dict(SPEC, n_layers=4), seed=3)
     m = nt.nt_model_create(cfg)
