@@ -490,7 +490,9 @@ def measure(nt, torch, wl, steps: int, warmup: int, args, dist, world: int, loca
                     "h2d_GB_per_step": round(h2d_b / steps / 1e9, 3), "overlap": round(ov / steps, 4),
                     "compute_ms_per_step": round(comp_ms / steps, 3),
                     "pcie_gen5_x16_nominal_GB_s": 64.0, "link": host_link(local),
-                    "h2d_timing": "copy-stream CUDA events around each layer's copy"}
+                    "h2d_timing": "copy-stream CUDA events around each layer's copy",
+                    "h2d_probe_GB_s": h2d_probe(torch, 1 << 30), "cpu_numa_node": cpu_numa_node(),
+                    "h2d_probe": "best of 5 plain 1 GiB copies from page-locked memory, same process"}
             else:
                 ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 ev0.record(stream)
@@ -575,6 +577,37 @@ def host_link(local: int) -> str:
         if "PCIe Generation" in line or "Link Width" in line:
             return "PCIe"
     return "unknown"
+
+
+def h2d_probe(torch, nbytes: int, reps: int = 5) -> float:
+    """GB/s of one plain host-to-device copy of nbytes from page-locked memory
+    (the rate the link gives a single copy, the bound of a layer copy)."""
+    src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dst.copy_(src, non_blocking=True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = 0.0
+    for _ in range(reps):
+        ev0.record()
+        dst.copy_(src, non_blocking=True)
+        ev1.record()
+        torch.cuda.synchronize()
+        best = max(best, nbytes / (ev0.elapsed_time(ev1) * 1e-3) / 1e9)
+    del src, dst
+    return round(best, 1)
+
+
+def cpu_numa_node() -> int | None:
+    """NUMA node of the CPU this process runs on (Linux sysfs), None if unknown."""
+    try:
+        with open("/proc/self/stat") as f:
+            cpu = int(f.read().rsplit(")", 1)[1].split()[36])
+        for d in os.listdir(f"/sys/devices/system/cpu/cpu{cpu}"):
+            if d.startswith("node") and d[4:].isdigit():
+                return int(d[4:])
+    except (OSError, ValueError, IndexError):
+        pass
+    return None
 
 
 def run_ours(args, wl, rank, world, local, dist):

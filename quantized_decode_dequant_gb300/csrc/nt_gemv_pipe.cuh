@@ -12,9 +12,10 @@
 //
 // Arithmetic.  Each 32-column block of x is carried as 16-bit fixed point: an
 // fp32 scale sx = max|x|/32512 and integers t_c = round(x_c/sx) split as
-// t = 256 h + l with h, l int8.  The codes are exact small integers, so
+// t = 256 h + l, h = floor(t / 256) a signed byte and l = t mod 256 an unsigned
+// one (the two bytes of t).  The codes are exact small integers, so
 // sum_c q_c t_c = 256 sum q h + sum q l is computed exactly with DP4A (four
-// int8 products per instruction) and only the per-block combination with the
+// byte products per instruction) and only the per-block combination with the
 // fp16 scales is floating point, accumulated in fp32.  The offsets of the
 // formats use the staged block sums T = sum t:
 //   Q8_0  d sx S,                       S = 256 Sh + Sl
@@ -86,7 +87,8 @@ __device__ __forceinline__ void cp_wait() {
 }
 // One staged x block in registers.
 struct XBlock {
-  int h[8], m[8], l[8];   // int8 slices, four per word, in the format's element order (m: three slices only)
+  int h[8], m[8], l[8];   // byte slices, four per word, in the format's element order (m: three slices only;
+                          // l: unsigned with two slices)
   float sx;         // block scale
   int t0, t1;       // sums of t over elements 0..15 and 16..31
 };
@@ -118,6 +120,13 @@ __device__ __forceinline__ float xacc_f(int v) { return __int2float_rn(v); }
 
 // sum over words [W0, W1) of (codes . t): 256 (codes . h) + (codes . l), or
 // 4096 (codes . h) + 16 (codes . m) + (codes . l)
+// DP4A of signed code bytes with unsigned x bytes (the low slice of a two-slice x)
+__device__ __forceinline__ int dp4a_su(int a, int b, int c) {
+  int d;
+  asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 template <int W0, int W1, int XS>
 __device__ __forceinline__ xacc_t<XS> idot(const int (&c)[8], const XBlock& x) {
   int ah0 = 0, ah1 = 0, am0 = 0, am1 = 0, al0 = 0, al1 = 0;
@@ -125,10 +134,10 @@ __device__ __forceinline__ xacc_t<XS> idot(const int (&c)[8], const XBlock& x) {
   for (int k = W0; k < W1; k += 2) {
     ah0 = __dp4a(c[k], x.h[k], ah0);
     if (XS == 3) am0 = __dp4a(c[k], x.m[k], am0);
-    al0 = __dp4a(c[k], x.l[k], al0);
+    al0 = XS == 3 ? __dp4a(c[k], x.l[k], al0) : dp4a_su(c[k], x.l[k], al0);
     ah1 = __dp4a(c[k + 1], x.h[k + 1], ah1);
     if (XS == 3) am1 = __dp4a(c[k + 1], x.m[k + 1], am1);
-    al1 = __dp4a(c[k + 1], x.l[k + 1], al1);
+    al1 = XS == 3 ? __dp4a(c[k + 1], x.l[k + 1], al1) : dp4a_su(c[k + 1], x.l[k + 1], al1);
   }
   if constexpr (XS == 3) return (ah0 + ah1) * 4096 + ((am0 + am1) * 16 + (al0 + al1));
   else return (ah0 + ah1) * 256 + (al0 + al1);
@@ -147,7 +156,8 @@ template <int FMT> struct Pipe;
 
 template <> struct Pipe<NT_Q8_0> {
   static constexpr int CB = 32, RB = 32 * 32 + 64;
-  __device__ static int xbyte(int c) { return c; }   // natural order
+  static constexpr bool NIB = false;                 // x bytes in natural order
+  __device__ static int xbyte(int c) { return c; }
   // copy plan per row: code bytes per tile, then scale pieces (source, smem offset, bytes per tile, size)
   static constexpr int CODE_STRIDE = 1024, NPA = 4, NPB = 0;
   __device__ static const uint8_t* code_base(const QMat& m, int64_t e_row) { return m.q + e_row; }
@@ -179,6 +189,7 @@ __device__ __forceinline__ int nibble_xbyte(int c) { return (c & ~7) + ((c & 1) 
 
 template <> struct Pipe<NT_Q4_0> {
   static constexpr int CB = 16, RB = 32 * 16 + 64;
+  static constexpr bool NIB = true;
   __device__ static int xbyte(int c) { return nibble_xbyte(c); }
   static constexpr int CODE_STRIDE = 512, NPA = 4, NPB = 0;
   __device__ static const uint8_t* code_base(const QMat& m, int64_t e_row) { return m.q + (e_row >> 1); }
@@ -218,6 +229,7 @@ __device__ __forceinline__ float kquant_unit(const uint4 meta, int lane, const i
 
 template <> struct Pipe<NT_Q4_K> {
   static constexpr int CB = 16, RB = 32 * 16 + 64;
+  static constexpr bool NIB = true;
   __device__ static int xbyte(int c) { return nibble_xbyte(c); }
   static constexpr int CODE_STRIDE = 512, NPA = 4, NPB = 0;
   __device__ static const uint8_t* code_base(const QMat& m, int64_t e_row) { return m.q + (e_row >> 1); }
@@ -247,6 +259,7 @@ template <> struct Pipe<NT_Q4_K> {
 // (byte i of H, bit v: code word v's byte i), OR-ed in at bit 4 of each byte.
 template <> struct Pipe<NT_Q5_K> {
   static constexpr int CB = 16, RB = 32 * 16 + 128 + 64;
+  static constexpr bool NIB = true;
   __device__ static int xbyte(int c) { return nibble_xbyte(c); }
   // 8 pieces of fifth-bit words (128 bytes per row and tile), 4 of super-block meta
   static constexpr int CODE_STRIDE = 512, NPA = 12, NPB = 0;
@@ -292,6 +305,7 @@ template <> struct Pipe<NT_Q5_K> {
 
 template <> struct Pipe<NT_Q6_K> {
   static constexpr int CB = 16, RB = 32 * 16 + 256 + 64 + 16;
+  static constexpr bool NIB = true;
   __device__ static int xbyte(int c) { return nibble_xbyte(c); }
   // 16 pieces of high-bit words and 4 of sub-block scales (16 bytes), 2 four-byte pieces of d
   static constexpr int CODE_STRIDE = 512, NPA = 20, NPB = 2;
@@ -555,53 +569,74 @@ __device__ __forceinline__ void pipe_issue(Cur& cur, const GemvArgs& a, int64_t 
 // [256 p, 256 p + 256) of the window are eight blocks, four lanes per block,
 // eight consecutive elements per lane.  Per block: sx = max|x|/T (T = 32512 or
 // 520192), t = round(x/sx) split into the slices, the sums T0, T1 of t over
-// elements 0..15 and 16..31, and the sum of squares (each lane's eight in
-// element order, then the four lanes as (l0 + l1) + (l2 + l3)).
+// elements 0..15 and 16..31, and with norm the sum of squares (each lane's
+// eight in element order, then the four lanes as (l0 + l1) + (l2 + l3)).
+// |t| <= T needs no clamp: |x| <= max|x|, and x (T / max|x|) with its two
+// roundings exceeds T by less than T 2^-22 < 1/2 (a NaN x, which the maximum
+// skips, converts to 0).  Two slices are the two bytes of t, gathered with byte
+// permutes; three slices are rounded as 4096 h + 16 m + l.
 template <int FMT, int XS>
-__device__ __forceinline__ void stage_convert(float4 f0, float4 f1, int p, uint8_t* xq) {
+__device__ __forceinline__ void stage_convert(float4 f0, float4 f1, int p, uint8_t* xq, bool norm) {
   using P = Pipe<FMT>;
   const int lane = threadIdx.x & 31, q = lane & 3;          // q: eighth of the block
   const int blk = p * 8 + (lane >> 2);
   const float v[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-  float amax = 0.f, sq = __fmul_rn(v[0], v[0]);
+  float amax = 0.f;
 #pragma unroll
   for (int j = 0; j < 8; j++) amax = fmaxf(amax, fabsf(v[j]));
-#pragma unroll
-  for (int j = 1; j < 8; j++) sq = __fmaf_rn(v[j], v[j], sq);
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-  sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, 1));   // (l0 + l1), (l2 + l3)
-  sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, 2));   // then their sum
+  float sq = 0.f;
+  if (norm) {
+    sq = __fmul_rn(v[0], v[0]);
+#pragma unroll
+    for (int j = 1; j < 8; j++) sq = __fmaf_rn(v[j], v[j], sq);
+    sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, 1));   // (l0 + l1), (l2 + l3)
+    sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, 2));   // then their sum
+  }
   constexpr int kT = XS == 3 ? 520192 : 32512;   // 127 * 4096, 127 * 256
   const float inv = amax > 0.f ? float(kT) / amax : 0.f;
-  uint32_t hw[2] = {0, 0}, mw[2] = {0, 0}, lw[2] = {0, 0};
+  uint8_t* dst = xq + size_t(blk) * x_unit<XS>();
   int ts = 0;
+  if constexpr (XS == 2) {
+    int t[8];
 #pragma unroll
-  for (int j = 0; j < 8; j++) {
-    int t = __float2int_rn(__fmul_rn(v[j], inv));
-    t = max(-kT, min(kT, t));
-    ts += t;
-    int h, m = 0, l;
-    if (XS == 3) {
-      h = (t + 2048) >> 12;            // |h| <= 127
-      const int r = t - 4096 * h;      // -2048 .. 2047
-      m = r >> 4;                      // -128 .. 127
-      l = r & 15;                      // 0 .. 15
-    } else {
-      h = (t + 128) >> 8;
-      l = t - 256 * h;
+    for (int j = 0; j < 8; j++) {
+      t[j] = __float2int_rn(__fmul_rn(v[j], inv));
+      ts += t[j];
     }
-    const int b = P::xbyte(j);   // position inside this lane's eight bytes (the 8-group order)
-    hw[b >> 2] |= uint32_t(uint8_t(int8_t(h))) << (8 * (b & 3));
-    if (XS == 3) mw[b >> 2] |= uint32_t(uint8_t(int8_t(m))) << (8 * (b & 3));
-    lw[b >> 2] |= uint32_t(uint8_t(int8_t(l))) << (8 * (b & 3));
+    // the lane's eight bytes in the format's order: elements e0..e3, then e4..e7
+    constexpr int e1 = P::NIB ? 2 : 1, e2 = P::NIB ? 4 : 2, e3 = P::NIB ? 6 : 3;
+    constexpr int e4 = P::NIB ? 1 : 4, e5 = P::NIB ? 3 : 5, e6 = P::NIB ? 5 : 6;
+    auto bytes4 = [](int a, int b, int c, int d, unsigned sel) {   // byte sel of a, b, c, d
+      return __byte_perm(__byte_perm(a, b, sel), __byte_perm(c, d, sel), 0x5410);
+    };
+    const uint32_t h0 = bytes4(t[0], t[e1], t[e2], t[e3], 0x0051), h1 = bytes4(t[e4], t[e5], t[e6], t[7], 0x0051);
+    const uint32_t l0 = bytes4(t[0], t[e1], t[e2], t[e3], 0x0040), l1 = bytes4(t[e4], t[e5], t[e6], t[7], 0x0040);
+    *reinterpret_cast<uint2*>(dst + q * 8) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2*>(dst + 32 + q * 8) = make_uint2(l0, l1);
+  } else {
+    uint32_t hw[2] = {0, 0}, mw[2] = {0, 0}, lw[2] = {0, 0};
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      int t = __float2int_rn(__fmul_rn(v[j], inv));
+      t = max(-kT, min(kT, t));
+      ts += t;
+      const int h = (t + 2048) >> 12;   // |h| <= 127
+      const int r = t - 4096 * h;       // -2048 .. 2047
+      const int m = r >> 4;             // -128 .. 127
+      const int l = r & 15;             // 0 .. 15
+      const int b = P::xbyte(j);        // position inside this lane's eight bytes (the format's order)
+      hw[b >> 2] |= uint32_t(uint8_t(int8_t(h))) << (8 * (b & 3));
+      mw[b >> 2] |= uint32_t(uint8_t(int8_t(m))) << (8 * (b & 3));
+      lw[b >> 2] |= uint32_t(uint8_t(int8_t(l))) << (8 * (b & 3));
+    }
+    *reinterpret_cast<uint2*>(dst + q * 8) = make_uint2(hw[0], hw[1]);
+    *reinterpret_cast<uint2*>(dst + 32 + q * 8) = make_uint2(mw[0], mw[1]);
+    *reinterpret_cast<uint2*>(dst + 64 + q * 8) = make_uint2(lw[0], lw[1]);
   }
   const int t01 = ts + __shfl_xor_sync(0xffffffffu, ts, 1);   // lanes q = 0,1: elements 0..15; q = 2,3: 16..31
   const int t_hi = __shfl_xor_sync(0xffffffffu, t01, 2);
-  uint8_t* dst = xq + size_t(blk) * x_unit<XS>();
-  *reinterpret_cast<uint2*>(dst + q * 8) = make_uint2(hw[0], hw[1]);
-  if (XS == 3) *reinterpret_cast<uint2*>(dst + 32 + q * 8) = make_uint2(mw[0], mw[1]);
-  *reinterpret_cast<uint2*>(dst + 32 * (XS - 1) + q * 8) = make_uint2(lw[0], lw[1]);
   if (q == 0)
     *reinterpret_cast<uint4*>(dst + 32 * XS) =
         make_uint4(__float_as_uint(amax / float(kT)), uint32_t(t01), uint32_t(t_hi), __float_as_uint(sq));
@@ -634,21 +669,25 @@ __device__ __forceinline__ float x_scale(const GemvArgs& a, const uint8_t* xq) {
 
 // Whole window staged up front by the CTA's NW warps (256-column pass p by warp
 // p % NW); each warp loads up to four of its passes before converting any, so
-// the staging costs one memory latency.  between() runs after the first loads
-// are issued and before they are used (the caller issues weight copies there,
-// behind the x loads).
+// the staging costs one memory latency per 16384 columns.  between() runs
+// after the first loads are issued and before they are used (the caller issues
+// weight copies there, behind the x loads).  (Measured on GB300: loading up to
+// eight passes at once, one latency for any window, made the 70B step 1%
+// slower.)
 struct NoOp {
   __device__ __forceinline__ void operator()() const {}
 };
-// The same for the window x[0, ncols) into xq, without the closing barrier.
+// The same for the window x[0, ncols) into xq, without the closing barrier;
+// norm: keep the per-block sums of squares of an RMSNorm.
 template <int FMT, int NW, int XS, class F>
-__device__ __forceinline__ void stage_x_from(const float* x, int64_t ncols, uint8_t* xq, F between) {
+__device__ __forceinline__ void stage_x_from(const float* x, int64_t ncols, uint8_t* xq, bool norm, F between) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, np = int(ncols / 256);
+  constexpr int kPasses = 4;
   bool first = true;
-  for (int p0 = warp; p0 < np || first; p0 += 4 * NW) {
-    float4 f[4][2];
+  for (int p0 = warp; p0 < np || first; p0 += kPasses * NW) {
+    float4 f[kPasses][2];
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
+    for (int i = 0; i < kPasses; i++) {
       const int p = p0 + i * NW;
       if (p < np) {
         const float4* src = reinterpret_cast<const float4*>(x + size_t(p) * 256 + lane * 8);
@@ -661,14 +700,14 @@ __device__ __forceinline__ void stage_x_from(const float* x, int64_t ncols, uint
       first = false;
     }
 #pragma unroll
-    for (int i = 0; i < 4; i++)
-      if (p0 + i * NW < np) stage_convert<FMT, XS>(f[i][0], f[i][1], p0 + i * NW, xq);
+    for (int i = 0; i < kPasses; i++)
+      if (p0 + i * NW < np) stage_convert<FMT, XS>(f[i][0], f[i][1], p0 + i * NW, xq, norm);
   }
 }
 
 template <int FMT, int NW, int XS, class F = NoOp>
 __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xq, F between = F()) {
-  stage_x_from<FMT, NW, XS>(a.x + a.col0, a.ncols, xq, between);
+  stage_x_from<FMT, NW, XS>(a.x + a.col0, a.ncols, xq, a.norm != 0, between);
   __syncthreads();
 }
 
@@ -848,8 +887,10 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe_batch(const __gr
   pipe_issue(cur, a, nrows, E);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int j = 0; j < b.n; j++) {
-    if (j == 0) stage_x_from<FMT, NW, XS>(b.tok[0].x + a.col0, a.ncols, xq, [&] { pipe_issue(cur, a, nrows, S - 1 - E); });
-    else stage_x_from<FMT, NW, XS>(b.tok[j].x + a.col0, a.ncols, xq + size_t(j) * xbytes, NoOp());
+    if (j == 0)
+      stage_x_from<FMT, NW, XS>(b.tok[0].x + a.col0, a.ncols, xq, a.norm != 0,
+                                   [&] { pipe_issue(cur, a, nrows, S - 1 - E); });
+    else stage_x_from<FMT, NW, XS>(b.tok[j].x + a.col0, a.ncols, xq + size_t(j) * xbytes, a.norm != 0, NoOp());
   }
   __syncthreads();
   float scale[kBatchMax];
@@ -981,6 +1022,11 @@ cudaError_t launch_gemv_pipe_rs(const GemvArgs& a, int epi, cudaStream_t s, bool
   return cudaErrorInvalidValue;
 }
 
+// Formats with a four-row kernel (the 4-bit ones; the shapes' chooser takes four
+// rows for no other).
+template <int FMT>
+constexpr bool kFourRows = FMT == NT_Q4_0 || FMT == NT_Q4_K || FMT == NT_Q5_K;
+
 template <int FMT, int R, int S, int EPI>
 cudaError_t launch_gemv_batch_t(const GemvArgs& a, const GemvBatch& b, cudaStream_t s, bool pdl) {
   constexpr int NW = kPipeWarps;
@@ -1024,7 +1070,9 @@ cudaError_t launch_gemv_batch_fmt(const GemvArgs& a, int epi, int R, int S, cons
     case EPI_STORE: return launch_gemv_batch_t<FMT, RR, SS, EPI_STORE>(a, b, s, pdl);         \
   }
   if (R == 4) {
-    if (S >= 4) { NT_BATCH_EPI(4, 4) } else { NT_BATCH_EPI(4, 3) }
+    if constexpr (kFourRows<FMT>) {
+      if (S >= 4) { NT_BATCH_EPI(4, 4) } else { NT_BATCH_EPI(4, 3) }
+    }
   } else {
     if (S >= 4) { NT_BATCH_EPI(2, 4) } else { NT_BATCH_EPI(2, 3) }
   }
@@ -1033,15 +1081,19 @@ cudaError_t launch_gemv_batch_fmt(const GemvArgs& a, int epi, int R, int S, cons
 }
 
 // Instantiated shapes: 16 warps per CTA (one CTA per SM) with S in {3, 4, 6, 8}
-// (R = 2) or {3, 4} (R = 4).  S is rounded down to the nearest instantiated depth.
+// (R = 2) or {3, 4} (R = 4, 4-bit formats only).  S is rounded down to the
+// nearest instantiated depth.
 // (A depth of 5, which fits beside the x of 8192 and 28672 columns, measured 1%
 // slower on the 70B Q4_K_M step and no faster on the down projection.)
 template <int FMT>
 cudaError_t launch_gemv_pipe_fmt(const GemvArgs& a, int epi, int R, int S, cudaStream_t s, bool pdl,
                                  int* grid_used) {
   if (R == 4) {
-    if (S >= 4) return launch_gemv_pipe_rs<FMT, 4, 4, kPipeWarps>(a, epi, s, pdl, grid_used);
-    return launch_gemv_pipe_rs<FMT, 4, 3, kPipeWarps>(a, epi, s, pdl, grid_used);
+    if constexpr (kFourRows<FMT>) {
+      if (S >= 4) return launch_gemv_pipe_rs<FMT, 4, 4, kPipeWarps>(a, epi, s, pdl, grid_used);
+      return launch_gemv_pipe_rs<FMT, 4, 3, kPipeWarps>(a, epi, s, pdl, grid_used);
+    }
+    return cudaErrorInvalidValue;
   }
   if (S >= 8) return launch_gemv_pipe_rs<FMT, 2, 8, kPipeWarps>(a, epi, s, pdl, grid_used);
   if (S >= 6) return launch_gemv_pipe_rs<FMT, 2, 6, kPipeWarps>(a, epi, s, pdl, grid_used);
