@@ -56,7 +56,9 @@ __host__ __device__ constexpr int x_slices(int epi) { return epi == EPI_QKV ? 3 
 // Before the producer of x is done only the first kPipeEarly tiles of a warp's
 // ring are copied: the x loads of the staging that follows would otherwise queue
 // behind a whole ring of weight copies; the rest is issued once x is staged.
-constexpr int kPipeEarly = 2;
+// (Measured on GB300: one tile made the 70B step 0.2% faster than two, a whole
+// ring 1% slower.)
+constexpr int kPipeEarly = 1;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -808,7 +810,10 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe(const __grid_con
 // run on as one range over the warps, a1's first; each warp works through its
 // a1 groups, then its a2 groups, with each format's own ring depth in one
 // per-warp slice.  Used for a Q4_K Q/K GEMV (four rows per warp, each x read
-// shared by four rows) with a Q6_K V GEMV (two).
+// shared by four rows) with a Q6_K V GEMV (two).  (Measured on GB300: cutting
+// the V groups into column parts spread over the warps of a CTA, added in
+// shared memory, balanced the launch and made the GEMVs 2.5% faster, yet the
+// 70B decode step 0.4% slower.)
 template <int F1, int F2, int R1, int R2, int S1, int S2, int EPI, int NW>
 __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe2(const __grid_constant__ GemvArgs a1,
                                                        const __grid_constant__ GemvArgs a2, const int64_t n1,
