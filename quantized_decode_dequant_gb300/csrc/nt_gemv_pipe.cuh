@@ -174,9 +174,15 @@ template <> struct Pipe<NT_Q8_0> {
     uint4 c0, c1;
     uint32_t d;
   };
+  // Lanes 4..7 of every eight read the second 16 bytes of their 32 first: the
+  // eight lanes of one phase of a 16-byte shared load then hit eight distinct
+  // 16-byte bank slots (at a 32-byte lane stride lanes j and j + 4 would share one).
   __device__ static void load(const uint8_t* blk, int lane, Frag& f) {
-    f.c0 = *reinterpret_cast<const uint4*>(blk + lane * 32);
-    f.c1 = *reinterpret_cast<const uint4*>(blk + lane * 32 + 16);
+    const int sw = (lane >> 2) & 1;
+    const uint4 u0 = *reinterpret_cast<const uint4*>(blk + lane * 32 + 16 * sw);
+    const uint4 u1 = *reinterpret_cast<const uint4*>(blk + lane * 32 + 16 * (sw ^ 1));
+    f.c0 = sw ? u1 : u0;
+    f.c1 = sw ? u0 : u1;
     f.d = *reinterpret_cast<const uint16_t*>(blk + 1024 + lane * 2);
   }
   template <int XS>
