@@ -318,9 +318,9 @@ def per_kernel_launches(spec) -> int:
 # DRAM bytes (read + write) per algorithmic byte of the step's GEMV launches, per
 # workload, from the ncu captures summarised in profiles/, and the SHA-256 of the
 # kernel sources they were taken on: a changed kernel reports no traffic.
-GEMV_DRAM_PER_BYTE: dict[str, float] = {}
+GEMV_DRAM_PER_BYTE: dict[str, float] = {"llama70b_q4_k_m": 1.047, "llama8b_q8_0": 1.013}
 GEMV_SOURCES = ("nt_gemv_pipe.cuh", "nt_gemv.cuh")
-GEMV_SOURCES_SHA256 = ""
+GEMV_SOURCES_SHA256 = "d6ce110bbed9f9a79239a1b87d7e61c04dc7bb5686d5c9772c8b520894932418"
 
 
 def gemv_sources_sha256() -> str:
@@ -455,22 +455,29 @@ def measure(nt, torch, wl, steps: int, warmup: int, args, dist, world: int, loca
                 # cycles until `steps` tokens are emitted; each cycle copies the
                 # host-tier layers once for up to K tokens
                 t0 = time.perf_counter()
-                t, emitted, cycles, accepted, h2d_b = tok0, 0, 0, 0, 0.0
+                t, emitted, cycles, accepted, h2d_b, vw_b = tok0, 0, 0, 0, 0.0, 0.0
                 while emitted < steps:
                     e, j = nt.nt_speculative_step(m, t, n_draft, args.speculative)
                     t = e[-1]
                     emitted += len(e)
                     cycles += 1
                     accepted += j
-                    h2d_b += nt.nt_get_stats(m).h2d_bytes
+                    st = nt.nt_get_stats(m)
+                    h2d_b += st.h2d_bytes
+                    vw_b += st.verify_weight_bytes
                 torch.cuda.synchronize()
                 sec = (time.perf_counter() - t0) * steps / emitted
                 out["speculative"] = {"k": args.speculative, "draft_layers": n_draft, "cycles": cycles,
                                       "tokens": emitted, "tokens_per_cycle": round(emitted / cycles, 3),
                                       "accepted_per_cycle": round(accepted / cycles, 3),
                                       "h2d_GB_per_token": round(h2d_b / emitted / 1e9, 3),
+                                      "verify_weight_GB_per_cycle": round(vw_b / cycles / 1e9, 3),
+                                      "verified_layers_weight_GB": round(
+                                          (W.weight_bytes(dict(spec, n_layers=spec["n_layers"] - n_draft))
+                                           - W.weight_bytes(dict(spec, n_layers=0))) / 1e9, 3),
                                       "note": "acceptance is meaningless on random weights; the cycle cost is "
-                                              "the measurement"}
+                                              "the measurement (verification reads each verified layer's weights "
+                                              "once per multi-token launch, not once per token)"}
             elif streamed:
                 t0 = time.perf_counter()
                 t = tok0
