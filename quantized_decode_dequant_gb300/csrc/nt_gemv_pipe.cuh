@@ -57,7 +57,9 @@ __host__ __device__ constexpr int x_slices(int epi) { return epi == EPI_QKV ? 3 
 // ring are copied: the x loads of the staging that follows would otherwise queue
 // behind a whole ring of weight copies; the rest is issued once x is staged.
 // (Measured on GB300: one tile made the 70B step 0.2% faster than two, a whole
-// ring 1% slower, and none 1.4% slower, 3.2% for the 8B step.)
+// ring 1% slower, and none 1.4% slower, 3.2% for the 8B step.  A bulk L2
+// prefetch of each warp's next eight tiles of codes, issued with that tile, made
+// the 70B step 2.3% slower.)
 constexpr int kPipeEarly = 1;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
