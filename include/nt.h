@@ -126,7 +126,10 @@ const char* nt_last_error(void);
  * quantizes every weight on the device.  Position starts at 0.
  * NT_E_INVAL: non-positive sizes, n_heads not a multiple of n_kv_heads,
  * head_dim odd, a column count not a multiple of the role format's block,
- * unsupported format.  NT_E_NOMEM: device allocation failed. */
+ * unsupported format.  NT_E_NOMEM: device allocation failed, or the model's
+ * device allocations would pass the byte cap in the environment variable
+ * NT_DEVICE_BYTES_LIMIT (decimal bytes; unset: no cap), a host-side stand-in
+ * for running out of device memory. */
 nt_status nt_model_create(const nt_config* cfg, nt_model** out);
 void nt_model_destroy(nt_model* m);
 
