@@ -131,6 +131,17 @@ __device__ __forceinline__ int dp4a_su(int a, int b, int c) {
   return d;
 }
 
+__device__ __forceinline__ int dp4a_us(int a, int b, int c) {   // unsigned a bytes, signed b bytes
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_uu(int a, int b, int c) {   // unsigned a and b bytes
+  int d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 template <int W0, int W1, int XS>
 __device__ __forceinline__ xacc_t<XS> idot(const int (&c)[8], const XBlock& x) {
   int ah0 = 0, ah1 = 0, am0 = 0, am1 = 0, al0 = 0, al1 = 0;
@@ -145,6 +156,36 @@ __device__ __forceinline__ xacc_t<XS> idot(const int (&c)[8], const XBlock& x) {
   }
   if constexpr (XS == 3) return (ah0 + ah1) * 4096 + ((am0 + am1) * 16 + (al0 + al1));
   else return (ah0 + ah1) * 256 + (al0 + al1);
+}
+
+// (codes . t) over one lane's 32 nibble codes straight from the four code words
+// w: the low nibbles (elements 8k+0,2,4,6 of word k) are masked to bytes; the
+// high nibbles (8k+1,3,5,7) stay in place as 16 x code (mask 0xF0), go through
+// DP4A as unsigned bytes, and their sums are divided by 16 exactly at the end.
+// The same integer as idot over nibble_bytes(w), one shift fewer per word.
+template <int XS>
+__device__ __forceinline__ xacc_t<XS> idot_nib(const uint4 w, const XBlock& x) {
+  const uint32_t L = 0x0F0F0F0Fu, H = 0xF0F0F0F0u;
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  int hl = 0, ml = 0, ll = 0, hh = 0, mh = 0, lh = 0;   // slice x (low | high nibbles)
+#pragma unroll
+  for (int k = 0; k < 4; k++) {
+    const int lo = int(ws[k] & L), hi = int(ws[k] & H);
+    hl = __dp4a(lo, x.h[2 * k], hl);
+    hh = dp4a_us(hi, x.h[2 * k + 1], hh);
+    if (XS == 3) {
+      ml = __dp4a(lo, x.m[2 * k], ml);
+      mh = dp4a_us(hi, x.m[2 * k + 1], mh);
+      ll = __dp4a(lo, x.l[2 * k], ll);
+      lh = dp4a_us(hi, x.l[2 * k + 1], lh);
+    } else {
+      ll = dp4a_su(lo, x.l[2 * k], ll);
+      lh = dp4a_uu(hi, x.l[2 * k + 1], lh);
+    }
+  }
+  // hh, mh, lh are 16 x the high nibbles' sums, exact multiples of 16
+  if constexpr (XS == 3) return (hl * 4096 + hh * 256) + ((ml * 16 + mh) + (ll + (lh >> 4)));
+  else return (hl * 256 + hh * 16) + (ll + (lh >> 4));
 }
 
 // even and odd nibbles of each code word as bytes: words 2k (elements 8k+0,2,4,6) and 2k+1 (8k+1,3,5,7)
@@ -220,21 +261,23 @@ template <> struct Pipe<NT_Q4_0> {
   }
   template <int XS>
   __device__ static float compute(const Frag& f, int lane, const XBlock& x) {
-    int c[8];
-    nibble_bytes(f.w, c);
-    return __fmul_rn(__fmul_rn(h2f_bits(f.d), x.sx), xacc_f(idot<0, 8, XS>(c, x) - xacc_t<XS>(8) * (x.t0 + x.t1)));
+    return __fmul_rn(__fmul_rn(h2f_bits(f.d), x.sx), xacc_f(idot_nib<XS>(f.w, x) - xacc_t<XS>(8) * (x.t0 + x.t1)));
   }
 };
 
 // One K-quant sub-block (Q4_K / Q5_K): sx * (d sc_j * sum q x - dmin m_j * sum x),
 // unit `lane` of the tile is sub-block j = lane % 8 of super-block lane / 8.
 template <int XS>
-__device__ __forceinline__ float kquant_unit(const uint4 meta, int lane, const int (&c)[8], const XBlock& x) {
+__device__ __forceinline__ float kquant_unit_s(const uint4 meta, int lane, xacc_t<XS> dot, const XBlock& x) {
   uint32_t sc, mm;
   kquant_scale_min(meta, lane & 7, sc, mm);
   const float a = __fmul_rn(h2f_bits(meta.x & 0xFFFFu), float(sc));
   const float b = __fmul_rn(h2f_bits(meta.x >> 16), float(mm));
-  return __fmul_rn(x.sx, __fmaf_rn(a, xacc_f(idot<0, 8, XS>(c, x)), -__fmul_rn(b, __int2float_rn(x.t0 + x.t1))));
+  return __fmul_rn(x.sx, __fmaf_rn(a, xacc_f(dot), -__fmul_rn(b, __int2float_rn(x.t0 + x.t1))));
+}
+template <int XS>
+__device__ __forceinline__ float kquant_unit(const uint4 meta, int lane, const int (&c)[8], const XBlock& x) {
+  return kquant_unit_s<XS>(meta, lane, idot<0, 8, XS>(c, x), x);
 }
 
 template <> struct Pipe<NT_Q4_K> {
@@ -259,9 +302,7 @@ template <> struct Pipe<NT_Q4_K> {
   }
   template <int XS>
   __device__ static float compute(const Frag& f, int lane, const XBlock& x) {
-    int c[8];
-    nibble_bytes(f.w, c);
-    return kquant_unit<XS>(f.meta, lane, c, x);
+    return kquant_unit_s<XS>(f.meta, lane, idot_nib<XS>(f.w, x), x);
   }
 };
 
