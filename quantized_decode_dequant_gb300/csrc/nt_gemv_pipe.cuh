@@ -16,8 +16,9 @@
 // one (the two bytes of t).  The codes are exact small integers, so
 // sum_c q_c t_c = 256 sum q h + sum q l is computed exactly with DP4A (four
 // byte products per instruction) and only the per-block combination with the
-// fp16 scales is floating point, accumulated in fp32.  The offsets of the
-// formats use the staged block sums T = sum t:
+// fp16 scales is floating point, accumulated in fp32 (the block's x scale sx
+// joins in the accumulating FMA).  The offsets of the formats use the staged
+// block sums T = sum t:
 //   Q8_0  d sx S,                       S = 256 Sh + Sl
 //   Q4_0  d sx (S - 8 T)
 //   Q4_K  sx (d sc S - dmin m T)
@@ -232,7 +233,7 @@ template <> struct Pipe<NT_Q8_0> {
   __device__ static float compute(const Frag& f, int lane, const XBlock& x) {
     const int c[8] = {int(f.c0.x), int(f.c0.y), int(f.c0.z), int(f.c0.w),
                       int(f.c1.x), int(f.c1.y), int(f.c1.z), int(f.c1.w)};
-    return __fmul_rn(__fmul_rn(h2f_bits(f.d), x.sx), xacc_f(idot<0, 8, XS>(c, x)));
+    return __fmul_rn(h2f_bits(f.d), xacc_f(idot<0, 8, XS>(c, x)));
   }
 };
 
@@ -261,7 +262,7 @@ template <> struct Pipe<NT_Q4_0> {
   }
   template <int XS>
   __device__ static float compute(const Frag& f, int lane, const XBlock& x) {
-    return __fmul_rn(__fmul_rn(h2f_bits(f.d), x.sx), xacc_f(idot_nib<XS>(f.w, x) - xacc_t<XS>(8) * (x.t0 + x.t1)));
+    return __fmul_rn(h2f_bits(f.d), xacc_f(idot_nib<XS>(f.w, x) - xacc_t<XS>(8) * (x.t0 + x.t1)));
   }
 };
 
@@ -271,9 +272,10 @@ template <int XS>
 __device__ __forceinline__ float kquant_unit_s(const uint4 meta, int lane, xacc_t<XS> dot, const XBlock& x) {
   uint32_t sc, mm;
   kquant_scale_min(meta, lane & 7, sc, mm);
-  const float a = __fmul_rn(h2f_bits(meta.x & 0xFFFFu), float(sc));
-  const float b = __fmul_rn(h2f_bits(meta.x >> 16), float(mm));
-  return __fmul_rn(x.sx, __fmaf_rn(a, xacc_f(dot), -__fmul_rn(b, __int2float_rn(x.t0 + x.t1))));
+  const float2 dm = __half22float2(*reinterpret_cast<const __half2*>(&meta.x));   // (d, dmin)
+  const float a = __fmul_rn(dm.x, float(sc));
+  const float b = __fmul_rn(dm.y, float(mm));
+  return __fmaf_rn(a, xacc_f(dot), -__fmul_rn(b, __int2float_rn(x.t0 + x.t1)));
 }
 template <int XS>
 __device__ __forceinline__ float kquant_unit(const uint4 meta, int lane, const int (&c)[8], const XBlock& x) {
@@ -408,7 +410,7 @@ template <> struct Pipe<NT_Q6_K> {
     const xacc_t<XS> s0 = idot<0, 4, XS>(c, x) - xacc_t<XS>(32) * x.t0;
     const xacc_t<XS> s1 = idot<4, 8, XS>(c, x) - xacc_t<XS>(32) * x.t1;
     const float sc0 = float(int8_t(sc2 & 0xFF)), sc1 = float(int8_t(sc2 >> 8));
-    return __fmul_rn(__fmul_rn(d, x.sx), __fmaf_rn(sc0, xacc_f(s0), __fmul_rn(sc1, xacc_f(s1))));
+    return __fmul_rn(d, __fmaf_rn(sc0, xacc_f(s0), __fmul_rn(sc1, xacc_f(s1))));
   }
 };
 
@@ -434,14 +436,6 @@ __device__ __forceinline__ WarpTiles warp_tiles(int64_t nrows, int R, int kiters
   w.stride = int64_t(ncta) * nw;
   w.ntiles = w.g0 < ngroups ? int((ngroups - 1 - w.g0) / w.stride + 1) * kiters : 0;
   return w;
-}
-
-// Dot product of one row unit straight from shared memory.
-template <int FMT, int XS>
-__device__ __forceinline__ float pipe_dot(const uint8_t* blk, int lane, const XBlock& x) {
-  typename Pipe<FMT>::Frag f;
-  Pipe<FMT>::load(blk, lane, f);
-  return Pipe<FMT>::template compute<XS>(f, lane, x);
 }
 
 // Copy cursor of one warp over its tiles.  Every lane issues the same copies
@@ -803,7 +797,7 @@ __device__ __forceinline__ void pipe_loop_w(const GemvArgs& a, int64_t nrows, co
 #pragma unroll 1
   for (int t = 0; t < w.ntiles; t++) {
 #pragma unroll
-    for (int r = 0; r < R; r++) acc[r] = __fadd_rn(acc[r], P::template compute<XS>(fr[r], lane, xb));   // dead rows read zeros
+    for (int r = 0; r < R; r++) acc[r] = __fmaf_rn(xb.sx, P::template compute<XS>(fr[r], lane, xb), acc[r]);   // dead rows read zeros
     rd += R * P::RB;
     if (rd == rd_end) rd = wring;
     xp += 32 * XU;
@@ -979,7 +973,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe_batch(const __gr
         XBlock xb;
         load_xblock<XS>(xp + size_t(j) * xbytes, xb);
 #pragma unroll
-        for (int r = 0; r < R; r++) acc[j][r] = __fadd_rn(acc[j][r], P::template compute<XS>(fr[r], lane, xb));
+        for (int r = 0; r < R; r++) acc[j][r] = __fmaf_rn(xb.sx, P::template compute<XS>(fr[r], lane, xb), acc[j][r]);
       }
     }
     rd += R * P::RB;
