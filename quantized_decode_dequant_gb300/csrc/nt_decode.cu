@@ -206,6 +206,12 @@ struct nt_model {
   cudaStream_t stream = nullptr, copy_stream = nullptr;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
+  // graph of a resident model's speculative cycle (draft and verification) for
+  // one draft depth, k and skip mask; verification weight bytes it reads
+  cudaGraphExec_t sp_exec = nullptr;
+  int sp_n_draft = -1, sp_k = -1;
+  std::vector<uint8_t> sp_skip;
+  double sp_vwb = 0;
   int out_grid = 0;
   int32_t pos = 0;
   int n_resident = 0;
@@ -545,6 +551,9 @@ static cudaError_t enqueue_streamed(nt_model* m, Launcher& L, float* hs, float* 
   auto issue_copy = [&](size_t k) -> cudaError_t { return issue_layer_copy(m, sl[k], int(k & 1), true); };
   for (size_t k = 0; k < sl.size() && k < 2; k++)
     if ((e = issue_copy(k))) return e;
+  // programmatic dependent launch when only resident layers run and no copy or
+  // event sits between the launches (a speculative draft); per-layer events otherwise
+  const bool pdl = sl.empty() && !hs;
   if ((e = enqueue_embed(m, L))) return e;
   size_t k = 0;
   for (int l = 0; l < nl; l++) {
@@ -555,9 +564,9 @@ static cudaError_t enqueue_streamed(nt_model* m, Launcher& L, float* hs, float* 
     if (hs && (e = cudaMemcpyAsync(hs + size_t(l) * m->c.hidden, m->x, xbytes, cudaMemcpyDeviceToDevice, s)))
       return e;
     if (streamed && (e = cudaStreamWaitEvent(s, m->ev_copy_done[b], 0))) return e;
-    if ((e = cudaEventRecord(m->ev_ls[size_t(l)], s))) return e;
-    if ((e = enqueue_layer(m, l, base, L, false))) return e;
-    if ((e = cudaEventRecord(m->ev_le[size_t(l)], s))) return e;
+    if (!pdl && (e = cudaEventRecord(m->ev_ls[size_t(l)], s))) return e;
+    if ((e = enqueue_layer(m, l, base, L, pdl))) return e;
+    if (!pdl && (e = cudaEventRecord(m->ev_le[size_t(l)], s))) return e;
     if (streamed) {
       if ((e = cudaEventRecord(m->ev_compute_done[b], s))) return e;
       if (k + 2 < sl.size() && (e = issue_copy(k + 2))) return e;
@@ -572,7 +581,7 @@ static cudaError_t enqueue_streamed(nt_model* m, Launcher& L, float* hs, float* 
       if ((e = cudaGetLastError())) return e;
     }
   }
-  return enqueue_head(m, L, false);
+  return enqueue_head(m, L, pdl);
 }
 
 static double watchdog_ms() {
@@ -603,6 +612,9 @@ static void drop_graph(nt_model* m) {
   if (m->graph) cudaGraphDestroy(m->graph);
   m->exec = nullptr;
   m->graph = nullptr;
+  if (m->sp_exec) cudaGraphExecDestroy(m->sp_exec);
+  m->sp_exec = nullptr;
+  m->sp_n_draft = m->sp_k = -1;
 }
 
 static nt_status ensure_graph(nt_model* m) {
@@ -916,19 +928,28 @@ nt_status nt_set_layer_skip(nt_model* m, const uint8_t* mask) {
   return NT_OK;
 }
 
+// The draft's tokens d_1..d_k of a speculative cycle from the token history at
+// positions sp_i[0] .. sp_i[0] + k - 1 into sp_i[16 .. 16 + k) (one warp; the
+// position comes from device memory, so a captured cycle replays at any position).
+__global__ void k_draft_tokens(const int32_t* __restrict__ hist, int32_t* sp_i, int k) {
+  const int j = int(threadIdx.x);
+  if (j < k) sp_i[16 + j] = hist[sp_i[0] + j];
+}
+
 // Verification pass of a speculative cycle: layers [n_draft, n_layers) that the
 // skip mask keeps, layer by layer, each for the k draft tokens (token i at
 // position p + i from its residual after the draft layers, enqueue_layer_batch:
 // a layer's weights are read once per multi-token launch); a host-tier layer is
 // copied once for all k.  Then the head for each token; token i's greedy
 // choice goes to sp_i[8 + i].  Returns the bytes copied from the host tier.
-// Layer l (weights at base) for the k tokens of a verification pass: token i
+// Layer l (weights at base) for the k tokens of a verification pass (pdl: its
+// GEMVs with programmatic dependent launch, for resident layers): token i
 // enters with residual sp_x[i] at position sp_i[i].  Each GEMV runs once for
 // several tokens (launch_gemv_batch: the weights are read once per launch, with
 // each token's single-token arithmetic); attention runs once per token, token i
 // over positions [0, p + i], after every token's K/V row of the layer is stored.
 // Bit for bit the same as k enqueue_layer calls in token order.
-static cudaError_t enqueue_layer_batch(nt_model* m, int l, uint8_t* base, Launcher& L, int k) {
+static cudaError_t enqueue_layer_batch(nt_model* m, int l, uint8_t* base, Launcher& L, int k, bool pdl) {
   const nt_config& c = m->c;
   const int hd = c.head_dim, G = c.n_heads / c.n_kv_heads;
   const size_t qd = size_t(c.n_heads) * hd, kd = size_t(c.n_kv_heads) * hd, h = size_t(c.hidden);
@@ -947,10 +968,10 @@ static cudaError_t enqueue_layer_batch(nt_model* m, int l, uint8_t* base, Launch
   }
   if (!g.v_split) {
     const double by = gemv_bytes(g.qk, 4.0 * qd + 4.0 * kd);
-    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_batch(g.qk, EPI_QKV, qkv, k, 0, s, false, &nq); }))) return e;
+    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_batch(g.qk, EPI_QKV, qkv, k, 0, s, pdl, &nq); }))) return e;
   } else {
     const double by = gemv_bytes(g.qk, 4.0 * qd + 2.0 * kd) + gemv_bytes(g.v, 2.0 * kd) - 4.0 * c.hidden;
-    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_pair_batch(g.qk, g.v, EPI_QKV, qkv, qkv, k, s, false, &nq); })))
+    if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_pair_batch(g.qk, g.v, EPI_QKV, qkv, qkv, k, s, pdl, &nq); })))
       return e;
   }
   for (int i = 0; i < k; i++) {
@@ -961,14 +982,18 @@ static cudaError_t enqueue_layer_batch(nt_model* m, int l, uint8_t* base, Launch
     aa.q = m->sp_q + size_t(i) * qd;
     aa.out = m->sp_att + size_t(i) * qd;
     const int32_t* pos = m->sp_i + i;
+    // no programmatic dependent launch here: an attention item copies the rows
+    // below its position before its dependency wait, and for token i > 0 rows
+    // p .. p + i - 1 come from this layer's Q/K/V launch, which the previous
+    // attention launch (it lets its dependents start at once) does not wait for
     if ((e = L.run(NT_KC_ATTN, by, [&] { return launch_attn(hd, G, grid, s, aa, pos, false); }))) return e;
   }
   double by = gemv_bytes(g.o, 8.0 * c.hidden);
-  if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_batch(g.o, EPI_ADD, o, k, 0, s, false, &no); }))) return e;
+  if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_batch(g.o, EPI_ADD, o, k, 0, s, pdl, &no); }))) return e;
   by = gemv_bytes(g.gu, 4.0 * c.ffn_dim);
-  if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_batch(g.gu, EPI_SWIGLU, gu, k, 0, s, false, &ng); }))) return e;
+  if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_batch(g.gu, EPI_SWIGLU, gu, k, 0, s, pdl, &ng); }))) return e;
   by = gemv_bytes(g.down, 8.0 * c.hidden);
-  if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_batch(g.down, EPI_ADD, dn, k, 0, s, false, &nd); }))) return e;
+  if ((e = L.run(NT_KC_GEMV, by, [&] { return launch_gemv_batch(g.down, EPI_ADD, dn, k, 0, s, pdl, &nd); }))) return e;
   // weight bytes the layer's launches read
   const Layer& ly = m->layers[size_t(l)];
   double wb = 0;
@@ -1002,7 +1027,7 @@ static cudaError_t enqueue_verify(nt_model* m, Launcher& L, int n_draft, int k, 
     const int b = int(j & 1);
     uint8_t* base = streamed ? m->staging[b] : m->layers[size_t(l)].dev;
     if (streamed && (e = cudaStreamWaitEvent(s, m->ev_copy_done[b], 0))) return e;
-    if ((e = enqueue_layer_batch(m, l, base, L, k))) return e;
+    if ((e = enqueue_layer_batch(m, l, base, L, k, sl.empty()))) return e;
     if (streamed) {
       if ((e = cudaEventRecord(m->ev_compute_done[b], s))) return e;
       if (j + 2 < sl.size() && (e = issue_copy(j + 2))) return e;
@@ -1012,10 +1037,43 @@ static cudaError_t enqueue_verify(nt_model* m, Launcher& L, int n_draft, int k, 
   for (int i = 0; i < k && !e; i++) {
     m->cur_x = m->sp_x + size_t(i) * h;
     m->cur_pos = m->sp_i + i;
-    e = enqueue_head(m, L, false, m->sp_i + 8 + i);
+    e = enqueue_head(m, L, sl.empty(), m->sp_i + 8 + i);
   }
   m->cur_x = nullptr;
   m->cur_pos = nullptr;
+  return e;
+}
+
+// One speculative cycle's device work from position sp_i[0]: k draft steps over
+// the layers below n_draft (and the head; each token's residual after them is
+// kept for the verification), the draft's tokens, then the verification.  h2d
+// receives the bytes copied from the host tier.
+static cudaError_t enqueue_cycle(nt_model* m, int n_draft, int k, double* h2d) {
+  const nt_config& c = m->c;
+  const size_t h = size_t(c.hidden);
+  *h2d = 0;
+  const std::vector<uint8_t> user = m->skip;
+  std::vector<uint8_t> dmask(size_t(c.n_layers), 0);
+  for (int l = 0; l < c.n_layers; l++) dmask[size_t(l)] = (l >= n_draft || (!user.empty() && user[size_t(l)])) ? 1 : 0;
+  m->skip = dmask;
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < k && !e; i++) {
+    Launcher L;
+    L.s = m->stream;
+    e = enqueue_streamed(m, L, nullptr, m->sp_x + size_t(i) * h);
+    for (int l = 0; l < c.n_layers; l++)
+      if (m->ran[size_t(l)] && l >= m->n_resident) *h2d += double(m->layers[size_t(l)].bytes);
+  }
+  m->skip = user;
+  if (e) return e;
+  k_draft_tokens<<<1, 32, 0, m->stream>>>(m->hist, m->sp_i, k);
+  if ((e = cudaGetLastError())) return e;
+  Launcher L;
+  L.s = m->stream;
+  double vb = 0;
+  m->stats.verify_weight_bytes = 0;
+  e = enqueue_verify(m, L, n_draft, k, &vb);
+  *h2d += vb;
   return e;
 }
 
@@ -1046,41 +1104,42 @@ nt_status nt_speculative_step(nt_model* m, int32_t token, int32_t n_draft, int32
   NT_CUDA(cudaMemcpyAsync(m->sp_i, hs, 8 * 4, cudaMemcpyHostToDevice, m->stream));
   NT_CUDA(cudaEventRecord(m->ev_step0, m->stream));
 
-  // draft: k greedy steps over the layers below n_draft (and the head); each
-  // token's residual after them is kept for the verification pass
-  const std::vector<uint8_t> user = m->skip;
-  std::vector<uint8_t> dmask(size_t(c.n_layers), 0);
-  for (int l = 0; l < c.n_layers; l++) dmask[size_t(l)] = (l >= n_draft || (!user.empty() && user[size_t(l)])) ? 1 : 0;
-  m->skip = dmask;
-  cudaError_t e = cudaSuccess;
-  double h2d = 0;
-  for (int i = 0; i < k && !e; i++) {
-    Launcher L;
-    L.s = m->stream;
-    e = enqueue_streamed(m, L, nullptr, m->sp_x + size_t(i) * h);
-    for (int l = 0; l < c.n_layers; l++)
-      if (m->ran[size_t(l)] && l >= m->n_resident) h2d += double(m->layers[size_t(l)].bytes);
-  }
-  m->skip = user;
-  // on failure the draft may have moved the device position: put it back
+  // on failure the cycle may have moved the device position: put it back
   auto resync = [&](nt_status st) {
     m->h_io[0] = m->pos;
     cudaMemcpyAsync(d_pos(m), m->h_io, 4, cudaMemcpyHostToDevice, m->stream);
     cudaStreamSynchronize(m->stream);
     return st;
   };
-  if (e) return resync(cuda_fail(e, "nt_speculative_step: draft"));
-  // the draft's tokens d_1..d_k sit in the history at positions p..p+k-1
-  e = cudaMemcpyAsync(m->sp_i + 16, m->hist + p, size_t(k) * 4, cudaMemcpyDeviceToDevice, m->stream);
-  if (e) return resync(cuda_fail(e, "nt_speculative_step: draft tokens"));
-  {
-    Launcher L;
-    L.s = m->stream;
-    double vb = 0;
-    m->stats.verify_weight_bytes = 0;
-    e = enqueue_verify(m, L, n_draft, k, &vb);
-    if (e) return resync(cuda_fail(e, "nt_speculative_step: verification"));
-    h2d += vb;
+  double h2d = 0;
+  cudaError_t e = cudaSuccess;
+  if (m->n_resident >= c.n_layers) {
+    // resident: the cycle's launches as one cached graph (they read positions and
+    // tokens from device memory, so it replays at any position)
+    if (!m->sp_exec || m->sp_n_draft != n_draft || m->sp_k != k || m->sp_skip != m->skip) {
+      if (m->sp_exec) cudaGraphExecDestroy(m->sp_exec);
+      m->sp_exec = nullptr;
+      e = cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal);
+      if (e) return resync(cuda_fail(e, "nt_speculative_step: cycle capture"));
+      double h2d_c = 0;
+      cudaError_t ec = enqueue_cycle(m, n_draft, k, &h2d_c);
+      cudaGraph_t g = nullptr;
+      const cudaError_t e2 = cudaStreamEndCapture(m->stream, &g);   // always leaves the capture
+      if (!ec && !e2) ec = cudaGraphInstantiate(&m->sp_exec, g, 0);
+      if (g) cudaGraphDestroy(g);
+      if (ec || e2) {
+        m->sp_exec = nullptr;
+        return resync(cuda_fail(ec ? ec : e2, "nt_speculative_step: cycle capture"));
+      }
+      m->sp_n_draft = n_draft;
+      m->sp_k = k;
+      m->sp_skip = m->skip;
+      m->sp_vwb = m->stats.verify_weight_bytes;
+    }
+    m->stats.verify_weight_bytes = m->sp_vwb;
+    if ((e = cudaGraphLaunch(m->sp_exec, m->stream))) return resync(cuda_fail(e, "nt_speculative_step: cycle"));
+  } else if ((e = enqueue_cycle(m, n_draft, k, &h2d))) {
+    return resync(cuda_fail(e, "nt_speculative_step: cycle"));
   }
   NT_CUDA(cudaEventRecord(m->ev_step1, m->stream));
   NT_CUDA(cudaMemcpyAsync(hs + 8, m->sp_i + 8, 16 * 4, cudaMemcpyDeviceToHost, m->stream));
