@@ -244,7 +244,10 @@ nt_status nt_plan_layer_skip(const double* cos, int32_t n_layers, double thresho
  * below n_draft are not recomputed, their K/V rows from the draft are the full
  * model's).  The verification runs each layer's GEMVs for several tokens per
  * launch (as nt_gemv_q_batch), so a resident layer's weights are read fewer than
- * k times; nt_stats.verify_weight_bytes reports the bytes read.  out_tokens (host, >= k entries) receives them, *n_out their count
+ * k times; nt_stats.verify_weight_bytes reports the bytes read.  For a model
+ * with every layer resident the cycle's device work is captured once as a CUDA
+ * graph per (n_draft, k, skip mask) and replayed (nt_stream_layers and
+ * nt_set_layer_skip discard it).  out_tokens (host, >= k entries) receives them, *n_out their count
  * (j + 1, or k when all are accepted), *n_accepted (nullable) j; the position
  * advances by *n_out.  Layers the skip mask names are skipped in both passes.
  * NT_E_INVAL: bad token, k or n_draft, or p + k > max_ctx. */
