@@ -148,3 +148,36 @@ def test_speculative_argument_checks(nt):
         assert 1 <= len(e) <= 2
     finally:
         nt.nt_model_destroy(m)
+
+
+def test_cycles_follow_draft_depth_k_and_skip_changes_on_one_model(nt):
+    """One resident model through cycles of changing (n_draft, k) and a layer-skip
+    change in between: each cycle's work must follow its own settings (the
+    captured cycle is rebuilt or discarded), so the emitted stream equals a
+    second model's plain greedy steps from the same state, bit for bit."""
+    cfg = nt.make_config(**WIDE, seed=54)
+    prefill = (20, 2)
+    a, b = nt.nt_model_create(cfg), nt.nt_model_create(cfg)
+    try:
+        for m in (a, b):
+            nt.nt_kv_prefill(m, *prefill)
+        t_a = t_b = 9
+        stream_a, stream_b = [], []
+        schedule = [(1, 4), (1, 4), (2, 3), (1, 4), (0, 2), (2, 3)]
+        for i, (n_draft, k) in enumerate(schedule):
+            if i == 3:   # skip layer 1 from here on, in both models
+                mask = np.zeros(WIDE["n_layers"], dtype=np.uint8)
+                mask[1] = 1
+                for m in (a, b):
+                    nt.nt_set_layer_skip(m, mask)
+            e, _ = nt.nt_speculative_step(a, t_a, n_draft, k)
+            stream_a += list(e)
+            t_a = e[-1]
+            for _ in range(len(e)):
+                t_b = nt.nt_decode_step(b, t_b)
+                stream_b.append(t_b)
+            assert stream_a == stream_b, (i, stream_a, stream_b)
+        assert nt.nt_get_stats(a).pos == nt.nt_get_stats(b).pos
+    finally:
+        nt.nt_model_destroy(a)
+        nt.nt_model_destroy(b)
