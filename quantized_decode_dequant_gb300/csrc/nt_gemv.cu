@@ -86,6 +86,9 @@ cudaError_t launch_gemv_batch(const GemvArgs& a_in, int epi, const BatchTok* tok
   if (pipe && epi != EPI_LOGITS)
     while (kb < kBatchMax && size_t(kb + 1) * xb + stage3 <= size_t(kPipeMaxSmem)) kb++;
   if (launches) *launches = kb < 2 ? k : (k + kb - 1) / kb;
+  // (Two-format pairs, R_single != 0, never take the per-token path: their x is
+  // at most 56 KB, and two staged x with a depth-3 ring of four Q4_K or two Q6_K
+  // rows per warp fit.)
   if (kb < 2) {   // one token per launch: the single-token kernel itself
     for (int i = 0; i < k; i++) {
       a.x = toks[i].x;
