@@ -323,6 +323,38 @@ nt_status nt_gemv_q(const nt_qtensor* t, const float* dev_x, float* dev_y, void*
 nt_status nt_gemv_q_batch(const nt_qtensor* t, const float* const* dev_x, float* const* dev_y, int32_t k,
                           int32_t* launches, void* stream);
 
+/* ------------------------------------------------------------ attention -- */
+
+/* GQA decode attention over an f16 cache, the step the decode step runs once
+ * per layer (hada "Überblick": Llama with GQA and a KV cache; "Architektur und
+ * Codestruktur": the softmax kernel).  For every query head j, with kv head
+ * g = j / (n_heads / n_kv_heads):
+ *   s_t = (q_j . K[g][t]) / sqrt(head_dim)  for t in [0, n_ctx),
+ *   out_j = sum_t softmax(s)_t V[g][t]      (softmax with the maximum subtracted).
+ * dev_q: fp32 [n_heads][head_dim], already rotated.  dev_k, dev_v: f16
+ * [n_kv_heads][max_ctx][head_dim] (one layer of a model's cache); only
+ * positions [0, n_ctx) are read.  dev_out: fp32 [n_heads][head_dim].
+ * It runs the kernel the decode step launches, split into the same items as a
+ * model with this max_ctx: chunks of C = min(320, max(32, 16 ceil(max_ctx/256)))
+ * positions, ceil(max_ctx / C) items per kv head, of which the first
+ * ceil(n_ctx / per) take per = max(32, ceil(n_ctx / items)) positions each
+ * (the last the rest); the item partials are merged in a fixed order, so
+ * results do not depend on timing.
+ * dev_workspace: nt_attention_workspace_bytes() bytes of device memory or more,
+ * owned by the caller; its contents on entry do not matter.  Calls that share a
+ * workspace must not overlap on the GPU.  All device pointers 16-byte aligned;
+ * dev_out and the workspace overlap no other buffer.
+ * Asynchronous on stream: a one-CTA setup kernel, then the attention kernel.
+ * NT_E_INVAL: n_ctx outside [1, max_ctx], non-positive sizes, n_heads not a
+ * multiple of n_kv_heads, NULL, misaligned or overlapping pointers, a workspace
+ * too small.  NT_E_UNSUPPORTED: head_dim other than 64 or 128, or n_heads /
+ * n_kv_heads other than 1, 2, 4, 8 or 16. */
+nt_status nt_attention_workspace_bytes(int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t max_ctx,
+                                       size_t* bytes);
+nt_status nt_attention(int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t max_ctx, int32_t n_ctx,
+                       const float* dev_q, const void* dev_k, const void* dev_v, float* dev_out, void* dev_workspace,
+                       size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------ allocation-free variant -- */
 
 /* y = W x as nt_gemv_q, then the index of the largest y (ties to the lowest

@@ -695,6 +695,42 @@ static nt_status validate(const nt_config* c) {
 
 using namespace nt;
 
+// Workspace of the isolated attention entry: kv-head tickets, the position the
+// kernel reads, then the chunk statistics and partial outputs, each 16-byte
+// aligned.
+struct AttnWorkspace {
+  int chunk = 0, n_chunks = 0;
+  size_t off_tickets = 0, off_pos = 0, off_ml = 0, off_o = 0, bytes = 0;
+};
+
+static nt_status attn_workspace(int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t max_ctx,
+                                AttnWorkspace* w) {
+  if (n_heads <= 0 || n_kv_heads <= 0 || max_ctx <= 0) return fail(NT_E_INVAL, "nt_attention: sizes must be positive");
+  if (n_heads % n_kv_heads) return fail(NT_E_INVAL, "nt_attention: n_heads must be a multiple of n_kv_heads");
+  if (head_dim != 64 && head_dim != 128) return fail(NT_E_UNSUPPORTED, "nt_attention: head_dim must be 64 or 128");
+  const int G = n_heads / n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
+    return fail(NT_E_UNSUPPORTED, "nt_attention: query heads per kv head must be 1, 2, 4, 8 or 16");
+  if (n_kv_heads > 65535) return fail(NT_E_INVAL, "nt_attention: more than 65535 kv heads");
+  w->chunk = attn_chunk_len(max_ctx);
+  w->n_chunks = (max_ctx + w->chunk - 1) / w->chunk;
+  if (w->n_chunks > 65535) return fail(NT_E_INVAL, "nt_attention: max_ctx needs more than 65535 items per kv head");
+  auto up = [](size_t b) { return (b + 15) & ~size_t(15); };
+  w->off_tickets = 0;
+  w->off_pos = up(size_t(n_kv_heads) * 4);
+  w->off_ml = w->off_pos + 16;
+  w->off_o = w->off_ml + up(size_t(n_heads) * size_t(w->n_chunks) * 8);
+  w->bytes = w->off_o + size_t(n_heads) * size_t(w->n_chunks) * size_t(head_dim) * 4;
+  return NT_OK;
+}
+
+// Clears the kv-head tickets and stores the position p (= n_ctx - 1) that the
+// attention kernel reads.
+__global__ void k_attn_setup(unsigned* tickets, int n_kv, int32_t* d_pos, int p) {
+  for (int i = threadIdx.x; i < n_kv; i += blockDim.x) tickets[i] = 0u;
+  if (threadIdx.x == 0) *d_pos = p;
+}
+
 extern "C" {
 
 nt_status nt_model_create(const nt_config* cfg, nt_model** out) {
@@ -1459,6 +1495,61 @@ nt_status nt_auto_residency(nt_model* m, int64_t margin_bytes, int32_t* n_reside
   if (st) return st;
   if ((st = nt_stream_layers(m, n, 2))) return st;
   if (n_resident_out) *n_resident_out = n;
+  return NT_OK;
+}
+
+// ---- isolated attention ----------------------------------------------------
+
+nt_status nt_attention_workspace_bytes(int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t max_ctx,
+                                       size_t* bytes) {
+  if (!bytes) return fail(NT_E_INVAL, "nt_attention_workspace_bytes: NULL argument");
+  AttnWorkspace w;
+  const nt_status st = attn_workspace(n_heads, n_kv_heads, head_dim, max_ctx, &w);
+  if (st) return st;
+  *bytes = w.bytes;
+  return NT_OK;
+}
+
+nt_status nt_attention(int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t max_ctx, int32_t n_ctx,
+                       const float* dev_q, const void* dev_k, const void* dev_v, float* dev_out, void* dev_workspace,
+                       size_t workspace_bytes, void* stream) {
+  AttnWorkspace w;
+  const nt_status st = attn_workspace(n_heads, n_kv_heads, head_dim, max_ctx, &w);
+  if (st) return st;
+  if (n_ctx < 1 || n_ctx > max_ctx) return fail(NT_E_INVAL, "nt_attention: n_ctx outside [1, max_ctx]");
+  if (!dev_q || !dev_k || !dev_v || !dev_out || !dev_workspace) return fail(NT_E_INVAL, "nt_attention: NULL pointer");
+  auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!a16(dev_q) || !a16(dev_k) || !a16(dev_v) || !a16(dev_out) || !a16(dev_workspace))
+    return fail(NT_E_INVAL, "nt_attention: pointers must be 16-byte aligned");
+  if (workspace_bytes < w.bytes) return fail(NT_E_INVAL, "nt_attention: workspace too small");
+  const int64_t qb = int64_t(n_heads) * head_dim * 4, cb = int64_t(n_kv_heads) * max_ctx * head_dim * 2;
+  auto overlap = [](const void* a, int64_t na, const void* b, int64_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + uintptr_t(nb) && y < x + uintptr_t(na);
+  };
+  if (overlap(dev_out, qb, dev_q, qb) || overlap(dev_out, qb, dev_k, cb) || overlap(dev_out, qb, dev_v, cb) ||
+      overlap(dev_out, qb, dev_workspace, int64_t(w.bytes)) || overlap(dev_workspace, int64_t(w.bytes), dev_q, qb) ||
+      overlap(dev_workspace, int64_t(w.bytes), dev_k, cb) || overlap(dev_workspace, int64_t(w.bytes), dev_v, cb))
+    return fail(NT_E_INVAL, "nt_attention: the output or the workspace overlaps another buffer");
+  uint8_t* base = static_cast<uint8_t*>(dev_workspace);
+  AttnArgs a;
+  a.q = dev_q;
+  a.kc = static_cast<const __half*>(dev_k);
+  a.vc = static_cast<const __half*>(dev_v);
+  a.max_ctx = max_ctx;
+  a.chunk = w.chunk;
+  a.scale = 1.0f / sqrtf(float(head_dim));
+  a.tickets = reinterpret_cast<unsigned*>(base + w.off_tickets);
+  a.part_ml = reinterpret_cast<float2*>(base + w.off_ml);
+  a.part_o = reinterpret_cast<float*>(base + w.off_o);
+  a.n_chunks = w.n_chunks;
+  a.out = dev_out;
+  int32_t* d_pos = reinterpret_cast<int32_t*>(base + w.off_pos);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  k_attn_setup<<<1, 128, 0, s>>>(a.tickets, n_kv_heads, d_pos, n_ctx - 1);
+  NT_CUDA(cudaGetLastError());
+  const dim3 grid(unsigned(n_kv_heads), unsigned(w.n_chunks));
+  NT_CUDA(launch_attn(head_dim, n_heads / n_kv_heads, grid, s, a, d_pos, false));
   return NT_OK;
 }
 

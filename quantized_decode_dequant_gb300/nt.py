@@ -92,6 +92,8 @@ _SIGS = {
     "nt_gemv_q": (C.c_int, [_vp, _vp, _vp, _vp]),
     "nt_gemv_q_batch": (C.c_int, [_vp, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p), _i32, C.POINTER(_i32), _vp]),
     "nt_gemv_argmax_noalloc": (C.c_int, [_vp, _vp, _vp, _vp, _vp, _vp]),
+    "nt_attention_workspace_bytes": (C.c_int, [_i32, _i32, _i32, _i32, C.POINTER(C.c_size_t)]),
+    "nt_attention": (C.c_int, [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, C.c_size_t, _vp]),
 }
 
 
@@ -333,6 +335,20 @@ def nt_gemv_q_batch(t: int, dev_xs, dev_ys, stream=None) -> int:
     n = C.c_int32()
     _check(lib().nt_gemv_q_batch(t, xs, ys, k, C.byref(n), _stream(stream)), "nt_gemv_q_batch")
     return int(n.value)
+
+
+def nt_attention_workspace_bytes(n_heads: int, n_kv_heads: int, head_dim: int, max_ctx: int) -> int:
+    n = C.c_size_t()
+    _check(lib().nt_attention_workspace_bytes(n_heads, n_kv_heads, head_dim, max_ctx, C.byref(n)),
+           "nt_attention_workspace_bytes")
+    return int(n.value)
+
+
+def nt_attention(n_heads: int, n_kv_heads: int, head_dim: int, max_ctx: int, n_ctx: int, dev_q: int, dev_k: int,
+                 dev_v: int, dev_out: int, dev_workspace: int, workspace_bytes: int, stream=None) -> None:
+    """GQA attention of fp32 q over positions [0, n_ctx) of an f16 [n_kv][max_ctx][hd] K/V cache."""
+    _check(lib().nt_attention(n_heads, n_kv_heads, head_dim, max_ctx, n_ctx, dev_q, dev_k, dev_v, dev_out,
+                              dev_workspace, workspace_bytes, _stream(stream)), "nt_attention")
 
 
 def nt_gemv_argmax_noalloc(t: int, dev_x: int, dev_y: int, dev_index: int, dev_margin: int, stream=None) -> None:

@@ -42,3 +42,21 @@ def test_validation_before_device_work(built):
         nt.nt_gemv_q(0, 0, 0)
     with pytest.raises(nt.NtError):
         nt.nt_decode_step(0, 0)
+
+
+def test_attention_workspace_and_validation(built):
+    # chunk C = min(320, max(32, 16 ceil(max_ctx / 256))) and ceil(max_ctx / C) items per kv head:
+    # tickets (n_kv x 4 B, to 16), the position (16 B), statistics (8 B), partial outputs (4 hd B) per item and head
+    for (nh, nkv, hd, mc) in [(64, 8, 128, 4224), (8, 8, 64, 12000), (8, 2, 64, 64), (32, 8, 128, 768)]:
+        c = min(320, max(32, 16 * -(-mc // 256)))
+        items = -(-mc // c)
+        want = -(-nkv * 4 // 16) * 16 + 16 + -(-nh * items * 8 // 16) * 16 + nh * items * hd * 4
+        assert nt.nt_attention_workspace_bytes(nh, nkv, hd, mc) == want
+    for args, status in [((8, 3, 64, 64), nt.NT_E_INVAL), ((8, 2, 96, 64), nt.NT_E_UNSUPPORTED),
+                         ((96, 3, 64, 64), nt.NT_E_UNSUPPORTED), ((8, 2, 64, 0), nt.NT_E_INVAL)]:
+        with pytest.raises(nt.NtError) as ei:
+            nt.nt_attention_workspace_bytes(*args)
+        assert ei.value.status == status
+    with pytest.raises(nt.NtError) as ei:   # NULL pointers: refused before any launch
+        nt.nt_attention(8, 2, 64, 64, 10, 0, 0, 0, 0, 0, 1 << 20)
+    assert ei.value.status == nt.NT_E_INVAL

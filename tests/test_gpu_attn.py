@@ -1,0 +1,187 @@
+"""GPU: GQA decode attention through nt_attention against the fp64 oracle.
+
+Covers every kernel instantiation (head_dim 64 and 128; 1, 2, 4, 8 and 16 query
+heads per kv head; the 64-, 128-, 256- and 320-position chunk layouts) at
+positions on the item boundaries: one position, one item, the first position
+past 32 per item, the whole cache, and contexts of more than 16 and more than 32
+items per kv head (the merge's second path)."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from gpu_util import torch_cuda, ensure_built
+from inputs import activation, f16_cache
+
+pytestmark = pytest.mark.gpu
+U = 2.0 ** -24
+
+
+@pytest.fixture(scope="module")
+def nt():
+    torch_cuda()
+    ensure_built()
+    from quantized_decode_dequant_gb300 import nt as _nt
+    return _nt
+
+
+def _chunk(max_ctx):
+    return min(320, max(32, 16 * ((max_ctx + 255) // 256)))
+
+
+class _Attn:
+    """Device q, K, V, output and workspace for one (heads, head_dim, max_ctx)."""
+
+    def __init__(self, nt, n_heads, n_kv, hd, max_ctx, seed):
+        torch = torch_cuda()
+        self.nt, self.torch = nt, torch
+        self.shape = (n_heads, n_kv, hd, max_ctx)
+        self.k = f16_cache(n_kv, max_ctx, hd, seed)
+        self.v = f16_cache(n_kv, max_ctx, hd, seed + 1000)
+        self.kd = torch.from_numpy(self.k.view(np.float16)).cuda()
+        self.vd = torch.from_numpy(self.v.view(np.float16)).cuda()
+        self.ws_bytes = nt.nt_attention_workspace_bytes(n_heads, n_kv, hd, max_ctx)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
+        self.out = torch.empty(n_heads * hd, dtype=torch.float32, device="cuda")
+
+    def run(self, q, n_ctx, ws_fill=None):
+        torch = self.torch
+        n_heads, n_kv, hd, max_ctx = self.shape
+        qd = torch.from_numpy(np.ascontiguousarray(q, np.float32)).cuda()
+        if ws_fill is not None:
+            self.ws.fill_(ws_fill)
+        self.out.fill_(float("nan"))
+        self.nt.nt_attention(n_heads, n_kv, hd, max_ctx, n_ctx, qd.data_ptr(), self.kd.data_ptr(),
+                             self.vd.data_ptr(), self.out.data_ptr(), self.ws.data_ptr(), self.ws_bytes,
+                             torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        return self.out.cpu().numpy().reshape(n_heads, hd)
+
+    def oracle(self, q, n_ctx):
+        n_heads, n_kv, hd, _ = self.shape
+        G = n_heads // n_kv
+        q = np.asarray(q, np.float32).astype(np.float64).reshape(n_heads, hd)
+        return np.stack([oracle.attend(q[j], self.k[j // G, :n_ctx], self.v[j // G, :n_ctx])
+                         for j in range(n_heads)])
+
+    def bound(self, q, n_ctx):
+        """First-order error bound per head, from the arithmetic of the kernel.
+        q and the softmax weights P enter the f16 tensor cores as hi = f16(v)
+        plus lo = f16(v - hi): relative residual 2^-22, and 2^-25 absolute where
+        lo falls below f16's normal range.  A score is a sum of hd / 16 tensor-core
+        steps of 16 exact products each, accumulated in fp32 (at most 2u per step,
+        u = 2^-24), then scaled and has the maximum subtracted (3u |s|):
+          |ds_t| <= ((hd / 16 + 3) 2u + 2^-22) sum_d |q_d K_td| / sqrt(hd) + 3u |s_t|.
+        A first-order change ds of the scores moves out = sum_t p_t V_t by
+        sum_t p_t ds_t (V_t - out), at most 2 max|V| max|ds|.  The weighted sum
+        of V (per / 16 steps of a chunk), the merge of the used chunks and the
+        division add at most ((per / 16 + used + 8) 2u + 2^-22) max|V|, the lo
+        parts lost below f16's range per 2^-25 max|V| each, and the fp32
+        exponential a few ulp of each weight (4u max|V|)."""
+        n_heads, n_kv, hd, max_ctx = self.shape
+        G = n_heads // n_kv
+        C = _chunk(max_ctx)
+        items = -(-max_ctx // C)
+        per = max(32, -(-n_ctx // items))
+        used = -(-n_ctx // per)
+        q = np.asarray(q, np.float32).astype(np.float64).reshape(n_heads, hd)
+        out = np.empty(n_heads)
+        for j in range(n_heads):
+            kf = self.k[j // G, :n_ctx].view(np.float16).astype(np.float64)
+            vm = np.abs(self.v[j // G, :n_ctx].view(np.float16).astype(np.float64)).max()
+            dot_abs = np.abs(kf) @ np.abs(q[j]) / math.sqrt(hd)          # per key
+            s_abs = np.abs(kf @ q[j]) / math.sqrt(hd)
+            ds = (((hd // 16 + 3) * 2 * U + 2.0 ** -22) * dot_abs + 3 * U * s_abs).max()
+            ds += 2.0 ** -25 * np.abs(kf).max() * hd / math.sqrt(hd)
+            out[j] = 2 * vm * ds + ((per // 16 + used + 8) * 2 * U + 2.0 ** -22 + 4 * U + 2.0 ** -25 * per) * vm
+        return out
+
+
+# (n_heads, n_kv, head_dim, max_ctx, positions attended): chunk C, items per kv head
+CASES = [
+    (64, 8, 128, 4224, [1, 32, 33, 512, 4097, 4224]),   # 70B geometry: C 272 (320 layout), 16 items
+    (32, 8, 128, 768, [1, 31, 48, 49, 513, 768]),       # 8B geometry: C 48 (64 layout), 16 items
+    (16, 1, 128, 3000, [2, 512, 2999, 3000]),           # G 16: C 192 (256 layout), 16 items
+    (8, 4, 64, 1500, [1, 96, 97, 1500]),                # G 2: C 96 (128 layout), 16 items
+    (16, 8, 128, 7000, [5120, 5121, 7000]),             # G 2: C 320, 22 items
+    (8, 8, 64, 12000, [1, 33, 1216, 1217, 10241, 12000]),   # G 1: C 320, 38 items (merge of more than 32)
+    (8, 2, 64, 64, [1, 17, 63, 64]),                    # tiny geometry: C 32, 2 items
+]
+
+
+@pytest.mark.parametrize("n_heads,n_kv,hd,max_ctx,ns", CASES)
+@pytest.mark.parametrize("q_std", [0.5, 4.0, 16.0])
+def test_attention_matches_oracle_on_item_boundaries(nt, n_heads, n_kv, hd, max_ctx, ns, q_std):
+    A = _Attn(nt, n_heads, n_kv, hd, max_ctx, seed=7 + max_ctx)
+    for i, n in enumerate(ns):
+        q = activation(n_heads * hd, seed=100 + i, std=q_std)
+        got = A.run(q, n)
+        want = A.oracle(q, n)
+        assert np.isfinite(got).all(), (n, q_std)
+        err = np.abs(got.astype(np.float64) - want).max(axis=1)
+        bound = A.bound(q, n)
+        assert (err <= bound).all(), (n, q_std, float((err / bound).max()), float(err.max()))
+        if q_std == 0.5 and n > 1:
+            # the bound is tight enough to see an off-by-one in the attended range: leaving out
+            # the current position moves the exact result of some head by more than it
+            assert (np.abs(A.oracle(q, n - 1) - want).max(axis=1) > bound).any(), n
+        print(f"heads {n_heads}/{n_kv} hd {hd} max_ctx {max_ctx} n {n} q_std {q_std}: "
+              f"max-abs {err.max():.2e} (bound {bound.min():.1e}..{bound.max():.1e})")
+
+
+def test_attention_is_deterministic_and_ignores_workspace_contents(nt):
+    A = _Attn(nt, 64, 8, 128, 4224, seed=11)
+    q = activation(64 * 128, seed=12, std=2.0)
+    first = A.run(q, 4100, ws_fill=0)
+    for fill in (0xFF, 0x7F, 0):
+        np.testing.assert_array_equal(A.run(q, 4100, ws_fill=fill).view(np.uint32), first.view(np.uint32))
+
+
+def test_attention_closed_forms(nt):
+    """Independent of the oracle: one position gives V_0 exactly; keys all equal
+    give the mean of V over the attended positions."""
+    torch = torch_cuda()
+    n_heads, n_kv, hd, max_ctx = 16, 2, 128, 1000
+    A = _Attn(nt, n_heads, n_kv, hd, max_ctx, seed=21)
+    q = activation(n_heads * hd, seed=22, std=3.0)
+    got = A.run(q, 1)
+    G = n_heads // n_kv
+    want = np.stack([A.v[j // G, 0].view(np.float16).astype(np.float32) for j in range(n_heads)])
+    np.testing.assert_array_equal(got, want)
+    # equal keys: every position of each kv head takes that head's row 0
+    A.k[:] = A.k[:, :1, :]
+    A.kd.copy_(torch.from_numpy(A.k.view(np.float16)))
+    vmax = float(np.abs(A.v.view(np.float16).astype(np.float64)).max())
+    for n in (5, 333, 1000):
+        got = A.run(q, n)
+        mean = np.stack([A.v[j // G, :n].view(np.float16).astype(np.float64).mean(0) for j in range(n_heads)])
+        # every weight is exactly 1: only the fp32 sums of V (16 keys per tensor-core step, the
+        # steps of a chunk, then the chunks) and the final division round
+        np.testing.assert_allclose(got, mean, rtol=0, atol=(n // 16 + 40) * U * vmax)
+
+
+def test_attention_argument_checks(nt):
+    torch = torch_cuda()
+    ws_n = nt.nt_attention_workspace_bytes(8, 2, 64, 64)
+    ws = torch.empty(ws_n + 16, dtype=torch.uint8, device="cuda")
+    q = torch.zeros(8 * 64, device="cuda")
+    out = torch.zeros(8 * 64, device="cuda")
+    kv = torch.zeros(2 * 64 * 64, dtype=torch.float16, device="cuda")
+    s = torch.cuda.current_stream()
+
+    def call(n_ctx=10, qp=None, op=None, wp=None, wb=ws_n, heads=(8, 2, 64, 64)):
+        nt.nt_attention(*heads, n_ctx, q.data_ptr() if qp is None else qp, kv.data_ptr(), kv.data_ptr(),
+                        out.data_ptr() if op is None else op, ws.data_ptr() if wp is None else wp, wb, s)
+
+    call()
+    torch.cuda.synchronize()
+    for kw, status in [(dict(n_ctx=0), nt.NT_E_INVAL), (dict(n_ctx=65), nt.NT_E_INVAL),
+                       (dict(wb=ws_n - 1), nt.NT_E_INVAL), (dict(qp=0), nt.NT_E_INVAL),
+                       (dict(wp=ws.data_ptr() + 8), nt.NT_E_INVAL), (dict(op=q.data_ptr()), nt.NT_E_INVAL),
+                       (dict(op=ws.data_ptr()), nt.NT_E_INVAL), (dict(heads=(8, 3, 64, 64)), nt.NT_E_INVAL),
+                       (dict(heads=(8, 2, 96, 64)), nt.NT_E_UNSUPPORTED),
+                       (dict(heads=(96, 3, 64, 64)), nt.NT_E_UNSUPPORTED)]:
+        with pytest.raises(nt.NtError) as ei:
+            call(**kw)
+        assert ei.value.status == status, kw
