@@ -335,11 +335,14 @@ nt_status nt_gemv_q_batch(const nt_qtensor* t, const float* const* dev_x, float*
  * [n_kv_heads][max_ctx][head_dim] (one layer of a model's cache); only
  * positions [0, n_ctx) are read.  dev_out: fp32 [n_heads][head_dim].
  * It runs the kernel the decode step launches, split into the same items as a
- * model with this max_ctx: chunks of C = min(320, max(32, 16 ceil(max_ctx/256)))
- * positions, ceil(max_ctx / C) items per kv head, of which the first
- * ceil(n_ctx / per) take per = max(32, ceil(n_ctx / items)) positions each
- * (the last the rest); the item partials are merged in a fixed order, so
- * results do not depend on timing.
+ * model with this max_ctx: chunks of C positions, C = max(32, 16 ceil(max_ctx/128))
+ * up to max_ctx 2560 and min(320, 16 ceil(max_ctx/256)) beyond, ceil(max_ctx / C)
+ * items per kv head, of which the first ceil(n_ctx / per) take
+ * per = max(32, ceil(n_ctx / items)) positions each (the last the rest).  The
+ * item partials are merged in a fixed order, so results do not depend on
+ * timing; where the GPU can hold one thread-block cluster of a kv head's items
+ * for every kv head at once the merge reads them across the cluster, otherwise
+ * through the workspace, with the same arithmetic and bit-identical results.
  * dev_workspace: nt_attention_workspace_bytes() bytes of device memory or more,
  * owned by the caller; its contents on entry do not matter.  Calls that share a
  * workspace must not overlap on the GPU.  All device pointers 16-byte aligned;

@@ -4,9 +4,13 @@
 // Split context: item (kv head g, chunk c) attends the G = n_heads/n_kv_heads
 // query heads that share g over the chunk's C cached positions.  It keeps the
 // chunk's softmax statistics (max m_c, sum of exponentials l_c) and the
-// unnormalised exp-weighted sum o_c of its values.  The CTA that finishes the
-// last chunk of kv head g (an atomic ticket per kv head) merges the chunks of
-// g's heads: M = max m_c, o = sum o_c e^(m_c - M) / sum l_c e^(m_c - M).
+// unnormalised exp-weighted sum o_c of its values.  The chunks of g's heads
+// are merged, M = max m_c, o = sum o_c e^(m_c - M) / sum l_c e^(m_c - M), in
+// one of two ways with the same arithmetic: where the items of every kv head
+// fit one thread-block cluster that the GPU can hold for all kv heads at once,
+// warps of the cluster merge from the items' shared memory (k_attn_cl);
+// otherwise the CTA that finishes the last chunk of kv head g (an atomic
+// ticket per kv head) merges from partials in global memory.
 //
 // The two contractions of an item are small dense products, run on the tensor
 // cores with mma.sync m16n8k16 (f16 operands, fp32 accumulation):
@@ -20,6 +24,8 @@
 // with G = 16 two tiles hold hi and lo of all heads.
 #pragma once
 
+#include <cooperative_groups.h>
+
 #include "nt_internal.cuh"
 
 namespace nt {
@@ -27,18 +33,27 @@ namespace nt {
 constexpr int kAttnWarps = 8;
 constexpr int kAttnThreads = 32 * kAttnWarps;
 
-// Chunk length: the context is cut into at most 16 items per kv head up to 5120
-// positions (the merge reads every chunk's partials in one round of loads), at
-// least 32 positions each, a multiple of 16: C = max(32, 16 ceil(max_ctx / 256)),
-// at most 320.  The items a step uses split its positions evenly (see k_attn).
-// Fixed per model.  (Measured on GB300, 70B step at ctx 4096, 8 kv heads: 19
-// items per kv head, one per SM, 0.6% slower: the O projection's CTAs then find
-// no free SM for their early weight copies; 14 items the same as 16, 12 items
-// 1% slower.  Scoring the chunk's rows block by block as their copies land, with
-// an acquire-release ticket, did not change the step either.)
+// Chunk length C, a multiple of 16 and at least 32, fixed per model: the
+// context is cut into at most 8 items per kv head up to 2560 positions,
+// C = max(32, 16 ceil(max_ctx / 128)), so that a kv head's items fit one
+// thread-block cluster of 8 (k_attn_cl); beyond that into at most 16 items up
+// to 5120 positions, C = 16 ceil(max_ctx / 256), at most 320 (the merge reads
+// every chunk's partials in one round of loads); longer contexts take more
+// items of 320.  The items a step uses split its positions evenly (see k_attn).
+// (Measured on GB300: 70B step at ctx 4096, 8 kv heads: 19 items per kv head,
+// one per SM, 0.6% slower, the O projection's CTAs then finding no free SM for
+// their early weight copies; 14 items the same as 16, 12 items 1% slower.
+// Scoring the chunk's rows block by block as their copies land, with an
+// acquire-release ticket, did not change the step either.  8B step at ctx 512:
+// 8 items with the ticket merge the same as 16, with the cluster merge 0.6%
+// faster.)
 inline int attn_chunk_len(int max_ctx) {
+  if (max_ctx <= 8 * 320) {
+    const int c8 = 16 * ((max_ctx + 127) / 128);
+    return c8 < 32 ? 32 : c8;
+  }
   const int c = 16 * ((max_ctx + 255) / 256);
-  return c < 32 ? 32 : (c > 320 ? 320 : c);   // 320: the largest instantiated chunk (longer contexts: more items)
+  return c > 320 ? 320 : c;   // 320: the largest instantiated chunk (longer contexts: more items)
 }
 // Largest chunk a kernel instantiation holds (its shared-memory layout).
 inline int attn_chunk_max(int chunk) { return chunk <= 64 ? 64 : (chunk <= 128 ? 128 : (chunk <= 256 ? 256 : 320)); }
@@ -205,6 +220,65 @@ __device__ __forceinline__ void attn_combine_head(const AttnArgs& a, int j, int 
   }
 }
 
+// An item's partials when the items of a kv head run as one thread-block
+// cluster: o_c of the G heads ([G][HD] floats), then (m_c, l_c) per head, in the
+// item's own K rows, which no thread reads once the scores are formed.
+template <int HD, int G, int CM>
+__device__ __forceinline__ float* attn_cluster_o(uint8_t* sm) {
+  static_assert(size_t(G) * HD * 4 + size_t(G) * 8 <= size_t(CM) * (HD + 8) * 2, "partials fit in the K rows");
+  return reinterpret_cast<float*>(sm + AttnLayout<HD, G, CM>::kK);
+}
+template <int HD, int G, int CM>
+__device__ __forceinline__ float2* attn_cluster_ml(uint8_t* sm) {
+  return reinterpret_cast<float2*>(sm + AttnLayout<HD, G, CM>::kK + size_t(G) * HD * 4);
+}
+
+// Merge of query head g G + h from the partials of the `used` live items of
+// kv head g, item c in the shared memory of cluster rank c, by one warp: the
+// arithmetic and order of attn_combine_head (used <= 32), with the partials
+// read from distributed shared memory instead of global memory.  Call after a
+// cluster barrier that follows every item's partial stores.
+template <int HD, int G, int CM>
+__device__ __forceinline__ void attn_merge_cluster(const AttnArgs& a, int g, int h, int used, int lane,
+                                                   uint8_t* sm) {
+  namespace cg = cooperative_groups;
+  constexpr int V = HD / 32;
+  cg::cluster_group cl = cg::this_cluster();
+  float2 mv = make_float2(-INFINITY, 0.f);
+  if (lane < used) mv = cl.map_shared_rank(attn_cluster_ml<HD, G, CM>(sm), unsigned(lane))[h];
+  float M = mv.x;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float w = lane < used ? expf(mv.x - M) : 0.f;
+  float L = __fmul_rn(mv.y, w);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) L = __fadd_rn(L, __shfl_xor_sync(0xffffffffu, L, o));
+  float acc[V];
+#pragma unroll
+  for (int v = 0; v < V; v++) acc[v] = 0.f;
+  const float* own = attn_cluster_o<HD, G, CM>(sm) + h * HD + lane * V;
+  for (int c = 0; c < used; c++) {
+    const float wi = __shfl_sync(0xffffffffu, w, c);
+    const float* po = cl.map_shared_rank(own, unsigned(c));
+    float t[V];
+    if (V == 4) {
+      const float4 u = *reinterpret_cast<const float4*>(po);
+      t[0] = u.x; t[1 % V] = u.y; t[2 % V] = u.z; t[3 % V] = u.w;
+    } else {
+      const float2 u = *reinterpret_cast<const float2*>(po);
+      t[0] = u.x; t[1 % V] = u.y;
+    }
+#pragma unroll
+    for (int v = 0; v < V; v++) acc[v] = __fmaf_rn(t[v], wi, acc[v]);
+  }
+  float* out = a.out + int64_t(g * G + h) * HD + lane * V;
+  if (V == 4) {
+    *reinterpret_cast<float4*>(out) = make_float4(acc[0] / L, acc[1 % V] / L, acc[2 % V] / L, acc[3 % V] / L);
+  } else {
+    *reinterpret_cast<float2*>(out) = make_float2(acc[0] / L, acc[1 % V] / L);
+  }
+}
+
 // One item by the whole CTA: kv head g, chunk `chunk` of C positions; n =
 // positions attended (pos + 1: the current one is stored by now), used =
 // ceil(n / C) items of kv head g exist; rows [0, r_done) of the chunk are
@@ -217,7 +291,7 @@ __device__ __forceinline__ void attn_combine_head(const AttnArgs& a, int j, int 
 // [8 HD/64 w, 8 HD/64 (w+1)) over all keys.  Sums of the hi and lo rows, of the
 // per-warp softmax sums and of the k-steps run in a fixed order, so the result
 // does not depend on timing.
-template <int HD, int G, int CM>
+template <int HD, int G, int CM, bool CL = false>
 __device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, int t0, int cnt, int used,
                                           uint8_t* sm, int r_done) {
   using Lay = AttnLayout<HD, G, CM>;
@@ -363,7 +437,8 @@ __device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, i
     for (int w = 0; w < NW; w++) M = fmaxf(M, red_max[w * G + t]);
 #pragma unroll
     for (int w = 0; w < NW; w++) L = __fadd_rn(L, red_sum[w * G + t]);
-    a.part_ml[int64_t(g * G + t) * a.n_chunks + chunk] = make_float2(M, L);
+    if constexpr (CL) attn_cluster_ml<HD, G, CM>(sm)[t] = make_float2(M, L);   // K rows are read by now
+    else a.part_ml[int64_t(g * G + t) * a.n_chunks + chunk] = make_float2(M, L);
   }
 
   // ---- P V: this warp's output dimension tiles over the live key steps ---------
@@ -404,7 +479,8 @@ __device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, i
     for (int h = 0; h < HPT; h++) {
       const int head = gi + 8 * h;
       if (head >= G) continue;
-      float* po = a.part_o + (int64_t(g * G + head) * a.n_chunks + chunk) * HD + n0 + 2 * tg;
+      float* po = (CL ? attn_cluster_o<HD, G, CM>(sm) + head * HD
+                      : a.part_o + (int64_t(g * G + head) * a.n_chunks + chunk) * HD) + n0 + 2 * tg;
 #pragma unroll
       for (int j = 0; j < NVW; j++) {
         float o0, o1;
@@ -419,6 +495,8 @@ __device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, i
       }
     }
   }
+
+  if constexpr (CL) return false;   // the cluster merges (attn_merge_cluster)
 
   // ---- the CTA that finishes kv head g's last chunk merges its heads --------
   // (the CTA barrier orders every thread's partials before thread 0's fence)

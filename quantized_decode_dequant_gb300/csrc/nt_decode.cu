@@ -20,6 +20,7 @@
 // on a copy stream while layer l-1 computes; the copy into a buffer waits for
 // the compute that last read it.
 #include <algorithm>
+#include <atomic>
 #include <chrono>
 #include <cmath>
 #include <cstdlib>
@@ -68,6 +69,43 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const __grid_constant_
   asm volatile("cp.async.commit_group;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   attn_item<HD, G, CM>(a, blockIdx.x, blockIdx.y, t0, cnt, used, sm, r_done);
+}
+
+// The same items with the items of each kv head launched as one thread-block
+// cluster (cluster rank = item): the items keep their partials in shared
+// memory, and after a cluster barrier the G heads are merged by warps spread
+// over the cluster, reading the partials across it (no global partials, fence
+// or ticket).  Every CTA takes part in both cluster barriers, items with no
+// positions included; the second keeps each CTA's partials in place until the
+// merges that read them are done.
+template <int HD, int G, int CM>
+__global__ void __launch_bounds__(kAttnThreads, 1) k_attn_cl(const __grid_constant__ AttnArgs a,
+                                                             const int32_t* __restrict__ d_pos) {
+  namespace cg = cooperative_groups;
+  extern __shared__ uint4 smem_u4[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(smem_u4);
+  cg::cluster_group cl = cg::this_cluster();
+  const int items = int(cl.num_blocks()), item = int(cl.block_rank());
+  const int n = __ldcg(d_pos) + 1;
+  const int per = max(32, (n + items - 1) / items);   // positions per item, <= C
+  const int used = (n + per - 1) / per;
+  asm volatile("griddepcontrol.launch_dependents;");
+  const bool live = item < used;
+  int t0 = 0, cnt = 0, r_done = 0;
+  if (live) {
+    t0 = item * per;
+    cnt = min(per, n - t0);
+    r_done = max(0, min(cnt, n - 1 - t0));
+    attn_copy_rows<HD, CM>(a, blockIdx.x, t0, 0, r_done, sm);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (live) attn_item<HD, G, CM, true>(a, blockIdx.x, item, t0, cnt, used, sm, r_done);
+  cl.sync();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int h = item + items * warp; h < G; h += items * kAttnWarps)
+    attn_merge_cluster<HD, G, CM>(a, blockIdx.x, h, used, lane, sm);
+  cl.sync();
 }
 
 // Greedy choice over the per-CTA top-2 summaries of the output GEMV (ties to the
@@ -305,6 +343,44 @@ struct Launcher {
 
 constexpr size_t kAttnMinSmem = 116 * 1024;   // more than half of an SM's shared memory
 
+// Whether the clusters of `items` CTAs of k_attn_cl<HD, G, CM> can all be
+// resident at once for n_kv kv heads (one cluster each), from the occupancy
+// query; cached per cluster size.  Sizes above 8 need the non-portable cluster
+// attribute.
+template <int HD, int G, int CM>
+static bool attn_clusters_fit(int items, int n_kv, size_t smem) {
+  static std::atomic<int> fit[17] = {};   // 0: not asked yet; else 1 + clusters resident at once
+  if (items < 2 || items > 16) return false;
+  int v = fit[items].load(std::memory_order_relaxed);
+  if (v == 0) {
+    auto kern = k_attn_cl<HD, G, CM>;
+    int clusters = 0;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(unsigned(n_kv), unsigned(items));
+      cfg.blockDim = dim3(kAttnThreads);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 1;
+      attr[0].val.clusterDim.y = unsigned(items);
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    }
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();   // a refused query only means: no clusters
+      clusters = 0;
+    }
+    v = 1 + clusters;
+    fit[items].store(v, std::memory_order_relaxed);
+  }
+  return v - 1 >= n_kv;
+}
+
 template <int HD, int G, int CM>
 static cudaError_t launch_attn_cm(dim3 grid, cudaStream_t s, const AttnArgs& a, const int32_t* pos, bool pdl) {
   auto kern = k_attn<HD, G, CM>;
@@ -314,17 +390,29 @@ static cudaError_t launch_attn_cm(dim3 grid, cudaStream_t s, const AttnArgs& a, 
   if (smem < kAttnMinSmem) smem = kAttnMinSmem;
   static const KernelSetup setup = kernel_setup(kern, int(smem));
   if (setup.err != cudaSuccess) return setup.err;
+  const bool cluster = attn_clusters_fit<HD, G, CM>(int(grid.y), int(grid.x), smem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (cluster) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = grid.y;
+    attr[na].val.clusterDim.z = 1;
+    na++;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    na++;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, a, pos);
+  cfg.numAttrs = unsigned(na);
+  return cluster ? cudaLaunchKernelEx(&cfg, k_attn_cl<HD, G, CM>, a, pos) : cudaLaunchKernelEx(&cfg, kern, a, pos);
 }
 
 template <int HD, int G>

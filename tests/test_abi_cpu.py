@@ -45,10 +45,11 @@ def test_validation_before_device_work(built):
 
 
 def test_attention_workspace_and_validation(built):
-    # chunk C = min(320, max(32, 16 ceil(max_ctx / 256))) and ceil(max_ctx / C) items per kv head:
+    # chunk C = max(32, 16 ceil(max_ctx / 128)) up to 2560 positions, min(320, 16 ceil(max_ctx / 256)) beyond,
+    # and ceil(max_ctx / C) items per kv head:
     # tickets (n_kv x 4 B, to 16), the position (16 B), statistics (8 B), partial outputs (4 hd B) per item and head
     for (nh, nkv, hd, mc) in [(64, 8, 128, 4224), (8, 8, 64, 12000), (8, 2, 64, 64), (32, 8, 128, 768)]:
-        c = min(320, max(32, 16 * -(-mc // 256)))
+        c = max(32, 16 * -(-mc // 128)) if mc <= 2560 else min(320, 16 * -(-mc // 256))
         items = -(-mc // c)
         want = -(-nkv * 4 // 16) * 16 + 16 + -(-nh * items * 8 // 16) * 16 + nh * items * hd * 4
         assert nt.nt_attention_workspace_bytes(nh, nkv, hd, mc) == want

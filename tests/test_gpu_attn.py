@@ -1,10 +1,11 @@
 """GPU: GQA decode attention through nt_attention against the fp64 oracle.
 
 Covers every kernel instantiation (head_dim 64 and 128; 1, 2, 4, 8 and 16 query
-heads per kv head; the 64-, 128-, 256- and 320-position chunk layouts) at
-positions on the item boundaries: one position, one item, the first position
-past 32 per item, the whole cache, and contexts of more than 16 and more than 32
-items per kv head (the merge's second path)."""
+heads per kv head; the 64-, 128-, 256- and 320-position chunk layouts), both
+merges (across a thread-block cluster of a kv head's items, and by the last item
+through global memory), at positions on the item boundaries: one position, one
+item, the first position past 32 per item, the whole cache, and contexts of more
+than 16 and more than 32 items per kv head (the merge's second path)."""
 import math
 
 import numpy as np
@@ -27,7 +28,10 @@ def nt():
 
 
 def _chunk(max_ctx):
-    return min(320, max(32, 16 * ((max_ctx + 255) // 256)))
+    """Positions per item: at most 8 items per kv head up to 2560 positions, else 16 up to 5120."""
+    if max_ctx <= 2560:
+        return max(32, 16 * ((max_ctx + 127) // 128))
+    return min(320, 16 * ((max_ctx + 255) // 256))
 
 
 class _Attn:
@@ -98,15 +102,16 @@ class _Attn:
         return out
 
 
-# (n_heads, n_kv, head_dim, max_ctx, positions attended): chunk C, items per kv head
+# (n_heads, n_kv, head_dim, max_ctx, positions attended): chunk C, items per kv head, merge.  On a
+# GB300 a cluster of 8 items fits for up to 15 kv heads at once and one of 16 for up to 7.
 CASES = [
-    (64, 8, 128, 4224, [1, 32, 33, 512, 4097, 4224]),   # 70B geometry: C 272 (320 layout), 16 items
-    (32, 8, 128, 768, [1, 31, 48, 49, 513, 768]),       # 8B geometry: C 48 (64 layout), 16 items
-    (16, 1, 128, 3000, [2, 512, 2999, 3000]),           # G 16: C 192 (256 layout), 16 items
-    (8, 4, 64, 1500, [1, 96, 97, 1500]),                # G 2: C 96 (128 layout), 16 items
-    (16, 8, 128, 7000, [5120, 5121, 7000]),             # G 2: C 320, 22 items
+    (64, 8, 128, 4224, [1, 32, 33, 512, 4097, 4224]),   # 70B geometry: C 272 (320 layout), 16 items, ticket
+    (32, 8, 128, 768, [1, 31, 96, 97, 513, 768]),       # 8B geometry: C 96 (128 layout), 8 items, cluster
+    (16, 1, 128, 3000, [2, 512, 2999, 3000]),           # G 16: C 192 (256 layout), 16 items, cluster of 16
+    (8, 4, 64, 1500, [1, 192, 193, 1500]),              # G 2: C 192 (256 layout), 8 items, cluster
+    (16, 8, 128, 7000, [5120, 5121, 7000]),             # G 2: C 320, 22 items, ticket
     (8, 8, 64, 12000, [1, 33, 1216, 1217, 10241, 12000]),   # G 1: C 320, 38 items (merge of more than 32)
-    (8, 2, 64, 64, [1, 17, 63, 64]),                    # tiny geometry: C 32, 2 items
+    (8, 2, 64, 64, [1, 17, 63, 64]),                    # tiny geometry: C 32, 2 items, cluster of 2
 ]
 
 
