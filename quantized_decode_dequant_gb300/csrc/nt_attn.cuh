@@ -503,10 +503,11 @@ __device__ __forceinline__ bool attn_item(const AttnArgs& a, int g, int chunk, i
   int* flag = reinterpret_cast<int*>(sm + Lay::kFlag);
   __syncthreads();
   if (t == 0) {
-    __threadfence();
-    const unsigned ticket = atomicAdd(a.tickets + g, 1u);
+    // release: the CTA's partials (ordered before this by the barrier); acquire:
+    // every earlier item's, for the CTA that takes the last ticket
+    unsigned ticket;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(ticket) : "l"(a.tickets + g) : "memory");
     *flag = ticket == unsigned(used - 1);
-    __threadfence();
   }
   __syncthreads();
   if (!*flag) return false;
