@@ -87,8 +87,8 @@ cudaError_t launch_gemv_batch(const GemvArgs& a_in, int epi, const BatchTok* tok
     while (kb < kBatchMax && size_t(kb + 1) * xb + stage3 <= size_t(kPipeMaxSmem)) kb++;
   if (launches) *launches = kb < 2 ? k : (k + kb - 1) / kb;
   // (Two-format pairs, R_single != 0, never take the per-token path: their x is
-  // at most 56 KB, and two staged x with a depth-3 ring of four Q4_K or two Q6_K
-  // rows per warp fit.)
+  // at most 56 KB, and two staged x with a depth-3 ring of four Q4_K rows or one
+  // Q6_K row per warp fit.)
   if (kb < 2) {   // one token per launch: the single-token kernel itself
     for (int i = 0; i < k; i++) {
       a.x = toks[i].x;
@@ -130,11 +130,11 @@ static bool pair_kernel(const GemvArgs& a1, const GemvArgs& a2, int epi) {
 
 cudaError_t launch_gemv_pair_batch(const GemvArgs& a1, const GemvArgs& a2, int epi, const BatchTok* toks1,
                                    const BatchTok* toks2, int k, cudaStream_t s, bool pdl, int* launches) {
-  // the two-format kernel's rows per warp: four for the Q4_K rows, two for the Q6_K rows
+  // the two-format kernel's rows per warp: four for the Q4_K rows, one for the Q6_K rows
   const bool pair = pair_kernel(a1, a2, epi);
   int n1 = 0, n2 = 0;
   cudaError_t e = launch_gemv_batch(a1, epi, toks1, k, pair ? 4 : 0, s, pdl, &n1);
-  if (e == cudaSuccess) e = launch_gemv_batch(a2, epi, toks2, k, pair ? 2 : 0, s, pdl, &n2);
+  if (e == cudaSuccess) e = launch_gemv_batch(a2, epi, toks2, k, pair ? 1 : 0, s, pdl, &n2);
   if (launches) *launches = n1 > n2 ? n1 : n2;
   return e;
 }

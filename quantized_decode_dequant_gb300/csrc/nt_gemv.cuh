@@ -347,6 +347,16 @@ __device__ __forceinline__ void epilogue_to(const GemvArgs& a, float* y, const i
   // pair epilogues need rows 2i and 2i+1: the odd row's sum moves onto the even holder
   const float other = __shfl_down_sync(0xffffffffu, k, LPR);
   if (!holder) return;
+  if constexpr (R == 1 && EPI == EPI_QKV) {
+    // one row per group, used only for V rows (the two-format Q/K/V launch's
+    // second range): no RoPE pair, the f16 store of the row at the current position
+    const int L = a.epi.row_base + int(row);
+    const int vr = L - a.epi.q_rows - a.epi.k_rows;
+    if (vr < 0) return;
+    const int hd = a.epi.head_dim, p = __ldcg(pos);
+    a.epi.v_cache[(int64_t(vr / hd) * a.epi.max_ctx + p) * hd + vr % hd] = __float2half_rn(k);
+    return;
+  }
   if (EPI == EPI_STORE) {
     y[row] = k;
   } else if (EPI == EPI_ADD) {

@@ -854,10 +854,13 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe(const __grid_con
 // run on as one range over the warps, a1's first; each warp works through its
 // a1 groups, then its a2 groups, with each format's own ring depth in one
 // per-warp slice.  Used for a Q4_K Q/K GEMV (four rows per warp, each x read
-// shared by four rows) with a Q6_K V GEMV (two).  (Measured on GB300: cutting
-// the V groups into column parts spread over the warps of a CTA, added in
-// shared memory, balanced the launch and made the GEMVs 2.5% faster, yet the
-// 70B decode step 0.4% slower.)
+// shared by four rows) with a Q6_K V GEMV (one row per warp: at 70B widths the
+// 2304 Q/K groups leave 128 of the 2432 warps free, and one-row V groups spread
+// the V rows' second round over 896 warps instead of two-row groups over 384,
+// so fewer warps run on alone at the end; 70B step 0.6% faster than two-row V
+// groups).  (Measured on GB300: cutting the V groups into column parts spread
+// over the warps of a CTA, added in shared memory, balanced the launch and made
+// the GEMVs 2.5% faster, yet the 70B decode step 0.4% slower.)
 template <int F1, int F2, int R1, int R2, int S1, int S2, int EPI, int NW>
 __global__ void __launch_bounds__(NW * 32, 16 / NW) k_gemv_pipe2(const __grid_constant__ GemvArgs a1,
                                                        const __grid_constant__ GemvArgs a2, const int64_t n1,
@@ -1122,6 +1125,13 @@ cudaError_t launch_gemv_batch_fmt(const GemvArgs& a, int epi, int R, int S, cons
     if constexpr (kFourRows<FMT>) {
       if (S >= 4) { NT_BATCH_EPI(4, 4) } else { NT_BATCH_EPI(4, 3) }
     }
+  } else if (R == 1) {   // the V rows of a two-format Q/K/V launch
+    if constexpr (FMT == NT_Q6_K) {
+      if (epi == EPI_QKV) {
+        if (S >= 4) return launch_gemv_batch_t<FMT, 1, 4, EPI_QKV>(a, b, s, pdl);
+        return launch_gemv_batch_t<FMT, 1, 3, EPI_QKV>(a, b, s, pdl);
+      }
+    }
   } else {
     if (S >= 4) { NT_BATCH_EPI(2, 4) } else { NT_BATCH_EPI(2, 3) }
   }
@@ -1154,7 +1164,7 @@ cudaError_t launch_gemv_pipe_fmt(const GemvArgs& a, int epi, int R, int S, cudaS
 // per CTA, one CTA per SM, the ring depths that fit beside x.
 template <int EPI>
 cudaError_t launch_gemv_pipe2_q4k_q6k(const GemvArgs& a1, const GemvArgs& a2, cudaStream_t s, bool pdl) {
-  constexpr int NW = kPipeWarps, R1 = 4, R2 = 2, S1 = 4, S2 = 6;
+  constexpr int NW = kPipeWarps, R1 = 4, R2 = 1, S1 = 4, S2 = 8;
   auto kern = k_gemv_pipe2<NT_Q4_K, NT_Q6_K, R1, R2, S1, S2, EPI, NW>;
   constexpr size_t slice = pipe_slice<NT_Q4_K, R1, S1, 0>() > pipe_slice<NT_Q6_K, R2, S2, 0>()
                                ? pipe_slice<NT_Q4_K, R1, S1, 0>()

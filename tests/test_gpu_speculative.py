@@ -181,3 +181,45 @@ def test_cycles_follow_draft_depth_k_and_skip_changes_on_one_model(nt):
     finally:
         nt.nt_model_destroy(a)
         nt.nt_model_destroy(b)
+
+
+# the Q4_K_M-style mix at whole-tile widths: Q/K in Q4_K and V in Q6_K go through the
+# two-format Q/K/V launch, and in the verification through its two multi-token launches
+Q4_K_M_WIDE = dict(WIDE, t_embd="q4_k", t_q="q4_k", t_k="q4_k", t_v="q6_k", t_o="q4_k", t_gate="q4_k",
+                   t_up="q4_k", t_down="q6_k", t_out="q6_k")
+
+
+@pytest.mark.parametrize("n_draft,k", [(1, 4), (0, 3)])
+def test_verification_writes_the_kv_rows_of_plain_steps_bit_for_bit(nt, n_draft, k):
+    """Every K and V row a speculative cycle leaves in the cache (draft steps and
+    multi-token verification, Q4_K_M mix) equals, bit for bit, the row plain greedy
+    steps write for the same tokens: the multi-token launches reproduce the
+    single-token arithmetic row for row."""
+    cfg = nt.make_config(**Q4_K_M_WIDE, seed=54)
+    prefill = (20, 2)
+    a, b = nt.nt_model_create(cfg), nt.nt_model_create(cfg)
+    try:
+        for m in (a, b):
+            nt.nt_kv_prefill(m, *prefill)
+        t_a = t_b = 9
+        stream_a, stream_b = [], []
+        for _ in range(4):
+            e, _ = nt.nt_speculative_step(a, t_a, n_draft, k)
+            stream_a += list(e)
+            t_a = e[-1]
+            for _ in range(len(e)):
+                t_b = nt.nt_decode_step(b, t_b)
+                stream_b.append(t_b)
+        assert stream_a == stream_b
+        pos = nt.nt_get_stats(a).pos
+        assert pos == nt.nt_get_stats(b).pos == prefill[0] + len(stream_a)
+        hd = WIDE["head_dim"]
+        for layer in range(WIDE["n_layers"]):
+            for kv in (0, 1):
+                for g in range(WIDE["n_kv_heads"]):
+                    ra = nt.nt_kv_export(a, layer, kv, g, 0, pos, hd)
+                    rb = nt.nt_kv_export(b, layer, kv, g, 0, pos, hd)
+                    np.testing.assert_array_equal(ra, rb, err_msg=f"layer {layer} kv {kv} head {g}")
+    finally:
+        nt.nt_model_destroy(a)
+        nt.nt_model_destroy(b)
