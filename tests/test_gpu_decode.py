@@ -189,6 +189,40 @@ def test_argument_and_resource_errors(nt, W):
         del os.environ["NT_DEVICE_BYTES_LIMIT"]
 
 
+@pytest.mark.parametrize("nr", [1, 0])
+def test_streamed_q4_k_m_layers_bitwise_equal_resident(nt, W, nr):
+    """The Q4_K_M mix at whole-tile widths, layers streamed through the staging
+    buffers: the two-format Q/K/V launch (Q4_K Q/K, Q6_K V rows one per warp),
+    the Q4_K O and gate/up and the Q6_K down read staging buffers, and every
+    step's logits equal the resident model's bit for bit."""
+    spec = dict(WIDE, n_layers=3, **W.Q4_K_M)
+    cfg = nt.make_config(**spec, seed=8)
+    a, b = nt.nt_model_create(cfg), nt.nt_model_create(cfg)
+    try:
+        for m in (a, b):
+            nt.nt_kv_prefill(m, 17, 2)
+        nt.nt_stream_layers(b, nr, 2)
+        la = np.empty(spec["vocab"], np.float32)
+        lb = np.empty(spec["vocab"], np.float32)
+        t = 11
+        for _ in range(5):
+            na = nt.nt_decode_step(a, t, la)
+            nb = nt.nt_decode_step(b, t, lb)
+            np.testing.assert_array_equal(la.view(np.uint32), lb.view(np.uint32))
+            assert na == nb
+            t = na
+        st = nt.nt_get_stats(b)
+        assert st.n_resident == nr and st.h2d_bytes > 0
+        hd = spec["head_dim"]
+        for layer in range(spec["n_layers"]):
+            for kv in (0, 1):
+                np.testing.assert_array_equal(nt.nt_kv_export(a, layer, kv, 1, 0, 22, hd),
+                                              nt.nt_kv_export(b, layer, kv, 1, 0, 22, hd))
+    finally:
+        nt.nt_model_destroy(a)
+        nt.nt_model_destroy(b)
+
+
 def test_llama8b_q8_0_teacher_forced(nt, W):
     """8B shape at full size: prefilled context 512, prompt token, GPU's own greedy tokens fed to both."""
     spec = W.LLAMA_8B_Q8_0

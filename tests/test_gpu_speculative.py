@@ -189,18 +189,21 @@ Q4_K_M_WIDE = dict(WIDE, t_embd="q4_k", t_q="q4_k", t_k="q4_k", t_v="q6_k", t_o=
                    t_up="q4_k", t_down="q6_k", t_out="q6_k")
 
 
-@pytest.mark.parametrize("n_draft,k", [(1, 4), (0, 3)])
-def test_verification_writes_the_kv_rows_of_plain_steps_bit_for_bit(nt, n_draft, k):
+@pytest.mark.parametrize("n_draft,k,resident", [(1, 4, 3), (0, 3, 3), (1, 4, 1)])
+def test_verification_writes_the_kv_rows_of_plain_steps_bit_for_bit(nt, n_draft, k, resident):
     """Every K and V row a speculative cycle leaves in the cache (draft steps and
-    multi-token verification, Q4_K_M mix) equals, bit for bit, the row plain greedy
-    steps write for the same tokens: the multi-token launches reproduce the
-    single-token arithmetic row for row."""
+    multi-token verification, Q4_K_M mix, verified layers resident or read from
+    the staging buffers) equals, bit for bit, the row plain greedy steps of a
+    resident model write for the same tokens: the multi-token launches reproduce
+    the single-token arithmetic row for row."""
     cfg = nt.make_config(**Q4_K_M_WIDE, seed=54)
     prefill = (20, 2)
     a, b = nt.nt_model_create(cfg), nt.nt_model_create(cfg)
     try:
         for m in (a, b):
             nt.nt_kv_prefill(m, *prefill)
+        if resident < WIDE["n_layers"]:
+            nt.nt_stream_layers(a, resident, 2)
         t_a = t_b = 9
         stream_a, stream_b = [], []
         for _ in range(4):
