@@ -482,6 +482,7 @@ def measure(nt, torch, wl, steps: int, warmup: int, args, dist, world: int, loca
                 t0 = time.perf_counter()
                 t = tok0
                 h2d_b = h2d_ms = comp_ms = ov = 0.0
+                lay_min, lay_max, slow_layers = [], [], []
                 for _ in range(steps):
                     t = nt.nt_decode_step(m, t)
                     st = nt.nt_get_stats(m)
@@ -489,6 +490,10 @@ def measure(nt, torch, wl, steps: int, warmup: int, args, dist, world: int, loca
                     h2d_ms += st.h2d_ms
                     comp_ms += st.compute_ms
                     ov += st.overlap
+                    if st.h2d_layer_min_idx >= 0:
+                        lay_min.append(st.h2d_layer_min_GBs)
+                        lay_max.append(st.h2d_layer_max_GBs)
+                        slow_layers.append(st.h2d_layer_min_idx)
                 torch.cuda.synchronize()
                 sec = time.perf_counter() - t0
                 out["streaming"] = {
@@ -498,7 +503,9 @@ def measure(nt, torch, wl, steps: int, warmup: int, args, dist, world: int, loca
                     "compute_ms_per_step": round(comp_ms / steps, 3),
                     "pcie_gen5_x16_nominal_GB_s": 64.0, "link": host_link(local),
                     "h2d_timing": "copy-stream CUDA events around each layer's copy",
-                    "cpu_numa_node": cpu_numa_node()}
+                    "cpu_numa_node": cpu_numa_node(),
+                    "h2d_layer_GB_s_min_max": [round(min(lay_min), 1), round(max(lay_max), 1)] if lay_min else None,
+                    "h2d_slowest_layers": sorted(set(slow_layers))[:8]}
                 pr = h2d_probe(torch, 1 << 30)
                 out["streaming"].update({
                     "h2d_probe_GB_s": pr["best"], "h2d_probe_median_GB_s": pr["median"],

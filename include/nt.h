@@ -104,6 +104,9 @@ typedef struct {
   double verify_weight_bytes; /* layer weight bytes the verification pass of the last
                               nt_speculative_step read (each multi-token launch reads
                               its weights once)                                      */
+  double h2d_layer_min_GBs;   /* slowest and fastest single layer copy of the last   */
+  double h2d_layer_max_GBs;   /* step, GB/s (0 when no layer was copied)             */
+  int32_t h2d_layer_min_idx;  /* the layer whose copy was slowest (-1: none)         */
 } nt_stats;
 
 /* Per-kernel-class device times of profiled steps (nt_profile_steps). */

@@ -1002,6 +1002,8 @@ static nt_status run_step(nt_model* m, int32_t token, int32_t* next_token, float
   NT_CUDA(cudaEventElapsedTime(&ms, m->ev_step0, m->ev_step1));
   m->stats.last_step_ms = ms;
   m->stats.steps++;
+  m->stats.h2d_layer_min_GBs = m->stats.h2d_layer_max_GBs = 0;
+  m->stats.h2d_layer_min_idx = -1;
   if (streamed || calib) {
     double h2d = 0, cms = 0, bytes = 0;
     for (int l = 0; l < c.n_layers; l++) {
@@ -1013,6 +1015,14 @@ static nt_status run_step(nt_model* m, int32_t token, int32_t* next_token, float
         NT_CUDA(cudaEventElapsedTime(&t, m->ev_cs[size_t(l)], m->ev_ce[size_t(l)]));
         h2d += t;
         bytes += double(m->layers[size_t(l)].bytes);
+        if (t > 0.f) {
+          const double r = double(m->layers[size_t(l)].bytes) / (double(t) * 1e6);
+          if (m->stats.h2d_layer_min_idx < 0 || r < m->stats.h2d_layer_min_GBs) {
+            m->stats.h2d_layer_min_GBs = r;
+            m->stats.h2d_layer_min_idx = l;
+          }
+          if (r > m->stats.h2d_layer_max_GBs) m->stats.h2d_layer_max_GBs = r;
+        }
       }
     }
     m->stats.h2d_ms = h2d;
@@ -1426,6 +1436,7 @@ nt_status nt_get_stats(const nt_model* m, nt_stats* out) {
   if (!m || !out) return fail(NT_E_INVAL, "nt_get_stats: NULL argument");
   *out = m->stats;
   out->pos = m->pos;
+  if (out->h2d_layer_max_GBs <= 0) out->h2d_layer_min_idx = -1;   // no layer copied in the last step
   int64_t wb = int64_t(m->output.nbytes) + int64_t(m->embd.m.cols) * 0;
   for (const auto& L : m->layers)
     for (int r = 0; r < 7; r++) wb += int64_t(L.view[r].nbytes);

@@ -51,7 +51,9 @@ class nt_stats(C.Structure):
     _fields_ = [("steps", C.c_int64), ("pos", C.c_int32), ("n_resident", C.c_int32),
                 ("last_step_ms", C.c_double), ("h2d_bytes", C.c_double), ("h2d_ms", C.c_double),
                 ("compute_ms", C.c_double), ("overlap", C.c_double), ("weight_bytes", C.c_int64),
-                ("kv_bytes_per_pos", C.c_int64), ("verify_weight_bytes", C.c_double)]
+                ("kv_bytes_per_pos", C.c_int64), ("verify_weight_bytes", C.c_double),
+                ("h2d_layer_min_GBs", C.c_double), ("h2d_layer_max_GBs", C.c_double),
+                ("h2d_layer_min_idx", C.c_int32)]
 
 
 class nt_kernel_times(C.Structure):

@@ -144,6 +144,10 @@ def test_streamed_layers_bitwise_equal_resident(nt, W, nr):
         st = nt.nt_get_stats(b)
         assert st.n_resident == nr and st.h2d_bytes > 0 and st.h2d_ms > 0
         assert 0.0 <= st.overlap <= 1.0
+        # per-layer copy rates: the slowest copied layer is a streamed one
+        assert 0 < st.h2d_layer_min_GBs <= st.h2d_layer_max_GBs
+        assert nr <= st.h2d_layer_min_idx < spec["n_layers"]
+        assert nt.nt_get_stats(a).h2d_layer_min_idx == -1
         # a streamed tensor still exports, but cannot be used in place
         tq = nt.nt_model_tensor(b, 4, "q")
         from gpu_util import blocks
