@@ -310,7 +310,9 @@ nt_status nt_dequant(const nt_qtensor* t, int64_t row0, int64_t nrows, float* de
  * stream; launched with programmatic dependent launch, so it may start (and
  * read W) before the previous kernel on the stream ends, but reads x and
  * writes y only after it.  dev_x and dev_y must not overlap and must be
- * 16-byte aligned. */
+ * 16-byte aligned.  Matrices wider than 32768 columns (a multiple of 1024;
+ * NT_E_UNSUPPORTED otherwise) run as launches over column windows of at most
+ * 32768, each adding its window's products to y in window order. */
 nt_status nt_gemv_q(const nt_qtensor* t, const float* dev_x, float* dev_y, void* stream);
 
 /* y_i = W x_i for k vectors (1 <= k <= 8) in as few launches as fit: the

@@ -65,6 +65,30 @@ cudaError_t launch_gemv(const GemvArgs& a_in, int epi, cudaStream_t s, bool pdl,
   return cudaErrorInvalidValue;
 }
 
+// The pipeline GEMV over the column window [col0, col0 + ncols) of a (ncols a
+// multiple of 1024, at most 32768): rows of W restricted to the window times
+// x[col0, col0 + ncols), through epi.
+static cudaError_t launch_gemv_window(const GemvArgs& a_in, int epi, int64_t col0, int64_t ncols, cudaStream_t s,
+                                      bool pdl) {
+  GemvArgs a = a_in;
+  if (ncols <= 0 || ncols % 1024 || ncols > 32768 || col0 < 0 || col0 + ncols > a.seg[0].cols || a.nseg != 1)
+    return cudaErrorInvalidValue;
+  if (a.max_grid <= 0 || a.max_grid > kMaxGemvGrid) a.max_grid = kMaxGemvGrid;
+  a.col0 = col0;
+  a.ncols = ncols;
+  int R = 0, S = 0;
+  const int64_t nrows = gemv_logical_rows(a);
+  if (!pipe_shape(a.seg[0].type, nrows, ncols, epi, R, S)) return cudaErrorInvalidValue;
+  switch (a.seg[0].type) {
+    case NT_Q8_0: return launch_gemv_pipe_q8_0(a, epi, R, S, s, pdl, nullptr);
+    case NT_Q4_0: return launch_gemv_pipe_q4_0(a, epi, R, S, s, pdl, nullptr);
+    case NT_Q4_K: return launch_gemv_pipe_q4_k(a, epi, R, S, s, pdl, nullptr);
+    case NT_Q6_K: return launch_gemv_pipe_q6_k(a, epi, R, S, s, pdl, nullptr);
+    case NT_Q5_K: return launch_gemv_pipe_q5_k(a, epi, R, S, s, pdl, nullptr);
+  }
+  return cudaErrorInvalidValue;
+}
+
 // Tokens [0, k) through the GEMV a, each with the arithmetic of its own
 // single-token launch (launch_gemv, or the two-format kernel for a pair),
 // several tokens per launch where their staged x fit beside a ring of depth 3:
@@ -196,7 +220,8 @@ extern "C" nt_status nt_gemv_q(const nt_qtensor* t, const float* dev_x, float* d
   if (t->on_host) return fail(NT_E_STATE, "nt_gemv_q: tensor lives in host memory (streamed layer)");
   if ((reinterpret_cast<uintptr_t>(dev_x) | reinterpret_cast<uintptr_t>(dev_y)) & 15)
     return fail(NT_E_INVAL, "nt_gemv_q: x and y must be 16-byte aligned");
-  if (t->m.cols > 32768) return fail(NT_E_UNSUPPORTED, "nt_gemv_q: more than 32768 columns");
+  if (t->m.cols > 32768 && t->m.cols % 1024)
+    return fail(NT_E_UNSUPPORTED, "nt_gemv_q: more than 32768 columns, not a multiple of 1024");
   const char* xb = reinterpret_cast<const char*>(dev_x);
   const char* yb = reinterpret_cast<const char*>(dev_y);
   if (xb < yb + t->m.rows * 4 && yb < xb + t->m.cols * 4) return fail(NT_E_INVAL, "nt_gemv_q: x and y overlap");
@@ -205,6 +230,15 @@ extern "C" nt_status nt_gemv_q(const nt_qtensor* t, const float* dev_x, float* d
   a.nseg = 1;
   a.x = dev_x;
   a.epi.y = dev_y;
+  if (t->m.cols > 32768) {   // column windows of at most 32768, their products added in window order
+    for (int64_t c0 = 0; c0 < t->m.cols; c0 += 32768) {
+      const int64_t n = t->m.cols - c0 < 32768 ? t->m.cols - c0 : 32768;
+      cudaError_t e = launch_gemv_window(a, c0 == 0 ? EPI_STORE : EPI_ADD, c0, n, static_cast<cudaStream_t>(stream),
+                                         true);
+      if (e != cudaSuccess) return cuda_fail(e, "nt_gemv_q");
+    }
+    return NT_OK;
+  }
   // programmatic dependent launch: the kernel reads only the (never rewritten)
   // weight codes before waiting for the previous kernel in the stream to finish
   cudaError_t e = launch_gemv(a, EPI_STORE, static_cast<cudaStream_t>(stream), true, nullptr);

@@ -51,6 +51,33 @@ def test_gemv_matches_oracle(nt, fmt, rows, cols):
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
+def test_gemv_wider_than_one_launch_in_column_windows(nt, fmt):
+    """More than 32768 columns: launches over column windows of at most 32768 add
+    their products in window order; against the oracle as any GEMV.  A width past
+    32768 that is not a multiple of 1024 is refused."""
+    rows, cols = 37, 2 * 32768 + 4096
+    t = nt.nt_qtensor_create(fmt, rows, cols, 3, 57, 0.02)
+    try:
+        x = activation(cols, seed=2)
+        got = _gemv(nt, t, x, rows)
+        want = oracle.gemv(fmt, oracle.qtensor_rows(fmt, rows, cols, 3, 57, 0.02, nthreads=8), rows, cols, x,
+                           nthreads=8)
+        assert np.isfinite(got).all()
+        err = rel_l2(got, want)
+        assert err < TOL and err < 1e-4, err
+        np.testing.assert_array_equal(_gemv(nt, t, x, rows), got)
+    finally:
+        nt.nt_qtensor_destroy(t)
+    t = nt.nt_qtensor_create(fmt, 4, 33024, 3, 58, 0.02)
+    try:
+        with pytest.raises(nt.NtError) as ei:
+            _gemv(nt, t, np.zeros(33024, np.float32), 4)
+        assert ei.value.status == nt.NT_E_UNSUPPORTED
+    finally:
+        nt.nt_qtensor_destroy(t)
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
 def test_gemv_degenerate_inputs(nt, fmt):
     rows, cols = 9, 768 if fmt in ("q8_0", "q4_0") else 1024
     t = nt.nt_qtensor_create(fmt, rows, cols, 3, 56, 0.02)
